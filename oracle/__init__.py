@@ -1,0 +1,189 @@
+"""CPU oracle for the bs=1 Llama-style decode step (ctypes wrapper of oracle.c).
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this package.  The product path (the
+``decode_megakernel_05_gb300`` package and its CUDA library) never calls it.
+
+Everything is computed in double from the same bf16 weights the GPU path
+receives; see oracle.c for the definition and the pages it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_P = ctypes.c_void_p
+
+
+class _OracleModelC(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32),
+        ("vocab", ctypes.c_int32), ("max_seq", ctypes.c_int32),
+        ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double),
+        ("embed", _P), ("lm_head", _P), ("final_norm", _P),
+        ("attn_norm", _P), ("wq", _P), ("wk", _P), ("wv", _P), ("wo", _P),
+        ("ffn_norm", _P), ("w_gate", _P), ("w_up", _P), ("w_down", _P),
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc -O2, OpenMP, no fast-math)."""
+    src = os.path.join(_HERE, "oracle.c")
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(src):
+        return _SO
+    os.makedirs(os.path.dirname(_SO), exist_ok=True)
+    tmp = _SO + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fno-fast-math", "-fno-semantic-interposition", "-shared", "-fPIC", "-o", tmp, src, "-lm"])
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            L.oracle_bf16_to_double.restype = ctypes.c_double
+            L.oracle_round_bf16.argtypes = [ctypes.c_double]
+            L.oracle_round_bf16.restype = ctypes.c_uint16
+            L.oracle_rmsnorm.argtypes = [_P, _P, ctypes.c_int, ctypes.c_double, _P]
+            L.oracle_gemv.argtypes = [_P, ctypes.c_int64, ctypes.c_int64, _P, _P]
+            L.oracle_rope.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_double]
+            L.oracle_softmax.argtypes = [_P, ctypes.c_int, _P]
+            L.oracle_attention_head.argtypes = [_P, _P, _P, ctypes.c_int, ctypes.c_int, _P]
+            L.oracle_silu.argtypes = [ctypes.c_double]
+            L.oracle_silu.restype = ctypes.c_double
+            L.oracle_argmax_f32.argtypes = [_P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+            L.oracle_argmax_f32.restype = ctypes.c_int
+            L.oracle_decode_step.argtypes = [ctypes.POINTER(_OracleModelC), _P, _P, ctypes.c_int, ctypes.c_int, _P, _P]
+            L.oracle_decode_step.restype = ctypes.c_int
+            for f in (L.oracle_rmsnorm, L.oracle_gemv, L.oracle_rope, L.oracle_softmax, L.oracle_attention_head):
+                f.restype = None
+            _lib = L
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data
+
+
+# ---------------------------------------------------------------- single ops
+
+def bf16_to_double(b: int) -> float:
+    return lib().oracle_bf16_to_double(int(b))
+
+
+def round_bf16(v: float) -> int:
+    return lib().oracle_round_bf16(float(v))
+
+
+def rmsnorm(x, g_bf16, eps: float) -> np.ndarray:
+    x, px = _c(x, np.float64)
+    g, pg = _c(g_bf16, np.uint16)
+    y = np.empty_like(x)
+    lib().oracle_rmsnorm(px, pg, x.size, eps, y.ctypes.data)
+    return y
+
+
+def gemv(w_bf16, x) -> np.ndarray:
+    w, pw = _c(w_bf16, np.uint16)
+    x, px = _c(x, np.float64)
+    y = np.empty(w.shape[0], dtype=np.float64)
+    lib().oracle_gemv(pw, w.shape[0], w.shape[1], px, y.ctypes.data)
+    return y
+
+
+def rope(v, pos: int, theta: float) -> np.ndarray:
+    v = np.array(v, dtype=np.float64, copy=True)
+    lib().oracle_rope(v.ctypes.data, v.size, int(pos), float(theta))
+    return v
+
+
+def softmax(s) -> np.ndarray:
+    s, ps = _c(s, np.float64)
+    p = np.empty_like(s)
+    lib().oracle_softmax(ps, s.size, p.ctypes.data)
+    return p
+
+
+def attention_head(q, k_bf16, v_bf16) -> np.ndarray:
+    q, pq = _c(q, np.float64)
+    k, pk = _c(k_bf16, np.uint16)
+    v, pv = _c(v_bf16, np.uint16)
+    out = np.empty(q.size, dtype=np.float64)
+    lib().oracle_attention_head(pq, pk, pv, k.shape[0], q.size, out.ctypes.data)
+    return out
+
+
+def silu(x: float) -> float:
+    return lib().oracle_silu(float(x))
+
+
+def argmax_f32(logits):
+    lg, pl = _c(logits, np.float64)
+    nf = ctypes.c_int(0)
+    idx = lib().oracle_argmax_f32(pl, lg.size, ctypes.byref(nf))
+    return idx, bool(nf.value)
+
+
+# ---------------------------------------------------------------- decode step
+
+class OracleDecoder:
+    """The oracle's model + its own bf16 K/V cache [L][kv_heads][max_seq][head_dim]."""
+
+    def __init__(self, model: dict, max_seq: int):
+        s = model["shape"]
+        self.shape, self.max_seq, self._keep = s, int(max_seq), []
+        c = _OracleModelC()
+        c.n_layers, c.hidden, c.n_q_heads, c.n_kv_heads = s.n_layers, s.hidden, s.n_q_heads, s.n_kv_heads
+        c.head_dim, c.ffn, c.vocab, c.max_seq = s.head_dim, s.ffn, s.vocab, self.max_seq
+        c.rms_eps, c.rope_theta = float(s.rms_eps), float(s.rope_theta)
+
+        def ptr(a):
+            a = np.ascontiguousarray(a, dtype=np.uint16)
+            self._keep.append(a)
+            return a.ctypes.data
+
+        def ptrs(lst):
+            arr = (ctypes.c_void_p * len(lst))(*[ptr(a) for a in lst])
+            self._keep.append(arr)
+            return ctypes.cast(arr, ctypes.c_void_p).value
+
+        c.embed = ptr(model["embed"])
+        c.lm_head = c.embed if model["lm_head"] is None else ptr(model["lm_head"])
+        c.final_norm = ptr(model["final_norm"])
+        for name in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down"):
+            setattr(c, name, ptrs(model[name]))
+        self._c = c
+        shp = (s.n_layers, s.n_kv_heads, self.max_seq, s.head_dim)
+        self.kcache = np.zeros(shp, dtype=np.uint16)
+        self.vcache = np.zeros(shp, dtype=np.uint16)
+
+    def set_kv(self, ks, vs, n_pos: int):
+        """Pre-fill positions 0..n_pos-1 of every layer (bf16 [kv_heads][n_pos][head_dim])."""
+        for l in range(self.shape.n_layers):
+            self.kcache[l, :, :n_pos, :] = ks[l]
+            self.vcache[l, :, :n_pos, :] = vs[l]
+
+    def step(self, token: int, pos: int):
+        """Returns (logits float64 [vocab], hidden float64 [hidden])."""
+        s = self.shape
+        logits = np.empty(s.vocab, dtype=np.float64)
+        hidden = np.empty(s.hidden, dtype=np.float64)
+        rc = lib().oracle_decode_step(ctypes.byref(self._c), self.kcache.ctypes.data, self.vcache.ctypes.data,
+                                      int(token), int(pos), logits.ctypes.data, hidden.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"oracle_decode_step rejected token={token} pos={pos}")
+        return logits, hidden

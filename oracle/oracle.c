@@ -1,0 +1,226 @@
+/*
+ * oracle.c - plain, slow CPU reference for one batch-size-1 decode step of a
+ * Llama-style decoder.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the package smoke check and the CPU
+ * baseline leg of the benchmark may load this code.  It shares nothing with
+ * the CUDA path: no headers, helpers, tables or kernels.
+ *
+ * What it computes is the unfused, sequential definition of the step: the
+ * "simple, synchronous, unfused reference" that the fused path is compared
+ * against layer by layer and token by token (stapisi.com/news/3904786,
+ * section 6.3 "software engineering practice").  Fusion and in-kernel
+ * pipelining change only the schedule of this computation, not its result
+ * (cloud.baidu.com/article/9434380, section 4.2).
+ *
+ * Precision: weights and the K/V cache are bf16 (widened exactly); every
+ * activation and every accumulation is double.  The only rounding steps are
+ * the ones the method itself has: K and V are stored to the cache as bf16,
+ * and the greedy argmax is taken over logits rounded to float, the precision
+ * the GPU path decides it in.
+ *
+ * Operator list of one layer (cloud.baidu.com/article/9434380, section 5,
+ * step 2, segments A/B/C): normalisation + Q/K/V projection + rotary position
+ * encoding; attention scores + causal mask + softmax + output projection;
+ * normalisation + FFN first layer + activation + FFN second layer + residual.
+ * The normalisation is RMSNorm (developer.baidu.com/article/detail.html?id=
+ * 8006242, section 4.1.2) and the activation is SwiGLU (Llama).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, max_seq;
+    double rms_eps, rope_theta;
+    const uint16_t* embed;      /* [vocab][hidden] */
+    const uint16_t* lm_head;    /* [vocab][hidden]; equal to embed when tied */
+    const uint16_t* final_norm; /* [hidden] */
+    const uint16_t* const* attn_norm; /* per layer [hidden] */
+    const uint16_t* const* wq;        /* per layer [n_q_heads*head_dim][hidden] */
+    const uint16_t* const* wk;        /* per layer [n_kv_heads*head_dim][hidden] */
+    const uint16_t* const* wv;        /* per layer [n_kv_heads*head_dim][hidden] */
+    const uint16_t* const* wo;        /* per layer [hidden][n_q_heads*head_dim] */
+    const uint16_t* const* ffn_norm;  /* per layer [hidden] */
+    const uint16_t* const* w_gate;    /* per layer [ffn][hidden] */
+    const uint16_t* const* w_up;      /* per layer [ffn][hidden] */
+    const uint16_t* const* w_down;    /* per layer [hidden][ffn] */
+} oracle_model;
+
+/* bf16 bit pattern -> double (exact). */
+static inline double bf2d(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+double oracle_bf16_to_double(uint16_t b) { return bf2d(b); }
+
+/* double -> bf16 bit pattern: first to float (the GPU path's activation
+ * precision), then to bf16, both rounding to nearest even. */
+uint16_t oracle_round_bf16(double v) {
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* RMSNorm (developer.baidu.com/article/detail.html?id=8006242, section 4.1.2
+ * names RMSNorm; Llama form): y_i = x_i / sqrt(mean_j(x_j^2) + eps) * g_i.
+ * No mean subtraction and no bias. */
+void oracle_rmsnorm(const double* x, const uint16_t* g, int n, double eps, double* y) {
+    double ss = 0.0;
+    for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+    double inv = 1.0 / sqrt(ss / (double)n + eps);
+    for (int i = 0; i < n; ++i) y[i] = x[i] * inv * bf2d(g[i]);
+}
+
+/* y = W x for a bf16 matrix W [rows][cols] (row-major, [out, in]). */
+void oracle_gemv(const uint16_t* W, int64_t rows, int64_t cols, const double* x, double* y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* w = W + r * cols;
+        double acc = 0.0;
+        for (int64_t c = 0; c < cols; ++c) acc += bf2d(w[c]) * x[c];
+        y[r] = acc;
+    }
+}
+
+/* Rotary position encoding of one head vector v[hd] at position pos
+ * (cloud.baidu.com/article/9434380, section 3 lists it among the decode
+ * operators; the pages give no formula).  Llama "rotate-half" form: dims i and
+ * i + hd/2 form a pair rotated by the angle pos * theta^(-2i/hd):
+ *   v'_i        = v_i cos(a) - v_{i+hd/2} sin(a)
+ *   v'_{i+hd/2} = v_{i+hd/2} cos(a) + v_i sin(a)                          */
+void oracle_rope(double* v, int hd, int pos, double theta) {
+    int half = hd / 2;
+    for (int i = 0; i < half; ++i) {
+        double inv_freq = pow(theta, -(2.0 * (double)i) / (double)hd);
+        double a = (double)pos * inv_freq;
+        double c = cos(a), s = sin(a);
+        double x0 = v[i], x1 = v[i + half];
+        v[i] = x0 * c - x1 * s;
+        v[i + half] = x1 * c + x0 * s;
+    }
+}
+
+/* Softmax with the maximum subtracted first, the overflow guard the pages ask
+ * for (cloud.baidu.com/article/9434380, section 8, problem 4). */
+void oracle_softmax(const double* s, int n, double* p) {
+    double m = -INFINITY;
+    for (int i = 0; i < n; ++i) if (s[i] > m) m = s[i];
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i) { p[i] = exp(s[i] - m); sum += p[i]; }
+    for (int i = 0; i < n; ++i) p[i] /= sum;
+}
+
+/* One query head over ctx cached positions (segment B of
+ * cloud.baidu.com/article/9434380, section 5, step 2: scores + mask + softmax
+ * + weighted sum).  K and V are bf16 [ctx][hd]; the causal mask is implicit:
+ * only positions 0..ctx-1 (the current token included) are passed in.
+ * out[d] = sum_p softmax_p(q . K_p / sqrt(hd)) V_p[d]. */
+void oracle_attention_head(const double* q, const uint16_t* K, const uint16_t* V, int ctx, int hd, double* out) {
+    double* s = (double*)malloc(sizeof(double) * (size_t)ctx);
+    double* p = (double*)malloc(sizeof(double) * (size_t)ctx);
+    double scale = 1.0 / sqrt((double)hd);
+    for (int t = 0; t < ctx; ++t) {
+        double acc = 0.0;
+        for (int d = 0; d < hd; ++d) acc += q[d] * bf2d(K[(int64_t)t * hd + d]);
+        s[t] = acc * scale;
+    }
+    oracle_softmax(s, ctx, p);
+    for (int d = 0; d < hd; ++d) out[d] = 0.0;
+    for (int t = 0; t < ctx; ++t)
+        for (int d = 0; d < hd; ++d) out[d] += p[t] * bf2d(V[(int64_t)t * hd + d]);
+    free(s);
+    free(p);
+}
+
+/* SiLU activation x / (1 + e^-x); SwiGLU u_j = silu(gate_j) * up_j. */
+double oracle_silu(double x) { return x / (1.0 + exp(-x)); }
+
+/* Greedy token: index of the largest logit after rounding to float, the
+ * lowest index on ties.  *nonfinite is set when any logit is NaN or infinite. */
+int oracle_argmax_f32(const double* logits, int n, int* nonfinite) {
+    int best = -1;
+    float bv = 0.0f;
+    *nonfinite = 0;
+    for (int i = 0; i < n; ++i) {
+        float v = (float)logits[i];
+        if (!isfinite(v)) { *nonfinite = 1; continue; }
+        if (best < 0 || v > bv) { best = i; bv = v; }
+    }
+    return best;
+}
+
+/* One decode step: feed `token` at position `pos`, append its K/V to the
+ * cache, return logits [vocab] and the final-norm hidden state [hidden].
+ * kcache / vcache: bf16 [n_layers][n_kv_heads][max_seq][head_dim]; positions
+ * 0..pos-1 must already hold the earlier steps' K (rotated) and V.
+ * Returns 0, or -1 for bad arguments. */
+int oracle_decode_step(const oracle_model* m, uint16_t* kcache, uint16_t* vcache, int token, int pos,
+                       double* logits, double* hidden) {
+    const int H = m->hidden, hd = m->head_dim, qh = m->n_q_heads, kvh = m->n_kv_heads, F = m->ffn;
+    if (token < 0 || token >= m->vocab || pos < 0 || pos >= m->max_seq || qh % kvh != 0) return -1;
+    const int group = qh / kvh;
+    double* x = (double*)malloc(sizeof(double) * H);
+    double* xn = (double*)malloc(sizeof(double) * H);
+    double* q = (double*)malloc(sizeof(double) * (size_t)qh * hd);
+    double* k = (double*)malloc(sizeof(double) * (size_t)kvh * hd);
+    double* v = (double*)malloc(sizeof(double) * (size_t)kvh * hd);
+    double* att = (double*)malloc(sizeof(double) * (size_t)qh * hd);
+    double* o = (double*)malloc(sizeof(double) * H);
+    double* gate = (double*)malloc(sizeof(double) * F);
+    double* up = (double*)malloc(sizeof(double) * F);
+    double* u = (double*)malloc(sizeof(double) * F);
+
+    /* embedding row */
+    for (int i = 0; i < H; ++i) x[i] = bf2d(m->embed[(int64_t)token * H + i]);
+
+    for (int l = 0; l < m->n_layers; ++l) {
+        /* segment A: RMSNorm, Q/K/V projections, RoPE on q and k, K/V append */
+        oracle_rmsnorm(x, m->attn_norm[l], H, m->rms_eps, xn);
+        oracle_gemv(m->wq[l], (int64_t)qh * hd, H, xn, q);
+        oracle_gemv(m->wk[l], (int64_t)kvh * hd, H, xn, k);
+        oracle_gemv(m->wv[l], (int64_t)kvh * hd, H, xn, v);
+        for (int h = 0; h < qh; ++h) oracle_rope(q + (int64_t)h * hd, hd, pos, m->rope_theta);
+        for (int g = 0; g < kvh; ++g) oracle_rope(k + (int64_t)g * hd, hd, pos, m->rope_theta);
+        for (int g = 0; g < kvh; ++g) {
+            int64_t base = (((int64_t)l * kvh + g) * m->max_seq + pos) * hd;
+            for (int d = 0; d < hd; ++d) {
+                kcache[base + d] = oracle_round_bf16(k[(int64_t)g * hd + d]);
+                vcache[base + d] = oracle_round_bf16(v[(int64_t)g * hd + d]);
+            }
+        }
+        /* segment B: attention over positions 0..pos; q head h reads kv head
+         * h / (qh/kvh) (grouped-query attention), then output projection and
+         * the residual add. */
+#pragma omp parallel for schedule(static)
+        for (int h = 0; h < qh; ++h) {
+            int g = h / group;
+            int64_t base = ((int64_t)l * kvh + g) * m->max_seq * hd;
+            oracle_attention_head(q + (int64_t)h * hd, kcache + base, vcache + base, pos + 1, hd, att + (int64_t)h * hd);
+        }
+        oracle_gemv(m->wo[l], H, (int64_t)qh * hd, att, o);
+        for (int i = 0; i < H; ++i) x[i] += o[i];
+        /* segment C: RMSNorm, gate/up projections, SwiGLU, down projection,
+         * residual add */
+        oracle_rmsnorm(x, m->ffn_norm[l], H, m->rms_eps, xn);
+        oracle_gemv(m->w_gate[l], F, H, xn, gate);
+        oracle_gemv(m->w_up[l], F, H, xn, up);
+        for (int j = 0; j < F; ++j) u[j] = oracle_silu(gate[j]) * up[j];
+        oracle_gemv(m->w_down[l], H, F, u, o);
+        for (int i = 0; i < H; ++i) x[i] += o[i];
+    }
+    /* final norm, LM head */
+    oracle_rmsnorm(x, m->final_norm, H, m->rms_eps, hidden);
+    oracle_gemv(m->lm_head, m->vocab, H, hidden, logits);
+
+    free(x); free(xn); free(q); free(k); free(v); free(att); free(o); free(gate); free(up); free(u);
+    return 0;
+}

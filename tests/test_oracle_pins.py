@@ -1,0 +1,335 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test checks one piece of the oracle against a closed form, an invariant
+of the definition, a library routine (torch fp64 ops, torch's bf16 rounding),
+or brute force on a model small enough to work out by hand.  They are chosen
+so that a plausible slip (a dropped term, a wrong sign or index, the other
+RoPE pairing, the wrong GQA head map, an off-by-one in the causal window)
+fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import synth
+
+RNG = np.random.default_rng(1234)
+
+
+def bf16_bits(a) -> np.ndarray:
+    """float values -> bf16 bit patterns via torch's own float32 -> bf16 rounding."""
+    t = torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def bf16_vals(bits) -> np.ndarray:
+    return synth.bf16_to_f32(np.asarray(bits, dtype=np.uint16)).astype(np.float64)
+
+
+# --------------------------------------------------------------- bf16 rounding
+
+def test_round_bf16_matches_torch():
+    x = np.concatenate([RNG.standard_normal(20000) * 10.0 ** RNG.integers(-6, 6, 20000),
+                        [0.0, -0.0, 1.0, -2.5, 1e30, -1e-30]])
+    ours = np.array([oracle.round_bf16(v) for v in x], dtype=np.uint16)
+    assert np.array_equal(ours, bf16_bits(x))
+
+
+def test_round_bf16_ties_to_even():
+    assert oracle.round_bf16(1.0 + 2.0 ** -8) == 0x3F80          # halfway, even below
+    assert oracle.round_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82      # halfway, even above
+    assert oracle.bf16_to_double(0x3F80) == 1.0
+    assert oracle.bf16_to_double(0xC040) == -3.0
+
+
+# --------------------------------------------------------------------- RMSNorm
+
+@pytest.mark.parametrize("c", [1.0, 1.5, -0.75])
+def test_rmsnorm_rms_equals_gain(c):
+    x = RNG.standard_normal(256) * 3.0
+    g = bf16_bits(np.full(256, c))
+    eps = 1e-5
+    y = oracle.rmsnorm(x, g, eps)
+    ms = np.mean(x * x)
+    assert math.isclose(np.sqrt(np.mean(y * y)), abs(c) * math.sqrt(ms / (ms + eps)), rel_tol=1e-12)
+    y0 = oracle.rmsnorm(x, g, 0.0)
+    assert math.isclose(np.sqrt(np.mean(y0 * y0)), abs(c), rel_tol=1e-12)
+
+
+def test_rmsnorm_scale_invariant_and_gain_elementwise():
+    x = RNG.standard_normal(512)
+    ones = bf16_bits(np.ones(512))
+    g = bf16_bits(RNG.normal(1.0, 0.1, 512))
+    a = oracle.rmsnorm(x, ones, 0.0)
+    b = oracle.rmsnorm(7.25 * x, ones, 0.0)
+    np.testing.assert_allclose(a, b, rtol=1e-13)
+    np.testing.assert_allclose(oracle.rmsnorm(x, g, 0.0), a * bf16_vals(g), rtol=1e-13)
+    # no mean subtraction: a constant vector normalises to +-1, not to 0
+    np.testing.assert_allclose(oracle.rmsnorm(np.full(8, 3.0), ones[:8], 0.0), np.ones(8), rtol=1e-15)
+
+
+# ------------------------------------------------------------------------ RoPE
+
+def test_rope_position_zero_is_identity():
+    v = RNG.standard_normal(64)
+    assert np.array_equal(oracle.rope(v, 0, 10000.0), v)
+
+
+def test_rope_closed_form_head_dim_4():
+    # hd = 4: pairs (0, 2) and (1, 3), frequencies theta^0 = 1 and theta^(-1/2)
+    v = np.array([1.0, 2.0, 3.0, 4.0])
+    pos, theta = 3, 10000.0
+    a0, a1 = pos * 1.0, pos / 100.0
+    want = [1 * math.cos(a0) - 3 * math.sin(a0), 2 * math.cos(a1) - 4 * math.sin(a1),
+            3 * math.cos(a0) + 1 * math.sin(a0), 4 * math.cos(a1) + 2 * math.sin(a1)]
+    np.testing.assert_allclose(oracle.rope(v, pos, theta), want, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("hd,theta", [(64, 10000.0), (128, 500000.0)])
+def test_rope_preserves_pair_norms(hd, theta):
+    v = RNG.standard_normal(hd)
+    r = oracle.rope(v, 1234, theta)
+    h = hd // 2
+    np.testing.assert_allclose(v[:h] ** 2 + v[h:] ** 2, r[:h] ** 2 + r[h:] ** 2, rtol=1e-12)
+
+
+def test_rope_relative_position_and_composition():
+    hd, theta = 64, 500000.0
+    q, k = RNG.standard_normal(hd), RNG.standard_normal(hd)
+    for m, n in [(5, 2), (100, 37), (4000, 3999), (31000, 7)]:
+        lhs = oracle.rope(q, m, theta) @ oracle.rope(k, n, theta)
+        rhs = oracle.rope(q, m - n, theta) @ k
+        assert math.isclose(lhs, rhs, rel_tol=1e-9, abs_tol=1e-9)
+    v = RNG.standard_normal(hd)
+    np.testing.assert_allclose(oracle.rope(oracle.rope(v, 17, theta), 230, theta), oracle.rope(v, 247, theta),
+                               rtol=1e-9, atol=1e-12)
+
+
+# --------------------------------------------------------------------- softmax
+
+def test_softmax_properties():
+    s = RNG.standard_normal(100) * 4
+    p = oracle.softmax(s)
+    assert math.isclose(p.sum(), 1.0, rel_tol=1e-14)
+    np.testing.assert_allclose(oracle.softmax(s + 123.5), p, rtol=1e-12)
+    big = oracle.softmax(np.array([1e4, 1e4 - 1.0, -1e4]))
+    assert np.all(np.isfinite(big))
+    np.testing.assert_allclose(big[:2], [1 / (1 + math.exp(-1)), 1 / (1 + math.exp(1))], rtol=1e-14)
+    assert big[2] == 0.0
+    a, b = 0.3, -1.7
+    np.testing.assert_allclose(oracle.softmax([a, b]), [1 / (1 + math.exp(b - a)), 1 / (1 + math.exp(a - b))],
+                               rtol=1e-15)
+
+
+# ------------------------------------------------------------------- attention
+
+def test_attention_single_position_returns_v():
+    hd = 64
+    q = RNG.standard_normal(hd)
+    k = bf16_bits(RNG.standard_normal((1, hd)))
+    v = bf16_bits(RNG.standard_normal((1, hd)))
+    assert np.array_equal(oracle.attention_head(q, k, v), bf16_vals(v[0]))
+
+
+def test_attention_two_positions_closed_form():
+    hd = 4
+    q = np.array([1.0, 0.5, -1.0, 2.0])
+    k = bf16_bits([[1, 0, 0, 1], [0, 2, 1, 0]])
+    v = bf16_bits([[1, 2, 3, 4], [-4, 0, 8, 1]])
+    s0 = (1 + 2) / 2.0
+    s1 = (1.0 - 1.0) / 2.0
+    w0 = 1 / (1 + math.exp(s1 - s0))
+    want = w0 * np.array([1, 2, 3, 4]) + (1 - w0) * np.array([-4, 0, 8, 1])
+    np.testing.assert_allclose(oracle.attention_head(q, k, v), want, rtol=1e-14)
+
+
+def test_attention_equal_keys_average_values():
+    hd, ctx = 8, 9
+    q = RNG.standard_normal(hd)
+    k = np.tile(bf16_bits(RNG.standard_normal(hd)), (ctx, 1))
+    v = bf16_bits(RNG.standard_normal((ctx, hd)))
+    np.testing.assert_allclose(oracle.attention_head(q, k, v), bf16_vals(v).mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def test_silu_and_argmax():
+    for x in (-3.0, -0.5, 0.0, 1.25, 8.0):
+        assert math.isclose(oracle.silu(x), x / (1 + math.exp(-x)), rel_tol=1e-15, abs_tol=1e-300)
+    assert oracle.argmax_f32([1.0, 3.0, 3.0, -2.0]) == (1, False)
+    assert oracle.argmax_f32([1.0, float("nan"), 0.5]) == (0, True)
+    # ties decided in float: these two differ only below float resolution
+    assert oracle.argmax_f32([1.0, 1.0 + 1e-12]) == (0, False)
+
+
+# ---------------------------------------------------------- whole decode step
+
+def tiny_shape(**kw):
+    d = dict(n_layers=2, hidden=64, n_q_heads=4, n_kv_heads=2, head_dim=16, ffn=96, vocab=50,
+             rms_eps=1e-5, rope_theta=10000.0, tie_embeddings=False)
+    d.update(kw)
+    return synth.ModelShape(**d)
+
+
+def as_t(bits):
+    return torch.from_numpy(bf16_vals(bits))
+
+
+def torch_causal_forward(m, tokens):
+    """Full causal forward over the whole sequence with torch fp64 library ops
+    (F.rms_norm, F.scaled_dot_product_attention with is_causal and enable_gqa,
+    F.silu, matmul).  K and V are rounded to bf16 (via float32, torch's
+    rounding) after RoPE, as a bf16 cache holds them."""
+    s = m["shape"]
+    T, hd = len(tokens), s.head_dim
+    x = as_t(m["embed"])[torch.as_tensor(tokens, dtype=torch.long)]
+    pos = torch.arange(T, dtype=torch.float64)
+    inv = torch.tensor([s.rope_theta ** (-(2.0 * i) / hd) for i in range(hd // 2)], dtype=torch.float64)
+    ang = pos[:, None] * inv[None, :]
+    cos, sin = torch.cos(ang), torch.sin(ang)
+
+    def rope(t):  # t [heads, T, hd]
+        a, b = t[..., : hd // 2], t[..., hd // 2:]
+        return torch.cat([a * cos - b * sin, b * cos + a * sin], dim=-1)
+
+    def rb(t):
+        return t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+
+    for l in range(s.n_layers):
+        xn = F.rms_norm(x, (s.hidden,), as_t(m["attn_norm"][l]), eps=s.rms_eps)
+        q = (xn @ as_t(m["wq"][l]).T).view(T, s.n_q_heads, hd).transpose(0, 1)
+        k = (xn @ as_t(m["wk"][l]).T).view(T, s.n_kv_heads, hd).transpose(0, 1)
+        v = (xn @ as_t(m["wv"][l]).T).view(T, s.n_kv_heads, hd).transpose(0, 1)
+        q, k, v = rope(q), rb(rope(k)), rb(v)
+        o = F.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True, enable_gqa=True)[0]
+        x = x + o.transpose(0, 1).reshape(T, -1) @ as_t(m["wo"][l]).T
+        xn = F.rms_norm(x, (s.hidden,), as_t(m["ffn_norm"][l]), eps=s.rms_eps)
+        u = F.silu(xn @ as_t(m["w_gate"][l]).T) * (xn @ as_t(m["w_up"][l]).T)
+        x = x + u @ as_t(m["w_down"][l]).T
+    h = F.rms_norm(x, (s.hidden,), as_t(m["final_norm"]), eps=s.rms_eps)
+    lm = m["embed"] if m["lm_head"] is None else m["lm_head"]
+    return (h @ as_t(lm).T).numpy(), h.numpy()
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(tie_embeddings=True), dict(n_kv_heads=4), dict(n_kv_heads=1)])
+def test_decode_matches_torch_causal_forward(kw):
+    s = tiny_shape(**kw)
+    m = synth.make_model(s, seed=7, std=0.2, gains="normal")
+    tokens = synth.uniform_tokens(12, s.vocab, 7, 99)
+    want_logits, want_h = torch_causal_forward(m, tokens)
+    o = oracle.OracleDecoder(m, max_seq=16)
+    for p, t in enumerate(tokens):
+        lg, h = o.step(int(t), p)
+        np.testing.assert_allclose(lg, want_logits[p], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(h, want_h[p], rtol=1e-9, atol=1e-11)
+    # slots above the last position are untouched
+    assert not o.kcache[:, :, len(tokens):, :].any()
+
+
+def test_gqa_equals_mha_with_repeated_kv():
+    """q head h must read kv head h // (q_heads / kv_heads): a GQA model equals
+    the MHA model whose K/V projections repeat each kv head for its q heads."""
+    s = tiny_shape(n_q_heads=4, n_kv_heads=2)
+    m = synth.make_model(s, seed=11, std=0.2)
+    s2 = tiny_shape(n_q_heads=4, n_kv_heads=4)
+    m2 = dict(m, shape=s2)
+    hd = s.head_dim
+    rep = lambda w: np.concatenate([w[(h // 2) * hd:(h // 2 + 1) * hd] for h in range(4)], axis=0)
+    m2["wk"] = [rep(w) for w in m["wk"]]
+    m2["wv"] = [rep(w) for w in m["wv"]]
+    a, b = oracle.OracleDecoder(m, 8), oracle.OracleDecoder(m2, 8)
+    for p, t in enumerate([3, 9, 27, 4, 4]):
+        la, _ = a.step(t, p)
+        lb, _ = b.step(t, p)
+        np.testing.assert_allclose(la, lb, rtol=1e-12, atol=1e-14)
+
+
+def _hand_model(E, W_lm=None, wq=None, wk=None, wv=None, wo=None, wg=None, wu=None, wd=None):
+    """H=2, 1 layer, 1 q head / 1 kv head, head_dim 2, ffn 2; all gains 1."""
+    V = len(E)
+    s = synth.ModelShape(1, 2, 1, 1, 2, 2, V, 1e-5, 10000.0, W_lm is None)
+    z = np.zeros((2, 2))
+    f = lambda w: bf16_bits(z if w is None else w)
+    ones = bf16_bits(np.ones(2))
+    return {"shape": s, "embed": bf16_bits(E), "lm_head": None if W_lm is None else bf16_bits(W_lm),
+            "final_norm": ones, "attn_norm": [ones], "ffn_norm": [ones], "wq": [f(wq)], "wk": [f(wk)],
+            "wv": [f(wv)], "wo": [f(wo)], "w_gate": [f(wg)], "w_up": [f(wu)], "w_down": [f(wd)]}
+
+
+def _rms(x, eps=1e-5):
+    x = np.asarray(x, dtype=np.float64)
+    return x / math.sqrt(float(np.mean(x * x)) + eps)
+
+
+def test_brute_force_zeroed_blocks():
+    E = [[3.0, 4.0], [1.0, -1.0], [0.5, 2.0], [-2.0, 0.25]]
+    W_lm = [[1.0, 0.0], [0.0, 1.0], [1.0, 1.0], [-1.0, 0.5]]
+    o = oracle.OracleDecoder(_hand_model(E, W_lm=W_lm), 4)
+    for p, t in enumerate([0, 1, 2]):
+        lg, h = o.step(t, p)
+        np.testing.assert_allclose(h, _rms(E[t]), rtol=1e-15)
+        np.testing.assert_allclose(lg, np.array(W_lm) @ _rms(E[t]), rtol=1e-15)
+
+
+def test_brute_force_tied_zeroed_blocks_argmax():
+    E = np.array([[3.0, 4.0], [1.0, -1.0], [0.5, 2.0], [-2.0, 0.25], [4.0, 4.0]])
+    o = oracle.OracleDecoder(_hand_model(E), 4)
+    for t in range(len(E)):
+        lg, _ = o.step(t, 0)
+        want = E @ _rms(E[t])
+        np.testing.assert_allclose(lg, want, rtol=1e-15)
+        assert oracle.argmax_f32(lg)[0] == int(np.argmax(want))
+
+
+def test_brute_force_attention_adds_normed_value():
+    """W_q = W_k = 0 (all scores 0: uniform attention), W_v = W_o = I, FFN off."""
+    E = [[1.0, 1.0], [3.0, 4.0], [0.0, 1.0]]
+    W_lm = [[1.0, 0.0], [0.0, 1.0], [1.0, -1.0]]
+    I = np.eye(2)
+    o = oracle.OracleDecoder(_hand_model(E, W_lm=W_lm, wv=I, wo=I), 4)
+    # pos 0: the only value is bf16(RMSNorm(E[0])) = bf16(0.999995..) = 1.0
+    v0 = bf16_vals(bf16_bits(_rms(E[0])))
+    assert np.array_equal(v0, [1.0, 1.0])
+    lg, h = o.step(0, 0)
+    np.testing.assert_allclose(h, _rms(np.array(E[0]) + v0), rtol=1e-15)
+    # pos 1: the uniform average of both cached values is added
+    v1 = bf16_vals(bf16_bits(_rms(E[1])))
+    lg, h = o.step(1, 1)
+    np.testing.assert_allclose(h, _rms(np.array(E[1]) + (v0 + v1) / 2), rtol=1e-14)
+    np.testing.assert_allclose(lg, np.array(W_lm) @ h, rtol=1e-14)
+
+
+def test_brute_force_swiglu_branch():
+    E = [[3.0, 4.0], [1.0, -2.0]]
+    W_lm = [[1.0, 0.0], [0.0, 1.0]]
+    wg, wu, wd = np.eye(2), np.array([[2.0, 0.0], [0.0, -1.0]]), np.array([[1.0, 1.0], [0.0, 1.0]])
+    o = oracle.OracleDecoder(_hand_model(E, W_lm=W_lm, wg=wg, wu=wu, wd=wd), 4)
+    silu = lambda a: a / (1 + math.exp(-a))
+    for p, t in enumerate([0, 1]):
+        x = np.array(E[t])
+        xn = _rms(x)
+        u = np.array([silu(xn[0]) * 2 * xn[0], silu(xn[1]) * -xn[1]])
+        x2 = x + wd @ u
+        lg, h = o.step(t, p)
+        np.testing.assert_allclose(h, _rms(x2), rtol=1e-14)
+        np.testing.assert_allclose(lg, _rms(x2), rtol=1e-14)
+
+
+def test_kv_append_is_bf16_of_rotated_k():
+    s = tiny_shape()
+    m = synth.make_model(s, seed=5, std=0.3)
+    o = oracle.OracleDecoder(m, 8)
+    tokens = [7, 1, 30]
+    for p, t in enumerate(tokens):
+        o.step(t, p)
+    # recompute layer 0's K/V at position 2 from its definition with torch ops
+    x = as_t(m["embed"])[tokens[2]]
+    xn = F.rms_norm(x, (s.hidden,), as_t(m["attn_norm"][0]), eps=s.rms_eps).numpy()
+    k = as_t(m["wk"][0]).numpy() @ xn
+    v = as_t(m["wv"][0]).numpy() @ xn
+    for g in range(s.n_kv_heads):
+        kr = oracle.rope(k[g * 16:(g + 1) * 16], 2, s.rope_theta)
+        assert np.array_equal(o.kcache[0, g, 2], bf16_bits(kr))
+        assert np.array_equal(o.vcache[0, g, 2], bf16_bits(v[g * 16:(g + 1) * 16]))
