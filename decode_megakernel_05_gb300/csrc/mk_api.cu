@@ -1,0 +1,774 @@
+// mk_api.cu - host runtime and C ABI of the decode megakernel library (see
+// include/mk.h for the contract of every entry point).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_aux.h"
+#include "mk_internal.h"
+#include "mk_perop.h"
+
+extern "C" int mk_kernel_variant(int hd, int G, const void** fn);
+
+namespace {
+
+thread_local std::string g_cuda_err;
+
+int cuda_fail(cudaError_t e, const char* what) {
+    char buf[256];
+    snprintf(buf, sizeof buf, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+    g_cuda_err = buf;
+    return e == cudaErrorMemoryAllocation ? MK_ERR_OOM : MK_ERR_CUDA;
+}
+
+#define MK_CU(call)                                   \
+    do {                                              \
+        cudaError_t e_ = (call);                      \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+    } while (0)
+
+struct Maps {
+    std::vector<std::vector<MkRowCopy>> q, k, v, o, gate, up;
+    std::vector<std::vector<MkColCopy>> down;
+    std::vector<MkRowCopy> lm;
+};
+
+// Tuning with defaults applied (grid size needs the SM count).
+struct Tune {
+    int ns_req, slot, l2pf, grid;
+};
+
+Tune resolve_tuning(const mk_tuning* t) {
+    Tune r;
+    r.ns_req = (t && t->ring_stages > 0) ? t->ring_stages : 6;
+    r.slot = (t && t->slot_kib > 0) ? t->slot_kib * 1024 : 32 * 1024;
+    r.l2pf = (t && t->l2_prefetch_kib != 0) ? (t->l2_prefetch_kib < 0 ? 0 : t->l2_prefetch_kib * 1024) : 256 * 1024;
+    r.grid = (t && t->grid_ctas > 0) ? t->grid_ctas : 0;
+    return r;
+}
+
+// Shape checks shared by mk_create and the host layout utilities.
+int check_shape(const mk_config* c) {
+    if (!c) return MK_ERR_INVALID_ARG;
+    if (c->n_layers < 1 || c->hidden < 8 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 2 ||
+        c->ffn < 1 || c->vocab < 1 || c->max_seq < 1 || !(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f))
+        return MK_ERR_INVALID_ARG;
+    if (c->n_q_heads % c->n_kv_heads) return MK_ERR_INVALID_ARG;
+    if (c->head_dim != 64 && c->head_dim != 128) return MK_ERR_UNSUPPORTED;
+    const int G = c->n_q_heads / c->n_kv_heads;
+    const void* fn = nullptr;
+    if (mk_kernel_variant(c->head_dim, G, &fn) != 0) return MK_ERR_UNSUPPORTED;
+    auto pow2_ok = [](int K) {   // K/8 divides 512 or is a multiple of 512
+        if (K % 8) return false;
+        const int n = K / 8;
+        return (n <= MK_NCT) ? (MK_NCT % n == 0) : (n % MK_NCT == 0 && n / MK_NCT <= 2);
+    };
+    if (!pow2_ok(c->hidden) || !pow2_ok(G * c->head_dim)) return MK_ERR_UNSUPPORTED;
+    return MK_OK;
+}
+
+int build_geom(const mk_config* c, const Tune& tu, int grid, int ns, MkGeom& g) {
+    if (!mk_geom_init(g, c->n_layers, c->hidden, c->n_q_heads, c->n_kv_heads, c->head_dim, c->ffn, c->vocab,
+                      c->max_seq, grid, tu.slot, ns))
+        return MK_ERR_INVALID_ARG;
+    if (g.TRh < 2 || g.TRo < 2 || g.JD < 1 || g.KB < 1 || tu.slot % 16) return MK_ERR_INVALID_ARG;
+    if (ns < 1 || ns > 16) return MK_ERR_INVALID_ARG;
+    if (g.max_rows > 4096 || g.max_nj > 8192) return MK_ERR_UNSUPPORTED;
+    mk_smem_layout(g);
+    return MK_OK;
+}
+
+void build_plans(const MkGeom& g, std::vector<MkCtaPlan>& plans, int64_t& arena) {
+    plans.resize(g.nC);
+    int64_t off = 0;
+    for (int c = 0; c < g.nC; ++c) {
+        mk_cta_plan(g, c, plans[c]);
+        plans[c].stream_off = off;
+        off += mk_cta_stream_bytes(g, plans[c]);
+    }
+    arena = off;
+}
+
+void build_maps(const MkGeom& g, const std::vector<MkCtaPlan>& plans, Maps& m) {
+    const int L = g.L, H = g.H, KO = g.G * g.hd;
+    m.q.assign(L, {}); m.k.assign(L, {}); m.v.assign(L, {}); m.o.assign(L, {});
+    m.gate.assign(L, {}); m.up.assign(L, {}); m.down.assign(L, {}); m.lm.clear();
+    for (int c = 0; c < g.nC; ++c) {
+        const MkCtaPlan& p = plans[c];
+        for (int l = 0; l < L; ++l) {
+            const int64_t base = p.stream_off + (int64_t)l * p.layer_bytes;
+            int64_t off = base;
+            for (int r = 0; r < 2 * p.npairs; ++r) {
+                int mat, row;
+                mk_qkv_row(g, p.g, p.pair0 + r / 2, r % 2, mat, row);
+                MkRowCopy rc{off, row, 0, H};
+                (mat == 0 ? m.q : mat == 1 ? m.k : m.v)[l].push_back(rc);
+                off += (int64_t)H * 2;
+            }
+            for (int r = 0; r < p.norows; ++r) {
+                m.o[l].push_back(MkRowCopy{off, (int64_t)(p.orow0 + r), p.g * KO, KO});
+                off += (int64_t)KO * 2;
+            }
+            for (int j = 0; j < p.nj; j += g.JT) {
+                const int n = std::min(g.JT, p.nj - j);
+                for (int jj = 0; jj < n; ++jj)
+                    m.gate[l].push_back(MkRowCopy{off + (int64_t)jj * H * 2, (int64_t)(p.j0 + j + jj), 0, H});
+                for (int jj = 0; jj < n; ++jj)
+                    m.up[l].push_back(MkRowCopy{off + (int64_t)(n + jj) * H * 2, (int64_t)(p.j0 + j + jj), 0, H});
+                off += (int64_t)2 * n * H * 2;
+            }
+            if (p.nj > 0) m.down[l].push_back(MkColCopy{off, p.j0, p.nj});
+        }
+        int64_t off = p.stream_off + (int64_t)L * p.layer_bytes;
+        for (int r = 0; r < p.nv; ++r) {
+            m.lm.push_back(MkRowCopy{off, (int64_t)(p.v0 + r), 0, H});
+            off += (int64_t)H * 2;
+        }
+    }
+}
+
+// Walks every CTA's tile stream (as the kernel will) for a few positions and
+// checks that every bulk copy stays inside its buffer, is 16-byte aligned and
+// sized, fits a ring slot, and that the weight tiles cover each CTA's stream.
+bool check_schedule(const MkGeom& g, const std::vector<MkCtaPlan>& plans, int64_t arena_bytes) {
+    const uint8_t* A = reinterpret_cast<const uint8_t*>((uintptr_t)1 << 40);   // fake, aligned bases
+    const uint16_t* K = reinterpret_cast<const uint16_t*>((uintptr_t)1 << 41);
+    const uint16_t* Vc = reinterpret_cast<const uint16_t*>((uintptr_t)3 << 41);
+    const int64_t kv_bytes = (int64_t)g.L * g.kvh * g.max_seq * g.hd * 2;
+    const int poss[4] = {0, 1, g.max_seq / 2, g.max_seq - 1};
+    for (int pi = 0; pi < 4; ++pi) {
+        const int pos = poss[pi];
+        if (pos < 0 || pos >= g.max_seq) continue;
+        for (int c = 0; c < g.nC; ++c) {
+            const MkCtaPlan& pl = plans[c];
+            const int64_t lo = pl.stream_off, hi = pl.stream_off + mk_cta_stream_bytes(g, pl);
+            int64_t wbytes = 0;
+            bool ok = true;
+            mk_walk_tiles(g, pl, A, K, Vc, pos, [&](const void* src, uint32_t bytes) {
+                const uint8_t* s = reinterpret_cast<const uint8_t*>(src);
+                if (bytes == 0 || bytes % 16 || (int64_t)bytes > g.slot || ((uintptr_t)s & 15)) ok = false;
+                const uint8_t* kb = reinterpret_cast<const uint8_t*>(K);
+                const uint8_t* vb = reinterpret_cast<const uint8_t*>(Vc);
+                if (s >= kb && s < kb + kv_bytes) {
+                    if (s + bytes > kb + kv_bytes) ok = false;
+                } else if (s >= vb && s < vb + kv_bytes) {
+                    if (s + bytes > vb + kv_bytes) ok = false;
+                } else {
+                    const int64_t off = s - A;
+                    if (off < lo || off + bytes > hi || off + bytes > arena_bytes) ok = false;
+                    wbytes += bytes;
+                }
+            });
+            if (!ok || wbytes != (int64_t)g.L * pl.layer_bytes + (int64_t)pl.nv * g.H * 2) return false;
+        }
+    }
+    return true;
+}
+
+int64_t weight_bytes_per_token(const mk_config* c) {
+    const int64_t H = c->hidden, qd = (int64_t)c->n_q_heads * c->head_dim, kvd = (int64_t)c->n_kv_heads * c->head_dim;
+    const int64_t per_layer = qd * H + 2 * kvd * H + H * qd + 3 * (int64_t)c->ffn * H + 2 * H;
+    return 2 * ((int64_t)c->n_layers * per_layer + (int64_t)c->vocab * H + H + H);
+}
+
+}  // namespace
+
+struct mk_ctx {
+    mk_config cfg;
+    Tune tune;
+    MkGeom geo;
+    int device = 0, sm_count = 0;
+    const void* kernel = nullptr;
+    std::vector<MkCtaPlan> plans;
+    int64_t arena_bytes = 0, device_bytes = 0;
+    bool weights_loaded = false;
+    cudaStream_t last_stream = nullptr;
+    std::vector<void*> allocs;
+    // device buffers
+    uint8_t* arena = nullptr;
+    MkCtaPlan* d_plans = nullptr;
+    uint16_t *embed = nullptr, *kc = nullptr, *vc = nullptr;
+    float *attn_norm = nullptr, *ffn_norm = nullptr, *final_norm = nullptr, *rope_cos = nullptr, *rope_sin = nullptr;
+    float *qbuf = nullptr, *part_ml = nullptr, *part_acc = nullptr, *xacc = nullptr, *hidden = nullptr;
+    uint32_t *cnt = nullptr, *status = nullptr, *seq = nullptr;
+    unsigned long long* amax = nullptr;
+    int32_t *next_token = nullptr, *tokens_dev = nullptr, *prompt_dev = nullptr;
+    // debug
+    int dbg_skip_cta = -1, dbg_skip_sync = -1;
+    int64_t wait_limit_ns = 1000000000LL;
+    // per-operator baseline
+    bool perop_enabled = false, perop_ready = false;
+    MkPerOp perop{};
+
+    template <class T>
+    int dalloc(T** p, size_t bytes) {
+        void* q = nullptr;
+        cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+        allocs.push_back(q);
+        device_bytes += (int64_t)bytes;
+        *p = reinterpret_cast<T*>(q);
+        return MK_OK;
+    }
+};
+
+namespace {
+
+MkParams base_params(const mk_ctx* c) {
+    MkParams p;
+    memset(&p, 0, sizeof p);
+    p.geo = c->geo;
+    p.eps = c->cfg.rms_eps;
+    p.l2_pf_bytes = c->tune.l2pf;
+    p.arena = c->arena;
+    p.plans = c->d_plans;
+    p.embed = c->embed;
+    p.attn_norm = c->attn_norm;
+    p.ffn_norm = c->ffn_norm;
+    p.final_norm = c->final_norm;
+    p.kc = c->kc;
+    p.vc = c->vc;
+    p.rope_cos = c->rope_cos;
+    p.rope_sin = c->rope_sin;
+    p.qbuf = c->qbuf;
+    p.part_ml = c->part_ml;
+    p.part_acc = c->part_acc;
+    p.xacc = c->xacc;
+    p.hidden = c->hidden;
+    p.cnt = c->cnt;
+    p.amax = c->amax;
+    p.next_token = c->next_token;
+    p.status = c->status;
+    p.seq = c->seq;
+    p.dbg_skip_cta = c->dbg_skip_cta;
+    p.dbg_skip_sync = c->dbg_skip_sync;
+    p.wait_limit_ns = c->wait_limit_ns;
+    p.out_idx = 0;
+    return p;
+}
+
+int launch_step(mk_ctx* c, MkParams& p, cudaStream_t st) {
+    cudaLaunchConfig_t lc;
+    memset(&lc, 0, sizeof lc);
+    lc.gridDim = dim3(c->geo.nC);
+    lc.blockDim = dim3(MK_BLOCK);
+    lc.dynamicSmemBytes = c->geo.smem_bytes;
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    void* args[] = {&p};
+    MK_CU(cudaLaunchKernelExC(&lc, c->kernel, args));
+    c->last_stream = st;
+    return MK_OK;
+}
+
+int copy_matrix_to_device(const void* src, int on_device, size_t bytes, uint16_t* staging, const uint16_t** out,
+                          cudaStream_t st) {
+    if (on_device) { *out = reinterpret_cast<const uint16_t*>(src); return MK_OK; }
+    MK_CU(cudaMemcpyAsync(staging, src, bytes, cudaMemcpyHostToDevice, st));
+    *out = staging;
+    return MK_OK;
+}
+
+template <class T>
+int upload_ops(const std::vector<T>& v, T** d, size_t* cap, cudaStream_t st) {
+    if (v.empty()) return MK_OK;
+    if (v.size() > *cap) {
+        MK_CU(cudaStreamSynchronize(st));
+        if (*d) cudaFree(*d);
+        *d = nullptr;
+        MK_CU(cudaMalloc(reinterpret_cast<void**>(d), v.size() * sizeof(T)));
+        *cap = v.size();
+    }
+    MK_CU(cudaMemcpyAsync(*d, v.data(), v.size() * sizeof(T), cudaMemcpyHostToDevice, st));
+    // the host vector must outlive the copy: callers synchronize before reusing it
+    return MK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mk_strerror(int code) {
+    switch (code) {
+        case MK_OK: return "ok";
+        case MK_ERR_INVALID_ARG: return "invalid argument";
+        case MK_ERR_OOM: return "out of memory";
+        case MK_ERR_CUDA: return "CUDA runtime error";
+        case MK_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case MK_ERR_NUMERIC: return "non-finite logit";
+        case MK_ERR_STATE: return "call out of order";
+        case MK_ERR_UNSUPPORTED: return "shape not supported by the kernels";
+        default: return "unknown error";
+    }
+}
+
+const char* mk_last_cuda_error(void) { return g_cuda_err.c_str(); }
+
+int64_t mk_arena_bytes(const mk_config* cfg, const mk_tuning* tuning, int32_t grid_ctas) {
+    if (check_shape(cfg) != MK_OK || grid_ctas < 1) return -1;
+    Tune tu = resolve_tuning(tuning);
+    MkGeom g;
+    if (build_geom(cfg, tu, grid_ctas, 1, g) != MK_OK) return -1;
+    std::vector<MkCtaPlan> plans;
+    int64_t arena = 0;
+    build_plans(g, plans, arena);
+    return arena;
+}
+
+int mk_relayout_host(const mk_config* cfg, const mk_tuning* tuning, int32_t grid_ctas, const mk_weights* w,
+                     void* arena_out) {
+    int rc = check_shape(cfg);
+    if (rc != MK_OK) return rc;
+    if (!w || !arena_out || grid_ctas < 1 || w->on_device) return MK_ERR_INVALID_ARG;
+    if (!cfg->tie_embeddings && !w->lm_head) return MK_ERR_INVALID_ARG;
+    Tune tu = resolve_tuning(tuning);
+    MkGeom g;
+    if ((rc = build_geom(cfg, tu, grid_ctas, 1, g)) != MK_OK) return rc;
+    std::vector<MkCtaPlan> plans;
+    int64_t arena = 0;
+    build_plans(g, plans, arena);
+    Maps m;
+    build_maps(g, plans, m);
+    uint8_t* A = reinterpret_cast<uint8_t*>(arena_out);
+    memset(A, 0, (size_t)arena);
+    auto rows = [&](const std::vector<MkRowCopy>& ops, const void* src, int64_t cols) {
+        const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
+        for (const MkRowCopy& op : ops) memcpy(A + op.dst_off, s + op.src_row * cols + op.col0, (size_t)op.ncols * 2);
+    };
+    const int64_t H = g.H, qd = (int64_t)g.qh * g.hd;
+    for (int l = 0; l < g.L; ++l) {
+        rows(m.q[l], w->wq[l], H);
+        rows(m.k[l], w->wk[l], H);
+        rows(m.v[l], w->wv[l], H);
+        rows(m.o[l], w->wo[l], qd);
+        rows(m.gate[l], w->w_gate[l], H);
+        rows(m.up[l], w->w_up[l], H);
+        const uint16_t* d = reinterpret_cast<const uint16_t*>(w->w_down[l]);
+        for (const MkColCopy& op : m.down[l]) {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(A + op.dst_off);
+            for (int jj = 0; jj < op.nj; ++jj)
+                for (int64_t r = 0; r < H; ++r) dst[jj * H + r] = d[r * g.F + op.j0 + jj];
+        }
+    }
+    rows(m.lm, cfg->tie_embeddings ? w->embed : w->lm_head, H);
+    return MK_OK;
+}
+
+int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx** out) {
+    if (!out) return MK_ERR_INVALID_ARG;
+    *out = nullptr;
+    int rc = check_shape(cfg);
+    if (rc != MK_OK) return rc;
+    mk_ctx* c = new mk_ctx();
+    c->cfg = *cfg;
+    c->tune = resolve_tuning(tuning);
+    c->device = device;
+    auto fail = [&](int code) { mk_destroy(c); return code; };
+    cudaError_t e = cudaSetDevice(device);
+    if (e != cudaSuccess) return fail(cuda_fail(e, "cudaSetDevice"));
+    int smem_optin = 0;
+    if ((e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device)) != cudaSuccess)
+        return fail(cuda_fail(e, "cudaDeviceGetAttribute"));
+    const int kvh = cfg->n_kv_heads;
+    int grid = c->tune.grid ? c->tune.grid : kvh * (c->sm_count / kvh);
+    if (grid < kvh || grid % kvh || grid > c->sm_count) return fail(MK_ERR_INVALID_ARG);
+    // ring stages: as many as requested that fit the opt-in shared memory
+    int ns = std::min(c->tune.ns_req, 16);
+    for (;; --ns) {
+        if (ns < 1) return fail(MK_ERR_UNSUPPORTED);
+        MkGeom g;
+        if ((rc = build_geom(cfg, c->tune, grid, ns, g)) != MK_OK) return fail(rc);
+        if (g.smem_bytes + 1024 <= smem_optin) { c->geo = g; break; }
+    }
+    mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, &c->kernel);
+    if ((e = cudaFuncSetAttribute(c->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, c->geo.smem_bytes)) !=
+        cudaSuccess)
+        return fail(cuda_fail(e, "cudaFuncSetAttribute"));
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c->kernel, MK_BLOCK, c->geo.smem_bytes)) !=
+        cudaSuccess)
+        return fail(cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor"));
+    if (per_sm < 1) return fail(MK_ERR_UNSUPPORTED);
+    build_plans(c->geo, c->plans, c->arena_bytes);
+    if (!check_schedule(c->geo, c->plans, c->arena_bytes)) return fail(MK_ERR_STATE);
+
+    const MkGeom& g = c->geo;
+    const size_t L = g.L, H = g.H, V = g.V;
+    const size_t kv_elems = L * g.kvh * (size_t)g.max_seq * g.hd;
+    if ((rc = c->dalloc(&c->arena, (size_t)c->arena_bytes)) ||
+        (rc = c->dalloc(&c->d_plans, sizeof(MkCtaPlan) * g.nC)) ||
+        (rc = c->dalloc(&c->embed, V * H * 2)) || (rc = c->dalloc(&c->kc, kv_elems * 2)) ||
+        (rc = c->dalloc(&c->vc, kv_elems * 2)) || (rc = c->dalloc(&c->attn_norm, L * H * 4)) ||
+        (rc = c->dalloc(&c->ffn_norm, L * H * 4)) || (rc = c->dalloc(&c->final_norm, H * 4)) ||
+        (rc = c->dalloc(&c->rope_cos, (size_t)g.max_seq * (g.hd / 2) * 4)) ||
+        (rc = c->dalloc(&c->rope_sin, (size_t)g.max_seq * (g.hd / 2) * 4)) ||
+        (rc = c->dalloc(&c->qbuf, L * g.qh * g.hd * 4)) ||
+        (rc = c->dalloc(&c->part_ml, L * g.kvh * g.CPG * g.G * 2 * 4)) ||
+        (rc = c->dalloc(&c->part_acc, L * g.kvh * g.CPG * g.G * (size_t)g.hd * 4)) ||
+        (rc = c->dalloc(&c->xacc, 2 * 2 * L * H * 4)) || (rc = c->dalloc(&c->hidden, H * 4)) ||
+        (rc = c->dalloc(&c->cnt, (size_t)mk_cnt_total(g) * 4)) || (rc = c->dalloc(&c->status, 4)) ||
+        (rc = c->dalloc(&c->seq, 4)) || (rc = c->dalloc(&c->amax, 8)) || (rc = c->dalloc(&c->next_token, 4)) ||
+        (rc = c->dalloc(&c->tokens_dev, (size_t)g.max_seq * 4)) ||
+        (rc = c->dalloc(&c->prompt_dev, (size_t)g.max_seq * 4)))
+        return fail(rc);
+    cudaStream_t st = nullptr;
+    if ((e = cudaMemcpy(c->d_plans, c->plans.data(), sizeof(MkCtaPlan) * g.nC, cudaMemcpyHostToDevice)) ||
+        (e = cudaMemset(c->kc, 0, kv_elems * 2)) || (e = cudaMemset(c->vc, 0, kv_elems * 2)) ||
+        (e = cudaMemset(c->xacc, 0, 2 * 2 * L * H * 4)) || (e = cudaMemset(c->cnt, 0, (size_t)mk_cnt_total(g) * 4)) ||
+        (e = cudaMemset(c->status, 0, 4)) || (e = cudaMemset(c->seq, 0, 4)) || (e = cudaMemset(c->amax, 0, 8)) ||
+        (e = cudaMemset(c->next_token, 0, 4)) || (e = cudaMemset(c->tokens_dev, 0, (size_t)g.max_seq * 4)))
+        return fail(cuda_fail(e, "context init"));
+    if ((e = mk_launch_rope_table(c->rope_cos, c->rope_sin, g.max_seq, g.hd, (double)cfg->rope_theta, st)) ||
+        (e = cudaDeviceSynchronize()))
+        return fail(cuda_fail(e, "rope table"));
+    *out = c;
+    return MK_OK;
+}
+
+void mk_destroy(mk_ctx* c) {
+    if (!c) return;
+    cudaSetDevice(c->device);
+    for (void* p : c->allocs) cudaFree(p);
+    for (uint16_t* p : c->perop.wqkv) cudaFree(p);
+    for (uint16_t* p : c->perop.wo) cudaFree(p);
+    for (uint16_t* p : c->perop.wgu) cudaFree(p);
+    for (uint16_t* p : c->perop.wd) cudaFree(p);
+    delete c;
+}
+
+int mk_enable_perop(mk_ctx* c, int32_t keep_rowmajor) {
+    if (!c) return MK_ERR_INVALID_ARG;
+    if (c->weights_loaded && keep_rowmajor && !c->perop_ready) return MK_ERR_STATE;
+    c->perop_enabled = keep_rowmajor != 0;
+    return MK_OK;
+}
+
+int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
+    if (!c || !w) return MK_ERR_INVALID_ARG;
+    const mk_config& cfg = c->cfg;
+    if (!w->embed || !w->final_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo || !w->ffn_norm ||
+        !w->w_gate || !w->w_up || !w->w_down)
+        return MK_ERR_INVALID_ARG;
+    if (cfg.tie_embeddings ? (w->lm_head != nullptr) : (w->lm_head == nullptr)) return MK_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    MK_CU(cudaSetDevice(c->device));
+    const MkGeom& g = c->geo;
+    const size_t H = g.H, F = g.F, V = g.V, qd = (size_t)g.qh * g.hd, kvd = (size_t)g.kvh * g.hd;
+    const int on_dev = w->on_device ? 1 : 0;
+    if (on_dev) {   // the device gathers copy 16-byte chunks
+        auto al = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
+        bool ok = al(w->embed) && (!w->lm_head || al(w->lm_head));
+        for (int l = 0; l < g.L && ok; ++l)
+            ok = al(w->wq[l]) && al(w->wk[l]) && al(w->wv[l]) && al(w->wo[l]) && al(w->w_gate[l]) &&
+                 al(w->w_up[l]) && al(w->w_down[l]);
+        if (!ok) return MK_ERR_INVALID_ARG;
+    }
+    Maps m;
+    build_maps(g, c->plans, m);
+
+    uint16_t* staging = nullptr;
+    size_t staging_elems = 0;
+    if (!on_dev) {
+        staging_elems = std::max({V * H, F * H, qd * H, kvd * H, H});
+        MK_CU(cudaMalloc(&staging, staging_elems * 2));
+    }
+    MkRowCopy* d_rows = nullptr;
+    MkColCopy* d_cols = nullptr;
+    size_t cap_rows = 0, cap_cols = 0;
+    uint16_t* gain_tmp = nullptr;
+    int rc = MK_OK;
+    auto cleanup = [&]() {
+        cudaStreamSynchronize(st);
+        if (staging) cudaFree(staging);
+        if (d_rows) cudaFree(d_rows);
+        if (d_cols) cudaFree(d_cols);
+        if (gain_tmp) cudaFree(gain_tmp);
+    };
+#define MK_TRY(x)                       \
+    do {                                \
+        rc = (x);                       \
+        if (rc != MK_OK) { cleanup(); return rc; } \
+    } while (0)
+#define MK_TRYCU(x)                     \
+    do {                                \
+        cudaError_t e_ = (x);           \
+        if (e_ != cudaSuccess) { rc = cuda_fail(e_, #x); cleanup(); return rc; } \
+    } while (0)
+
+    auto gather_rows = [&](const std::vector<MkRowCopy>& ops, const void* src, size_t rows, size_t cols) -> int {
+        const uint16_t* d = nullptr;
+        int r = copy_matrix_to_device(src, on_dev, rows * cols * 2, staging, &d, st);
+        if (r != MK_OK) return r;
+        r = upload_ops(ops, &d_rows, &cap_rows, st);
+        if (r != MK_OK) return r;
+        cudaError_t e = mk_launch_relayout_rows(c->arena, d, (int64_t)cols, d_rows, (int)ops.size(), st);
+        if (e != cudaSuccess) return cuda_fail(e, "relayout rows");
+        e = cudaStreamSynchronize(st);   // staging and the op buffer are reused by the next matrix
+        return e == cudaSuccess ? MK_OK : cuda_fail(e, "relayout rows sync");
+    };
+    // per-operator copies (plain row-major) of the same weights, when enabled
+    auto keep_rowmajor = [&](uint16_t** dst, const void* src, size_t elems, size_t dst_off_elems) -> int {
+        cudaError_t e = cudaMemcpyAsync(*dst + dst_off_elems, src, elems * 2, cudaMemcpyDefault, st);
+        return e == cudaSuccess ? MK_OK : cuda_fail(e, "row-major copy");
+    };
+    if (c->perop_enabled && !c->perop_ready) {
+        MkPerOp& P = c->perop;
+        P.wqkv.assign(g.L, nullptr); P.wo.assign(g.L, nullptr); P.wgu.assign(g.L, nullptr); P.wd.assign(g.L, nullptr);
+        for (int l = 0; l < g.L; ++l) {
+            MK_TRYCU(cudaMalloc(&P.wqkv[l], (qd + 2 * kvd) * H * 2));
+            MK_TRYCU(cudaMalloc(&P.wo[l], H * qd * 2));
+            MK_TRYCU(cudaMalloc(&P.wgu[l], 2 * F * H * 2));
+            MK_TRYCU(cudaMalloc(&P.wd[l], H * F * 2));
+        }
+    }
+
+    for (int l = 0; l < g.L; ++l) {
+        MK_TRY(gather_rows(m.q[l], w->wq[l], qd, H));
+        MK_TRY(gather_rows(m.k[l], w->wk[l], kvd, H));
+        MK_TRY(gather_rows(m.v[l], w->wv[l], kvd, H));
+        MK_TRY(gather_rows(m.o[l], w->wo[l], H, qd));
+        MK_TRY(gather_rows(m.gate[l], w->w_gate[l], F, H));
+        MK_TRY(gather_rows(m.up[l], w->w_up[l], F, H));
+        {
+            const uint16_t* d = nullptr;
+            MK_TRY(copy_matrix_to_device(w->w_down[l], on_dev, H * F * 2, staging, &d, st));
+            MK_TRY(upload_ops(m.down[l], &d_cols, &cap_cols, st));
+            MK_TRYCU(mk_launch_relayout_cols(c->arena, d, (int)H, (int)F, d_cols, (int)m.down[l].size(), st));
+            MK_TRYCU(cudaStreamSynchronize(st));
+        }
+        if (c->perop_enabled && !c->perop_ready) {
+            MkPerOp& P = c->perop;
+            MK_TRY(keep_rowmajor(&P.wqkv[l], w->wq[l], qd * H, 0));
+            MK_TRY(keep_rowmajor(&P.wqkv[l], w->wk[l], kvd * H, qd * H));
+            MK_TRY(keep_rowmajor(&P.wqkv[l], w->wv[l], kvd * H, (qd + kvd) * H));
+            MK_TRY(keep_rowmajor(&P.wo[l], w->wo[l], H * qd, 0));
+            MK_TRY(keep_rowmajor(&P.wgu[l], w->w_gate[l], F * H, 0));
+            MK_TRY(keep_rowmajor(&P.wgu[l], w->w_up[l], F * H, F * H));
+            MK_TRY(keep_rowmajor(&P.wd[l], w->w_down[l], H * F, 0));
+            MK_TRYCU(cudaStreamSynchronize(st));
+        }
+    }
+    MK_TRY(gather_rows(m.lm, cfg.tie_embeddings ? w->embed : w->lm_head, V, H));
+    MK_TRYCU(cudaMemcpyAsync(c->embed, w->embed, V * H * 2, cudaMemcpyDefault, st));
+    // norm gains: bf16 -> fp32 on the device
+    MK_TRYCU(cudaMalloc(&gain_tmp, H * 2));
+    auto gain = [&](const void* src, float* dst) -> int {
+        cudaError_t e = cudaMemcpyAsync(gain_tmp, src, H * 2, cudaMemcpyDefault, st);
+        if (e == cudaSuccess) e = mk_launch_bf16_to_f32(gain_tmp, dst, (int64_t)H, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        return e == cudaSuccess ? MK_OK : cuda_fail(e, "norm gains");
+    };
+    for (int l = 0; l < g.L; ++l) {
+        MK_TRY(gain(w->attn_norm[l], c->attn_norm + (size_t)l * H));
+        MK_TRY(gain(w->ffn_norm[l], c->ffn_norm + (size_t)l * H));
+    }
+    MK_TRY(gain(w->final_norm, c->final_norm));
+    if (c->perop_enabled && !c->perop_ready) {
+        MkPerOp& P = c->perop;
+        P.L = g.L; P.H = g.H; P.qh = g.qh; P.kvh = g.kvh; P.hd = g.hd; P.F = g.F; P.V = g.V; P.max_seq = g.max_seq;
+        P.eps = cfg.rms_eps;
+        P.attn_chunk = 1024;
+        P.amax_blocks = 256;
+        P.embed = c->embed;
+        if (cfg.tie_embeddings) {
+            P.lm = c->embed;
+        } else {
+            uint16_t* lm = nullptr;
+            MK_TRYCU(cudaMalloc(&lm, V * H * 2));
+            c->allocs.push_back(lm);
+            MK_TRYCU(cudaMemcpyAsync(lm, w->lm_head, V * H * 2, cudaMemcpyDefault, st));
+            P.lm = lm;
+        }
+        P.attn_norm = c->attn_norm; P.ffn_norm = c->ffn_norm; P.final_norm = c->final_norm;
+        P.rope_cos = c->rope_cos; P.rope_sin = c->rope_sin; P.kc = c->kc; P.vc = c->vc;
+        const size_t nsplit_max = ((size_t)g.max_seq + P.attn_chunk - 1) / P.attn_chunk;
+        MK_TRY(c->dalloc(&P.x, H * 4)); MK_TRY(c->dalloc(&P.xn, H * 4));
+        MK_TRY(c->dalloc(&P.qkv, (qd + 2 * kvd) * 4)); MK_TRY(c->dalloc(&P.attn, qd * 4));
+        MK_TRY(c->dalloc(&P.u, F * 4)); MK_TRY(c->dalloc(&P.hidden, H * 4));
+        MK_TRY(c->dalloc(&P.pml, (size_t)g.qh * nsplit_max * 2 * 4));
+        MK_TRY(c->dalloc(&P.pacc, (size_t)g.qh * nsplit_max * g.hd * 4));
+        MK_TRY(c->dalloc(&P.logits_tmp, V * 4));
+        MK_TRY(c->dalloc(&P.amax_part, (size_t)P.amax_blocks * 8));
+        P.next_token = c->next_token;
+        P.status = c->status;
+        const int smem_need = (int)std::max({H, F, qd, (size_t)(g.hd + P.attn_chunk)}) * 4;
+        MK_TRYCU(mk_perop_prepare(smem_need));
+        c->perop_ready = true;
+    }
+    cleanup();
+    c->weights_loaded = true;
+    c->last_stream = st;
+#undef MK_TRY
+#undef MK_TRYCU
+    return MK_OK;
+}
+
+int mk_set_kv(mk_ctx* c, int32_t layer, const void* k, const void* v, int32_t n_pos, void* stream) {
+    if (!c || !k || !v || layer < 0 || layer >= c->geo.L || n_pos < 0 || n_pos > c->geo.max_seq)
+        return MK_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    MK_CU(cudaSetDevice(c->device));
+    const MkGeom& g = c->geo;
+    const size_t row = (size_t)n_pos * g.hd * 2;
+    for (int h = 0; h < g.kvh; ++h) {
+        const size_t dst = (((size_t)layer * g.kvh + h) * g.max_seq) * g.hd;
+        MK_CU(cudaMemcpyAsync(c->kc + dst, (const uint8_t*)k + h * row, row, cudaMemcpyDefault, st));
+        MK_CU(cudaMemcpyAsync(c->vc + dst, (const uint8_t*)v + h * row, row, cudaMemcpyDefault, st));
+    }
+    MK_CU(cudaStreamSynchronize(st));
+    return MK_OK;
+}
+
+int mk_get_kv(mk_ctx* c, int32_t layer, int32_t pos0, int32_t n_pos, void* k_out, void* v_out, void* stream) {
+    if (!c || !k_out || !v_out || layer < 0 || layer >= c->geo.L || pos0 < 0 || n_pos < 0 ||
+        (int64_t)pos0 + n_pos > c->geo.max_seq)
+        return MK_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    MK_CU(cudaSetDevice(c->device));
+    const MkGeom& g = c->geo;
+    const size_t row = (size_t)n_pos * g.hd * 2;
+    for (int h = 0; h < g.kvh; ++h) {
+        const size_t src = (((size_t)layer * g.kvh + h) * g.max_seq + pos0) * g.hd;
+        MK_CU(cudaMemcpyAsync((uint8_t*)k_out + h * row, c->kc + src, row, cudaMemcpyDefault, st));
+        MK_CU(cudaMemcpyAsync((uint8_t*)v_out + h * row, c->vc + src, row, cudaMemcpyDefault, st));
+    }
+    MK_CU(cudaStreamSynchronize(st));
+    return MK_OK;
+}
+
+int mk_decode_step(mk_ctx* c, int32_t token, int32_t pos, float* logits_out, void* stream) {
+    if (!c) return MK_ERR_INVALID_ARG;
+    if (!c->weights_loaded) return MK_ERR_STATE;
+    if (token < 0 || token >= c->geo.V || pos < 0 || pos >= c->geo.max_seq) return MK_ERR_INVALID_ARG;
+    MkParams p = base_params(c);
+    p.pos = pos;
+    p.token = token;
+    p.token_ptr = nullptr;
+    p.logits = logits_out;
+    p.tokens_out = nullptr;
+    return launch_step(c, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mk_decode_step_greedy(mk_ctx* c, int32_t pos, float* logits_out, void* stream) {
+    if (!c) return MK_ERR_INVALID_ARG;
+    if (!c->weights_loaded) return MK_ERR_STATE;
+    if (pos < 0 || pos >= c->geo.max_seq) return MK_ERR_INVALID_ARG;
+    MkParams p = base_params(c);
+    p.pos = pos;
+    p.token_ptr = c->next_token;
+    p.logits = logits_out;
+    p.tokens_out = nullptr;
+    return launch_step(c, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mk_generate_greedy(mk_ctx* c, const int32_t* prompt, int32_t n_prompt, int32_t start_pos, int32_t n_new,
+                       int32_t* out_tokens, void* stream) {
+    if (!c || !prompt || !out_tokens || n_prompt < 1 || n_new < 1 || start_pos < 0) return MK_ERR_INVALID_ARG;
+    if (!c->weights_loaded) return MK_ERR_STATE;
+    const int64_t steps = (int64_t)n_prompt + n_new - 1;
+    if (start_pos + steps > c->geo.max_seq) return MK_ERR_INVALID_ARG;
+    for (int i = 0; i < n_prompt; ++i)
+        if (prompt[i] < 0 || prompt[i] >= c->geo.V) return MK_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    MK_CU(cudaMemcpyAsync(c->prompt_dev, prompt, (size_t)n_prompt * 4, cudaMemcpyHostToDevice, st));
+    for (int64_t k = 0; k < steps; ++k) {
+        MkParams p = base_params(c);
+        p.pos = (int32_t)(start_pos + k);
+        p.token = 0;
+        p.token_ptr = (k < n_prompt) ? c->prompt_dev + k : c->next_token;
+        p.logits = nullptr;
+        p.tokens_out = (k >= n_prompt - 1) ? c->tokens_dev : nullptr;
+        p.out_idx = (int32_t)(k - (n_prompt - 1));
+        int rc = launch_step(c, p, st);
+        if (rc != MK_OK) return rc;
+    }
+    MK_CU(cudaMemcpyAsync(out_tokens, c->tokens_dev, (size_t)n_new * 4, cudaMemcpyDeviceToHost, st));
+    MK_CU(cudaStreamSynchronize(st));
+    return mk_status(c);
+}
+
+int mk_get_hidden(mk_ctx* c, float* out, void* stream) {
+    if (!c || !out) return MK_ERR_INVALID_ARG;
+    MK_CU(cudaMemcpyAsync(out, c->hidden, (size_t)c->geo.H * 4, cudaMemcpyDeviceToDevice,
+                          reinterpret_cast<cudaStream_t>(stream)));
+    return MK_OK;
+}
+
+int mk_get_argmax(mk_ctx* c, int32_t* out, void* stream) {
+    if (!c || !out) return MK_ERR_INVALID_ARG;
+    MK_CU(cudaMemcpyAsync(out, c->next_token, 4, cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
+    return MK_OK;
+}
+
+int mk_status(mk_ctx* c) {
+    if (!c) return MK_ERR_INVALID_ARG;
+    MK_CU(cudaSetDevice(c->device));
+    MK_CU(cudaStreamSynchronize(c->last_stream));
+    uint32_t st = 0;
+    MK_CU(cudaMemcpy(&st, c->status, 4, cudaMemcpyDeviceToHost));
+    MK_CU(cudaMemset(c->status, 0, 4));
+    if (st & (MK_ST_TIMEOUT | MK_ST_SCHEDULE)) return MK_ERR_DEVICE_TIMEOUT;
+    if (st & MK_ST_NUMERIC) return MK_ERR_NUMERIC;
+    if (st & MK_ST_BADTOKEN) return MK_ERR_INVALID_ARG;
+    return MK_OK;
+}
+
+int mk_decode_step_perop(mk_ctx* c, int32_t token, int32_t pos, float* logits_out, void* stream,
+                         int32_t* n_launches) {
+    if (!c) return MK_ERR_INVALID_ARG;
+    if (!c->weights_loaded || !c->perop_ready) return MK_ERR_STATE;
+    if (token < 0 || token >= c->geo.V || pos < 0 || pos >= c->geo.max_seq) return MK_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    const int n = mk_perop_step(c->perop, token, nullptr, pos, logits_out, st, &e);
+    if (e != cudaSuccess) return cuda_fail(e, "per-operator step");
+    if (n_launches) *n_launches = n;
+    c->last_stream = st;
+    return MK_OK;
+}
+
+int mk_get_info(const mk_ctx* c, mk_info* o) {
+    if (!c || !o) return MK_ERR_INVALID_ARG;
+    memset(o, 0, sizeof *o);
+    o->grid_ctas = c->geo.nC;
+    o->ctas_per_group = c->geo.CPG;
+    o->block_threads = MK_BLOCK;
+    o->ring_stages = c->geo.ns;
+    o->slot_bytes = c->geo.slot;
+    o->smem_bytes = c->geo.smem_bytes;
+    o->sm_count = c->sm_count;
+    o->l2_prefetch_bytes = c->tune.l2pf;
+    o->arena_bytes = c->arena_bytes;
+    o->weight_bytes_per_token = weight_bytes_per_token(&c->cfg);
+    o->kv_bytes_per_position = (int64_t)2 * c->geo.L * c->geo.kvh * c->geo.hd * 2;
+    o->device_bytes = c->device_bytes;
+    return MK_OK;
+}
+
+int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
+    if (!c) return MK_ERR_INVALID_ARG;
+    if (knob == MK_DBG_SKIP_ARRIVAL) {
+        if (value < 0) { c->dbg_skip_cta = -1; c->dbg_skip_sync = -1; }
+        else { c->dbg_skip_cta = (int)(value >> 16); c->dbg_skip_sync = (int)(value & 0xFFFF); }
+        return MK_OK;
+    }
+    if (knob == MK_DBG_WAIT_LIMIT_NS) {
+        if (value < 1000) return MK_ERR_INVALID_ARG;
+        c->wait_limit_ns = value;
+        return MK_OK;
+    }
+    return MK_ERR_INVALID_ARG;
+}
+
+}  // extern "C"

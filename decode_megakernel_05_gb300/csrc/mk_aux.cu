@@ -1,0 +1,76 @@
+// mk_aux.cu - one-time device kernels used when a context is set up: the weight
+// re-layout gathers, the RoPE cos/sin table and the widening of norm gains.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "mk_aux.h"
+
+// One block per stored row: copy ncols bf16 (a multiple of 8) from
+// src[src_row][col0 ..] to arena + dst_off, 16 bytes per thread step.
+__global__ void mk_relayout_rows_kernel(uint8_t* arena, const uint16_t* src, int64_t src_cols, const MkRowCopy* ops,
+                                        int n) {
+    const int i = blockIdx.x;
+    if (i >= n) return;
+    const MkRowCopy op = ops[i];
+    const uint4* s = reinterpret_cast<const uint4*>(src + op.src_row * src_cols + op.col0);
+    uint4* d = reinterpret_cast<uint4*>(arena + op.dst_off);
+    for (int k = threadIdx.x; k < op.ncols / 8; k += blockDim.x) d[k] = s[k];
+}
+
+// Column gather of W_down [H][F]: arena + dst_off receives columns j0 .. j0+nj-1,
+// each as H contiguous bf16.  Block (op, row chunk); thread = one row.
+__global__ void mk_relayout_cols_kernel(uint8_t* arena, const uint16_t* src, int H, int F, const MkColCopy* ops,
+                                        int n) {
+    const int i = blockIdx.x;
+    if (i >= n) return;
+    const MkColCopy op = ops[i];
+    const int r = blockIdx.y * blockDim.x + threadIdx.x;
+    if (r >= H) return;
+    uint16_t* d = reinterpret_cast<uint16_t*>(arena + op.dst_off);
+    const uint16_t* s = src + (int64_t)r * F + op.j0;
+    for (int jj = 0; jj < op.nj; ++jj) d[(int64_t)jj * H + r] = s[jj];
+}
+
+// cos/sin of pos * theta^(-2i/hd) for pos < max_seq, i < hd/2, evaluated in
+// double and stored as float [max_seq][hd/2].
+__global__ void mk_rope_table_kernel(float* cs, float* sn, int max_seq, int hd, double theta) {
+    const int half = hd / 2;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (int64_t)max_seq * half) return;
+    const int pos = (int)(idx / half), i = (int)(idx % half);
+    const double inv = pow(theta, -(2.0 * (double)i) / (double)hd);
+    double s, c;
+    sincos((double)pos * inv, &s, &c);
+    cs[idx] = (float)c;
+    sn[idx] = (float)s;
+}
+
+__global__ void mk_bf16_to_f32_kernel(const uint16_t* src, float* dst, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = __uint_as_float((uint32_t)src[i] << 16);
+}
+
+cudaError_t mk_launch_relayout_rows(uint8_t* arena, const uint16_t* src, int64_t src_cols, const MkRowCopy* ops, int n,
+                                    cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    mk_relayout_rows_kernel<<<n, 128, 0, st>>>(arena, src, src_cols, ops, n);
+    return cudaGetLastError();
+}
+cudaError_t mk_launch_relayout_cols(uint8_t* arena, const uint16_t* src, int H, int F, const MkColCopy* ops, int n,
+                                    cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    dim3 grid(n, (H + 255) / 256);
+    mk_relayout_cols_kernel<<<grid, 256, 0, st>>>(arena, src, H, F, ops, n);
+    return cudaGetLastError();
+}
+cudaError_t mk_launch_rope_table(float* cs, float* sn, int max_seq, int hd, double theta, cudaStream_t st) {
+    const int64_t n = (int64_t)max_seq * (hd / 2);
+    mk_rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(cs, sn, max_seq, hd, theta);
+    return cudaGetLastError();
+}
+cudaError_t mk_launch_bf16_to_f32(const uint16_t* src, float* dst, int64_t n, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    mk_bf16_to_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, dst, n);
+    return cudaGetLastError();
+}

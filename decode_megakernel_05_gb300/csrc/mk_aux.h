@@ -1,0 +1,21 @@
+// mk_aux.h - set-up kernels and the re-layout copy descriptors (internal).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+struct MkRowCopy {     // arena + dst_off <- src[src_row][col0 .. col0 + ncols)
+    int64_t dst_off;
+    int64_t src_row;
+    int32_t col0, ncols;
+};
+struct MkColCopy {     // arena + dst_off <- columns j0 .. j0+nj-1 of W_down, each H contiguous
+    int64_t dst_off;
+    int32_t j0, nj;
+};
+
+cudaError_t mk_launch_relayout_rows(uint8_t* arena, const uint16_t* src, int64_t src_cols, const MkRowCopy* ops, int n,
+                                    cudaStream_t st);
+cudaError_t mk_launch_relayout_cols(uint8_t* arena, const uint16_t* src, int H, int F, const MkColCopy* ops, int n,
+                                    cudaStream_t st);
+cudaError_t mk_launch_rope_table(float* cs, float* sn, int max_seq, int hd, double theta, cudaStream_t st);
+cudaError_t mk_launch_bf16_to_f32(const uint16_t* src, float* dst, int64_t n, cudaStream_t st);

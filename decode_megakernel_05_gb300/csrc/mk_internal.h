@@ -1,0 +1,245 @@
+// mk_internal.h - layout and launch description shared by the host runtime and
+// the decode megakernel.  Nothing here is part of the public ABI.
+//
+// Weight arena layout (the offline re-layout, "lay weights out in memory-access
+// order ahead of time", cloud.baidu.com/article/9434380, section 9).
+//
+//   nC  = CTAs of the persistent grid, kvh | nC, CPG = nC / kvh CTAs per KV group
+//   G   = qh / kvh query heads per KV group, hd2 = hd / 2
+//   CTA c belongs to KV group g = c / CPG and has index i = c % CPG in it.
+//   split(n, parts, k) = [floor(k n / parts), floor((k+1) n / parts))
+//
+// Each CTA owns one contiguous byte stream (256-byte aligned start) holding
+// every weight tile it reads during one decode step, in consumption order:
+//   for layer l:
+//     QKV : pairs p in split(NP, CPG, i), NP = (G + 2) * hd2.  Pair p is head
+//           slot s = p / hd2 (s < G: query head g*G + s; s == G: key head g;
+//           s == G + 1: value head g) and dim d = p % hd2; it is stored as the
+//           two rows (d, d + hd2) of that head, each H bf16, so a RoPE pair
+//           never leaves the CTA.
+//     O   : rows r in split(H, CPG, i) of W_o, columns [g*G*hd, (g+1)*G*hd):
+//           each stored row is the G*hd slice this KV group's heads feed.
+//     GU  : j in split(F, nC, c) = [j0, j0 + nj), in groups of JT: the gate rows
+//           of the group, then the up rows of the same j's.
+//     D   : columns j0 .. j0 + nj - 1 of W_down, each stored as H contiguous bf16.
+//   LM    : rows v in split(V, nC, c) of the LM head (the embedding when tied).
+// A tile is TRh rows (QKV, LM), TRo rows (O), one GU group, or JD columns (D);
+// the last tile of a block may be short.  Every tile is a multiple of 16 bytes.
+#pragma once
+#include <stdint.h>
+
+#define MK_NCW 16                    // consumer warps
+#define MK_NCT (MK_NCW * 32)         // consumer threads
+#define MK_PRODUCER_WARP MK_NCW      // bulk-copy producer
+#define MK_PREFETCH_WARP (MK_NCW + 1)// L2 prefetch walker
+#define MK_BLOCK ((MK_NCW + 2) * 32) // 576 threads
+
+// Device status word bits.
+#define MK_ST_TIMEOUT 0x1u
+#define MK_ST_NUMERIC 0x2u
+#define MK_ST_BADTOKEN 0x4u
+#define MK_ST_SCHEDULE 0x8u
+#define MK_ST_ABORT 0x80000000u
+
+#ifdef __CUDACC__
+#define MK_HD __host__ __device__ __forceinline__
+#else
+#define MK_HD inline
+#endif
+
+MK_HD int64_t mk_split(int64_t n, int64_t parts, int64_t k) { return (k * n) / parts; }
+
+// Rows per tile for a row-major GEMV tile of K bf16 columns.  The consumer
+// mapping gives each thread 8 consecutive columns; NCt = min(K/8, 512)
+// threads share a row, RG = 512/NCt row groups, at most 4 rows per thread.
+MK_HD int mk_gemv_nct(int K) { return (K / 8) < MK_NCT ? (K / 8) : MK_NCT; }
+MK_HD int mk_tile_rows(int K, int slot_bytes) {
+    int rg = MK_NCT / mk_gemv_nct(K);
+    int r = slot_bytes / (2 * K);
+    if (r > 4 * rg) r = 4 * rg;
+    return r & ~1;
+}
+
+struct MkCtaPlan {
+    int64_t stream_off;   // byte offset of this CTA's stream in the arena
+    int64_t layer_bytes;  // bytes of one layer's tiles in the stream
+    int32_t g, i;         // KV group, index in the group
+    int32_t pair0, npairs;
+    int32_t orow0, norows;
+    int32_t j0, nj;
+    int32_t v0, nv;
+};
+
+struct MkGeom {
+    int32_t L, H, qh, kvh, hd, F, V, max_seq;
+    int32_t G, CPG, nC, NP;
+    int32_t slot, ns;            // ring slot bytes, ring stages
+    int32_t TRh, TRo, JT, JD, KB;
+    int32_t max_rows, max_nj;    // per-CTA maxima (QKV rows, FFN slice)
+    int32_t smem_bytes;
+    // shared-memory carve-up (byte offsets from the dynamic smem base)
+    int32_t off_full, off_empty, off_xv, off_ov, off_acc, off_rows, off_u, off_red, off_sc, off_misc;
+};
+
+// Fills everything but smem offsets from the shape; returns false if the
+// shape is outside what the kernels support.
+MK_HD bool mk_geom_init(MkGeom& g, int L, int H, int qh, int kvh, int hd, int F, int V, int max_seq, int nC,
+                        int slot_bytes, int ns) {
+    g.L = L; g.H = H; g.qh = qh; g.kvh = kvh; g.hd = hd; g.F = F; g.V = V; g.max_seq = max_seq;
+    if (L < 1 || H < 8 || qh < 1 || kvh < 1 || F < 1 || V < 1 || max_seq < 1 || nC < 1) return false;
+    if (qh % kvh != 0 || nC % kvh != 0) return false;
+    g.G = qh / kvh;
+    g.CPG = nC / kvh;
+    g.nC = nC;
+    g.NP = (g.G + 2) * (hd / 2);
+    g.slot = slot_bytes;
+    g.ns = ns;
+    g.TRh = mk_tile_rows(H, slot_bytes);
+    g.TRo = mk_tile_rows(g.G * hd, slot_bytes);
+    g.JT = g.TRh / 2;
+    g.JD = slot_bytes / (2 * H);
+    g.KB = slot_bytes / (2 * hd);
+    g.max_rows = 2 * (int)((g.NP + g.CPG - 1) / g.CPG);
+    g.max_nj = (F + nC - 1) / nC;
+    return true;
+}
+
+// Shared-memory carve-up; returns total bytes.
+MK_HD int mk_smem_layout(MkGeom& g) {
+    int o = g.ns * g.slot;                    // ring (1024-aligned base)
+    g.off_full = o; o += 8 * g.ns;
+    g.off_empty = o; o += 8 * g.ns;
+    o = (o + 15) & ~15;
+    g.off_xv = o; o += 4 * g.H;               // normalised GEMV input / down-proj combine
+    g.off_ov = o; o += 4 * g.G * g.hd;        // q (attention) then o (O-proj input)
+    g.off_acc = o; o += 4 * g.G * g.hd;       // attention accumulator combine
+    g.off_rows = o; o += 4 * ((g.max_rows + 3) & ~3);
+    g.off_u = o; o += 4 * ((g.max_nj + 3) & ~3);
+    g.off_red = o; o += 4 * 2 * MK_NCT;       // double-buffered row partials
+    g.off_sc = o; o += 4 * g.G * g.KB;        // attention scores of one KV block
+    g.off_misc = o; o += 2048;                // softmax state, staging, flags
+    g.smem_bytes = o;
+    return o;
+}
+
+// Kernel parameters (passed by value, __grid_constant__).
+struct MkParams {
+    MkGeom geo;
+    float eps;
+    int32_t l2_pf_bytes;
+    const uint8_t* arena;
+    const MkCtaPlan* plans;
+    const uint16_t* embed;       // [V][H] bf16
+    const float* attn_norm;      // [L][H]
+    const float* ffn_norm;       // [L][H]
+    const float* final_norm;     // [H]
+    uint16_t* kc;                // [L][kvh][max_seq][hd] bf16
+    uint16_t* vc;
+    const float* rope_cos;       // [max_seq][hd/2]
+    const float* rope_sin;
+    float* qbuf;                 // [L][qh*hd]
+    float* part_ml;              // [L][kvh][CPG][G][2]
+    float* part_acc;             // [L][kvh][CPG][G][hd]
+    float* xacc;                 // [2][2L][H] residual states (parity double-buffered)
+    float* hidden;               // [H]
+    uint32_t* cnt;               // flag counters (see mk_cnt_*) then the done counter
+    unsigned long long* amax;    // packed argmax key
+    int32_t* next_token;
+    uint32_t* status;
+    uint32_t* seq;               // launch sequence number (selects the xacc parity)
+    int32_t pos;
+    int32_t token;               // used when token_ptr == nullptr
+    const int32_t* token_ptr;
+    float* logits;               // [V] or nullptr
+    int32_t* tokens_out;         // greedy output buffer or nullptr
+    int32_t out_idx;
+    int32_t dbg_skip_cta, dbg_skip_sync;
+    int64_t wait_limit_ns;
+};
+
+MK_HD int mk_cnt_A(const MkGeom& g, int l, int grp) { return l * g.kvh + grp; }
+MK_HD int mk_cnt_B(const MkGeom& g, int l, int grp) { return g.L * g.kvh + l * g.kvh + grp; }
+MK_HD int mk_cnt_C(const MkGeom& g, int l) { return 2 * g.L * g.kvh + l; }
+MK_HD int mk_cnt_E(const MkGeom& g, int l) { return 2 * g.L * g.kvh + g.L + l; }
+MK_HD int mk_cnt_done(const MkGeom& g) { return 2 * g.L * g.kvh + 2 * g.L; }
+MK_HD int mk_cnt_total(const MkGeom& g) { return mk_cnt_done(g) + 1; }
+
+// Per-CTA plan; stream offsets are filled by the caller.
+MK_HD void mk_cta_plan(const MkGeom& g, int c, MkCtaPlan& p) {
+    p.g = c / g.CPG;
+    p.i = c % g.CPG;
+    int64_t a = mk_split(g.NP, g.CPG, p.i), b = mk_split(g.NP, g.CPG, p.i + 1);
+    p.pair0 = (int)a; p.npairs = (int)(b - a);
+    a = mk_split(g.H, g.CPG, p.i); b = mk_split(g.H, g.CPG, p.i + 1);
+    p.orow0 = (int)a; p.norows = (int)(b - a);
+    a = mk_split(g.F, g.nC, c); b = mk_split(g.F, g.nC, c + 1);
+    p.j0 = (int)a; p.nj = (int)(b - a);
+    a = mk_split(g.V, g.nC, c); b = mk_split(g.V, g.nC, c + 1);
+    p.v0 = (int)a; p.nv = (int)(b - a);
+    p.layer_bytes = (int64_t)2 * p.npairs * g.H * 2 + (int64_t)p.norows * g.G * g.hd * 2 +
+                    (int64_t)2 * p.nj * g.H * 2 + (int64_t)p.nj * g.H * 2;
+    p.stream_off = 0;
+}
+
+MK_HD int64_t mk_cta_stream_bytes(const MkGeom& g, const MkCtaPlan& p) {
+    int64_t b = (int64_t)g.L * p.layer_bytes + (int64_t)p.nv * g.H * 2;
+    return (b + 255) & ~(int64_t)255;
+}
+
+MK_HD int mk_imin(int a, int b) { return a < b ? a : b; }
+
+// Walks every tile CTA `pl` consumes during the step at position `pos`, in
+// consumption order, calling f(src, bytes): per layer the QKV rows, then the
+// K and V blocks of its share of positions [0, pos) (the current position is
+// read directly, not streamed), then the O, gate/up and down tiles; then the
+// LM-head rows.  KV share of CTA i of its group: split(pos + 1, CPG, i)
+// clipped to [0, pos).
+template <class F>
+MK_HD void mk_walk_tiles(const MkGeom& g, const MkCtaPlan& pl, const uint8_t* arena, const uint16_t* kc,
+                         const uint16_t* vc, int pos, F&& f) {
+    const uint8_t* cur = arena + pl.stream_off;
+    const int H = g.H, ctx = pos + 1;
+    const int a = (int)mk_split(ctx, g.CPG, pl.i);
+    const int b = (int)mk_split(ctx, g.CPG, pl.i + 1);
+    const int e = b < pos ? b : pos;
+    const int KO = g.G * g.hd;
+    for (int l = 0; l < g.L; ++l) {
+        const int nr = 2 * pl.npairs;
+        for (int r = 0; r < nr; r += g.TRh) {
+            uint32_t by = (uint32_t)(mk_imin(g.TRh, nr - r) * H * 2);
+            f((const void*)cur, by); cur += by;
+        }
+        const int64_t kvoff = ((int64_t)l * g.kvh + pl.g) * g.max_seq * g.hd;
+        for (int q = a; q < e; q += g.KB) {
+            uint32_t by = (uint32_t)(mk_imin(g.KB, e - q) * g.hd * 2);
+            f((const void*)(kc + kvoff + (int64_t)q * g.hd), by);
+            f((const void*)(vc + kvoff + (int64_t)q * g.hd), by);
+        }
+        for (int r = 0; r < pl.norows; r += g.TRo) {
+            uint32_t by = (uint32_t)(mk_imin(g.TRo, pl.norows - r) * KO * 2);
+            f((const void*)cur, by); cur += by;
+        }
+        for (int j = 0; j < pl.nj; j += g.JT) {
+            uint32_t by = (uint32_t)(2 * mk_imin(g.JT, pl.nj - j) * H * 2);
+            f((const void*)cur, by); cur += by;
+        }
+        for (int j = 0; j < pl.nj; j += g.JD) {
+            uint32_t by = (uint32_t)(mk_imin(g.JD, pl.nj - j) * H * 2);
+            f((const void*)cur, by); cur += by;
+        }
+    }
+    for (int r = 0; r < pl.nv; r += g.TRh) {
+        uint32_t by = (uint32_t)(mk_imin(g.TRh, pl.nv - r) * H * 2);
+        f((const void*)cur, by); cur += by;
+    }
+}
+
+// Source row of QKV stored row k (0 .. 2*npairs-1) of a CTA in group grp:
+// which matrix (0 q, 1 k, 2 v) and the row inside it.
+MK_HD void mk_qkv_row(const MkGeom& g, int grp, int pair, int half, int& mat, int& row) {
+    int hd2 = g.hd / 2;
+    int s = pair / hd2, d = pair % hd2 + half * hd2;
+    if (s < g.G) { mat = 0; row = (grp * g.G + s) * g.hd + d; }
+    else if (s == g.G) { mat = 1; row = grp * g.hd + d; }
+    else { mat = 2; row = grp * g.hd + d; }
+}

@@ -1,0 +1,208 @@
+/*
+ * mk.h - C ABI of the GB300 batch-size-1 decode megakernel library.
+ *
+ * The library runs autoregressive decode of a Llama-style decoder one token at
+ * a time with a KV cache (the single-request, bs=1 decode problem of
+ * cloud.baidu.com/article/9434380, sections 1-3), as ONE persistent CUDA
+ * kernel launch per token.  Inside that launch the per-layer segments
+ * (cloud.baidu.com/article/9434380, section 5, step 2):
+ *   A: RMSNorm + fused Q/K/V GEMV + RoPE + K/V append,
+ *   B: GQA attention over the cache (split over CTAs) + output projection
+ *      + residual,
+ *   C: RMSNorm + gate/up GEMV + SiLU*up + down GEMV + residual,
+ * and finally RMSNorm, the LM-head GEMV and the greedy argmax, are separated
+ * by inter-CTA flags instead of kernel boundaries, while a producer warp per
+ * CTA streams pre-laid-out bf16 weight tiles into a shared-memory ring with
+ * bulk asynchronous copies so that weight loading never stops between
+ * segments (cloud.baidu.com/article/9434380, sections 4.2 and 5, step 3;
+ * developer.baidu.com/article/detail.html?id=8006242, section 4.1).
+ *
+ * Conventions (all entry points):
+ *   - Every function returns MK_OK (0) or a negative MK_ERR_* code.  Argument
+ *     errors are detected on the host before anything is launched.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued on it and the call returns without waiting,
+ *     unless the function says it synchronizes.
+ *   - Device-side errors (a bounded wait that timed out, a non-finite logit,
+ *     a token id read from device memory that is out of range) are latched
+ *     into a status word on the device; mk_status() reads and clears it, and
+ *     mk_generate_greedy() checks it before returning.
+ *   - A context is not thread-safe and must be used from one stream at a time.
+ *   - All pointers to caller data are borrowed for the duration of the call;
+ *     the caller keeps ownership.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_OK 0
+#define MK_ERR_INVALID_ARG (-1)    /* bad pointer, size, shape, token or position */
+#define MK_ERR_OOM (-2)            /* device or host allocation failed */
+#define MK_ERR_CUDA (-3)           /* a CUDA runtime call failed (see mk_last_cuda_error) */
+#define MK_ERR_DEVICE_TIMEOUT (-4) /* a device-side wait ran past its limit; the launch gave up */
+#define MK_ERR_NUMERIC (-5)        /* a logit was NaN or infinite */
+#define MK_ERR_STATE (-6)          /* call out of order (e.g. decode before weights are loaded) */
+#define MK_ERR_UNSUPPORTED (-7)    /* shape outside what the kernels are built for */
+
+typedef struct mk_ctx mk_ctx; /* opaque, owned by the library */
+
+/* Model shape.  Weights are bf16, activations fp32. */
+typedef struct {
+    int32_t n_layers;
+    int32_t hidden;        /* H */
+    int32_t n_q_heads;     /* qh */
+    int32_t n_kv_heads;    /* kvh; qh % kvh == 0 (grouped-query attention) */
+    int32_t head_dim;      /* hd: 64 or 128 */
+    int32_t ffn;           /* F (SwiGLU inner size) */
+    int32_t vocab;         /* V */
+    int32_t max_seq;       /* KV-cache capacity in positions */
+    float rms_eps;         /* RMSNorm epsilon */
+    float rope_theta;      /* RoPE base */
+    int32_t tie_embeddings;/* 1: LM head = embedding matrix */
+} mk_config;
+
+/* Tuning knobs of the fused kernel (cloud.baidu.com/article/9434380, section 6:
+ * tile granularity, pipeline depth and on-chip buffer split are configuration,
+ * not constants).  Zero in any field selects the default. */
+typedef struct {
+    int32_t ring_stages;     /* shared-memory ring slots per CTA (default: as many as fit, <= 6);
+                                1 = no overlap of loading and compute ("prefetch off") */
+    int32_t slot_kib;        /* bytes per ring slot / weight tile, KiB (default 32) */
+    int32_t l2_prefetch_kib; /* how far (KiB of tile stream) each CTA prefetches into L2 ahead of
+                                its ring copies (default 256; negative = off) */
+    int32_t grid_ctas;       /* CTAs of the persistent grid (default: n_kv_heads * floor(SMs / n_kv_heads));
+                                must be a multiple of n_kv_heads and fit one CTA per SM */
+} mk_tuning;
+
+/* Weights, row-major [out, in] bf16 (raw 16-bit patterns).  Either all host
+ * pointers (on_device = 0) or all device pointers (on_device = 1). */
+typedef struct {
+    const void* embed;              /* [V][H] */
+    const void* lm_head;            /* [V][H]; NULL iff tie_embeddings */
+    const void* final_norm;         /* [H] */
+    const void* const* attn_norm;   /* n_layers pointers, each [H] */
+    const void* const* wq;          /* each [qh*hd][H] */
+    const void* const* wk;          /* each [kvh*hd][H] */
+    const void* const* wv;          /* each [kvh*hd][H] */
+    const void* const* wo;          /* each [H][qh*hd] */
+    const void* const* ffn_norm;    /* each [H] */
+    const void* const* w_gate;      /* each [F][H] */
+    const void* const* w_up;        /* each [F][H] */
+    const void* const* w_down;      /* each [H][F] */
+    int32_t on_device;
+} mk_weights;
+
+/* Read-only facts about a context (for benchmarks and tests). */
+typedef struct {
+    int32_t grid_ctas, ctas_per_group, block_threads, ring_stages, slot_bytes;
+    int32_t smem_bytes, sm_count, l2_prefetch_bytes;
+    int64_t arena_bytes;             /* re-laid-out weight stream bytes on the device */
+    int64_t weight_bytes_per_token;  /* bf16 weight bytes one step reads (matrices + gains + 1 embedding row) */
+    int64_t kv_bytes_per_position;   /* bf16 K+V bytes one attended position costs (all layers) */
+    int64_t device_bytes;            /* everything the context allocated on the device */
+} mk_info;
+
+/* Create a context on CUDA device `device`: validates the shape, sizes the
+ * persistent grid to the SM count, allocates the weight arena, the bf16 KV
+ * cache [n_layers][kvh][max_seq][hd] (K and V), fp32 scratch and the RoPE
+ * table.  `tuning` may be NULL.  On success *out owns everything. */
+int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx** out);
+
+/* Offline weight re-layout (cloud.baidu.com/article/9434380, section 9: lay
+ * weights out in access order ahead of time).  Copies every matrix into the
+ * arena as per-CTA streams of contiguous bf16 tiles in the order the kernel
+ * consumes them.  Synchronizes `stream` before returning, so the caller may
+ * free its buffers afterwards. */
+int mk_load_weights(mk_ctx* ctx, const mk_weights* w, void* stream);
+
+/* Pre-fill cache positions [0, n_pos) of one layer.  k, v: bf16 [kvh][n_pos][hd],
+ * host or device memory; K must already be rotated (post-RoPE), as decode
+ * steps store it.  Synchronizes `stream`. */
+int mk_set_kv(mk_ctx* ctx, int32_t layer, const void* k, const void* v, int32_t n_pos, void* stream);
+
+/* Copy cache positions [pos0, pos0 + n_pos) of one layer out to k_out, v_out
+ * (bf16 [kvh][n_pos][hd], host or device memory).  Synchronizes `stream`. */
+int mk_get_kv(mk_ctx* ctx, int32_t layer, int32_t pos0, int32_t n_pos, void* k_out, void* v_out, void* stream);
+
+/* One decode step (one kernel launch): feed `token` at position `pos`, write
+ * its K/V into cache slot `pos`, attend over slots [0, pos], and write the
+ * fp32 logits [V] to `logits_out` (device memory, caller-owned; NULL = do not
+ * store logits).  The greedy argmax is always computed and kept on the device
+ * (mk_get_argmax).  Requires 0 <= token < V and 0 <= pos < max_seq; slots
+ * above `pos` are ignored, so rewinding to an earlier `pos` is allowed.
+ * Asynchronous. */
+int mk_decode_step(mk_ctx* ctx, int32_t token, int32_t pos, float* logits_out, void* stream);
+
+/* One decode step fed with the previous step's greedy token, which the kernel
+ * reads from device memory (no host round trip between tokens).  Otherwise as
+ * mk_decode_step.  The token after mk_create is 0.  Asynchronous. */
+int mk_decode_step_greedy(mk_ctx* ctx, int32_t pos, float* logits_out, void* stream);
+
+/* Greedy generation (cloud.baidu.com/article/9434380, section 5, step 5:
+ * sampling and multi-step state advance run on the fused path).  Feeds the
+ * n_prompt prompt tokens (host int32) at positions start_pos.., then n_new - 1
+ * more steps, each fed the previous step's argmax, which the kernel reads from
+ * device memory: no host round trip between tokens.  Writes the n_new
+ * generated tokens to out_tokens (host int32 [n_new]).  Launches
+ * n_prompt + n_new - 1 kernels, synchronizes `stream`, and returns the device
+ * status (MK_ERR_DEVICE_TIMEOUT / MK_ERR_NUMERIC) if one was latched. */
+int mk_generate_greedy(mk_ctx* ctx, const int32_t* prompt, int32_t n_prompt, int32_t start_pos,
+                       int32_t n_new, int32_t* out_tokens, void* stream);
+
+/* The last step's final-norm hidden state (fp32 [H]) into `out` (device). */
+int mk_get_hidden(mk_ctx* ctx, float* out, void* stream);
+
+/* The last step's greedy token (int32) into `out` (device). */
+int mk_get_argmax(mk_ctx* ctx, int32_t* out, void* stream);
+
+/* Synchronizes the context's last stream, reads and clears the device status
+ * word.  Returns MK_OK, MK_ERR_DEVICE_TIMEOUT, MK_ERR_NUMERIC or
+ * MK_ERR_INVALID_ARG (a device-read token id was out of range). */
+int mk_status(mk_ctx* ctx);
+
+/* Unfused baseline of the same step: the same arithmetic launched as one
+ * kernel per operator (about 7 per layer + 4), on plain row-major weights
+ * (cloud.baidu.com/article/9434380, section 5, step 5 keeps the per-operator
+ * path for comparison and debugging; section 7 asks for the fusion-off
+ * ablation).  Needs mk_load_weights to have run with keep_rowmajor = 1 in
+ * mk_enable_perop before it.  Asynchronous; returns the number of kernel
+ * launches it issued through *n_launches (may be NULL). */
+int mk_enable_perop(mk_ctx* ctx, int32_t keep_rowmajor);
+int mk_decode_step_perop(mk_ctx* ctx, int32_t token, int32_t pos, float* logits_out, void* stream,
+                         int32_t* n_launches);
+
+int mk_get_info(const mk_ctx* ctx, mk_info* out);
+
+/* Debug knobs (off by default).  MK_DBG_SKIP_ARRIVAL: value = cta * 65536 + sync_id
+ * makes that CTA skip one flag arrival, so every CTA waiting on it runs into its
+ * bounded wait (used by the failure-detection test; -1 = off).  sync_id = 4 * layer
+ * + {0: q/k/v ready, 1: attention partials ready, 2: attention block done,
+ * 3: FFN block done}.  MK_DBG_WAIT_LIMIT_NS: limit of every device-side wait
+ * (default 1e9 ns). */
+#define MK_DBG_SKIP_ARRIVAL 1
+#define MK_DBG_WAIT_LIMIT_NS 2
+int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
+
+const char* mk_strerror(int code);
+/* Text of the last CUDA error seen by this thread's calls into the library. */
+const char* mk_last_cuda_error(void);
+void mk_destroy(mk_ctx* ctx);
+
+/* Host-only layout utilities (no GPU needed).  mk_arena_bytes: size of the
+ * re-laid-out weight arena for `grid_ctas` CTAs.  mk_relayout_host: build that
+ * arena on the host from host weights (the same layout mk_load_weights writes
+ * on the device). */
+int64_t mk_arena_bytes(const mk_config* cfg, const mk_tuning* tuning, int32_t grid_ctas);
+int mk_relayout_host(const mk_config* cfg, const mk_tuning* tuning, int32_t grid_ctas, const mk_weights* w,
+                     void* arena_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MK_H */

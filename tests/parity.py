@@ -1,0 +1,94 @@
+"""Teacher-forced parity harness: the GPU decode step against the CPU oracle.
+
+At every step both paths are fed the same token at the same position (prompt
+tokens first, then the ORACLE's greedy token), so one divergence cannot
+cascade.  Per step it records
+
+  - max |logit_gpu - logit_oracle| over the whole vocabulary,
+  - ||h_gpu - h_oracle||_inf / ||h_oracle||_inf of the final-norm hidden state,
+  - whether the GPU's fused argmax equals the oracle's argmax, and whether the
+    oracle's top-2 gap was below 2 * max|dlogit| (a near tie, where a flip is
+    explained by rounding),
+  - whether the GPU's fused argmax equals the argmax of the GPU's own logits
+    (exact: same floats, lowest index on ties).
+
+Tolerances (stated for the decode step): max |dlogit| <= 5e-2, hidden relative
+error <= 1e-2, greedy agreement >= 99% of steps with every disagreement a near tie.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import oracle
+
+LOGIT_TOL = 5e-2
+HIDDEN_TOL = 1e-2
+ARGMAX_AGREE = 0.99
+
+
+@dataclasses.dataclass
+class Report:
+    steps: int = 0
+    max_dlogit: float = 0.0
+    max_hidden_rel: float = 0.0
+    agree: int = 0
+    flips_not_near_tie: int = 0
+    self_argmax_mismatch: int = 0
+    tokens: list = dataclasses.field(default_factory=list)
+
+    def check(self):
+        assert self.steps > 0
+        assert self.max_dlogit <= LOGIT_TOL, f"max |dlogit| {self.max_dlogit:.3e} > {LOGIT_TOL}"
+        assert self.max_hidden_rel <= HIDDEN_TOL, f"hidden rel err {self.max_hidden_rel:.3e} > {HIDDEN_TOL}"
+        assert self.self_argmax_mismatch == 0, "fused argmax differs from argmax of the GPU's own logits"
+        assert self.flips_not_near_tie == 0, f"{self.flips_not_near_tie} argmax flips without a near tie"
+        if self.steps >= 100:
+            assert self.agree / self.steps >= ARGMAX_AGREE, f"argmax agreement {self.agree}/{self.steps}"
+
+    def summary(self):
+        return (f"steps={self.steps} max|dlogit|={self.max_dlogit:.3e} hidden_rel={self.max_hidden_rel:.3e} "
+                f"argmax {self.agree}/{self.steps}")
+
+
+def gpu_argmax_of(logits: np.ndarray) -> int:
+    return int(np.argmax(logits))  # first occurrence = lowest index on ties
+
+
+def run_teacher_forced(dec, orc: oracle.OracleDecoder, tokens_in, start_pos: int, n_steps: int,
+                       perop: bool = False, report: Report | None = None) -> Report:
+    """tokens_in: tokens fed at the first len(tokens_in) steps; after that the
+    oracle's argmax of the previous step is fed."""
+    rep = report or Report()
+    tok = int(tokens_in[0])
+    for k in range(n_steps):
+        pos = start_pos + k
+        if k < len(tokens_in):
+            tok = int(tokens_in[k])
+        lg_ref, h_ref = orc.step(tok, pos)
+        if perop:
+            dec.step_perop(tok, pos)
+        else:
+            dec.step(tok, pos)
+        lg = dec.logits.cpu().numpy().astype(np.float64)
+        h = dec.get_hidden().cpu().numpy().astype(np.float64)
+        g_arg = dec.get_argmax()
+        r_arg, _ = oracle.argmax_f32(lg_ref)
+        dl = float(np.max(np.abs(lg - lg_ref)))
+        rep.max_dlogit = max(rep.max_dlogit, dl)
+        rep.max_hidden_rel = max(rep.max_hidden_rel, float(np.max(np.abs(h - h_ref)) / np.max(np.abs(h_ref))))
+        if g_arg != gpu_argmax_of(lg.astype(np.float32)):
+            rep.self_argmax_mismatch += 1
+        if g_arg == r_arg:
+            rep.agree += 1
+        else:
+            top2 = np.sort(lg_ref.astype(np.float32))[-2:]
+            if float(top2[1] - top2[0]) >= 2 * max(dl, 1e-6):
+                rep.flips_not_near_tie += 1
+        rep.steps += 1
+        rep.tokens.append(r_arg)
+        tok = r_arg
+    st = dec.status()
+    assert st == 0, f"device status {st}"
+    return rep

@@ -1,0 +1,54 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, and exports every
+function include/mk.h declares; the Python binding covers each one."""
+import ctypes
+import os
+import re
+
+from decode_megakernel_05_gb300 import mk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mk.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mk_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    lib = mk.load()
+    names = declared_functions()
+    assert len(names) >= 18, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in mk.h but not exported"
+    bound = {n for n, _, _ in mk.SIGNATURES}
+    assert set(names) == bound, set(names) ^ bound
+
+
+def test_library_is_sm103a_and_self_contained():
+    path = mk.library_path()
+    assert os.path.exists(path)
+    log = open(os.path.join(os.path.dirname(path), "ptxas.log")).read()
+    assert "for 'sm_103a'" in log
+    # the CUDA runtime is linked statically: no libcudart dependency to resolve at load time
+    ctypes.CDLL(path)
+
+
+def test_host_only_entry_points():
+    assert mk.mk_strerror(mk.MK_ERR_DEVICE_TIMEOUT) == "device-side wait timed out"
+    cfg = mk.mk_config(2, 256, 4, 2, 64, 688, 1024, 80, 1e-5, 1e4, 0)
+    assert mk.mk_arena_bytes(cfg, None, 152) > 0
+    bad = mk.mk_config(2, 256, 4, 3, 64, 688, 1024, 80, 1e-5, 1e4, 0)   # 4 % 3 != 0
+    assert mk.mk_arena_bytes(bad, None, 150) == -1
+    odd = mk.mk_config(2, 256, 4, 2, 96, 688, 1024, 80, 1e-5, 1e4, 0)   # head_dim 96 unsupported
+    assert mk.mk_arena_bytes(odd, None, 152) == -1
+
+
+def test_no_closed_cuda_calls_in_sources():
+    """The batched-memcpy family is closed on the GPU pool; no source may name it."""
+    pat = re.compile(r"(cuda|cu)Memcpy(3D)?BatchAsync")
+    for d in ("decode_megakernel_05_gb300", "include", "oracle", "synth", "tests"):
+        for base, _, files in os.walk(os.path.join(ROOT, d)):
+            for f in files:
+                if f.endswith((".cu", ".h", ".c", ".cpp", ".py")) and f != "test_abi.py":
+                    assert not pat.search(open(os.path.join(base, f), errors="ignore").read()), f

@@ -1,0 +1,138 @@
+"""GPU decode megakernel vs the CPU oracle, through the C ABI.
+
+Small shapes run every step of their workload teacher-forced; they span several
+tiles per CTA, ragged last tiles (FFN slice, vocab, O rows), multi-block KV
+chunks, odd CTAs-per-group counts and both GQA ratios.  The five workloads run
+at full size in the launch configuration the benchmark uses, on sampled steps
+the oracle computes one by one from the same initial state.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from decode_megakernel_05_gb300 import Decoder, mk
+from tests.parity import Report, run_teacher_forced
+
+pytestmark = pytest.mark.gpu
+
+
+def make(shape, seed, max_seq, gains="ones", std=0.02, tuning=None, perop=False):
+    m = synth.make_model(shape, seed, std=std, gains=gains)
+    return m, Decoder(m, max_seq, tuning=tuning, perop=perop), oracle.OracleDecoder(m, max_seq)
+
+
+def test_tiny_workload_teacher_forced():
+    w = synth.WORKLOADS["tiny"]
+    m, dec, orc = make(w.shape, w.seed_weights, w.max_seq())
+    prompt = synth.make_prompt(w)
+    rep = run_teacher_forced(dec, orc, prompt, 0, w.prompt_len + w.decode - 1)
+    print(rep.summary())
+    rep.check()
+    # K/V appended by the fused kernel equal the oracle's bf16 cache (up to a rounding flip)
+    for l in range(w.shape.n_layers):
+        k, v = dec.get_kv(l, 0, rep.steps)
+        for got, ref in ((k, orc.kcache[l, :, :rep.steps]), (v, orc.vcache[l, :, :rep.steps])):
+            g32, r32 = synth.bf16_to_f32(got), synth.bf16_to_f32(ref)
+            assert np.mean(got == ref) > 0.97
+            assert np.max(np.abs(g32 - r32)) <= 2 ** -7 * np.max(np.abs(r32))
+    dec.close()
+
+
+@pytest.mark.parametrize("tied,gains", [(True, "normal"), (False, "normal")])
+def test_tiny_variants(tied, gains):
+    s = synth.ModelShape(2, 256, 4, 2, 64, 688, 1024, 1e-5, 10000.0, tied)
+    m, dec, orc = make(s, 17, 128, gains=gains, std=0.05)
+    toks = synth.uniform_tokens(20, s.vocab, 17, 5)
+    rep = run_teacher_forced(dec, orc, toks, 0, 40)
+    print(rep.summary())
+    rep.check()
+    dec.close()
+
+
+MID = synth.ModelShape(2, 512, 8, 2, 64, 1000, 5003, 1e-5, 10000.0, False)
+
+
+@pytest.mark.parametrize("grid,prefill", [(0, 0), (14, 0), (2, 700), (6, 300)])
+def test_mid_shape_ragged(grid, prefill):
+    """H=512, G=4, F=1000 (ragged FFN slices), V=5003 (ragged LM rows); grid 2
+    and 6 put one and three CTAs in each KV group, so a CTA walks several KV
+    blocks (online softmax across blocks)."""
+    tun = mk.tuning(grid_ctas=grid) if grid else None
+    m, dec, orc = make(MID, 23, 1024, gains="normal", std=0.04, tuning=tun)
+    if prefill:
+        ks, vs = synth.make_kv(MID, prefill, 29)
+        dec.set_kv(ks, vs, prefill)
+        orc.set_kv(ks, vs, prefill)
+    toks = synth.uniform_tokens(8, MID.vocab, 23, 7)
+    rep = run_teacher_forced(dec, orc, toks, prefill, 24)
+    print(rep.summary())
+    rep.check()
+    dec.close()
+
+
+def test_head_dim_128_shape():
+    s = synth.ModelShape(2, 1024, 8, 2, 128, 1536, 4099, 1e-5, 500000.0, False)
+    m, dec, orc = make(s, 31, 512, gains="normal", std=0.03)
+    ks, vs = synth.make_kv(s, 200, 37)
+    dec.set_kv(ks, vs, 200)
+    orc.set_kv(ks, vs, 200)
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, s.vocab, 31, 3), 200, 12)
+    print(rep.summary())
+    rep.check()
+    dec.close()
+
+
+def test_greedy_generate_matches_oracle_tokens():
+    """mk_generate_greedy (device-side token feedback, host prompt in / tokens out)
+    reproduces the oracle's own greedy continuation of the tiny workload."""
+    w = synth.WORKLOADS["tiny"]
+    m, dec, orc = make(w.shape, w.seed_weights, w.max_seq())
+    prompt = synth.make_prompt(w)
+    rc, out = dec.generate_greedy(prompt, 0, w.decode)
+    assert rc == 0
+    tok, want = None, []
+    for p in range(w.prompt_len + w.decode - 1):
+        t_in = int(prompt[p]) if p < w.prompt_len else tok
+        lg, _ = orc.step(t_in, p)
+        tok, _ = oracle.argmax_f32(lg)
+        if p >= w.prompt_len - 1:
+            want.append(tok)
+    assert list(out) == want
+    dec.close()
+
+
+def test_perop_baseline_matches_oracle():
+    w = synth.WORKLOADS["tiny"]
+    m, dec, orc = make(w.shape, w.seed_weights, w.max_seq(), perop=True)
+    prompt = synth.make_prompt(w)
+    rep = run_teacher_forced(dec, orc, prompt, 0, 20, perop=True)
+    print(rep.summary())
+    rep.check()
+    n = dec.step_perop(1, 20)
+    assert n == 9 * w.shape.n_layers + 5
+    dec.close()
+
+
+# ------------------------------------------------------------ full-size workloads
+
+def _full(name, n_steps):
+    w = synth.WORKLOADS[name]
+    m, dec, orc = make(w.shape, w.seed_weights, w.max_seq())
+    if w.prefill:
+        ks, vs = synth.make_kv(w.shape, w.prefill, w.seed_kv)
+        dec.set_kv(ks, vs, w.prefill)
+        orc.set_kv(ks, vs, w.prefill)
+        toks = [synth.make_first_token(w)]
+    else:
+        toks = synth.make_prompt(w)
+    rep = run_teacher_forced(dec, orc, toks, w.start_pos if w.prefill else 0, n_steps)
+    print(name, rep.summary(), "grid", dec.info.grid_ctas, "stages", dec.info.ring_stages)
+    rep.check()
+    dec.close()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,n_steps", [("1b", 6), ("1b-2k", 4), ("1b-32k", 3), ("8b-4k", 3)])
+def test_full_size_workloads_sampled(name, n_steps):
+    _full(name, n_steps)
