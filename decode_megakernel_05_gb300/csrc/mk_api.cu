@@ -595,7 +595,8 @@ int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
         const size_t nsplit_max = ((size_t)g.max_seq + P.attn_chunk - 1) / P.attn_chunk;
         MK_TRY(c->dalloc(&P.x, H * 4)); MK_TRY(c->dalloc(&P.xn, H * 4));
         MK_TRY(c->dalloc(&P.qkv, (qd + 2 * kvd) * 4)); MK_TRY(c->dalloc(&P.attn, qd * 4));
-        MK_TRY(c->dalloc(&P.u, F * 4)); MK_TRY(c->dalloc(&P.hidden, H * 4));
+        MK_TRY(c->dalloc(&P.u, F * 4));
+        P.hidden = c->hidden;   // mk_get_hidden reads the same buffer for both paths
         MK_TRY(c->dalloc(&P.pml, (size_t)g.qh * nsplit_max * 2 * 4));
         MK_TRY(c->dalloc(&P.pacc, (size_t)g.qh * nsplit_max * g.hd * 4));
         MK_TRY(c->dalloc(&P.logits_tmp, V * 4));

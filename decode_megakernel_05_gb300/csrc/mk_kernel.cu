@@ -821,6 +821,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     }
 
     // ---------------- end of step: the last CTA publishes the token and resets the flags
+    if (t == 0 && ab) s.misc->abort = 1;   // lets the producer warps stop and drain
     if (t == 0) {
         __threadfence();
         const uint32_t prev = atomicAdd(p.cnt + mk_cnt_done(g), 1u);

@@ -1,0 +1,78 @@
+"""Failure detection without a GPU fault.
+
+A debug knob makes one CTA skip one flag arrival, so every CTA waiting on that
+flag runs into its bounded wait (here 20 ms): the launch gives up, latches
+MK_ERR_DEVICE_TIMEOUT in the device status word, resets its flags, and the
+context stays usable -- the next step (rewound to the same position) matches
+the oracle again.  Nothing traps, faults or spins without a limit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from decode_megakernel_05_gb300 import Decoder, mk
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    w = synth.WORKLOADS["tiny"]
+    m = synth.make_model(w.shape, w.seed_weights)
+    dec = Decoder(m, w.max_seq())
+    yield w, m, dec
+    dec.close()
+
+
+@pytest.mark.parametrize("sync_id", [0, 1, 2, 3, 4 + 2])
+def test_skipped_arrival_times_out_and_context_recovers(tiny, sync_id):
+    w, m, dec = tiny
+    orc = oracle.OracleDecoder(m, w.max_seq())
+    prompt = synth.make_prompt(w)
+    for p in range(3):
+        orc.step(int(prompt[p]), p)
+        dec.step(int(prompt[p]), p)
+    assert dec.status() == mk.MK_OK
+    dec.set_debug(mk.MK_DBG_WAIT_LIMIT_NS, 20_000_000)
+    dec.set_debug(mk.MK_DBG_SKIP_ARRIVAL, 5 * 65536 + sync_id)
+    dec.step(int(prompt[3]), 3)
+    assert dec.status() == mk.MK_ERR_DEVICE_TIMEOUT
+    dec.set_debug(mk.MK_DBG_SKIP_ARRIVAL, -1)
+    dec.set_debug(mk.MK_DBG_WAIT_LIMIT_NS, 1_000_000_000)
+    ref, _ = orc.step(int(prompt[3]), 3)
+    got = dec.step(int(prompt[3]), 3).cpu().numpy()
+    assert dec.status() == mk.MK_OK
+    assert np.max(np.abs(got - ref)) <= 5e-2
+
+
+def test_generate_greedy_reports_timeout(tiny):
+    w, m, dec = tiny
+    dec.set_debug(mk.MK_DBG_WAIT_LIMIT_NS, 20_000_000)
+    dec.set_debug(mk.MK_DBG_SKIP_ARRIVAL, 0 * 65536 + 3)
+    rc, _ = dec.generate_greedy([1, 2, 3], 0, 2)
+    assert rc == mk.MK_ERR_DEVICE_TIMEOUT
+    dec.set_debug(mk.MK_DBG_SKIP_ARRIVAL, -1)
+    dec.set_debug(mk.MK_DBG_WAIT_LIMIT_NS, 1_000_000_000)
+    rc, _ = dec.generate_greedy([1, 2, 3], 0, 2)
+    assert rc == mk.MK_OK
+
+
+def test_argument_errors_return_codes_without_launch(tiny):
+    w, m, dec = tiny
+    lib = mk.load()
+    assert lib.mk_decode_step(dec.ctx, w.shape.vocab, 0, None, dec.stream) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_decode_step(dec.ctx, -1, 0, None, dec.stream) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_decode_step(dec.ctx, 1, dec.max_seq, None, dec.stream) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_decode_step_greedy(dec.ctx, -5, None, dec.stream) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_set_debug(dec.ctx, 99, 0) == mk.MK_ERR_INVALID_ARG
+    assert dec.status() == mk.MK_OK
+
+
+def test_decode_before_weights_is_a_state_error():
+    w = synth.WORKLOADS["tiny"]
+    ctx = mk.mk_create(mk.config_from_shape(w.shape, 64))
+    try:
+        assert mk.load().mk_decode_step(ctx, 1, 0, None, None) == mk.MK_ERR_STATE
+    finally:
+        mk.mk_destroy(ctx)
