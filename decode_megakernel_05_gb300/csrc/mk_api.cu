@@ -202,6 +202,7 @@ struct mk_ctx {
     // debug
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
     int64_t wait_limit_ns = 1000000000LL;
+    unsigned long long* trace = nullptr;
     // per-operator baseline
     bool perop_enabled = false, perop_ready = false;
     MkPerOp perop{};
@@ -249,6 +250,7 @@ MkParams base_params(const mk_ctx* c) {
     p.dbg_skip_cta = c->dbg_skip_cta;
     p.dbg_skip_sync = c->dbg_skip_sync;
     p.wait_limit_ns = c->wait_limit_ns;
+    p.trace = c->trace;
     p.out_idx = 0;
     return p;
 }
@@ -762,6 +764,11 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_SKIP_ARRIVAL) {
         if (value < 0) { c->dbg_skip_cta = -1; c->dbg_skip_sync = -1; }
         else { c->dbg_skip_cta = (int)(value >> 16); c->dbg_skip_sync = (int)(value & 0xFFFF); }
+        return MK_OK;
+    }
+    if (knob == MK_DBG_TRACE) {
+        if (value != 0 && c->geo.L > MK_TRACE_MAX_LAYERS) return MK_ERR_UNSUPPORTED;
+        c->trace = reinterpret_cast<unsigned long long*>((uintptr_t)value);
         return MK_OK;
     }
     if (knob == MK_DBG_WAIT_LIMIT_NS) {

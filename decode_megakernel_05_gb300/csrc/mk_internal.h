@@ -155,7 +155,14 @@ struct MkParams {
     int32_t out_idx;
     int32_t dbg_skip_cta, dbg_skip_sync;
     int64_t wait_limit_ns;
+    // Optional segment trace (%globaltimer ns), nullptr = off.  Per CTA
+    // MK_TRACE_STRIDE slots: consumer events 16*l + e (e = MK_EV_*), end
+    // events at 16*L + k, consumer ring-wait ns per layer at 1024 + l,
+    // producer ring-wait ns per layer at 1536 + l.
+    unsigned long long* trace;
 };
+#define MK_TRACE_STRIDE 2048
+#define MK_TRACE_MAX_LAYERS 63
 
 MK_HD int mk_cnt_A(const MkGeom& g, int l, int grp) { return l * g.kvh + grp; }
 MK_HD int mk_cnt_B(const MkGeom& g, int l, int grp) { return g.L * g.kvh + l * g.kvh + grp; }

@@ -119,7 +119,7 @@ struct Misc {                // lives at geo.off_misc (2048 bytes)
     int par;
     int is_last;
     unsigned long long copy_bytes;  // bytes issued by the copy producer (paces the L2 prefetcher)
-    int pad0[2];
+    unsigned long long cwait;       // trace: ns thread 0 spent waiting for ring data
     float alpha[8], mrun[8], lrun[8];
     float best_val[64];
     int best_idx[64];
@@ -141,6 +141,14 @@ struct Smem {
     float* sc;    // [G][KB]
     Misc* misc;
 };
+
+// Segment trace (off unless MkParams::trace is set): thread 0 of the consumers
+// stamps %globaltimer at the end of each segment.
+#define MK_TRACE(slot_)                                                                  \
+    do {                                                                                  \
+        if (p.trace && threadIdx.x == 0)                                                  \
+            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + (slot_)] = gtimer();           \
+    } while (0)
 
 // ------------------------------------------------------------------ waits
 
@@ -195,16 +203,24 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
     const uint32_t slot_bytes = (uint32_t)p.geo.slot;
     uint32_t k = 0;
     bool stop = false;
+    unsigned long long pwait = 0;
+    unsigned long long* tr = p.trace ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
     walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
         if (stop) return;
         const uint32_t slot = k % ns, ph = (k / ns) & 1u;
+        const uint64_t tw = tr ? gtimer() : 0;
         if (!wait_mbar(p, &s.empty[slot], ph ^ 1u, abort)) { stop = true; return; }
+        if (tr) {
+            pwait += gtimer() - tw;
+            if ((k & 15u) == 0 && 1536 + (k >> 4) < MK_TRACE_STRIDE) tr[1536 + (k >> 4)] = pwait;
+        }
         s.misc->tile_bytes[slot] = bytes;
         mbar_expect_tx(&s.full[slot], bytes);
         bulk_g2s(s.ring + (size_t)slot * slot_bytes, src, bytes, &s.full[slot]);
         ++k;
         *(volatile unsigned long long*)&s.misc->copy_bytes += bytes;
     });
+    if (tr) tr[1535] = gtimer();
     // Drain: wait for the copies still in flight before this warp leaves.
     const uint32_t first = k > (uint32_t)ns ? k - ns : 0u;
     for (uint32_t q = first; q < k; ++q) {
@@ -254,7 +270,9 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     const uint32_t slot = rg.k % ns, ph = (rg.k / ns) & 1u;
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {
+        const uint64_t tw = (p.trace && threadIdx.x == 0) ? gtimer() : 0;
         ok = !s.misc->abort && wait_mbar(p, &s.full[slot], ph, &s.misc->abort);
+        if (tw) s.misc->cwait += gtimer() - tw;
         if (ok && s.misc->tile_bytes[slot] != expect_bytes) {
             atomicOr(p.status, MK_ST_SCHEDULE | MK_ST_ABORT);
             s.misc->abort = 1;
@@ -502,6 +520,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s.misc->abort = 0;
         s.misc->copy_bytes = 0;
+        s.misc->cwait = 0;
         s.misc->is_last = 0;
         int tok = p.token_ptr ? *p.token_ptr : p.token;
         if (tok < 0 || tok >= g.V) {
@@ -549,10 +568,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     const GemvMap mo = gemv_map(G * HD);
     float xr[2][8];
 
+    MK_TRACE(16 * L + 3);
     for (int l = 0; l < L && !ab; ++l) {
         // ---------------- segment A: RMSNorm + QKV GEMV + RoPE + K/V append
+        MK_TRACE(16 * l + 0);
         const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
         ab = rmsnorm_to_xv(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab);
+        MK_TRACE(16 * l + 1);
         load_x(s.xv, mh, xr);
         const int nr = 2 * pl.npairs;
         for (int r0 = 0; r0 < nr; r0 += g.TRh) {
@@ -562,6 +584,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             buf ^= 1;
         }
         ab = bar_or(ab);
+        MK_TRACE(16 * l + 2);
         if (!ab) {
             for (int j = t; j < pl.npairs; j += MK_NCT) {
                 const int pair = pl.pair0 + j, slot = pair / hd2, d = pair % hd2;
@@ -582,8 +605,10 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
         }
         ab = bar_or(ab);
+        MK_TRACE(16 * l + 3);
         if (t == 0 && !ab) arrive(p, mk_cnt_A(g, l, pl.g), 4 * l + 0);
         ab = sync_wait(p, mk_cnt_A(g, l, pl.g), (uint32_t)g.CPG, ab);
+        MK_TRACE(16 * l + 4);
 
         // ---------------- segment B: split-K attention over this CTA's positions
         if (!ab) {
@@ -648,8 +673,10 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
         }
         ab = bar_or(ab);
+        MK_TRACE(16 * l + 5);
         if (t == 0 && !ab) arrive(p, mk_cnt_B(g, l, pl.g), 4 * l + 1);
         ab = sync_wait(p, mk_cnt_B(g, l, pl.g), (uint32_t)g.CPG, ab);
+        MK_TRACE(16 * l + 6);
 
         // combine the group's partials -> o (the G heads of this KV group)
         if (!ab) {
@@ -670,6 +697,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
         }
         ab = bar_or(ab);
+        MK_TRACE(16 * l + 7);
 
         // O-proj (rows of this CTA, columns of this group) + residual, atomically
         load_x(s.ov, mo, xr);
@@ -686,11 +714,14 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             buf ^= 1;
         }
         ab = bar_or(ab);
+        MK_TRACE(16 * l + 8);
         if (t == 0 && !ab) arrive(p, mk_cnt_C(g, l), 4 * l + 2);
         ab = sync_wait(p, mk_cnt_C(g, l), (uint32_t)g.nC, ab);
+        MK_TRACE(16 * l + 9);
 
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
         ab = rmsnorm_to_xv(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab);
+        MK_TRACE(16 * l + 10);
         load_x(s.xv, mh, xr);
         for (int j0 = 0; j0 < pl.nj; j0 += g.JT) {
             const int n = min(g.JT, pl.nj - j0);
@@ -701,6 +732,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
             buf ^= 1;
         }
+        MK_TRACE(16 * l + 11);
         // down projection: this CTA's FFN columns, all H rows (split-K)
         const int U = H / 8;
         const int JG = U < MK_NCT ? MK_NCT / U : 1;
@@ -771,14 +803,21 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
         }
         ab = bar_or(ab);
+        MK_TRACE(16 * l + 12);
         if (t == 0 && !ab) arrive(p, mk_cnt_E(g, l), 4 * l + 3);
         ab = sync_wait(p, mk_cnt_E(g, l), (uint32_t)g.nC, ab);
+        MK_TRACE(16 * l + 13);
+        if (p.trace && t == 0) {
+            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + l] = s.misc->cwait;
+            s.misc->cwait = 0;
+        }
     }
 
     // ---------------- final RMSNorm + LM head + argmax
     {
         const float* xl = xa + (size_t)(2 * L - 1) * state;
         ab = rmsnorm_to_xv(p, s, xl, nullptr, p.final_norm, ab);
+        MK_TRACE(16 * L + 0);
         if (c == 0 && !ab)
             for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv[i];
         load_x(s.xv, mh, xr);
@@ -800,6 +839,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
             buf ^= 1;
         }
+        MK_TRACE(16 * L + 1);
+        if (p.trace && t == 0) p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + L] = s.misc->cwait;
         if (nonfinite) atomicOr(p.status, MK_ST_NUMERIC);
         if (t < 64) { s.misc->best_val[t] = bv; s.misc->best_idx[t] = bi; }
         ab = bar_or(ab);
@@ -821,6 +862,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     }
 
     // ---------------- end of step: the last CTA publishes the token and resets the flags
+    MK_TRACE(16 * L + 2);
     if (t == 0 && ab) s.misc->abort = 1;   // lets the producer warps stop and drain
     if (t == 0) {
         __threadfence();

@@ -27,6 +27,7 @@ MK_ERR_STATE = -6
 MK_ERR_UNSUPPORTED = -7
 MK_DBG_SKIP_ARRIVAL = 1
 MK_DBG_WAIT_LIMIT_NS = 2
+MK_DBG_TRACE = 3
 
 _i32, _i64, _f32, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 

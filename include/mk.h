@@ -186,6 +186,16 @@ int mk_get_info(const mk_ctx* ctx, mk_info* out);
  * (default 1e9 ns). */
 #define MK_DBG_SKIP_ARRIVAL 1
 #define MK_DBG_WAIT_LIMIT_NS 2
+/* MK_DBG_TRACE: value = device address of a uint64 buffer [grid_ctas][2048]
+ * (0 = off).  Each step then records per CTA the %globaltimer (ns) at the end
+ * of every segment: slot 16*layer + e for e = 0 layer start, 1 RMSNorm,
+ * 2 QKV GEMV, 3 RoPE/KV append, 4 q/k/v flag seen, 5 attention partials,
+ * 6 partials flag seen, 7 combine, 8 O-proj, 9 attention-block flag seen,
+ * 10 RMSNorm, 11 gate/up, 12 down, 13 FFN-block flag seen; slot 16*L + 0
+ * final RMSNorm, +1 LM head, +2 end, +3 start; slot 1024 + layer: ns the
+ * consumers waited for ring data; slot 1536 + k/16: cumulative ns the copy
+ * producer waited for a free slot after its k-th tile; slot 1535: producer done. */
+#define MK_DBG_TRACE 3
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
 const char* mk_strerror(int code);
