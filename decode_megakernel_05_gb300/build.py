@@ -20,7 +20,9 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmk.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["mk_kernel.cu", "mk_api.cu", "mk_aux.cu", "mk_perop.cu"]
+SOURCES = ["mk_api.cu", "mk_aux.cu", "mk_perop.cu"]
+# (head_dim, query heads per KV group) pairs of the fused kernel, one object each
+VARIANTS = [(64, 1), (64, 2), (64, 4), (64, 8), (128, 2), (128, 4), (128, 8)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -52,20 +54,23 @@ def build(force: bool = False, verbose: bool = False) -> str:
     cc = nvcc()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
                     "-I", INCLUDE, "-I", CSRC]
+    jobs = [(src, os.path.join(BUILD, src.replace(".cu", ".o")), []) for src in SOURCES]
+    for hd, g in VARIANTS:
+        jobs.append(("mk_kernel.cu", os.path.join(BUILD, f"mk_kernel_{hd}_{g}.o"), [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}"]))
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        src, obj, defs = job
+        cmd = [cc, *flags, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed for {src} {defs}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr
 
-    with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
+    with cf.ThreadPoolExecutor(min(len(jobs), os.cpu_count() or 4)) as ex:
+        results = list(ex.map(compile_one, jobs))
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
-        for (obj, log), src in zip(results, SOURCES):
-            f.write(f"==== {src}\n{log}\n")
+        for (obj, log), (src, _, defs) in zip(results, jobs):
+            f.write(f"==== {src} {' '.join(defs)}\n{log}\n")
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -14,7 +14,20 @@
 #include "mk_internal.h"
 #include "mk_perop.h"
 
-extern "C" int mk_kernel_variant(int hd, int G, const void** fn);
+// One object per kernel variant (mk_kernel.cu compiled with -DMK_HD_V -DMK_G_V).
+#define MK_VARIANTS(X) X(64, 1) X(64, 2) X(64, 4) X(64, 8) X(128, 2) X(128, 4) X(128, 8)
+#define MK_DECL(hd, g) extern "C" const void* mk_kernel_ptr_##hd##_##g(void);
+MK_VARIANTS(MK_DECL)
+#undef MK_DECL
+
+static int mk_kernel_variant(int hd, int G, const void** fn) {
+#define MK_PICK(hd_, g_) \
+    if (hd == hd_ && G == g_) { *fn = mk_kernel_ptr_##hd_##_##g_(); return 0; }
+    MK_VARIANTS(MK_PICK)
+#undef MK_PICK
+    *fn = nullptr;
+    return -1;
+}
 
 namespace {
 
@@ -69,7 +82,7 @@ int check_shape(const mk_config* c) {
         const int n = K / 8;
         return (n <= MK_NCT) ? (MK_NCT % n == 0) : (n % MK_NCT == 0 && n / MK_NCT <= 2);
     };
-    if (!pow2_ok(c->hidden) || !pow2_ok(G * c->head_dim)) return MK_ERR_UNSUPPORTED;
+    if (!pow2_ok(c->hidden) || !pow2_ok(G * c->head_dim) || c->hidden < 256) return MK_ERR_UNSUPPORTED;
     return MK_OK;
 }
 
@@ -80,6 +93,7 @@ int build_geom(const mk_config* c, const Tune& tu, int grid, int ns, MkGeom& g) 
     if (g.TRh < 2 || g.TRo < 2 || g.JD < 1 || g.KB < 1 || tu.slot % 16) return MK_ERR_INVALID_ARG;
     if (ns < 1 || ns > 16) return MK_ERR_INVALID_ARG;
     if (g.max_rows > 4096 || g.max_nj > 8192) return MK_ERR_UNSUPPORTED;
+    if (g.CPG * g.G > MK_MAX_CPG_G) return MK_ERR_UNSUPPORTED;
     mk_smem_layout(g);
     return MK_OK;
 }

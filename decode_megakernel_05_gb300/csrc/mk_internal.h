@@ -34,6 +34,10 @@
 #define MK_PREFETCH_WARP (MK_NCW + 1)// L2 prefetch walker
 #define MK_BLOCK ((MK_NCW + 2) * 32) // 576 threads
 
+#define MK_MAX_CPG_G 640               // CTAs per group x query heads per group (combine weights)
+#define MK_COMBINE_LOADS 8            // float4 loads per thread in the attention combine
+#define MK_MISC_BYTES 6656
+
 // Device status word bits.
 #define MK_ST_TIMEOUT 0x1u
 #define MK_ST_NUMERIC 0x2u
@@ -49,16 +53,9 @@
 
 MK_HD int64_t mk_split(int64_t n, int64_t parts, int64_t k) { return (k * n) / parts; }
 
-// Rows per tile for a row-major GEMV tile of K bf16 columns.  The consumer
-// mapping gives each thread 8 consecutive columns; NCt = min(K/8, 512)
-// threads share a row, RG = 512/NCt row groups, at most 4 rows per thread.
-MK_HD int mk_gemv_nct(int K) { return (K / 8) < MK_NCT ? (K / 8) : MK_NCT; }
-MK_HD int mk_tile_rows(int K, int slot_bytes) {
-    int rg = MK_NCT / mk_gemv_nct(K);
-    int r = slot_bytes / (2 * K);
-    if (r > 4 * rg) r = 4 * rg;
-    return r & ~1;
-}
+// Rows per tile for a row-major GEMV tile of K bf16 columns: as many as fill
+// a ring slot, even (QKV pairs and gate/up groups never straddle a tile).
+MK_HD int mk_tile_rows(int K, int slot_bytes) { return (slot_bytes / (2 * K)) & ~1; }
 
 struct MkCtaPlan {
     int64_t stream_off;   // byte offset of this CTA's stream in the arena
@@ -78,7 +75,7 @@ struct MkGeom {
     int32_t max_rows, max_nj;    // per-CTA maxima (QKV rows, FFN slice)
     int32_t smem_bytes;
     // shared-memory carve-up (byte offsets from the dynamic smem base)
-    int32_t off_full, off_empty, off_xv, off_ov, off_acc, off_rows, off_u, off_red, off_sc, off_misc;
+    int32_t off_full, off_empty, off_xv, off_ov, off_acc, off_rows, off_u, off_gs, off_red, off_sc, off_misc;
 };
 
 // Fills everything but smem offsets from the shape; returns false if the
@@ -115,9 +112,10 @@ MK_HD int mk_smem_layout(MkGeom& g) {
     g.off_acc = o; o += 4 * g.G * g.hd;       // attention accumulator combine
     g.off_rows = o; o += 4 * ((g.max_rows + 3) & ~3);
     g.off_u = o; o += 4 * ((g.max_nj + 3) & ~3);
+    g.off_gs = o; o += 4 * ((g.max_nj + 3) & ~3);
     g.off_red = o; o += 4 * 2 * MK_NCT;       // double-buffered row partials
     g.off_sc = o; o += 4 * g.G * g.KB;        // attention scores of one KV block
-    g.off_misc = o; o += 2048;                // softmax state, staging, flags
+    g.off_misc = o; o += MK_MISC_BYTES;       // softmax state, staging, flags
     g.smem_bytes = o;
     return o;
 }

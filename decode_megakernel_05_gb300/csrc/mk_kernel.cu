@@ -1,906 +1,16 @@
-// mk_kernel.cu - the persistent bs=1 decode megakernel (one launch per token).
-//
-// One CTA per SM (grid = n_kv_heads * floor(SMs / n_kv_heads)).  Each CTA has
-//   - 16 consumer warps that run the segments of every layer,
-//   - a producer warp that streams the CTA's pre-laid-out weight tiles (and its
-//     share of the KV cache) into a ring of shared-memory slots with bulk
-//     asynchronous copies, guarded by full/empty mbarriers, so tile k+1..k+S
-//     load while tile k is consumed (the in-kernel prefetch loop of
-//     cloud.baidu.com/article/9434380, section 5, step 3),
-//   - a prefetch warp that walks the same tile stream further ahead and asks
-//     L2 to fetch it, so HBM keeps streaming while consumers wait on a flag.
-// Weights do not depend on activations, so the producer never waits on a
-// flag: it runs ahead through segment and layer boundaries, which is what keeps
-// the weight stream from stalling at the points where a per-operator framework
-// ends one kernel and starts the next (same page, section 4.1).
-//
-// Segment boundaries are inter-CTA flags (counters in global memory, release
-// increments and acquire polls, every wait bounded by %globaltimer):
-//   A[l][g]: query/key/value rows of KV group g written (the group's CTAs)
-//   B[l][g]: attention partials of group g written       (the group's CTAs)
-//   C[l]   : attention block added into the residual      (all CTAs)
-//   E[l]   : FFN block added into the residual            (all CTAs)
-// Per layer: segment A (RMSNorm + QKV GEMV + RoPE + K/V append) -> A ->
-// segment B (split-K GQA attention -> B -> combine + O-proj split by KV group,
-// atomically added to the residual) -> C -> segment C (RMSNorm + gate/up GEMV +
-// SiLU*up, then the down projection split over the FFN dimension, atomically
-// added to the residual) -> E.  After the last layer: RMSNorm, LM-head GEMV,
-// greedy argmax (packed 64-bit atomicMax), and the last CTA to finish resets
-// the flags for the next launch.
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <stdint.h>
+// mk_kernel.cu - one instantiation of the decode megakernel per translation
+// unit: the build compiles this file once for every (head_dim, query heads per
+// KV group) pair it supports, with -DMK_HD_V=<hd> -DMK_G_V=<G>, so the
+// variants compile in parallel.
+#include "mk_kernel.cuh"
 
-#include "mk_internal.h"
+#if !defined(MK_HD_V) || !defined(MK_G_V)
+#error "compile with -DMK_HD_V=<head_dim> -DMK_G_V=<q heads per kv head>"
+#endif
 
-namespace mk {
+#define MK_CAT2(a, b, c) a##b##_##c
+#define MK_CAT(a, b, c) MK_CAT2(a, b, c)
 
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t gtimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Barrier over the 512 consumer threads that also ORs a per-thread flag: every
-// participant gets the same answer, so an abort decision is uniform.
-__device__ __forceinline__ bool bar_or(bool f) {
-    uint32_t r;
-    asm volatile(
-        "{ .reg .pred p, q; setp.ne.u32 q, %1, 0; bar.red.or.pred p, 1, %2, q; selp.u32 %0, 1, 0, p; }"
-        : "=r"(r)
-        : "r"((uint32_t)f), "n"(MK_NCT)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
-
-// 8 bf16 (one 16-byte chunk, lower address first) -> fp32
-__device__ __forceinline__ void unpack8(const uint4 w, float f[8]) {
-    f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
-    f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xFFFF0000u);
-    f[4] = __uint_as_float(w.z << 16); f[5] = __uint_as_float(w.z & 0xFFFF0000u);
-    f[6] = __uint_as_float(w.w << 16); f[7] = __uint_as_float(w.w & 0xFFFF0000u);
-}
-__device__ __forceinline__ float dot8(const uint4 w, const float* x) {
-    float f[8];
-    unpack8(w, f);
-    float a = f[0] * x[0];
-#pragma unroll
-    for (int e = 1; e < 8; ++e) a = fmaf(f[e], x[e], a);
-    return a;
-}
-__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
-
-// ------------------------------------------------------------------ shared state
-
-struct Misc {                // lives at geo.off_misc (2048 bytes)
-    int abort;               // CTA-local: consumers gave up (producers stop)
-    int token;
-    int par;
-    int is_last;
-    unsigned long long copy_bytes;  // bytes issued by the copy producer (paces the L2 prefetcher)
-    unsigned long long cwait;       // trace: ns thread 0 spent waiting for ring data
-    float alpha[8], mrun[8], lrun[8];
-    float best_val[64];
-    int best_idx[64];
-    uint32_t tile_bytes[16]; // bytes of the tile in each ring slot (schedule check)
-    uint4 stage[32];         // K and V rows of the current position (2 * hd bf16)
-};
-static_assert(sizeof(Misc) <= 2048, "misc area");
-
-struct Smem {
-    uint8_t* ring;
-    uint64_t* full;
-    uint64_t* empty;
-    float* xv;    // [H]
-    float* ov;    // [G*hd]
-    float* acc;   // [G*hd]
-    float* rows;  // [max_rows]
-    float* u;     // [max_nj]
-    float* red;   // [2][512]
-    float* sc;    // [G][KB]
-    Misc* misc;
-};
-
-// Segment trace (off unless MkParams::trace is set): thread 0 of the consumers
-// stamps %globaltimer at the end of each segment.
-#define MK_TRACE(slot_)                                                                  \
-    do {                                                                                  \
-        if (p.trace && threadIdx.x == 0)                                                  \
-            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + (slot_)] = gtimer();           \
-    } while (0)
-
-// ------------------------------------------------------------------ waits
-
-__device__ bool wait_counter(const MkParams& p, const uint32_t* ctr, uint32_t target) {
-    uint64_t t0 = gtimer();
-    uint32_t it = 0;
-    while (ld_acquire(ctr) < target) {
-        if ((++it & 15u) == 0) {
-            if (*(volatile uint32_t*)p.status & MK_ST_ABORT) return false;
-            if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) {
-                atomicOr(p.status, MK_ST_TIMEOUT | MK_ST_ABORT);
-                return false;
-            }
-        }
-    }
-    __threadfence();
-    return true;
-}
-
-__device__ bool wait_mbar(const MkParams& p, uint64_t* b, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(b, parity)) return true;
-    uint64_t t0 = gtimer();
-    while (!mbar_try_wait(b, parity)) {
-        if (*abort) return false;
-        if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) {
-            atomicOr(p.status, MK_ST_TIMEOUT | MK_ST_ABORT);
-            *abort = 1;
-            return false;
-        }
-    }
-    return true;
-}
-
-// Arrive on a flag counter (thread 0 of the consumers, after a consumer barrier).
-__device__ __forceinline__ void arrive(const MkParams& p, int idx, int sync_id) {
-    if (p.dbg_skip_sync == sync_id && p.dbg_skip_cta == (int)blockIdx.x) return;
-    __threadfence();
-    red_release_add(p.cnt + idx, 1u);
-}
-
-// ------------------------------------------------------------------ tile stream
-
-// The tile walk (mk_walk_tiles) lives in mk_internal.h so the host can check it.
-template <class F>
-__device__ __forceinline__ void walk_tiles(const MkParams& p, const MkCtaPlan& pl, F&& f) {
-    mk_walk_tiles(p.geo, pl, p.arena, p.kc, p.vc, p.pos, f);
-}
-
-__device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem& s) {
-    volatile int* abort = &s.misc->abort;
-    const int ns = p.geo.ns;
-    const uint32_t slot_bytes = (uint32_t)p.geo.slot;
-    uint32_t k = 0;
-    bool stop = false;
-    unsigned long long pwait = 0;
-    unsigned long long* tr = p.trace ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
-    walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
-        if (stop) return;
-        const uint32_t slot = k % ns, ph = (k / ns) & 1u;
-        const uint64_t tw = tr ? gtimer() : 0;
-        if (!wait_mbar(p, &s.empty[slot], ph ^ 1u, abort)) { stop = true; return; }
-        if (tr) {
-            pwait += gtimer() - tw;
-            if ((k & 15u) == 0 && 1536 + (k >> 4) < MK_TRACE_STRIDE) tr[1536 + (k >> 4)] = pwait;
-        }
-        s.misc->tile_bytes[slot] = bytes;
-        mbar_expect_tx(&s.full[slot], bytes);
-        bulk_g2s(s.ring + (size_t)slot * slot_bytes, src, bytes, &s.full[slot]);
-        ++k;
-        *(volatile unsigned long long*)&s.misc->copy_bytes += bytes;
-    });
-    if (tr) tr[1535] = gtimer();
-    // Drain: wait for the copies still in flight before this warp leaves.
-    const uint32_t first = k > (uint32_t)ns ? k - ns : 0u;
-    for (uint32_t q = first; q < k; ++q) {
-        uint64_t t0 = gtimer();
-        while (!mbar_try_wait(&s.full[q % ns], (q / ns) & 1u)) {
-            if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) {
-                atomicOr(p.status, MK_ST_TIMEOUT | MK_ST_ABORT);
-                break;
-            }
-        }
-    }
-}
-
-__device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const Smem& s) {
-    if (p.l2_pf_bytes <= 0) return;
-    volatile int* abort = &s.misc->abort;
-    const unsigned long long ahead = (unsigned long long)p.l2_pf_bytes;
-    unsigned long long issued = 0;
-    bool stop = false;
-    walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
-        if (stop) return;
-        uint64_t t0 = 0;
-        while (issued > *(volatile unsigned long long*)&s.misc->copy_bytes + ahead) {
-            if (*abort) { stop = true; return; }
-            if (t0 == 0) t0 = gtimer();
-            else if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) { stop = true; return; }
-            __nanosleep(256);
-        }
-        // tiles the copy producer has already issued need no prefetch
-        if (issued + bytes > *(volatile unsigned long long*)&s.misc->copy_bytes) prefetch_l2(src, bytes);
-        issued += bytes;
-    });
-}
-
-// ------------------------------------------------------------------ consumer pieces
-
-// Consumer-side cursor over the ring.
-struct Ring {
-    uint32_t k = 0;
-    __device__ __forceinline__ uint32_t slot(int ns) const { return k % ns; }
-};
-
-// Waits for the ring slot of tile k (warp-cooperative; lane 0 polls).
-__device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t expect_bytes,
-                                          const uint8_t*& tile) {
-    const int ns = p.geo.ns;
-    const uint32_t slot = rg.k % ns, ph = (rg.k / ns) & 1u;
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) {
-        const uint64_t tw = (p.trace && threadIdx.x == 0) ? gtimer() : 0;
-        ok = !s.misc->abort && wait_mbar(p, &s.full[slot], ph, &s.misc->abort);
-        if (tw) s.misc->cwait += gtimer() - tw;
-        if (ok && s.misc->tile_bytes[slot] != expect_bytes) {
-            atomicOr(p.status, MK_ST_SCHEDULE | MK_ST_ABORT);
-            s.misc->abort = 1;
-            ok = false;
-        }
-    }
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    tile = s.ring + (size_t)slot * p.geo.slot;
-    return ok;
-}
-__device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, Ring& rg) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[rg.k % p.geo.ns]);
-    ++rg.k;
-}
-
-// Thread mapping of a row-major GEMV tile with K columns.
-struct GemvMap {
-    int K, nct, RG, rg, ct, m, S;
-};
-__device__ __forceinline__ GemvMap gemv_map(int K) {
-    GemvMap mp;
-    const int t = threadIdx.x;
-    mp.K = K;
-    mp.nct = mk_gemv_nct(K);
-    mp.RG = MK_NCT / mp.nct;
-    mp.rg = t / mp.nct;
-    mp.ct = t % mp.nct;
-    mp.m = (K / 8) / mp.nct;
-    mp.S = mp.nct < 32 ? mp.nct : 32;
-    return mp;
-}
-__device__ __forceinline__ void load_x(const float* vec, const GemvMap& mp, float xr[2][8]) {
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        if (c < mp.m) {
-            const float4* v = reinterpret_cast<const float4*>(vec + (mp.ct + c * mp.nct) * 8);
-            float4 a = v[0], b = v[1];
-            xr[c][0] = a.x; xr[c][1] = a.y; xr[c][2] = a.z; xr[c][3] = a.w;
-            xr[c][4] = b.x; xr[c][5] = b.y; xr[c][6] = b.z; xr[c][7] = b.w;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xr[c][e] = 0.f;
-        }
-    }
-}
-
-// Partial dot products of one tile, reduced to per-warp row sums written to
-// red[buf]; returns the uniform abort flag of the barrier that follows.
-__device__ __forceinline__ bool gemv_tile(const MkParams& p, const Smem& s, Ring& ring, const GemvMap& mp,
-                                          const float xr[2][8], int R, int buf, bool abort_in) {
-    const uint8_t* tile;
-    const uint32_t bytes = (uint32_t)(R * mp.K * 2);
-    bool ok = !abort_in && take_tile(p, s, ring, bytes, tile);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (ok) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int r = mp.rg + k * mp.RG;
-            if (r < R) {
-                const uint8_t* row = tile + (size_t)r * mp.K * 2;
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    if (c < mp.m) acc[k] += dot8(lds128(row + (mp.ct + c * mp.nct) * 16), xr[c]);
-            }
-        }
-    }
-    if (!abort_in) release_tile(p, s, ring);
-    // reduce-scatter 4 row partials over the S lanes of a sub-group
-    const int S = mp.S, ls = threadIdx.x & (S - 1);
-    const bool b1 = ls & (S >> 1), b2 = ls & (S >> 2);
-    float s0 = b1 ? acc[0] : acc[2], s1 = b1 ? acc[1] : acc[3];
-    float r0 = __shfl_xor_sync(0xFFFFFFFFu, s0, S >> 1);
-    float r1 = __shfl_xor_sync(0xFFFFFFFFu, s1, S >> 1);
-    float k0 = (b1 ? acc[2] : acc[0]) + r0, k1 = (b1 ? acc[3] : acc[1]) + r1;
-    float s2 = b2 ? k0 : k1;
-    float r2 = __shfl_xor_sync(0xFFFFFFFFu, s2, S >> 2);
-    float v = (b2 ? k1 : k0) + r2;
-    for (int o = S >> 3; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    if ((ls & ((S >> 2) - 1)) == 0) s.red[buf * MK_NCT + (threadIdx.x / S) * 4 + (b1 ? 2 : 0) + (b2 ? 1 : 0)] = v;
-    return bar_or(!ok || abort_in);
-}
-// Full sum of tile row r (valid after gemv_tile's barrier).
-__device__ __forceinline__ float row_sum(const Smem& s, const GemvMap& mp, int buf, int r) {
-    const int rg = r % mp.RG, k = r / mp.RG, nsg = mp.nct / mp.S;
-    const float* red = s.red + buf * MK_NCT;
-    float a = 0.f;
-    for (int w = 0; w < nsg; ++w) a += red[(rg * nsg + w) * 4 + k];
-    return a;
-}
-
-// RMSNorm of x (fp32 global, or the bf16 embedding row when xb != nullptr) into
-// s.xv, with gain g (fp32).  Returns the uniform abort flag.
-__device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, const uint16_t* xb, const float* g,
-                              bool abort_in) {
-    const int H = p.geo.H, t = threadIdx.x;
-    float ss = 0.f;
-    for (int i = t; i < H; i += MK_NCT) {
-        float v = xb ? bf2f(xb[i]) : __ldcg(x + i);
-        s.xv[i] = v;
-        ss = fmaf(v, v, ss);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-    if ((t & 31) == 0) s.red[t >> 5] = ss;
-    bool ab = bar_or(abort_in);
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < MK_NCW; ++w) tot += s.red[w];
-    const float inv = rsqrtf(tot / (float)H + p.eps);
-    for (int i = t; i < H; i += MK_NCT) s.xv[i] = s.xv[i] * inv * g[i];
-    return bar_or(ab);
-}
-
-// Thread 0 waits on a counter; the result is made uniform by the barrier.
-__device__ __forceinline__ bool sync_wait(const MkParams& p, int idx, uint32_t target, bool abort_in) {
-    bool bad = abort_in;
-    if (threadIdx.x == 0 && !bad) bad = !wait_counter(p, p.cnt + idx, target);
-    return bar_or(bad);
-}
-
-// ------------------------------------------------------------------ attention
-
-template <int HD, int G>
-struct Attn {
-    static constexpr int LP = HD / 8;            // lanes per position (8 dims each)
-    static constexpr int PPP = MK_NCT / LP;      // positions per pass
-
-    // One K/V block of n positions at kt / vt (bf16 [n][HD]); updates the
-    // running max / sum in smem and the accumulators in registers.
-    static __device__ __forceinline__ bool block(const Smem& s, const uint8_t* kt, const uint8_t* vt, int n,
-                                                 const float qr[G][8], float acc[G][8], int KB, bool abort_in,
-                                                 const MkParams& p, Ring* ring, bool from_ring, bool& ok_k) {
-        const int t = threadIdx.x, pl = t / LP, dc = t % LP;
-        if (ok_k) {
-            // warp-uniform trip count: every lane runs every shuffle
-            for (int q0 = 0; q0 < n; q0 += PPP) {
-                const int q = q0 + pl;
-                const bool valid = q < n;
-                float f[8];
-                if (valid) unpack8(lds128(kt + ((size_t)q * HD + dc * 8) * 2), f);
-                else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = 0.f;
-                }
-                float sh[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float a = f[0] * qr[h][0];
-#pragma unroll
-                    for (int e = 1; e < 8; ++e) a = fmaf(f[e], qr[h][e], a);
-                    sh[h] = a;
-                }
-#pragma unroll
-                for (int o = LP / 2; o >= 1; o >>= 1)
-#pragma unroll
-                    for (int h = 0; h < G; ++h) sh[h] += __shfl_xor_sync(0xFFFFFFFFu, sh[h], o);
-                if (dc == 0 && valid)
-#pragma unroll
-                    for (int h = 0; h < G; ++h) s.sc[h * KB + q] = sh[h];
-            }
-        }
-        // the loop above has a data-dependent trip count, so re-converge before shuffles elsewhere
-        __syncwarp();
-        if (from_ring) release_tile(p, s, *ring);
-        bool ab = bar_or(abort_in || !ok_k);
-        const int w = t >> 5, lane = t & 31;
-        if (w < G && !ab) {
-            const int h = w;
-            float mx = -INFINITY;
-            for (int q = lane; q < n; q += 32) mx = fmaxf(mx, s.sc[h * KB + q]);
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-            const float mold = s.misc->mrun[h];
-            const float mn = fmaxf(mold, mx);
-            const float alpha = (mold == -INFINITY) ? 0.f : exp2f(mold - mn);
-            float sum = 0.f;
-            for (int q = lane; q < n; q += 32) {
-                float e = exp2f(s.sc[h * KB + q] - mn);
-                s.sc[h * KB + q] = e;
-                sum += e;
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-            if (lane == 0) {
-                s.misc->lrun[h] = s.misc->lrun[h] * alpha + sum;
-                s.misc->mrun[h] = mn;
-                s.misc->alpha[h] = alpha;
-            }
-        }
-        ab = bar_or(ab);
-        return ab;
-    }
-    static __device__ __forceinline__ void accumulate_v(const Smem& s, const uint8_t* vt, int n, float acc[G][8],
-                                                        int KB, bool ok) {
-        const int t = threadIdx.x, pl = t / LP, dc = t % LP;
-        if (!ok) return;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float a = s.misc->alpha[h];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] *= a;
-        }
-        for (int q = pl; q < n; q += PPP) {
-            float f[8];
-            unpack8(lds128(vt + ((size_t)q * HD + dc * 8) * 2), f);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float wgt = s.sc[h * KB + q];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wgt, f[e], acc[h][e]);
-            }
-        }
-    }
-};
-
-// ------------------------------------------------------------------ the kernel
-
-template <int HD, int G>
-__global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const MkGeom& g = p.geo;
-    Smem s;
-    s.ring = smem;
-    s.full = reinterpret_cast<uint64_t*>(smem + g.off_full);
-    s.empty = reinterpret_cast<uint64_t*>(smem + g.off_empty);
-    s.xv = reinterpret_cast<float*>(smem + g.off_xv);
-    s.ov = reinterpret_cast<float*>(smem + g.off_ov);
-    s.acc = reinterpret_cast<float*>(smem + g.off_acc);
-    s.rows = reinterpret_cast<float*>(smem + g.off_rows);
-    s.u = reinterpret_cast<float*>(smem + g.off_u);
-    s.red = reinterpret_cast<float*>(smem + g.off_red);
-    s.sc = reinterpret_cast<float*>(smem + g.off_sc);
-    s.misc = reinterpret_cast<Misc*>(smem + g.off_misc);
-
-    const int t = threadIdx.x;
-    const int c = blockIdx.x;
-    const MkCtaPlan pl = p.plans[c];
-
-    if (t == 0) {
-        for (int i = 0; i < g.ns; ++i) {
-            mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], MK_NCW);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        s.misc->abort = 0;
-        s.misc->copy_bytes = 0;
-        s.misc->cwait = 0;
-        s.misc->is_last = 0;
-        int tok = p.token_ptr ? *p.token_ptr : p.token;
-        if (tok < 0 || tok >= g.V) {
-            if (c == 0) atomicOr(p.status, MK_ST_BADTOKEN);
-            tok = 0;
-        }
-        s.misc->token = tok;
-        s.misc->par = (int)(*(volatile uint32_t*)p.seq & 1u);
-        for (int h = 0; h < 8; ++h) { s.misc->mrun[h] = -INFINITY; s.misc->lrun[h] = 0.f; s.misc->alpha[h] = 0.f; }
-    }
-    __syncthreads();
-
-    const int warp = t >> 5;
-    if (warp == MK_PRODUCER_WARP) {
-        if ((t & 31) == 0) producer_copy(p, pl, s);
-        return;
-    }
-    if (warp == MK_PREFETCH_WARP) {
-        if ((t & 31) == 0) producer_prefetch(p, pl, s);
-        return;
-    }
-
-    // ======================= consumers (512 threads) =======================
-    const int H = g.H, L = g.L, hd2 = HD / 2;
-    const int par = s.misc->par, token = s.misc->token;
-    const size_t state = (size_t)H;
-    float* xa = p.xacc + (size_t)par * 2 * L * state;              // this launch's residual states
-    {   // zero the other parity's states for the next launch
-        float* xz = p.xacc + (size_t)(par ^ 1) * 2 * L * state;
-        const size_t n = 2 * (size_t)L * state;
-        const size_t lo = mk_split((int64_t)n, g.nC, c), hi = mk_split((int64_t)n, g.nC, c + 1);
-        for (size_t i = lo + t; i < hi; i += MK_NCT) xz[i] = 0.f;
-    }
-    const uint16_t* emb = p.embed + (size_t)token * H;
-    const int ctx = p.pos + 1;
-    const int ka = (int)mk_split(ctx, g.CPG, pl.i), kb_ = (int)mk_split(ctx, g.CPG, pl.i + 1);
-    const int ke = kb_ < p.pos ? kb_ : p.pos;
-    const bool has_cur = (pl.i == g.CPG - 1);
-    const float qscale = rsqrtf((float)HD) * 1.4426950408889634f;  // 1/sqrt(hd) * log2(e)
-
-    Ring ring;
-    int buf = 0;
-    bool ab = false;
-    const GemvMap mh = gemv_map(H);
-    const GemvMap mo = gemv_map(G * HD);
-    float xr[2][8];
-
-    MK_TRACE(16 * L + 3);
-    for (int l = 0; l < L && !ab; ++l) {
-        // ---------------- segment A: RMSNorm + QKV GEMV + RoPE + K/V append
-        MK_TRACE(16 * l + 0);
-        const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
-        ab = rmsnorm_to_xv(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab);
-        MK_TRACE(16 * l + 1);
-        load_x(s.xv, mh, xr);
-        const int nr = 2 * pl.npairs;
-        for (int r0 = 0; r0 < nr; r0 += g.TRh) {
-            const int R = min(g.TRh, nr - r0);
-            ab = gemv_tile(p, s, ring, mh, xr, R, buf, ab);
-            if (t < R) s.rows[r0 + t] = row_sum(s, mh, buf, t);
-            buf ^= 1;
-        }
-        ab = bar_or(ab);
-        MK_TRACE(16 * l + 2);
-        if (!ab) {
-            for (int j = t; j < pl.npairs; j += MK_NCT) {
-                const int pair = pl.pair0 + j, slot = pair / hd2, d = pair % hd2;
-                float a = s.rows[2 * j], b = s.rows[2 * j + 1];
-                if (slot <= G) {
-                    const float cs = p.rope_cos[(size_t)p.pos * hd2 + d], sn = p.rope_sin[(size_t)p.pos * hd2 + d];
-                    const float a2 = a * cs - b * sn, b2 = b * cs + a * sn;
-                    a = a2; b = b2;
-                }
-                if (slot < G) {
-                    float* q = p.qbuf + (size_t)l * g.qh * HD + (size_t)(pl.g * G + slot) * HD;
-                    q[d] = a; q[d + hd2] = b;
-                } else {
-                    uint16_t* dst = (slot == G ? p.kc : p.vc) +
-                                    (((size_t)l * g.kvh + pl.g) * g.max_seq + p.pos) * HD;
-                    dst[d] = f2bf(a); dst[d + hd2] = f2bf(b);
-                }
-            }
-        }
-        ab = bar_or(ab);
-        MK_TRACE(16 * l + 3);
-        if (t == 0 && !ab) arrive(p, mk_cnt_A(g, l, pl.g), 4 * l + 0);
-        ab = sync_wait(p, mk_cnt_A(g, l, pl.g), (uint32_t)g.CPG, ab);
-        MK_TRACE(16 * l + 4);
-
-        // ---------------- segment B: split-K attention over this CTA's positions
-        if (!ab) {
-            const float* qsrc = p.qbuf + (size_t)l * g.qh * HD + (size_t)pl.g * G * HD;
-            for (int i = t; i < G * HD; i += MK_NCT) { s.ov[i] = __ldcg(qsrc + i) * qscale; s.acc[i] = 0.f; }
-            if (t < G) { s.misc->mrun[t] = -INFINITY; s.misc->lrun[t] = 0.f; }
-            if (has_cur && t < HD / 4) {   // stage K[pos], V[pos] written by this group this launch
-                const size_t off = (((size_t)l * g.kvh + pl.g) * g.max_seq + p.pos) * HD;
-                const uint4* src = reinterpret_cast<const uint4*>((t < HD / 8 ? p.kc : p.vc) + off);
-                s.misc->stage[t] = __ldcg(src + (t % (HD / 8)));
-            }
-        }
-        ab = bar_or(ab);
-        {
-            using A = Attn<HD, G>;
-            const int pl_ = t / A::LP, dc = t % A::LP;
-            float qr[G][8], acc[G][8];
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) { qr[h][e] = s.ov[h * HD + dc * 8 + e]; acc[h][e] = 0.f; }
-            (void)pl_;
-            for (int q0 = ka; q0 < ke; q0 += g.KB) {
-                const int n = min(g.KB, ke - q0);
-                const uint8_t *kt, *vt;
-                bool okk = !ab && take_tile(p, s, ring, (uint32_t)(n * HD * 2), kt);
-                ab = A::block(s, kt, nullptr, n, qr, acc, g.KB, ab, p, &ring, true, okk);
-                bool okv = !ab && take_tile(p, s, ring, (uint32_t)(n * HD * 2), vt);
-                A::accumulate_v(s, vt, n, acc, g.KB, okv);
-                __syncwarp();
-                release_tile(p, s, ring);
-                ab = bar_or(ab || !okv);
-            }
-            if (has_cur) {
-                const uint8_t* st = reinterpret_cast<const uint8_t*>(s.misc->stage);
-                bool okc = !ab;
-                ab = A::block(s, st, nullptr, 1, qr, acc, g.KB, ab, p, nullptr, false, okc);
-                A::accumulate_v(s, st + HD * 2, 1, acc, g.KB, !ab);
-                ab = bar_or(ab);
-            }
-            // combine the position lanes: in-warp, then across warps with smem atomics
-#pragma unroll
-            for (int o = A::LP; o < 32; o <<= 1)
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[h][e], o);
-            if ((t & 31) < A::LP && !ab) {
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) atomicAdd(&s.acc[h * HD + dc * 8 + e], acc[h][e]);
-            }
-        }
-        ab = bar_or(ab);
-        if (!ab) {
-            const size_t pbase = (((size_t)l * g.kvh + pl.g) * g.CPG + pl.i) * G;
-            for (int i = t; i < G * HD; i += MK_NCT) p.part_acc[pbase * HD + i] = s.acc[i];
-            if (t < G) {
-                p.part_ml[(pbase + t) * 2 + 0] = s.misc->mrun[t];
-                p.part_ml[(pbase + t) * 2 + 1] = s.misc->lrun[t];
-            }
-        }
-        ab = bar_or(ab);
-        MK_TRACE(16 * l + 5);
-        if (t == 0 && !ab) arrive(p, mk_cnt_B(g, l, pl.g), 4 * l + 1);
-        ab = sync_wait(p, mk_cnt_B(g, l, pl.g), (uint32_t)g.CPG, ab);
-        MK_TRACE(16 * l + 6);
-
-        // combine the group's partials -> o (the G heads of this KV group)
-        if (!ab) {
-            const size_t gbase = ((size_t)l * g.kvh + pl.g) * g.CPG * G;
-            for (int i = t; i < G * HD; i += MK_NCT) {
-                const int h = i / HD;
-                float mx = -INFINITY;
-                for (int j = 0; j < g.CPG; ++j) mx = fmaxf(mx, __ldcg(p.part_ml + ((gbase + (size_t)j * G + h) * 2)));
-                float num = 0.f, den = 0.f;
-                for (int j = 0; j < g.CPG; ++j) {
-                    const size_t pj = gbase + (size_t)j * G + h;
-                    const float mj = __ldcg(p.part_ml + pj * 2);
-                    const float w = (mj == -INFINITY) ? 0.f : exp2f(mj - mx);
-                    den = fmaf(w, __ldcg(p.part_ml + pj * 2 + 1), den);
-                    num = fmaf(w, __ldcg(p.part_acc + pj * HD + (i % HD)), num);
-                }
-                s.ov[i] = num / den;
-            }
-        }
-        ab = bar_or(ab);
-        MK_TRACE(16 * l + 7);
-
-        // O-proj (rows of this CTA, columns of this group) + residual, atomically
-        load_x(s.ov, mo, xr);
-        float* xo = xa + (size_t)(2 * l) * state;
-        for (int r0 = 0; r0 < pl.norows; r0 += g.TRo) {
-            const int R = min(g.TRo, pl.norows - r0);
-            ab = gemv_tile(p, s, ring, mo, xr, R, buf, ab);
-            if (t < R && !ab) {
-                const int row = pl.orow0 + r0 + t;
-                float v = row_sum(s, mo, buf, t);
-                if (pl.g == 0) v += (l == 0) ? bf2f(emb[row]) : __ldcg(xin + row);
-                atomicAdd(xo + row, v);
-            }
-            buf ^= 1;
-        }
-        ab = bar_or(ab);
-        MK_TRACE(16 * l + 8);
-        if (t == 0 && !ab) arrive(p, mk_cnt_C(g, l), 4 * l + 2);
-        ab = sync_wait(p, mk_cnt_C(g, l), (uint32_t)g.nC, ab);
-        MK_TRACE(16 * l + 9);
-
-        // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
-        ab = rmsnorm_to_xv(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab);
-        MK_TRACE(16 * l + 10);
-        load_x(s.xv, mh, xr);
-        for (int j0 = 0; j0 < pl.nj; j0 += g.JT) {
-            const int n = min(g.JT, pl.nj - j0);
-            ab = gemv_tile(p, s, ring, mh, xr, 2 * n, buf, ab);
-            if (t < n && !ab) {
-                const float gt = row_sum(s, mh, buf, t), up = row_sum(s, mh, buf, t + n);
-                s.u[j0 + t] = gt / (1.f + __expf(-gt)) * up;
-            }
-            buf ^= 1;
-        }
-        MK_TRACE(16 * l + 11);
-        // down projection: this CTA's FFN columns, all H rows (split-K)
-        const int U = H / 8;
-        const int JG = U < MK_NCT ? MK_NCT / U : 1;
-        const int MU = U > MK_NCT ? U / MK_NCT : 1;
-        const int jg = U < MK_NCT ? t / U : 0, unit = U < MK_NCT ? t % U : t;
-        ab = bar_or(ab);                                        // every thread has its x registers
-        for (int i = t; i < H; i += MK_NCT) s.xv[i] = 0.f;     // xv is free now: combine buffer
-        ab = bar_or(ab);
-        float dacc[2][8];
-#pragma unroll
-        for (int mu = 0; mu < 2; ++mu)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dacc[mu][e] = 0.f;
-        for (int j0 = 0; j0 < pl.nj; j0 += g.JD) {
-            const int n = min(g.JD, pl.nj - j0);
-            const uint8_t* tile;
-            bool ok = !ab && take_tile(p, s, ring, (uint32_t)(n * H * 2), tile);
-            if (ok) {
-                for (int jj = jg; jj < n; jj += JG) {
-                    const float uj = s.u[j0 + jj];
-#pragma unroll
-                    for (int mu = 0; mu < 2; ++mu) {
-                        if (mu < MU) {
-                            float f[8];
-                            unpack8(lds128(tile + ((size_t)jj * H + (unit + mu * MK_NCT) * 8) * 2), f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) dacc[mu][e] = fmaf(f[e], uj, dacc[mu][e]);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (!ab) release_tile(p, s, ring);
-            if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
-        }
-        ab = bar_or(ab);
-        float* xf = xa + (size_t)(2 * l + 1) * state;
-        if (JG > 1) {
-            if (!ab)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) atomicAdd(&s.xv[unit * 8 + e], dacc[0][e]);
-            ab = bar_or(ab);
-            if (!ab)
-                for (int i = t; i < H / 4; i += MK_NCT) {
-                    float4 v = reinterpret_cast<const float4*>(s.xv)[i];
-                    if (c == 0) {
-                        v.x += __ldcg(xo + 4 * i + 0); v.y += __ldcg(xo + 4 * i + 1);
-                        v.z += __ldcg(xo + 4 * i + 2); v.w += __ldcg(xo + 4 * i + 3);
-                    }
-                    atomicAdd(reinterpret_cast<float4*>(xf) + i, v);
-                }
-        } else if (!ab) {
-#pragma unroll
-            for (int mu = 0; mu < 2; ++mu) {
-                if (mu < MU) {
-                    const int r = (unit + mu * MK_NCT) * 8;
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float4 v = make_float4(dacc[mu][4 * hh + 0], dacc[mu][4 * hh + 1], dacc[mu][4 * hh + 2],
-                                               dacc[mu][4 * hh + 3]);
-                        if (c == 0) {
-                            v.x += __ldcg(xo + r + 4 * hh + 0); v.y += __ldcg(xo + r + 4 * hh + 1);
-                            v.z += __ldcg(xo + r + 4 * hh + 2); v.w += __ldcg(xo + r + 4 * hh + 3);
-                        }
-                        atomicAdd(reinterpret_cast<float4*>(xf + r) + hh, v);
-                    }
-                }
-            }
-        }
-        ab = bar_or(ab);
-        MK_TRACE(16 * l + 12);
-        if (t == 0 && !ab) arrive(p, mk_cnt_E(g, l), 4 * l + 3);
-        ab = sync_wait(p, mk_cnt_E(g, l), (uint32_t)g.nC, ab);
-        MK_TRACE(16 * l + 13);
-        if (p.trace && t == 0) {
-            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + l] = s.misc->cwait;
-            s.misc->cwait = 0;
-        }
-    }
-
-    // ---------------- final RMSNorm + LM head + argmax
-    {
-        const float* xl = xa + (size_t)(2 * L - 1) * state;
-        ab = rmsnorm_to_xv(p, s, xl, nullptr, p.final_norm, ab);
-        MK_TRACE(16 * L + 0);
-        if (c == 0 && !ab)
-            for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv[i];
-        load_x(s.xv, mh, xr);
-        float bv = -INFINITY;
-        int bi = -1;
-        bool nonfinite = false;
-        for (int r0 = 0; r0 < pl.nv; r0 += g.TRh) {
-            const int R = min(g.TRh, pl.nv - r0);
-            ab = gemv_tile(p, s, ring, mh, xr, R, buf, ab);
-            if (t < R && !ab) {
-                const int v = pl.v0 + r0 + t;
-                const float lg = row_sum(s, mh, buf, t);
-                if (p.logits) p.logits[v] = lg;
-                if (isfinite(lg)) {
-                    if (lg > bv || (lg == bv && v < bi)) { bv = lg; bi = v; }
-                } else {
-                    nonfinite = true;
-                }
-            }
-            buf ^= 1;
-        }
-        MK_TRACE(16 * L + 1);
-        if (p.trace && t == 0) p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + L] = s.misc->cwait;
-        if (nonfinite) atomicOr(p.status, MK_ST_NUMERIC);
-        if (t < 64) { s.misc->best_val[t] = bv; s.misc->best_idx[t] = bi; }
-        ab = bar_or(ab);
-        if (t == 0 && !ab) {
-            float v = -INFINITY;
-            int idx = -1;
-            for (int i = 0; i < 64; ++i) {
-                const int ii = s.misc->best_idx[i];
-                const float vv = s.misc->best_val[i];
-                if (ii >= 0 && (idx < 0 || vv > v || (vv == v && ii < idx))) { v = vv; idx = ii; }
-            }
-            if (idx >= 0) {
-                uint32_t u = __float_as_uint(v);
-                u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-                const unsigned long long key = ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)idx);
-                atomicMax(p.amax, key);
-            }
-        }
-    }
-
-    // ---------------- end of step: the last CTA publishes the token and resets the flags
-    MK_TRACE(16 * L + 2);
-    if (t == 0 && ab) s.misc->abort = 1;   // lets the producer warps stop and drain
-    if (t == 0) {
-        __threadfence();
-        const uint32_t prev = atomicAdd(p.cnt + mk_cnt_done(g), 1u);
-        s.misc->is_last = (prev == (uint32_t)g.nC - 1) ? 1 : 0;
-    }
-    bar_or(false);
-    if (s.misc->is_last) {
-        __threadfence();
-        const int ntot = mk_cnt_done(g);
-        for (int i = t; i < ntot; i += MK_NCT) p.cnt[i] = 0u;
-        if (t == 0) {
-            const unsigned long long key = atomicMax(p.amax, 0ull);
-            int tok = 0;
-            if (key == 0ull) atomicOr(p.status, MK_ST_NUMERIC);
-            else tok = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-            *p.next_token = tok;
-            if (p.tokens_out) p.tokens_out[p.out_idx] = tok;
-            *p.amax = 0ull;
-            p.cnt[ntot] = 0u;
-            atomicAdd(p.seq, 1u);
-            atomicAnd(p.status, ~MK_ST_ABORT);
-            __threadfence();
-        }
-    }
-}
-
-}  // namespace mk
-
-// ------------------------------------------------------------------ launch entry (host side)
-
-typedef void (*mk_kernel_fn)(MkParams);
-
-extern "C" int mk_kernel_variant(int hd, int G, const void** fn) {
-#define MK_V(HD_, G_) \
-    if (hd == HD_ && G == G_) { *fn = (const void*)&mk::mk_decode_kernel<HD_, G_>; return 0; }
-    MK_V(64, 1) MK_V(64, 2) MK_V(64, 4) MK_V(64, 8) MK_V(128, 2) MK_V(128, 4) MK_V(128, 8)
-#undef MK_V
-    *fn = nullptr;
-    return -1;
+extern "C" const void* MK_CAT(mk_kernel_ptr_, MK_HD_V, MK_G_V)(void) {
+    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V>;
 }

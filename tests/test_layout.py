@@ -14,9 +14,7 @@ def split(n, parts, k):
 
 
 def tile_rows(K, slot):
-    nct = min(K // 8, 512)
-    r = min(slot // (2 * K), 4 * (512 // nct))
-    return r & ~1
+    return (slot // (2 * K)) & ~1
 
 
 def decode_arena(arena, s, grid, slot=32768):
