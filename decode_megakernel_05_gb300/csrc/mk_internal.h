@@ -37,6 +37,7 @@
 #define MK_MAX_CPG_G 640               // CTAs per group x query heads per group (combine weights)
 #define MK_COMBINE_LOADS 8            // float4 loads per thread in the attention combine
 #define MK_MISC_BYTES 6656
+#define MK_DOWN_UNITS 4               // 4-row units per consumer thread in the down projection (H <= 8192)
 
 // Device status word bits.
 #define MK_ST_TIMEOUT 0x1u
@@ -114,7 +115,7 @@ MK_HD int mk_smem_layout(MkGeom& g) {
     g.off_u = o; o += 4 * ((g.max_nj + 3) & ~3);
     g.off_gs = o; o += 4 * ((g.max_nj + 3) & ~3);
     g.off_red = o; o += 4 * 2 * MK_NCT;       // double-buffered row partials
-    g.off_sc = o; o += 4 * g.G * g.KB;        // attention scores of one KV block
+    g.off_sc = o; o += 4 * g.G * (g.KB + 4);  // attention scores of one KV block (+ the current position)
     g.off_misc = o; o += MK_MISC_BYTES;       // softmax state, staging, flags
     g.smem_bytes = o;
     return o;

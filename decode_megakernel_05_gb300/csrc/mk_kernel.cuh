@@ -82,6 +82,11 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Vector fp32 reduction into global memory (no return value).
+__device__ __forceinline__ void red_add_v4(float* p, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
 // Barrier over the 512 consumer threads that also ORs a per-thread flag: every
 // participant gets the same answer, so an abort decision is uniform.
 __device__ __forceinline__ bool bar_or(bool f) {
@@ -425,9 +430,11 @@ struct Attn {
 
     // One K/V block of n positions at kt / vt (bf16 [n][HD]); updates the
     // running max / sum in smem and the accumulators in registers.
-    static __device__ __forceinline__ bool block(const Smem& s, const uint8_t* kt, const uint8_t* vt, int n,
-                                                 const float qr[G][8], float acc[G][8], int KB, bool abort_in,
-                                                 const MkParams& p, Ring* ring, bool from_ring, bool& ok_k) {
+    // Positions q < nr come from the ring tile kt, position nr (when n > nr)
+    // from the staged row st.
+    static __device__ __forceinline__ bool block(const Smem& s, const uint8_t* kt, int nr, const uint8_t* st, int n,
+                                                 const float qr[G][8], int KB, bool abort_in, const MkParams& p,
+                                                 Ring* ring, bool from_ring, bool& ok_k) {
         const int t = threadIdx.x, pl = t / LP, dc = t % LP;
         if (ok_k) {
             // warp-uniform trip count: every lane runs every shuffle
@@ -435,7 +442,7 @@ struct Attn {
                 const int q = q0 + pl;
                 const bool valid = q < n;
                 float f[8];
-                if (valid) unpack8(lds128(kt + ((size_t)q * HD + dc * 8) * 2), f);
+                if (valid) unpack8(lds128((q < nr ? kt + (size_t)q * HD * 2 : st) + dc * 16), f);
                 else {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] = 0.f;
@@ -488,8 +495,8 @@ struct Attn {
         ab = bar_or(ab);
         return ab;
     }
-    static __device__ __forceinline__ void accumulate_v(const Smem& s, const uint8_t* vt, int n, float acc[G][8],
-                                                        int KB, bool ok) {
+    static __device__ __forceinline__ void accumulate_v(const Smem& s, const uint8_t* vt, int nr, const uint8_t* stv,
+                                                        int n, float acc[G][8], int KB, bool ok) {
         const int t = threadIdx.x, pl = t / LP, dc = t % LP;
         if (!ok) return;
 #pragma unroll
@@ -500,7 +507,7 @@ struct Attn {
         }
         for (int q = pl; q < n; q += PPP) {
             float f[8];
-            unpack8(lds128(vt + ((size_t)q * HD + dc * 8) * 2), f);
+            unpack8(lds128((q < nr ? vt + (size_t)q * HD * 2 : stv) + dc * 16), f);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 const float wgt = s.sc[h * KB + q];
@@ -642,23 +649,25 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 #pragma unroll
                 for (int e = 0; e < 8; ++e) { qr[h][e] = s.ov[h * HD + dc * 8 + e]; acc[h][e] = 0.f; }
             (void)pl_;
-            for (int q0 = ka; q0 < ke; q0 += g.KB) {
-                const int n = min(g.KB, ke - q0);
-                const uint8_t *kt, *vt;
-                bool okk = !ab && take_tile(p, s, ring, (uint32_t)(n * HD * 2), kt);
-                ab = A::block(s, kt, nullptr, n, qr, acc, g.KB, ab, p, &ring, true, okk);
-                bool okv = !ab && take_tile(p, s, ring, (uint32_t)(n * HD * 2), vt);
-                A::accumulate_v(s, vt, n, acc, g.KB, okv);
+            // Blocks of up to KB past positions from the ring; the last CTA of the
+            // group appends the current position (staged from global) to its
+            // last block, or runs it as a block of its own when it has no past.
+            const int nring = ke > ka ? ke - ka : 0;
+            const int nblk = (nring + g.KB - 1) / g.KB;
+            const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
+            const uint8_t* st = reinterpret_cast<const uint8_t*>(s.misc->stage);
+            for (int b = 0; b < nbt; ++b) {
+                const int q0 = ka + b * g.KB;
+                const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
+                const int n = nr + ((has_cur && b == nbt - 1) ? 1 : 0);
+                const uint8_t *kt = st, *vt = st;
+                bool okk = !ab && (nr == 0 || take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt));
+                ab = A::block(s, kt, nr, st, n, qr, g.KB + 4, ab, p, &ring, nr > 0, okk);   // sc stride KB + 4
+                bool okv = !ab && (nr == 0 || take_tile(p, s, ring, (uint32_t)(nr * HD * 2), vt));
+                A::accumulate_v(s, vt, nr, st + HD * 2, n, acc, g.KB + 4, okv);
                 __syncwarp();
-                release_tile(p, s, ring);
+                if (nr > 0) release_tile(p, s, ring);
                 ab = bar_or(ab || !okv);
-            }
-            if (has_cur) {
-                const uint8_t* st = reinterpret_cast<const uint8_t*>(s.misc->stage);
-                bool okc = !ab;
-                ab = A::block(s, st, nullptr, 1, qr, acc, g.KB, ab, p, nullptr, false, okc);
-                A::accumulate_v(s, st + HD * 2, 1, acc, g.KB, !ab);
-                ab = bar_or(ab);
             }
             // combine the position lanes: in-warp, then across warps with smem atomics
 #pragma unroll
@@ -769,71 +778,50 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
         }
         MK_TRACE(16 * l + 11);
-        // down projection: this CTA's FFN columns, all H rows (split-K)
-        const int U = H / 8;
-        const int JG = U < MK_NCT ? MK_NCT / U : 1;
-        const int MU = U > MK_NCT ? U / MK_NCT : 1;
-        const int jg = U < MK_NCT ? t / U : 0, unit = U < MK_NCT ? t % U : t;
-        ab = bar_or(ab);                                        // every thread has its x registers
-        for (int i = t; i < H; i += MK_NCT) s.xv[i] = 0.f;     // xv is free now: combine buffer
-        ab = bar_or(ab);
-        float dacc[2][8];
-#pragma unroll
-        for (int mu = 0; mu < 2; ++mu)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dacc[mu][e] = 0.f;
-        for (int j0 = 0; j0 < pl.nj; j0 += g.JD) {
-            const int n = min(g.JD, pl.nj - j0);
-            const uint8_t* tile;
-            bool ok = !ab && take_tile(p, s, ring, (uint32_t)(n * H * 2), tile);
-            if (ok) {
-                for (int jj = jg; jj < n; jj += JG) {
-                    const float uj = s.u[j0 + jj];
-#pragma unroll
-                    for (int mu = 0; mu < 2; ++mu) {
-                        if (mu < MU) {
-                            float f[8];
-                            unpack8(lds128(tile + ((size_t)jj * H + (unit + mu * MK_NCT) * 8) * 2), f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) dacc[mu][e] = fmaf(f[e], uj, dacc[mu][e]);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (!ab) release_tile(p, s, ring);
-            if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
-        }
-        ab = bar_or(ab);
+        // down projection: this CTA's FFN columns, all H rows (split-K).  Thread t
+        // owns 4-row units t, t + 512, ... of the output and runs over every
+        // column j of the slice: a D tile is [j][H] bf16, so lane-consecutive
+        // units read consecutive 8-byte chunks.
+        ab = bar_or(ab);                                        // u complete
         float* xf = xa + (size_t)(2 * l + 1) * state;
-        if (JG > 1) {
-            if (!ab)
+        {
+            const int NU = H / 4;
+            float2 da[MK_DOWN_UNITS][2];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) atomicAdd(&s.xv[unit * 8 + e], dacc[0][e]);
-            ab = bar_or(ab);
-            if (!ab)
-                for (int i = t; i < H / 4; i += MK_NCT) {
-                    float4 v = reinterpret_cast<const float4*>(s.xv)[i];
-                    if (c == 0) {
-                        v.x += __ldcg(xo + 4 * i + 0); v.y += __ldcg(xo + 4 * i + 1);
-                        v.z += __ldcg(xo + 4 * i + 2); v.w += __ldcg(xo + 4 * i + 3);
-                    }
-                    atomicAdd(reinterpret_cast<float4*>(xf) + i, v);
-                }
-        } else if (!ab) {
+            for (int mu = 0; mu < MK_DOWN_UNITS; ++mu) da[mu][0] = da[mu][1] = make_float2(0.f, 0.f);
+            for (int j0 = 0; j0 < pl.nj && !ab; j0 += g.JD) {
+                const int n = min(g.JD, pl.nj - j0);
+                const uint8_t* tile;
+                const bool ok = take_tile(p, s, ring, (uint32_t)(n * H * 2), tile);
+                if (ok) {
+                    for (int jj = 0; jj < n; ++jj) {
+                        const float uj = s.u[j0 + jj];
+                        const float2 u2 = make_float2(uj, uj);
 #pragma unroll
-            for (int mu = 0; mu < 2; ++mu) {
-                if (mu < MU) {
-                    const int r = (unit + mu * MK_NCT) * 8;
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float4 v = make_float4(dacc[mu][4 * hh + 0], dacc[mu][4 * hh + 1], dacc[mu][4 * hh + 2],
-                                               dacc[mu][4 * hh + 3]);
-                        if (c == 0) {
-                            v.x += __ldcg(xo + r + 4 * hh + 0); v.y += __ldcg(xo + r + 4 * hh + 1);
-                            v.z += __ldcg(xo + r + 4 * hh + 2); v.w += __ldcg(xo + r + 4 * hh + 3);
+                        for (int mu = 0; mu < MK_DOWN_UNITS; ++mu) {
+                            const int unit = t + mu * MK_NCT;
+                            if (unit < NU) {
+                                const uint2 w = *reinterpret_cast<const uint2*>(tile + ((size_t)jj * H + unit * 4) * 2);
+                                da[mu][0] = __ffma2_rn(bf2_lo_hi(w.x), u2, da[mu][0]);
+                                da[mu][1] = __ffma2_rn(bf2_lo_hi(w.y), u2, da[mu][1]);
+                            }
                         }
-                        atomicAdd(reinterpret_cast<float4*>(xf + r) + hh, v);
+                    }
+                }
+                release_tile(p, s, ring);
+                if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
+            }
+            if (!ab) {
+#pragma unroll
+                for (int mu = 0; mu < MK_DOWN_UNITS; ++mu) {
+                    const int unit = t + mu * MK_NCT;
+                    if (unit < NU) {
+                        float4 v = make_float4(da[mu][0].x, da[mu][0].y, da[mu][1].x, da[mu][1].y);
+                        if (c == 0) {   // CTA 0 also carries the residual
+                            const float4 r = __ldcg(reinterpret_cast<const float4*>(xo) + unit);
+                            v.x += r.x; v.y += r.y; v.z += r.z; v.w += r.w;
+                        }
+                        red_add_v4(xf + unit * 4, v);
                     }
                 }
             }
