@@ -160,6 +160,15 @@ struct Smem {
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + (slot_)] = gtimer();           \
     } while (0)
 
+// Per-phase consumer ring-wait (trace only): slot 1024 + 8*layer + phase.
+#define MK_TRACE_CWAIT(slot_)                                                            \
+    do {                                                                                  \
+        if (p.trace && threadIdx.x == 0) {                                                \
+            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + (slot_)] = s.misc->cwait; \
+            s.misc->cwait = 0;                                                            \
+        }                                                                                 \
+    } while (0)
+
 // ------------------------------------------------------------------ waits
 
 __device__ bool wait_counter(const MkParams& p, const uint32_t* ctr, uint32_t target) {
@@ -603,6 +612,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 1);
         ab = gemv_phase(p, s, ring, s.xv, H, 2 * pl.npairs, g.TRh, ab, [&](int r, float v) { s.rows[r] = v; });
         MK_TRACE(16 * l + 2);
+        MK_TRACE_CWAIT(8 * l + 0);
         if (!ab) {
             for (int j = t; j < pl.npairs; j += MK_NCT) {
                 const int pair = pl.pair0 + j, slot = pair / hd2, d = pair % hd2;
@@ -694,6 +704,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         }
         ab = bar_or(ab);
         MK_TRACE(16 * l + 5);
+        MK_TRACE_CWAIT(8 * l + 1);
         if (t == 0 && !ab) arrive(p, mk_cnt_B(g, l, pl.g), 4 * l + 1);
         ab = sync_wait(p, mk_cnt_B(g, l, pl.g), (uint32_t)g.CPG, ab);
         MK_TRACE(16 * l + 6);
@@ -756,6 +767,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             atomicAdd(xo + row, v);
         });
         MK_TRACE(16 * l + 8);
+        MK_TRACE_CWAIT(8 * l + 2);
         if (t == 0 && !ab) arrive(p, mk_cnt_C(g, l), 4 * l + 2);
         ab = sync_wait(p, mk_cnt_C(g, l), (uint32_t)g.nC, ab);
         MK_TRACE(16 * l + 9);
@@ -778,6 +790,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
         }
         MK_TRACE(16 * l + 11);
+        MK_TRACE_CWAIT(8 * l + 3);
         // down projection: this CTA's FFN columns, all H rows (split-K).  Thread t
         // owns 4-row units t, t + 512, ... of the output and runs over every
         // column j of the slice: a D tile is [j][H] bf16, so lane-consecutive
@@ -828,13 +841,10 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         }
         ab = bar_or(ab);
         MK_TRACE(16 * l + 12);
+        MK_TRACE_CWAIT(8 * l + 4);
         if (t == 0 && !ab) arrive(p, mk_cnt_E(g, l), 4 * l + 3);
         ab = sync_wait(p, mk_cnt_E(g, l), (uint32_t)g.nC, ab);
         MK_TRACE(16 * l + 13);
-        if (p.trace && t == 0) {
-            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + l] = s.misc->cwait;
-            s.misc->cwait = 0;
-        }
     }
 
     // ---------------- final RMSNorm + LM head + argmax
@@ -857,7 +867,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
         });
         MK_TRACE(16 * L + 1);
-        if (p.trace && t == 0) p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + L] = s.misc->cwait;
+        MK_TRACE_CWAIT(8 * L + 5);
         if (nonfinite) atomicOr(p.status, MK_ST_NUMERIC);
         if ((t & 31) == 0) { s.misc->best_val[t >> 5] = bv; s.misc->best_idx[t >> 5] = bi; }
         ab = bar_or(ab);

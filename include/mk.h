@@ -192,7 +192,8 @@ int mk_get_info(const mk_ctx* ctx, mk_info* out);
  * 2 QKV GEMV, 3 RoPE/KV append, 4 q/k/v flag seen, 5 attention partials,
  * 6 partials flag seen, 7 combine, 8 O-proj, 9 attention-block flag seen,
  * 10 RMSNorm, 11 gate/up, 12 down, 13 FFN-block flag seen; slot 16*L + 0
- * final RMSNorm, +1 LM head, +2 end, +3 start; slot 1024 + layer: ns the
+ * final RMSNorm, +1 LM head, +2 end, +3 start; slot 1024 + 8*layer + phase
+ * (0 QKV, 1 attention, 2 O-proj, 3 gate/up, 4 down; 8*L + 5 LM head): ns the
  * consumers waited for ring data; slot 1536 + k/16: cumulative ns the copy
  * producer waited for a free slot after its k-th tile; slot 1535: producer done. */
 #define MK_DBG_TRACE 3
