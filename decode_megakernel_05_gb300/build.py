@@ -21,8 +21,9 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmk.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["mk_api.cu", "mk_aux.cu", "mk_perop.cu"]
-# (head_dim, query heads per KV group) pairs of the fused kernel, one object each
-VARIANTS = [(64, 1), (64, 2), (64, 4), (64, 8), (128, 2), (128, 4), (128, 8)]
+# (head_dim, query heads per KV group, hidden / 256) of the fused kernel, one
+# object each; keep in sync with MK_VARIANTS in csrc/mk_api.cu
+VARIANTS = [(64, 2, 1), (64, 4, 2), (64, 4, 4), (64, 4, 8), (64, 4, 16), (128, 4, 4), (128, 4, 8), (128, 4, 16)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -55,8 +56,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
                     "-I", INCLUDE, "-I", CSRC]
     jobs = [(src, os.path.join(BUILD, src.replace(".cu", ".o")), []) for src in SOURCES]
-    for hd, g in VARIANTS:
-        jobs.append(("mk_kernel.cu", os.path.join(BUILD, f"mk_kernel_{hd}_{g}.o"), [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}"]))
+    for hd, g, mh in VARIANTS:
+        jobs.append(("mk_kernel.cu", os.path.join(BUILD, f"mk_kernel_{hd}_{g}_{mh}.o"),
+                     [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}", f"-DMK_MH_V={mh}"]))
 
     def compile_one(job):
         src, obj, defs = job

@@ -14,15 +14,18 @@
 #include "mk_internal.h"
 #include "mk_perop.h"
 
-// One object per kernel variant (mk_kernel.cu compiled with -DMK_HD_V -DMK_G_V).
-#define MK_VARIANTS(X) X(64, 1) X(64, 2) X(64, 4) X(64, 8) X(128, 2) X(128, 4) X(128, 8)
-#define MK_DECL(hd, g) extern "C" const void* mk_kernel_ptr_##hd##_##g(void);
+// One object per kernel variant: mk_kernel.cu compiled with -DMK_HD_V=<head_dim>
+// -DMK_G_V=<q heads per kv head> -DMK_MH_V=<hidden / 256>; keep in sync with
+// VARIANTS in build.py.
+#define MK_VARIANTS(X) \
+    X(64, 2, 1) X(64, 4, 2) X(64, 4, 4) X(64, 4, 8) X(64, 4, 16) X(128, 4, 4) X(128, 4, 8) X(128, 4, 16)
+#define MK_DECL(hd, g, mh) extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh(void);
 MK_VARIANTS(MK_DECL)
 #undef MK_DECL
 
-static int mk_kernel_variant(int hd, int G, const void** fn) {
-#define MK_PICK(hd_, g_) \
-    if (hd == hd_ && G == g_) { *fn = mk_kernel_ptr_##hd_##_##g_(); return 0; }
+static int mk_kernel_variant(int hd, int G, int H, const void** fn) {
+#define MK_PICK(hd_, g_, mh_) \
+    if (hd == hd_ && G == g_ && H == 256 * mh_) { *fn = mk_kernel_ptr_##hd_##_##g_##_##mh_(); return 0; }
     MK_VARIANTS(MK_PICK)
 #undef MK_PICK
     *fn = nullptr;
@@ -66,8 +69,9 @@ Tune resolve_tuning(const mk_tuning* t) {
     return r;
 }
 
-// Shape checks shared by mk_create and the host layout utilities.
-int check_shape(const mk_config* c) {
+// Shape checks shared by mk_create and the host layout utilities; the fused
+// kernel must also be built for the shape when need_kernel is set.
+int check_shape(const mk_config* c, bool need_kernel = true) {
     if (!c) return MK_ERR_INVALID_ARG;
     if (c->n_layers < 1 || c->hidden < 8 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 2 ||
         c->ffn < 1 || c->vocab < 1 || c->max_seq < 1 || !(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f))
@@ -76,7 +80,7 @@ int check_shape(const mk_config* c) {
     if (c->head_dim != 64 && c->head_dim != 128) return MK_ERR_UNSUPPORTED;
     const int G = c->n_q_heads / c->n_kv_heads;
     const void* fn = nullptr;
-    if (mk_kernel_variant(c->head_dim, G, &fn) != 0) return MK_ERR_UNSUPPORTED;
+    if (need_kernel && mk_kernel_variant(c->head_dim, G, c->hidden, &fn) != 0) return MK_ERR_UNSUPPORTED;
     auto pow2_ok = [](int K) {   // K/8 divides 512 or is a multiple of 512
         if (K % 8) return false;
         const int n = K / 8;
@@ -331,7 +335,7 @@ const char* mk_strerror(int code) {
 const char* mk_last_cuda_error(void) { return g_cuda_err.c_str(); }
 
 int64_t mk_arena_bytes(const mk_config* cfg, const mk_tuning* tuning, int32_t grid_ctas) {
-    if (check_shape(cfg) != MK_OK || grid_ctas < 1) return -1;
+    if (check_shape(cfg, false) != MK_OK || grid_ctas < 1) return -1;
     Tune tu = resolve_tuning(tuning);
     MkGeom g;
     if (build_geom(cfg, tu, grid_ctas, 1, g) != MK_OK) return -1;
@@ -343,7 +347,7 @@ int64_t mk_arena_bytes(const mk_config* cfg, const mk_tuning* tuning, int32_t gr
 
 int mk_relayout_host(const mk_config* cfg, const mk_tuning* tuning, int32_t grid_ctas, const mk_weights* w,
                      void* arena_out) {
-    int rc = check_shape(cfg);
+    int rc = check_shape(cfg, false);
     if (rc != MK_OK) return rc;
     if (!w || !arena_out || grid_ctas < 1 || w->on_device) return MK_ERR_INVALID_ARG;
     if (!cfg->tie_embeddings && !w->lm_head) return MK_ERR_INVALID_ARG;
@@ -407,7 +411,7 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         if ((rc = build_geom(cfg, c->tune, grid, ns, g)) != MK_OK) return fail(rc);
         if (g.smem_bytes + 1024 <= smem_optin) { c->geo = g; break; }
     }
-    mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, &c->kernel);
+    mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, &c->kernel);
     if ((e = cudaFuncSetAttribute(c->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, c->geo.smem_bytes)) !=
         cudaSuccess)
         return fail(cuda_fail(e, "cudaFuncSetAttribute"));

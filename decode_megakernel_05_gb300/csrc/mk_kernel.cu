@@ -1,16 +1,16 @@
 // mk_kernel.cu - one instantiation of the decode megakernel per translation
 // unit: the build compiles this file once for every (head_dim, query heads per
-// KV group) pair it supports, with -DMK_HD_V=<hd> -DMK_G_V=<G>, so the
-// variants compile in parallel.
+// KV group, hidden/256) triple it supports, with -DMK_HD_V=<hd> -DMK_G_V=<G>
+// -DMK_MH_V=<H/256>, so the variants compile in parallel.
 #include "mk_kernel.cuh"
 
-#if !defined(MK_HD_V) || !defined(MK_G_V)
-#error "compile with -DMK_HD_V=<head_dim> -DMK_G_V=<q heads per kv head>"
+#if !defined(MK_HD_V) || !defined(MK_G_V) || !defined(MK_MH_V)
+#error "compile with -DMK_HD_V=<head_dim> -DMK_G_V=<q heads per kv head> -DMK_MH_V=<hidden/256>"
 #endif
 
-#define MK_CAT2(a, b, c) a##b##_##c
-#define MK_CAT(a, b, c) MK_CAT2(a, b, c)
+#define MK_CAT2(a, b, c, d) a##b##_##c##_##d
+#define MK_CAT(a, b, c, d) MK_CAT2(a, b, c, d)
 
-extern "C" const void* MK_CAT(mk_kernel_ptr_, MK_HD_V, MK_G_V)(void) {
-    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V>;
+extern "C" const void* MK_CAT(mk_kernel_ptr_, MK_HD_V, MK_G_V, MK_MH_V)(void) {
+    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V>;
 }

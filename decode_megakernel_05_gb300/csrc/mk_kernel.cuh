@@ -56,12 +56,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
 }
+// Waits (suspended, up to a hint of 20 us per call) for the phase of the
+// given parity to complete; returns false when the hint ran out first.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
         : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
+        : "r"(smem_u32(b)), "r"(parity), "r"(20000u)
         : "memory");
     return ok != 0;
 }
@@ -385,21 +387,6 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
     return bar_or(ab);
 }
 
-// Dispatch on MR = K / (8 * LPR) (powers of two up to 32).
-template <class Epi>
-__device__ __forceinline__ bool gemv_phase(const MkParams& p, const Smem& s, Ring& ring, const float* vec, int K,
-                                           int nrows, int TR, bool ab, Epi&& epi) {
-    const int LPR = (K / 8) < 32 ? (K / 8) : 32;
-    switch (K / (8 * LPR)) {
-        case 1: return gemv_phase_t<1>(p, s, ring, vec, K, nrows, TR, ab, epi);
-        case 2: return gemv_phase_t<2>(p, s, ring, vec, K, nrows, TR, ab, epi);
-        case 4: return gemv_phase_t<4>(p, s, ring, vec, K, nrows, TR, ab, epi);
-        case 8: return gemv_phase_t<8>(p, s, ring, vec, K, nrows, TR, ab, epi);
-        case 16: return gemv_phase_t<16>(p, s, ring, vec, K, nrows, TR, ab, epi);
-        default: return gemv_phase_t<32>(p, s, ring, vec, K, nrows, TR, ab, epi);
-    }
-}
-
 // RMSNorm of x (fp32 global, or the bf16 embedding row when xb != nullptr) into
 // s.xv, with gain g (fp32).  Returns the uniform abort flag.
 __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, const uint16_t* xb, const float* g,
@@ -529,8 +516,13 @@ struct Attn {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int HD, int G>
+// HD: head_dim; G: query heads per KV head; MH = H / 256, the 8-column chunks
+// each lane owns in a row of H (the GEMV width of QKV, gate/up and LM head).
+template <int HD, int G, int MH>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
+    constexpr int KO = G * HD;                         // O-proj row length
+    constexpr int LPRO = (KO / 8) < 32 ? (KO / 8) : 32;
+    constexpr int MO = KO / (8 * LPRO);
     extern __shared__ __align__(1024) uint8_t smem[];
     const MkGeom& g = p.geo;
     Smem s;
@@ -610,7 +602,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
         ab = rmsnorm_to_xv(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab);
         MK_TRACE(16 * l + 1);
-        ab = gemv_phase(p, s, ring, s.xv, H, 2 * pl.npairs, g.TRh, ab, [&](int r, float v) { s.rows[r] = v; });
+        ab = gemv_phase_t<MH>(p, s, ring, s.xv, H, 2 * pl.npairs, g.TRh, ab, [&](int r, float v) { s.rows[r] = v; });
         MK_TRACE(16 * l + 2);
         MK_TRACE_CWAIT(8 * l + 0);
         if (!ab) {
@@ -761,7 +753,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
         // O-proj (rows of this CTA, columns of this group) + residual, atomically
         float* xo = xa + (size_t)(2 * l) * state;
-        ab = gemv_phase(p, s, ring, s.ov, G * HD, pl.norows, g.TRo, ab, [&](int r, float v) {
+        ab = gemv_phase_t<MO>(p, s, ring, s.ov, G * HD, pl.norows, g.TRo, ab, [&](int r, float v) {
             const int row = pl.orow0 + r;
             if (pl.g == 0) v += (l == 0) ? bf2f(emb[row]) : __ldcg(xin + row);
             atomicAdd(xo + row, v);
@@ -778,7 +770,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
             const int JT = g.JT;
-            ab = gemv_phase(p, s, ring, s.xv, H, 2 * pl.nj, 2 * JT, ab, [&](int r, float v) {
+            ab = gemv_phase_t<MH>(p, s, ring, s.xv, H, 2 * pl.nj, 2 * JT, ab, [&](int r, float v) {
                 const int q = r / (2 * JT), rr = r % (2 * JT);
                 const int n = min(JT, pl.nj - q * JT);
                 if (rr < n) s.gs[q * JT + rr] = v;
@@ -857,7 +849,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         float bv = -INFINITY;
         int bi = -1;
         bool nonfinite = false;
-        ab = gemv_phase(p, s, ring, s.xv, H, pl.nv, g.TRh, ab, [&](int r, float lg) {
+        ab = gemv_phase_t<MH>(p, s, ring, s.xv, H, pl.nv, g.TRh, ab, [&](int r, float lg) {
             const int v = pl.v0 + r;
             if (p.logits) p.logits[v] = lg;
             if (isfinite(lg)) {
