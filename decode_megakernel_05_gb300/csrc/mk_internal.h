@@ -76,7 +76,8 @@ struct MkGeom {
     int32_t max_rows, max_nj;    // per-CTA maxima (QKV rows, FFN slice)
     int32_t smem_bytes;
     // shared-memory carve-up (byte offsets from the dynamic smem base)
-    int32_t off_full, off_empty, off_xv, off_ov, off_acc, off_rows, off_u, off_gs, off_red, off_sc, off_misc;
+    int32_t off_full, off_empty, off_xv, off_ov, off_acc, off_rows, off_u, off_gs, off_xres, off_xres2, off_rope,
+        off_red, off_sc, off_misc;
 };
 
 // Fills everything but smem offsets from the shape; returns false if the
@@ -114,6 +115,9 @@ MK_HD int mk_smem_layout(MkGeom& g) {
     g.off_rows = o; o += 4 * ((g.max_rows + 3) & ~3);
     g.off_u = o; o += 4 * ((g.max_nj + 3) & ~3);
     g.off_gs = o; o += 4 * ((g.max_nj + 3) & ~3);
+    g.off_xres = o; o += 4 * ((g.H / g.CPG + 4) & ~3);
+    g.off_xres2 = o; o += 4 * ((g.H / g.nC + 4) & ~3);
+    g.off_rope = o; o += 4 * g.hd;
     g.off_red = o; o += 4 * 2 * MK_NCT;       // double-buffered row partials
     g.off_sc = o; o += 4 * g.G * (g.KB + 4);  // attention scores of one KV block (+ the current position)
     g.off_misc = o; o += MK_MISC_BYTES;       // softmax state, staging, flags
@@ -160,7 +164,7 @@ struct MkParams {
     // producer ring-wait ns per layer at 1536 + l.
     unsigned long long* trace;
 };
-#define MK_TRACE_STRIDE 2048
+#define MK_TRACE_STRIDE 4096
 #define MK_TRACE_MAX_LAYERS 63
 
 MK_HD int mk_cnt_A(const MkGeom& g, int l, int grp) { return l * g.kvh + grp; }

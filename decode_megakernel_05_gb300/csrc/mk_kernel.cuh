@@ -149,6 +149,9 @@ struct Smem {
     float* rows;  // [max_rows]
     float* u;     // [max_nj] up rows, then SiLU(gate)*up
     float* gs;    // [max_nj] gate rows
+    float* xres;  // raw residual of this CTA's O rows (group 0 only)
+    float* xres2; // raw residual of rows split(H, nC, c)
+    float* rope;  // cos[hd/2], sin[hd/2] at this position
     float* red;   // [2][512]
     float* sc;    // [G][KB]
     Misc* misc;
@@ -352,7 +355,7 @@ __device__ __forceinline__ void dot_rows2(const uint8_t* r0, const uint8_t* r1, 
 
 template <int MR, class Epi>
 __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec, int K,
-                                             int nrows, int TR, bool ab, Epi&& epi) {
+                                             int nrows, int TR, bool ab, Epi&& epi, int trace_slot = -1) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int LPR = (K / 8) < 32 ? (K / 8) : 32;
     const int RPP = 32 / LPR, sub = lane / LPR, ll = lane % LPR;
@@ -366,6 +369,8 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
         const int R = min(TR, nrows - ti * TR);
         const uint8_t* tile;
         const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
+        if (trace_slot >= 0 && p.trace && threadIdx.x == 0 && ti < 256)
+            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
         if (ok && (ti % ngrp) == grp) {
             for (int base = wg * rows_per_warp; base < R; base += wpg * rows_per_warp) {
                 const int r0 = base + sub, r1 = base + RPP + sub;
@@ -388,14 +393,17 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
 }
 
 // RMSNorm of x (fp32 global, or the bf16 embedding row when xb != nullptr) into
-// s.xv, with gain g (fp32).  Returns the uniform abort flag.
+// s.xv, with gain g (fp32).  The raw values of rows [keep0, keep0 + nkeep) are
+// also kept in `keep` (the residual this CTA adds later).  Returns the uniform
+// abort flag.
 __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, const uint16_t* xb, const float* g,
-                              bool abort_in) {
+                              bool abort_in, float* keep, int keep0, int nkeep) {
     const int H = p.geo.H, t = threadIdx.x;
     float ss = 0.f;
     for (int i = t; i < H; i += MK_NCT) {
         float v = xb ? bf2f(xb[i]) : __ldcg(x + i);
         s.xv[i] = v;
+        if ((unsigned)(i - keep0) < (unsigned)nkeep) keep[i - keep0] = v;
         ss = fmaf(v, v, ss);
     }
 #pragma unroll
@@ -535,6 +543,9 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     s.rows = reinterpret_cast<float*>(smem + g.off_rows);
     s.u = reinterpret_cast<float*>(smem + g.off_u);
     s.gs = reinterpret_cast<float*>(smem + g.off_gs);
+    s.xres = reinterpret_cast<float*>(smem + g.off_xres);
+    s.xres2 = reinterpret_cast<float*>(smem + g.off_xres2);
+    s.rope = reinterpret_cast<float*>(smem + g.off_rope);
     s.red = reinterpret_cast<float*>(smem + g.off_red);
     s.sc = reinterpret_cast<float*>(smem + g.off_sc);
     s.misc = reinterpret_cast<Misc*>(smem + g.off_misc);
@@ -590,6 +601,11 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     const int ka = (int)mk_split(ctx, g.CPG, pl.i), kb_ = (int)mk_split(ctx, g.CPG, pl.i + 1);
     const int ke = kb_ < p.pos ? kb_ : p.pos;
     const bool has_cur = (pl.i == g.CPG - 1);
+    const int dr0 = (int)mk_split(H, g.nC, c), dr1 = (int)mk_split(H, g.nC, c + 1);   // rows whose residual I add
+    for (int d = t; d < hd2; d += MK_NCT) {       // RoPE angles of this position
+        s.rope[d] = p.rope_cos[(size_t)p.pos * hd2 + d];
+        s.rope[hd2 + d] = p.rope_sin[(size_t)p.pos * hd2 + d];
+    }
     const float qscale = rsqrtf((float)HD) * 1.4426950408889634f;  // 1/sqrt(hd) * log2(e)
 
     Ring ring;
@@ -600,7 +616,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment A: RMSNorm + QKV GEMV + RoPE + K/V append
         MK_TRACE(16 * l + 0);
         const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
-        ab = rmsnorm_to_xv(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab);
+        ab = rmsnorm_to_xv(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres, pl.orow0,
+                           pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
         ab = gemv_phase_t<MH>(p, s, ring, s.xv, H, 2 * pl.npairs, g.TRh, ab, [&](int r, float v) { s.rows[r] = v; });
         MK_TRACE(16 * l + 2);
@@ -610,7 +627,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 const int pair = pl.pair0 + j, slot = pair / hd2, d = pair % hd2;
                 float a = s.rows[2 * j], b = s.rows[2 * j + 1];
                 if (slot <= G) {
-                    const float cs = p.rope_cos[(size_t)p.pos * hd2 + d], sn = p.rope_sin[(size_t)p.pos * hd2 + d];
+                    const float cs = s.rope[d], sn = s.rope[hd2 + d];
                     const float a2 = a * cs - b * sn, b2 = b * cs + a * sn;
                     a = a2; b = b2;
                 }
@@ -754,9 +771,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // O-proj (rows of this CTA, columns of this group) + residual, atomically
         float* xo = xa + (size_t)(2 * l) * state;
         ab = gemv_phase_t<MO>(p, s, ring, s.ov, G * HD, pl.norows, g.TRo, ab, [&](int r, float v) {
-            const int row = pl.orow0 + r;
-            if (pl.g == 0) v += (l == 0) ? bf2f(emb[row]) : __ldcg(xin + row);
-            atomicAdd(xo + row, v);
+            if (pl.g == 0) v += s.xres[r];   // group 0 carries the residual of these rows
+            atomicAdd(xo + pl.orow0 + r, v);
         });
         MK_TRACE(16 * l + 8);
         MK_TRACE_CWAIT(8 * l + 2);
@@ -765,7 +781,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 9);
 
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
-        ab = rmsnorm_to_xv(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab);
+        ab = rmsnorm_to_xv(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2, dr0, dr1 - dr0);
         MK_TRACE(16 * l + 10);
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
@@ -822,9 +838,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     const int unit = t + mu * MK_NCT;
                     if (unit < NU) {
                         float4 v = make_float4(da[mu][0].x, da[mu][0].y, da[mu][1].x, da[mu][1].y);
-                        if (c == 0) {   // CTA 0 also carries the residual
-                            const float4 r = __ldcg(reinterpret_cast<const float4*>(xo) + unit);
-                            v.x += r.x; v.y += r.y; v.z += r.z; v.w += r.w;
+                        // each CTA carries the residual of its own rows [dr0, dr1)
+                        const int r4 = unit * 4 - dr0;
+                        if ((unsigned)(r4 + 3) < (unsigned)(dr1 - dr0 + 3)) {
+                            if ((unsigned)(r4 + 0) < (unsigned)(dr1 - dr0)) v.x += s.xres2[r4 + 0];
+                            if ((unsigned)(r4 + 1) < (unsigned)(dr1 - dr0)) v.y += s.xres2[r4 + 1];
+                            if ((unsigned)(r4 + 2) < (unsigned)(dr1 - dr0)) v.z += s.xres2[r4 + 2];
+                            if ((unsigned)(r4 + 3) < (unsigned)(dr1 - dr0)) v.w += s.xres2[r4 + 3];
                         }
                         red_add_v4(xf + unit * 4, v);
                     }
@@ -842,7 +862,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     // ---------------- final RMSNorm + LM head + argmax
     {
         const float* xl = xa + (size_t)(2 * L - 1) * state;
-        ab = rmsnorm_to_xv(p, s, xl, nullptr, p.final_norm, ab);
+        ab = rmsnorm_to_xv(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0);
         MK_TRACE(16 * L + 0);
         if (c == 0 && !ab)
             for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv[i];
@@ -857,7 +877,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             } else {
                 nonfinite = true;
             }
-        });
+        }, 2048);
         MK_TRACE(16 * L + 1);
         MK_TRACE_CWAIT(8 * L + 5);
         if (nonfinite) atomicOr(p.status, MK_ST_NUMERIC);

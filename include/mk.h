@@ -186,7 +186,7 @@ int mk_get_info(const mk_ctx* ctx, mk_info* out);
  * (default 1e9 ns). */
 #define MK_DBG_SKIP_ARRIVAL 1
 #define MK_DBG_WAIT_LIMIT_NS 2
-/* MK_DBG_TRACE: value = device address of a uint64 buffer [grid_ctas][2048]
+/* MK_DBG_TRACE: value = device address of a uint64 buffer [grid_ctas][4096]
  * (0 = off).  Each step then records per CTA the %globaltimer (ns) at the end
  * of every segment: slot 16*layer + e for e = 0 layer start, 1 RMSNorm,
  * 2 QKV GEMV, 3 RoPE/KV append, 4 q/k/v flag seen, 5 attention partials,
@@ -195,7 +195,8 @@ int mk_get_info(const mk_ctx* ctx, mk_info* out);
  * final RMSNorm, +1 LM head, +2 end, +3 start; slot 1024 + 8*layer + phase
  * (0 QKV, 1 attention, 2 O-proj, 3 gate/up, 4 down; 8*L + 5 LM head): ns the
  * consumers waited for ring data; slot 1536 + k/16: cumulative ns the copy
- * producer waited for a free slot after its k-th tile; slot 1535: producer done. */
+ * producer waited for a free slot after its k-th tile; slot 1535: producer done;
+ * slot 2048 + k (k < 256): thread 0 got LM-head tile k. */
 #define MK_DBG_TRACE 3
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
