@@ -37,6 +37,7 @@
 #define MK_MAX_CPG_G 640               // CTAs per group x query heads per group (combine weights)
 #define MK_COMBINE_LOADS 8            // float4 loads per thread in the attention combine
 #define MK_MISC_BYTES 6656
+#define MK_MAX_H 8192                 // largest hidden size the kernels take
 #define MK_DOWN_UNITS 4               // 4-row units per consumer thread in the down projection (H <= 8192)
 
 // Device status word bits.

@@ -316,41 +316,49 @@ __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, R
 //
 // A tile holds up to TR rows of K bf16 (row-major).  LPR = min(32, K/8) lanes
 // share a row, each owning MR = K/(8*LPR) chunks of 8 consecutive columns
-// (chunk j of lane ll covers columns (j*LPR + ll)*8 ..); a warp works on 2
-// rows at a time, so every activation chunk read from shared memory feeds two
-// rows.  When a tile needs fewer than 16 warps the consumer warps form groups
-// that take alternate tiles; otherwise every warp works on every tile.  A row
-// is reduced inside its LPR lanes and its first lane hands the sum to epi().
-// Every warp waits for every tile and arrives on its empty barrier (the
-// barrier's arrival count stays 16), but only the tile's group reads it.
+// (chunk j of lane ll covers columns (j*LPR + ll)*8 ..).  The activation
+// vector sits in shared memory in "split" order (xsplit): the first 4 values
+// of every 8-column chunk c at [4c, 4c+4), the last 4 at [K/2 + 4c, ...), so
+// a warp's 16-byte reads of one half are consecutive and bank-conflict free.
+// A warp works on 4 rows at a time, so every activation chunk read from shared
+// memory feeds 4 rows.  When a tile needs fewer than 16 warps the consumer
+// warps form groups that take alternate tiles; otherwise every warp works on
+// every tile.  A row is reduced inside its LPR lanes and its first lane hands
+// the sum to epi().  Every warp waits for every tile and arrives on its empty
+// barrier (the barrier's arrival count stays 16), but only the tile's group
+// reads it.
+__device__ __forceinline__ int xsplit(int i, int K) { return ((i >> 3) << 2) + (i & 3) + ((i & 4) ? (K >> 1) : 0); }
+
 __device__ __forceinline__ float2 bf2_lo_hi(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+__device__ __forceinline__ void fma_chunk(const uint4 w, const float4 xl, const float4 xh, float2& a0, float2& a1) {
+    a0 = __ffma2_rn(bf2_lo_hi(w.x), make_float2(xl.x, xl.y), a0);
+    a1 = __ffma2_rn(bf2_lo_hi(w.y), make_float2(xl.z, xl.w), a1);
+    a0 = __ffma2_rn(bf2_lo_hi(w.z), make_float2(xh.x, xh.y), a0);
+    a1 = __ffma2_rn(bf2_lo_hi(w.w), make_float2(xh.z, xh.w), a1);
+}
+
+// Dot products of up to 4 rows (nv valid) with the split-order vector xs.
 template <int MR>
-__device__ __forceinline__ void dot_rows2(const uint8_t* r0, const uint8_t* r1, bool two, const float* xs, int LPR,
-                                          int ll, float& o0, float& o1) {
-    float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
+__device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t rb, int nv, const float* xs, int K, int LPR,
+                                          int ll, float o[4]) {
+    float2 a[4][2];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a[r][0] = a[r][1] = make_float2(0.f, 0.f);
+    const float4* xlo = reinterpret_cast<const float4*>(xs);
+    const float4* xhi = reinterpret_cast<const float4*>(xs + (K >> 1));
 #pragma unroll (MR < 8 ? MR : 8)
     for (int j = 0; j < MR; ++j) {
         const int ch = j * LPR + ll;
-        const float4 xa = reinterpret_cast<const float4*>(xs)[ch * 2];
-        const float4 xb = reinterpret_cast<const float4*>(xs)[ch * 2 + 1];
-        const uint4 w = lds128(r0 + (size_t)ch * 16);
-        a0 = __ffma2_rn(bf2_lo_hi(w.x), make_float2(xa.x, xa.y), a0);
-        a1 = __ffma2_rn(bf2_lo_hi(w.y), make_float2(xa.z, xa.w), a1);
-        a0 = __ffma2_rn(bf2_lo_hi(w.z), make_float2(xb.x, xb.y), a0);
-        a1 = __ffma2_rn(bf2_lo_hi(w.w), make_float2(xb.z, xb.w), a1);
-        if (two) {
-            const uint4 v = lds128(r1 + (size_t)ch * 16);
-            b0 = __ffma2_rn(bf2_lo_hi(v.x), make_float2(xa.x, xa.y), b0);
-            b1 = __ffma2_rn(bf2_lo_hi(v.y), make_float2(xa.z, xa.w), b1);
-            b0 = __ffma2_rn(bf2_lo_hi(v.z), make_float2(xb.x, xb.y), b0);
-            b1 = __ffma2_rn(bf2_lo_hi(v.w), make_float2(xb.z, xb.w), b1);
-        }
+        const float4 xl = xlo[ch], xh = xhi[ch];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            if (r < nv) fma_chunk(lds128(r0 + r * rb + (size_t)ch * 16), xl, xh, a[r][0], a[r][1]);
     }
-    o0 = (a0.x + a0.y) + (a1.x + a1.y);
-    o1 = (b0.x + b0.y) + (b1.x + b1.y);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) o[r] = (a[r][0].x + a[r][0].y) + (a[r][1].x + a[r][1].y);
 }
 
 template <int MR, class Epi>
@@ -359,7 +367,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int LPR = (K / 8) < 32 ? (K / 8) : 32;
     const int RPP = 32 / LPR, sub = lane / LPR, ll = lane % LPR;
-    const int rows_per_warp = 2 * RPP;                         // rows a warp covers per pass
+    const int rows_per_warp = 4 * RPP;                          // rows a warp covers per pass
     int wpg = (TR + rows_per_warp - 1) / rows_per_warp;         // warps one tile needs
     wpg = wpg >= MK_NCW ? MK_NCW : (wpg > 8 ? MK_NCW : wpg > 4 ? 8 : wpg > 2 ? 4 : wpg);
     const int ngrp = MK_NCW / wpg, grp = w / wpg, wg = w % wpg;
@@ -373,16 +381,18 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
         if (ok && (ti % ngrp) == grp) {
             for (int base = wg * rows_per_warp; base < R; base += wpg * rows_per_warp) {
-                const int r0 = base + sub, r1 = base + RPP + sub;
-                float v0 = 0.f, v1 = 0.f;
-                if (r0 < R) dot_rows2<MR>(tile + r0 * rb, tile + r1 * rb, r1 < R, vec, LPR, ll, v0, v1);
-                for (int o = LPR >> 1; o >= 1; o >>= 1) {
-                    v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, o);
-                    v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, o);
-                }
+                // this lane's rows: base + sub + k*RPP, k < 4
+                const int r0 = base + sub;
+                const int nv = r0 < R ? min(4, (R - r0 + RPP - 1) / RPP) : 0;
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (nv > 0) dot_rows4<MR>(tile + r0 * rb, rb * RPP, nv, vec, K, LPR, ll, v);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    for (int o = LPR >> 1; o >= 1; o >>= 1) v[k] += __shfl_xor_sync(0xFFFFFFFFu, v[k], o);
                 if (ll == 0) {
-                    if (r0 < R) epi(ti * TR + r0, v0);
-                    if (r1 < R) epi(ti * TR + r1, v1);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (k < nv) epi(ti * TR + r0 + k * RPP, v[k]);
                 }
             }
         }
@@ -396,6 +406,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
 // s.xv, with gain g (fp32).  The raw values of rows [keep0, keep0 + nkeep) are
 // also kept in `keep` (the residual this CTA adds later).  Returns the uniform
 // abort flag.
+template <int NPT>   // ceil(H / 512) values per thread
 __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, const uint16_t* xb, const float* g,
                               bool abort_in, float* keep, int keep0, int nkeep) {
     const int H = p.geo.H, t = threadIdx.x;
@@ -414,7 +425,18 @@ __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, 
 #pragma unroll
     for (int w = 0; w < MK_NCW; ++w) tot += s.red[w];
     const float inv = rsqrtf(tot / (float)H + p.eps);
-    for (int i = t; i < H; i += MK_NCT) s.xv[i] = s.xv[i] * inv * g[i];
+    float nv[NPT];
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) {
+        const int i = t + k * MK_NCT;
+        if (i < H) nv[k] = s.xv[i] * inv * g[i];
+    }
+    ab = bar_or(ab);   // everyone has read the raw values before they are overwritten
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) {
+        const int i = t + k * MK_NCT;
+        if (i < H) s.xv[xsplit(i, H)] = nv[k];   // split order for the GEMV
+    }
     return bar_or(ab);
 }
 
@@ -616,7 +638,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment A: RMSNorm + QKV GEMV + RoPE + K/V append
         MK_TRACE(16 * l + 0);
         const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
-        ab = rmsnorm_to_xv(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres, pl.orow0,
+        ab = rmsnorm_to_xv<(MH + 1) / 2>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres, pl.orow0,
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
         ab = gemv_phase_t<MH>(p, s, ring, s.xv, H, 2 * pl.npairs, g.TRh, ab, [&](int r, float v) { s.rows[r] = v; });
@@ -758,7 +780,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     if (i < n4) {
                         const int jh = i / (HD / 4), d4 = i % (HD / 4), h = jh % G;
                         const float wt = s.misc->cwt[jh] * s.misc->alpha[h];
-                        float* o = s.ov + h * HD + d4 * 4;
+                        const int i0 = h * HD + d4 * 4;     // 4 consecutive values: one split half
+                        float* o = s.ov + xsplit(i0, G * HD);
                         atomicAdd(o + 0, wt * v[k].x); atomicAdd(o + 1, wt * v[k].y);
                         atomicAdd(o + 2, wt * v[k].z); atomicAdd(o + 3, wt * v[k].w);
                     }
@@ -781,7 +804,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 9);
 
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
-        ab = rmsnorm_to_xv(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2, dr0, dr1 - dr0);
+        ab = rmsnorm_to_xv<(MH + 1) / 2>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2, dr0, dr1 - dr0);
         MK_TRACE(16 * l + 10);
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
@@ -862,10 +885,10 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     // ---------------- final RMSNorm + LM head + argmax
     {
         const float* xl = xa + (size_t)(2 * L - 1) * state;
-        ab = rmsnorm_to_xv(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0);
+        ab = rmsnorm_to_xv<(MH + 1) / 2>(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0);
         MK_TRACE(16 * L + 0);
         if (c == 0 && !ab)
-            for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv[i];
+            for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv[xsplit(i, H)];
         float bv = -INFINITY;
         int bi = -1;
         bool nonfinite = false;
