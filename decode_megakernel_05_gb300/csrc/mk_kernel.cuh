@@ -53,8 +53,8 @@ __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+__device__ __forceinline__ void mbar_arrive(uint64_t* b, uint32_t count = 1) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
 }
 // Waits (suspended, up to a hint of 20 us per call) for the phase of the
 // given parity to complete; returns false when the hint ran out first.
@@ -133,6 +133,7 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     float best_val[64];
     int best_idx[64];
     uint32_t tile_bytes[16]; // bytes of the tile in each ring slot (schedule check)
+    int slot_tile[16];       // index (in the step's tile stream) of the tile each slot holds
     float cwt[MK_MAX_CPG_G]; // attention-combine weights [CPG][G]
     float cl[MK_MAX_CPG_G];  // attention partial sums l [CPG][G]
     uint4 stage[32];         // K and V rows of the current position (2 * hd bf16)
@@ -238,6 +239,7 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
             if ((k & 15u) == 0 && 1536 + (k >> 4) < MK_TRACE_STRIDE) tr[1536 + (k >> 4)] = pwait;
         }
         s.misc->tile_bytes[slot] = bytes;
+        *(volatile int*)&s.misc->slot_tile[slot] = (int)k;
         mbar_expect_tx(&s.full[slot], bytes);
         bulk_g2s(s.ring + (size_t)slot * slot_bytes, src, bytes, &s.full[slot]);
         ++k;
@@ -286,7 +288,13 @@ struct Ring {
     __device__ __forceinline__ uint32_t slot(int ns) const { return k % ns; }
 };
 
-// Waits for the ring slot of tile k (warp-cooperative; lane 0 polls).
+// Ring protocol.  Tile k of the step's stream lives in slot k % ns.  A warp
+// that reads tile k first waits until the producer has claimed the slot for
+// tile k (slot_tile), then for the slot's full barrier (the parity is then
+// unambiguous even if the warp skipped earlier tiles), reads it, and arrives
+// on the slot's empty barrier with weight 16 / (number of warps reading the
+// tile), so the barrier completes exactly when every reader is done.  Warps
+// that do not read a tile only advance their cursor.
 __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t expect_bytes,
                                           const uint8_t*& tile) {
     const int ns = p.geo.ns;
@@ -294,7 +302,21 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {
         const uint64_t tw = (p.trace && threadIdx.x == 0) ? gtimer() : 0;
-        ok = !s.misc->abort && wait_mbar(p, &s.full[slot], ph, &s.misc->abort);
+        ok = !s.misc->abort;
+        if (ok && *(volatile int*)&s.misc->slot_tile[slot] != (int)rg.k) {
+            const uint64_t t0 = gtimer();
+            while (*(volatile int*)&s.misc->slot_tile[slot] != (int)rg.k) {
+                if (s.misc->abort) { ok = false; break; }
+                if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) {
+                    atomicOr(p.status, MK_ST_TIMEOUT | MK_ST_ABORT);
+                    s.misc->abort = 1;
+                    ok = false;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        ok = ok && wait_mbar(p, &s.full[slot], ph, &s.misc->abort);
         if (tw) s.misc->cwait += gtimer() - tw;
         if (ok && s.misc->tile_bytes[slot] != expect_bytes) {
             atomicOr(p.status, MK_ST_SCHEDULE | MK_ST_ABORT);
@@ -306,9 +328,10 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     tile = s.ring + (size_t)slot * p.geo.slot;
     return ok;
 }
-__device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, Ring& rg) {
+// Done reading tile k; `weight` = 16 / (warps reading it).  Advances the cursor.
+__device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t weight = 1) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[rg.k % p.geo.ns]);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[rg.k % p.geo.ns], weight);
     ++rg.k;
 }
 
@@ -374,12 +397,13 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
     const int ntiles = (nrows + TR - 1) / TR;
     const size_t rb = (size_t)K * 2;
     for (int ti = 0; ti < ntiles && !ab; ++ti) {
+        if ((ti % ngrp) != grp) { ++ring.k; continue; }   // another group's tile
         const int R = min(TR, nrows - ti * TR);
         const uint8_t* tile;
         const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
         if (trace_slot >= 0 && p.trace && threadIdx.x == 0 && ti < 256)
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
-        if (ok && (ti % ngrp) == grp) {
+        if (ok) {
             for (int base = wg * rows_per_warp; base < R; base += wpg * rows_per_warp) {
                 // this lane's rows: base + sub + k*RPP, k < 4
                 const int r0 = base + sub;
@@ -396,7 +420,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                 }
             }
         }
-        release_tile(p, s, ring);
+        release_tile(p, s, ring, (uint32_t)(MK_NCW / wpg));
         if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
     }
     return bar_or(ab);
@@ -580,6 +604,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         for (int i = 0; i < g.ns; ++i) {
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], MK_NCW);
+            s.misc->slot_tile[i] = -1;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s.misc->abort = 0;
