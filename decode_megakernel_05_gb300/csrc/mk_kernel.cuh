@@ -240,6 +240,7 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
         }
         s.misc->tile_bytes[slot] = bytes;
         *(volatile int*)&s.misc->slot_tile[slot] = (int)k;
+        if (tr && k < 512) tr[2560 + k] = gtimer();   // trace: issue time of tile k
         mbar_expect_tx(&s.full[slot], bytes);
         bulk_g2s(s.ring + (size_t)slot * slot_bytes, src, bytes, &s.full[slot]);
         ++k;
@@ -326,12 +327,17 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     }
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     tile = s.ring + (size_t)slot * p.geo.slot;
+    if (p.trace && (threadIdx.x & 31) == 0 && rg.k < 512)   // trace: a reader got tile k
+        p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3072 + rg.k] = gtimer();
     return ok;
 }
 // Done reading tile k; `weight` = 16 / (warps reading it).  Advances the cursor.
 __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t weight = 1) {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&s.empty[rg.k % p.geo.ns], weight);
+    if ((threadIdx.x & 31) == 0) {
+        mbar_arrive(&s.empty[rg.k % p.geo.ns], weight);
+        if (p.trace && rg.k < 512) p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3584 + rg.k] = gtimer();
+    }
     ++rg.k;
 }
 

@@ -196,7 +196,9 @@ int mk_get_info(const mk_ctx* ctx, mk_info* out);
  * (0 QKV, 1 attention, 2 O-proj, 3 gate/up, 4 down; 8*L + 5 LM head): ns the
  * consumers waited for ring data; slot 1536 + k/16: cumulative ns the copy
  * producer waited for a free slot after its k-th tile; slot 1535: producer done;
- * slot 2048 + k (k < 256): thread 0 got LM-head tile k. */
+ * slot 2048 + k (k < 256): thread 0 got LM-head tile k; for the first 512
+ * tiles of the step's stream: 2560 + k issue time, 3072 + k time a reader got
+ * it, 3584 + k time a reader released it. */
 #define MK_DBG_TRACE 3
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
