@@ -260,8 +260,13 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
     }
 }
 
+// L2 prefetch walker (the whole prefetch warp): walks the same tile stream as
+// the copy producer and asks L2 for each tile's 128-byte lines with per-lane
+// prefetches (load/store path, so the bulk-copy queue is not held up), staying
+// at most l2_pf_bytes ahead of the copies.
 __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const Smem& s) {
     if (p.l2_pf_bytes <= 0) return;
+    const int lane = threadIdx.x & 31;
     volatile int* abort = &s.misc->abort;
     const unsigned long long ahead = (unsigned long long)p.l2_pf_bytes;
     unsigned long long issued = 0;
@@ -269,14 +274,22 @@ __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const 
     walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
         if (stop) return;
         uint64_t t0 = 0;
-        while (issued > *(volatile unsigned long long*)&s.misc->copy_bytes + ahead) {
+        for (;;) {
+            const unsigned long long cb = *(volatile unsigned long long*)&s.misc->copy_bytes;
+            if (issued <= cb + ahead) {
+                // tiles the copy producer has already issued need no prefetch
+                if (issued + bytes > cb) {
+                    const char* b = reinterpret_cast<const char*>(src);
+                    for (uint32_t off = (uint32_t)lane * 128u; off < bytes; off += 32u * 128u)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(b + off));
+                }
+                break;
+            }
             if (*abort) { stop = true; return; }
             if (t0 == 0) t0 = gtimer();
             else if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) { stop = true; return; }
             __nanosleep(256);
         }
-        // tiles the copy producer has already issued need no prefetch
-        if (issued + bytes > *(volatile unsigned long long*)&s.misc->copy_bytes) prefetch_l2(src, bytes);
         issued += bytes;
     });
 }
@@ -634,7 +647,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         return;
     }
     if (warp == MK_PREFETCH_WARP) {
-        if ((t & 31) == 0) producer_prefetch(p, pl, s);
+        producer_prefetch(p, pl, s);
         return;
     }
 
