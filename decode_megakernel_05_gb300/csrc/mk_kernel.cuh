@@ -67,11 +67,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
+// Bulk copy global -> shared completing on an mbarrier.  The L2 policy marks
+// the lines evict-first: every byte streamed here is read once per step, so
+// consumed lines should leave L2 before lines prefetched for later tiles.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -225,6 +234,7 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
     volatile int* abort = &s.misc->abort;
     const int ns = p.geo.ns;
     const uint32_t slot_bytes = (uint32_t)p.geo.slot;
+    const uint64_t pol = l2_evict_first_policy();
     uint32_t k = 0;
     bool stop = false;
     unsigned long long pwait = 0;
@@ -242,7 +252,7 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
         *(volatile int*)&s.misc->slot_tile[slot] = (int)k;
         if (tr && k < 512) tr[2560 + k] = gtimer();   // trace: issue time of tile k
         mbar_expect_tx(&s.full[slot], bytes);
-        bulk_g2s(s.ring + (size_t)slot * slot_bytes, src, bytes, &s.full[slot]);
+        bulk_g2s(s.ring + (size_t)slot * slot_bytes, src, bytes, &s.full[slot], pol);
         ++k;
         *(volatile unsigned long long*)&s.misc->copy_bytes += bytes;
     });
