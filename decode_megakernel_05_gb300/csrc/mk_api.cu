@@ -81,12 +81,15 @@ int check_shape(const mk_config* c, bool need_kernel = true) {
     const int G = c->n_q_heads / c->n_kv_heads;
     const void* fn = nullptr;
     if (need_kernel && mk_kernel_variant(c->head_dim, G, c->hidden, &fn) != 0) return MK_ERR_UNSUPPORTED;
-    auto pow2_ok = [](int K) {   // K/8 divides 512 or is a multiple of 512
+    // GEMV row length K: 8-column chunks spread over min(32, K/8) lanes, so
+    // K/8 divides 32 (short rows) or K is a multiple of 256 (long rows).
+    auto width_ok = [](int K) {
         if (K % 8) return false;
         const int n = K / 8;
-        return (n <= MK_NCT) ? (MK_NCT % n == 0) : (n % MK_NCT == 0 && n / MK_NCT <= 2);
+        return n < 32 ? (32 % n == 0) : (K % 256 == 0);
     };
-    if (!pow2_ok(c->hidden) || !pow2_ok(G * c->head_dim) || c->hidden < 256) return MK_ERR_UNSUPPORTED;
+    if (!width_ok(c->hidden) || !width_ok(G * c->head_dim) || c->hidden < 256 || c->hidden > MK_MAX_H)
+        return MK_ERR_UNSUPPORTED;
     return MK_OK;
 }
 

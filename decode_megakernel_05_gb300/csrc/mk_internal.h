@@ -28,17 +28,17 @@
 #pragma once
 #include <stdint.h>
 
-#define MK_NCW 16                    // consumer warps
+#define MK_NCW 12                    // consumer warps
 #define MK_NCT (MK_NCW * 32)         // consumer threads
 #define MK_PRODUCER_WARP MK_NCW      // bulk-copy producer
 #define MK_PREFETCH_WARP (MK_NCW + 1)// L2 prefetch walker
-#define MK_BLOCK ((MK_NCW + 2) * 32) // 576 threads
+#define MK_BLOCK ((MK_NCW + 2) * 32) // 448 threads: at most 4 warps per SM sub-partition (128 registers)
 
 #define MK_MAX_CPG_G 640               // CTAs per group x query heads per group (combine weights)
 #define MK_COMBINE_LOADS 8            // float4 loads per thread in the attention combine
 #define MK_MISC_BYTES 6656
 #define MK_MAX_H 8192                 // largest hidden size the kernels take
-#define MK_DOWN_UNITS 4               // 4-row units per consumer thread in the down projection (H <= 8192)
+#define MK_DOWN_UNITS ((MK_MAX_H / 4 + MK_NCT - 1) / MK_NCT)   // 4-row units per thread in the down projection
 
 // Device status word bits.
 #define MK_ST_TIMEOUT 0x1u

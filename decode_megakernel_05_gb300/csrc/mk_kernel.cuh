@@ -2,7 +2,7 @@
 // mk_kernel.cuh - the persistent bs=1 decode megakernel (one launch per token).
 //
 // One CTA per SM (grid = n_kv_heads * floor(SMs / n_kv_heads)).  Each CTA has
-//   - 16 consumer warps that run the segments of every layer,
+//   - MK_NCW (12) consumer warps that run the segments of every layer,
 //   - a producer warp that streams the CTA's pre-laid-out weight tiles (and its
 //     share of the KV cache) into a ring of shared-memory slots with bulk
 //     asynchronous copies, guarded by full/empty mbarriers, so tile k+1..k+S
@@ -98,7 +98,7 @@ __device__ __forceinline__ void red_add_v4(float* p, float4 v) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
 }
-// Barrier over the 512 consumer threads that also ORs a per-thread flag: every
+// Barrier over the consumer threads that also ORs a per-thread flag: every
 // participant gets the same answer, so an abort decision is uniform.
 __device__ __forceinline__ bool bar_or(bool f) {
     uint32_t r;
@@ -162,7 +162,7 @@ struct Smem {
     float* xres;  // raw residual of this CTA's O rows (group 0 only)
     float* xres2; // raw residual of rows split(H, nC, c)
     float* rope;  // cos[hd/2], sin[hd/2] at this position
-    float* red;   // [2][512]
+    float* red;   // [2][MK_NCT]
     float* sc;    // [G][KB]
     Misc* misc;
 };
@@ -316,8 +316,8 @@ struct Ring {
 // that reads tile k first waits until the producer has claimed the slot for
 // tile k (slot_tile), then for the slot's full barrier (the parity is then
 // unambiguous even if the warp skipped earlier tiles), reads it, and arrives
-// on the slot's empty barrier with weight 16 / (number of warps reading the
-// tile), so the barrier completes exactly when every reader is done.  Warps
+// on the slot's empty barrier with weight MK_NCW / (number of warps reading
+// the tile), so the barrier completes exactly when every reader is done.  Warps
 // that do not read a tile only advance their cursor.
 __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t expect_bytes,
                                           const uint8_t*& tile) {
@@ -354,7 +354,7 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
         p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3072 + rg.k] = gtimer();
     return ok;
 }
-// Done reading tile k; `weight` = 16 / (warps reading it).  Advances the cursor.
+// Done reading tile k; `weight` = MK_NCW / (warps reading it).  Advances the cursor.
 __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t weight = 1) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
@@ -373,12 +373,21 @@ __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, R
 // of every 8-column chunk c at [4c, 4c+4), the last 4 at [K/2 + 4c, ...), so
 // a warp's 16-byte reads of one half are consecutive and bank-conflict free.
 // A warp works on 4 rows at a time, so every activation chunk read from shared
-// memory feeds 4 rows.  When a tile needs fewer than 16 warps the consumer
+// memory feeds 4 rows.  When a tile needs fewer than MK_NCW warps the consumer
 // warps form groups that take alternate tiles; otherwise every warp works on
 // every tile.  A row is reduced inside its LPR lanes and its first lane hands
 // the sum to epi().  Every warp waits for every tile and arrives on its empty
-// barrier (the barrier's arrival count stays 16), but only the tile's group
+// barrier (total weight MK_NCW per tile), but only the tile's group
 // reads it.
+// Smallest divisor of the consumer warp count that is >= need (warps that
+// share a tile; a divisor, so every tile's readers arrive with equal weights).
+__device__ __forceinline__ int group_size(int need) {
+#pragma unroll
+    for (int d = 1; d < MK_NCW; ++d)
+        if (MK_NCW % d == 0 && d >= need) return d;
+    return MK_NCW;
+}
+
 __device__ __forceinline__ int xsplit(int i, int K) { return ((i >> 3) << 2) + (i & 3) + ((i & 4) ? (K >> 1) : 0); }
 
 __device__ __forceinline__ float2 bf2_lo_hi(uint32_t w) {
@@ -420,8 +429,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
     const int LPR = (K / 8) < 32 ? (K / 8) : 32;
     const int RPP = 32 / LPR, sub = lane / LPR, ll = lane % LPR;
     const int rows_per_warp = 4 * RPP;                          // rows a warp covers per pass
-    int wpg = (TR + rows_per_warp - 1) / rows_per_warp;         // warps one tile needs
-    wpg = wpg >= MK_NCW ? MK_NCW : (wpg > 8 ? MK_NCW : wpg > 4 ? 8 : wpg > 2 ? 4 : wpg);
+    const int wpg = group_size((TR + rows_per_warp - 1) / rows_per_warp);   // warps per tile
     const int ngrp = MK_NCW / wpg, grp = w / wpg, wg = w % wpg;
     const int ntiles = (nrows + TR - 1) / TR;
     const size_t rb = (size_t)K * 2;
@@ -459,7 +467,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
 // s.xv, with gain g (fp32).  The raw values of rows [keep0, keep0 + nkeep) are
 // also kept in `keep` (the residual this CTA adds later).  Returns the uniform
 // abort flag.
-template <int NPT>   // ceil(H / 512) values per thread
+template <int NPT>   // ceil(H / consumer threads) values per thread
 __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, const uint16_t* xb, const float* g,
                               bool abort_in, float* keep, int keep0, int nkeep) {
     const int H = p.geo.H, t = threadIdx.x;
@@ -661,7 +669,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         return;
     }
 
-    // ======================= consumers (512 threads) =======================
+    // ======================= consumers (MK_NCT threads) =======================
     const int H = g.H, L = g.L, hd2 = HD / 2;
     const int par = s.misc->par, token = s.misc->token;
     const size_t state = (size_t)H;
@@ -692,7 +700,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment A: RMSNorm + QKV GEMV + RoPE + K/V append
         MK_TRACE(16 * l + 0);
         const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
-        ab = rmsnorm_to_xv<(MH + 1) / 2>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres, pl.orow0,
+        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres, pl.orow0,
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
         ab = gemv_phase_t<MH>(p, s, ring, s.xv, H, 2 * pl.npairs, g.TRh, ab, [&](int r, float v) { s.rows[r] = v; });
@@ -858,7 +866,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 9);
 
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
-        ab = rmsnorm_to_xv<(MH + 1) / 2>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2, dr0, dr1 - dr0);
+        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2, dr0, dr1 - dr0);
         MK_TRACE(16 * l + 10);
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
@@ -939,7 +947,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     // ---------------- final RMSNorm + LM head + argmax
     {
         const float* xl = xa + (size_t)(2 * L - 1) * state;
-        ab = rmsnorm_to_xv<(MH + 1) / 2>(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0);
+        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0);
         MK_TRACE(16 * L + 0);
         if (c == 0 && !ab)
             for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv[xsplit(i, H)];
