@@ -44,7 +44,7 @@ def test_host_only_entry_points():
     assert mk.mk_arena_bytes(odd, None, 152) == -1
     ragged = mk.mk_config(2, 3000, 24, 8, 128, 8192, 1024, 80, 1e-5, 1e4, 0)   # 3000 is not a multiple of 256
     assert mk.mk_arena_bytes(ragged, None, 152) == -1
-    wide = mk.mk_config(2, 3072, 24, 8, 128, 8192, 1024, 80, 1e-5, 1e4, 0)     # layout fine; no kernel variant
+    wide = mk.mk_config(2, 3072, 32, 8, 128, 8192, 1024, 80, 1e-5, 1e4, 0)     # layout fine; no kernel variant
     assert mk.mk_arena_bytes(wide, None, 152) > 0
 
 
