@@ -401,10 +401,11 @@ __device__ __forceinline__ void fma_chunk(const uint4 w, const float4 xl, const 
     a1 = __ffma2_rn(bf2_lo_hi(w.w), make_float2(xh.z, xh.w), a1);
 }
 
-// Dot products of up to 4 rows (nv valid) with the split-order vector xs.
-template <int MR>
-__device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t rb, int nv, const float* xs, int K, int LPR,
-                                          int ll, float o[4]) {
+// Dot products of up to 4 rows (nv valid, rows r0 + k*step) with the
+// split-order vector xs; each lane covers MR chunks of 8 columns.
+template <int MR, int LPR>
+__device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t step, int nv, const float* xs, int K, int ll,
+                                          float o[4]) {
     float2 a[4][2];
 #pragma unroll
     for (int r = 0; r < 4; ++r) a[r][0] = a[r][1] = make_float2(0.f, 0.f);
@@ -416,22 +417,36 @@ __device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t rb, int nv, 
         const float4 xl = xlo[ch], xh = xhi[ch];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-            if (r < nv) fma_chunk(lds128(r0 + r * rb + (size_t)ch * 16), xl, xh, a[r][0], a[r][1]);
+            if (r < nv) fma_chunk(lds128(r0 + r * step + (size_t)ch * 16), xl, xh, a[r][0], a[r][1]);
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) o[r] = (a[r][0].x + a[r][0].y) + (a[r][1].x + a[r][1].y);
 }
 
-template <int MR, class Epi>
-__device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec, int K,
+// GEMV over one phase's tiles (rows of K = MR * 8 * LPR columns, LPR lanes per
+// row, RPP = 32 / LPR rows side by side in a warp).  A warp handles rw rows
+// per lane group and pass (rw in {1, 2, 4}): with many tiles rw = 4 (each
+// activation chunk feeds 4 rows: least shared-memory traffic), with few tiles
+// rw shrinks so more warps share a tile and the phase ends sooner.
+template <int MR, int LPR, class Epi>
+__device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec,
                                              int nrows, int TR, bool ab, Epi&& epi, int trace_slot = -1) {
+    constexpr int K = MR * 8 * LPR;
+    constexpr int RPP = 32 / LPR;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int LPR = (K / 8) < 32 ? (K / 8) : 32;
-    const int RPP = 32 / LPR, sub = lane / LPR, ll = lane % LPR;
-    const int rows_per_warp = 4 * RPP;                          // rows a warp covers per pass
-    const int wpg = group_size((TR + rows_per_warp - 1) / rows_per_warp);   // warps per tile
-    const int ngrp = MK_NCW / wpg, grp = w / wpg, wg = w % wpg;
+    const int sub = lane / LPR, ll = lane % LPR;
     const int ntiles = (nrows + TR - 1) / TR;
+    // rows per lane group: the largest of 4, 2, 1 that still lets every tile
+    // of a short phase run at once (or 4 when the phase has many tiles)
+    int rw = 4, wpg = group_size((TR + 4 * RPP - 1) / (4 * RPP));
+    if (ntiles < MK_NCW / wpg) {
+        for (int cand = 1; cand <= 4; cand <<= 1) {
+            const int wp = group_size((TR + cand * RPP - 1) / (cand * RPP));
+            if (MK_NCW / wp >= ntiles) { rw = cand; wpg = wp; break; }
+        }
+    }
+    const int rows_per_warp = rw * RPP;
+    const int ngrp = MK_NCW / wpg, grp = w / wpg, wg = w % wpg;
     const size_t rb = (size_t)K * 2;
     for (int ti = 0; ti < ntiles && !ab; ++ti) {
         if ((ti % ngrp) != grp) { ++ring.k; continue; }   // another group's tile
@@ -442,14 +457,18 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
         if (ok) {
             for (int base = wg * rows_per_warp; base < R; base += wpg * rows_per_warp) {
-                // this lane's rows: base + sub + k*RPP, k < 4
+                // this lane group's rows: base + sub + k*RPP, k < rw
                 const int r0 = base + sub;
-                const int nv = r0 < R ? min(4, (R - r0 + RPP - 1) / RPP) : 0;
+                const int nv = r0 < R ? min(rw, (R - r0 + RPP - 1) / RPP) : 0;
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
-                if (nv > 0) dot_rows4<MR>(tile + r0 * rb, rb * RPP, nv, vec, K, LPR, ll, v);
+                if (nv > 0) dot_rows4<MR, LPR>(tile + r0 * rb, rb * RPP, nv, vec, K, ll, v);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    for (int o = LPR >> 1; o >= 1; o >>= 1) v[k] += __shfl_xor_sync(0xFFFFFFFFu, v[k], o);
+                for (int k = 0; k < 4; ++k) {
+                    if (k < rw) {
+#pragma unroll
+                        for (int o = LPR >> 1; o >= 1; o >>= 1) v[k] += __shfl_xor_sync(0xFFFFFFFFu, v[k], o);
+                    }
+                }
                 if (ll == 0) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -510,97 +529,78 @@ __device__ __forceinline__ bool sync_wait(const MkParams& p, int idx, uint32_t t
 
 // ------------------------------------------------------------------ attention
 
+// Split-K decode attention for one CTA's share of positions.  Lane layout:
+// TPP = G*HD/8 consecutive threads cover one position, thread (h, dc) owning
+// head h and dims [8dc, 8dc+8) of that position; NCT/TPP positions are
+// processed side by side.  Scores: 8-dim partial dots reduced over the HD/8
+// lanes of a head.  Softmax is online (exp2, running max per head, rescaled
+// sums).  V: each thread accumulates its head's 8 dims over its positions, and
+// the position groups are summed with shared-memory atomics at the end.
 template <int HD, int G>
 struct Attn {
-    static constexpr int LP = HD / 8;            // lanes per position (8 dims each)
-    static constexpr int PPP = MK_NCT / LP;      // positions per pass
+    static constexpr int DC = HD / 8;                // lanes per head
+    static constexpr int TPP = G * DC;               // threads per position
+    static constexpr int PPP = MK_NCT / TPP;         // positions per pass
+    static_assert(MK_NCT % TPP == 0 && (DC & (DC - 1)) == 0 && DC <= 32, "attention lane layout");
 
-    // One K/V block of n positions at kt / vt (bf16 [n][HD]); updates the
-    // running max / sum in smem and the accumulators in registers.
-    // Positions q < nr come from the ring tile kt, position nr (when n > nr)
-    // from the staged row st.
-    static __device__ __forceinline__ bool block(const Smem& s, const uint8_t* kt, int nr, const uint8_t* st, int n,
-                                                 const float qr[G][8], int KB, bool abort_in, const MkParams& p,
-                                                 Ring* ring, bool from_ring, bool& ok_k) {
-        const int t = threadIdx.x, pl = t / LP, dc = t % LP;
-        if (ok_k) {
-            // warp-uniform trip count: every lane runs every shuffle
-            for (int q0 = 0; q0 < n; q0 += PPP) {
-                const int q = q0 + pl;
-                const bool valid = q < n;
+    // Scores of positions [0, n): q < nr from the ring tile kt, q == nr from
+    // the staged row st.  qr: this thread's 8 query dims (scaled by log2(e)/sqrt(hd)).
+    static __device__ __forceinline__ void scores(const Smem& s, const uint8_t* kt, int nr, const uint8_t* st, int n,
+                                                  const float qr[8], int SC) {
+        const int t = threadIdx.x, pp = t / TPP, h = (t % TPP) / DC, dc = t % DC;
+        for (int q0 = 0; q0 < n; q0 += PPP) {          // uniform trip count across the warp
+            const int q = q0 + pp;
+            float a = 0.f;
+            if (q < n) {
                 float f[8];
-                if (valid) unpack8(lds128((q < nr ? kt + (size_t)q * HD * 2 : st) + dc * 16), f);
-                else {
+                unpack8(lds128((q < nr ? kt + (size_t)q * HD * 2 : st) + dc * 16), f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = 0.f;
-                }
-                float sh[G];
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float a = f[0] * qr[h][0];
-#pragma unroll
-                    for (int e = 1; e < 8; ++e) a = fmaf(f[e], qr[h][e], a);
-                    sh[h] = a;
-                }
-#pragma unroll
-                for (int o = LP / 2; o >= 1; o >>= 1)
-#pragma unroll
-                    for (int h = 0; h < G; ++h) sh[h] += __shfl_xor_sync(0xFFFFFFFFu, sh[h], o);
-                if (dc == 0 && valid)
-#pragma unroll
-                    for (int h = 0; h < G; ++h) s.sc[h * KB + q] = sh[h];
+                for (int e = 0; e < 8; ++e) a = fmaf(f[e], qr[e], a);
             }
+#pragma unroll
+            for (int o = DC / 2; o >= 1; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            if (dc == 0 && q < n) s.sc[h * SC + q] = a;
         }
-        // the loop above has a data-dependent trip count, so re-converge before shuffles elsewhere
-        __syncwarp();
-        if (from_ring) release_tile(p, s, *ring);
-        bool ab = bar_or(abort_in || !ok_k);
-        const int w = t >> 5, lane = t & 31;
-        if (w < G && !ab) {
-            const int h = w;
-            float mx = -INFINITY;
-            for (int q = lane; q < n; q += 32) mx = fmaxf(mx, s.sc[h * KB + q]);
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-            const float mold = s.misc->mrun[h];
-            const float mn = fmaxf(mold, mx);
-            const float alpha = (mold == -INFINITY) ? 0.f : exp2f(mold - mn);
-            float sum = 0.f;
-            for (int q = lane; q < n; q += 32) {
-                float e = exp2f(s.sc[h * KB + q] - mn);
-                s.sc[h * KB + q] = e;
-                sum += e;
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-            if (lane == 0) {
-                s.misc->lrun[h] = s.misc->lrun[h] * alpha + sum;
-                s.misc->mrun[h] = mn;
-                s.misc->alpha[h] = alpha;
-            }
-        }
-        ab = bar_or(ab);
-        return ab;
     }
-    static __device__ __forceinline__ void accumulate_v(const Smem& s, const uint8_t* vt, int nr, const uint8_t* stv,
-                                                        int n, float acc[G][8], int KB, bool ok) {
-        const int t = threadIdx.x, pl = t / LP, dc = t % LP;
-        if (!ok) return;
+    // Online-softmax update of head h = warp (warps < G), over n scores.
+    static __device__ __forceinline__ void softmax_update(const Smem& s, int n, int SC) {
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (w >= G) return;
+        const int h = w;
+        float mx = -INFINITY;
+        for (int q = lane; q < n; q += 32) mx = fmaxf(mx, s.sc[h * SC + q]);
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float a = s.misc->alpha[h];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] *= a;
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        const float mold = s.misc->mrun[h];
+        const float mn = fmaxf(mold, mx);
+        const float alpha = (mold == -INFINITY) ? 0.f : exp2f(mold - mn);
+        float sum = 0.f;
+        for (int q = lane; q < n; q += 32) {
+            const float e = exp2f(s.sc[h * SC + q] - mn);
+            s.sc[h * SC + q] = e;
+            sum += e;
         }
-        for (int q = pl; q < n; q += PPP) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        if (lane == 0) {
+            s.misc->lrun[h] = s.misc->lrun[h] * alpha + sum;
+            s.misc->mrun[h] = mn;
+            s.misc->alpha[h] = alpha;
+        }
+    }
+    // acc <- acc * alpha_h + sum_q p[h][q] V[q][8dc..]
+    static __device__ __forceinline__ void accumulate_v(const Smem& s, const uint8_t* vt, int nr, const uint8_t* stv,
+                                                        int n, float acc[8], int SC) {
+        const int t = threadIdx.x, pp = t / TPP, h = (t % TPP) / DC, dc = t % DC;
+        const float al = s.misc->alpha[h];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= al;
+        for (int q = pp; q < n; q += PPP) {
             float f[8];
             unpack8(lds128((q < nr ? vt + (size_t)q * HD * 2 : stv) + dc * 16), f);
+            const float wgt = s.sc[h * SC + q];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float wgt = s.sc[h * KB + q];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(wgt, f[e], acc[h][e]);
-            }
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wgt, f[e], acc[e]);
         }
     }
 };
@@ -612,8 +612,9 @@ struct Attn {
 template <int HD, int G, int MH>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
     constexpr int KO = G * HD;                         // O-proj row length
-    constexpr int LPRO = (KO / 8) < 32 ? (KO / 8) : 32;
+    constexpr int LPRO = KO >= 32 * 4 ? KO / 32 : 4;   // short rows: 4 chunks per lane
     constexpr int MO = KO / (8 * LPRO);
+    static_assert(LPRO <= 32 && 32 % LPRO == 0 && MO * 8 * LPRO == KO, "O-proj row mapping");
     extern __shared__ __align__(1024) uint8_t smem[];
     const MkGeom& g = p.geo;
     Smem s;
@@ -703,7 +704,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres, pl.orow0,
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
-        ab = gemv_phase_t<MH>(p, s, ring, s.xv, H, 2 * pl.npairs, g.TRh, ab, [&](int r, float v) { s.rows[r] = v; });
+        ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv, 2 * pl.npairs, g.TRh, ab, [&](int r, float v) { s.rows[r] = v; });
         MK_TRACE(16 * l + 2);
         MK_TRACE_CWAIT(8 * l + 0);
         if (!ab) {
@@ -732,58 +733,56 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 4);
 
         // ---------------- segment B: split-K attention over this CTA's positions
-        if (!ab) {
-            const float* qsrc = p.qbuf + (size_t)l * g.qh * HD + (size_t)pl.g * G * HD;
-            for (int i = t; i < G * HD; i += MK_NCT) { s.ov[i] = __ldcg(qsrc + i) * qscale; s.acc[i] = 0.f; }
-            if (t < G) { s.misc->mrun[t] = -INFINITY; s.misc->lrun[t] = 0.f; }
-            if (has_cur && t < HD / 4) {   // stage K[pos], V[pos] written by this group this launch
-                const size_t off = (((size_t)l * g.kvh + pl.g) * g.max_seq + p.pos) * HD;
-                const uint4* src = reinterpret_cast<const uint4*>((t < HD / 8 ? p.kc : p.vc) + off);
-                s.misc->stage[t] = __ldcg(src + (t % (HD / 8)));
-            }
-        }
-        ab = bar_or(ab);
         {
             using A = Attn<HD, G>;
-            const int pl_ = t / A::LP, dc = t % A::LP;
-            float qr[G][8], acc[G][8];
+            const int h_ = (t % A::TPP) / A::DC, dc_ = t % A::DC;
+            float qr[8], acc[8];
+            if (!ab) {
+                // this thread's 8 query dims straight from L2 (written by the group this launch)
+                const float4* qs = reinterpret_cast<const float4*>(
+                    p.qbuf + (size_t)l * g.qh * HD + ((size_t)pl.g * G + h_) * HD + dc_ * 8);
+                const float4 qa = __ldcg(qs), qb = __ldcg(qs + 1);
+                qr[0] = qa.x * qscale; qr[1] = qa.y * qscale; qr[2] = qa.z * qscale; qr[3] = qa.w * qscale;
+                qr[4] = qb.x * qscale; qr[5] = qb.y * qscale; qr[6] = qb.z * qscale; qr[7] = qb.w * qscale;
+                for (int i = t; i < G * HD; i += MK_NCT) s.acc[i] = 0.f;
+                if (t < G) { s.misc->mrun[t] = -INFINITY; s.misc->lrun[t] = 0.f; }
+                if (has_cur && t < HD / 4) {   // stage K[pos], V[pos] written by this group this launch
+                    const size_t off = (((size_t)l * g.kvh + pl.g) * g.max_seq + p.pos) * HD;
+                    const uint4* src = reinterpret_cast<const uint4*>((t < HD / 8 ? p.kc : p.vc) + off);
+                    s.misc->stage[t] = __ldcg(src + (t % (HD / 8)));
+                }
+            }
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) { qr[h][e] = s.ov[h * HD + dc * 8 + e]; acc[h][e] = 0.f; }
-            (void)pl_;
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+            ab = bar_or(ab);
             // Blocks of up to KB past positions from the ring; the last CTA of the
             // group appends the current position (staged from global) to its
             // last block, or runs it as a block of its own when it has no past.
+            const int SC = g.KB + 4;   // score row stride (room for the current position)
             const int nring = ke > ka ? ke - ka : 0;
             const int nblk = (nring + g.KB - 1) / g.KB;
             const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
             const uint8_t* st = reinterpret_cast<const uint8_t*>(s.misc->stage);
-            for (int b = 0; b < nbt; ++b) {
+            for (int b = 0; b < nbt && !ab; ++b) {
                 const int q0 = ka + b * g.KB;
                 const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
                 const int n = nr + ((has_cur && b == nbt - 1) ? 1 : 0);
                 const uint8_t *kt = st, *vt = st;
-                bool okk = !ab && (nr == 0 || take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt));
-                ab = A::block(s, kt, nr, st, n, qr, g.KB + 4, ab, p, &ring, nr > 0, okk);   // sc stride KB + 4
-                bool okv = !ab && (nr == 0 || take_tile(p, s, ring, (uint32_t)(nr * HD * 2), vt));
-                A::accumulate_v(s, vt, nr, st + HD * 2, n, acc, g.KB + 4, okv);
-                __syncwarp();
+                bool ok = nr == 0 || take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt);
+                if (ok) A::scores(s, kt, nr, st, n, qr, SC);
                 if (nr > 0) release_tile(p, s, ring);
-                ab = bar_or(ab || !okv);
+                ab = bar_or(ab || !ok);
+                if (!ab) A::softmax_update(s, n, SC);
+                ab = bar_or(ab);
+                ok = ab || nr == 0 || take_tile(p, s, ring, (uint32_t)(nr * HD * 2), vt);
+                if (!ab && ok) A::accumulate_v(s, vt, nr, st + HD * 2, n, acc, SC);
+                if (nr > 0) release_tile(p, s, ring);
+                ab = bar_or(ab || !ok);
             }
-            // combine the position lanes: in-warp, then across warps with smem atomics
+            // sum the position groups into s.acc
+            if (!ab && nbt > 0 && t / A::TPP < nbt * g.KB + 1) {
 #pragma unroll
-            for (int o = A::LP; o < 32; o <<= 1)
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[h][e], o);
-            if ((t & 31) < A::LP && !ab) {
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) atomicAdd(&s.acc[h * HD + dc * 8 + e], acc[h][e]);
+                for (int e = 0; e < 8; ++e) atomicAdd(&s.acc[h_ * HD + dc_ * 8 + e], acc[e]);
             }
         }
         ab = bar_or(ab);
@@ -803,10 +802,19 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 6);
 
         // combine the group's partials -> o (the G heads of this KV group):
-        // weights exp2(m_j - M) / sum_j exp2(m_j - M) l_j, then one parallel
-        // pass of float4 loads of the partial accumulators into smem atomics
+        // weights exp2(m_j - M) / sum_j exp2(m_j - M) l_j.  The first batch of
+        // partial-accumulator loads is issued together with the (m, l) loads,
+        // so the combine costs one L2 round trip for short groups.
         if (!ab) {
             const size_t gbase = ((size_t)l * g.kvh + pl.g) * g.CPG * G;
+            const int n4 = g.CPG * G * (HD / 4);
+            const float4* pa = reinterpret_cast<const float4*>(p.part_acc + gbase * HD);
+            float4 v[MK_COMBINE_LOADS];
+#pragma unroll
+            for (int k = 0; k < MK_COMBINE_LOADS; ++k) {
+                const int i = t + k * MK_NCT;
+                v[k] = (i < n4) ? __ldcg(pa + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             float* cw = s.red;                       // [CPG*G] maxima (red is free here)
             for (int i = t; i < g.CPG * G; i += MK_NCT) {
                 cw[i] = __ldcg(p.part_ml + (gbase + i) * 2);
@@ -827,14 +835,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 s.misc->alpha[t] = 1.f / den;
             }
             bar_or(false);
-            const int n4 = g.CPG * G * (HD / 4);
-            const float4* pa = reinterpret_cast<const float4*>(p.part_acc + gbase * HD);
-            for (int base = 0; base < n4; base += MK_COMBINE_LOADS * MK_NCT) {   // batches of independent loads
-                float4 v[MK_COMBINE_LOADS];
+            for (int base = 0; base < n4; base += MK_COMBINE_LOADS * MK_NCT) {
+                if (base > 0) {   // further batches for large groups
 #pragma unroll
-                for (int k = 0; k < MK_COMBINE_LOADS; ++k) {
-                    const int i = base + t + k * MK_NCT;
-                    v[k] = (i < n4) ? __ldcg(pa + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = 0; k < MK_COMBINE_LOADS; ++k) {
+                        const int i = base + t + k * MK_NCT;
+                        v[k] = (i < n4) ? __ldcg(pa + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
 #pragma unroll
                 for (int k = 0; k < MK_COMBINE_LOADS; ++k) {
@@ -855,7 +862,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
         // O-proj (rows of this CTA, columns of this group) + residual, atomically
         float* xo = xa + (size_t)(2 * l) * state;
-        ab = gemv_phase_t<MO>(p, s, ring, s.ov, G * HD, pl.norows, g.TRo, ab, [&](int r, float v) {
+        ab = gemv_phase_t<MO, LPRO>(p, s, ring, s.ov, pl.norows, g.TRo, ab, [&](int r, float v) {
             if (pl.g == 0) v += s.xres[r];   // group 0 carries the residual of these rows
             atomicAdd(xo + pl.orow0 + r, v);
         });
@@ -871,7 +878,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
             const int JT = g.JT;
-            ab = gemv_phase_t<MH>(p, s, ring, s.xv, H, 2 * pl.nj, 2 * JT, ab, [&](int r, float v) {
+            ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv, 2 * pl.nj, 2 * JT, ab, [&](int r, float v) {
                 const int q = r / (2 * JT), rr = r % (2 * JT);
                 const int n = min(JT, pl.nj - q * JT);
                 if (rr < n) s.gs[q * JT + rr] = v;
@@ -954,7 +961,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         float bv = -INFINITY;
         int bi = -1;
         bool nonfinite = false;
-        ab = gemv_phase_t<MH>(p, s, ring, s.xv, H, pl.nv, g.TRh, ab, [&](int r, float lg) {
+        ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv, pl.nv, g.TRh, ab, [&](int r, float lg) {
             const int v = pl.v0 + r;
             if (p.logits) p.logits[v] = lg;
             if (isfinite(lg)) {
