@@ -28,6 +28,8 @@ MK_ERR_UNSUPPORTED = -7
 MK_DBG_SKIP_ARRIVAL = 1
 MK_DBG_WAIT_LIMIT_NS = 2
 MK_DBG_TRACE = 3
+MK_NOALLOC_ARGMAX_BLOCKS = 1024
+MK_NOALLOC_ARGMAX_MAX_N = MK_NOALLOC_ARGMAX_BLOCKS * 4096
 
 _i32, _i64, _f32, _P = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -70,6 +72,7 @@ SIGNATURES = [
     ("mk_enable_perop", _i32, [_P, _i32]),
     ("mk_decode_step_perop", _i32, [_P, _i32, _i32, _P, _P, ctypes.POINTER(_i32)]),
     ("mk_get_info", _i32, [_P, ctypes.POINTER(mk_info)]),
+    ("mk_argmax_f32_noalloc", _i32, [_P, _i32, _P, _P]),
     ("mk_set_debug", _i32, [_P, _i32, _i64]),
     ("mk_strerror", ctypes.c_char_p, [ctypes.c_int]),
     ("mk_last_cuda_error", ctypes.c_char_p, []),
@@ -214,6 +217,12 @@ def mk_get_info(ctx: int) -> mk_info:
     info = mk_info()
     check(load().mk_get_info(ctx, ctypes.byref(info)), "mk_get_info")
     return info
+
+
+def mk_argmax_f32_noalloc(logits_ptr: int, n: int, out_ptr: int, stream: int = 0) -> int:
+    """Greedy token of n device fp32 logits into out_ptr (device int32) with no
+    allocation; returns the library's code without raising."""
+    return load().mk_argmax_f32_noalloc(logits_ptr, n, out_ptr, stream)
 
 
 def mk_set_debug(ctx: int, knob: int, value: int) -> None:

@@ -178,6 +178,25 @@ int mk_decode_step_perop(mk_ctx* ctx, int32_t token, int32_t pos, float* logits_
 
 int mk_get_info(const mk_ctx* ctx, mk_info* out);
 
+/* Greedy token over a caller's fp32 logits without allocating anything (the
+ * pages have no counterpart: this serves callers that cannot call cudaMalloc,
+ * e.g. engines that reserve all device memory up front and hand out pointers
+ * into their own pool, or latency-critical code that must not allocate).
+ * logits: device fp32 [n]; out_token: device int32, receives the index of the
+ * largest finite logit (lowest index on ties), or -1 if none is finite.
+ * The scratch (one partial result per block) is a fixed device array inside
+ * the library, MK_NOALLOC_ARGMAX_BLOCKS * 8 bytes, held by every GPU that
+ * loads the library until the process exits.  n > MK_NOALLOC_ARGMAX_MAX_N (or
+ * n < 1, or a NULL pointer) returns MK_ERR_INVALID_ARG without launching.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call shares the array: calls whose kernels overlap on the GPU (e.g. two
+ * streams at once) race and must be serialized by the caller.  Runs on the
+ * calling thread's current device; asynchronous on `stream`. */
+#define MK_NOALLOC_ARGMAX_BLOCKS 1024
+#define MK_NOALLOC_ARGMAX_MAX_N (MK_NOALLOC_ARGMAX_BLOCKS * 4096)
+int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, void* stream);
+
 /* Debug knobs (off by default).  MK_DBG_SKIP_ARRIVAL: value = cta * 65536 + sync_id
  * makes that CTA skip one flag arrival, so every CTA waiting on it runs into its
  * bounded wait (used by the failure-detection test; -1 = off).  sync_id = 4 * layer
