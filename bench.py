@@ -183,10 +183,16 @@ def measured_peak():
 
 
 def load_profile_traffic(workload: str):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if any."""
-    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary
+    (profiles/traffic_<workload>.txt, "key: value" lines), if any."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
     try:
-        return json.load(open(p))
+        out = {}
+        for line in open(p):
+            if ":" in line and not line.lstrip().startswith("#"):
+                k, v = line.split(":", 1)
+                out[k.strip()] = v.strip()
+        return {"dram_bytes_per_launch": float(out["dram_bytes_per_launch"]), "kernel": out.get("kernel")}
     except Exception:
         return None
 
