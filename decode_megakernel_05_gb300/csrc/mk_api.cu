@@ -64,7 +64,7 @@ Tune resolve_tuning(const mk_tuning* t) {
     Tune r;
     r.ns_req = (t && t->ring_stages > 0) ? t->ring_stages : 6;
     r.slot = (t && t->slot_kib > 0) ? t->slot_kib * 1024 : 32 * 1024;
-    r.l2pf = (t && t->l2_prefetch_kib != 0) ? (t->l2_prefetch_kib < 0 ? 0 : t->l2_prefetch_kib * 1024) : 256 * 1024;
+    r.l2pf = (t && t->l2_prefetch_kib > 0) ? t->l2_prefetch_kib * 1024 : 0;   // default off (measured slower)
     r.grid = (t && t->grid_ctas > 0) ? t->grid_ctas : 0;
     return r;
 }

@@ -38,7 +38,6 @@
 #define MK_COMBINE_LOADS 8            // float4 loads per thread in the attention combine
 #define MK_MISC_BYTES 6656
 #define MK_MAX_H 8192                 // largest hidden size the kernels take
-#define MK_DOWN_UNITS ((MK_MAX_H / 4 + MK_NCT - 1) / MK_NCT)   // 4-row units per thread in the down projection
 
 // Device status word bits.
 #define MK_ST_TIMEOUT 0x1u
@@ -77,7 +76,7 @@ struct MkGeom {
     int32_t max_rows, max_nj;    // per-CTA maxima (QKV rows, FFN slice)
     int32_t smem_bytes;
     // shared-memory carve-up (byte offsets from the dynamic smem base)
-    int32_t off_full, off_empty, off_xv, off_ov, off_acc, off_rows, off_u, off_gs, off_xres, off_xres2, off_rope,
+    int32_t off_full, off_empty, off_xv, off_ov, off_rows, off_u, off_gs, off_xres, off_xres2, off_rope,
         off_red, off_sc, off_misc;
 };
 
@@ -110,9 +109,10 @@ MK_HD int mk_smem_layout(MkGeom& g) {
     g.off_full = o; o += 8 * g.ns;
     g.off_empty = o; o += 8 * g.ns;
     o = (o + 15) & ~15;
-    g.off_xv = o; o += 4 * g.H;               // normalised GEMV input / down-proj combine
-    g.off_ov = o; o += 4 * g.G * g.hd;        // q (attention) then o (O-proj input)
-    g.off_acc = o; o += 4 * g.G * g.hd;       // attention accumulator combine
+    // normalised GEMV input; between QKV and the FFN norm also the attention
+    // position-group partials (8 floats per consumer thread); the down-proj fold
+    g.off_xv = o; o += 4 * (g.H > 8 * MK_NCT ? g.H : 8 * MK_NCT);
+    g.off_ov = o; o += 4 * g.G * g.hd;        // o (O-proj input, split order)
     g.off_rows = o; o += 4 * ((g.max_rows + 3) & ~3);
     g.off_u = o; o += 4 * ((g.max_nj + 3) & ~3);
     g.off_gs = o; o += 4 * ((g.max_nj + 3) & ~3);

@@ -155,7 +155,6 @@ struct Smem {
     uint64_t* empty;
     float* xv;    // [H]
     float* ov;    // [G*hd]
-    float* acc;   // [G*hd]
     float* rows;  // [max_rows]
     float* u;     // [max_nj] up rows, then SiLU(gate)*up
     float* gs;    // [max_nj] gate rows
@@ -309,6 +308,9 @@ __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const 
 // Consumer-side cursor over the ring.
 struct Ring {
     uint32_t k = 0;
+    // trace only (lane 0 of each warp): ns spent taking tiles, between take
+    // and release, and releasing
+    unsigned long long t_take = 0, t_comp = 0, t_rel = 0, t_mark = 0;
     __device__ __forceinline__ uint32_t slot(int ns) const { return k % ns; }
 };
 
@@ -325,7 +327,7 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     const uint32_t slot = rg.k % ns, ph = (rg.k / ns) & 1u;
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {
-        const uint64_t tw = (p.trace && threadIdx.x == 0) ? gtimer() : 0;
+        const uint64_t tw = p.trace ? gtimer() : 0;
         ok = !s.misc->abort;
         if (ok && *(volatile int*)&s.misc->slot_tile[slot] != (int)rg.k) {
             const uint64_t t0 = gtimer();
@@ -341,7 +343,12 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
             }
         }
         ok = ok && wait_mbar(p, &s.full[slot], ph, &s.misc->abort);
-        if (tw) s.misc->cwait += gtimer() - tw;
+        if (tw) {
+            const uint64_t t1 = gtimer();
+            if (threadIdx.x == 0) s.misc->cwait += t1 - tw;
+            rg.t_take += t1 - tw;
+            rg.t_mark = t1;
+        }
         if (ok && s.misc->tile_bytes[slot] != expect_bytes) {
             atomicOr(p.status, MK_ST_SCHEDULE | MK_ST_ABORT);
             s.misc->abort = 1;
@@ -356,12 +363,26 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
 }
 // Done reading tile k; `weight` = MK_NCW / (warps reading it).  Advances the cursor.
 __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t weight = 1) {
+    const uint64_t t2 = (p.trace && (threadIdx.x & 31) == 0) ? gtimer() : 0;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
         mbar_arrive(&s.empty[rg.k % p.geo.ns], weight);
         if (p.trace && rg.k < 512) p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3584 + rg.k] = gtimer();
+        if (t2) {
+            rg.t_comp += t2 - rg.t_mark;
+            rg.t_rel += gtimer() - t2;
+        }
     }
     ++rg.k;
+}
+// Trace only: lane 0 of each warp stores its ring accounting at slots
+// 2304 + 16 * warp + 3 * e + {0 take, 1 between, 2 release} and clears it.
+__device__ __forceinline__ void trace_ring(const MkParams& p, Ring& rg, int e) {
+    if (p.trace && (threadIdx.x & 31) == 0) {
+        unsigned long long* tr = p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE + 2304 + 16 * (threadIdx.x >> 5) + 3 * e;
+        tr[0] = rg.t_take; tr[1] = rg.t_comp; tr[2] = rg.t_rel;
+    }
+    rg.t_take = rg.t_comp = rg.t_rel = 0;
 }
 
 // ---- warp-row GEMV over one phase's tiles
@@ -623,7 +644,6 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     s.empty = reinterpret_cast<uint64_t*>(smem + g.off_empty);
     s.xv = reinterpret_cast<float*>(smem + g.off_xv);
     s.ov = reinterpret_cast<float*>(smem + g.off_ov);
-    s.acc = reinterpret_cast<float*>(smem + g.off_acc);
     s.rows = reinterpret_cast<float*>(smem + g.off_rows);
     s.u = reinterpret_cast<float*>(smem + g.off_u);
     s.gs = reinterpret_cast<float*>(smem + g.off_gs);
@@ -744,7 +764,6 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 const float4 qa = __ldcg(qs), qb = __ldcg(qs + 1);
                 qr[0] = qa.x * qscale; qr[1] = qa.y * qscale; qr[2] = qa.z * qscale; qr[3] = qa.w * qscale;
                 qr[4] = qb.x * qscale; qr[5] = qb.y * qscale; qr[6] = qb.z * qscale; qr[7] = qb.w * qscale;
-                for (int i = t; i < G * HD; i += MK_NCT) s.acc[i] = 0.f;
                 if (t < G) { s.misc->mrun[t] = -INFINITY; s.misc->lrun[t] = 0.f; }
                 if (has_cur && t < HD / 4) {   // stage K[pos], V[pos] written by this group this launch
                     const size_t off = (((size_t)l * g.kvh + pl.g) * g.max_seq + p.pos) * HD;
@@ -779,16 +798,24 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 if (nr > 0) release_tile(p, s, ring);
                 ab = bar_or(ab || !ok);
             }
-            // sum the position groups into s.acc
-            if (!ab && nbt > 0 && t / A::TPP < nbt * g.KB + 1) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) atomicAdd(&s.acc[h_ * HD + dc_ * 8 + e], acc[e]);
+            // sum the position groups: every thread parks its 8 dims in xv
+            // ([position group][G*HD], free between QKV and the FFN norm), then
+            // each output element is summed over the groups and stored
+            if (!ab) {
+                float4* sp = reinterpret_cast<float4*>(s.xv + (t / A::TPP) * (G * HD) + h_ * HD + dc_ * 8);
+                sp[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                sp[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
             }
         }
         ab = bar_or(ab);
         if (!ab) {
             const size_t pbase = (((size_t)l * g.kvh + pl.g) * g.CPG + pl.i) * G;
-            for (int i = t; i < G * HD; i += MK_NCT) p.part_acc[pbase * HD + i] = s.acc[i];
+            for (int i = t; i < G * HD; i += MK_NCT) {
+                float a = 0.f;
+#pragma unroll
+                for (int q = 0; q < Attn<HD, G>::PPP; ++q) a += s.xv[q * (G * HD) + i];
+                p.part_acc[pbase * HD + i] = a;
+            }
             if (t < G) {
                 p.part_ml[(pbase + t) * 2 + 0] = s.misc->mrun[t];
                 p.part_ml[(pbase + t) * 2 + 1] = s.misc->lrun[t];
@@ -802,25 +829,35 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 6);
 
         // combine the group's partials -> o (the G heads of this KV group):
-        // weights exp2(m_j - M) / sum_j exp2(m_j - M) l_j.  The first batch of
-        // partial-accumulator loads is issued together with the (m, l) loads,
-        // so the combine costs one L2 round trip for short groups.
+        // weights exp2(m_j - M) / sum_j exp2(m_j - M) l_j.  A team of CT lanes
+        // owns one float4 of o and takes the partials j = lane (mod CT); the
+        // team sums with shuffles.  The first CB loads of every thread are
+        // issued together with the (m, l) loads, so a short group costs one
+        // L2 round trip.
         if (!ab) {
+            constexpr int NO4 = G * HD / 4;                     // float4s of o
+            constexpr int CT = (NO4 * 32 <= MK_NCT) ? 32 : (NO4 * 16 <= MK_NCT) ? 16 : (NO4 * 8 <= MK_NCT) ? 8
+                             : (NO4 * 4 <= MK_NCT) ? 4 : (NO4 * 2 <= MK_NCT) ? 2 : 1;
+            constexpr int CB = MK_COMBINE_LOADS;
+            constexpr int NPASS = (NO4 * CT + MK_NCT - 1) / MK_NCT;   // team passes over o
+            static_assert(NPASS == 1 || CT == 1, "combine mapping");
             const size_t gbase = ((size_t)l * g.kvh + pl.g) * g.CPG * G;
-            const int n4 = g.CPG * G * (HD / 4);
             const float4* pa = reinterpret_cast<const float4*>(p.part_acc + gbase * HD);
-            float4 v[MK_COMBINE_LOADS];
+            const int cl_ = t % CT;
+            float4 v[CB];
+            {
+                const int o4 = t / CT;
 #pragma unroll
-            for (int k = 0; k < MK_COMBINE_LOADS; ++k) {
-                const int i = t + k * MK_NCT;
-                v[k] = (i < n4) ? __ldcg(pa + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < CB; ++k) {
+                    const int j = cl_ + k * CT;
+                    v[k] = (o4 < NO4 && j < g.CPG) ? __ldcg(pa + (size_t)j * NO4 + o4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
             float* cw = s.red;                       // [CPG*G] maxima (red is free here)
             for (int i = t; i < g.CPG * G; i += MK_NCT) {
                 cw[i] = __ldcg(p.part_ml + (gbase + i) * 2);
                 s.misc->cl[i] = __ldcg(p.part_ml + (gbase + i) * 2 + 1);
             }
-            for (int i = t; i < G * HD; i += MK_NCT) s.ov[i] = 0.f;
             bar_or(false);
             if (t < G) {
                 float mx = -INFINITY;
@@ -835,25 +872,40 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 s.misc->alpha[t] = 1.f / den;
             }
             bar_or(false);
-            for (int base = 0; base < n4; base += MK_COMBINE_LOADS * MK_NCT) {
-                if (base > 0) {   // further batches for large groups
+#pragma unroll 1
+            for (int ps = 0; ps < NPASS; ++ps) {
+                const int o4 = t / CT + ps * (MK_NCT / CT);
+                const int h = (o4 * 4) / HD;
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k0 = 0; k0 * CT < g.CPG; k0 += CB) {
+                    if (k0 > 0 || ps > 0) {   // further batches (large groups or several passes)
 #pragma unroll
-                    for (int k = 0; k < MK_COMBINE_LOADS; ++k) {
-                        const int i = base + t + k * MK_NCT;
-                        v[k] = (i < n4) ? __ldcg(pa + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int k = 0; k < CB; ++k) {
+                            const int j = cl_ + (k0 + k) * CT;
+                            v[k] = (o4 < NO4 && j < g.CPG) ? __ldcg(pa + (size_t)j * NO4 + o4)
+                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < CB; ++k) {
+                        const int j = cl_ + (k0 + k) * CT;
+                        if (o4 < NO4 && j < g.CPG) {
+                            const float wt = s.misc->cwt[j * G + h];
+                            a.x = fmaf(wt, v[k].x, a.x); a.y = fmaf(wt, v[k].y, a.y);
+                            a.z = fmaf(wt, v[k].z, a.z); a.w = fmaf(wt, v[k].w, a.w);
+                        }
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < MK_COMBINE_LOADS; ++k) {
-                    const int i = base + t + k * MK_NCT;
-                    if (i < n4) {
-                        const int jh = i / (HD / 4), d4 = i % (HD / 4), h = jh % G;
-                        const float wt = s.misc->cwt[jh] * s.misc->alpha[h];
-                        const int i0 = h * HD + d4 * 4;     // 4 consecutive values: one split half
-                        float* o = s.ov + xsplit(i0, G * HD);
-                        atomicAdd(o + 0, wt * v[k].x); atomicAdd(o + 1, wt * v[k].y);
-                        atomicAdd(o + 2, wt * v[k].z); atomicAdd(o + 3, wt * v[k].w);
-                    }
+                for (int o = CT >> 1; o >= 1; o >>= 1) {
+                    a.x += __shfl_xor_sync(0xFFFFFFFFu, a.x, o); a.y += __shfl_xor_sync(0xFFFFFFFFu, a.y, o);
+                    a.z += __shfl_xor_sync(0xFFFFFFFFu, a.z, o); a.w += __shfl_xor_sync(0xFFFFFFFFu, a.w, o);
+                }
+                if (cl_ == 0 && o4 < NO4) {
+                    const float sc = s.misc->alpha[h];
+                    // 4 consecutive values of one head: one half of a split chunk
+                    *reinterpret_cast<float4*>(s.ov + xsplit(o4 * 4, G * HD)) =
+                        make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
                 }
             }
         }
@@ -875,6 +927,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
         ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2, dr0, dr1 - dr0);
         MK_TRACE(16 * l + 10);
+        if (l == 3) trace_ring(p, ring, 4);   // everything before this layer's FFN (discarded)
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
             const int JT = g.JT;
@@ -891,57 +944,93 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         }
         MK_TRACE(16 * l + 11);
         MK_TRACE_CWAIT(8 * l + 3);
-        // down projection: this CTA's FFN columns, all H rows (split-K).  Thread t
-        // owns 4-row units t, t + 512, ... of the output and runs over every
-        // column j of the slice: a D tile is [j][H] bf16, so lane-consecutive
-        // units read consecutive 8-byte chunks.
-        ab = bar_or(ab);                                        // u complete
+        if (l == 3) trace_ring(p, ring, 0);
+        // down projection: this CTA's FFN columns j, all H rows (split-K).  A D
+        // tile is [j][H] bf16.  The consumer threads form P j-phases of TP
+        // threads; phase jp takes the columns j = jp (mod P) of the slice, and
+        // thread tp of a phase owns the 8-row chunks tp + m*TP (m < CPT) of the
+        // output, so a warp reads 32 consecutive 16-byte chunks of one column.
+        // The phases' partial sums are folded through xv (P-1 -> ... -> 0),
+        // then phase 0 adds the residual of this CTA's rows and reduces into
+        // the residual stream with vector atomics.
+        ab = bar_or(ab);                                        // u complete, xv free
         float* xf = xa + (size_t)(2 * l + 1) * state;
         {
-            const int NU = H / 4;
-            float2 da[MK_DOWN_UNITS][2];
+            constexpr int NCH = 32 * MH;                        // 8-row chunks of H
+            constexpr int TP = NCH < 128 ? NCH : 128;           // threads per j-phase
+            constexpr int P = MK_NCT / TP;                      // j-phases
+            constexpr int CPT = NCH / TP;                       // chunks per thread
+            static_assert(MK_NCT % TP == 0 && NCH % TP == 0 && P >= 2, "down-projection mapping");
+            const int jp = t / TP, tp = t % TP;
+            float2 da[CPT][4];
 #pragma unroll
-            for (int mu = 0; mu < MK_DOWN_UNITS; ++mu) da[mu][0] = da[mu][1] = make_float2(0.f, 0.f);
+            for (int m = 0; m < CPT; ++m)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) da[m][k] = make_float2(0.f, 0.f);
             for (int j0 = 0; j0 < pl.nj && !ab; j0 += g.JD) {
                 const int n = min(g.JD, pl.nj - j0);
                 const uint8_t* tile;
                 const bool ok = take_tile(p, s, ring, (uint32_t)(n * H * 2), tile);
                 if (ok) {
-                    for (int jj = 0; jj < n; ++jj) {
+                    int jj = jp - j0 % P;
+                    if (jj < 0) jj += P;
+                    for (; jj < n; jj += P) {
                         const float uj = s.u[j0 + jj];
                         const float2 u2 = make_float2(uj, uj);
+                        const uint8_t* col = tile + (size_t)jj * H * 2;
 #pragma unroll
-                        for (int mu = 0; mu < MK_DOWN_UNITS; ++mu) {
-                            const int unit = t + mu * MK_NCT;
-                            if (unit < NU) {
-                                const uint2 w = *reinterpret_cast<const uint2*>(tile + ((size_t)jj * H + unit * 4) * 2);
-                                da[mu][0] = __ffma2_rn(bf2_lo_hi(w.x), u2, da[mu][0]);
-                                da[mu][1] = __ffma2_rn(bf2_lo_hi(w.y), u2, da[mu][1]);
-                            }
+                        for (int m = 0; m < CPT; ++m) {
+                            const uint4 w = lds128(col + (size_t)(tp + m * TP) * 16);
+                            da[m][0] = __ffma2_rn(bf2_lo_hi(w.x), u2, da[m][0]);
+                            da[m][1] = __ffma2_rn(bf2_lo_hi(w.y), u2, da[m][1]);
+                            da[m][2] = __ffma2_rn(bf2_lo_hi(w.z), u2, da[m][2]);
+                            da[m][3] = __ffma2_rn(bf2_lo_hi(w.w), u2, da[m][3]);
                         }
                     }
                 }
                 release_tile(p, s, ring);
                 if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
             }
-            if (!ab) {
+            MK_TRACE(16 * l + 14);
+            if (l == 3) trace_ring(p, ring, 1);
+            // fold the phases: phase q adds what phase q+1 left in xv (element
+            // e of chunk c at xv[e * NCH + c]: lane-consecutive, conflict free)
+#pragma unroll 1
+            for (int q = P - 1; q >= 0; --q) {
+                if (q < P - 1) ab = bar_or(ab);
+                if (jp == q && !ab) {
 #pragma unroll
-                for (int mu = 0; mu < MK_DOWN_UNITS; ++mu) {
-                    const int unit = t + mu * MK_NCT;
-                    if (unit < NU) {
-                        float4 v = make_float4(da[mu][0].x, da[mu][0].y, da[mu][1].x, da[mu][1].y);
-                        // each CTA carries the residual of its own rows [dr0, dr1)
-                        const int r4 = unit * 4 - dr0;
-                        if ((unsigned)(r4 + 3) < (unsigned)(dr1 - dr0 + 3)) {
-                            if ((unsigned)(r4 + 0) < (unsigned)(dr1 - dr0)) v.x += s.xres2[r4 + 0];
-                            if ((unsigned)(r4 + 1) < (unsigned)(dr1 - dr0)) v.y += s.xres2[r4 + 1];
-                            if ((unsigned)(r4 + 2) < (unsigned)(dr1 - dr0)) v.z += s.xres2[r4 + 2];
-                            if ((unsigned)(r4 + 3) < (unsigned)(dr1 - dr0)) v.w += s.xres2[r4 + 3];
+                    for (int m = 0; m < CPT; ++m) {
+                        const int cc = tp + m * TP;
+                        if (q < P - 1) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                da[m][k].x += s.xv[(2 * k) * NCH + cc];
+                                da[m][k].y += s.xv[(2 * k + 1) * NCH + cc];
+                            }
                         }
-                        red_add_v4(xf + unit * 4, v);
+                        if (q > 0) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                s.xv[(2 * k) * NCH + cc] = da[m][k].x;
+                                s.xv[(2 * k + 1) * NCH + cc] = da[m][k].y;
+                            }
+                        } else {
+                            // rows 8cc .. 8cc+7; this CTA carries the residual of rows [dr0, dr1)
+                            float r[8] = {da[m][0].x, da[m][0].y, da[m][1].x, da[m][1].y,
+                                          da[m][2].x, da[m][2].y, da[m][3].x, da[m][3].y};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int rr = 8 * cc + e - dr0;
+                                if ((unsigned)rr < (unsigned)(dr1 - dr0)) r[e] += s.xres2[rr];
+                            }
+                            red_add_v4(xf + 8 * cc, make_float4(r[0], r[1], r[2], r[3]));
+                            red_add_v4(xf + 8 * cc + 4, make_float4(r[4], r[5], r[6], r[7]));
+                        }
                     }
                 }
             }
+            MK_TRACE(16 * l + 15);
         }
         ab = bar_or(ab);
         MK_TRACE(16 * l + 12);

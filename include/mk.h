@@ -74,7 +74,8 @@ typedef struct {
                                 1 = no overlap of loading and compute ("prefetch off") */
     int32_t slot_kib;        /* bytes per ring slot / weight tile, KiB (default 32) */
     int32_t l2_prefetch_kib; /* how far (KiB of tile stream) each CTA prefetches into L2 ahead of
-                                its ring copies (default 256; negative = off) */
+                                its ring copies (default, zero or negative: off -- on this path the
+                                extra L2 traffic cost more than the hidden latency saved) */
     int32_t grid_ctas;       /* CTAs of the persistent grid (default: n_kv_heads * floor(SMs / n_kv_heads));
                                 must be a multiple of n_kv_heads and fit one CTA per SM */
 } mk_tuning;
