@@ -222,6 +222,7 @@ struct mk_ctx {
     int32_t *next_token = nullptr, *tokens_dev = nullptr, *prompt_dev = nullptr;
     // debug
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
+    int gemv_groups = 0;
     int64_t wait_limit_ns = 1000000000LL;
     unsigned long long* trace = nullptr;
     // per-operator baseline
@@ -270,6 +271,7 @@ MkParams base_params(const mk_ctx* c) {
     p.seq = c->seq;
     p.dbg_skip_cta = c->dbg_skip_cta;
     p.dbg_skip_sync = c->dbg_skip_sync;
+    p.gemv_groups = c->gemv_groups;
     p.wait_limit_ns = c->wait_limit_ns;
     p.trace = c->trace;
     p.out_idx = 0;
@@ -790,6 +792,11 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_TRACE) {
         if (value != 0 && c->geo.L > MK_TRACE_MAX_LAYERS) return MK_ERR_UNSUPPORTED;
         c->trace = reinterpret_cast<unsigned long long*>((uintptr_t)value);
+        return MK_OK;
+    }
+    if (knob == MK_DBG_GEMV_GROUPS) {
+        if (value != 0 && value != 1 && value != 2 && value != 3 && value != 6) return MK_ERR_INVALID_ARG;
+        c->gemv_groups = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_WAIT_LIMIT_NS) {

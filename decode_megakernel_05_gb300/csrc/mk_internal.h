@@ -58,6 +58,10 @@ MK_HD int64_t mk_split(int64_t n, int64_t parts, int64_t k) { return (k * n) / p
 // a ring slot, even (QKV pairs and gate/up groups never straddle a tile).
 MK_HD int mk_tile_rows(int K, int slot_bytes) { return (slot_bytes / (2 * K)) & ~1; }
 
+// Column blocks of the hidden-width GEMV (QKV, gate/up): rows of H = 256 * MH
+// columns are split into min(4, MH) blocks, one per consumer warp of a row slot.
+MK_HD int mk_wide_nkb(int H) { return H / 256 < 4 ? H / 256 : 4; }
+
 struct MkCtaPlan {
     int64_t stream_off;   // byte offset of this CTA's stream in the arena
     int64_t layer_bytes;  // bytes of one layer's tiles in the stream
@@ -76,7 +80,7 @@ struct MkGeom {
     int32_t max_rows, max_nj;    // per-CTA maxima (QKV rows, FFN slice)
     int32_t smem_bytes;
     // shared-memory carve-up (byte offsets from the dynamic smem base)
-    int32_t off_full, off_empty, off_xv, off_ov, off_rows, off_u, off_gs, off_xres, off_xres2, off_rope,
+    int32_t off_full, off_empty, off_xv, off_ov, off_part, off_u, off_xres, off_xres2, off_rope,
         off_red, off_sc, off_misc;
 };
 
@@ -113,9 +117,11 @@ MK_HD int mk_smem_layout(MkGeom& g) {
     // position-group partials (8 floats per consumer thread); the down-proj fold
     g.off_xv = o; o += 4 * (g.H > 8 * MK_NCT ? g.H : 8 * MK_NCT);
     g.off_ov = o; o += 4 * g.G * g.hd;        // o (O-proj input, split order)
-    g.off_rows = o; o += 4 * ((g.max_rows + 3) & ~3);
+    {   // per-column-block partial sums of the QKV / gate-up rows
+        const int rows = g.max_rows > 2 * g.max_nj ? g.max_rows : 2 * g.max_nj;
+        g.off_part = o; o += 4 * ((rows * mk_wide_nkb(g.H) + 3) & ~3);
+    }
     g.off_u = o; o += 4 * ((g.max_nj + 3) & ~3);
-    g.off_gs = o; o += 4 * ((g.max_nj + 3) & ~3);
     g.off_xres = o; o += 4 * ((g.H / g.CPG + 4) & ~3);
     g.off_xres2 = o; o += 4 * ((g.H / g.nC + 4) & ~3);
     g.off_rope = o; o += 4 * g.hd;
@@ -158,6 +164,7 @@ struct MkParams {
     int32_t* tokens_out;         // greedy output buffer or nullptr
     int32_t out_idx;
     int32_t dbg_skip_cta, dbg_skip_sync;
+    int32_t gemv_groups;         // warp groups taking turns on hidden-width GEMV tiles (0 = default)
     int64_t wait_limit_ns;
     // Optional segment trace (%globaltimer ns), nullptr = off.  Per CTA
     // MK_TRACE_STRIDE slots: consumer events 16*l + e (e = MK_EV_*), end

@@ -155,9 +155,8 @@ struct Smem {
     uint64_t* empty;
     float* xv;    // [H]
     float* ov;    // [G*hd]
-    float* rows;  // [max_rows]
-    float* u;     // [max_nj] up rows, then SiLU(gate)*up
-    float* gs;    // [max_nj] gate rows
+    float* part;  // [rows][NKB] column-block partial sums of the QKV / gate-up rows
+    float* u;     // [max_nj] SiLU(gate)*up
     float* xres;  // raw residual of this CTA's O rows (group 0 only)
     float* xres2; // raw residual of rows split(H, nC, c)
     float* rope;  // cos[hd/2], sin[hd/2] at this position
@@ -503,6 +502,123 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
     return bar_or(ab);
 }
 
+// ---- GEMV for rows of K = 256 * MH columns (QKV, gate/up)
+//
+// The consumer warps form NG groups of WPG = MK_NCW / NG warps; tile ti goes to
+// group ti % NG, so NG tiles are worked on at once and each is held for the
+// time its group needs.  Inside a group warp (row slot rs, column block cb):
+// the column block is CPL = MH / NKB chunks of 8 columns per lane, chunk
+// (cb * CPL + j) * 32 + lane, whose activations the lane keeps in registers
+// for the whole phase.  Row R of the phase (tiles of TR rows in order) belongs
+// to row slot R % NRS; a warp takes its rows of a tile four at a time, reduces
+// the four partial dot products over the warp with a transposed butterfly
+// (6 shuffles) and stores them in part[R * NKB + cb].  The caller sums the NKB
+// partials of a row after the phase barrier.
+template <int MH, int NG>
+struct WideGemv {
+    static constexpr int K = MH * 256;
+    static constexpr int WPG = MK_NCW / NG;
+    static constexpr int NKB0 = (WPG % 4 == 0) ? 4 : (WPG % 2 == 0) ? 2 : 1;
+    static constexpr int NKB = MH < NKB0 ? MH : NKB0;
+    static constexpr int CPL = MH / NKB;
+    static constexpr int NRS = WPG / NKB;
+    static constexpr bool ok = (MK_NCW % NG == 0) && (MH % NKB == 0) && (WPG % NKB == 0) && CPL <= 4;
+};
+// part[] stride per row: the largest NKB any group count uses for this width
+template <int MH>
+struct WidePart { static constexpr int NKB = MH < 4 ? MH : 4; };
+
+template <int MH, int NG>
+__device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring& ring, const float* xs, int nrows,
+                                          int TR, bool ab, float* part) {
+    using W = WideGemv<MH, NG>;
+    constexpr int K = W::K, NKB = W::NKB, CPL = W::CPL, NRS = W::NRS, WPG = W::WPG;
+    constexpr int PS = WidePart<MH>::NKB;
+    static_assert(W::ok && NKB <= PS, "wide GEMV mapping");
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = w / WPG, wg = w % WPG;
+    const int cb = wg % NKB, rs = wg / NKB;
+    float4 xl[CPL], xh[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const int ch = (cb * CPL + j) * 32 + lane;
+        xl[j] = reinterpret_cast<const float4*>(xs)[ch];
+        xh[j] = reinterpret_cast<const float4*>(xs + K / 2)[ch];
+    }
+    const int ntiles = (nrows + TR - 1) / TR;
+    for (int ti = 0; ti < ntiles && !ab; ++ti) {
+        if (NG > 1 && (ti % NG) != grp) { ++ring.k; continue; }   // another group's tile
+        const int R0 = ti * TR, R = min(TR, nrows - R0);
+        const uint8_t* tile;
+        const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
+        if (ok) {
+            int r = rs - R0 % NRS;
+            if (r < 0) r += NRS;
+            for (; r < R; r += 4 * NRS) {          // rows r, r + NRS, r + 2 NRS, r + 3 NRS
+                const int nv = min(4, (R - r + NRS - 1) / NRS);
+                float2 a[4][2];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) a[q][0] = a[q][1] = make_float2(0.f, 0.f);
+                const uint8_t* rp = tile + (size_t)r * (K * 2);
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    const int ch = (cb * CPL + j) * 32 + lane;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q < nv) fma_chunk(lds128(rp + (size_t)q * NRS * (K * 2) + ch * 16), xl[j], xh[j], a[q][0], a[q][1]);
+                }
+                float v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = (a[q][0].x + a[q][0].y) + (a[q][1].x + a[q][1].y);
+                // transposed butterfly: lane bit 4 picks rows {0,1} / {2,3},
+                // bit 3 one row of the pair; bits 0-2 finish the sum
+                const bool up = lane & 16, b3 = lane & 8;
+                float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+                k0 += __shfl_xor_sync(0xFFFFFFFFu, up ? v[0] : v[2], 16);
+                k1 += __shfl_xor_sync(0xFFFFFFFFu, up ? v[1] : v[3], 16);
+                float kk = b3 ? k1 : k0;
+                kk += __shfl_xor_sync(0xFFFFFFFFu, b3 ? k0 : k1, 8);
+                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 4);
+                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 2);
+                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 1);
+                const int q = lane >> 3;               // row of the four this lane holds
+                if ((lane & 7) == 0 && q < nv) {
+                    float* pr = part + (R0 + r + q * NRS) * PS;
+                    pr[cb] = kk;
+                    if (NKB < PS && cb == 0) {     // unused column-block slots read as zero
+#pragma unroll
+                        for (int c2 = NKB; c2 < PS; ++c2) pr[c2] = 0.f;
+                    }
+                }
+            }
+        }
+        release_tile(p, s, ring, (uint32_t)NG);
+        if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
+    }
+    return bar_or(ab);
+}
+// Runtime choice of the group count (1, 2, 3 or 6; others use the default 3).
+template <int MH>
+__device__ __forceinline__ bool gemv_fifo(const MkParams& p, const Smem& s, Ring& ring, const float* xs, int nrows,
+                                          int TR, bool ab, float* part) {
+    switch (p.gemv_groups) {
+        case 1: if constexpr (WideGemv<MH, 1>::ok) return gemv_wide<MH, 1>(p, s, ring, xs, nrows, TR, ab, part); break;
+        case 2: if constexpr (WideGemv<MH, 2>::ok) return gemv_wide<MH, 2>(p, s, ring, xs, nrows, TR, ab, part); break;
+        case 6: if constexpr (WideGemv<MH, 6>::ok) return gemv_wide<MH, 6>(p, s, ring, xs, nrows, TR, ab, part); break;
+        default: break;
+    }
+    return gemv_wide<MH, 3>(p, s, ring, xs, nrows, TR, ab, part);
+}
+// Sum of the NKB column-block partials of row R of a FIFO GEMV phase.
+template <int MH>
+__device__ __forceinline__ float wide_row(const float* part, int R) {
+    constexpr int NKB = WidePart<MH>::NKB;
+    float a = part[R * NKB];
+#pragma unroll
+    for (int c = 1; c < NKB; ++c) a += part[R * NKB + c];
+    return a;
+}
+
 // RMSNorm of x (fp32 global, or the bf16 embedding row when xb != nullptr) into
 // s.xv, with gain g (fp32).  The raw values of rows [keep0, keep0 + nkeep) are
 // also kept in `keep` (the residual this CTA adds later).  Returns the uniform
@@ -644,9 +760,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     s.empty = reinterpret_cast<uint64_t*>(smem + g.off_empty);
     s.xv = reinterpret_cast<float*>(smem + g.off_xv);
     s.ov = reinterpret_cast<float*>(smem + g.off_ov);
-    s.rows = reinterpret_cast<float*>(smem + g.off_rows);
+    s.part = reinterpret_cast<float*>(smem + g.off_part);
     s.u = reinterpret_cast<float*>(smem + g.off_u);
-    s.gs = reinterpret_cast<float*>(smem + g.off_gs);
     s.xres = reinterpret_cast<float*>(smem + g.off_xres);
     s.xres2 = reinterpret_cast<float*>(smem + g.off_xres2);
     s.rope = reinterpret_cast<float*>(smem + g.off_rope);
@@ -724,13 +839,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres, pl.orow0,
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
-        ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv, 2 * pl.npairs, g.TRh, ab, [&](int r, float v) { s.rows[r] = v; });
+        ab = gemv_fifo<MH>(p, s, ring, s.xv, 2 * pl.npairs, g.TRh, ab, s.part);
         MK_TRACE(16 * l + 2);
         MK_TRACE_CWAIT(8 * l + 0);
         if (!ab) {
             for (int j = t; j < pl.npairs; j += MK_NCT) {
                 const int pair = pl.pair0 + j, slot = pair / hd2, d = pair % hd2;
-                float a = s.rows[2 * j], b = s.rows[2 * j + 1];
+                float a = wide_row<MH>(s.part, 2 * j), b = wide_row<MH>(s.part, 2 * j + 1);
                 if (slot <= G) {
                     const float cs = s.rope[d], sn = s.rope[hd2 + d];
                     const float a2 = a * cs - b * sn, b2 = b * cs + a * sn;
@@ -931,15 +1046,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
             const int JT = g.JT;
-            ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv, 2 * pl.nj, 2 * JT, ab, [&](int r, float v) {
-                const int q = r / (2 * JT), rr = r % (2 * JT);
-                const int n = min(JT, pl.nj - q * JT);
-                if (rr < n) s.gs[q * JT + rr] = v;
-                else s.u[q * JT + rr - n] = v;
-            });
+            ab = gemv_fifo<MH>(p, s, ring, s.xv, 2 * pl.nj, 2 * JT, ab, s.part);
             for (int j = t; j < pl.nj; j += MK_NCT) {
-                const float gt = s.gs[j];
-                s.u[j] = gt / (1.f + __expf(-gt)) * s.u[j];
+                const int q = j / JT, jj = j % JT;
+                const int n = min(JT, pl.nj - q * JT);
+                const float gt = wide_row<MH>(s.part, q * 2 * JT + jj);
+                const float up = wide_row<MH>(s.part, q * 2 * JT + n + jj);
+                s.u[j] = gt / (1.f + __expf(-gt)) * up;
             }
         }
         MK_TRACE(16 * l + 11);
