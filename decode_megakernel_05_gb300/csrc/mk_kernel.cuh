@@ -1059,9 +1059,9 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE_CWAIT(8 * l + 3);
         if (l == 3) trace_ring(p, ring, 0);
         // down projection: this CTA's FFN columns j, all H rows (split-K).  A D
-        // tile is [j][H] bf16.  The consumer threads form P j-phases of TP
-        // threads; phase jp takes the columns j = jp (mod P) of the slice, and
-        // thread tp of a phase owns the 8-row chunks tp + m*TP (m < CPT) of the
+        // tile is [j][H] bf16.  The consumer threads form P groups of TP
+        // threads that take turns on the tiles (tile b goes to group b % P), and
+        // thread tp of a group owns the 8-row chunks tp + m*TP (m < CPT) of the
         // output, so a warp reads 32 consecutive 16-byte chunks of one column.
         // The phases' partial sums are folded through xv (P-1 -> ... -> 0),
         // then phase 0 adds the residual of this CTA's rows and reduces into
@@ -1080,14 +1080,14 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             for (int m = 0; m < CPT; ++m)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) da[m][k] = make_float2(0.f, 0.f);
-            for (int j0 = 0; j0 < pl.nj && !ab; j0 += g.JD) {
+            for (int j0 = 0, b = 0; j0 < pl.nj && !ab; j0 += g.JD, ++b) {
+                if (b % P != jp) { ++ring.k; continue; }   // another group's tile
                 const int n = min(g.JD, pl.nj - j0);
                 const uint8_t* tile;
                 const bool ok = take_tile(p, s, ring, (uint32_t)(n * H * 2), tile);
                 if (ok) {
-                    int jj = jp - j0 % P;
-                    if (jj < 0) jj += P;
-                    for (; jj < n; jj += P) {
+#pragma unroll (CPT <= 2 ? 2 : 1)
+                    for (int jj = 0; jj < n; ++jj) {
                         const float uj = s.u[j0 + jj];
                         const float2 u2 = make_float2(uj, uj);
                         const uint8_t* col = tile + (size_t)jj * H * 2;
@@ -1101,7 +1101,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                         }
                     }
                 }
-                release_tile(p, s, ring);
+                release_tile(p, s, ring, (uint32_t)P);      // TP / 32 readers, weight P each
                 if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
             }
             MK_TRACE(16 * l + 14);
