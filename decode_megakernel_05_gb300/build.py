@@ -56,9 +56,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
                     "-I", INCLUDE, "-I", CSRC]
     jobs = [(src, os.path.join(BUILD, src.replace(".cu", ".o")), []) for src in SOURCES]
-    for hd, g, mh in VARIANTS:
-        jobs.append(("mk_kernel.cu", os.path.join(BUILD, f"mk_kernel_{hd}_{g}_{mh}.o"),
-                     [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}", f"-DMK_MH_V={mh}"]))
+    for hd, g, mh in VARIANTS:   # each without and with the segment trace compiled in
+        for tr in (False, True):
+            jobs.append(("mk_kernel.cu", os.path.join(BUILD, f"mk_kernel_{hd}_{g}_{mh}{'_trace' if tr else ''}.o"),
+                         [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}", f"-DMK_MH_V={mh}"] + ([] if tr else ["-DMK_NO_TRACE"])))
 
     def compile_one(job):
         src, obj, defs = job

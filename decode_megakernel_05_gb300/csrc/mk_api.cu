@@ -19,16 +19,24 @@
 // VARIANTS in build.py.
 #define MK_VARIANTS(X) \
     X(64, 2, 1) X(64, 4, 2) X(64, 4, 4) X(64, 4, 8) X(64, 4, 16) X(128, 4, 4) X(128, 4, 8) X(128, 4, 16)
-#define MK_DECL(hd, g, mh) extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh(void);
+// Each variant exists twice: without trace code (launched normally) and with
+// it (launched while a segment trace is requested).
+#define MK_DECL(hd, g, mh)                                         \
+    extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh(void); \
+    extern "C" const void* mk_kernel_trace_ptr_##hd##_##g##_##mh(void);
 MK_VARIANTS(MK_DECL)
 #undef MK_DECL
 
-static int mk_kernel_variant(int hd, int G, int H, const void** fn) {
-#define MK_PICK(hd_, g_, mh_) \
-    if (hd == hd_ && G == g_ && H == 256 * mh_) { *fn = mk_kernel_ptr_##hd_##_##g_##_##mh_(); return 0; }
+static int mk_kernel_variant(int hd, int G, int H, const void** fn, const void** fn_trace) {
+#define MK_PICK(hd_, g_, mh_)                                         \
+    if (hd == hd_ && G == g_ && H == 256 * mh_) {                     \
+        *fn = mk_kernel_ptr_##hd_##_##g_##_##mh_();                   \
+        *fn_trace = mk_kernel_trace_ptr_##hd_##_##g_##_##mh_();       \
+        return 0;                                                     \
+    }
     MK_VARIANTS(MK_PICK)
 #undef MK_PICK
-    *fn = nullptr;
+    *fn = *fn_trace = nullptr;
     return -1;
 }
 
@@ -79,8 +87,8 @@ int check_shape(const mk_config* c, bool need_kernel = true) {
     if (c->n_q_heads % c->n_kv_heads) return MK_ERR_INVALID_ARG;
     if (c->head_dim != 64 && c->head_dim != 128) return MK_ERR_UNSUPPORTED;
     const int G = c->n_q_heads / c->n_kv_heads;
-    const void* fn = nullptr;
-    if (need_kernel && mk_kernel_variant(c->head_dim, G, c->hidden, &fn) != 0) return MK_ERR_UNSUPPORTED;
+    const void *fn = nullptr, *fn_trace = nullptr;
+    if (need_kernel && mk_kernel_variant(c->head_dim, G, c->hidden, &fn, &fn_trace) != 0) return MK_ERR_UNSUPPORTED;
     // GEMV row length K: 8-column chunks spread over min(32, K/8) lanes, so
     // K/8 divides 32 (short rows) or K is a multiple of 256 (long rows).
     auto width_ok = [](int K) {
@@ -205,7 +213,8 @@ struct mk_ctx {
     Tune tune;
     MkGeom geo;
     int device = 0, sm_count = 0;
-    const void* kernel = nullptr;
+    const void* kernel = nullptr;        // the fused step without trace code
+    const void* kernel_trace = nullptr;  // the same with the segment trace compiled in
     std::vector<MkCtaPlan> plans;
     int64_t arena_bytes = 0, device_bytes = 0;
     bool weights_loaded = false;
@@ -223,6 +232,7 @@ struct mk_ctx {
     // debug
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
     int gemv_groups = 0;
+    int trace_detail = 1;
     int64_t wait_limit_ns = 1000000000LL;
     unsigned long long* trace = nullptr;
     // per-operator baseline
@@ -272,6 +282,7 @@ MkParams base_params(const mk_ctx* c) {
     p.dbg_skip_cta = c->dbg_skip_cta;
     p.dbg_skip_sync = c->dbg_skip_sync;
     p.gemv_groups = c->gemv_groups;
+    p.trace_detail = c->trace_detail;
     p.wait_limit_ns = c->wait_limit_ns;
     p.trace = c->trace;
     p.out_idx = 0;
@@ -291,7 +302,7 @@ int launch_step(mk_ctx* c, MkParams& p, cudaStream_t st) {
     lc.attrs = attr;
     lc.numAttrs = 1;
     void* args[] = {&p};
-    MK_CU(cudaLaunchKernelExC(&lc, c->kernel, args));
+    MK_CU(cudaLaunchKernelExC(&lc, c->trace ? c->kernel_trace : c->kernel, args));
     c->last_stream = st;
     return MK_OK;
 }
@@ -416,10 +427,11 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         if ((rc = build_geom(cfg, c->tune, grid, ns, g)) != MK_OK) return fail(rc);
         if (g.smem_bytes + 1024 <= smem_optin) { c->geo = g; break; }
     }
-    mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, &c->kernel);
-    if ((e = cudaFuncSetAttribute(c->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, c->geo.smem_bytes)) !=
-        cudaSuccess)
-        return fail(cuda_fail(e, "cudaFuncSetAttribute"));
+    mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, &c->kernel, &c->kernel_trace);
+    for (const void* k : {c->kernel, c->kernel_trace})
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c->geo.smem_bytes)) !=
+            cudaSuccess)
+            return fail(cuda_fail(e, "cudaFuncSetAttribute"));
     int per_sm = 0;
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c->kernel, MK_BLOCK, c->geo.smem_bytes)) !=
         cudaSuccess)
@@ -792,6 +804,11 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_TRACE) {
         if (value != 0 && c->geo.L > MK_TRACE_MAX_LAYERS) return MK_ERR_UNSUPPORTED;
         c->trace = reinterpret_cast<unsigned long long*>((uintptr_t)value);
+        return MK_OK;
+    }
+    if (knob == MK_DBG_TRACE_DETAIL) {
+        if (value != 0 && value != 1) return MK_ERR_INVALID_ARG;
+        c->trace_detail = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_GEMV_GROUPS) {

@@ -11,6 +11,15 @@
 #define MK_CAT2(a, b, c, d) a##b##_##c##_##d
 #define MK_CAT(a, b, c, d) MK_CAT2(a, b, c, d)
 
+// Built twice per variant: with -DMK_NO_TRACE (the production kernel, no trace
+// code at all: a smaller instruction footprint per layer) and without (the
+// kernel launched while a segment trace is requested).
+#ifdef MK_NO_TRACE
 extern "C" const void* MK_CAT(mk_kernel_ptr_, MK_HD_V, MK_G_V, MK_MH_V)(void) {
     return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V>;
 }
+#else
+extern "C" const void* MK_CAT(mk_kernel_trace_ptr_, MK_HD_V, MK_G_V, MK_MH_V)(void) {
+    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V>;
+}
+#endif

@@ -34,6 +34,13 @@
 
 #include "mk_internal.h"
 
+// Building with -DMK_NO_TRACE compiles the segment/tile trace out entirely.
+#ifdef MK_NO_TRACE
+#define MK_TRACE_ON false
+#else
+#define MK_TRACE_ON true
+#endif
+
 namespace mk {
 namespace {  // internal linkage: every kernel variant is its own translation unit
 
@@ -169,14 +176,14 @@ struct Smem {
 // stamps %globaltimer at the end of each segment.
 #define MK_TRACE(slot_)                                                                  \
     do {                                                                                  \
-        if (p.trace && threadIdx.x == 0)                                                  \
+        if (MK_TRACE_ON && p.trace && threadIdx.x == 0)                                                  \
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + (slot_)] = gtimer();           \
     } while (0)
 
 // Per-phase consumer ring-wait (trace only): slot 1024 + 8*layer + phase.
 #define MK_TRACE_CWAIT(slot_)                                                            \
     do {                                                                                  \
-        if (p.trace && threadIdx.x == 0) {                                                \
+        if (MK_TRACE_ON && p.trace && threadIdx.x == 0) {                                                \
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + (slot_)] = s.misc->cwait; \
             s.misc->cwait = 0;                                                            \
         }                                                                                 \
@@ -236,7 +243,7 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
     uint32_t k = 0;
     bool stop = false;
     unsigned long long pwait = 0;
-    unsigned long long* tr = p.trace ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
+    unsigned long long* tr = (MK_TRACE_ON && p.trace && p.trace_detail) ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
     walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
         if (stop) return;
         const uint32_t slot = k % ns, ph = (k / ns) & 1u;
@@ -326,7 +333,7 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     const uint32_t slot = rg.k % ns, ph = (rg.k / ns) & 1u;
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {
-        const uint64_t tw = p.trace ? gtimer() : 0;
+        const uint64_t tw = (MK_TRACE_ON && p.trace && p.trace_detail) ? gtimer() : 0;
         ok = !s.misc->abort;
         if (ok && *(volatile int*)&s.misc->slot_tile[slot] != (int)rg.k) {
             const uint64_t t0 = gtimer();
@@ -356,17 +363,17 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     }
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     tile = s.ring + (size_t)slot * p.geo.slot;
-    if (p.trace && (threadIdx.x & 31) == 0 && rg.k < 512)   // trace: a reader got tile k
+    if (MK_TRACE_ON && p.trace && p.trace_detail && (threadIdx.x & 31) == 0 && rg.k < 512)   // trace: a reader got tile k
         p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3072 + rg.k] = gtimer();
     return ok;
 }
 // Done reading tile k; `weight` = MK_NCW / (warps reading it).  Advances the cursor.
 __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t weight = 1) {
-    const uint64_t t2 = (p.trace && (threadIdx.x & 31) == 0) ? gtimer() : 0;
+    const uint64_t t2 = (MK_TRACE_ON && p.trace && p.trace_detail && (threadIdx.x & 31) == 0) ? gtimer() : 0;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
         mbar_arrive(&s.empty[rg.k % p.geo.ns], weight);
-        if (p.trace && rg.k < 512) p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3584 + rg.k] = gtimer();
+        if (t2 && rg.k < 512) p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3584 + rg.k] = gtimer();
         if (t2) {
             rg.t_comp += t2 - rg.t_mark;
             rg.t_rel += gtimer() - t2;
@@ -377,7 +384,7 @@ __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, R
 // Trace only: lane 0 of each warp stores its ring accounting at slots
 // 2304 + 16 * warp + 3 * e + {0 take, 1 between, 2 release} and clears it.
 __device__ __forceinline__ void trace_ring(const MkParams& p, Ring& rg, int e) {
-    if (p.trace && (threadIdx.x & 31) == 0) {
+    if (MK_TRACE_ON && p.trace && p.trace_detail && (threadIdx.x & 31) == 0) {
         unsigned long long* tr = p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE + 2304 + 16 * (threadIdx.x >> 5) + 3 * e;
         tr[0] = rg.t_take; tr[1] = rg.t_comp; tr[2] = rg.t_rel;
     }
@@ -473,7 +480,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
         const int R = min(TR, nrows - ti * TR);
         const uint8_t* tile;
         const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
-        if (trace_slot >= 0 && p.trace && threadIdx.x == 0 && ti < 256)
+        if (trace_slot >= 0 && MK_TRACE_ON && p.trace && p.trace_detail && threadIdx.x == 0 && ti < 256)
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
         if (ok) {
             for (int base = wg * rows_per_warp; base < R; base += wpg * rows_per_warp) {

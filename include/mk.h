@@ -224,6 +224,9 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
  * the tiles of the hidden-width GEMVs (QKV, gate/up): 1, 2, 3 or 6 (0 = the
  * default, 3).  Values the shape cannot use fall back to the default. */
 #define MK_DBG_GEMV_GROUPS 4
+/* MK_DBG_TRACE_DETAIL: 1 (default) = the trace also records the per-tile and
+ * ring-wait slots; 0 = segment ends only (the least perturbed timing). */
+#define MK_DBG_TRACE_DETAIL 5
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
 const char* mk_strerror(int code);
