@@ -233,6 +233,7 @@ struct mk_ctx {
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
     int gemv_groups = 0;
     int trace_detail = 1;
+    int inflight = 0;
     int64_t wait_limit_ns = 1000000000LL;
     unsigned long long* trace = nullptr;
     // per-operator baseline
@@ -283,6 +284,7 @@ MkParams base_params(const mk_ctx* c) {
     p.dbg_skip_sync = c->dbg_skip_sync;
     p.gemv_groups = c->gemv_groups;
     p.trace_detail = c->trace_detail;
+    p.inflight = c->inflight > 0 ? c->inflight : 3;
     p.wait_limit_ns = c->wait_limit_ns;
     p.trace = c->trace;
     p.out_idx = 0;
@@ -804,6 +806,11 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_TRACE) {
         if (value != 0 && c->geo.L > MK_TRACE_MAX_LAYERS) return MK_ERR_UNSUPPORTED;
         c->trace = reinterpret_cast<unsigned long long*>((uintptr_t)value);
+        return MK_OK;
+    }
+    if (knob == MK_DBG_INFLIGHT) {
+        if (value < 0 || value > 16) return MK_ERR_INVALID_ARG;
+        c->inflight = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_TRACE_DETAIL) {

@@ -244,10 +244,15 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
     bool stop = false;
     unsigned long long pwait = 0;
     unsigned long long* tr = (MK_TRACE_ON && p.trace && p.trace_detail) ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
+    const uint32_t lim = (uint32_t)(p.inflight < ns ? p.inflight : ns);
     walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
         if (stop) return;
         const uint32_t slot = k % ns, ph = (k / ns) & 1u;
         const uint64_t tw = tr ? gtimer() : 0;
+        // at most lim copies in flight: tile k - lim has landed (its slot is
+        // not reused before tile k + ns - lim, so the parity is unambiguous)
+        if (lim < (uint32_t)ns && k >= lim &&
+            !wait_mbar(p, &s.full[(k - lim) % ns], ((k - lim) / ns) & 1u, abort)) { stop = true; return; }
         if (!wait_mbar(p, &s.empty[slot], ph ^ 1u, abort)) { stop = true; return; }
         if (tr) {
             pwait += gtimer() - tw;

@@ -30,6 +30,7 @@ MK_DBG_WAIT_LIMIT_NS = 2
 MK_DBG_TRACE = 3
 MK_DBG_GEMV_GROUPS = 4
 MK_DBG_TRACE_DETAIL = 5
+MK_DBG_INFLIGHT = 6
 MK_NOALLOC_ARGMAX_BLOCKS = 1024
 MK_NOALLOC_ARGMAX_MAX_N = MK_NOALLOC_ARGMAX_BLOCKS * 4096
 

@@ -227,6 +227,11 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
 /* MK_DBG_TRACE_DETAIL: 1 (default) = the trace also records the per-tile and
  * ring-wait slots; 0 = segment ends only (the least perturbed timing). */
 #define MK_DBG_TRACE_DETAIL 5
+/* MK_DBG_INFLIGHT: value = most weight tiles each CTA keeps in flight (issued,
+ * not yet landed) at once, 1..ring_stages (0 = the default).  Fewer bytes in
+ * flight per SM shorten the queues every other global access of the step
+ * (flags, activations) waits in, at the same streaming bandwidth. */
+#define MK_DBG_INFLIGHT 6
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
 const char* mk_strerror(int code);
