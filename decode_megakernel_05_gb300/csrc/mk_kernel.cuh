@@ -632,19 +632,27 @@ __device__ __forceinline__ float wide_row(const float* part, int R) {
 }
 
 // RMSNorm of x (fp32 global, or the bf16 embedding row when xb != nullptr) into
-// s.xv, with gain g (fp32).  The raw values of rows [keep0, keep0 + nkeep) are
-// also kept in `keep` (the residual this CTA adds later).  Returns the uniform
-// abort flag.
+// s.xv (split order, for the GEMV), with gain g (fp32).  The raw values of rows
+// [keep0, keep0 + nkeep) are also kept in `keep` (the residual this CTA adds
+// later).  All loads of a thread (x and gains) are issued together, so the
+// norm costs one L2 round trip.  Returns the uniform abort flag.
 template <int NPT>   // ceil(H / consumer threads) values per thread
 __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, const uint16_t* xb, const float* g,
                               bool abort_in, float* keep, int keep0, int nkeep) {
     const int H = p.geo.H, t = threadIdx.x;
+    float xr[NPT], gv[NPT];
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) {
+        const int i = t + k * MK_NCT;
+        xr[k] = i < H ? (xb ? bf2f(xb[i]) : __ldcg(x + i)) : 0.f;
+        gv[k] = i < H ? __ldg(g + i) : 0.f;
+    }
     float ss = 0.f;
-    for (int i = t; i < H; i += MK_NCT) {
-        float v = xb ? bf2f(xb[i]) : __ldcg(x + i);
-        s.xv[i] = v;
-        if ((unsigned)(i - keep0) < (unsigned)nkeep) keep[i - keep0] = v;
-        ss = fmaf(v, v, ss);
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) {
+        const int i = t + k * MK_NCT;
+        if ((unsigned)(i - keep0) < (unsigned)nkeep) keep[i - keep0] = xr[k];
+        ss = fmaf(xr[k], xr[k], ss);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
@@ -654,17 +662,10 @@ __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, 
 #pragma unroll
     for (int w = 0; w < MK_NCW; ++w) tot += s.red[w];
     const float inv = rsqrtf(tot / (float)H + p.eps);
-    float nv[NPT];
 #pragma unroll
     for (int k = 0; k < NPT; ++k) {
         const int i = t + k * MK_NCT;
-        if (i < H) nv[k] = s.xv[i] * inv * g[i];
-    }
-    ab = bar_or(ab);   // everyone has read the raw values before they are overwritten
-#pragma unroll
-    for (int k = 0; k < NPT; ++k) {
-        const int i = t + k * MK_NCT;
-        if (i < H) s.xv[xsplit(i, H)] = nv[k];   // split order for the GEMV
+        if (i < H) s.xv[xsplit(i, H)] = xr[k] * inv * gv[k];   // split order for the GEMV
     }
     return bar_or(ab);
 }
