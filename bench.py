@@ -182,9 +182,25 @@ def measured_peak():
         return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
+KERNEL_SOURCES = ("mk_kernel.cuh", "mk_kernel.cu", "mk_internal.h")
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the fused kernel's source files (the ncu traffic figure is
+    only valid for the kernel it was measured on)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "decode_megakernel_05_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def load_profile_traffic(workload: str):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary
-    (profiles/traffic_<workload>.txt, "key: value" lines), if any."""
+    (profiles/traffic_<workload>.txt, "key: value" lines), if any, and only if
+    it was measured on the kernel sources as they are now."""
     p = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
     try:
         out = {}
@@ -192,6 +208,8 @@ def load_profile_traffic(workload: str):
             if ":" in line and not line.lstrip().startswith("#"):
                 k, v = line.split(":", 1)
                 out[k.strip()] = v.strip()
+        if out.get("kernel_source_sha256") != kernel_source_hash():
+            return None
         return {"dram_bytes_per_launch": float(out["dram_bytes_per_launch"]), "kernel": out.get("kernel")}
     except Exception:
         return None

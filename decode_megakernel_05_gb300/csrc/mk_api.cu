@@ -233,7 +233,7 @@ struct mk_ctx {
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
     int gemv_groups = 0;
     int trace_detail = 1;
-    int inflight = 0;
+    int inflight = 0, inflight_lat = 0;
     int64_t wait_limit_ns = 1000000000LL;
     unsigned long long* trace = nullptr;
     // per-operator baseline
@@ -285,6 +285,7 @@ MkParams base_params(const mk_ctx* c) {
     p.gemv_groups = c->gemv_groups;
     p.trace_detail = c->trace_detail;
     p.inflight = c->inflight > 0 ? c->inflight : 3;
+    p.inflight_lat = c->inflight_lat > 0 ? c->inflight_lat : 1;
     p.wait_limit_ns = c->wait_limit_ns;
     p.trace = c->trace;
     p.out_idx = 0;
@@ -808,9 +809,9 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
         c->trace = reinterpret_cast<unsigned long long*>((uintptr_t)value);
         return MK_OK;
     }
-    if (knob == MK_DBG_INFLIGHT) {
+    if (knob == MK_DBG_INFLIGHT || knob == MK_DBG_INFLIGHT_LAT) {
         if (value < 0 || value > 16) return MK_ERR_INVALID_ARG;
-        c->inflight = (int)value;
+        (knob == MK_DBG_INFLIGHT ? c->inflight : c->inflight_lat) = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_TRACE_DETAIL) {

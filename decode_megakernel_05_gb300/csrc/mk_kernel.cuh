@@ -150,6 +150,7 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     int best_idx[64];
     uint32_t tile_bytes[16]; // bytes of the tile in each ring slot (schedule check)
     int slot_tile[16];       // index (in the step's tile stream) of the tile each slot holds
+    int streaming;           // consumers are in a streaming segment (sets the producer's in-flight limit)
     float cwt[MK_MAX_CPG_G]; // attention-combine weights [CPG][G]
     float cl[MK_MAX_CPG_G];  // attention partial sums l [CPG][G]
     uint4 stage[32];         // K and V rows of the current position (2 * hd bf16)
@@ -244,13 +245,17 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
     bool stop = false;
     unsigned long long pwait = 0;
     unsigned long long* tr = (MK_TRACE_ON && p.trace && p.trace_detail) ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
-    const uint32_t lim = (uint32_t)(p.inflight < ns ? p.inflight : ns);
+    const uint32_t lim_s = (uint32_t)(p.inflight < ns ? p.inflight : ns);
+    const uint32_t lim_l = (uint32_t)(p.inflight_lat < ns ? p.inflight_lat : ns);
     walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
         if (stop) return;
         const uint32_t slot = k % ns, ph = (k / ns) & 1u;
         const uint64_t tw = tr ? gtimer() : 0;
         // at most lim copies in flight: tile k - lim has landed (its slot is
-        // not reused before tile k + ns - lim, so the parity is unambiguous)
+        // not reused before tile k + ns - lim, so the parity is unambiguous).
+        // Few bytes in flight while the consumers are latency-bound keep the
+        // queues short for their flag polls and activation loads.
+        const uint32_t lim = *(volatile int*)&s.misc->streaming ? lim_s : lim_l;
         if (lim < (uint32_t)ns && k >= lim &&
             !wait_mbar(p, &s.full[(k - lim) % ns], ((k - lim) / ns) & 1u, abort)) { stop = true; return; }
         if (!wait_mbar(p, &s.empty[slot], ph ^ 1u, abort)) { stop = true; return; }
@@ -794,6 +799,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s.misc->abort = 0;
+        s.misc->streaming = 0;
         s.misc->copy_bytes = 0;
         s.misc->cwait = 0;
         s.misc->is_last = 0;
@@ -1055,6 +1061,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
         ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2, dr0, dr1 - dr0);
         MK_TRACE(16 * l + 10);
+        if (t == 0) *(volatile int*)&s.misc->streaming = 1;   // gate/up and down stream
         if (l == 3) trace_ring(p, ring, 4);   // everything before this layer's FFN (discarded)
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
@@ -1118,6 +1125,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
             }
             MK_TRACE(16 * l + 14);
+            if (t == 0) *(volatile int*)&s.misc->streaming = 0;
             if (l == 3) trace_ring(p, ring, 1);
             // fold the phases: phase q adds what phase q+1 left in xv (element
             // e of chunk c at xv[e * NCH + c]: lane-consecutive, conflict free)
@@ -1171,6 +1179,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         const float* xl = xa + (size_t)(2 * L - 1) * state;
         ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0);
         MK_TRACE(16 * L + 0);
+        if (t == 0) *(volatile int*)&s.misc->streaming = 1;   // the LM head streams
         if (c == 0 && !ab)
             for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv[xsplit(i, H)];
         float bv = -INFINITY;

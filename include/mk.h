@@ -228,10 +228,16 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
  * ring-wait slots; 0 = segment ends only (the least perturbed timing). */
 #define MK_DBG_TRACE_DETAIL 5
 /* MK_DBG_INFLIGHT: value = most weight tiles each CTA keeps in flight (issued,
- * not yet landed) at once, 1..ring_stages (0 = the default).  Fewer bytes in
+ * not yet landed) at once during the streaming segments, 1..16 (0 = the
+ * default, 3).  Fewer bytes in
  * flight per SM shorten the queues every other global access of the step
  * (flags, activations) waits in, at the same streaming bandwidth. */
 #define MK_DBG_INFLIGHT 6
+/* MK_DBG_INFLIGHT_LAT: the same limit while the consumers are in a
+ * latency-bound segment (norms, QKV, attention, O-proj, flag waits); the first
+ * limit applies during the streaming segments (gate/up, down, LM head).
+ * 0 = the default (1). */
+#define MK_DBG_INFLIGHT_LAT 7
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
 const char* mk_strerror(int code);
