@@ -225,7 +225,8 @@ struct mk_ctx {
     MkCtaPlan* d_plans = nullptr;
     uint16_t *embed = nullptr, *kc = nullptr, *vc = nullptr;
     float *attn_norm = nullptr, *ffn_norm = nullptr, *final_norm = nullptr, *rope_cos = nullptr, *rope_sin = nullptr;
-    float *qbuf = nullptr, *part_ml = nullptr, *part_acc = nullptr, *xacc = nullptr, *hidden = nullptr;
+    uint64_t *qll = nullptr, *kvll = nullptr, *partll = nullptr;
+    float *xacc = nullptr, *hidden = nullptr;
     uint32_t *cnt = nullptr, *status = nullptr, *seq = nullptr;
     unsigned long long* amax = nullptr;
     int32_t *next_token = nullptr, *tokens_dev = nullptr, *prompt_dev = nullptr;
@@ -270,9 +271,9 @@ MkParams base_params(const mk_ctx* c) {
     p.vc = c->vc;
     p.rope_cos = c->rope_cos;
     p.rope_sin = c->rope_sin;
-    p.qbuf = c->qbuf;
-    p.part_ml = c->part_ml;
-    p.part_acc = c->part_acc;
+    p.qll = c->qll;
+    p.kvll = c->kvll;
+    p.partll = c->partll;
     p.xacc = c->xacc;
     p.hidden = c->hidden;
     p.cnt = c->cnt;
@@ -446,6 +447,8 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
     const MkGeom& g = c->geo;
     const size_t L = g.L, H = g.H, V = g.V;
     const size_t kv_elems = L * g.kvh * (size_t)g.max_seq * g.hd;
+    const size_t qll_bytes = L * g.qh * (size_t)g.hd * 8, kvll_bytes = L * g.kvh * 2 * (size_t)g.hd * 8;
+    const size_t partll_bytes = L * g.kvh * g.CPG * ((size_t)g.G * g.hd + 2 * g.G) * 8;
     if ((rc = c->dalloc(&c->arena, (size_t)c->arena_bytes)) ||
         (rc = c->dalloc(&c->d_plans, sizeof(MkCtaPlan) * g.nC)) ||
         (rc = c->dalloc(&c->embed, V * H * 2)) || (rc = c->dalloc(&c->kc, kv_elems * 2)) ||
@@ -453,9 +456,8 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         (rc = c->dalloc(&c->ffn_norm, L * H * 4)) || (rc = c->dalloc(&c->final_norm, H * 4)) ||
         (rc = c->dalloc(&c->rope_cos, (size_t)g.max_seq * (g.hd / 2) * 4)) ||
         (rc = c->dalloc(&c->rope_sin, (size_t)g.max_seq * (g.hd / 2) * 4)) ||
-        (rc = c->dalloc(&c->qbuf, L * g.qh * g.hd * 4)) ||
-        (rc = c->dalloc(&c->part_ml, L * g.kvh * g.CPG * g.G * 2 * 4)) ||
-        (rc = c->dalloc(&c->part_acc, L * g.kvh * g.CPG * g.G * (size_t)g.hd * 4)) ||
+        (rc = c->dalloc(&c->qll, qll_bytes)) || (rc = c->dalloc(&c->kvll, kvll_bytes)) ||
+        (rc = c->dalloc(&c->partll, partll_bytes)) ||
         (rc = c->dalloc(&c->xacc, 2 * 2 * L * H * 4)) || (rc = c->dalloc(&c->hidden, H * 4)) ||
         (rc = c->dalloc(&c->cnt, (size_t)mk_cnt_total(g) * 4)) || (rc = c->dalloc(&c->status, 4)) ||
         (rc = c->dalloc(&c->seq, 4)) || (rc = c->dalloc(&c->amax, 8)) || (rc = c->dalloc(&c->next_token, 4)) ||
@@ -465,7 +467,8 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
     cudaStream_t st = nullptr;
     if ((e = cudaMemcpy(c->d_plans, c->plans.data(), sizeof(MkCtaPlan) * g.nC, cudaMemcpyHostToDevice)) ||
         (e = cudaMemset(c->kc, 0, kv_elems * 2)) || (e = cudaMemset(c->vc, 0, kv_elems * 2)) ||
-        (e = cudaMemset(c->xacc, 0, 2 * 2 * L * H * 4)) || (e = cudaMemset(c->cnt, 0, (size_t)mk_cnt_total(g) * 4)) ||
+        (e = cudaMemset(c->xacc, 0, 2 * 2 * L * H * 4)) || (e = cudaMemset(c->qll, 0, qll_bytes)) ||
+        (e = cudaMemset(c->kvll, 0, kvll_bytes)) || (e = cudaMemset(c->partll, 0, partll_bytes)) || (e = cudaMemset(c->cnt, 0, (size_t)mk_cnt_total(g) * 4)) ||
         (e = cudaMemset(c->status, 0, 4)) || (e = cudaMemset(c->seq, 0, 4)) || (e = cudaMemset(c->amax, 0, 8)) ||
         (e = cudaMemset(c->next_token, 0, 4)) || (e = cudaMemset(c->tokens_dev, 0, (size_t)g.max_seq * 4)))
         return fail(cuda_fail(e, "context init"));

@@ -35,7 +35,7 @@
 #define MK_BLOCK ((MK_NCW + 2) * 32) // 448 threads: at most 4 warps per SM sub-partition (128 registers)
 
 #define MK_MAX_CPG_G 640               // CTAs per group x query heads per group (combine weights)
-#define MK_COMBINE_LOADS 8            // float4 loads per thread in the attention combine
+#define MK_COMBINE_LOADS 5            // float4 loads per thread in the attention combine
 #define MK_MISC_BYTES 6656
 #define MK_MAX_H 8192                 // largest hidden size the kernels take
 
@@ -147,9 +147,12 @@ struct MkParams {
     uint16_t* vc;
     const float* rope_cos;       // [max_seq][hd/2]
     const float* rope_sin;
-    float* qbuf;                 // [L][qh*hd]
-    float* part_ml;              // [L][kvh][CPG][G][2]
-    float* part_acc;             // [L][kvh][CPG][G][hd]
+    // Tagged words (low 32 bits: fp32 value, high 32 bits: launch tag = seq + 1).
+    // A reader polls the words it needs until every tag is this launch's: the
+    // data carries its own ready flag (no fence, counter or separate poll).
+    uint64_t* qll;               // [L][qh*hd] rotated q
+    uint64_t* kvll;              // [L][kvh][2][hd] K (rotated) and V of the current position, bf16-rounded
+    uint64_t* partll;            // [L][kvh][CPG][G*hd + 2G] attention partials: acc[G][hd], then (m, l) per head
     float* xacc;                 // [2][2L][H] residual states (parity double-buffered)
     float* hidden;               // [H]
     uint32_t* cnt;               // flag counters (see mk_cnt_*) then the done counter

@@ -105,6 +105,27 @@ __device__ __forceinline__ void red_add_v4(float* p, float4 v) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
 }
+// Tagged words: fp32 value in the low half, the launch tag in the high half.
+// A naturally aligned 64-bit access is single-copy atomic, so a reader that
+// sees this launch's tag in a word also sees the value written with it.
+__device__ __forceinline__ uint64_t ll_pack(float v, uint32_t tag) {
+    return ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+}
+__device__ __forceinline__ void st_ll(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_ll2(uint64_t* p, uint64_t a, uint64_t b) {
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ ulonglong2 ld_ll2(const uint64_t* p) {
+    ulonglong2 r;
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(r.x), "=l"(r.y) : "l"(p) : "memory");
+    return r;
+}
+__device__ __forceinline__ bool ll_ok(const ulonglong2 w, uint32_t tag) {
+    return ((uint32_t)(w.x >> 32) == tag) & ((uint32_t)(w.y >> 32) == tag);
+}
+
 // Barrier over the consumer threads that also ORs a per-thread flag: every
 // participant gets the same answer, so an abort decision is uniform.
 __device__ __forceinline__ bool bar_or(bool f) {
@@ -151,6 +172,8 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     uint32_t tile_bytes[16]; // bytes of the tile in each ring slot (schedule check)
     int slot_tile[16];       // index (in the step's tile stream) of the tile each slot holds
     int streaming;           // consumers are in a streaming segment (sets the producer's in-flight limit)
+    uint32_t tag;            // this launch's tag for tagged words (sequence number + 1)
+    MkCtaPlan plan;          // this CTA's plan (read from here: keeps registers free in the layer loop)
     float cwt[MK_MAX_CPG_G]; // attention-combine weights [CPG][G]
     float cl[MK_MAX_CPG_G];  // attention partial sums l [CPG][G]
     uint4 stage[32];         // K and V rows of the current position (2 * hd bf16)
@@ -219,6 +242,35 @@ __device__ bool wait_mbar(const MkParams& p, uint64_t* b, uint32_t parity, volat
         }
     }
     return true;
+}
+
+// Between polls of tagged words: false (and the abort bit, and on time-out the
+// timeout bit) when the wait must end.  t0 = 0 on the first call.
+__device__ __forceinline__ bool ll_backoff(const MkParams& p, uint64_t& t0) {
+    if (*(volatile uint32_t*)p.status & MK_ST_ABORT) return false;
+    const uint64_t now = gtimer();
+    if (t0 == 0) t0 = now;
+    else if (now - t0 > (uint64_t)p.wait_limit_ns) {
+        atomicOr(p.status, MK_ST_TIMEOUT | MK_ST_ABORT);
+        return false;
+    }
+    __nanosleep(64);
+    return true;
+}
+// Reads 8 tagged words (16-byte aligned) once all carry `tag`.
+__device__ __forceinline__ bool ll_read8(const MkParams& p, const uint64_t* src, uint32_t tag, float v[8]) {
+    uint64_t t0 = 0;
+    for (;;) {
+        const ulonglong2 a = ld_ll2(src), b = ld_ll2(src + 2), c = ld_ll2(src + 4), d = ld_ll2(src + 6);
+        if (ll_ok(a, tag) & ll_ok(b, tag) & ll_ok(c, tag) & ll_ok(d, tag)) {
+            v[0] = __uint_as_float((uint32_t)a.x); v[1] = __uint_as_float((uint32_t)a.y);
+            v[2] = __uint_as_float((uint32_t)b.x); v[3] = __uint_as_float((uint32_t)b.y);
+            v[4] = __uint_as_float((uint32_t)c.x); v[5] = __uint_as_float((uint32_t)c.y);
+            v[6] = __uint_as_float((uint32_t)d.x); v[7] = __uint_as_float((uint32_t)d.y);
+            return true;
+        }
+        if (!ll_backoff(p, t0)) return false;
+    }
 }
 
 // Arrive on a flag counter (thread 0 of the consumers, after a consumer barrier).
@@ -789,7 +841,6 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
     const int t = threadIdx.x;
     const int c = blockIdx.x;
-    const MkCtaPlan pl = p.plans[c];
 
     if (t == 0) {
         for (int i = 0; i < g.ns; ++i) {
@@ -809,10 +860,16 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             tok = 0;
         }
         s.misc->token = tok;
-        s.misc->par = (int)(*(volatile uint32_t*)p.seq & 1u);
+        s.misc->plan = p.plans[c];
+        {
+            const uint32_t sq = *(volatile uint32_t*)p.seq;
+            s.misc->par = (int)(sq & 1u);
+            s.misc->tag = sq + 1u;
+        }
         for (int h = 0; h < 8; ++h) { s.misc->mrun[h] = -INFINITY; s.misc->lrun[h] = 0.f; s.misc->alpha[h] = 0.f; }
     }
     __syncthreads();
+    const MkCtaPlan& pl = s.misc->plan;
 
     const int warp = t >> 5;
     if (warp == MK_PRODUCER_WARP) {
@@ -827,6 +884,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     // ======================= consumers (MK_NCT threads) =======================
     const int H = g.H, L = g.L, hd2 = HD / 2;
     const int par = s.misc->par, token = s.misc->token;
+    // the launch tag of the tagged words is read from s.misc->tag where used
+    // (the layer loop runs at the register limit)
     const size_t state = (size_t)H;
     float* xa = p.xacc + (size_t)par * 2 * L * state;              // this launch's residual states
     {   // zero the other parity's states for the next launch
@@ -870,20 +929,24 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     const float a2 = a * cs - b * sn, b2 = b * cs + a * sn;
                     a = a2; b = b2;
                 }
+                // q and the current K/V go out as tagged words (the debug knob
+                // can withhold them, so that the readers' bounded wait runs out)
+                const bool pub = !(p.dbg_skip_sync == 4 * l + 0 && p.dbg_skip_cta == c);
                 if (slot < G) {
-                    float* q = p.qbuf + (size_t)l * g.qh * HD + (size_t)(pl.g * G + slot) * HD;
-                    q[d] = a; q[d + hd2] = b;
+                    uint64_t* q = p.qll + (size_t)l * g.qh * HD + (size_t)(pl.g * G + slot) * HD;
+                    if (pub) { st_ll(q + d, ll_pack(a, s.misc->tag)); st_ll(q + d + hd2, ll_pack(b, s.misc->tag)); }
                 } else {
                     uint16_t* dst = (slot == G ? p.kc : p.vc) +
                                     (((size_t)l * g.kvh + pl.g) * g.max_seq + p.pos) * HD;
-                    dst[d] = f2bf(a); dst[d + hd2] = f2bf(b);
+                    const uint16_t ab16 = f2bf(a), bb16 = f2bf(b);
+                    dst[d] = ab16; dst[d + hd2] = bb16;
+                    uint64_t* kv = p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (slot - G)) * HD;
+                    if (pub) { st_ll(kv + d, ll_pack(bf2f(ab16), s.misc->tag)); st_ll(kv + d + hd2, ll_pack(bf2f(bb16), s.misc->tag)); }
                 }
             }
         }
         ab = bar_or(ab);
         MK_TRACE(16 * l + 3);
-        if (t == 0 && !ab) arrive(p, mk_cnt_A(g, l, pl.g), 4 * l + 0);
-        ab = sync_wait(p, mk_cnt_A(g, l, pl.g), (uint32_t)g.CPG, ab);
         MK_TRACE(16 * l + 4);
 
         // ---------------- segment B: split-K attention over this CTA's positions
@@ -891,23 +954,29 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             using A = Attn<HD, G>;
             const int h_ = (t % A::TPP) / A::DC, dc_ = t % A::DC;
             float qr[8], acc[8];
+            bool late = false;
             if (!ab) {
-                // this thread's 8 query dims straight from L2 (written by the group this launch)
-                const float4* qs = reinterpret_cast<const float4*>(
-                    p.qbuf + (size_t)l * g.qh * HD + ((size_t)pl.g * G + h_) * HD + dc_ * 8);
-                const float4 qa = __ldcg(qs), qb = __ldcg(qs + 1);
-                qr[0] = qa.x * qscale; qr[1] = qa.y * qscale; qr[2] = qa.z * qscale; qr[3] = qa.w * qscale;
-                qr[4] = qb.x * qscale; qr[5] = qb.y * qscale; qr[6] = qb.z * qscale; qr[7] = qb.w * qscale;
+                // this thread's 8 query dims: tagged words written by the group this launch
+                float qv[8];
+                late = !ll_read8(p, p.qll + (size_t)l * g.qh * HD + ((size_t)pl.g * G + h_) * HD + dc_ * 8, s.misc->tag, qv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qr[e] = qv[e] * qscale;
                 if (t < G) { s.misc->mrun[t] = -INFINITY; s.misc->lrun[t] = 0.f; }
-                if (has_cur && t < HD / 4) {   // stage K[pos], V[pos] written by this group this launch
-                    const size_t off = (((size_t)l * g.kvh + pl.g) * g.max_seq + p.pos) * HD;
-                    const uint4* src = reinterpret_cast<const uint4*>((t < HD / 8 ? p.kc : p.vc) + off);
-                    s.misc->stage[t] = __ldcg(src + (t % (HD / 8)));
+                if (has_cur && t < HD / 4 && !late) {   // stage K[pos], V[pos] (bf16) from their tagged copies
+                    float kv[8];
+                    late = !ll_read8(p, p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (t < HD / 8 ? 0 : 1)) * HD +
+                                            (t % (HD / 8)) * 8, s.misc->tag, kv);
+                    uint4 w;
+                    w.x = (uint32_t)f2bf(kv[0]) | ((uint32_t)f2bf(kv[1]) << 16);
+                    w.y = (uint32_t)f2bf(kv[2]) | ((uint32_t)f2bf(kv[3]) << 16);
+                    w.z = (uint32_t)f2bf(kv[4]) | ((uint32_t)f2bf(kv[5]) << 16);
+                    w.w = (uint32_t)f2bf(kv[6]) | ((uint32_t)f2bf(kv[7]) << 16);
+                    s.misc->stage[t] = w;
                 }
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-            ab = bar_or(ab);
+            ab = bar_or(ab || late);
             // Blocks of up to KB past positions from the ring; the last CTA of the
             // group appends the current position (staged from global) to its
             // last block, or runs it as a block of its own when it has no past.
@@ -942,32 +1011,29 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
         }
         ab = bar_or(ab);
-        if (!ab) {
-            const size_t pbase = (((size_t)l * g.kvh + pl.g) * g.CPG + pl.i) * G;
+        constexpr int PSTR = G * HD + 2 * G;                   // tagged words per partial
+        if (!ab && !(p.dbg_skip_sync == 4 * l + 1 && p.dbg_skip_cta == c)) {
+            uint64_t* dst = p.partll + (((size_t)l * g.kvh + pl.g) * g.CPG + pl.i) * PSTR;
             for (int i = t; i < G * HD; i += MK_NCT) {
                 float a = 0.f;
 #pragma unroll
                 for (int q = 0; q < Attn<HD, G>::PPP; ++q) a += s.xv[q * (G * HD) + i];
-                p.part_acc[pbase * HD + i] = a;
+                st_ll(dst + i, ll_pack(a, s.misc->tag));
             }
-            if (t < G) {
-                p.part_ml[(pbase + t) * 2 + 0] = s.misc->mrun[t];
-                p.part_ml[(pbase + t) * 2 + 1] = s.misc->lrun[t];
-            }
+            if (t < G) st_ll2(dst + G * HD + 2 * t, ll_pack(s.misc->mrun[t], s.misc->tag), ll_pack(s.misc->lrun[t], s.misc->tag));
         }
         ab = bar_or(ab);
         MK_TRACE(16 * l + 5);
         MK_TRACE_CWAIT(8 * l + 1);
-        if (t == 0 && !ab) arrive(p, mk_cnt_B(g, l, pl.g), 4 * l + 1);
-        ab = sync_wait(p, mk_cnt_B(g, l, pl.g), (uint32_t)g.CPG, ab);
         MK_TRACE(16 * l + 6);
 
         // combine the group's partials -> o (the G heads of this KV group):
         // weights exp2(m_j - M) / sum_j exp2(m_j - M) l_j.  A team of CT lanes
         // owns one float4 of o and takes the partials j = lane (mod CT); the
-        // team sums with shuffles.  The first CB loads of every thread are
-        // issued together with the (m, l) loads, so a short group costs one
-        // L2 round trip.
+        // team sums with shuffles.  The partials are tagged words polled
+        // directly (no flag): the first CB of every thread and the (m, l)
+        // words go out in one poll, so a short group costs one L2 round trip
+        // once its last member has written.
         if (!ab) {
             constexpr int NO4 = G * HD / 4;                     // float4s of o
             constexpr int CT = (NO4 * 32 <= MK_NCT) ? 32 : (NO4 * 16 <= MK_NCT) ? 16 : (NO4 * 8 <= MK_NCT) ? 8
@@ -975,25 +1041,53 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             constexpr int CB = MK_COMBINE_LOADS;
             constexpr int NPASS = (NO4 * CT + MK_NCT - 1) / MK_NCT;   // team passes over o
             static_assert(NPASS == 1 || CT == 1, "combine mapping");
-            const size_t gbase = ((size_t)l * g.kvh + pl.g) * g.CPG * G;
-            const float4* pa = reinterpret_cast<const float4*>(p.part_acc + gbase * HD);
+            const uint64_t* pg = p.partll + ((size_t)l * g.kvh + pl.g) * g.CPG * PSTR;   // this group's partials
             const int cl_ = t % CT;
             float4 v[CB];
-            {
-                const int o4 = t / CT;
+            bool late = false;
+            // (o4, batch k0) -> v[]: the tagged words of partials j = cl_ + (k0 + k) * CT,
+            // polled until every one carries this launch's tag
+            auto load_batch_once = [&](int o4, int k0) {
+                bool ok = true;
 #pragma unroll
                 for (int k = 0; k < CB; ++k) {
-                    const int j = cl_ + k * CT;
-                    v[k] = (o4 < NO4 && j < g.CPG) ? __ldcg(pa + (size_t)j * NO4 + o4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const int j = cl_ + (k0 + k) * CT;
+                    if (o4 < NO4 && j < g.CPG) {
+                        const uint64_t* w = pg + (size_t)j * PSTR + o4 * 4;
+                        const ulonglong2 a = ld_ll2(w), b = ld_ll2(w + 2);
+                        ok = ok & ll_ok(a, s.misc->tag) & ll_ok(b, s.misc->tag);
+                        v[k] = make_float4(__uint_as_float((uint32_t)a.x), __uint_as_float((uint32_t)a.y),
+                                           __uint_as_float((uint32_t)b.x), __uint_as_float((uint32_t)b.y));
+                    } else {
+                        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+                return ok;
+            };
+            auto load_batch = [&](int o4, int k0) {
+                uint64_t t0 = 0;
+                for (;;) {
+                    if (load_batch_once(o4, k0)) return true;
+                    if (!ll_backoff(p, t0)) return false;
+                }
+            };
+            float* cw = s.red;                       // [CPG*G] maxima (red is free here)
+            {   // first batch and this thread's (m, l) words in one poll: one round trip
+                uint64_t t0 = 0;
+                for (;;) {
+                    bool ok = load_batch_once(t / CT, 0);
+                    for (int i = t; i < g.CPG * G; i += MK_NCT) {
+                        const ulonglong2 w = ld_ll2(pg + (size_t)(i / G) * PSTR + G * HD + 2 * (i % G));
+                        ok = ok & ll_ok(w, s.misc->tag);
+                        cw[i] = __uint_as_float((uint32_t)w.x);
+                        s.misc->cl[i] = __uint_as_float((uint32_t)w.y);
+                    }
+                    if (ok) break;
+                    if (!ll_backoff(p, t0)) { late = true; break; }
                 }
             }
-            float* cw = s.red;                       // [CPG*G] maxima (red is free here)
-            for (int i = t; i < g.CPG * G; i += MK_NCT) {
-                cw[i] = __ldcg(p.part_ml + (gbase + i) * 2);
-                s.misc->cl[i] = __ldcg(p.part_ml + (gbase + i) * 2 + 1);
-            }
-            bar_or(false);
-            if (t < G) {
+            if (bar_or(late)) ab = true;
+            if (!ab && t < G) {
                 float mx = -INFINITY;
                 for (int j = 0; j < g.CPG; ++j) mx = fmaxf(mx, cw[j * G + t]);
                 float den = 0.f;
@@ -1007,18 +1101,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
             bar_or(false);
 #pragma unroll 1
-            for (int ps = 0; ps < NPASS; ++ps) {
+            for (int ps = 0; ps < NPASS && !ab; ++ps) {
                 const int o4 = t / CT + ps * (MK_NCT / CT);
                 const int h = (o4 * 4) / HD;
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int k0 = 0; k0 * CT < g.CPG; k0 += CB) {
                     if (k0 > 0 || ps > 0) {   // further batches (large groups or several passes)
-#pragma unroll
-                        for (int k = 0; k < CB; ++k) {
-                            const int j = cl_ + (k0 + k) * CT;
-                            v[k] = (o4 < NO4 && j < g.CPG) ? __ldcg(pa + (size_t)j * NO4 + o4)
-                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
+                        if (!load_batch(o4, k0)) late = true;
                     }
 #pragma unroll
                     for (int k = 0; k < CB; ++k) {
@@ -1042,6 +1131,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                         make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
                 }
             }
+            if (late) ab = true;      // made uniform by the barrier below
         }
         ab = bar_or(ab);
         MK_TRACE(16 * l + 7);
