@@ -232,7 +232,6 @@ struct mk_ctx {
     int32_t *next_token = nullptr, *tokens_dev = nullptr, *prompt_dev = nullptr;
     // debug
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
-    int gemv_groups = 0;
     int trace_detail = 1;
     int inflight = 0, inflight_lat = 0;
     int64_t wait_limit_ns = 1000000000LL;
@@ -283,7 +282,6 @@ MkParams base_params(const mk_ctx* c) {
     p.seq = c->seq;
     p.dbg_skip_cta = c->dbg_skip_cta;
     p.dbg_skip_sync = c->dbg_skip_sync;
-    p.gemv_groups = c->gemv_groups;
     p.trace_detail = c->trace_detail;
     p.inflight = c->inflight > 0 ? c->inflight : 3;
     p.inflight_lat = c->inflight_lat > 0 ? c->inflight_lat : 1;
@@ -820,11 +818,6 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_TRACE_DETAIL) {
         if (value != 0 && value != 1) return MK_ERR_INVALID_ARG;
         c->trace_detail = (int)value;
-        return MK_OK;
-    }
-    if (knob == MK_DBG_GEMV_GROUPS) {
-        if (value != 0 && value != 1 && value != 2 && value != 3 && value != 6) return MK_ERR_INVALID_ARG;
-        c->gemv_groups = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_WAIT_LIMIT_NS) {

@@ -167,7 +167,6 @@ struct MkParams {
     int32_t* tokens_out;         // greedy output buffer or nullptr
     int32_t out_idx;
     int32_t dbg_skip_cta, dbg_skip_sync;
-    int32_t gemv_groups;         // warp groups taking turns on hidden-width GEMV tiles (0 = default)
     int32_t trace_detail;        // with trace: also per-tile and ring-wait slots
     int32_t inflight;            // most tiles in flight per CTA in streaming segments (>= ns: no limit)
     int32_t inflight_lat;        // the same in latency-bound segments

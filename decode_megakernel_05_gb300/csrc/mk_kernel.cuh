@@ -666,17 +666,13 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
     }
     return bar_or(ab);
 }
-// Runtime choice of the group count (1, 2, 3 or 6; others use the default 3).
+// Three groups of four warps measured fastest of 1, 2, 3 and 6 groups on the
+// 1B shape; a compile-time choice keeps one copy of the loop in the layer code.
+constexpr int MK_GEMV_GROUPS = 3;
 template <int MH>
 __device__ __forceinline__ bool gemv_fifo(const MkParams& p, const Smem& s, Ring& ring, const float* xs, int nrows,
                                           int TR, bool ab, float* part) {
-    switch (p.gemv_groups) {
-        case 1: if constexpr (WideGemv<MH, 1>::ok) return gemv_wide<MH, 1>(p, s, ring, xs, nrows, TR, ab, part); break;
-        case 2: if constexpr (WideGemv<MH, 2>::ok) return gemv_wide<MH, 2>(p, s, ring, xs, nrows, TR, ab, part); break;
-        case 6: if constexpr (WideGemv<MH, 6>::ok) return gemv_wide<MH, 6>(p, s, ring, xs, nrows, TR, ab, part); break;
-        default: break;
-    }
-    return gemv_wide<MH, 3>(p, s, ring, xs, nrows, TR, ab, part);
+    return gemv_wide<MH, MK_GEMV_GROUPS>(p, s, ring, xs, nrows, TR, ab, part);
 }
 // Sum of the NKB column-block partials of row R of a FIFO GEMV phase.
 template <int MH>

@@ -28,7 +28,6 @@ MK_ERR_UNSUPPORTED = -7
 MK_DBG_SKIP_ARRIVAL = 1
 MK_DBG_WAIT_LIMIT_NS = 2
 MK_DBG_TRACE = 3
-MK_DBG_GEMV_GROUPS = 4
 MK_DBG_TRACE_DETAIL = 5
 MK_DBG_INFLIGHT = 6
 MK_DBG_INFLIGHT_LAT = 7

@@ -220,10 +220,6 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
  * tiles of the step's stream: 2560 + k issue time, 3072 + k time a reader got
  * it, 3584 + k time a reader released it. */
 #define MK_DBG_TRACE 3
-/* MK_DBG_GEMV_GROUPS: value = number of consumer-warp groups that take turns on
- * the tiles of the hidden-width GEMVs (QKV, gate/up): 1, 2, 3 or 6 (0 = the
- * default, 3).  Values the shape cannot use fall back to the default. */
-#define MK_DBG_GEMV_GROUPS 4
 /* MK_DBG_TRACE_DETAIL: 1 (default) = the trace also records the per-tile and
  * ring-wait slots; 0 = segment ends only (the least perturbed timing). */
 #define MK_DBG_TRACE_DETAIL 5

@@ -141,15 +141,13 @@ def test_full_size_workloads_sampled(name, n_steps):
 WIDE = synth.ModelShape(2, 2048, 32, 8, 64, 2304, 4099, 1e-5, 500000.0, False)
 
 
-@pytest.mark.parametrize("groups", [1, 2, 3, 6])
-def test_hidden_width_gemv_groups(groups):
-    """Every warp-group split of the hidden-width GEMVs (QKV, gate/up) on the
-    1B-like width H=2048 (four column blocks per row, transposed butterfly)
-    and on H=512, with ragged FFN slices and LM rows."""
-    for shape, seed in ((WIDE, 41), (MID, 43)):
-        m, dec, orc = make(shape, seed, 256, gains="normal", std=0.03)
-        dec.set_debug(mk.MK_DBG_GEMV_GROUPS, groups)
-        rep = run_teacher_forced(dec, orc, synth.uniform_tokens(6, shape.vocab, seed, 3), 0, 10)
-        print(groups, shape.hidden, rep.summary())
-        rep.check()
-        dec.close()
+@pytest.mark.parametrize("shape,seed", [(WIDE, 41), (MID, 43)], ids=["H2048", "H512"])
+def test_hidden_width_gemv(shape, seed):
+    """The hidden-width GEMVs (QKV, gate/up: column blocks with activations in
+    registers, transposed butterfly, groups taking turns on tiles) on the
+    1B-like width H=2048 and on H=512, with ragged FFN slices and LM rows."""
+    m, dec, orc = make(shape, seed, 256, gains="normal", std=0.03)
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(6, shape.vocab, seed, 3), 0, 10)
+    print(shape.hidden, rep.summary())
+    rep.check()
+    dec.close()
