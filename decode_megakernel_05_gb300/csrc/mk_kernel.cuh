@@ -159,6 +159,14 @@ __device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(
 
 // ------------------------------------------------------------------ shared state
 
+// Work split of a warp-row GEMV phase (O-proj, LM head), computed once per
+// launch: the tile count, rows per lane group and pass, warps per group, and
+// each warp's group and index in it (the divisions stay out of the layer loop).
+struct GemvCfg {
+    int16_t ntiles, rw, wpg, ngrp;
+    int8_t grp[MK_NCW], wg[MK_NCW];
+};
+
 struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     int abort;               // CTA-local: consumers gave up (producers stop)
     int token;
@@ -174,6 +182,7 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     int streaming;           // consumers are in a streaming segment (sets the producer's in-flight limit)
     uint32_t tag;            // this launch's tag for tagged words (sequence number + 1)
     MkCtaPlan plan;          // this CTA's plan (read from here: keeps registers free in the layer loop)
+    GemvCfg ocfg, lmcfg;     // work split of the O-proj and LM-head phases
     float cwt[MK_MAX_CPG_G]; // attention-combine weights [CPG][G]
     float cl[MK_MAX_CPG_G];  // attention partial sums l [CPG][G]
     uint4 stage[32];         // K and V rows of the current position (2 * hd bf16)
@@ -299,17 +308,20 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
     unsigned long long* tr = (MK_TRACE_ON && p.trace && p.trace_detail) ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
     const uint32_t lim_s = (uint32_t)(p.inflight < ns ? p.inflight : ns);
     const uint32_t lim_l = (uint32_t)(p.inflight_lat < ns ? p.inflight_lat : ns);
+    uint32_t slot = 0, ph = 0;   // k mod ns and floor(k / ns) mod 2, kept incrementally
     walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
         if (stop) return;
-        const uint32_t slot = k % ns, ph = (k / ns) & 1u;
         const uint64_t tw = tr ? gtimer() : 0;
         // at most lim copies in flight: tile k - lim has landed (its slot is
         // not reused before tile k + ns - lim, so the parity is unambiguous).
         // Few bytes in flight while the consumers are latency-bound keep the
         // queues short for their flag polls and activation loads.
         const uint32_t lim = *(volatile int*)&s.misc->streaming ? lim_s : lim_l;
-        if (lim < (uint32_t)ns && k >= lim &&
-            !wait_mbar(p, &s.full[(k - lim) % ns], ((k - lim) / ns) & 1u, abort)) { stop = true; return; }
+        if (lim < (uint32_t)ns && k >= lim) {
+            const bool wrap = slot < lim;   // tile k - lim sits in the previous round of slots
+            const uint32_t s2 = wrap ? slot + ns - lim : slot - lim, ph2 = wrap ? ph ^ 1u : ph;
+            if (!wait_mbar(p, &s.full[s2], ph2, abort)) { stop = true; return; }
+        }
         if (!wait_mbar(p, &s.empty[slot], ph ^ 1u, abort)) { stop = true; return; }
         if (tr) {
             pwait += gtimer() - tw;
@@ -321,6 +333,7 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
         mbar_expect_tx(&s.full[slot], bytes);
         bulk_g2s(s.ring + (size_t)slot * slot_bytes, src, bytes, &s.full[slot], pol);
         ++k;
+        if (++slot == (uint32_t)ns) { slot = 0; ph ^= 1u; }
         *(volatile unsigned long long*)&s.misc->copy_bytes += bytes;
     });
     if (tr) tr[1535] = gtimer();
@@ -376,10 +389,17 @@ __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const 
 // Consumer-side cursor over the ring.
 struct Ring {
     uint32_t k = 0;
+    uint32_t sp = 0;   // slot k mod ns (low 16 bits) and phase floor(k / ns) mod 2 (bit 16), kept incrementally
     // trace only (lane 0 of each warp): ns spent taking tiles, between take
     // and release, and releasing
     unsigned long long t_take = 0, t_comp = 0, t_rel = 0, t_mark = 0;
-    __device__ __forceinline__ uint32_t slot(int ns) const { return k % ns; }
+    __device__ __forceinline__ uint32_t slot() const { return sp & 0xFFFFu; }
+    __device__ __forceinline__ uint32_t ph() const { return sp >> 16; }
+    // next tile (no division: slot and phase wrap by comparison)
+    __device__ __forceinline__ void advance(int ns) {
+        ++k;
+        sp = ((sp & 0xFFFFu) + 1u == (uint32_t)ns) ? ((sp ^ 0x10000u) & 0x10000u) : sp + 1u;
+    }
 };
 
 // Ring protocol.  Tile k of the step's stream lives in slot k % ns.  A warp
@@ -391,8 +411,7 @@ struct Ring {
 // that do not read a tile only advance their cursor.
 __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t expect_bytes,
                                           const uint8_t*& tile) {
-    const int ns = p.geo.ns;
-    const uint32_t slot = rg.k % ns, ph = (rg.k / ns) & 1u;
+    const uint32_t slot = rg.slot(), ph = rg.ph();
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {
         const uint64_t tw = (MK_TRACE_ON && p.trace && p.trace_detail) ? gtimer() : 0;
@@ -434,14 +453,14 @@ __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, R
     const uint64_t t2 = (MK_TRACE_ON && p.trace && p.trace_detail && (threadIdx.x & 31) == 0) ? gtimer() : 0;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
-        mbar_arrive(&s.empty[rg.k % p.geo.ns], weight);
+        mbar_arrive(&s.empty[rg.slot()], weight);
         if (t2 && rg.k < 512) p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3584 + rg.k] = gtimer();
         if (t2) {
             rg.t_comp += t2 - rg.t_mark;
             rg.t_rel += gtimer() - t2;
         }
     }
-    ++rg.k;
+    rg.advance(p.geo.ns);
 }
 // Trace only: lane 0 of each warp stores its ring accounting at slots
 // 2304 + 16 * warp + 3 * e + {0 take, 1 between, 2 release} and clears it.
@@ -517,16 +536,12 @@ __device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t step, int nv
 // per lane group and pass (rw in {1, 2, 4}): with many tiles rw = 4 (each
 // activation chunk feeds 4 rows: least shared-memory traffic), with few tiles
 // rw shrinks so more warps share a tile and the phase ends sooner.
-template <int MR, int LPR, class Epi>
-__device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec,
-                                             int nrows, int TR, bool ab, Epi&& epi, int trace_slot = -1) {
-    constexpr int K = MR * 8 * LPR;
-    constexpr int RPP = 32 / LPR;
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane / LPR, ll = lane % LPR;
+// The work split of a warp-row GEMV phase over nrows rows in tiles of TR rows,
+// RPP rows side by side per warp: rows per lane group (rw) the largest of 4, 2,
+// 1 that still lets every tile of a short phase run at once (or 4 when the
+// phase has many tiles); groups of wpg warps take the tiles in turn.
+__device__ void gemv_cfg(GemvCfg& c, int nrows, int TR, int RPP) {
     const int ntiles = (nrows + TR - 1) / TR;
-    // rows per lane group: the largest of 4, 2, 1 that still lets every tile
-    // of a short phase run at once (or 4 when the phase has many tiles)
     int rw = 4, wpg = group_size((TR + 4 * RPP - 1) / (4 * RPP));
     if (ntiles < MK_NCW / wpg) {
         for (int cand = 1; cand <= 4; cand <<= 1) {
@@ -534,11 +549,27 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
             if (MK_NCW / wp >= ntiles) { rw = cand; wpg = wp; break; }
         }
     }
+    c.ntiles = (int16_t)ntiles; c.rw = (int16_t)rw; c.wpg = (int16_t)wpg; c.ngrp = (int16_t)(MK_NCW / wpg);
+    for (int w = 0; w < MK_NCW; ++w) { c.grp[w] = (int8_t)(w / wpg); c.wg[w] = (int8_t)(w % wpg); }
+}
+
+template <int MR, int LPR, class Epi>
+__device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec,
+                                             int nrows, int TR, const GemvCfg& cfg, bool ab, Epi&& epi,
+                                             int trace_slot = -1) {
+    constexpr int K = MR * 8 * LPR;
+    constexpr int RPP = 32 / LPR;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane / LPR, ll = lane % LPR;
+    const int ntiles = cfg.ntiles, rw = cfg.rw, wpg = cfg.wpg, ngrp = cfg.ngrp;
+    const int grp = cfg.grp[w], wg = cfg.wg[w];
     const int rows_per_warp = rw * RPP;
-    const int ngrp = MK_NCW / wpg, grp = w / wpg, wg = w % wpg;
     const size_t rb = (size_t)K * 2;
+    int turn = 0;   // ti mod ngrp
     for (int ti = 0; ti < ntiles && !ab; ++ti) {
-        if ((ti % ngrp) != grp) { ++ring.k; continue; }   // another group's tile
+        const bool mine = turn == grp;
+        if (++turn == ngrp) turn = 0;
+        if (!mine) { ring.advance(p.geo.ns); continue; }   // another group's tile
         const int R = min(TR, nrows - ti * TR);
         const uint8_t* tile;
         const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
@@ -616,7 +647,7 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
     }
     const int ntiles = (nrows + TR - 1) / TR;
     for (int ti = 0; ti < ntiles && !ab; ++ti) {
-        if (NG > 1 && (ti % NG) != grp) { ++ring.k; continue; }   // another group's tile
+        if (NG > 1 && (ti % NG) != grp) { ring.advance(p.geo.ns); continue; }   // another group's tile
         const int R0 = ti * TR, R = min(TR, nrows - R0);
         const uint8_t* tile;
         const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
@@ -857,6 +888,11 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         }
         s.misc->token = tok;
         s.misc->plan = p.plans[c];
+        {
+            constexpr int KO = G * HD, LPRO = KO >= 32 * 4 ? KO / 32 : 4;
+            gemv_cfg(s.misc->ocfg, s.misc->plan.norows, g.TRo, 32 / LPRO);
+            gemv_cfg(s.misc->lmcfg, s.misc->plan.nv, g.TRh, 1);
+        }
         {
             const uint32_t sq = *(volatile uint32_t*)p.seq;
             s.misc->par = (int)(sq & 1u);
@@ -1134,7 +1170,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
         // O-proj (rows of this CTA, columns of this group) + residual, atomically
         float* xo = xa + (size_t)(2 * l) * state;
-        ab = gemv_phase_t<MO, LPRO>(p, s, ring, s.ov, pl.norows, g.TRo, ab, [&](int r, float v) {
+        ab = gemv_phase_t<MO, LPRO>(p, s, ring, s.ov, pl.norows, g.TRo, s.misc->ocfg, ab, [&](int r, float v) {
             if (pl.g == 0) v += s.xres[r];   // group 0 carries the residual of these rows
             atomicAdd(xo + pl.orow0 + r, v);
         });
@@ -1187,7 +1223,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 #pragma unroll
                 for (int k = 0; k < 4; ++k) da[m][k] = make_float2(0.f, 0.f);
             for (int j0 = 0, b = 0; j0 < pl.nj && !ab; j0 += g.JD, ++b) {
-                if (b % P != jp) { ++ring.k; continue; }   // another group's tile
+                if (b % P != jp) { ring.advance(p.geo.ns); continue; }   // another group's tile
                 const int n = min(g.JD, pl.nj - j0);
                 const uint8_t* tile;
                 const bool ok = take_tile(p, s, ring, (uint32_t)(n * H * 2), tile);
@@ -1271,7 +1307,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         float bv = -INFINITY;
         int bi = -1;
         bool nonfinite = false;
-        ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv, pl.nv, g.TRh, ab, [&](int r, float lg) {
+        ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv, pl.nv, g.TRh, s.misc->lmcfg, ab, [&](int r, float lg) {
             const int v = pl.v0 + r;
             if (p.logits) p.logits[v] = lg;
             if (isfinite(lg)) {
