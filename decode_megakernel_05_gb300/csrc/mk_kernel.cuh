@@ -254,14 +254,19 @@ __device__ bool wait_mbar(const MkParams& p, uint64_t* b, uint32_t parity, volat
 }
 
 // Between polls of tagged words: false (and the abort bit, and on time-out the
-// timeout bit) when the wait must end.  t0 = 0 on the first call.
+// timeout bit) when the wait must end.  t0 = 0 on the first call.  The abort
+// bit (a global load, an L2 round trip) is read on every 8th call only.
 __device__ __forceinline__ bool ll_backoff(const MkParams& p, uint64_t& t0) {
-    if (*(volatile uint32_t*)p.status & MK_ST_ABORT) return false;
-    const uint64_t now = gtimer();
-    if (t0 == 0) t0 = now;
-    else if (now - t0 > (uint64_t)p.wait_limit_ns) {
-        atomicOr(p.status, MK_ST_TIMEOUT | MK_ST_ABORT);
-        return false;
+    if ((t0 & 7u) == 7u && (*(volatile uint32_t*)p.status & MK_ST_ABORT)) return false;
+    const uint64_t now = gtimer() | 1u;   // never 0: t0 == 0 marks the first call
+    if (t0 == 0) {
+        t0 = now & ~7ull;   // the low 3 bits count calls
+    } else {
+        if (now - t0 > (uint64_t)p.wait_limit_ns) {
+            atomicOr(p.status, MK_ST_TIMEOUT | MK_ST_ABORT);
+            return false;
+        }
+        t0 = (t0 & ~7ull) | ((t0 + 1u) & 7ull);
     }
     __nanosleep(64);
     return true;
@@ -845,6 +850,7 @@ struct Attn {
 // each lane owns in a row of H (the GEMV width of QKV, gate/up and LM head).
 template <int HD, int G, int MH>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
+    static_assert(G <= MK_NCW, "one consumer warp per query head of a KV group (softmax, combine weights)");
     constexpr int KO = G * HD;                         // O-proj row length
     constexpr int LPRO = KO >= 32 * 4 ? KO / 32 : 4;   // short rows: 4 chunks per lane
     constexpr int MO = KO / (8 * LPRO);
@@ -1119,17 +1125,22 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 }
             }
             if (bar_or(late)) ab = true;
-            if (!ab && t < G) {
+            if (!ab && (t >> 5) < G) {   // warp h: head h, lanes over the partials
+                const int hh = t >> 5, ln = t & 31;
                 float mx = -INFINITY;
-                for (int j = 0; j < g.CPG; ++j) mx = fmaxf(mx, cw[j * G + t]);
+                for (int j = ln; j < g.CPG; j += 32) mx = fmaxf(mx, cw[j * G + hh]);
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
                 float den = 0.f;
-                for (int j = 0; j < g.CPG; ++j) {
-                    const float mj = cw[j * G + t];
+                for (int j = ln; j < g.CPG; j += 32) {
+                    const float mj = cw[j * G + hh];
                     const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - mx);
-                    den = fmaf(wj, s.misc->cl[j * G + t], den);
-                    s.misc->cwt[j * G + t] = wj;
+                    den = fmaf(wj, s.misc->cl[j * G + hh], den);
+                    s.misc->cwt[j * G + hh] = wj;
                 }
-                s.misc->alpha[t] = 1.f / den;
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
+                if (ln == 0) s.misc->alpha[hh] = 1.f / den;
             }
             bar_or(false);
 #pragma unroll 1
