@@ -126,7 +126,7 @@ MK_HD int mk_smem_layout(MkGeom& g) {
     g.off_xres2 = o; o += 4 * ((g.H / g.nC + 4) & ~3);
     g.off_rope = o; o += 4 * g.hd;
     g.off_red = o; o += 4 * 2 * MK_NCT;       // double-buffered row partials
-    g.off_sc = o; o += 4 * g.G * (g.KB + 4);  // attention scores of one KV block (+ the current position)
+    g.off_sc = o; o += 4 * 2 * (8 * MK_NCT / g.hd);   // attention (m, l) per position group and head
     g.off_misc = o; o += MK_MISC_BYTES;       // softmax state, staging, flags
     g.smem_bytes = o;
     return o;

@@ -174,7 +174,7 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     int is_last;
     unsigned long long copy_bytes;  // bytes issued by the copy producer (paces the L2 prefetcher)
     unsigned long long cwait;       // trace: ns thread 0 spent waiting for ring data
-    float alpha[8], mrun[8], lrun[8];
+    float alpha[8];          // per head: 1 / (sum of the combine weights)
     float best_val[64];
     int best_idx[64];
     uint32_t tile_bytes[16]; // bytes of the tile in each ring slot (schedule check)
@@ -201,7 +201,7 @@ struct Smem {
     float* xres2; // raw residual of rows split(H, nC, c)
     float* rope;  // cos[hd/2], sin[hd/2] at this position
     float* red;   // [2][MK_NCT]
-    float* sc;    // [G][KB]
+    float* sc;    // attention (m, l) per position group and head: [2][PPP][G]
     Misc* misc;
 };
 
@@ -782,64 +782,39 @@ struct Attn {
     static constexpr int PPP = MK_NCT / TPP;         // positions per pass
     static_assert(MK_NCT % TPP == 0 && (DC & (DC - 1)) == 0 && DC <= 32, "attention lane layout");
 
-    // Scores of positions [0, n): q < nr from the ring tile kt, q == nr from
-    // the staged row st.  qr: this thread's 8 query dims (scaled by log2(e)/sqrt(hd)).
-    static __device__ __forceinline__ void scores(const Smem& s, const uint8_t* kt, int nr, const uint8_t* st, int n,
-                                                  const float qr[8], int SC) {
-        const int t = threadIdx.x, pp = t / TPP, h = (t % TPP) / DC, dc = t % DC;
+    // Per-thread online softmax over positions [0, n) of a block: thread
+    // (pp, h, dc) takes positions q = pp, pp + PPP, ..., scores them (8-dim
+    // partial dots reduced over the head's DC lanes) and folds each into its
+    // running (m, l, acc) with exp2 weights.  q < nr from the ring tiles kt/vt,
+    // q == nr from the staged current row (st: K, then V).  No barrier.
+    static __device__ __forceinline__ void online(const uint8_t* kt, const uint8_t* vt, int nr, const uint8_t* st,
+                                                  int n, const float qr[8], float& m, float& lsum, float acc[8]) {
+        const int t = threadIdx.x, pp = t / TPP, dc = t % DC;
         for (int q0 = 0; q0 < n; q0 += PPP) {          // uniform trip count across the warp
             const int q = q0 + pp;
-            float a = 0.f;
-            if (q < n) {
+            const bool valid = q < n;
+            float sc = 0.f;
+            uint4 vw = make_uint4(0u, 0u, 0u, 0u);
+            if (valid) {
                 float f[8];
                 unpack8(lds128((q < nr ? kt + (size_t)q * HD * 2 : st) + dc * 16), f);
+                vw = lds128((q < nr ? vt + (size_t)q * HD * 2 : st + HD * 2) + dc * 16);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) a = fmaf(f[e], qr[e], a);
+                for (int e = 0; e < 8; ++e) sc = fmaf(f[e], qr[e], sc);
             }
 #pragma unroll
-            for (int o = DC / 2; o >= 1; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
-            if (dc == 0 && q < n) s.sc[h * SC + q] = a;
-        }
-    }
-    // Online-softmax update of head h = warp (warps < G), over n scores.
-    static __device__ __forceinline__ void softmax_update(const Smem& s, int n, int SC) {
-        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        if (w >= G) return;
-        const int h = w;
-        float mx = -INFINITY;
-        for (int q = lane; q < n; q += 32) mx = fmaxf(mx, s.sc[h * SC + q]);
+            for (int o = DC / 2; o >= 1; o >>= 1) sc += __shfl_xor_sync(0xFFFFFFFFu, sc, o);
+            if (valid) {
+                float v[8];
+                unpack8(vw, v);
+                const float mn = fmaxf(m, sc);
+                const float c = exp2f(m - mn);     // m = -inf at the first position: c = 0
+                const float pw = exp2f(sc - mn);
+                lsum = fmaf(lsum, c, pw);
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-        const float mold = s.misc->mrun[h];
-        const float mn = fmaxf(mold, mx);
-        const float alpha = (mold == -INFINITY) ? 0.f : exp2f(mold - mn);
-        float sum = 0.f;
-        for (int q = lane; q < n; q += 32) {
-            const float e = exp2f(s.sc[h * SC + q] - mn);
-            s.sc[h * SC + q] = e;
-            sum += e;
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-        if (lane == 0) {
-            s.misc->lrun[h] = s.misc->lrun[h] * alpha + sum;
-            s.misc->mrun[h] = mn;
-            s.misc->alpha[h] = alpha;
-        }
-    }
-    // acc <- acc * alpha_h + sum_q p[h][q] V[q][8dc..]
-    static __device__ __forceinline__ void accumulate_v(const Smem& s, const uint8_t* vt, int nr, const uint8_t* stv,
-                                                        int n, float acc[8], int SC) {
-        const int t = threadIdx.x, pp = t / TPP, h = (t % TPP) / DC, dc = t % DC;
-        const float al = s.misc->alpha[h];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] *= al;
-        for (int q = pp; q < n; q += PPP) {
-            float f[8];
-            unpack8(lds128((q < nr ? vt + (size_t)q * HD * 2 : stv) + dc * 16), f);
-            const float wgt = s.sc[h * SC + q];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wgt, f[e], acc[e]);
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(acc[e], c, pw * v[e]);
+                m = mn;
+            }
         }
     }
 };
@@ -904,7 +879,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             s.misc->par = (int)(sq & 1u);
             s.misc->tag = sq + 1u;
         }
-        for (int h = 0; h < 8; ++h) { s.misc->mrun[h] = -INFINITY; s.misc->lrun[h] = 0.f; s.misc->alpha[h] = 0.f; }
+        for (int h = 0; h < 8; ++h) s.misc->alpha[h] = 0.f;
     }
     __syncthreads();
     const MkCtaPlan& pl = s.misc->plan;
@@ -999,7 +974,6 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 late = !ll_read8(p, p.qll + (size_t)l * g.qh * HD + ((size_t)pl.g * G + h_) * HD + dc_ * 8, s.misc->tag, qv);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) qr[e] = qv[e] * qscale;
-                if (t < G) { s.misc->mrun[t] = -INFINITY; s.misc->lrun[t] = 0.f; }
                 if (has_cur && t < HD / 4 && !late) {   // stage K[pos], V[pos] (bf16) from their tagged copies
                     float kv[8];
                     late = !ll_read8(p, p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (t < HD / 8 ? 0 : 1)) * HD +
@@ -1014,11 +988,12 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+            float m_ = -INFINITY, l_ = 0.f;
             ab = bar_or(ab || late);
-            // Blocks of up to KB past positions from the ring; the last CTA of the
-            // group appends the current position (staged from global) to its
-            // last block, or runs it as a block of its own when it has no past.
-            const int SC = g.KB + 4;   // score row stride (room for the current position)
+            // Blocks of up to KB past positions from the ring (the K tile and
+            // the V tile of a block are held together); the last CTA of the
+            // group appends the current position (staged) to its last block,
+            // or runs it as a block of its own when it has no past.
             const int nring = ke > ka ? ke - ka : 0;
             const int nblk = (nring + g.KB - 1) / g.KB;
             const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
@@ -1028,37 +1003,51 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
                 const int n = nr + ((has_cur && b == nbt - 1) ? 1 : 0);
                 const uint8_t *kt = st, *vt = st;
-                bool ok = nr == 0 || take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt);
-                if (ok) A::scores(s, kt, nr, st, n, qr, SC);
-                if (nr > 0) release_tile(p, s, ring);
-                ab = bar_or(ab || !ok);
-                if (!ab) A::softmax_update(s, n, SC);
-                ab = bar_or(ab);
-                ok = ab || nr == 0 || take_tile(p, s, ring, (uint32_t)(nr * HD * 2), vt);
-                if (!ab && ok) A::accumulate_v(s, vt, nr, st + HD * 2, n, acc, SC);
-                if (nr > 0) release_tile(p, s, ring);
-                ab = bar_or(ab || !ok);
+                bool ok = true;
+                if (nr > 0) {
+                    Ring rv = ring;
+                    rv.advance(g.ns);      // the V tile follows the K tile in the stream
+                    ok = take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt) &&
+                         take_tile(p, s, rv, (uint32_t)(nr * HD * 2), vt);
+                }
+                if (ok) A::online(kt, vt, nr, st, n, qr, m_, l_, acc);
+                if (nr > 0) { release_tile(p, s, ring); release_tile(p, s, ring); }
+                if (!ok) ab = true;     // made uniform by the barrier below
             }
-            // sum the position groups: every thread parks its 8 dims in xv
-            // ([position group][G*HD], free between QKV and the FFN norm), then
-            // each output element is summed over the groups and stored
+            // merge the position groups: each parks (m, l) per head and its
+            // 8 dims of acc in smem ([position group][G*HD] in xv, free between
+            // QKV and the FFN norm); after the barrier each output element is
+            // rescaled to the group-wide maximum and summed
             if (!ab) {
-                float4* sp = reinterpret_cast<float4*>(s.xv + (t / A::TPP) * (G * HD) + h_ * HD + dc_ * 8);
+                const int pp = t / A::TPP;
+                float4* sp = reinterpret_cast<float4*>(s.xv + pp * (G * HD) + h_ * HD + dc_ * 8);
                 sp[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 sp[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                if (dc_ == 0) { s.sc[pp * G + h_] = m_; s.sc[A::PPP * G + pp * G + h_] = l_; }
             }
         }
         ab = bar_or(ab);
         constexpr int PSTR = G * HD + 2 * G;                   // tagged words per partial
         if (!ab && !(p.dbg_skip_sync == 4 * l + 1 && p.dbg_skip_cta == c)) {
+            constexpr int PPP = Attn<HD, G>::PPP;
             uint64_t* dst = p.partll + (((size_t)l * g.kvh + pl.g) * g.CPG + pl.i) * PSTR;
             for (int i = t; i < G * HD; i += MK_NCT) {
-                float a = 0.f;
+                const int h = i / HD;
+                float M = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < Attn<HD, G>::PPP; ++q) a += s.xv[q * (G * HD) + i];
+                for (int q = 0; q < PPP; ++q) M = fmaxf(M, s.sc[q * G + h]);
+                float a = 0.f, L = 0.f;
+                if (M != -INFINITY) {   // no position at all: an empty partial (m = -inf, l = 0)
+#pragma unroll
+                    for (int q = 0; q < PPP; ++q) {
+                        const float wq = exp2f(s.sc[q * G + h] - M);
+                        a = fmaf(wq, s.xv[q * (G * HD) + i], a);
+                        L = fmaf(wq, s.sc[PPP * G + q * G + h], L);
+                    }
+                }
                 st_ll(dst + i, ll_pack(a, s.misc->tag));
+                if (i % HD == 0) st_ll2(dst + G * HD + 2 * h, ll_pack(M, s.misc->tag), ll_pack(L, s.misc->tag));
             }
-            if (t < G) st_ll2(dst + G * HD + 2 * t, ll_pack(s.misc->mrun[t], s.misc->tag), ll_pack(s.misc->lrun[t], s.misc->tag));
         }
         ab = bar_or(ab);
         MK_TRACE(16 * l + 5);
