@@ -355,29 +355,39 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
     }
 }
 
-// L2 prefetch walker (the whole prefetch warp): walks the same tile stream as
-// the copy producer and asks L2 for each tile's 128-byte lines with per-lane
-// prefetches (load/store path, so the bulk-copy queue is not held up), staying
-// at most l2_pf_bytes ahead of the copies.
+// L2 warmer (the whole prefetch warp): walks the same tile stream as the copy
+// producer, at most l2_pf_bytes ahead of its copies, and brings each tile's
+// 128-byte lines into L2 with one plain 4-byte load per line, so the copy
+// later reads L2 instead of HBM.  (Measured: a plain load per line leaves the
+// whole line in L2 for a later bulk copy; prefetch.global.L2 and non-coherent
+// loads do so only in part.)  It works only while the consumers are
+// latency-bound, when HBM is otherwise idle, and waits for each tile's loads
+// before the next, so at most one tile of warming loads is in flight.
 __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const Smem& s) {
     if (p.l2_pf_bytes <= 0) return;
     const int lane = threadIdx.x & 31;
     volatile int* abort = &s.misc->abort;
     const unsigned long long ahead = (unsigned long long)p.l2_pf_bytes;
     unsigned long long issued = 0;
+    uint32_t sink = 0;
     bool stop = false;
     walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
         if (stop) return;
         uint64_t t0 = 0;
         for (;;) {
             const unsigned long long cb = *(volatile unsigned long long*)&s.misc->copy_bytes;
-            if (issued <= cb + ahead) {
-                // tiles the copy producer has already issued need no prefetch
-                if (issued + bytes > cb) {
-                    const char* b = reinterpret_cast<const char*>(src);
-                    for (uint32_t off = (uint32_t)lane * 128u; off < bytes; off += 32u * 128u)
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(b + off));
+            const bool streaming = *(volatile int*)&s.misc->streaming;
+            if (issued + bytes <= cb) break;   // already copied: nothing to warm
+            if (!streaming && issued <= cb + ahead) {
+                const char* b = reinterpret_cast<const char*>(src);
+                uint32_t acc = 0;
+                for (uint32_t off = (uint32_t)lane * 128u; off < bytes; off += 32u * 128u) {
+                    uint32_t v;
+                    asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(b + off) : "memory");
+                    acc ^= v;
                 }
+                // consumed here, in order with the loads: the next tile's loads wait for these
+                asm volatile("xor.b32 %0, %0, %1;" : "+r"(sink) : "r"(acc));
                 break;
             }
             if (*abort) { stop = true; return; }
@@ -387,6 +397,7 @@ __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const 
         }
         issued += bytes;
     });
+    if (sink == 0x9E3779B9u && lane == 32) s.misc->abort = 2;   // never true (lane < 32): keeps the loads
 }
 
 // ------------------------------------------------------------------ consumer pieces
