@@ -794,39 +794,70 @@ struct Attn {
     static_assert(MK_NCT % TPP == 0 && (DC & (DC - 1)) == 0 && DC <= 32, "attention lane layout");
 
     // Per-thread online softmax over positions [0, n) of a block: thread
-    // (pp, h, dc) takes positions q = pp, pp + PPP, ..., scores them (8-dim
-    // partial dots reduced over the head's DC lanes) and folds each into its
-    // running (m, l, acc) with exp2 weights.  q < nr from the ring tiles kt/vt,
-    // q == nr from the staged current row (st: K, then V).  No barrier.
+    // (pp, h, dc) takes positions q = pp, pp + PPP, ..., four at a time: it
+    // scores them (8-dim partial dots in packed fp32x2, reduced over the
+    // head's DC lanes), rescales its running (m, l, acc) once to the chunk's
+    // maximum and folds each position in with its exp2 weight.  q < nr from
+    // the ring tiles kt/vt, q == nr from the staged current row (st: K, then
+    // V).  No barrier.
     static __device__ __forceinline__ void online(const uint8_t* kt, const uint8_t* vt, int nr, const uint8_t* st,
                                                   int n, const float qr[8], float& m, float& lsum, float acc[8]) {
+        constexpr int CH = 4;                          // positions per thread and chunk
         const int t = threadIdx.x, pp = t / TPP, dc = t % DC;
-        for (int q0 = 0; q0 < n; q0 += PPP) {          // uniform trip count across the warp
-            const int q = q0 + pp;
-            const bool valid = q < n;
-            float sc = 0.f;
-            uint4 vw = make_uint4(0u, 0u, 0u, 0u);
-            if (valid) {
-                float f[8];
-                unpack8(lds128((q < nr ? kt + (size_t)q * HD * 2 : st) + dc * 16), f);
-                vw = lds128((q < nr ? vt + (size_t)q * HD * 2 : st + HD * 2) + dc * 16);
+        const float2 q01 = make_float2(qr[0], qr[1]), q23 = make_float2(qr[2], qr[3]);
+        const float2 q45 = make_float2(qr[4], qr[5]), q67 = make_float2(qr[6], qr[7]);
+        float2 a2[4] = {make_float2(acc[0], acc[1]), make_float2(acc[2], acc[3]), make_float2(acc[4], acc[5]),
+                        make_float2(acc[6], acc[7])};
+        for (int q0 = 0; q0 < n; q0 += CH * PPP) {     // uniform trip count across the warp
+            float sc[CH];
+            uint4 vw[CH];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sc = fmaf(f[e], qr[e], sc);
+            for (int c = 0; c < CH; ++c) {
+                const int q = q0 + c * PPP + pp;
+                float2 d = make_float2(0.f, 0.f);
+                vw[c] = make_uint4(0u, 0u, 0u, 0u);
+                if (q < n) {
+                    const uint4 kw = lds128((q < nr ? kt + (size_t)q * HD * 2 : st) + dc * 16);
+                    vw[c] = lds128((q < nr ? vt + (size_t)q * HD * 2 : st + HD * 2) + dc * 16);
+                    d = __ffma2_rn(bf2_lo_hi(kw.x), q01, d);
+                    d = __ffma2_rn(bf2_lo_hi(kw.y), q23, d);
+                    d = __ffma2_rn(bf2_lo_hi(kw.z), q45, d);
+                    d = __ffma2_rn(bf2_lo_hi(kw.w), q67, d);
+                }
+                sc[c] = d.x + d.y;
             }
 #pragma unroll
-            for (int o = DC / 2; o >= 1; o >>= 1) sc += __shfl_xor_sync(0xFFFFFFFFu, sc, o);
-            if (valid) {
-                float v[8];
-                unpack8(vw, v);
-                const float mn = fmaxf(m, sc);
-                const float c = exp2f(m - mn);     // m = -inf at the first position: c = 0
-                const float pw = exp2f(sc - mn);
-                lsum = fmaf(lsum, c, pw);
+            for (int c = 0; c < CH; ++c) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaf(acc[e], c, pw * v[e]);
-                m = mn;
+                for (int o = DC / 2; o >= 1; o >>= 1) sc[c] += __shfl_xor_sync(0xFFFFFFFFu, sc[c], o);
+            }
+            float cm = m;
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+                if (q0 + c * PPP + pp < n) cm = fmaxf(cm, sc[c]);
+            if (cm != -INFINITY) {                     // this thread has a position in the chunk (or before)
+                const float corr = exp2f(m - cm);      // m = -inf before the first position: 0
+                const float2 c2 = make_float2(corr, corr);
+                lsum *= corr;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) a2[k] = __ffma2_rn(a2[k], c2, make_float2(0.f, 0.f));
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    if (q0 + c * PPP + pp < n) {
+                        const float pw = exp2f(sc[c] - cm);
+                        const float2 p2 = make_float2(pw, pw);
+                        lsum += pw;
+                        a2[0] = __ffma2_rn(bf2_lo_hi(vw[c].x), p2, a2[0]);
+                        a2[1] = __ffma2_rn(bf2_lo_hi(vw[c].y), p2, a2[1]);
+                        a2[2] = __ffma2_rn(bf2_lo_hi(vw[c].z), p2, a2[2]);
+                        a2[3] = __ffma2_rn(bf2_lo_hi(vw[c].w), p2, a2[3]);
+                    }
+                }
+                m = cm;
             }
         }
+        acc[0] = a2[0].x; acc[1] = a2[0].y; acc[2] = a2[1].x; acc[3] = a2[1].y;
+        acc[4] = a2[2].x; acc[5] = a2[2].y; acc[6] = a2[3].x; acc[7] = a2[3].y;
     }
 };
 
@@ -1009,6 +1040,9 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             const int nblk = (nring + g.KB - 1) / g.KB;
             const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
             const uint8_t* st = reinterpret_cast<const uint8_t*>(s.misc->stage);
+            // several K/V blocks (long contexts) stream like weights: lift the
+            // producer's latency-phase in-flight limit for the block loop
+            if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 1;
             for (int b = 0; b < nbt && !ab; ++b) {
                 const int q0 = ka + b * g.KB;
                 const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
@@ -1025,6 +1059,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 if (nr > 0) { release_tile(p, s, ring); release_tile(p, s, ring); }
                 if (!ok) ab = true;     // made uniform by the barrier below
             }
+            if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 0;
             // merge the position groups: each parks (m, l) per head and its
             // 8 dims of acc in smem ([position group][G*HD] in xv, free between
             // QKV and the FFN norm); after the barrier each output element is
