@@ -24,6 +24,9 @@ SOURCES = ["mk_api.cu", "mk_aux.cu", "mk_perop.cu", "mk_noalloc.cu"]
 # (head_dim, query heads per KV group, hidden / 256) of the fused kernel, one
 # object each; keep in sync with MK_VARIANTS in csrc/mk_api.cu
 VARIANTS = [(64, 2, 1), (64, 4, 2), (64, 4, 4), (64, 4, 8), (64, 4, 16), (128, 4, 4), (128, 4, 8), (128, 4, 16)]
+# long-context builds (two query heads per attention lane), used when max_seq >= MK_LONG_CTX;
+# keep in sync with MK_LC_VARIANTS in csrc/mk_api.cu
+LC_VARIANTS = [(64, 4, 2), (64, 4, 8)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -56,10 +59,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
                     "-I", INCLUDE, "-I", CSRC]
     jobs = [(src, os.path.join(BUILD, src.replace(".cu", ".o")), []) for src in SOURCES]
-    for hd, g, mh in VARIANTS:   # each without and with the segment trace compiled in
-        for tr in (False, True):
-            jobs.append(("mk_kernel.cu", os.path.join(BUILD, f"mk_kernel_{hd}_{g}_{mh}{'_trace' if tr else ''}.o"),
-                         [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}", f"-DMK_MH_V={mh}"] + ([] if tr else ["-DMK_NO_TRACE"])))
+    for hd, g, mh, lc in [v + (0,) for v in VARIANTS] + [v + (1,) for v in LC_VARIANTS]:
+        for tr in (False, True):   # each without and with the segment trace compiled in
+            name = f"mk_kernel_{hd}_{g}_{mh}{'_lc' if lc else ''}{'_trace' if tr else ''}.o"
+            jobs.append(("mk_kernel.cu", os.path.join(BUILD, name),
+                         [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}", f"-DMK_MH_V={mh}", f"-DMK_LC_V={lc}"] +
+                         ([] if tr else ["-DMK_NO_TRACE"])))
 
     def compile_one(job):
         src, obj, defs = job

@@ -15,19 +15,35 @@
 #include "mk_perop.h"
 
 // One object per kernel variant: mk_kernel.cu compiled with -DMK_HD_V=<head_dim>
-// -DMK_G_V=<q heads per kv head> -DMK_MH_V=<hidden / 256>; keep in sync with
-// VARIANTS in build.py.
+// -DMK_G_V=<q heads per kv head> -DMK_MH_V=<hidden / 256> (-DMK_LC_V=1 for the
+// long-context builds); keep in sync with VARIANTS in build.py.
 #define MK_VARIANTS(X) \
     X(64, 2, 1) X(64, 4, 2) X(64, 4, 4) X(64, 4, 8) X(64, 4, 16) X(128, 4, 4) X(128, 4, 8) X(128, 4, 16)
+#define MK_LC_VARIANTS(X) X(64, 4, 2) X(64, 4, 8)
 // Each variant exists twice: without trace code (launched normally) and with
 // it (launched while a segment trace is requested).
 #define MK_DECL(hd, g, mh)                                         \
     extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh(void); \
     extern "C" const void* mk_kernel_trace_ptr_##hd##_##g##_##mh(void);
+#define MK_DECL_LC(hd, g, mh)                                          \
+    extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh##_lc(void); \
+    extern "C" const void* mk_kernel_trace_ptr_##hd##_##g##_##mh##_lc(void);
 MK_VARIANTS(MK_DECL)
+MK_LC_VARIANTS(MK_DECL_LC)
 #undef MK_DECL
+#undef MK_DECL_LC
 
-static int mk_kernel_variant(int hd, int G, int H, const void** fn, const void** fn_trace) {
+// The kernel for a shape; with long_ctx, its long-context build where one exists.
+// Returns 1 for a long-context build, 0 for the standard one, -1 if none fits.
+static int mk_kernel_variant(int hd, int G, int H, bool long_ctx, const void** fn, const void** fn_trace) {
+#define MK_PICK_LC(hd_, g_, mh_)                                      \
+    if (long_ctx && hd == hd_ && G == g_ && H == 256 * mh_) {         \
+        *fn = mk_kernel_ptr_##hd_##_##g_##_##mh_##_lc();              \
+        *fn_trace = mk_kernel_trace_ptr_##hd_##_##g_##_##mh_##_lc();  \
+        return 1;                                                     \
+    }
+    MK_LC_VARIANTS(MK_PICK_LC)
+#undef MK_PICK_LC
 #define MK_PICK(hd_, g_, mh_)                                         \
     if (hd == hd_ && G == g_ && H == 256 * mh_) {                     \
         *fn = mk_kernel_ptr_##hd_##_##g_##_##mh_();                   \
@@ -88,7 +104,8 @@ int check_shape(const mk_config* c, bool need_kernel = true) {
     if (c->head_dim != 64 && c->head_dim != 128) return MK_ERR_UNSUPPORTED;
     const int G = c->n_q_heads / c->n_kv_heads;
     const void *fn = nullptr, *fn_trace = nullptr;
-    if (need_kernel && mk_kernel_variant(c->head_dim, G, c->hidden, &fn, &fn_trace) != 0) return MK_ERR_UNSUPPORTED;
+    if (need_kernel && mk_kernel_variant(c->head_dim, G, c->hidden, false, &fn, &fn_trace) < 0)
+        return MK_ERR_UNSUPPORTED;
     // GEMV row length K: 8-column chunks spread over min(32, K/8) lanes, so
     // K/8 divides 32 (short rows) or K is a multiple of 256 (long rows).
     auto width_ok = [](int K) {
@@ -215,6 +232,7 @@ struct mk_ctx {
     int device = 0, sm_count = 0;
     const void* kernel = nullptr;        // the fused step without trace code
     const void* kernel_trace = nullptr;  // the same with the segment trace compiled in
+    bool long_ctx = false;               // kernel is the long-context build
     std::vector<MkCtaPlan> plans;
     int64_t arena_bytes = 0, device_bytes = 0;
     bool weights_loaded = false;
@@ -429,7 +447,8 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         if ((rc = build_geom(cfg, c->tune, grid, ns, g)) != MK_OK) return fail(rc);
         if (g.smem_bytes + 1024 <= smem_optin) { c->geo = g; break; }
     }
-    mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, &c->kernel, &c->kernel_trace);
+    c->long_ctx = mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, cfg->max_seq >= MK_LONG_CTX,
+                                    &c->kernel, &c->kernel_trace) == 1;
     for (const void* k : {c->kernel, c->kernel_trace})
         if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c->geo.smem_bytes)) !=
             cudaSuccess)
@@ -795,6 +814,7 @@ int mk_get_info(const mk_ctx* c, mk_info* o) {
     o->weight_bytes_per_token = weight_bytes_per_token(&c->cfg);
     o->kv_bytes_per_position = (int64_t)2 * c->geo.L * c->geo.kvh * c->geo.hd * 2;
     o->device_bytes = c->device_bytes;
+    o->long_context = c->long_ctx ? 1 : 0;
     return MK_OK;
 }
 

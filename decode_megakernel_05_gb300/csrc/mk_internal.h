@@ -38,6 +38,7 @@
 #define MK_COMBINE_LOADS 5            // float4 loads per thread in the attention combine
 #define MK_MISC_BYTES 6656
 #define MK_MAX_H 8192                 // largest hidden size the kernels take
+#define MK_LONG_CTX 8192              // max_seq from which the long-context kernel build is used (if built)
 
 // Device status word bits.
 #define MK_ST_TIMEOUT 0x1u

@@ -8,18 +8,26 @@
 #error "compile with -DMK_HD_V=<head_dim> -DMK_G_V=<q heads per kv head> -DMK_MH_V=<hidden/256>"
 #endif
 
-#define MK_CAT2(a, b, c, d) a##b##_##c##_##d
-#define MK_CAT(a, b, c, d) MK_CAT2(a, b, c, d)
+#ifndef MK_LC_V
+#define MK_LC_V 0   // 1: the long-context build (see mk_decode_kernel)
+#endif
+#if MK_LC_V
+#define MK_SFX _lc
+#else
+#define MK_SFX
+#endif
+#define MK_CAT2(a, b, c, d, e) a##b##_##c##_##d##e
+#define MK_CAT(a, b, c, d, e) MK_CAT2(a, b, c, d, e)
 
 // Built twice per variant: with -DMK_NO_TRACE (the production kernel, no trace
 // code at all: a smaller instruction footprint per layer) and without (the
 // kernel launched while a segment trace is requested).
 #ifdef MK_NO_TRACE
-extern "C" const void* MK_CAT(mk_kernel_ptr_, MK_HD_V, MK_G_V, MK_MH_V)(void) {
-    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V>;
+extern "C" const void* MK_CAT(mk_kernel_ptr_, MK_HD_V, MK_G_V, MK_MH_V, MK_SFX)(void) {
+    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V, MK_LC_V>;
 }
 #else
-extern "C" const void* MK_CAT(mk_kernel_trace_ptr_, MK_HD_V, MK_G_V, MK_MH_V)(void) {
-    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V>;
+extern "C" const void* MK_CAT(mk_kernel_trace_ptr_, MK_HD_V, MK_G_V, MK_MH_V, MK_SFX)(void) {
+    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V, MK_LC_V>;
 }
 #endif

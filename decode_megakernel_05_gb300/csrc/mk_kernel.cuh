@@ -793,86 +793,220 @@ __device__ __forceinline__ bool sync_wait(const MkParams& p, int idx, uint32_t t
 // lanes of a head.  Softmax is online (exp2, running max per head, rescaled
 // sums).  V: each thread accumulates its head's 8 dims over its positions, and
 // the position groups are summed with shared-memory atomics at the end.
+// HPL_: heads per lane.  Two (long contexts, where the K/V chunks then load
+// and unpack once for two heads) needs an even G and the parked partials to
+// fit the smem scratch; attn_long_ok tells.
 template <int HD, int G>
+__host__ __device__ constexpr bool attn_long_ok() {
+    // even G; one head per lane puts a position within one warp (so both
+    // layouts park one group per warp); the parked partials fit xv
+    return G % 2 == 0 && (HD / 8) * G <= 32 && MK_NCW * G * HD <= 8 * MK_NCT;
+}
+template <int HD, int G, int HPL_ = 1>
 struct Attn {
-    static constexpr int DC = HD / 8;                // lanes per head
-    static constexpr int TPP = G * DC;               // threads per position
-    static constexpr int PPP = MK_NCT / TPP;         // positions per pass
-    static_assert(MK_NCT % TPP == 0 && (DC & (DC - 1)) == 0 && DC <= 32, "attention lane layout");
+    static constexpr int DC = HD / 8;                // lanes per head and position (8 dims each)
+    static constexpr int HPL = HPL_;
+    static constexpr int HG = G / HPL;               // head groups per position
+    static constexpr int TPP = HG * DC;              // threads per position
+    static constexpr int PPP = MK_NCT / TPP;         // positions per pass (position groups)
+    static constexpr int PPW = TPP < 32 ? 32 / TPP : 1;   // position groups per warp
+    static constexpr int NMG = PPP / PPW;            // groups after merging within warps
+    static_assert(MK_NCT % TPP == 0 && (DC & (DC - 1)) == 0 && DC <= 32 && (32 % TPP == 0 || TPP % 32 == 0),
+                  "attention lane layout");
+    static_assert(NMG * G * HD <= 8 * MK_NCT, "parked attention partials fit the xv scratch");
+    static_assert(NMG == MK_NCW || TPP >= 32, "one parked group per warp when positions share warps");
 
     // Per-thread online softmax over positions [0, n) of a block: thread
-    // (pp, h, dc) takes positions q = pp, pp + PPP, ..., four at a time: it
-    // scores them (8-dim partial dots in packed fp32x2, reduced over the
-    // head's DC lanes), rescales its running (m, l, acc) once to the chunk's
-    // maximum and folds each position in with its exp2 weight.  q < nr from
-    // the ring tiles kt/vt, q == nr from the staged current row (st: K, then
-    // V).  No barrier.
+    // (pp, hg, dc) takes positions q = pp, pp + PPP, ..., four at a time, for
+    // its HPL heads: it scores them (8-dim partial dots in packed fp32x2,
+    // reduced over the DC lanes), rescales each head's running (m, l, acc)
+    // once to the chunk's maximum and folds each position in with its exp2
+    // weight.  q < nr from the ring tiles kt/vt, q == nr from the staged
+    // current row (st: K, then V).  No barrier.
     static __device__ __forceinline__ void online(const uint8_t* kt, const uint8_t* vt, int nr, const uint8_t* st,
-                                                  int n, const float qr[8], float& m, float& lsum, float acc[8]) {
+                                                  int n, const float (&qr)[HPL][8], float (&m)[HPL],
+                                                  float (&lsum)[HPL], float2 (&a2)[HPL][4]) {
         constexpr int CH = 4;                          // positions per thread and chunk
         const int t = threadIdx.x, pp = t / TPP, dc = t % DC;
-        const float2 q01 = make_float2(qr[0], qr[1]), q23 = make_float2(qr[2], qr[3]);
-        const float2 q45 = make_float2(qr[4], qr[5]), q67 = make_float2(qr[6], qr[7]);
-        float2 a2[4] = {make_float2(acc[0], acc[1]), make_float2(acc[2], acc[3]), make_float2(acc[4], acc[5]),
-                        make_float2(acc[6], acc[7])};
         for (int q0 = 0; q0 < n; q0 += CH * PPP) {     // uniform trip count across the warp
-            float sc[CH];
+            float sc[CH][HPL];
             uint4 vw[CH];
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
                 const int q = q0 + c * PPP + pp;
-                float2 d = make_float2(0.f, 0.f);
+                float2 d[HPL];
+#pragma unroll
+                for (int j = 0; j < HPL; ++j) d[j] = make_float2(0.f, 0.f);
                 vw[c] = make_uint4(0u, 0u, 0u, 0u);
                 if (q < n) {
                     const uint4 kw = lds128((q < nr ? kt + (size_t)q * HD * 2 : st) + dc * 16);
                     vw[c] = lds128((q < nr ? vt + (size_t)q * HD * 2 : st + HD * 2) + dc * 16);
-                    d = __ffma2_rn(bf2_lo_hi(kw.x), q01, d);
-                    d = __ffma2_rn(bf2_lo_hi(kw.y), q23, d);
-                    d = __ffma2_rn(bf2_lo_hi(kw.z), q45, d);
-                    d = __ffma2_rn(bf2_lo_hi(kw.w), q67, d);
-                }
-                sc[c] = d.x + d.y;
-            }
+                    const float2 k0 = bf2_lo_hi(kw.x), k1 = bf2_lo_hi(kw.y), k2 = bf2_lo_hi(kw.z), k3 = bf2_lo_hi(kw.w);
 #pragma unroll
-            for (int c = 0; c < CH; ++c) {
-#pragma unroll
-                for (int o = DC / 2; o >= 1; o >>= 1) sc[c] += __shfl_xor_sync(0xFFFFFFFFu, sc[c], o);
-            }
-            float cm = m;
-#pragma unroll
-            for (int c = 0; c < CH; ++c)
-                if (q0 + c * PPP + pp < n) cm = fmaxf(cm, sc[c]);
-            if (cm != -INFINITY) {                     // this thread has a position in the chunk (or before)
-                const float corr = ex2_approx(m - cm);      // m = -inf before the first position: 0
-                const float2 c2 = make_float2(corr, corr);
-                lsum *= corr;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) a2[k] = __ffma2_rn(a2[k], c2, make_float2(0.f, 0.f));
-#pragma unroll
-                for (int c = 0; c < CH; ++c) {
-                    if (q0 + c * PPP + pp < n) {
-                        const float pw = ex2_approx(sc[c] - cm);
-                        const float2 p2 = make_float2(pw, pw);
-                        lsum += pw;
-                        a2[0] = __ffma2_rn(bf2_lo_hi(vw[c].x), p2, a2[0]);
-                        a2[1] = __ffma2_rn(bf2_lo_hi(vw[c].y), p2, a2[1]);
-                        a2[2] = __ffma2_rn(bf2_lo_hi(vw[c].z), p2, a2[2]);
-                        a2[3] = __ffma2_rn(bf2_lo_hi(vw[c].w), p2, a2[3]);
+                    for (int j = 0; j < HPL; ++j) {
+                        d[j] = __ffma2_rn(k0, make_float2(qr[j][0], qr[j][1]), d[j]);
+                        d[j] = __ffma2_rn(k1, make_float2(qr[j][2], qr[j][3]), d[j]);
+                        d[j] = __ffma2_rn(k2, make_float2(qr[j][4], qr[j][5]), d[j]);
+                        d[j] = __ffma2_rn(k3, make_float2(qr[j][6], qr[j][7]), d[j]);
                     }
                 }
-                m = cm;
+#pragma unroll
+                for (int j = 0; j < HPL; ++j) sc[c][j] = d[j].x + d[j].y;
+            }
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+#pragma unroll
+                for (int j = 0; j < HPL; ++j)
+#pragma unroll
+                    for (int o = DC / 2; o >= 1; o >>= 1) sc[c][j] += __shfl_xor_sync(0xFFFFFFFFu, sc[c][j], o);
+#pragma unroll
+            for (int j = 0; j < HPL; ++j) {
+                float cm = m[j];
+#pragma unroll
+                for (int c = 0; c < CH; ++c)
+                    if (q0 + c * PPP + pp < n) cm = fmaxf(cm, sc[c][j]);
+                if (cm != -INFINITY) {                 // this thread has a position in the chunk (or before)
+                    const float corr = ex2_approx(m[j] - cm);   // m = -inf before the first position: 0
+                    const float2 c2 = make_float2(corr, corr);
+                    lsum[j] *= corr;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) a2[j][k] = __ffma2_rn(a2[j][k], c2, make_float2(0.f, 0.f));
+#pragma unroll
+                    for (int c = 0; c < CH; ++c) {
+                        if (q0 + c * PPP + pp < n) {
+                            const float pw = ex2_approx(sc[c][j] - cm);
+                            const float2 p2 = make_float2(pw, pw);
+                            lsum[j] += pw;
+                            a2[j][0] = __ffma2_rn(bf2_lo_hi(vw[c].x), p2, a2[j][0]);
+                            a2[j][1] = __ffma2_rn(bf2_lo_hi(vw[c].y), p2, a2[j][1]);
+                            a2[j][2] = __ffma2_rn(bf2_lo_hi(vw[c].z), p2, a2[j][2]);
+                            a2[j][3] = __ffma2_rn(bf2_lo_hi(vw[c].w), p2, a2[j][3]);
+                        }
+                    }
+                    m[j] = cm;
+                }
             }
         }
-        acc[0] = a2[0].x; acc[1] = a2[0].y; acc[2] = a2[1].x; acc[3] = a2[1].y;
-        acc[4] = a2[2].x; acc[5] = a2[2].y; acc[6] = a2[3].x; acc[7] = a2[3].y;
+    }
+    // Merges the PPW position groups that share a warp (lanes TPP apart) into
+    // the lanes of the first one (same head group and dims), with exp2 weights
+    // to the common maximum.
+    static __device__ __forceinline__ void merge_warp(float (&m)[HPL], float (&lsum)[HPL], float2 (&a2)[HPL][4]) {
+#pragma unroll
+        for (int o = TPP; o < 32; o <<= 1) {
+#pragma unroll
+            for (int j = 0; j < HPL; ++j) {
+                const float mo = __shfl_xor_sync(0xFFFFFFFFu, m[j], o);
+                const float lo = __shfl_xor_sync(0xFFFFFFFFu, lsum[j], o);
+                float2 ao[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    ao[k].x = __shfl_xor_sync(0xFFFFFFFFu, a2[j][k].x, o);
+                    ao[k].y = __shfl_xor_sync(0xFFFFFFFFu, a2[j][k].y, o);
+                }
+                const float M = fmaxf(m[j], mo);
+                const float w1 = (m[j] == -INFINITY) ? 0.f : ex2_approx(m[j] - M);
+                const float w2 = (mo == -INFINITY) ? 0.f : ex2_approx(mo - M);
+                lsum[j] = w1 * lsum[j] + w2 * lo;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    a2[j][k] = make_float2(w1 * a2[j][k].x + w2 * ao[k].x, w1 * a2[j][k].y + w2 * ao[k].y);
+                m[j] = M;
+            }
+        }
+    }
+    // The merged group's lanes park (m, l) per head in sc and acc in xv:
+    // xv[group][G*HD], sc[group*G + h] (m) and sc[NMG*G + group*G + h] (l).
+    static __device__ __forceinline__ void park(const Smem& s, const float (&m)[HPL], const float (&lsum)[HPL],
+                                                const float2 (&a2)[HPL][4]) {
+        const int t = threadIdx.x, pp = t / TPP, hg = (t % TPP) / DC, dc = t % DC;
+        if (pp % PPW != 0) return;                     // merged into the warp's first group
+        const int grp = pp / PPW;
+#pragma unroll
+        for (int j = 0; j < HPL; ++j) {
+            const int h = hg * HPL + j;
+            float4* sp = reinterpret_cast<float4*>(s.xv + grp * (G * HD) + h * HD + dc * 8);
+            sp[0] = make_float4(a2[j][0].x, a2[j][0].y, a2[j][1].x, a2[j][1].y);
+            sp[1] = make_float4(a2[j][2].x, a2[j][2].y, a2[j][3].x, a2[j][3].y);
+            if (dc == 0) { s.sc[grp * G + h] = m[j]; s.sc[NMG * G + grp * G + h] = lsum[j]; }
+        }
     }
 };
+
+// The attention of one CTA over its positions with HPL heads per lane: this
+// thread's q dims (tagged words), the block loop (online softmax), the merge
+// of the position groups sharing a warp and the parking of the warps' groups
+// in smem for the partial.  Returns the uniform abort flag (one barrier).
+template <int HD, int G, int HPL>
+__device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
+                                         bool has_cur, float qscale, bool ab, bool late) {
+    using A = Attn<HD, G, HPL>;
+    const MkGeom& g = p.geo;
+    const MkCtaPlan& pl = s.misc->plan;
+    const int t = threadIdx.x;
+    const int hg_ = (t % A::TPP) / A::DC, dc_ = t % A::DC;
+    float qr[HPL][8];
+    if (!ab) {
+#pragma unroll
+        for (int j = 0; j < HPL; ++j) {
+            float qv[8];
+            const int h = hg_ * HPL + j;
+            if (!ll_read8(p, p.qll + (size_t)l * g.qh * HD + ((size_t)pl.g * G + h) * HD + dc_ * 8, s.misc->tag, qv))
+                late = true;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qr[j][e] = qv[e] * qscale;
+        }
+    }
+    float m_[HPL], l_[HPL];
+    float2 acc[HPL][4];
+#pragma unroll
+    for (int j = 0; j < HPL; ++j) {
+        m_[j] = -INFINITY;
+        l_[j] = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[j][k] = make_float2(0.f, 0.f);
+    }
+    ab = bar_or(ab || late);
+    const int nring = ke > ka ? ke - ka : 0;
+    const int nblk = (nring + g.KB - 1) / g.KB;
+    const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
+    const uint8_t* st = reinterpret_cast<const uint8_t*>(s.misc->stage);
+    // several K/V blocks (long contexts) stream like weights: lift the
+    // producer's latency-phase in-flight limit for the block loop
+    if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 1;
+    for (int b = 0; b < nbt && !ab; ++b) {
+        const int q0 = ka + b * g.KB;
+        const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
+        const int n = nr + ((has_cur && b == nbt - 1) ? 1 : 0);
+        const uint8_t *kt = st, *vt = st;
+        bool ok = true;
+        if (nr > 0) {
+            Ring rv = ring;
+            rv.advance(g.ns);      // the V tile follows the K tile in the stream
+            ok = take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt) && take_tile(p, s, rv, (uint32_t)(nr * HD * 2), vt);
+        }
+        if (ok) A::online(kt, vt, nr, st, n, qr, m_, l_, acc);
+        if (nr > 0) { release_tile(p, s, ring); release_tile(p, s, ring); }
+        if (!ok) ab = true;     // made uniform by the barrier below
+    }
+    if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 0;
+    // merge the position groups: first those sharing a warp (shuffles), then
+    // the warps' groups park (m, l) per head and acc in smem (xv, free between
+    // QKV and the FFN norm); after the caller's barrier each output element is
+    // rescaled to the group-wide maximum and summed
+    A::merge_warp(m_, l_, acc);
+    if (!ab) A::park(s, m_, l_, acc);
+    return ab;
+}
 
 // ------------------------------------------------------------------ the kernel
 
 // HD: head_dim; G: query heads per KV head; MH = H / 256, the 8-column chunks
-// each lane owns in a row of H (the GEMV width of QKV, gate/up and LM head).
-template <int HD, int G, int MH>
+// each lane owns in a row of H (the GEMV width of QKV, gate/up and LM head);
+// LC: long-context build (two query heads per attention lane where the shape
+// allows: fewer instructions per position when a CTA attends to thousands of
+// positions, more registers held, slower on short contexts).
+template <int HD, int G, int MH, int LC>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
     static_assert(G <= MK_NCW, "one consumer warp per query head of a KV group (softmax, combine weights)");
     constexpr int KO = G * HD;                         // O-proj row length
@@ -1013,76 +1147,32 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
         // ---------------- segment B: split-K attention over this CTA's positions
         {
-            using A = Attn<HD, G>;
-            const int h_ = (t % A::TPP) / A::DC, dc_ = t % A::DC;
-            float qr[8], acc[8];
+            // stage K[pos], V[pos] (bf16) from their tagged copies (last CTA of the group)
             bool late = false;
-            if (!ab) {
-                // this thread's 8 query dims: tagged words written by the group this launch
-                float qv[8];
-                late = !ll_read8(p, p.qll + (size_t)l * g.qh * HD + ((size_t)pl.g * G + h_) * HD + dc_ * 8, s.misc->tag, qv);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) qr[e] = qv[e] * qscale;
-                if (has_cur && t < HD / 4 && !late) {   // stage K[pos], V[pos] (bf16) from their tagged copies
-                    float kv[8];
-                    late = !ll_read8(p, p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (t < HD / 8 ? 0 : 1)) * HD +
-                                            (t % (HD / 8)) * 8, s.misc->tag, kv);
-                    uint4 w;
-                    w.x = (uint32_t)f2bf(kv[0]) | ((uint32_t)f2bf(kv[1]) << 16);
-                    w.y = (uint32_t)f2bf(kv[2]) | ((uint32_t)f2bf(kv[3]) << 16);
-                    w.z = (uint32_t)f2bf(kv[4]) | ((uint32_t)f2bf(kv[5]) << 16);
-                    w.w = (uint32_t)f2bf(kv[6]) | ((uint32_t)f2bf(kv[7]) << 16);
-                    s.misc->stage[t] = w;
-                }
+            if (!ab && has_cur && t < HD / 4) {
+                float kv[8];
+                late = !ll_read8(p, p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (t < HD / 8 ? 0 : 1)) * HD +
+                                        (t % (HD / 8)) * 8, s.misc->tag, kv);
+                uint4 w;
+                w.x = (uint32_t)f2bf(kv[0]) | ((uint32_t)f2bf(kv[1]) << 16);
+                w.y = (uint32_t)f2bf(kv[2]) | ((uint32_t)f2bf(kv[3]) << 16);
+                w.z = (uint32_t)f2bf(kv[4]) | ((uint32_t)f2bf(kv[5]) << 16);
+                w.w = (uint32_t)f2bf(kv[6]) | ((uint32_t)f2bf(kv[7]) << 16);
+                s.misc->stage[t] = w;
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-            float m_ = -INFINITY, l_ = 0.f;
-            ab = bar_or(ab || late);
             // Blocks of up to KB past positions from the ring (the K tile and
             // the V tile of a block are held together); the last CTA of the
             // group appends the current position (staged) to its last block,
             // or runs it as a block of its own when it has no past.
             const int nring = ke > ka ? ke - ka : 0;
             const int nblk = (nring + g.KB - 1) / g.KB;
-            const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
-            const uint8_t* st = reinterpret_cast<const uint8_t*>(s.misc->stage);
-            // several K/V blocks (long contexts) stream like weights: lift the
-            // producer's latency-phase in-flight limit for the block loop
-            if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 1;
-            for (int b = 0; b < nbt && !ab; ++b) {
-                const int q0 = ka + b * g.KB;
-                const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
-                const int n = nr + ((has_cur && b == nbt - 1) ? 1 : 0);
-                const uint8_t *kt = st, *vt = st;
-                bool ok = true;
-                if (nr > 0) {
-                    Ring rv = ring;
-                    rv.advance(g.ns);      // the V tile follows the K tile in the stream
-                    ok = take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt) &&
-                         take_tile(p, s, rv, (uint32_t)(nr * HD * 2), vt);
-                }
-                if (ok) A::online(kt, vt, nr, st, n, qr, m_, l_, acc);
-                if (nr > 0) { release_tile(p, s, ring); release_tile(p, s, ring); }
-                if (!ok) ab = true;     // made uniform by the barrier below
-            }
-            if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 0;
-            // merge the position groups: each parks (m, l) per head and its
-            // 8 dims of acc in smem ([position group][G*HD] in xv, free between
-            // QKV and the FFN norm); after the barrier each output element is
-            // rescaled to the group-wide maximum and summed
-            if (!ab) {
-                const int pp = t / A::TPP;
-                float4* sp = reinterpret_cast<float4*>(s.xv + pp * (G * HD) + h_ * HD + dc_ * 8);
-                sp[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                sp[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-                if (dc_ == 0) { s.sc[pp * G + h_] = m_; s.sc[A::PPP * G + pp * G + h_] = l_; }
-            }
+            (void)nblk;
+            ab = attn_run<HD, G, (LC && attn_long_ok<HD, G>()) ? 2 : 1>(p, s, ring, l, ka, ke, has_cur, qscale, ab, late);
         }
         ab = bar_or(ab);
         constexpr int PSTR = G * HD + 2 * G;                   // tagged words per partial
         if (!ab && !(p.dbg_skip_sync == 4 * l + 1 && p.dbg_skip_cta == c)) {
-            constexpr int PPP = Attn<HD, G>::PPP;
+            constexpr int PPP = Attn<HD, G>::NMG;               // parked groups (the same for both lane layouts)
             uint64_t* dst = p.partll + (((size_t)l * g.kvh + pl.g) * g.CPG + pl.i) * PSTR;
             for (int i = t; i < G * HD; i += MK_NCT) {
                 const int h = i / HD;

@@ -57,7 +57,7 @@ class mk_info(ctypes.Structure):
     _fields_ = [("grid_ctas", _i32), ("ctas_per_group", _i32), ("block_threads", _i32), ("ring_stages", _i32),
                 ("slot_bytes", _i32), ("smem_bytes", _i32), ("sm_count", _i32), ("l2_prefetch_bytes", _i32),
                 ("arena_bytes", _i64), ("weight_bytes_per_token", _i64), ("kv_bytes_per_position", _i64),
-                ("device_bytes", _i64)]
+                ("device_bytes", _i64), ("long_context", _i32)]
 
 
 # (name, restype, argtypes) of every exported function, in header order.

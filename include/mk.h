@@ -106,6 +106,9 @@ typedef struct {
     int64_t weight_bytes_per_token;  /* bf16 weight bytes one step reads (matrices + gains + 1 embedding row) */
     int64_t kv_bytes_per_position;   /* bf16 K+V bytes one attended position costs (all layers) */
     int64_t device_bytes;            /* everything the context allocated on the device */
+    int32_t long_context;            /* 1: the kernel build for long contexts runs (max_seq >= 8192
+                                        and one was built for this shape: two query heads per
+                                        attention lane, fewer instructions per cached position) */
 } mk_info;
 
 /* Create a context on CUDA device `device`: validates the shape, sizes the

@@ -71,6 +71,24 @@ def test_mid_shape_ragged(grid, prefill):
     dec.close()
 
 
+@pytest.mark.parametrize("grid,prefill", [(0, 5001), (6, 3000)])
+def test_long_context_build(grid, prefill):
+    """max_seq >= 8192 selects the long-context kernel build (two query heads
+    per attention lane) for H=512, G=4; a 5001-position prefill on the full grid
+    (ragged per-CTA chunks) and 3000 positions on 3 CTAs per KV group (each CTA
+    walks about a thousand positions, many KV blocks)."""
+    tun = mk.tuning(grid_ctas=grid) if grid else None
+    m, dec, orc = make(MID, 47, 8192, gains="normal", std=0.04, tuning=tun)
+    assert dec.info.long_context == 1
+    ks, vs = synth.make_kv(MID, prefill, 53)
+    dec.set_kv(ks, vs, prefill)
+    orc.set_kv(ks, vs, prefill)
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, MID.vocab, 47, 3), prefill, 8)
+    print(rep.summary())
+    rep.check()
+    dec.close()
+
+
 def test_head_dim_128_shape():
     s = synth.ModelShape(2, 1024, 8, 2, 128, 1536, 4099, 1e-5, 500000.0, False)
     m, dec, orc = make(s, 31, 512, gains="normal", std=0.03)
