@@ -252,6 +252,7 @@ struct mk_ctx {
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
     int trace_detail = 1;
     int inflight = 0, inflight_lat = 0;
+    int pf_lead_tiles = -1, pf_depth = 0;  // L2 warmer (debug knobs; -1 / 0 = defaults)
     int64_t wait_limit_ns = 1000000000LL;
     unsigned long long* trace = nullptr;
     // per-operator baseline
@@ -303,6 +304,8 @@ MkParams base_params(const mk_ctx* c) {
     p.trace_detail = c->trace_detail;
     p.inflight = c->inflight > 0 ? c->inflight : 3;
     p.inflight_lat = c->inflight_lat > 0 ? c->inflight_lat : 1;
+    p.pf_lead_bytes = (c->pf_lead_tiles >= 0 ? c->pf_lead_tiles : c->geo.ns) * c->geo.slot;
+    p.pf_depth = c->pf_depth > 0 ? c->pf_depth : 1;
     p.wait_limit_ns = c->wait_limit_ns;
     p.trace = c->trace;
     p.out_idx = 0;
@@ -833,6 +836,16 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_INFLIGHT || knob == MK_DBG_INFLIGHT_LAT) {
         if (value < 0 || value > 16) return MK_ERR_INVALID_ARG;
         (knob == MK_DBG_INFLIGHT ? c->inflight : c->inflight_lat) = (int)value;
+        return MK_OK;
+    }
+    if (knob == MK_DBG_PF_LEAD) {
+        if (value < -1 || value > 64) return MK_ERR_INVALID_ARG;
+        c->pf_lead_tiles = (int)value;
+        return MK_OK;
+    }
+    if (knob == MK_DBG_PF_DEPTH) {
+        if (value < 0 || value > 2) return MK_ERR_INVALID_ARG;
+        c->pf_depth = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_TRACE_DETAIL) {

@@ -180,6 +180,7 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     int par;
     int is_last;
     unsigned long long copy_bytes;  // bytes issued by the copy producer (paces the L2 prefetcher)
+    uint32_t pf_sink;               // the L2 warmer's xor of what it loaded (keeps the loads)
     unsigned long long cwait;       // trace: ns thread 0 spent waiting for ring data
     float alpha[8];          // per head: 1 / (sum of the combine weights)
     float best_val[64];
@@ -218,6 +219,14 @@ struct Smem {
     do {                                                                                  \
         if (MK_TRACE_ON && p.trace && threadIdx.x == 0)                                                  \
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + (slot_)] = gtimer();           \
+    } while (0)
+
+// Detail marks (trace with detail only): slot 1600 + 8*layer + (ev_), thread 0's
+// time, for the first 24 layers.
+#define MK_TRACE_D(l_, ev_)                                                              \
+    do {                                                                                  \
+        if (MK_TRACE_ON && p.trace && p.trace_detail && threadIdx.x == 0 && (l_) < 24)    \
+            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1600 + 8 * (l_) + (ev_)] = gtimer(); \
     } while (0)
 
 // Per-phase consumer ring-wait (trace only): slot 1024 + 8*layer + phase.
@@ -278,12 +287,20 @@ __device__ __forceinline__ bool ll_backoff(const MkParams& p, uint64_t& t0) {
     __nanosleep(64);
     return true;
 }
-// Reads 8 tagged words (16-byte aligned) once all carry `tag`.
-__device__ __forceinline__ bool ll_read8(const MkParams& p, const uint64_t* src, uint32_t tag, float v[8]) {
-    uint64_t t0 = 0;
+// Reads 8 tagged words (16-byte aligned) once all carry `tag`.  stat (trace
+// only): polls made, ns of the first poll, ns in total.
+__device__ __forceinline__ bool ll_read8(const MkParams& p, const uint64_t* src, uint32_t tag, float v[8],
+                                         unsigned long long* stat = nullptr) {
+    uint64_t t0 = 0, ts = stat ? gtimer() : 0;
     for (;;) {
         const ulonglong2 a = ld_ll2(src), b = ld_ll2(src + 2), c = ld_ll2(src + 4), d = ld_ll2(src + 6);
-        if (ll_ok(a, tag) & ll_ok(b, tag) & ll_ok(c, tag) & ll_ok(d, tag)) {
+        const bool all = ll_ok(a, tag) & ll_ok(b, tag) & ll_ok(c, tag) & ll_ok(d, tag);
+        if (stat) {
+            const uint64_t now = gtimer();
+            if (stat[0]++ == 0) stat[1] = now - ts;
+            stat[2] = now - ts;
+        }
+        if (all) {
             v[0] = __uint_as_float((uint32_t)a.x); v[1] = __uint_as_float((uint32_t)a.y);
             v[2] = __uint_as_float((uint32_t)b.x); v[3] = __uint_as_float((uint32_t)b.y);
             v[4] = __uint_as_float((uint32_t)c.x); v[5] = __uint_as_float((uint32_t)c.y);
@@ -337,7 +354,7 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
         if (!wait_mbar(p, &s.empty[slot], ph ^ 1u, abort)) { stop = true; return; }
         if (tr) {
             pwait += gtimer() - tw;
-            if ((k & 15u) == 0 && 1536 + (k >> 4) < MK_TRACE_STRIDE) tr[1536 + (k >> 4)] = pwait;
+            if ((k & 15u) == 0 && (k >> 4) < 64) tr[1536 + (k >> 4)] = pwait;
         }
         s.misc->tile_bytes[slot] = bytes;
         *(volatile int*)&s.misc->slot_tile[slot] = (int)k;
@@ -363,29 +380,36 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
 }
 
 // L2 warmer (the whole prefetch warp): walks the same tile stream as the copy
-// producer, at most l2_pf_bytes ahead of its copies, and brings each tile's
-// 128-byte lines into L2 with one plain 4-byte load per line, so the copy
-// later reads L2 instead of HBM.  (Measured: a plain load per line leaves the
-// whole line in L2 for a later bulk copy; prefetch.global.L2 and non-coherent
-// loads do so only in part.)  It works only while the consumers are
-// latency-bound, when HBM is otherwise idle, and waits for each tile's loads
-// before the next, so at most one tile of warming loads is in flight.
+// producer and brings tiles' 128-byte lines into L2 with one plain 4-byte load
+// per line, so the copy later reads L2 instead of HBM.  (Measured: a plain
+// load per line leaves the whole line in L2 for a later bulk copy;
+// prefetch.global.L2 and non-coherent loads do so only in part.)  It leaves
+// the first pf_lead_bytes past the copy cursor alone -- the ring fetches those
+// as soon as consumers free slots -- and warms at most l2_pf_bytes beyond
+// them.  It works only while the consumers are latency-bound, when HBM is
+// otherwise idle, with pf_depth tiles of warming loads in flight.
 __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const Smem& s) {
     if (p.l2_pf_bytes <= 0) return;
     const int lane = threadIdx.x & 31;
     volatile int* abort = &s.misc->abort;
     const unsigned long long ahead = (unsigned long long)p.l2_pf_bytes;
+    const unsigned long long lead = (unsigned long long)p.pf_lead_bytes;
+    const bool two = p.pf_depth > 1;
     unsigned long long issued = 0;
-    uint32_t sink = 0;
+    uint32_t sink = 0, prev = 0, kw = 0;
     bool stop = false;
+    unsigned long long* tr = (MK_TRACE_ON && p.trace && p.trace_detail && lane == 0)
+                                 ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
     walk_tiles(p, pl, [&](const void* src, uint32_t bytes) {
         if (stop) return;
         uint64_t t0 = 0;
+        const uint32_t kt = kw++;
         for (;;) {
             const unsigned long long cb = *(volatile unsigned long long*)&s.misc->copy_bytes;
             const bool streaming = *(volatile int*)&s.misc->streaming;
-            if (issued + bytes <= cb) break;   // already copied: nothing to warm
-            if (!streaming && issued <= cb + ahead) {
+            if (issued + bytes <= cb + lead) break;   // copied, or the ring fetches it next
+            if (!streaming && issued <= cb + lead + ahead) {
+                if (tr && kt < 256) tr[1792 + kt] = gtimer();   // trace: when tile kt was warmed
                 const char* b = reinterpret_cast<const char*>(src);
                 uint32_t acc = 0;
                 for (uint32_t off = (uint32_t)lane * 128u; off < bytes; off += 32u * 128u) {
@@ -393,8 +417,14 @@ __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const 
                     asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(b + off) : "memory");
                     acc ^= v;
                 }
-                // consumed here, in order with the loads: the next tile's loads wait for these
-                asm volatile("xor.b32 %0, %0, %1;" : "+r"(sink) : "r"(acc));
+                // consumed in order with the loads: with depth 1 the next tile's
+                // loads wait for these, with depth 2 for the previous tile's
+                if (two) {
+                    asm volatile("xor.b32 %0, %0, %1;" : "+r"(sink) : "r"(prev));
+                    prev = acc;
+                } else {
+                    asm volatile("xor.b32 %0, %0, %1;" : "+r"(sink) : "r"(acc));
+                }
                 break;
             }
             if (*abort) { stop = true; return; }
@@ -404,7 +434,10 @@ __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const 
         }
         issued += bytes;
     });
-    if (sink == 0x9E3779B9u && lane == 32) s.misc->abort = 2;   // never true (lane < 32): keeps the loads
+    asm volatile("xor.b32 %0, %0, %1;" : "+r"(sink) : "r"(prev));
+    // a real use of every loaded word: without it the compiler may drop the
+    // xors and with them the loads (or the waits for them)
+    if (lane == 0) *(volatile uint32_t*)&s.misc->pf_sink = sink;
 }
 
 // ------------------------------------------------------------------ consumer pieces
@@ -941,6 +974,7 @@ template <int HD, int G, int HPL>
 __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
                                          bool has_cur, float qscale, bool ab, bool late) {
     using A = Attn<HD, G, HPL>;
+    MK_TRACE_D(l, 5);        // attention entered
     const MkGeom& g = p.geo;
     const MkCtaPlan& pl = s.misc->plan;
     const int t = threadIdx.x;
@@ -951,12 +985,20 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
         for (int j = 0; j < HPL; ++j) {
             float qv[8];
             const int h = hg_ * HPL + j;
-            if (!ll_read8(p, p.qll + (size_t)l * g.qh * HD + ((size_t)pl.g * G + h) * HD + dc_ * 8, s.misc->tag, qv))
+            unsigned long long st3[3] = {0, 0, 0};
+            const bool tr = MK_TRACE_ON && p.trace && p.trace_detail && t == 0 && j == 0 && l < 24;
+            if (!ll_read8(p, p.qll + (size_t)l * g.qh * HD + ((size_t)pl.g * G + h) * HD + dc_ * 8, s.misc->tag, qv,
+                          tr ? st3 : nullptr))
                 late = true;
+            if (tr) {
+                unsigned long long* o = p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE + 1600 + 8 * l + 6;
+                o[0] = st3[1];   // ns of the first poll
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) qr[j][e] = qv[e] * qscale;
         }
     }
+    MK_TRACE_D(l, 0);   // thread 0 has its q
     float m_[HPL], l_[HPL];
     float2 acc[HPL][4];
 #pragma unroll
@@ -967,6 +1009,7 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
         for (int k = 0; k < 4; ++k) acc[j][k] = make_float2(0.f, 0.f);
     }
     ab = bar_or(ab || late);
+    MK_TRACE_D(l, 1);   // every thread has its q
     const int nring = ke > ka ? ke - ka : 0;
     const int nblk = (nring + g.KB - 1) / g.KB;
     const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
@@ -990,6 +1033,7 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
         if (!ok) ab = true;     // made uniform by the barrier below
     }
     if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 0;
+    MK_TRACE_D(l, 2);   // softmax over the blocks done
     // merge the position groups: first those sharing a warp (shuffles), then
     // the warps' groups park (m, l) per head and acc in smem (xv, free between
     // QKV and the FFN norm); after the caller's barrier each output element is
@@ -1146,6 +1190,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 4);
 
         // ---------------- segment B: split-K attention over this CTA's positions
+        MK_TRACE_D(l, 7);        // segment B entered
         {
             // stage K[pos], V[pos] (bf16) from their tagged copies (last CTA of the group)
             bool late = false;
@@ -1256,7 +1301,9 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     if (!ll_backoff(p, t0)) { late = true; break; }
                 }
             }
+            MK_TRACE_D(l, 3);   // thread 0's first partials arrived
             if (bar_or(late)) ab = true;
+            MK_TRACE_D(l, 4);   // every thread's first partials arrived
             if (!ab && (t >> 5) < G) {   // warp h: head h, lanes over the partials
                 const int hh = t >> 5, ln = t & 31;
                 float mx = -INFINITY;

@@ -31,6 +31,8 @@ MK_DBG_TRACE = 3
 MK_DBG_TRACE_DETAIL = 5
 MK_DBG_INFLIGHT = 6
 MK_DBG_INFLIGHT_LAT = 7
+MK_DBG_PF_LEAD = 8
+MK_DBG_PF_DEPTH = 9
 MK_NOALLOC_ARGMAX_BLOCKS = 1024
 MK_NOALLOC_ARGMAX_MAX_N = MK_NOALLOC_ARGMAX_BLOCKS * 4096
 

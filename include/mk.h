@@ -237,6 +237,14 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
  * limit applies during the streaming segments (gate/up, down, LM head).
  * 0 = the default (1). */
 #define MK_DBG_INFLIGHT_LAT 7
+/* MK_DBG_PF_LEAD: the L2 warmer (tuning l2_prefetch_kib > 0) leaves the first
+ * `value` tiles past the copy producer's cursor alone (the ring fetches those
+ * as soon as slots free up) and warms the tiles after them; 0..64, -1 = the
+ * default (the ring's slot count). */
+#define MK_DBG_PF_LEAD 8
+/* MK_DBG_PF_DEPTH: tiles of warming loads the L2 warmer keeps in flight,
+ * 1 or 2 (0 = the default, 1). */
+#define MK_DBG_PF_DEPTH 9
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
 const char* mk_strerror(int code);
