@@ -287,20 +287,12 @@ __device__ __forceinline__ bool ll_backoff(const MkParams& p, uint64_t& t0) {
     __nanosleep(64);
     return true;
 }
-// Reads 8 tagged words (16-byte aligned) once all carry `tag`.  stat (trace
-// only): polls made, ns of the first poll, ns in total.
-__device__ __forceinline__ bool ll_read8(const MkParams& p, const uint64_t* src, uint32_t tag, float v[8],
-                                         unsigned long long* stat = nullptr) {
-    uint64_t t0 = 0, ts = stat ? gtimer() : 0;
+// Reads 8 tagged words (16-byte aligned) once all carry `tag`.
+__device__ __forceinline__ bool ll_read8(const MkParams& p, const uint64_t* src, uint32_t tag, float v[8]) {
+    uint64_t t0 = 0;
     for (;;) {
         const ulonglong2 a = ld_ll2(src), b = ld_ll2(src + 2), c = ld_ll2(src + 4), d = ld_ll2(src + 6);
-        const bool all = ll_ok(a, tag) & ll_ok(b, tag) & ll_ok(c, tag) & ll_ok(d, tag);
-        if (stat) {
-            const uint64_t now = gtimer();
-            if (stat[0]++ == 0) stat[1] = now - ts;
-            stat[2] = now - ts;
-        }
-        if (all) {
+        if (ll_ok(a, tag) & ll_ok(b, tag) & ll_ok(c, tag) & ll_ok(d, tag)) {
             v[0] = __uint_as_float((uint32_t)a.x); v[1] = __uint_as_float((uint32_t)a.y);
             v[2] = __uint_as_float((uint32_t)b.x); v[3] = __uint_as_float((uint32_t)b.y);
             v[4] = __uint_as_float((uint32_t)c.x); v[5] = __uint_as_float((uint32_t)c.y);
@@ -979,26 +971,43 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
     const MkCtaPlan& pl = s.misc->plan;
     const int t = threadIdx.x;
     const int hg_ = (t % A::TPP) / A::DC, dc_ = t % A::DC;
+    // q of the group's G heads (G*HD tagged words): every 16-byte chunk is
+    // polled by one thread, consecutive chunks by consecutive lanes, so one
+    // warp instruction reads four whole 128-byte lines and the CTA reads each
+    // line once (had every thread read the q values it needs, the 12 position
+    // groups would read the same words, ~48x the requests on the same L2
+    // lines, in all CTAs of the group at once).  They meet in `ov`, free until
+    // the combine.
+    constexpr int NQC = G * HD / 2;
+    float* qs = s.ov;
+    if (!ab) {
+        const uint32_t tag = s.misc->tag;
+        const uint64_t* qsrc = p.qll + (size_t)l * g.qh * HD + (size_t)pl.g * G * HD;
+        for (int c = t; c < NQC && !late; c += MK_NCT) {
+            uint64_t t0 = 0;
+            for (;;) {
+                const ulonglong2 w = ld_ll2(qsrc + 2 * c);
+                if (ll_ok(w, tag)) {
+                    *reinterpret_cast<float2*>(qs + 2 * c) =
+                        make_float2(__uint_as_float((uint32_t)w.x), __uint_as_float((uint32_t)w.y));
+                    break;
+                }
+                if (!ll_backoff(p, t0)) { late = true; break; }
+            }
+        }
+    }
+    ab = bar_or(ab || late);
+    MK_TRACE_D(l, 0);   // q in shared memory
     float qr[HPL][8];
     if (!ab) {
 #pragma unroll
         for (int j = 0; j < HPL; ++j) {
-            float qv[8];
-            const int h = hg_ * HPL + j;
-            unsigned long long st3[3] = {0, 0, 0};
-            const bool tr = MK_TRACE_ON && p.trace && p.trace_detail && t == 0 && j == 0 && l < 24;
-            if (!ll_read8(p, p.qll + (size_t)l * g.qh * HD + ((size_t)pl.g * G + h) * HD + dc_ * 8, s.misc->tag, qv,
-                          tr ? st3 : nullptr))
-                late = true;
-            if (tr) {
-                unsigned long long* o = p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE + 1600 + 8 * l + 6;
-                o[0] = st3[1];   // ns of the first poll
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qr[j][e] = qv[e] * qscale;
+            const float4* q4 = reinterpret_cast<const float4*>(qs + (hg_ * HPL + j) * HD + dc_ * 8);
+            const float4 a = q4[0], b = q4[1];
+            qr[j][0] = a.x * qscale; qr[j][1] = a.y * qscale; qr[j][2] = a.z * qscale; qr[j][3] = a.w * qscale;
+            qr[j][4] = b.x * qscale; qr[j][5] = b.y * qscale; qr[j][6] = b.z * qscale; qr[j][7] = b.w * qscale;
         }
     }
-    MK_TRACE_D(l, 0);   // thread 0 has its q
     float m_[HPL], l_[HPL];
     float2 acc[HPL][4];
 #pragma unroll
@@ -1008,7 +1017,6 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[j][k] = make_float2(0.f, 0.f);
     }
-    ab = bar_or(ab || late);
     MK_TRACE_D(l, 1);   // every thread has its q
     const int nring = ke > ka ? ke - ka : 0;
     const int nblk = (nring + g.KB - 1) / g.KB;
