@@ -98,6 +98,9 @@ MK_HD bool mk_geom_init(MkGeom& g, int L, int H, int qh, int kvh, int hd, int F,
     g.NP = (g.G + 2) * (hd / 2);
     g.slot = slot_bytes;
     g.ns = ns;
+    // a consumer lane holds its share of a hidden-width tile in registers
+    // (16 chunks of 16 bytes at most): slots of 32 KB at most
+    if (slot_bytes > 32768) return false;
     g.TRh = mk_tile_rows(H, slot_bytes);
     g.TRo = mk_tile_rows(g.G * hd, slot_bytes);
     g.JT = g.TRh / 2;

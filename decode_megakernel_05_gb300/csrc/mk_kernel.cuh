@@ -683,6 +683,7 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
     constexpr int K = W::K, NKB = W::NKB, CPL = W::CPL, NRS = W::NRS, WPG = W::WPG;
     constexpr int PS = WidePart<MH>::NKB;
     static_assert(W::ok && NKB <= PS, "wide GEMV mapping");
+    constexpr int RPW = 16 / CPL;   // rows of a tile per warp at most (16 chunks per lane: slots of 32 KB at most)
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = w / WPG, wg = w % WPG;
     const int cb = wg % NKB, rs = wg / NKB;
@@ -699,48 +700,69 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
         const int R0 = ti * TR, R = min(TR, nrows - R0);
         const uint8_t* tile;
         const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
-        if (ok) {
-            int r = rs - R0 % NRS;
-            if (r < 0) r += NRS;
-            for (; r < R; r += 4 * NRS) {          // rows r, r + NRS, r + 2 NRS, r + 3 NRS
-                const int nv = min(4, (R - r + NRS - 1) / NRS);
-                float2 a[4][2];
+        // this warp's rows of the tile: r0, r0 + NRS, ... (nrow of them)
+        int r0 = rs - R0 % NRS;
+        if (r0 < 0) r0 += NRS;
+        const int nrow = (ok && r0 < R) ? (R - r0 + NRS - 1) / NRS : 0;
+        // rows qb .. qb+3 of the share: dot products, transposed butterfly (lane
+        // bit 4 picks rows {0,1} / {2,3}, bit 3 one row of the pair; bits 0-2
+        // finish the sum) and the column-block partials into `part`
+        auto pass = [&](int qb, auto&& chunk) {
+            const int nv = min(4, nrow - qb);
+            float2 a[4][2];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) a[q][0] = a[q][1] = make_float2(0.f, 0.f);
-                const uint8_t* rp = tile + (size_t)r * (K * 2);
+            for (int q = 0; q < 4; ++q) a[q][0] = a[q][1] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int j = 0; j < CPL; ++j) {
-                    const int ch = (cb * CPL + j) * 32 + lane;
+            for (int j = 0; j < CPL; ++j)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (q < nv) fma_chunk(lds128(rp + (size_t)q * NRS * (K * 2) + ch * 16), xl[j], xh[j], a[q][0], a[q][1]);
-                }
-                float v[4];
+                for (int q = 0; q < 4; ++q)
+                    if (qb + q < nrow) fma_chunk(chunk(qb + q, j), xl[j], xh[j], a[q][0], a[q][1]);
+            float v[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) v[q] = (a[q][0].x + a[q][0].y) + (a[q][1].x + a[q][1].y);
-                // transposed butterfly: lane bit 4 picks rows {0,1} / {2,3},
-                // bit 3 one row of the pair; bits 0-2 finish the sum
-                const bool up = lane & 16, b3 = lane & 8;
-                float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
-                k0 += __shfl_xor_sync(0xFFFFFFFFu, up ? v[0] : v[2], 16);
-                k1 += __shfl_xor_sync(0xFFFFFFFFu, up ? v[1] : v[3], 16);
-                float kk = b3 ? k1 : k0;
-                kk += __shfl_xor_sync(0xFFFFFFFFu, b3 ? k0 : k1, 8);
-                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 4);
-                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 2);
-                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 1);
-                const int q = lane >> 3;               // row of the four this lane holds
-                if ((lane & 7) == 0 && q < nv) {
-                    float* pr = part + (R0 + r + q * NRS) * PS;
-                    pr[cb] = kk;
-                    if (NKB < PS && cb == 0) {     // unused column-block slots read as zero
+            for (int q = 0; q < 4; ++q) v[q] = (a[q][0].x + a[q][0].y) + (a[q][1].x + a[q][1].y);
+            const bool up = lane & 16, b3 = lane & 8;
+            float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
+            k0 += __shfl_xor_sync(0xFFFFFFFFu, up ? v[0] : v[2], 16);
+            k1 += __shfl_xor_sync(0xFFFFFFFFu, up ? v[1] : v[3], 16);
+            float kk = b3 ? k1 : k0;
+            kk += __shfl_xor_sync(0xFFFFFFFFu, b3 ? k0 : k1, 8);
+            kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 4);
+            kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 2);
+            kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 1);
+            const int q = lane >> 3;               // row of the four this lane holds
+            if ((lane & 7) == 0 && q < nv) {
+                float* pr = part + (R0 + r0 + (qb + q) * NRS) * PS;
+                pr[cb] = kk;
+                if (NKB < PS && cb == 0) {         // unused column-block slots read as zero
 #pragma unroll
-                        for (int c2 = NKB; c2 < PS; ++c2) pr[c2] = 0.f;
-                    }
+                    for (int c2 = NKB; c2 < PS; ++c2) pr[c2] = 0.f;
                 }
             }
+        };
+        auto at = [&](int q, int j) {              // this lane's 16 bytes of row q, chunk j of the share
+            return tile + (size_t)(r0 + q * NRS) * (K * 2) + ((cb * CPL + j) * 32 + lane) * 16;
+        };
+        if constexpr (CPL <= 2) {
+            // Load the warp's whole share of the tile, then release the slot at
+            // once: the copy producer refills it while this warp computes (the
+            // arrival's release semantics order it after these loads).
+            uint4 wv[RPW][CPL];
+#pragma unroll
+            for (int q = 0; q < RPW; ++q)
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) wv[q][j] = q < nrow ? lds128(at(q, j)) : make_uint4(0u, 0u, 0u, 0u);
+            release_tile(p, s, ring, (uint32_t)NG);
+#pragma unroll
+            for (int qb = 0; qb < RPW; qb += 4)
+                if (qb < nrow) pass(qb, [&](int q, int j) { return wv[q][j]; });
+        } else {
+            // four or more activation chunks per lane: the share would not fit
+            // the registers beside them, so it is read as used, released after
+#pragma unroll
+            for (int qb = 0; qb < RPW; qb += 4)
+                if (qb < nrow) pass(qb, [&](int q, int j) { return lds128(at(q, j)); });
+            release_tile(p, s, ring, (uint32_t)NG);
         }
-        release_tile(p, s, ring, (uint32_t)NG);
         if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
     }
     return bar_or(ab);
@@ -1425,23 +1447,53 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 const int n = min(g.JD, pl.nj - j0);
                 const uint8_t* tile;
                 const bool ok = take_tile(p, s, ring, (uint32_t)(n * H * 2), tile);
-                if (ok) {
-#pragma unroll (CPT <= 2 ? 2 : 1)
-                    for (int jj = 0; jj < n; ++jj) {
-                        const float uj = s.u[j0 + jj];
-                        const float2 u2 = make_float2(uj, uj);
-                        const uint8_t* col = tile + (size_t)jj * H * 2;
+                if constexpr (TP == 128 && CPT <= 2 && !LC) {
+                    // a thread's share is 16 chunks (slots of 32 KB): loaded
+                    // whole, then the slot is released before the arithmetic
+                    // (not in the long-context build, whose attention already
+                    // holds more registers)
+                    constexpr int NJ = 16 / CPT;
+                    uint4 wv[NJ][CPT];
 #pragma unroll
-                        for (int m = 0; m < CPT; ++m) {
-                            const uint4 w = lds128(col + (size_t)(tp + m * TP) * 16);
-                            da[m][0] = __ffma2_rn(bf2_lo_hi(w.x), u2, da[m][0]);
-                            da[m][1] = __ffma2_rn(bf2_lo_hi(w.y), u2, da[m][1]);
-                            da[m][2] = __ffma2_rn(bf2_lo_hi(w.z), u2, da[m][2]);
-                            da[m][3] = __ffma2_rn(bf2_lo_hi(w.w), u2, da[m][3]);
+                    for (int jj = 0; jj < NJ; ++jj)
+#pragma unroll
+                        for (int m = 0; m < CPT; ++m)
+                            wv[jj][m] = (ok && jj < n) ? lds128(tile + (size_t)jj * H * 2 + (size_t)(tp + m * TP) * 16)
+                                                       : make_uint4(0u, 0u, 0u, 0u);
+                    release_tile(p, s, ring, (uint32_t)P);  // TP / 32 readers, weight P each
+#pragma unroll
+                    for (int jj = 0; jj < NJ; ++jj) {
+                        if (ok && jj < n) {
+                            const float uj = s.u[j0 + jj];
+                            const float2 u2 = make_float2(uj, uj);
+#pragma unroll
+                            for (int m = 0; m < CPT; ++m) {
+                                da[m][0] = __ffma2_rn(bf2_lo_hi(wv[jj][m].x), u2, da[m][0]);
+                                da[m][1] = __ffma2_rn(bf2_lo_hi(wv[jj][m].y), u2, da[m][1]);
+                                da[m][2] = __ffma2_rn(bf2_lo_hi(wv[jj][m].z), u2, da[m][2]);
+                                da[m][3] = __ffma2_rn(bf2_lo_hi(wv[jj][m].w), u2, da[m][3]);
+                            }
                         }
                     }
+                } else {
+                    if (ok) {
+#pragma unroll (CPT <= 2 ? 2 : 1)
+                        for (int jj = 0; jj < n; ++jj) {
+                            const float uj = s.u[j0 + jj];
+                            const float2 u2 = make_float2(uj, uj);
+                            const uint8_t* col = tile + (size_t)jj * H * 2;
+#pragma unroll
+                            for (int m = 0; m < CPT; ++m) {
+                                const uint4 w = lds128(col + (size_t)(tp + m * TP) * 16);
+                                da[m][0] = __ffma2_rn(bf2_lo_hi(w.x), u2, da[m][0]);
+                                da[m][1] = __ffma2_rn(bf2_lo_hi(w.y), u2, da[m][1]);
+                                da[m][2] = __ffma2_rn(bf2_lo_hi(w.z), u2, da[m][2]);
+                                da[m][3] = __ffma2_rn(bf2_lo_hi(w.w), u2, da[m][3]);
+                            }
+                        }
+                    }
+                    release_tile(p, s, ring, (uint32_t)P);  // TP / 32 readers, weight P each
                 }
-                release_tile(p, s, ring, (uint32_t)P);      // TP / 32 readers, weight P each
                 if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
             }
             MK_TRACE(16 * l + 14);
