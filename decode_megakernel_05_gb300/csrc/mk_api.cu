@@ -849,7 +849,7 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
         return MK_OK;
     }
     if (knob == MK_DBG_TRACE_DETAIL) {
-        if (value != 0 && value != 1) return MK_ERR_INVALID_ARG;
+        if (value < 0 || value > 2) return MK_ERR_INVALID_ARG;
         c->trace_detail = (int)value;
         return MK_OK;
     }

@@ -222,11 +222,12 @@ struct Smem {
     } while (0)
 
 // Detail marks (trace with detail only): slot 1600 + 8*layer + (ev_), thread 0's
-// time, for the first 24 layers.
+// time (detail 2: its SM clock instead, and no per-tile records), for the first 24 layers.
 #define MK_TRACE_D(l_, ev_)                                                              \
     do {                                                                                  \
         if (MK_TRACE_ON && p.trace && p.trace_detail && threadIdx.x == 0 && (l_) < 24)    \
-            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1600 + 8 * (l_) + (ev_)] = gtimer(); \
+            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1600 + 8 * (l_) + (ev_)] =      \
+                p.trace_detail == 2 ? (unsigned long long)clock64() : gtimer();             \
     } while (0)
 
 // Per-phase consumer ring-wait (trace only): slot 1024 + 8*layer + phase.
@@ -326,7 +327,7 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
     uint32_t k = 0;
     bool stop = false;
     unsigned long long pwait = 0;
-    unsigned long long* tr = (MK_TRACE_ON && p.trace && p.trace_detail) ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
+    unsigned long long* tr = (MK_TRACE_ON && p.trace && p.trace_detail == 1) ? p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE : nullptr;
     const uint32_t lim_s = (uint32_t)(p.inflight < ns ? p.inflight : ns);
     const uint32_t lim_l = (uint32_t)(p.inflight_lat < ns ? p.inflight_lat : ns);
     uint32_t slot = 0, ph = 0;   // k mod ns and floor(k / ns) mod 2, kept incrementally
@@ -462,7 +463,7 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     const uint32_t slot = rg.slot(), ph = rg.ph();
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {
-        const uint64_t tw = (MK_TRACE_ON && p.trace && p.trace_detail) ? gtimer() : 0;
+        const uint64_t tw = (MK_TRACE_ON && p.trace && p.trace_detail == 1) ? gtimer() : 0;
         ok = !s.misc->abort;
         if (ok && *(volatile int*)&s.misc->slot_tile[slot] != (int)rg.k) {
             const uint64_t t0 = gtimer();
@@ -492,13 +493,13 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     }
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     tile = s.ring + (size_t)slot * p.geo.slot;
-    if (MK_TRACE_ON && p.trace && p.trace_detail && (threadIdx.x & 31) == 0 && rg.k < 512)   // trace: a reader got tile k
+    if (MK_TRACE_ON && p.trace && p.trace_detail == 1 && (threadIdx.x & 31) == 0 && rg.k < 512)   // trace: a reader got tile k
         p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3072 + rg.k] = gtimer();
     return ok;
 }
 // Done reading tile k; `weight` = MK_NCW / (warps reading it).  Advances the cursor.
 __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, Ring& rg, uint32_t weight = 1) {
-    const uint64_t t2 = (MK_TRACE_ON && p.trace && p.trace_detail && (threadIdx.x & 31) == 0) ? gtimer() : 0;
+    const uint64_t t2 = (MK_TRACE_ON && p.trace && p.trace_detail == 1 && (threadIdx.x & 31) == 0) ? gtimer() : 0;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
         mbar_arrive(&s.empty[rg.slot()], weight);
@@ -513,7 +514,7 @@ __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, R
 // Trace only: lane 0 of each warp stores its ring accounting at slots
 // 2304 + 16 * warp + 3 * e + {0 take, 1 between, 2 release} and clears it.
 __device__ __forceinline__ void trace_ring(const MkParams& p, Ring& rg, int e) {
-    if (MK_TRACE_ON && p.trace && p.trace_detail && (threadIdx.x & 31) == 0) {
+    if (MK_TRACE_ON && p.trace && p.trace_detail == 1 && (threadIdx.x & 31) == 0) {
         unsigned long long* tr = p.trace + (size_t)blockIdx.x * MK_TRACE_STRIDE + 2304 + 16 * (threadIdx.x >> 5) + 3 * e;
         tr[0] = rg.t_take; tr[1] = rg.t_comp; tr[2] = rg.t_rel;
     }
@@ -621,7 +622,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
         const int R = min(TR, nrows - ti * TR);
         const uint8_t* tile;
         const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
-        if (trace_slot >= 0 && MK_TRACE_ON && p.trace && p.trace_detail && threadIdx.x == 0 && ti < 256)
+        if (trace_slot >= 0 && MK_TRACE_ON && p.trace && p.trace_detail == 1 && threadIdx.x == 0 && ti < 256)
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
         if (ok) {
             for (int base = wg * rows_per_warp; base < R; base += wpg * rows_per_warp) {
@@ -988,7 +989,6 @@ template <int HD, int G, int HPL>
 __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
                                          bool has_cur, float qscale, bool ab, bool late) {
     using A = Attn<HD, G, HPL>;
-    MK_TRACE_D(l, 5);        // attention entered
     const MkGeom& g = p.geo;
     const MkCtaPlan& pl = s.misc->plan;
     const int t = threadIdx.x;
@@ -1058,7 +1058,9 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
             rv.advance(g.ns);      // the V tile follows the K tile in the stream
             ok = take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt) && take_tile(p, s, rv, (uint32_t)(nr * HD * 2), vt);
         }
+        if (b == 0) MK_TRACE_D(l, 5);   // first block's K and V taken
         if (ok) A::online(kt, vt, nr, st, n, qr, m_, l_, acc);
+        if (b == 0) MK_TRACE_D(l, 6);   // first block's softmax done
         if (nr > 0) { release_tile(p, s, ring); release_tile(p, s, ring); }
         if (!ok) ab = true;     // made uniform by the barrier below
     }

@@ -224,7 +224,9 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
  * it, 3584 + k time a reader released it. */
 #define MK_DBG_TRACE 3
 /* MK_DBG_TRACE_DETAIL: 1 (default) = the trace also records the per-tile and
- * ring-wait slots; 0 = segment ends only (the least perturbed timing). */
+ * ring-wait slots; 0 = segment ends only (the least perturbed timing); 2 =
+ * segment ends, and the attention and combine detail marks as SM clock counts
+ * (for durations within a CTA) without the per-tile records. */
 #define MK_DBG_TRACE_DETAIL 5
 /* MK_DBG_INFLIGHT: value = most weight tiles each CTA keeps in flight (issued,
  * not yet landed) at once during the streaming segments, 1..16 (0 = the
