@@ -48,6 +48,28 @@ def test_host_only_entry_points():
     assert mk.mk_arena_bytes(wide, None, 152) > 0
 
 
+def test_ring_slot_limit():
+    """A consumer lane holds its share of a hidden-width tile in registers, so
+    ring slots are 32 KB at most; larger requests are refused at planning."""
+    cfg = mk.mk_config(2, 2048, 32, 8, 64, 8192, 1024, 80, 1e-5, 1e4, 1)
+    assert mk.mk_arena_bytes(cfg, mk.tuning(slot_kib=32), 152) > 0
+    assert mk.mk_arena_bytes(cfg, mk.tuning(slot_kib=16), 152) > 0
+    assert mk.mk_arena_bytes(cfg, mk.tuning(slot_kib=64), 152) == -1
+
+
+def test_every_kernel_build_is_in_the_library():
+    """Each (head_dim, q heads per kv head, hidden/256) variant exists twice
+    (without and with the segment trace), and so does each long-context build."""
+    from decode_megakernel_05_gb300 import build
+    lib = mk.load()
+    for hd, g, mh in build.VARIANTS:
+        for pre in ("mk_kernel_ptr_", "mk_kernel_trace_ptr_"):
+            assert hasattr(lib, f"{pre}{hd}_{g}_{mh}"), (pre, hd, g, mh)
+    for hd, g, mh in build.LC_VARIANTS:
+        for pre in ("mk_kernel_ptr_", "mk_kernel_trace_ptr_"):
+            assert hasattr(lib, f"{pre}{hd}_{g}_{mh}_lc"), (pre, hd, g, mh)
+
+
 def test_no_closed_cuda_calls_in_sources():
     """The batched-memcpy family is closed on the GPU pool; no source may name it."""
     pat = re.compile(r"(cuda|cu)Memcpy(3D)?BatchAsync")
