@@ -248,6 +248,7 @@ struct mk_ctx {
     uint32_t *cnt = nullptr, *status = nullptr, *seq = nullptr;
     unsigned long long* amax = nullptr;
     int32_t *next_token = nullptr, *tokens_dev = nullptr, *prompt_dev = nullptr;
+    int32_t* stop = nullptr;             // generation stopped (mk_generate with a stop token)
     // debug
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
     int trace_detail = 1;
@@ -482,7 +483,7 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         (rc = c->dalloc(&c->cnt, (size_t)mk_cnt_total(g) * 4)) || (rc = c->dalloc(&c->status, 4)) ||
         (rc = c->dalloc(&c->seq, 4)) || (rc = c->dalloc(&c->amax, 8)) || (rc = c->dalloc(&c->next_token, 4)) ||
         (rc = c->dalloc(&c->tokens_dev, (size_t)g.max_seq * 4)) ||
-        (rc = c->dalloc(&c->prompt_dev, (size_t)g.max_seq * 4)))
+        (rc = c->dalloc(&c->prompt_dev, (size_t)g.max_seq * 4)) || (rc = c->dalloc(&c->stop, 4)))
         return fail(rc);
     cudaStream_t st = nullptr;
     if ((e = cudaMemcpy(c->d_plans, c->plans.data(), sizeof(MkCtaPlan) * g.nC, cudaMemcpyHostToDevice)) ||
@@ -490,7 +491,8 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         (e = cudaMemset(c->xacc, 0, 2 * 2 * L * H * 4)) || (e = cudaMemset(c->qll, 0, qll_bytes)) ||
         (e = cudaMemset(c->kvll, 0, kvll_bytes)) || (e = cudaMemset(c->partll, 0, partll_bytes)) || (e = cudaMemset(c->cnt, 0, (size_t)mk_cnt_total(g) * 4)) ||
         (e = cudaMemset(c->status, 0, 4)) || (e = cudaMemset(c->seq, 0, 4)) || (e = cudaMemset(c->amax, 0, 8)) ||
-        (e = cudaMemset(c->next_token, 0, 4)) || (e = cudaMemset(c->tokens_dev, 0, (size_t)g.max_seq * 4)))
+        (e = cudaMemset(c->next_token, 0, 4)) || (e = cudaMemset(c->tokens_dev, 0, (size_t)g.max_seq * 4)) ||
+        (e = cudaMemset(c->stop, 0, 4)))
         return fail(cuda_fail(e, "context init"));
     if ((e = mk_launch_rope_table(c->rope_cos, c->rope_sin, g.max_seq, g.hd, (double)cfg->rope_theta, st)) ||
         (e = cudaDeviceSynchronize()))
@@ -759,6 +761,63 @@ int mk_generate_greedy(mk_ctx* c, const int32_t* prompt, int32_t n_prompt, int32
     }
     MK_CU(cudaMemcpyAsync(out_tokens, c->tokens_dev, (size_t)n_new * 4, cudaMemcpyDeviceToHost, st));
     MK_CU(cudaStreamSynchronize(st));
+    return mk_status(c);
+}
+
+int mk_decode_step_sample(mk_ctx* c, int32_t token, int32_t pos, float temperature, uint64_t seed,
+                          float* logits_out, void* stream) {
+    if (!c) return MK_ERR_INVALID_ARG;
+    if (!c->weights_loaded) return MK_ERR_STATE;
+    if (token < -1 || token >= c->geo.V || pos < 0 || pos >= c->geo.max_seq || !(temperature == temperature))
+        return MK_ERR_INVALID_ARG;
+    MkParams p = base_params(c);
+    p.pos = pos;
+    p.token = token < 0 ? 0 : token;
+    p.token_ptr = token < 0 ? c->next_token : nullptr;
+    p.logits = logits_out;
+    p.tokens_out = nullptr;
+    p.inv_temp = temperature > 0.f ? 1.0f / temperature : 0.f;
+    p.seed = seed;
+    return launch_step(c, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mk_generate(mk_ctx* c, const int32_t* prompt, int32_t n_prompt, int32_t start_pos, int32_t n_new,
+                float temperature, uint64_t seed, int32_t eos_id, int32_t* out_tokens, int32_t* n_out, void* stream) {
+    if (!c || !prompt || !out_tokens || n_prompt < 1 || n_new < 1 || start_pos < 0 || !(temperature == temperature))
+        return MK_ERR_INVALID_ARG;
+    if (!c->weights_loaded) return MK_ERR_STATE;
+    const int64_t steps = (int64_t)n_prompt + n_new - 1;
+    if (start_pos + steps > c->geo.max_seq) return MK_ERR_INVALID_ARG;
+    for (int i = 0; i < n_prompt; ++i)
+        if (prompt[i] < 0 || prompt[i] >= c->geo.V) return MK_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    MK_CU(cudaMemcpyAsync(c->prompt_dev, prompt, (size_t)n_prompt * 4, cudaMemcpyHostToDevice, st));
+    MK_CU(cudaMemsetAsync(c->stop, 0, 4, st));
+    const float inv_temp = temperature > 0.f ? 1.0f / temperature : 0.f;
+    for (int64_t k = 0; k < steps; ++k) {
+        MkParams p = base_params(c);
+        p.pos = (int32_t)(start_pos + k);
+        p.token = 0;
+        p.token_ptr = (k < n_prompt) ? c->prompt_dev + k : c->next_token;
+        p.logits = nullptr;
+        p.tokens_out = (k >= n_prompt - 1) ? c->tokens_dev : nullptr;
+        p.out_idx = (int32_t)(k - (n_prompt - 1));
+        p.inv_temp = inv_temp;
+        p.seed = seed;
+        p.eos_id = eos_id;
+        p.stop = eos_id >= 0 ? c->stop : nullptr;
+        int rc = launch_step(c, p, st);
+        if (rc != MK_OK) return rc;
+    }
+    MK_CU(cudaMemcpyAsync(out_tokens, c->tokens_dev, (size_t)n_new * 4, cudaMemcpyDeviceToHost, st));
+    MK_CU(cudaStreamSynchronize(st));
+    // the tokens up to and including the first stop token; the launches after it returned at once
+    int32_t n = n_new;
+    if (eos_id >= 0)
+        for (int32_t i = 0; i < n_new; ++i)
+            if (out_tokens[i] == eos_id) { n = i + 1; break; }
+    for (int32_t i = n; i < n_new; ++i) out_tokens[i] = -1;
+    if (n_out) *n_out = n;
     return mk_status(c);
 }
 

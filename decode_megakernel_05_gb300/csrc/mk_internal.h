@@ -170,6 +170,12 @@ struct MkParams {
     float* logits;               // [V] or nullptr
     int32_t* tokens_out;         // greedy output buffer or nullptr
     int32_t out_idx;
+    // sampling (cloud.baidu.com/article/9434380, section 5, steps 1 and 5: temperature
+    // as a fixed sampling parameter; sampling and the stop condition on the fused path)
+    float inv_temp;              // 1 / temperature; 0 = greedy
+    uint64_t seed;               // noise generator seed
+    int32_t eos_id;              // with stop: a generated token equal to it sets *stop
+    int32_t* stop;               // nullptr, or a flag that makes every later launch return at once
     int32_t dbg_skip_cta, dbg_skip_sync;
     int32_t trace_detail;        // with trace: also per-tile and ring-wait slots
     int32_t inflight;            // most tiles in flight per CTA in streaming segments (>= ns: no limit)

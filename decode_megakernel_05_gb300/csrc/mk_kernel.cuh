@@ -1112,6 +1112,24 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
     return ab;
 }
 
+// ------------------------------------------------------------------ sampling
+
+// Gumbel noise for sampling by the Gumbel-max rule: argmax_v (logit_v / T + G_v)
+// is distributed as softmax(logit / T).  U_v comes from SplitMix64 (Steele,
+// Lea and Flood, "Fast splittable pseudorandom number generators", OOPSLA
+// 2014) in its counter form -- output i of the generator seeded with s is
+// mix(s + (i + 1) * 0x9E3779B97F4A7C15) -- with i = pos * 2^32 + v; U takes
+// the top 23 bits, (bits + 0.5) * 2^-23, exact in fp32 and never 0 or 1;
+// G = -ln(-ln U) in fp32.
+__device__ __forceinline__ float mk_gumbel(uint64_t seed, int pos, int v) {
+    uint64_t z = seed + ((((uint64_t)(uint32_t)pos << 32) | (uint32_t)v) + 1ull) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    const float u = ((float)(uint32_t)(z >> 41) + 0.5f) * 1.1920928955078125e-07f;   // exact: 24 significant bits
+    return -logf(-logf(u));
+}
+
 // ------------------------------------------------------------------ the kernel
 
 // HD: head_dim; G: query heads per KV head; MH = H / 256, the 8-column chunks
@@ -1122,6 +1140,9 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
 template <int HD, int G, int MH, int LC>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
     static_assert(G <= MK_NCW, "one consumer warp per query head of a KV group (softmax, combine weights)");
+    // generation already stopped (an earlier launch sampled the stop token):
+    // every CTA returns before touching any state
+    if (p.stop && *(volatile int32_t*)p.stop) return;
     constexpr int KO = G * HD;                         // O-proj row length
     constexpr int LPRO = KO >= 32 * 4 ? KO / 32 : 4;   // short rows: 4 chunks per lane
     constexpr int MO = KO / (8 * LPRO);
@@ -1600,7 +1621,10 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             const int v = pl.v0 + r;
             if (p.logits) p.logits[v] = lg;
             if (isfinite(lg)) {
-                if (lg > bv || (lg == bv && v < bi)) { bv = lg; bi = v; }
+                // greedy: the logit; sampling: logit / T plus this token's Gumbel noise
+                // (inline behind a uniform branch: measured the cheapest form for greedy steps)
+                const float key = p.inv_temp > 0.f ? fmaf(lg, p.inv_temp, mk_gumbel(p.seed, p.pos, v)) : lg;
+                if (key > bv || (key == bv && v < bi)) { bv = key; bi = v; }
             } else {
                 nonfinite = true;
             }
@@ -1647,6 +1671,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             else tok = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
             *p.next_token = tok;
             if (p.tokens_out) p.tokens_out[p.out_idx] = tok;
+            if (p.stop && p.tokens_out && tok == p.eos_id) *p.stop = 1;   // generated the stop token
             *p.amax = 0ull;
             p.cnt[ntot] = 0u;
             atomicAdd(p.seq, 1u);

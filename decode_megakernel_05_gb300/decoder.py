@@ -82,6 +82,13 @@ class Decoder:
         ptr = self.logits.data_ptr() if logits else None
         mk.mk_decode_step_greedy(self.ctx, int(pos), ptr, self.stream)
 
+    def step_sample(self, token: int, pos: int, temperature: float, seed: int, logits=False):
+        """One fused step whose next token is sampled at `temperature` (<= 0: greedy);
+        token = -1 feeds the previous step's chosen token from device memory."""
+        ptr = self.logits.data_ptr() if logits else None
+        mk.mk_decode_step_sample(self.ctx, int(token), int(pos), float(temperature), int(seed), ptr, self.stream)
+        return self.logits if logits else None
+
     def step_perop(self, token: int, pos: int, logits=True) -> int:
         ptr = self.logits.data_ptr() if logits else None
         return mk.mk_decode_step_perop(self.ctx, int(token), int(pos), ptr, self.stream)
@@ -100,6 +107,15 @@ class Decoder:
         out = np.zeros(n_new, dtype=np.int32)
         rc = mk.mk_generate_greedy(self.ctx, p.ctypes.data, p.size, start_pos, n_new, out.ctypes.data, self.stream)
         return rc, out
+
+    def generate(self, prompt, start_pos: int, n_new: int, temperature: float = 0.0, seed: int = 0, eos_id: int = -1):
+        """Sampled generation with an optional stop token: (code, tokens with -1 after the stop, count)."""
+        p = np.ascontiguousarray(prompt, dtype=np.int32)
+        out = np.zeros(n_new, dtype=np.int32)
+        n = np.zeros(1, dtype=np.int32)
+        rc = mk.mk_generate(self.ctx, p.ctypes.data, p.size, start_pos, n_new, float(temperature), int(seed),
+                            int(eos_id), out.ctypes.data, n.ctypes.data, self.stream)
+        return rc, out, int(n[0])
 
     def status(self) -> int:
         return mk.mk_status(self.ctx)

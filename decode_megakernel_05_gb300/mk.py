@@ -71,6 +71,8 @@ SIGNATURES = [
     ("mk_decode_step", _i32, [_P, _i32, _i32, _P, _P]),
     ("mk_decode_step_greedy", _i32, [_P, _i32, _P, _P]),
     ("mk_generate_greedy", _i32, [_P, _P, _i32, _i32, _i32, _P, _P]),
+    ("mk_decode_step_sample", _i32, [_P, _i32, _i32, ctypes.c_float, ctypes.c_uint64, _P, _P]),
+    ("mk_generate", _i32, [_P, _P, _i32, _i32, _i32, ctypes.c_float, ctypes.c_uint64, _i32, _P, _P, _P]),
     ("mk_get_hidden", _i32, [_P, _P, _P]),
     ("mk_get_argmax", _i32, [_P, _P, _P]),
     ("mk_status", _i32, [_P]),
@@ -194,6 +196,18 @@ def mk_generate_greedy(ctx: int, prompt_ptr: int, n_prompt: int, start_pos: int,
                        stream: int = 0) -> int:
     """Returns the library's code (MK_OK or a latched device status) without raising."""
     return load().mk_generate_greedy(ctx, prompt_ptr, n_prompt, start_pos, n_new, out_ptr, stream)
+
+
+def mk_decode_step_sample(ctx: int, token: int, pos: int, temperature: float, seed: int, logits_ptr: int | None,
+                          stream: int = 0) -> None:
+    check(load().mk_decode_step_sample(ctx, token, pos, temperature, seed, logits_ptr, stream), "mk_decode_step_sample")
+
+
+def mk_generate(ctx: int, prompt_ptr: int, n_prompt: int, start_pos: int, n_new: int, temperature: float, seed: int,
+                eos_id: int, out_ptr: int, n_out_ptr: int | None, stream: int = 0) -> int:
+    """Returns the library's code (MK_OK or a latched device status) without raising."""
+    return load().mk_generate(ctx, prompt_ptr, n_prompt, start_pos, n_new, temperature, seed, eos_id, out_ptr,
+                              n_out_ptr, stream)
 
 
 def mk_get_hidden(ctx: int, out_ptr: int, stream: int = 0) -> None:

@@ -158,6 +158,34 @@ int mk_decode_step_greedy(mk_ctx* ctx, int32_t pos, float* logits_out, void* str
 int mk_generate_greedy(mk_ctx* ctx, const int32_t* prompt, int32_t n_prompt, int32_t start_pos,
                        int32_t n_new, int32_t* out_tokens, void* stream);
 
+/* Sampling (cloud.baidu.com/article/9434380, section 5: step 1 fixes the
+ * sampling parameters such as the temperature; step 5 re-verifies sampling
+ * and the stop condition on the fused path).  The next token is drawn from
+ * softmax(logits / temperature) by the Gumbel-max rule, inside the argmax of
+ * the same launch: token = argmax_v fmaf(logit_v, 1/temperature, G_v) over
+ * the finite logits (lowest index on ties), G_v = -ln(-ln U_v) in fp32, and
+ * U_v = ((z >> 41) + 0.5) * 2^-23 with z output i = pos * 2^32 + v of
+ * SplitMix64 seeded with `seed` in its counter form, mix(seed + (i + 1) *
+ * 0x9E3779B97F4A7C15) (Steele, Lea and Flood, OOPSLA 2014).  temperature <= 0
+ * is greedy.  Top-p is not supported.
+ *
+ * One sampled step: as mk_decode_step, fed `token` (0..V-1), or with token =
+ * -1 the previous step's chosen token from device memory.  The chosen token
+ * is left on the device (mk_get_argmax).  Asynchronous. */
+int mk_decode_step_sample(mk_ctx* ctx, int32_t token, int32_t pos, float temperature, uint64_t seed,
+                          float* logits_out, void* stream);
+
+/* Generation with sampling and a stop token: as mk_generate_greedy, with the
+ * tokens chosen as in mk_decode_step_sample.  With eos_id >= 0, generation
+ * stops at the first generated token equal to eos_id: every later launch
+ * returns at once (no K/V written, no state advanced).  out_tokens (host
+ * int32 [n_new]) receives the tokens up to and including it and -1 after;
+ * *n_out (may be NULL) their number.  Synchronizes `stream`; returns the
+ * device status like mk_generate_greedy. */
+int mk_generate(mk_ctx* ctx, const int32_t* prompt, int32_t n_prompt, int32_t start_pos, int32_t n_new,
+                float temperature, uint64_t seed, int32_t eos_id, int32_t* out_tokens, int32_t* n_out,
+                void* stream);
+
 /* The last step's final-norm hidden state (fp32 [H]) into `out` (device). */
 int mk_get_hidden(mk_ctx* ctx, float* out, void* stream);
 

@@ -68,6 +68,15 @@ def lib():
             L.oracle_argmax_f32.restype = ctypes.c_int
             L.oracle_decode_step.argtypes = [ctypes.POINTER(_OracleModelC), _P, _P, ctypes.c_int, ctypes.c_int, _P, _P]
             L.oracle_decode_step.restype = ctypes.c_int
+            L.oracle_splitmix64_output.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+            L.oracle_splitmix64_output.restype = ctypes.c_uint64
+            L.oracle_uniform_f32.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int]
+            L.oracle_uniform_f32.restype = ctypes.c_float
+            L.oracle_gumbel_f32.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int]
+            L.oracle_gumbel_f32.restype = ctypes.c_float
+            L.oracle_sample_f32.argtypes = [_P, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_int,
+                                            ctypes.POINTER(ctypes.c_int)]
+            L.oracle_sample_f32.restype = ctypes.c_int
             for f in (L.oracle_rmsnorm, L.oracle_gemv, L.oracle_rope, L.oracle_softmax, L.oracle_attention_head):
                 f.restype = None
             _lib = L
@@ -135,6 +144,27 @@ def argmax_f32(logits):
     lg, pl = _c(logits, np.float64)
     nf = ctypes.c_int(0)
     idx = lib().oracle_argmax_f32(pl, lg.size, ctypes.byref(nf))
+    return idx, bool(nf.value)
+
+
+def splitmix64_output(seed: int, i: int) -> int:
+    return int(lib().oracle_splitmix64_output(ctypes.c_uint64(seed), ctypes.c_uint64(i)))
+
+
+def uniform_f32(seed: int, pos: int, v: int) -> float:
+    return float(lib().oracle_uniform_f32(ctypes.c_uint64(seed), int(pos), int(v)))
+
+
+def gumbel_f32(seed: int, pos: int, v: int) -> float:
+    return float(lib().oracle_gumbel_f32(ctypes.c_uint64(seed), int(pos), int(v)))
+
+
+def sample_f32(logits, inv_temp: float, seed: int, pos: int):
+    """(token, any non-finite logit): Gumbel-max sample of softmax(logits * inv_temp); inv_temp <= 0 is greedy."""
+    lg, pl = _c(logits, np.float64)
+    nf = ctypes.c_int(0)
+    idx = lib().oracle_sample_f32(pl, lg.size, ctypes.c_float(inv_temp), ctypes.c_uint64(seed), int(pos),
+                                  ctypes.byref(nf))
     return idx, bool(nf.value)
 
 

@@ -158,6 +158,61 @@ int oracle_argmax_f32(const double* logits, int n, int* nonfinite) {
     return best;
 }
 
+/* Sampling (cloud.baidu.com/article/9434380, section 5: step 1 names the
+ * temperature among the sampling parameters, step 5 the sampling logic and the
+ * stop condition on the fused path).  The pages name no sampling rule; the one
+ * taken is exact sampling from softmax(logits / T) by the Gumbel-max rule:
+ * the token is argmax_v (logit_v / T + G_v) with G_v independent standard
+ * Gumbel noise, G = -ln(-ln U), U uniform on (0, 1).
+ *
+ * U comes from SplitMix64 (Steele, Lea and Flood, "Fast splittable
+ * pseudorandom number generators", OOPSLA 2014): the generator's state starts
+ * at the seed and advances by the constant 0x9E3779B97F4A7C15 before each
+ * output; an output is the state passed through the mix
+ *   z ^= z >> 30; z *= 0xBF58476D1CE4E5B9; z ^= z >> 27; z *= 0x94D049BB133111EB; z ^= z >> 31.
+ * Output number i (0-based) therefore mixes seed + (i + 1) * 0x9E3779B97F4A7C15.
+ * For token v at position pos, i = pos * 2^32 + v.  U = ((z >> 41) + 0.5) * 2^-23
+ * (23 bits plus the half: 24 significant bits, exact in float; never 0 or 1).  Everything after U is fp32 (the precision the
+ * GPU decides the token in): G = -logf(-logf(U)), key = fmaf(logit, 1/T, G),
+ * with the logit rounded to float first. */
+uint64_t oracle_splitmix64_output(uint64_t seed, uint64_t i) {
+    uint64_t z = seed + (i + 1u) * 0x9E3779B97F4A7C15ull;   /* the state after i + 1 advances */
+    z ^= z >> 30;
+    z *= 0xBF58476D1CE4E5B9ull;
+    z ^= z >> 27;
+    z *= 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return z;
+}
+
+float oracle_uniform_f32(uint64_t seed, int pos, int v) {
+    const uint64_t i = ((uint64_t)(uint32_t)pos << 32) | (uint32_t)v;
+    const uint64_t z = oracle_splitmix64_output(seed, i);
+    return ((float)(uint32_t)(z >> 41) + 0.5f) * (1.0f / 8388608.0f);
+}
+
+float oracle_gumbel_f32(uint64_t seed, int pos, int v) {
+    const float u = oracle_uniform_f32(seed, pos, v);
+    return -logf(-logf(u));
+}
+
+/* Sampled token: inv_temp <= 0 is the greedy argmax; otherwise the largest
+ * key over the finite logits, the lowest index on ties.  *nonfinite as in
+ * oracle_argmax_f32. */
+int oracle_sample_f32(const double* logits, int n, float inv_temp, uint64_t seed, int pos, int* nonfinite) {
+    if (!(inv_temp > 0.0f)) return oracle_argmax_f32(logits, n, nonfinite);
+    int best = -1;
+    float bk = 0.0f;
+    *nonfinite = 0;
+    for (int i = 0; i < n; ++i) {
+        const float v = (float)logits[i];
+        if (!isfinite(v)) { *nonfinite = 1; continue; }
+        const float key = fmaf(v, inv_temp, oracle_gumbel_f32(seed, pos, i));
+        if (best < 0 || key > bk) { best = i; bk = key; }
+    }
+    return best;
+}
+
 /* One decode step: feed `token` at position `pos`, append its K/V to the
  * cache, return logits [vocab] and the final-norm hidden state [hidden].
  * kcache / vcache: bf16 [n_layers][n_kv_heads][max_seq][head_dim]; positions

@@ -333,3 +333,86 @@ def test_kv_append_is_bf16_of_rotated_k():
         kr = oracle.rope(k[g * 16:(g + 1) * 16], 2, s.rope_theta)
         assert np.array_equal(o.kcache[0, g, 2], bf16_bits(kr))
         assert np.array_equal(o.vcache[0, g, 2], bf16_bits(v[g * 16:(g + 1) * 16]))
+
+
+# ---------------------------------------------------------------- sampling
+#
+# The sampler draws from softmax(logits / T) by the Gumbel-max rule with
+# SplitMix64 noise (cloud.baidu.com/article/9434380, section 5, steps 1 and 5;
+# the rule and the generator are the reading taken where the page names only
+# the temperature).  Pinned: the generator's output indexing against the
+# generator stepped one output at a time and its widely reproduced first
+# output for seed 0; the uniformity of U; the sampled frequencies against the
+# softmax probabilities at two temperatures (a wrong sign of G, a missing log
+# or a wrong temperature scale fails it); the greedy limits.
+
+_GAMMA = 0x9E3779B97F4A7C15
+_M64 = (1 << 64) - 1
+
+
+def _stepped_splitmix64(seed, n):
+    """The generator as published: add gamma to the state, output the mixed state."""
+    out, st = [], seed
+    for _ in range(n):
+        st = (st + _GAMMA) & _M64
+        z = st
+        z ^= z >> 30
+        z = (z * 0xBF58476D1CE4E5B9) & _M64
+        z ^= z >> 27
+        z = (z * 0x94D049BB133111EB) & _M64
+        out.append(z ^ (z >> 31))
+    return out
+
+
+def test_splitmix64_output_indexing():
+    for seed in (0, 1, 0xDEADBEEF, _M64):
+        assert [oracle.splitmix64_output(seed, i) for i in range(24)] == _stepped_splitmix64(seed, 24)
+    assert oracle.splitmix64_output(0, 0) == 0xE220A8397B1DCDAF   # the first output for seed 0
+    # counter i = pos * 2^32 + v
+    z = oracle.splitmix64_output(5, (3 << 32) | 7)
+    assert oracle.uniform_f32(5, 3, 7) == ((z >> 41) + 0.5) / 2.0 ** 23   # exact in fp32
+    # the extremes of U stay inside (0, 1) in fp32
+    assert np.float32((0 + 0.5) / 2.0 ** 23) > 0 and np.float32(((1 << 23) - 1 + 0.5) / 2.0 ** 23) < 1
+
+
+def test_uniform_noise_is_uniform_and_open():
+    u = np.array([oracle.uniform_f32(123, p, v) for p in range(4) for v in range(5000)])
+    assert 0.0 < u.min() and u.max() < 1.0
+    counts, _ = np.histogram(u, bins=20, range=(0.0, 1.0))
+    expect = len(u) / 20
+    chi2 = float(np.sum((counts - expect) ** 2 / expect))
+    assert chi2 < 43.8, chi2   # 19 degrees of freedom, p = 0.001
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.5])
+def test_gumbel_max_draws_follow_softmax(temperature):
+    logits = np.array([0.5, -1.0, 2.0, 0.0, 1.2, -0.3])
+    inv = float(np.float32(1.0 / temperature))
+    n = 30000
+    counts = np.zeros(len(logits))
+    for k in range(n):
+        tok, nf = oracle.sample_f32(logits, inv, 99, k)
+        assert not nf
+        counts[tok] += 1
+    z = logits * inv
+    prob = np.exp(z - z.max())
+    prob /= prob.sum()
+    chi2 = float(np.sum((counts - n * prob) ** 2 / (n * prob)))
+    assert chi2 < 20.5, (chi2, counts / n, prob)   # 5 degrees of freedom, p = 0.001
+
+
+def test_sampling_limits_and_special_values():
+    rng = np.random.default_rng(4)
+    logits = rng.normal(size=50)
+    greedy = int(np.argmax(logits))
+    for pos in range(20):
+        assert oracle.sample_f32(logits, 0.0, 7, pos)[0] == greedy          # temperature <= 0: greedy
+        assert oracle.sample_f32(logits, 1e6, 7, pos)[0] == greedy          # temperature -> 0
+    dominant = logits.copy()
+    dominant[17] += 60.0                                                    # P(any other) < 50 e^-60
+    assert all(oracle.sample_f32(dominant, 1.0, 11, pos)[0] == 17 for pos in range(50))
+    bad = logits.copy()
+    bad[greedy] = np.nan
+    tok, nf = oracle.sample_f32(bad, 1.0, 3, 0)
+    assert nf and tok != greedy
+    assert oracle.sample_f32(np.full(4, np.inf), 1.0, 3, 0) == (-1, True)   # no finite logit

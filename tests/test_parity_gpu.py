@@ -169,3 +169,74 @@ def test_hidden_width_gemv(shape, seed):
     print(shape.hidden, rep.summary())
     rep.check()
     dec.close()
+
+
+# ------------------------------------------------------------ sampling and stop
+
+def _oracle_keys(lg_ref, inv, seed, pos):
+    """The oracle's sampling keys fmaf(logit, 1/T, G) for every token (for near-tie checks)."""
+    g = np.array([oracle.gumbel_f32(seed, pos, v) for v in range(len(lg_ref))], dtype=np.float32)
+    return lg_ref.astype(np.float32) * np.float32(inv) + g
+
+
+@pytest.mark.parametrize("temperature", [0.7, 1.3])
+def test_sampling_matches_oracle(temperature):
+    """Teacher-forced sampled steps on the H=512 shape (V = 5003): the fused
+    Gumbel-max choice equals the oracle's from its own logits, except where
+    the oracle's top two keys are within the logit error (a near tie)."""
+    m, dec, orc = make(MID, 61, 256, gains="normal", std=0.04)
+    inv = float(np.float32(1.0 / temperature))
+    seed = 0x5EED0000 + int(temperature * 10)
+    tok, agree, steps = 5, 0, 24
+    for pos in range(steps):
+        lg_ref, _ = orc.step(tok, pos)
+        dec.step_sample(tok, pos, temperature, seed, logits=True)
+        lg = dec.logits.cpu().numpy().astype(np.float64)
+        got = dec.get_argmax()
+        want, nf = oracle.sample_f32(lg_ref, inv, seed, pos)
+        assert not nf
+        dl = float(np.max(np.abs(lg - lg_ref)))
+        assert dl <= 5e-2
+        if got == want:
+            agree += 1
+        else:
+            keys = np.sort(_oracle_keys(lg_ref, inv, seed, pos))
+            assert keys[-1] - keys[-2] <= 2 * dl * inv + 1e-5, (pos, got, want)
+        tok = want
+    assert agree >= steps - 1, agree
+    assert dec.status() == 0
+    dec.close()
+
+
+def test_generate_with_sampling_and_stop_token():
+    """mk_generate: the sampled sequence equals the oracle's (each fed its own
+    previous token); with a stop token it ends right after the first one
+    (-1 after it, later launches do nothing), and the next call runs again."""
+    s = synth.ModelShape(2, 256, 4, 2, 64, 688, 1024, 1e-5, 10000.0, False)
+    m, dec, orc = make(s, 71, 128, gains="normal", std=0.05)
+    prompt = synth.uniform_tokens(6, s.vocab, 71, 9)
+    n_new, temperature, seed = 16, 0.9, 1234
+    inv = float(np.float32(1.0 / temperature))
+
+    def oracle_generate():
+        out, tok = [], 0
+        for k in range(len(prompt) + n_new - 1):
+            tok = int(prompt[k]) if k < len(prompt) else out[-1]
+            lg_ref, _ = orc.step(tok, k)
+            if k >= len(prompt) - 1:
+                out.append(oracle.sample_f32(lg_ref, inv, seed, k)[0])
+        return out
+
+    want = oracle_generate()
+    rc, got, n = dec.generate(prompt, 0, n_new, temperature, seed)
+    assert rc == 0 and n == n_new
+    assert list(got) == want
+    # stop at the first generated token that has not appeared before it (index >= 2)
+    j = next(i for i in range(2, n_new) if want[i] not in want[:i])
+    rc, got, n = dec.generate(prompt, 0, n_new, temperature, seed, eos_id=want[j])
+    assert rc == 0 and n == j + 1
+    assert list(got[:j + 1]) == want[:j + 1] and all(t == -1 for t in got[j + 1:])
+    # a full run again: the stop flag is reset by every call
+    rc, got, n = dec.generate(prompt, 0, n_new, temperature, seed)
+    assert rc == 0 and n == n_new and list(got) == want
+    dec.close()
