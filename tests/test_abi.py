@@ -71,7 +71,7 @@ def test_every_kernel_build_is_in_the_library():
 
 
 def test_no_closed_cuda_calls_in_sources():
-    """The batched-memcpy family is closed on the GPU pool; no source may name it."""
+    """The batched-memcpy family of CUDA calls is not used, and no source names it."""
     pat = re.compile(r"(cuda|cu)Memcpy(3D)?BatchAsync")
     for d in ("decode_megakernel_05_gb300", "include", "oracle", "synth", "tests"):
         for base, _, files in os.walk(os.path.join(ROOT, d)):
