@@ -453,6 +453,7 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
     }
     c->long_ctx = mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, cfg->max_seq >= MK_LONG_CTX,
                                     &c->kernel, &c->kernel_trace) == 1;
+    c->geo.kv_swz = c->long_ctx ? 1 : 0;   // the long-context build reads chunk-permuted K/V rows
     for (const void* k : {c->kernel, c->kernel_trace})
         if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c->geo.smem_bytes)) !=
             cudaSuccess)
@@ -656,7 +657,7 @@ int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
             P.lm = lm;
         }
         P.attn_norm = c->attn_norm; P.ffn_norm = c->ffn_norm; P.final_norm = c->final_norm;
-        P.rope_cos = c->rope_cos; P.rope_sin = c->rope_sin; P.kc = c->kc; P.vc = c->vc;
+        P.rope_cos = c->rope_cos; P.rope_sin = c->rope_sin; P.kc = c->kc; P.vc = c->vc; P.kv_swz = c->geo.kv_swz;
         const size_t nsplit_max = ((size_t)g.max_seq + P.attn_chunk - 1) / P.attn_chunk;
         MK_TRY(c->dalloc(&P.x, H * 4)); MK_TRY(c->dalloc(&P.xn, H * 4));
         MK_TRY(c->dalloc(&P.qkv, (qd + 2 * kvd) * 4)); MK_TRY(c->dalloc(&P.attn, qd * 4));
@@ -680,6 +681,12 @@ int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
     return MK_OK;
 }
 
+// A device buffer that lives for one call.
+struct MkDevTmp {
+    void* p = nullptr;
+    ~MkDevTmp() { if (p) cudaFree(p); }
+};
+
 int mk_set_kv(mk_ctx* c, int32_t layer, const void* k, const void* v, int32_t n_pos, void* stream) {
     if (!c || !k || !v || layer < 0 || layer >= c->geo.L || n_pos < 0 || n_pos > c->geo.max_seq)
         return MK_ERR_INVALID_ARG;
@@ -687,8 +694,24 @@ int mk_set_kv(mk_ctx* c, int32_t layer, const void* k, const void* v, int32_t n_
     MK_CU(cudaSetDevice(c->device));
     const MkGeom& g = c->geo;
     const size_t row = (size_t)n_pos * g.hd * 2;
+    const size_t lay = ((size_t)layer * g.kvh * g.max_seq) * g.hd;
+    if (g.kv_swz) {
+        // rows chunk-permuted in the cache: stage the plain rows on the device, then permute
+        if (n_pos == 0) return MK_OK;
+        MkDevTmp tmp;
+        const size_t bytes = row * g.kvh;
+        MK_CU(cudaMalloc(&tmp.p, 2 * bytes));
+        uint16_t* tk = static_cast<uint16_t*>(tmp.p);
+        uint16_t* tv = tk + bytes / 2;
+        MK_CU(cudaMemcpyAsync(tk, k, bytes, cudaMemcpyDefault, st));
+        MK_CU(cudaMemcpyAsync(tv, v, bytes, cudaMemcpyDefault, st));
+        MK_CU(mk_launch_kv_rows(tk, c->kc + lay, g.kvh, n_pos, 0, g.max_seq, g.hd, 1, 1, st));
+        MK_CU(mk_launch_kv_rows(tv, c->vc + lay, g.kvh, n_pos, 0, g.max_seq, g.hd, 1, 1, st));
+        MK_CU(cudaStreamSynchronize(st));
+        return MK_OK;
+    }
     for (int h = 0; h < g.kvh; ++h) {
-        const size_t dst = (((size_t)layer * g.kvh + h) * g.max_seq) * g.hd;
+        const size_t dst = lay + ((size_t)h * g.max_seq) * g.hd;
         MK_CU(cudaMemcpyAsync(c->kc + dst, (const uint8_t*)k + h * row, row, cudaMemcpyDefault, st));
         MK_CU(cudaMemcpyAsync(c->vc + dst, (const uint8_t*)v + h * row, row, cudaMemcpyDefault, st));
     }
@@ -704,8 +727,23 @@ int mk_get_kv(mk_ctx* c, int32_t layer, int32_t pos0, int32_t n_pos, void* k_out
     MK_CU(cudaSetDevice(c->device));
     const MkGeom& g = c->geo;
     const size_t row = (size_t)n_pos * g.hd * 2;
+    const size_t lay = ((size_t)layer * g.kvh * g.max_seq) * g.hd;
+    if (g.kv_swz) {
+        if (n_pos == 0) return MK_OK;
+        MkDevTmp tmp;
+        const size_t bytes = row * g.kvh;
+        MK_CU(cudaMalloc(&tmp.p, 2 * bytes));
+        uint16_t* tk = static_cast<uint16_t*>(tmp.p);
+        uint16_t* tv = tk + bytes / 2;
+        MK_CU(mk_launch_kv_rows(tk, c->kc + lay, g.kvh, n_pos, pos0, g.max_seq, g.hd, 1, 0, st));
+        MK_CU(mk_launch_kv_rows(tv, c->vc + lay, g.kvh, n_pos, pos0, g.max_seq, g.hd, 1, 0, st));
+        MK_CU(cudaMemcpyAsync(k_out, tk, bytes, cudaMemcpyDefault, st));
+        MK_CU(cudaMemcpyAsync(v_out, tv, bytes, cudaMemcpyDefault, st));
+        MK_CU(cudaStreamSynchronize(st));
+        return MK_OK;
+    }
     for (int h = 0; h < g.kvh; ++h) {
-        const size_t src = (((size_t)layer * g.kvh + h) * g.max_seq + pos0) * g.hd;
+        const size_t src = lay + ((size_t)h * g.max_seq + pos0) * g.hd;
         MK_CU(cudaMemcpyAsync((uint8_t*)k_out + h * row, c->kc + src, row, cudaMemcpyDefault, st));
         MK_CU(cudaMemcpyAsync((uint8_t*)v_out + h * row, c->vc + src, row, cudaMemcpyDefault, st));
     }

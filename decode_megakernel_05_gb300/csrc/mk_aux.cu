@@ -51,6 +51,32 @@ __global__ void mk_bf16_to_f32_kernel(const uint16_t* src, float* dst, int64_t n
     if (i < n) dst[i] = __uint_as_float((uint32_t)src[i] << 16);
 }
 
+// One thread per 16-byte chunk of a row; chunk cc of position pos sits at
+// chunk cc ^ (pos mod 8) of the cache row when swz.
+__global__ void mk_kv_rows_kernel(uint4* plain, uint4* cache_layer, int kvh, int n_pos, int pos0, int max_seq, int nch,
+                                  int swz, int to_cache) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)kvh * n_pos * nch) return;
+    const int cc = (int)(i % nch);
+    const int64_t r = i / nch;
+    const int h = (int)(r / n_pos), pos = pos0 + (int)(r % n_pos);
+    uint4* c = cache_layer + ((int64_t)h * max_seq + pos) * nch + (swz ? (cc ^ (pos & 7)) : cc);
+    if (to_cache) *c = plain[i];
+    else plain[i] = *c;
+}
+
+cudaError_t mk_launch_kv_rows(uint16_t* plain, uint16_t* cache_layer, int kvh, int n_pos, int pos0, int max_seq, int hd,
+                              int swz, int to_cache, cudaStream_t st) {
+    const int nch = hd / 8;
+    if (swz && nch < 8) return cudaErrorInvalidValue;
+    const int64_t n = (int64_t)kvh * n_pos * nch;
+    if (n <= 0) return cudaSuccess;
+    mk_kv_rows_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(reinterpret_cast<uint4*>(plain),
+                                                                  reinterpret_cast<uint4*>(cache_layer), kvh, n_pos,
+                                                                  pos0, max_seq, nch, swz, to_cache);
+    return cudaGetLastError();
+}
+
 cudaError_t mk_launch_relayout_rows(uint8_t* arena, const uint16_t* src, int64_t src_cols, const MkRowCopy* ops, int n,
                                     cudaStream_t st) {
     if (n <= 0) return cudaSuccess;

@@ -19,3 +19,9 @@ cudaError_t mk_launch_relayout_cols(uint8_t* arena, const uint16_t* src, int H, 
                                     cudaStream_t st);
 cudaError_t mk_launch_rope_table(float* cs, float* sn, int max_seq, int hd, double theta, cudaStream_t st);
 cudaError_t mk_launch_bf16_to_f32(const uint16_t* src, float* dst, int64_t n, cudaStream_t st);
+// K or V rows of one layer between a plain [kvh][n_pos][hd] bf16 buffer and the
+// cache ([kvh][max_seq][hd] from cache_layer), positions pos0 .. pos0+n_pos-1,
+// each row's 16-byte chunks permuted as the cache keeps them (swz); to_cache
+// selects the direction.  Both buffers are device memory.
+cudaError_t mk_launch_kv_rows(uint16_t* plain, uint16_t* cache_layer, int kvh, int n_pos, int pos0, int max_seq, int hd,
+                              int swz, int to_cache, cudaStream_t st);

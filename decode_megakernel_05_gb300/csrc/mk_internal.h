@@ -80,16 +80,30 @@ struct MkGeom {
     int32_t TRh, TRo, JT, JD, KB;
     int32_t max_rows, max_nj;    // per-CTA maxima (QKV rows, FFN slice)
     int32_t smem_bytes;
+    int32_t kv_swz;              // K/V cache rows chunk-permuted (mk_kv_index); set with the long-context build
     // shared-memory carve-up (byte offsets from the dynamic smem base)
     int32_t off_full, off_empty, off_xv, off_ov, off_part, off_u, off_xres, off_xres2, off_rope,
         off_red, off_sc, off_misc;
 };
+
+// Element index of dim d of position pos in one KV head's rows of the cache
+// ([max_seq][hd] bf16).  With swz, the 16-byte chunk index of a row is XORed
+// with pos mod 8 (hd >= 64): eight consecutive positions then keep a given
+// chunk in eight different shared-memory bank groups once a block of rows is
+// copied into shared memory, which the long-context attention's 8x8 matrix
+// loads (one chunk of eight consecutive positions each) need to be free of
+// bank conflicts.
+MK_HD int64_t mk_kv_index(int64_t pos, int d, int hd, int swz) {
+    const int c = d >> 3;
+    return pos * hd + ((int64_t)((swz ? (c ^ (int)(pos & 7)) : c) << 3) | (d & 7));
+}
 
 // Fills everything but smem offsets from the shape; returns false if the
 // shape is outside what the kernels support.
 MK_HD bool mk_geom_init(MkGeom& g, int L, int H, int qh, int kvh, int hd, int F, int V, int max_seq, int nC,
                         int slot_bytes, int ns) {
     g.L = L; g.H = H; g.qh = qh; g.kvh = kvh; g.hd = hd; g.F = F; g.V = V; g.max_seq = max_seq;
+    g.kv_swz = 0;
     if (L < 1 || H < 8 || qh < 1 || kvh < 1 || F < 1 || V < 1 || max_seq < 1 || nC < 1) return false;
     if (qh % kvh != 0 || nC % kvh != 0) return false;
     g.G = qh / kvh;

@@ -203,6 +203,7 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     float cwt[MK_MAX_CPG_G]; // attention-combine weights [CPG][G]
     float cl[MK_MAX_CPG_G];  // attention partial sums l [CPG][G]
     uint4 stage[32];         // K and V rows of the current position (2 * hd bf16)
+    uint4 zrow;              // 16 zero bytes: the rows past a block's end in the tensor-core attention
 };
 static_assert(sizeof(Misc) <= MK_MISC_BYTES, "misc area");
 
@@ -1012,11 +1013,197 @@ struct Attn {
     }
 };
 
+// ---- long-context attention on the tensor cores (HD = 64, G = 4)
+//
+// At long contexts a CTA attends to thousands of positions per layer, and the
+// per-position arithmetic of the lane-parallel softmax above (partial dots
+// reduced by shuffles, bf16 unpacking, one dependent FMA chain per head) takes
+// about twice as long as the K/V bytes take to arrive.  The contraction is
+// dense, though: per 16 positions, S = [q_hi; q_lo] K^T is a 16x8x64 product
+// and O += P V a 16x64x16 one, so each warp runs them as mma.m16n8k16 (bf16
+// in, fp32 accumulate), keeping q, P and O in registers:
+//   - scores: A = q of the group's 4 heads split into a bf16 high part (rows
+//     0-3) and the bf16 rounding of the remainder (rows 4-7), B = 8 K rows
+//     from ldmatrix; row h plus row h+4 is q.k to about 2^-16 relative, and
+//     the two halves meet with one shuffle (lanes 16 apart hold them);
+//   - the accumulator of two score tiles is, lane for lane, the A fragment of
+//     the P.V product (positions along k), so P never leaves registers; P is
+//     split the same way (rows 0-3 high part, rows 4-7 remainder);
+//   - V^T comes from ldmatrix.trans of the same rows.
+// The cache's chunk permutation (mk_kv_index) keeps each 8x8 matrix load free
+// of bank conflicts.  Warps take the 16-position chunks of the CTA's range in
+// turn (continuing across blocks); each keeps its own online softmax state
+// (m, l per head, O rows) and parks it in the same form as the lane-parallel
+// version, so the partial that leaves the CTA is computed the same way.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+// D = A B + C for one m16n8k16 tile whose A rows 8-15 are zero: only the
+// accumulator of rows 0-7 (c0, c1 of each lane) is carried.
+__device__ __forceinline__ void mma_rows8(float& c0, float& c1, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    float d2, d3;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %12, %13};"
+        : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(0.f), "f"(0.f));
+}
+// bf16x2 of (x, y) rounded to nearest even: x in the low half.
+__device__ __forceinline__ uint32_t pack_bf2(float x, float y) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(y), "f"(x));
+    return r;
+}
+// (x, y) as bf16 high parts (lo == false) or as the bf16 of what they leave (lo).
+__device__ __forceinline__ uint32_t split_bf2(float x, float y, bool lo) {
+    const uint32_t h = pack_bf2(x, y);
+    if (!lo) return h;
+    return pack_bf2(x - __uint_as_float(h << 16), y - __uint_as_float(h & 0xFFFF0000u));
+}
+
+// The block loop of the tensor-core attention (q of the group's heads already
+// in qs, unscaled).  Positions [ka, ke) come from the ring in blocks of KB
+// (K tile then V tile, rows chunk-permuted by position); the current position
+// (staged, plain row order) follows the last block when has_cur.  Returns the
+// abort flag (not yet uniform); the warps' states are parked for the caller.
+template <int HD, int G>
+__device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
+                                               bool has_cur, float qscale, bool ab, const float* qs) {
+    static_assert(HD == 64 && G == 4, "tensor-core attention: 4 heads of 64 dims per KV group");
+    constexpr int NMG = Attn<HD, G>::NMG;
+    static_assert(NMG == MK_NCW, "one parked group per consumer warp");
+    const MkGeom& g = p.geo;
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    const bool lo = lane >= 16;          // this lane's rows hold the remainder parts (4-7)
+    const int qd = 2 * (lane & 3);       // first of this lane's two k (or n) indices in a tile
+    // A fragments of [q_hi; q_lo] (pre-scaled by log2(e)/sqrt(hd)) for the four
+    // 16-dim k steps: row lane/4 (head (lane/4) mod 4), dims 16ks + qd (+8)
+    uint32_t qa[4][2];
+    {
+        const float* qh = qs + ((lane >> 2) & 3) * HD;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int d = 16 * ks + 8 * hf + qd;
+                qa[ks][hf] = split_bf2(qh[d] * qscale, qh[d + 1] * qscale, lo);
+            }
+    }
+    float o[8][2];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = 0.f;
+    float m = -INFINITY, lsum = 0.f;
+    MK_TRACE_D(l, 1);
+    const uint32_t zaddr = smem_u32(&s.misc->zrow);
+    const uint32_t staddr = smem_u32(s.misc->stage);
+    const int nring = ke > ka ? ke - ka : 0;
+    const int nblk = (nring + g.KB - 1) / g.KB;
+    const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
+    if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 1;
+    int cbase = 0;                       // chunks of the earlier blocks (warp w takes chunk indices = w mod NCW)
+    for (int b = 0; b < nbt && !ab; ++b) {
+        const int q0 = ka + b * g.KB;
+        const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
+        const int n = nr + ((has_cur && b == nbt - 1) ? 1 : 0);
+        const uint8_t *kt = nullptr, *vt = nullptr;
+        bool ok = true;
+        if (nr > 0) {
+            Ring rv = ring;
+            rv.advance(g.ns);            // the V tile follows the K tile in the stream
+            ok = take_landed(p, s, ring, (uint32_t)(nr * HD * 2), kt) && take_landed(p, s, rv, (uint32_t)(nr * HD * 2), vt);
+        }
+        if (b == 0) MK_TRACE_D(l, 5);
+        if (ok) {
+            const uint32_t ka_ = kt ? smem_u32(kt) : 0u, va_ = vt ? smem_u32(vt) : 0u;
+            // shared-memory address of 16-byte chunk cc of block row i (K or V):
+            // ring rows below nr, then the staged current row, then a zero row
+            auto row = [&](uint32_t base, uint32_t stoff, int i, int cc) -> uint32_t {
+                if (i < nr) return base + (uint32_t)i * (HD * 2) + ((uint32_t)(cc ^ ((q0 + i) & 7)) << 4);
+                if (i < n) return staddr + stoff + ((uint32_t)cc << 4);
+                return zaddr;
+            };
+            const int nch = (n + 15) >> 4;
+            int ci = w - cbase % MK_NCW;
+            if (ci < 0) ci += MK_NCW;
+            for (; ci < nch; ci += MK_NCW) {
+                const int c0 = 16 * ci;
+                // scores of the chunk's two 8-position tiles
+                float sv[2][2];
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int i = c0 + 8 * tt + (lane & 7);
+                    uint32_t kb[2][4];
+                    ldsm_x4(kb[0], row(ka_, 0u, i, lane >> 3));
+                    ldsm_x4(kb[1], row(ka_, 0u, i, 4 + (lane >> 3)));
+                    float c0_ = 0.f, c1_ = 0.f;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_rows8(c0_, c1_, qa[ks][0], qa[ks][1], kb[ks >> 1][2 * (ks & 1)], kb[ks >> 1][2 * (ks & 1) + 1]);
+                    // high part + remainder: lanes 16 apart hold the same head and positions
+                    c0_ += __shfl_xor_sync(0xFFFFFFFFu, c0_, 16);
+                    c1_ += __shfl_xor_sync(0xFFFFFFFFu, c1_, 16);
+                    const int pi = c0 + 8 * tt + qd;
+                    sv[tt][0] = pi < n ? c0_ : -INFINITY;
+                    sv[tt][1] = pi + 1 < n ? c1_ : -INFINITY;
+                }
+                // online softmax per head (row): the quad of lanes sharing a row agrees on the maximum
+                float cm = fmaxf(fmaxf(m, fmaxf(sv[0][0], sv[0][1])), fmaxf(sv[1][0], sv[1][1]));
+                cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 1));
+                cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 2));
+                const float corr = ex2_approx(m - cm);   // 0 before the first position
+                const float p00 = ex2_approx(sv[0][0] - cm), p01 = ex2_approx(sv[0][1] - cm);
+                const float p10 = ex2_approx(sv[1][0] - cm), p11 = ex2_approx(sv[1][1] - cm);
+                lsum = fmaf(lsum, corr, (p00 + p01) + (p10 + p11));
+                m = cm;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { o[j][0] *= corr; o[j][1] *= corr; }
+                const uint32_t pa0 = split_bf2(p00, p01, lo), pa2 = split_bf2(p10, p11, lo);
+                // O += P V: V^T fragments of d tiles 2jj, 2jj+1 (rows c0.. and c0+8..)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int mt = lane >> 3;
+                    uint32_t vb[4];
+                    ldsm_x4_trans(vb, row(va_, (uint32_t)(HD * 2), c0 + 8 * (mt & 1) + (lane & 7), 2 * jj + (mt >> 1)));
+                    mma_rows8(o[2 * jj][0], o[2 * jj][1], pa0, pa2, vb[0], vb[1]);
+                    mma_rows8(o[2 * jj + 1][0], o[2 * jj + 1][1], pa0, pa2, vb[2], vb[3]);
+                }
+            }
+            cbase += nch;
+        }
+        if (b == 0) MK_TRACE_D(l, 6);
+        if (nr > 0) { release_tile(p, s, ring); release_tile(p, s, ring); }
+        if (!ok) ab = true;     // made uniform by the caller's barrier
+    }
+    if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 0;
+    MK_TRACE_D(l, 2);
+    // the warp's state: l summed over the quad, O rows h and h+4 added; park
+    // (m, l) per head in sc and O in xv[warp] like the lane-parallel version
+    lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
+    lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        o[j][0] += __shfl_xor_sync(0xFFFFFFFFu, o[j][0], 16);
+        o[j][1] += __shfl_xor_sync(0xFFFFFFFFu, o[j][1], 16);
+    }
+    if (!ab && !lo) {
+        const int h = lane >> 2;
+        float* xp = s.xv + w * (G * HD) + h * HD + qd;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) *reinterpret_cast<float2*>(xp + 8 * j) = make_float2(o[j][0], o[j][1]);
+        if ((lane & 3) == 0) { s.sc[w * G + h] = m; s.sc[NMG * G + w * G + h] = lsum; }
+    }
+    return ab;
+}
+
 // The attention of one CTA over its positions with HPL heads per lane: this
 // thread's q dims (tagged words), the block loop (online softmax), the merge
 // of the position groups sharing a warp and the parking of the warps' groups
 // in smem for the partial.  Returns the uniform abort flag (one barrier).
-template <int HD, int G, int HPL>
+template <int HD, int G, int HPL, bool TC>
 __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
                                          bool has_cur, float qscale, bool ab, bool late) {
     using A = Attn<HD, G, HPL>;
@@ -1051,6 +1238,7 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
     }
     ab = bar_or(ab || late);
     MK_TRACE_D(l, 0);   // q in shared memory
+    if constexpr (TC) return attn_tc_blocks<HD, G>(p, s, ring, l, ka, ke, has_cur, qscale, ab, qs);
     float qr[HPL][8];
     if (!ab) {
 #pragma unroll
@@ -1140,6 +1328,7 @@ __device__ __forceinline__ float mk_gumbel(uint64_t seed, int pos, int v) {
 template <int HD, int G, int MH, int LC>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
     static_assert(G <= MK_NCW, "one consumer warp per query head of a KV group (softmax, combine weights)");
+    static_assert(!LC || (HD == 64 && G == 4), "the long-context build's attention runs on 4 heads of 64 dims");
     // generation already stopped (an earlier launch sampled the stop token):
     // every CTA returns before touching any state
     if (p.stop && *(volatile int32_t*)p.stop) return;
@@ -1185,6 +1374,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             tok = 0;
         }
         s.misc->token = tok;
+        s.misc->zrow = make_uint4(0u, 0u, 0u, 0u);
         s.misc->plan = p.plans[c];
         {
             constexpr int KO = G * HD, LPRO = KO >= 32 * 4 ? KO / 32 : 4;
@@ -1266,10 +1456,10 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     uint64_t* q = p.qll + (size_t)l * g.qh * HD + (size_t)(pl.g * G + slot) * HD;
                     if (pub) { st_ll(q + d, ll_pack(a, s.misc->tag)); st_ll(q + d + hd2, ll_pack(b, s.misc->tag)); }
                 } else {
-                    uint16_t* dst = (slot == G ? p.kc : p.vc) +
-                                    (((size_t)l * g.kvh + pl.g) * g.max_seq + p.pos) * HD;
+                    uint16_t* dst = (slot == G ? p.kc : p.vc) + ((size_t)l * g.kvh + pl.g) * g.max_seq * HD;
                     const uint16_t ab16 = f2bf(a), bb16 = f2bf(b);
-                    dst[d] = ab16; dst[d + hd2] = bb16;
+                    dst[mk_kv_index(p.pos, d, HD, LC)] = ab16;
+                    dst[mk_kv_index(p.pos, d + hd2, HD, LC)] = bb16;
                     uint64_t* kv = p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (slot - G)) * HD;
                     if (pub) { st_ll(kv + d, ll_pack(bf2f(ab16), s.misc->tag)); st_ll(kv + d + hd2, ll_pack(bf2f(bb16), s.misc->tag)); }
                 }
@@ -1302,7 +1492,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             const int nring = ke > ka ? ke - ka : 0;
             const int nblk = (nring + g.KB - 1) / g.KB;
             (void)nblk;
-            ab = attn_run<HD, G, (LC && attn_long_ok<HD, G>()) ? 2 : 1>(p, s, ring, l, ka, ke, has_cur, qscale, ab, late);
+            ab = attn_run<HD, G, 1, LC != 0>(p, s, ring, l, ka, ke, has_cur, qscale, ab, late);
         }
         ab = bar_or(ab);
         constexpr int PSTR = G * HD + 2 * G;                   // tagged words per partial

@@ -17,6 +17,13 @@
 namespace {
 
 __device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+// Element of dim d of position p in a KV head's cache rows: with swz the
+// row's 16-byte chunk index is XORed with p mod 8 (the layout the
+// long-context fused kernel reads).
+__device__ __forceinline__ int64_t kvi(int64_t p, int d, int hd, int swz) {
+    const int c = d >> 3;
+    return p * hd + (((swz ? (c ^ (int)(p & 7)) : c) << 3) | (d & 7));
+}
 
 __global__ void embed_kernel(const uint16_t* E, const int32_t* tok_ptr, int tok_arg, int V, int H, float* x,
                              uint32_t* status) {
@@ -88,7 +95,7 @@ __global__ void gemv_kernel(const uint16_t* W, const float* v, int K, int nout, 
 
 // RoPE on q and k heads of the fused qkv vector, then K/V append (bf16).
 __global__ void rope_append_kernel(float* qkv, const float* cs, const float* sn, int pos, int qh, int kvh, int hd,
-                                   int max_seq, int layer, uint16_t* kc, uint16_t* vc) {
+                                   int max_seq, int layer, uint16_t* kc, uint16_t* vc, int swz) {
     const int half = hd / 2;
     const int nh = qh + 2 * kvh;
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -105,16 +112,16 @@ __global__ void rope_append_kernel(float* qkv, const float* cs, const float* sn,
         v[d] = a; v[d + half] = b;
     } else {
         const int g = (h < qh + kvh) ? h - qh : h - qh - kvh;
-        uint16_t* dst = ((h < qh + kvh) ? kc : vc) + (((int64_t)layer * kvh + g) * max_seq + pos) * hd;
-        dst[d] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-        dst[d + half] = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+        uint16_t* dst = ((h < qh + kvh) ? kc : vc) + ((int64_t)layer * kvh + g) * max_seq * hd;
+        dst[kvi(pos, d, hd, swz)] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+        dst[kvi(pos, d + half, hd, swz)] = __bfloat16_as_ushort(__float2bfloat16_rn(b));
     }
 }
 
 // Attention partials: block (q head, split); positions split into `nsplit`
 // chunks of ctx; writes (m, l) and the unnormalised accumulator.
 __global__ void attn_partial_kernel(const float* q, const uint16_t* kc, const uint16_t* vc, int ctx, int qh, int kvh,
-                                    int hd, int max_seq, int layer, int nsplit, float* pml, float* pacc) {
+                                    int hd, int max_seq, int layer, int nsplit, float* pml, float* pacc, int swz) {
     extern __shared__ float sm[];
     float* qs = sm;            // [hd]
     float* sc = sm + hd;       // [chunk]
@@ -127,7 +134,7 @@ __global__ void attn_partial_kernel(const float* q, const uint16_t* kc, const ui
     const uint16_t* Vv = vc + ((int64_t)layer * kvh + g) * max_seq * hd;
     for (int p = a + threadIdx.x; p < b; p += blockDim.x) {
         float s = 0.f;
-        for (int d = 0; d < hd; ++d) s = fmaf(qs[d], bf(K[(int64_t)p * hd + d]), s);
+        for (int d = 0; d < hd; ++d) s = fmaf(qs[d], bf(K[kvi(p, d, hd, swz)]), s);
         sc[p - a] = s;
     }
     __syncthreads();
@@ -153,7 +160,7 @@ __global__ void attn_partial_kernel(const float* q, const uint16_t* kc, const ui
     const int64_t pb = (int64_t)h * nsplit + sp;
     for (int d = threadIdx.x; d < hd; d += blockDim.x) {
         float acc = 0.f;
-        for (int p = a; p < b; ++p) acc = fmaf(sc[p - a], bf(Vv[(int64_t)p * hd + d]), acc);
+        for (int p = a; p < b; ++p) acc = fmaf(sc[p - a], bf(Vv[kvi(p, d, hd, swz)]), acc);
         pacc[pb * hd + d] = acc;
     }
     if (threadIdx.x == 0) { pml[pb * 2] = (b > a) ? m : -INFINITY; pml[pb * 2 + 1] = l; }
@@ -235,9 +242,9 @@ int mk_perop_step(const MkPerOp& P, int token, const int32_t* token_ptr, int pos
         rmsnorm_kernel<<<1, 1024, 0, st>>>(P.x, P.attn_norm + (int64_t)l * H, H, P.eps, P.xn); ++n;
         gemv_kernel<0><<<blocks(nqkv), 256, H * 4, st>>>(P.wqkv[l], P.xn, H, nqkv, nullptr, P.qkv); ++n;
         rope_append_kernel<<<((qh + 2 * kvh) * hd / 2 + 255) / 256, 256, 0, st>>>(
-            P.qkv, P.rope_cos, P.rope_sin, pos, qh, kvh, hd, P.max_seq, l, P.kc, P.vc); ++n;
+            P.qkv, P.rope_cos, P.rope_sin, pos, qh, kvh, hd, P.max_seq, l, P.kc, P.vc, P.kv_swz); ++n;
         attn_partial_kernel<<<dim3(qh, nsplit), 128, (hd + P.attn_chunk) * 4, st>>>(
-            P.qkv, P.kc, P.vc, ctx, qh, kvh, hd, P.max_seq, l, nsplit, P.pml, P.pacc); ++n;
+            P.qkv, P.kc, P.vc, ctx, qh, kvh, hd, P.max_seq, l, nsplit, P.pml, P.pacc, P.kv_swz); ++n;
         attn_combine_kernel<<<qh, 128, 0, st>>>(P.pml, P.pacc, nsplit, hd, P.attn); ++n;
         gemv_kernel<1><<<blocks(H), 256, qh * hd * 4, st>>>(P.wo[l], P.attn, qh * hd, H, P.x, P.x); ++n;
         rmsnorm_kernel<<<1, 1024, 0, st>>>(P.x, P.ffn_norm + (int64_t)l * H, H, P.eps, P.xn); ++n;

@@ -16,6 +16,7 @@ struct MkPerOp {
     std::vector<uint16_t*> wqkv, wo, wgu, wd;   // [qkv rows][H], [H][qh*hd], [2F][H] (gate then up), [H][F]
     const float *attn_norm, *ffn_norm, *final_norm, *rope_cos, *rope_sin;
     uint16_t *kc, *vc;
+    int kv_swz;              // cache rows chunk-permuted by position (the long-context layout)
     // activations / scratch
     float *x, *xn, *qkv, *attn, *u, *hidden, *pml, *pacc, *logits_tmp;
     unsigned long long* amax_part;

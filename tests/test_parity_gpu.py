@@ -71,21 +71,48 @@ def test_mid_shape_ragged(grid, prefill):
     dec.close()
 
 
-@pytest.mark.parametrize("grid,prefill", [(0, 5001), (6, 3000)])
+@pytest.mark.parametrize("grid,prefill", [(0, 5001), (6, 3000), (0, 0), (14, 37)])
 def test_long_context_build(grid, prefill):
-    """max_seq >= 8192 selects the long-context kernel build (two query heads
-    per attention lane) for H=512, G=4; a 5001-position prefill on the full grid
-    (ragged per-CTA chunks) and 3000 positions on 3 CTAs per KV group (each CTA
-    walks about a thousand positions, many KV blocks)."""
+    """max_seq >= 8192 selects the long-context kernel build (attention on the
+    tensor cores, K/V rows chunk-permuted in the cache) for H=512, G=4.
+    A 5001-position prefill on the full grid (ragged per-CTA chunks) and 3000
+    positions on 3 CTAs per KV group (each CTA walks about a thousand positions,
+    many KV blocks); decoding from position 0 (blocks of the current row alone,
+    16-position chunks mostly past the end) and a 37-position prefill on 7 CTAs
+    per group (a few positions per CTA).  The K/V rows the kernel appends read
+    back (through the permuted layout) as the oracle's."""
     tun = mk.tuning(grid_ctas=grid) if grid else None
     m, dec, orc = make(MID, 47, 8192, gains="normal", std=0.04, tuning=tun)
     assert dec.info.long_context == 1
-    ks, vs = synth.make_kv(MID, prefill, 53)
-    dec.set_kv(ks, vs, prefill)
-    orc.set_kv(ks, vs, prefill)
-    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, MID.vocab, 47, 3), prefill, 8)
+    if prefill:
+        ks, vs = synth.make_kv(MID, prefill, 53)
+        dec.set_kv(ks, vs, prefill)
+        orc.set_kv(ks, vs, prefill)
+    steps = 8 if prefill > 1000 else 20
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, MID.vocab, 47, 3), prefill, steps)
     print(rep.summary())
     rep.check()
+    for l in range(MID.n_layers):
+        k, v = dec.get_kv(l, prefill, rep.steps)
+        for got, ref in ((k, orc.kcache[l, :, prefill:prefill + rep.steps]),
+                         (v, orc.vcache[l, :, prefill:prefill + rep.steps])):
+            g32, r32 = synth.bf16_to_f32(got), synth.bf16_to_f32(ref)
+            assert np.mean(got == ref) > 0.97
+            assert np.max(np.abs(g32 - r32)) <= 2 ** -7 * np.max(np.abs(r32))
+    dec.close()
+
+
+def test_kv_rows_round_trip_long_context():
+    """set_kv / get_kv hide the long-context build's chunk-permuted rows: a
+    window at an odd offset reads back bit for bit."""
+    m = synth.make_model(MID, 5, std=0.04)
+    dec = Decoder(m, 8192)
+    assert dec.info.long_context == 1
+    ks, vs = synth.make_kv(MID, 301, 7)
+    dec.set_kv(ks, vs, 301)
+    for l in range(MID.n_layers):
+        k, v = dec.get_kv(l, 13, 251)
+        assert np.array_equal(k, ks[l][:, 13:264]) and np.array_equal(v, vs[l][:, 13:264])
     dec.close()
 
 
@@ -129,6 +156,20 @@ def test_perop_baseline_matches_oracle():
     rep.check()
     n = dec.step_perop(1, 20)
     assert n == 9 * w.shape.n_layers + 5
+    dec.close()
+
+
+def test_perop_baseline_long_context_layout():
+    """The per-operator path appends to and reads the cache in the long-context
+    build's chunk-permuted layout, after a prefill through set_kv."""
+    m, dec, orc = make(MID, 61, 8192, gains="normal", std=0.04, perop=True)
+    assert dec.info.long_context == 1
+    ks, vs = synth.make_kv(MID, 45, 67)
+    dec.set_kv(ks, vs, 45)
+    orc.set_kv(ks, vs, 45)
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, MID.vocab, 61, 3), 45, 12, perop=True)
+    print(rep.summary())
+    rep.check()
     dec.close()
 
 
