@@ -24,8 +24,9 @@ SOURCES = ["mk_api.cu", "mk_aux.cu", "mk_perop.cu", "mk_noalloc.cu"]
 # (head_dim, query heads per KV group, hidden / 256) of the fused kernel, one
 # object each; keep in sync with MK_VARIANTS in csrc/mk_api.cu
 VARIANTS = [(64, 2, 1), (64, 4, 2), (64, 4, 4), (64, 4, 8), (64, 4, 16), (128, 4, 4), (128, 4, 8), (128, 4, 16)]
-# long-context builds (two query heads per attention lane), used when max_seq >= MK_LONG_CTX;
-# keep in sync with MK_LC_VARIANTS in csrc/mk_api.cu
+# long-context builds (attention on the tensor cores), launched for steps whose context gives
+# each CTA at least MK_ATTN_TC_MIN_PER_CTA positions; keep in sync with MK_LC_VARIANTS in
+# csrc/mk_api.cu
 LC_VARIANTS = [(64, 4, 2), (64, 4, 8)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -16,7 +16,8 @@
 
 // One object per kernel variant: mk_kernel.cu compiled with -DMK_HD_V=<head_dim>
 // -DMK_G_V=<q heads per kv head> -DMK_MH_V=<hidden / 256> (-DMK_LC_V=1 for the
-// long-context builds); keep in sync with VARIANTS in build.py.
+// long-context builds, whose attention runs on the tensor cores); keep in sync
+// with VARIANTS in build.py.
 #define MK_VARIANTS(X) \
     X(64, 2, 1) X(64, 4, 2) X(64, 4, 4) X(64, 4, 8) X(64, 4, 16) X(128, 4, 4) X(128, 4, 8) X(128, 4, 16)
 #define MK_LC_VARIANTS(X) X(64, 4, 2) X(64, 4, 8)
@@ -33,7 +34,8 @@ MK_LC_VARIANTS(MK_DECL_LC)
 #undef MK_DECL
 #undef MK_DECL_LC
 
-// The kernel for a shape; with long_ctx, its long-context build where one exists.
+// The kernel for a shape; with long_ctx, its long-context (tensor-core
+// attention) build where one exists.
 // Returns 1 for a long-context build, 0 for the standard one, -1 if none fits.
 static int mk_kernel_variant(int hd, int G, int H, bool long_ctx, const void** fn, const void** fn_trace) {
 #define MK_PICK_LC(hd_, g_, mh_)                                      \
@@ -232,7 +234,13 @@ struct mk_ctx {
     int device = 0, sm_count = 0;
     const void* kernel = nullptr;        // the fused step without trace code
     const void* kernel_trace = nullptr;  // the same with the segment trace compiled in
-    bool long_ctx = false;               // kernel is the long-context build
+    // the build whose attention runs on the tensor cores (shapes with 4 query
+    // heads of 64 dims per KV group; null otherwise) and the context length
+    // per CTA from which a step launches it
+    const void* kernel_tc = nullptr;
+    const void* kernel_tc_trace = nullptr;
+    int tc_min_per_cta = MK_ATTN_TC_MIN_PER_CTA;
+    int attn_build = 0;                  // debug: 0 by context length, 1 lane-parallel, 2 tensor cores
     std::vector<MkCtaPlan> plans;
     int64_t arena_bytes = 0, device_bytes = 0;
     bool weights_loaded = false;
@@ -313,6 +321,9 @@ MkParams base_params(const mk_ctx* c) {
     return p;
 }
 
+// Context length from which steps launch the tensor-core attention build.
+int64_t mk_tc_min_ctx(const mk_ctx* c) { return (int64_t)c->tc_min_per_cta * c->geo.CPG; }
+
 int launch_step(mk_ctx* c, MkParams& p, cudaStream_t st) {
     cudaLaunchConfig_t lc;
     memset(&lc, 0, sizeof lc);
@@ -326,7 +337,13 @@ int launch_step(mk_ctx* c, MkParams& p, cudaStream_t st) {
     lc.attrs = attr;
     lc.numAttrs = 1;
     void* args[] = {&p};
-    MK_CU(cudaLaunchKernelExC(&lc, c->trace ? c->kernel_trace : c->kernel, args));
+    // attention build by context length: the tensor-core build from
+    // tc_min_per_cta positions per CTA (default 0: always, where it exists),
+    // the lane-parallel build below that
+    const bool tc = c->kernel_tc && (c->attn_build == 2 ||
+                                     (c->attn_build == 0 && (int64_t)(p.pos + 1) >= mk_tc_min_ctx(c)));
+    const void* fn = tc ? (c->trace ? c->kernel_tc_trace : c->kernel_tc) : (c->trace ? c->kernel_trace : c->kernel);
+    MK_CU(cudaLaunchKernelExC(&lc, fn, args));
     c->last_stream = st;
     return MK_OK;
 }
@@ -451,18 +468,24 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         if ((rc = build_geom(cfg, c->tune, grid, ns, g)) != MK_OK) return fail(rc);
         if (g.smem_bytes + 1024 <= smem_optin) { c->geo = g; break; }
     }
-    c->long_ctx = mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, cfg->max_seq >= MK_LONG_CTX,
-                                    &c->kernel, &c->kernel_trace) == 1;
-    c->geo.kv_swz = c->long_ctx ? 1 : 0;   // the long-context build reads chunk-permuted K/V rows
-    for (const void* k : {c->kernel, c->kernel_trace})
+    if (mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, false, &c->kernel, &c->kernel_trace) < 0)
+        return fail(MK_ERR_UNSUPPORTED);
+    if (mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, true, &c->kernel_tc,
+                          &c->kernel_tc_trace) != 1)
+        c->kernel_tc = c->kernel_tc_trace = nullptr;
+    // both builds of a tensor-core shape read (and append) chunk-permuted K/V rows
+    c->geo.kv_swz = mk_attn_tc(cfg->head_dim, cfg->n_q_heads / kvh) ? 1 : 0;
+    for (const void* k : {c->kernel, c->kernel_trace, c->kernel_tc, c->kernel_tc_trace}) {
+        if (!k) continue;
         if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, c->geo.smem_bytes)) !=
             cudaSuccess)
             return fail(cuda_fail(e, "cudaFuncSetAttribute"));
-    int per_sm = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c->kernel, MK_BLOCK, c->geo.smem_bytes)) !=
-        cudaSuccess)
-        return fail(cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor"));
-    if (per_sm < 1) return fail(MK_ERR_UNSUPPORTED);
+        int per_sm = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, MK_BLOCK, c->geo.smem_bytes)) !=
+            cudaSuccess)
+            return fail(cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor"));
+        if (per_sm < 1) return fail(MK_ERR_UNSUPPORTED);
+    }
     build_plans(c->geo, c->plans, c->arena_bytes);
     if (!check_schedule(c->geo, c->plans, c->arena_bytes)) return fail(MK_ERR_STATE);
 
@@ -914,7 +937,8 @@ int mk_get_info(const mk_ctx* c, mk_info* o) {
     o->weight_bytes_per_token = weight_bytes_per_token(&c->cfg);
     o->kv_bytes_per_position = (int64_t)2 * c->geo.L * c->geo.kvh * c->geo.hd * 2;
     o->device_bytes = c->device_bytes;
-    o->long_context = c->long_ctx ? 1 : 0;
+    o->attn_tc = c->kernel_tc ? 1 : 0;
+    o->attn_tc_min_ctx = c->kernel_tc ? (int32_t)std::min<int64_t>(mk_tc_min_ctx(c), INT32_MAX) : -1;
     return MK_OK;
 }
 
@@ -948,6 +972,16 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_TRACE_DETAIL) {
         if (value < 0 || value > 2) return MK_ERR_INVALID_ARG;
         c->trace_detail = (int)value;
+        return MK_OK;
+    }
+    if (knob == MK_DBG_ATTN_BUILD) {
+        if (value < 0 || value > 2 || (value == 2 && !c->kernel_tc)) return MK_ERR_INVALID_ARG;
+        c->attn_build = (int)value;
+        return MK_OK;
+    }
+    if (knob == MK_DBG_ATTN_TC_MIN) {
+        if (value < 0 || value > (int64_t)c->geo.max_seq) return MK_ERR_INVALID_ARG;
+        c->tc_min_per_cta = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_WAIT_LIMIT_NS) {

@@ -38,7 +38,11 @@
 #define MK_COMBINE_LOADS 5            // float4 loads per thread in the attention combine
 #define MK_MISC_BYTES 6656
 #define MK_MAX_H 8192                 // largest hidden size the kernels take
-#define MK_LONG_CTX 8192              // max_seq from which the long-context kernel build is used (if built)
+// Positions per CTA from which a step runs the tensor-core attention build.
+// Measured on the 1B shape (19 CTAs per KV group) it is as fast as the
+// lane-parallel build at 13 positions per CTA and faster from there on (2% at
+// 54, 6% at 216), so every step of a shape that has it runs it.
+#define MK_ATTN_TC_MIN_PER_CTA 0
 
 // Device status word bits.
 #define MK_ST_TIMEOUT 0x1u
@@ -97,6 +101,10 @@ MK_HD int64_t mk_kv_index(int64_t pos, int d, int hd, int swz) {
     const int c = d >> 3;
     return pos * hd + ((int64_t)((swz ? (c ^ (int)(pos & 7)) : c) << 3) | (d & 7));
 }
+
+// Shapes whose attention runs on the tensor cores (4 query heads of 64 dims
+// per KV group); their K/V cache rows are chunk-permuted (mk_kv_index).
+MK_HD constexpr bool mk_attn_tc(int hd, int G) { return hd == 64 && G == 4; }
 
 // Fills everything but smem offsets from the shape; returns false if the
 // shape is outside what the kernels support.

@@ -873,15 +873,8 @@ __device__ __forceinline__ bool sync_wait(const MkParams& p, int idx, uint32_t t
 // lanes of a head.  Softmax is online (exp2, running max per head, rescaled
 // sums).  V: each thread accumulates its head's 8 dims over its positions, and
 // the position groups are summed with shared-memory atomics at the end.
-// HPL_: heads per lane.  Two (long contexts, where the K/V chunks then load
-// and unpack once for two heads) needs an even G and the parked partials to
-// fit the smem scratch; attn_long_ok tells.
-template <int HD, int G>
-__host__ __device__ constexpr bool attn_long_ok() {
-    // even G; one head per lane puts a position within one warp (so both
-    // layouts park one group per warp); the parked partials fit xv
-    return G % 2 == 0 && (HD / 8) * G <= 32 && MK_NCW * G * HD <= 8 * MK_NCT;
-}
+// HPL_: heads per lane (the K/V chunks load and unpack once for HPL heads);
+// the kernel runs one.
 template <int HD, int G, int HPL_ = 1>
 struct Attn {
     static constexpr int DC = HD / 8;                // lanes per head and position (8 dims each)
@@ -904,9 +897,10 @@ struct Attn {
     // weight.  q < nr from the ring tiles kt/vt, q == nr from the staged
     // current row (st: K, then V).  No barrier.
     static __device__ __forceinline__ void online(const uint8_t* kt, const uint8_t* vt, int nr, const uint8_t* st,
-                                                  int n, const float (&qr)[HPL][8], float (&m)[HPL],
+                                                  int n, int pos0, const float (&qr)[HPL][8], float (&m)[HPL],
                                                   float (&lsum)[HPL], float2 (&a2)[HPL][4]) {
         constexpr int CH = 4;                          // positions per thread and chunk
+        constexpr bool SWZ = mk_attn_tc(HD, G);        // ring rows chunk-permuted by position (pos0 + q)
         const int t = threadIdx.x, pp = t / TPP, dc = t % DC;
         for (int q0 = 0; q0 < n; q0 += CH * PPP) {     // uniform trip count across the warp
             float sc[CH][HPL];
@@ -919,8 +913,9 @@ struct Attn {
                 for (int j = 0; j < HPL; ++j) d[j] = make_float2(0.f, 0.f);
                 vw[c] = make_uint4(0u, 0u, 0u, 0u);
                 if (q < n) {
-                    const uint4 kw = lds128((q < nr ? kt + (size_t)q * HD * 2 : st) + dc * 16);
-                    vw[c] = lds128((q < nr ? vt + (size_t)q * HD * 2 : st + HD * 2) + dc * 16);
+                    const size_t ro = (size_t)q * HD * 2 + ((SWZ ? (dc ^ ((pos0 + q) & 7)) : dc) << 4);
+                    const uint4 kw = lds128(q < nr ? kt + ro : st + dc * 16);
+                    vw[c] = lds128(q < nr ? vt + ro : st + HD * 2 + dc * 16);
                     const float2 k0 = bf2_lo_hi(kw.x), k1 = bf2_lo_hi(kw.y), k2 = bf2_lo_hi(kw.z), k3 = bf2_lo_hi(kw.w);
 #pragma unroll
                     for (int j = 0; j < HPL; ++j) {
@@ -1275,16 +1270,10 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
         if (nr > 0) {
             Ring rv = ring;
             rv.advance(g.ns);      // the V tile follows the K tile in the stream
-            // long contexts (two heads per lane) take a K/V block pair per 256 positions, all
-            // landed long ago: the vote-based fast take pays there (measured +1.4% at 32K),
-            // while for a single short block it measured slower (1B -1.1%)
-            if constexpr (HPL > 1)
-                ok = take_landed(p, s, ring, (uint32_t)(nr * HD * 2), kt) && take_landed(p, s, rv, (uint32_t)(nr * HD * 2), vt);
-            else
-                ok = take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt) && take_tile(p, s, rv, (uint32_t)(nr * HD * 2), vt);
+            ok = take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt) && take_tile(p, s, rv, (uint32_t)(nr * HD * 2), vt);
         }
         if (b == 0) MK_TRACE_D(l, 5);   // first block's K and V taken
-        if (ok) A::online(kt, vt, nr, st, n, qr, m_, l_, acc);
+        if (ok) A::online(kt, vt, nr, st, n, q0, qr, m_, l_, acc);
         if (b == 0) MK_TRACE_D(l, 6);   // first block's softmax done
         if (nr > 0) { release_tile(p, s, ring); release_tile(p, s, ring); }
         if (!ok) ab = true;     // made uniform by the barrier below
@@ -1322,9 +1311,11 @@ __device__ __forceinline__ float mk_gumbel(uint64_t seed, int pos, int v) {
 
 // HD: head_dim; G: query heads per KV head; MH = H / 256, the 8-column chunks
 // each lane owns in a row of H (the GEMV width of QKV, gate/up and LM head);
-// LC: long-context build (two query heads per attention lane where the shape
-// allows: fewer instructions per position when a CTA attends to thousands of
-// positions, more registers held, slower on short contexts).
+// LC: long-context build: the attention runs on the tensor cores (16-position
+// chunks per warp; shapes with 4 query heads of 64 dims per KV group), which
+// pays once every CTA attends to more positions than one chunk per warp; on
+// short contexts the lane-parallel attention of the standard build has the
+// shorter dependency chain.  The host picks the build per step.
 template <int HD, int G, int MH, int LC>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
     static_assert(G <= MK_NCW, "one consumer warp per query head of a KV group (softmax, combine weights)");
@@ -1458,8 +1449,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 } else {
                     uint16_t* dst = (slot == G ? p.kc : p.vc) + ((size_t)l * g.kvh + pl.g) * g.max_seq * HD;
                     const uint16_t ab16 = f2bf(a), bb16 = f2bf(b);
-                    dst[mk_kv_index(p.pos, d, HD, LC)] = ab16;
-                    dst[mk_kv_index(p.pos, d + hd2, HD, LC)] = bb16;
+                    dst[mk_kv_index(p.pos, d, HD, mk_attn_tc(HD, G))] = ab16;
+                    dst[mk_kv_index(p.pos, d + hd2, HD, mk_attn_tc(HD, G))] = bb16;
                     uint64_t* kv = p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (slot - G)) * HD;
                     if (pub) { st_ll(kv + d, ll_pack(bf2f(ab16), s.misc->tag)); st_ll(kv + d + hd2, ll_pack(bf2f(bb16), s.misc->tag)); }
                 }

@@ -33,6 +33,8 @@ MK_DBG_INFLIGHT = 6
 MK_DBG_INFLIGHT_LAT = 7
 MK_DBG_PF_LEAD = 8
 MK_DBG_PF_DEPTH = 9
+MK_DBG_ATTN_BUILD = 10
+MK_DBG_ATTN_TC_MIN = 11
 MK_NOALLOC_ARGMAX_BLOCKS = 1024
 MK_NOALLOC_ARGMAX_MAX_N = MK_NOALLOC_ARGMAX_BLOCKS * 4096
 
@@ -59,7 +61,7 @@ class mk_info(ctypes.Structure):
     _fields_ = [("grid_ctas", _i32), ("ctas_per_group", _i32), ("block_threads", _i32), ("ring_stages", _i32),
                 ("slot_bytes", _i32), ("smem_bytes", _i32), ("sm_count", _i32), ("l2_prefetch_bytes", _i32),
                 ("arena_bytes", _i64), ("weight_bytes_per_token", _i64), ("kv_bytes_per_position", _i64),
-                ("device_bytes", _i64), ("long_context", _i32)]
+                ("device_bytes", _i64), ("attn_tc", _i32), ("attn_tc_min_ctx", _i32)]
 
 
 # (name, restype, argtypes) of every exported function, in header order.

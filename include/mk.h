@@ -106,9 +106,11 @@ typedef struct {
     int64_t weight_bytes_per_token;  /* bf16 weight bytes one step reads (matrices + gains + 1 embedding row) */
     int64_t kv_bytes_per_position;   /* bf16 K+V bytes one attended position costs (all layers) */
     int64_t device_bytes;            /* everything the context allocated on the device */
-    int32_t long_context;            /* 1: the kernel build for long contexts runs (max_seq >= 8192
-                                        and one was built for this shape: two query heads per
-                                        attention lane, fewer instructions per cached position) */
+    int32_t attn_tc;                 /* 1: a build whose attention runs on the tensor cores exists
+                                        for this shape (4 query heads of 64 dims per KV group) */
+    int32_t attn_tc_min_ctx;         /* context length (pos + 1) from which a step launches that
+                                        build; shorter contexts run the lane-parallel attention
+                                        (-1 without attn_tc) */
 } mk_info;
 
 /* Create a context on CUDA device `device`: validates the shape, sizes the
@@ -275,6 +277,13 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
 /* MK_DBG_PF_DEPTH: tiles of warming loads the L2 warmer keeps in flight,
  * 1 or 2 (0 = the default, 1). */
 #define MK_DBG_PF_DEPTH 9
+/* MK_DBG_ATTN_BUILD: which build a step launches: 0 (default) by context length
+ * (attn_tc_min_ctx), 1 the lane-parallel attention always, 2 the tensor-core
+ * attention always (MK_ERR_INVALID_ARG without attn_tc).  MK_DBG_ATTN_TC_MIN:
+ * positions per CTA from which the default picks the tensor-core build
+ * (default 0: every step; 0 .. max_seq). */
+#define MK_DBG_ATTN_BUILD 10
+#define MK_DBG_ATTN_TC_MIN 11
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
 const char* mk_strerror(int code);

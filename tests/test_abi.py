@@ -78,3 +78,20 @@ def test_no_closed_cuda_calls_in_sources():
             for f in files:
                 if f.endswith((".cu", ".h", ".c", ".cpp", ".py")) and f != "test_abi.py":
                     assert not pat.search(open(os.path.join(base, f), errors="ignore").read()), f
+
+
+def test_binding_constants_match_header():
+    """Every MK_DBG_* / MK_ERR_* / MK_OK number the header defines has the same
+    value in the Python binding, and mk_info's fields are mirrored in order."""
+    src = open(os.path.join(ROOT, "include", "mk.h")).read()
+    defs = dict(re.findall(r"#define\s+(MK_(?:DBG|ERR)_[A-Z0-9_]+|MK_OK)\s+\(?(-?\d+)\)?", src))
+    assert "MK_DBG_ATTN_BUILD" in defs and "MK_DBG_ATTN_TC_MIN" in defs
+    for name, val in defs.items():
+        if hasattr(mk, name):
+            assert getattr(mk, name) == int(val), name
+    assert all(hasattr(mk, n) for n in defs if n.startswith("MK_DBG_")), defs
+    end = src.index("} mk_info;")
+    body = src[src.rindex("typedef struct {", 0, end):end]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = [f.strip() for decl in re.findall(r"int(?:32|64)_t\s+([^;]+);", body) for f in decl.split(",")]
+    assert fields == [f for f, _ in mk.mk_info._fields_], fields

@@ -71,19 +71,22 @@ def test_mid_shape_ragged(grid, prefill):
     dec.close()
 
 
-@pytest.mark.parametrize("grid,prefill", [(0, 5001), (6, 3000), (0, 0), (14, 37)])
-def test_long_context_build(grid, prefill):
-    """max_seq >= 8192 selects the long-context kernel build (attention on the
-    tensor cores, K/V rows chunk-permuted in the cache) for H=512, G=4.
-    A 5001-position prefill on the full grid (ragged per-CTA chunks) and 3000
-    positions on 3 CTAs per KV group (each CTA walks about a thousand positions,
-    many KV blocks); decoding from position 0 (blocks of the current row alone,
-    16-position chunks mostly past the end) and a 37-position prefill on 7 CTAs
-    per group (a few positions per CTA).  The K/V rows the kernel appends read
-    back (through the permuted layout) as the oracle's."""
+@pytest.mark.parametrize("grid,prefill,build", [(0, 5001, 2), (6, 3000, 2), (6, 3000, 1), (0, 0, 2), (14, 37, 2),
+                                               (14, 37, 1)])
+def test_long_context_build(grid, prefill, build):
+    """H=512, G=4 has a build whose attention runs on the tensor cores (build 2)
+    beside the lane-parallel one (build 1); both read the K/V rows
+    chunk-permuted in the cache.  A 5001-position prefill on the full grid
+    (ragged per-CTA chunks) and 3000 positions on 3 CTAs per KV group (each CTA
+    walks about a thousand positions, many KV blocks); decoding from position 0
+    (blocks of the current row alone, 16-position chunks mostly past the end)
+    and a 37-position prefill on 7 CTAs per group (a few positions per CTA).
+    The K/V rows the kernel appends read back (through the permuted layout) as
+    the oracle's."""
     tun = mk.tuning(grid_ctas=grid) if grid else None
     m, dec, orc = make(MID, 47, 8192, gains="normal", std=0.04, tuning=tun)
-    assert dec.info.long_context == 1
+    assert dec.info.attn_tc == 1
+    dec.set_debug(mk.MK_DBG_ATTN_BUILD, build)
     if prefill:
         ks, vs = synth.make_kv(MID, prefill, 53)
         dec.set_kv(ks, vs, prefill)
@@ -102,12 +105,27 @@ def test_long_context_build(grid, prefill):
     dec.close()
 
 
+def test_attention_build_switch_by_context():
+    """By default a step runs the tensor-core attention build once the context
+    gives every CTA attn_tc_min_ctx / CTAs-per-group positions: with 3 per CTA on
+    7 CTAs per group the switch comes at context 21, inside one teacher-forced
+    run from position 0, and parity holds on both sides of it."""
+    m, dec, orc = make(MID, 71, 8192, gains="normal", std=0.04, tuning=mk.tuning(grid_ctas=14))
+    dec.set_debug(mk.MK_DBG_ATTN_TC_MIN, 3)
+    info = mk.mk_get_info(dec.ctx)
+    assert info.attn_tc == 1 and info.attn_tc_min_ctx == 21
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, MID.vocab, 71, 3), 0, 40)
+    print(rep.summary())
+    rep.check()
+    dec.close()
+
+
 def test_kv_rows_round_trip_long_context():
     """set_kv / get_kv hide the long-context build's chunk-permuted rows: a
     window at an odd offset reads back bit for bit."""
     m = synth.make_model(MID, 5, std=0.04)
     dec = Decoder(m, 8192)
-    assert dec.info.long_context == 1
+    assert dec.info.attn_tc == 1
     ks, vs = synth.make_kv(MID, 301, 7)
     dec.set_kv(ks, vs, 301)
     for l in range(MID.n_layers):
@@ -163,7 +181,7 @@ def test_perop_baseline_long_context_layout():
     """The per-operator path appends to and reads the cache in the long-context
     build's chunk-permuted layout, after a prefill through set_kv."""
     m, dec, orc = make(MID, 61, 8192, gains="normal", std=0.04, perop=True)
-    assert dec.info.long_context == 1
+    assert dec.info.attn_tc == 1
     ks, vs = synth.make_kv(MID, 45, 67)
     dec.set_kv(ks, vs, 45)
     orc.set_kv(ks, vs, 45)
