@@ -1014,8 +1014,8 @@ struct Attn {
 // per-position arithmetic of the lane-parallel softmax above (partial dots
 // reduced by shuffles, bf16 unpacking, one dependent FMA chain per head) takes
 // about twice as long as the K/V bytes take to arrive.  The contraction is
-// dense, though: per 16 positions, S = [q_hi; q_lo] K^T is a 16x8x64 product
-// and O += P V a 16x64x16 one, so each warp runs them as mma.m16n8k16 (bf16
+// dense, though: per 16 positions, S = [q_hi; q_lo] K^T is a 16x8xHD product
+// and O += P V a 16xHDx16 one, so each warp runs them as mma.m16n8k16 (bf16
 // in, fp32 accumulate), keeping q, P and O in registers:
 //   - scores: A = q of the group's 4 heads split into a bf16 high part (rows
 //     0-3) and the bf16 rounding of the remainder (rows 4-7), B = 8 K rows
@@ -1068,29 +1068,31 @@ __device__ __forceinline__ uint32_t split_bf2(float x, float y, bool lo) {
 template <int HD, int G>
 __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
                                                bool has_cur, float qscale, bool ab, const float* qs) {
-    static_assert(HD == 64 && G == 4, "tensor-core attention: 4 heads of 64 dims per KV group");
+    static_assert(mk_attn_tc(HD, G), "tensor-core attention: 4 heads of 64 dims per KV group");
+    constexpr int NKS = HD / 16;         // 16-dim k steps of a score tile
+    constexpr int ND = HD / 8;           // 8-dim tiles of O
     constexpr int NMG = Attn<HD, G>::NMG;
     static_assert(NMG == MK_NCW, "one parked group per consumer warp");
     const MkGeom& g = p.geo;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     const bool lo = lane >= 16;          // this lane's rows hold the remainder parts (4-7)
     const int qd = 2 * (lane & 3);       // first of this lane's two k (or n) indices in a tile
-    // A fragments of [q_hi; q_lo] (pre-scaled by log2(e)/sqrt(hd)) for the four
+    // A fragments of [q_hi; q_lo] (pre-scaled by log2(e)/sqrt(hd)) for the
     // 16-dim k steps: row lane/4 (head (lane/4) mod 4), dims 16ks + qd (+8)
-    uint32_t qa[4][2];
+    uint32_t qa[NKS][2];
     {
         const float* qh = qs + ((lane >> 2) & 3) * HD;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
+        for (int ks = 0; ks < NKS; ++ks)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int d = 16 * ks + 8 * hf + qd;
                 qa[ks][hf] = split_bf2(qh[d] * qscale, qh[d + 1] * qscale, lo);
             }
     }
-    float o[8][2];
+    float o[ND][2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = 0.f;
+    for (int j = 0; j < ND; ++j) o[j][0] = o[j][1] = 0.f;
     float m = -INFINITY, lsum = 0.f;
     MK_TRACE_D(l, 1);
     const uint32_t zaddr = smem_u32(&s.misc->zrow);
@@ -1131,12 +1133,12 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
                     const int i = c0 + 8 * tt + (lane & 7);
-                    uint32_t kb[2][4];
-                    ldsm_x4(kb[0], row(ka_, 0u, i, lane >> 3));
-                    ldsm_x4(kb[1], row(ka_, 0u, i, 4 + (lane >> 3)));
+                    uint32_t kb[NKS / 2][4];   // 8x8 matrices of chunks 4x .. 4x+3: two k steps each
+#pragma unroll
+                    for (int x = 0; x < NKS / 2; ++x) ldsm_x4(kb[x], row(ka_, 0u, i, 4 * x + (lane >> 3)));
                     float c0_ = 0.f, c1_ = 0.f;
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
+                    for (int ks = 0; ks < NKS; ++ks)
                         mma_rows8(c0_, c1_, qa[ks][0], qa[ks][1], kb[ks >> 1][2 * (ks & 1)], kb[ks >> 1][2 * (ks & 1) + 1]);
                     // high part + remainder: lanes 16 apart hold the same head and positions
                     c0_ += __shfl_xor_sync(0xFFFFFFFFu, c0_, 16);
@@ -1155,11 +1157,11 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
                 lsum = fmaf(lsum, corr, (p00 + p01) + (p10 + p11));
                 m = cm;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) { o[j][0] *= corr; o[j][1] *= corr; }
+                for (int j = 0; j < ND; ++j) { o[j][0] *= corr; o[j][1] *= corr; }
                 const uint32_t pa0 = split_bf2(p00, p01, lo), pa2 = split_bf2(p10, p11, lo);
                 // O += P V: V^T fragments of d tiles 2jj, 2jj+1 (rows c0.. and c0+8..)
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
+                for (int jj = 0; jj < ND / 2; ++jj) {
                     const int mt = lane >> 3;
                     uint32_t vb[4];
                     ldsm_x4_trans(vb, row(va_, (uint32_t)(HD * 2), c0 + 8 * (mt & 1) + (lane & 7), 2 * jj + (mt >> 1)));
@@ -1180,7 +1182,7 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
     lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
     lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < ND; ++j) {
         o[j][0] += __shfl_xor_sync(0xFFFFFFFFu, o[j][0], 16);
         o[j][1] += __shfl_xor_sync(0xFFFFFFFFu, o[j][1], 16);
     }
@@ -1188,7 +1190,7 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
         const int h = lane >> 2;
         float* xp = s.xv + w * (G * HD) + h * HD + qd;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) *reinterpret_cast<float2*>(xp + 8 * j) = make_float2(o[j][0], o[j][1]);
+        for (int j = 0; j < ND; ++j) *reinterpret_cast<float2*>(xp + 8 * j) = make_float2(o[j][0], o[j][1]);
         if ((lane & 3) == 0) { s.sc[w * G + h] = m; s.sc[NMG * G + w * G + h] = lsum; }
     }
     return ab;
@@ -1319,7 +1321,7 @@ __device__ __forceinline__ float mk_gumbel(uint64_t seed, int pos, int v) {
 template <int HD, int G, int MH, int LC>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
     static_assert(G <= MK_NCW, "one consumer warp per query head of a KV group (softmax, combine weights)");
-    static_assert(!LC || (HD == 64 && G == 4), "the long-context build's attention runs on 4 heads of 64 dims");
+    static_assert(!LC || mk_attn_tc(HD, G), "the long-context build's attention runs on 4 heads of 64 dims");
     // generation already stopped (an earlier launch sampled the stop token):
     // every CTA returns before touching any state
     if (p.stop && *(volatile int32_t*)p.stop) return;

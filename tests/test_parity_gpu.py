@@ -134,9 +134,15 @@ def test_kv_rows_round_trip_long_context():
     dec.close()
 
 
-def test_head_dim_128_shape():
+@pytest.mark.parametrize("grid", [0, 6])
+def test_head_dim_128_shape(grid):
+    """hd=128, G=4 (the 8B head layout, lane-parallel attention on plain rows):
+    200 pre-filled positions spread over the full grid and over 3 CTAs per KV
+    group (two 128-row blocks per CTA)."""
     s = synth.ModelShape(2, 1024, 8, 2, 128, 1536, 4099, 1e-5, 500000.0, False)
-    m, dec, orc = make(s, 31, 512, gains="normal", std=0.03)
+    tun = mk.tuning(grid_ctas=grid) if grid else None
+    m, dec, orc = make(s, 31, 512, gains="normal", std=0.03, tuning=tun)
+    assert dec.info.attn_tc == 0
     ks, vs = synth.make_kv(s, 200, 37)
     dec.set_kv(ks, vs, 200)
     orc.set_kv(ks, vs, 200)
