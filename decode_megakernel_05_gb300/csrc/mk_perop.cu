@@ -133,8 +133,17 @@ __global__ void attn_partial_kernel(const float* q, const uint16_t* kc, const ui
     const uint16_t* K = kc + ((int64_t)layer * kvh + g) * max_seq * hd;
     const uint16_t* Vv = vc + ((int64_t)layer * kvh + g) * max_seq * hd;
     for (int p = a + threadIdx.x; p < b; p += blockDim.x) {
+        // the row's 16-byte chunks in dim order (each one load), dims ascending
+        const uint4* kr = reinterpret_cast<const uint4*>(K + (int64_t)p * hd);
         float s = 0.f;
-        for (int d = 0; d < hd; ++d) s = fmaf(qs[d], bf(K[kvi(p, d, hd, swz)]), s);
+        for (int c = 0; c < hd / 8; ++c) {
+            const uint4 w = kr[swz ? (c ^ (p & 7)) : c];
+            const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+            for (int j = 0; j < 4; ++j) {
+                s = fmaf(qs[8 * c + 2 * j], bf((uint16_t)(e[j] & 0xFFFFu)), s);
+                s = fmaf(qs[8 * c + 2 * j + 1], bf((uint16_t)(e[j] >> 16)), s);
+            }
+        }
         sc[p - a] = s;
     }
     __syncthreads();
