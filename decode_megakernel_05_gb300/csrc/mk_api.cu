@@ -257,6 +257,7 @@ struct mk_ctx {
     unsigned long long* amax = nullptr;
     int32_t *next_token = nullptr, *tokens_dev = nullptr, *prompt_dev = nullptr;
     int32_t* stop = nullptr;             // generation stopped (mk_generate with a stop token)
+    uint32_t* status_host = nullptr;     // pinned copy of the status word (read behind generate calls)
     // debug
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
     int trace_detail = 1;
@@ -509,6 +510,9 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         (rc = c->dalloc(&c->tokens_dev, (size_t)g.max_seq * 4)) ||
         (rc = c->dalloc(&c->prompt_dev, (size_t)g.max_seq * 4)) || (rc = c->dalloc(&c->stop, 4)))
         return fail(rc);
+    if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->status_host), 4, cudaHostAllocDefault)) != cudaSuccess)
+        return fail(cuda_fail(e, "cudaHostAlloc"));
+    *c->status_host = 0;
     cudaStream_t st = nullptr;
     if ((e = cudaMemcpy(c->d_plans, c->plans.data(), sizeof(MkCtaPlan) * g.nC, cudaMemcpyHostToDevice)) ||
         (e = cudaMemset(c->kc, 0, kv_elems * 2)) || (e = cudaMemset(c->vc, 0, kv_elems * 2)) ||
@@ -529,6 +533,7 @@ void mk_destroy(mk_ctx* c) {
     if (!c) return;
     cudaSetDevice(c->device);
     for (void* p : c->allocs) cudaFree(p);
+    if (c->status_host) cudaFreeHost(c->status_host);
     for (uint16_t* p : c->perop.wqkv) cudaFree(p);
     for (uint16_t* p : c->perop.wo) cudaFree(p);
     for (uint16_t* p : c->perop.wgu) cudaFree(p);
@@ -799,6 +804,8 @@ int mk_decode_step_greedy(mk_ctx* c, int32_t pos, float* logits_out, void* strea
     return launch_step(c, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+static int sync_status(mk_ctx* c, cudaStream_t st, int* dev_rc);
+
 int mk_generate_greedy(mk_ctx* c, const int32_t* prompt, int32_t n_prompt, int32_t start_pos, int32_t n_new,
                        int32_t* out_tokens, void* stream) {
     if (!c || !prompt || !out_tokens || n_prompt < 1 || n_new < 1 || start_pos < 0) return MK_ERR_INVALID_ARG;
@@ -821,8 +828,9 @@ int mk_generate_greedy(mk_ctx* c, const int32_t* prompt, int32_t n_prompt, int32
         if (rc != MK_OK) return rc;
     }
     MK_CU(cudaMemcpyAsync(out_tokens, c->tokens_dev, (size_t)n_new * 4, cudaMemcpyDeviceToHost, st));
-    MK_CU(cudaStreamSynchronize(st));
-    return mk_status(c);
+    int dev = MK_OK;
+    const int rc = sync_status(c, st, &dev);
+    return rc != MK_OK ? rc : dev;
 }
 
 int mk_decode_step_sample(mk_ctx* c, int32_t token, int32_t pos, float temperature, uint64_t seed,
@@ -871,7 +879,9 @@ int mk_generate(mk_ctx* c, const int32_t* prompt, int32_t n_prompt, int32_t star
         if (rc != MK_OK) return rc;
     }
     MK_CU(cudaMemcpyAsync(out_tokens, c->tokens_dev, (size_t)n_new * 4, cudaMemcpyDeviceToHost, st));
-    MK_CU(cudaStreamSynchronize(st));
+    int dev = MK_OK;
+    const int rc = sync_status(c, st, &dev);
+    if (rc != MK_OK) return rc;
     // the tokens up to and including the first stop token; the launches after it returned at once
     int32_t n = n_new;
     if (eos_id >= 0)
@@ -879,7 +889,7 @@ int mk_generate(mk_ctx* c, const int32_t* prompt, int32_t n_prompt, int32_t star
             if (out_tokens[i] == eos_id) { n = i + 1; break; }
     for (int32_t i = n; i < n_new; ++i) out_tokens[i] = -1;
     if (n_out) *n_out = n;
-    return mk_status(c);
+    return dev;
 }
 
 int mk_get_hidden(mk_ctx* c, float* out, void* stream) {
@@ -895,6 +905,14 @@ int mk_get_argmax(mk_ctx* c, int32_t* out, void* stream) {
     return MK_OK;
 }
 
+// The error a device status word stands for.
+static int status_code(uint32_t st) {
+    if (st & (MK_ST_TIMEOUT | MK_ST_SCHEDULE)) return MK_ERR_DEVICE_TIMEOUT;
+    if (st & MK_ST_NUMERIC) return MK_ERR_NUMERIC;
+    if (st & MK_ST_BADTOKEN) return MK_ERR_INVALID_ARG;
+    return MK_OK;
+}
+
 int mk_status(mk_ctx* c) {
     if (!c) return MK_ERR_INVALID_ARG;
     MK_CU(cudaSetDevice(c->device));
@@ -902,9 +920,23 @@ int mk_status(mk_ctx* c) {
     uint32_t st = 0;
     MK_CU(cudaMemcpy(&st, c->status, 4, cudaMemcpyDeviceToHost));
     MK_CU(cudaMemset(c->status, 0, 4));
-    if (st & (MK_ST_TIMEOUT | MK_ST_SCHEDULE)) return MK_ERR_DEVICE_TIMEOUT;
-    if (st & MK_ST_NUMERIC) return MK_ERR_NUMERIC;
-    if (st & MK_ST_BADTOKEN) return MK_ERR_INVALID_ARG;
+    return status_code(st);
+}
+
+// mk_status for the generate calls: the status word is copied to pinned host
+// memory behind the work already queued on st, so one synchronization covers
+// the tokens and the status; the word is cleared only when it is set.  The
+// return value is the CUDA outcome (the queued work is complete when it is
+// MK_OK); *dev_rc receives the device status as mk_status reports it.
+static int sync_status(mk_ctx* c, cudaStream_t st, int* dev_rc) {
+    *dev_rc = MK_OK;
+    MK_CU(cudaMemcpyAsync(c->status_host, c->status, 4, cudaMemcpyDeviceToHost, st));
+    MK_CU(cudaStreamSynchronize(st));
+    const uint32_t v = *c->status_host;
+    if (v == 0) return MK_OK;
+    MK_CU(cudaMemsetAsync(c->status, 0, 4, st));
+    MK_CU(cudaStreamSynchronize(st));
+    *dev_rc = status_code(v);
     return MK_OK;
 }
 

@@ -155,8 +155,11 @@ int mk_decode_step_greedy(mk_ctx* ctx, int32_t pos, float* logits_out, void* str
  * more steps, each fed the previous step's argmax, which the kernel reads from
  * device memory: no host round trip between tokens.  Writes the n_new
  * generated tokens to out_tokens (host int32 [n_new]).  Launches
- * n_prompt + n_new - 1 kernels, synchronizes `stream`, and returns the device
- * status (MK_ERR_DEVICE_TIMEOUT / MK_ERR_NUMERIC) if one was latched. */
+ * n_prompt + n_new - 1 kernels, synchronizes `stream` once (the tokens and the
+ * status word are copied back behind the launches) and returns the device
+ * status (MK_ERR_DEVICE_TIMEOUT / MK_ERR_NUMERIC), clearing it, if one was
+ * latched.  The library holds 4 bytes of pinned host memory per context for
+ * that status copy. */
 int mk_generate_greedy(mk_ctx* ctx, const int32_t* prompt, int32_t n_prompt, int32_t start_pos,
                        int32_t n_new, int32_t* out_tokens, void* stream);
 
