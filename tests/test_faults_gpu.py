@@ -66,6 +66,20 @@ def test_argument_errors_return_codes_without_launch(tiny):
     assert lib.mk_decode_step(dec.ctx, 1, dec.max_seq, None, dec.stream) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_decode_step_greedy(dec.ctx, -5, None, dec.stream) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_set_debug(dec.ctx, 99, 0) == mk.MK_ERR_INVALID_ARG
+    # attention-build knobs: this shape (2 query heads per KV group) has no tensor-core build
+    assert dec.info.attn_tc == 0 and dec.info.attn_tc_min_ctx == -1
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_BUILD, 2) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_BUILD, 3) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_TC_MIN, -1) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_TC_MIN, dec.max_seq + 1) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_BUILD, 0) == mk.MK_OK
+    # a K/V window past the end of the cache
+    k = np.zeros((w.shape.n_kv_heads, 2, w.shape.head_dim), dtype=np.uint16)
+    v = np.zeros_like(k)
+    assert lib.mk_get_kv(dec.ctx, 0, dec.max_seq - 1, 2, k.ctypes.data, v.ctypes.data, dec.stream) == \
+        mk.MK_ERR_INVALID_ARG
+    assert lib.mk_set_kv(dec.ctx, 0, k.ctypes.data, v.ctypes.data, dec.max_seq + 1, dec.stream) == \
+        mk.MK_ERR_INVALID_ARG
     assert dec.status() == mk.MK_OK
 
 

@@ -120,6 +120,20 @@ def test_attention_build_switch_by_context():
     dec.close()
 
 
+def test_decode_up_to_the_last_cache_slot():
+    """max_seq = 40: forty teacher-forced steps from position 0 end at the last
+    cache slot (pos = max_seq - 1) on the tensor-core build; position max_seq
+    is refused."""
+    m, dec, orc = make(MID, 73, 40, gains="normal", std=0.04)
+    assert dec.info.attn_tc == 1
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, MID.vocab, 73, 3), 0, 40)
+    print(rep.summary())
+    rep.check()
+    assert mk.load().mk_decode_step(dec.ctx, 1, 40, None, dec.stream) == mk.MK_ERR_INVALID_ARG
+    assert dec.status() == mk.MK_OK
+    dec.close()
+
+
 def test_kv_rows_round_trip_long_context():
     """set_kv / get_kv hide the long-context build's chunk-permuted rows: a
     window at an odd offset reads back bit for bit."""
