@@ -128,11 +128,17 @@ int mk_load_weights(mk_ctx* ctx, const mk_weights* w, void* stream);
 
 /* Pre-fill cache positions [0, n_pos) of one layer.  k, v: bf16 [kvh][n_pos][hd],
  * host or device memory; K must already be rotated (post-RoPE), as decode
- * steps store it.  Synchronizes `stream`. */
+ * steps store it.  Synchronizes `stream`.  Where the cache keeps its rows
+ * chunk-permuted (mk_info.attn_tc), the rows pass through a temporary device
+ * buffer of 4 * kvh * n_pos * hd bytes, allocated and freed by the call
+ * (MK_ERR_OOM if it cannot be had); the caller's layout is the same either
+ * way. */
 int mk_set_kv(mk_ctx* ctx, int32_t layer, const void* k, const void* v, int32_t n_pos, void* stream);
 
 /* Copy cache positions [pos0, pos0 + n_pos) of one layer out to k_out, v_out
- * (bf16 [kvh][n_pos][hd], host or device memory).  Synchronizes `stream`. */
+ * (bf16 [kvh][n_pos][hd], host or device memory, rows in plain order whatever
+ * the cache's layout; a temporary device buffer as for mk_set_kv).
+ * Synchronizes `stream`. */
 int mk_get_kv(mk_ctx* ctx, int32_t layer, int32_t pos0, int32_t n_pos, void* k_out, void* v_out, void* stream);
 
 /* One decode step (one kernel launch): feed `token` at position `pos`, write
