@@ -69,6 +69,12 @@ int cuda_fail(cudaError_t e, const char* what) {
     return e == cudaErrorMemoryAllocation ? MK_ERR_OOM : MK_ERR_CUDA;
 }
 
+}  // namespace
+
+int mk_record_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
+namespace {
+
 #define MK_CU(call)                                   \
     do {                                              \
         cudaError_t e_ = (call);                      \

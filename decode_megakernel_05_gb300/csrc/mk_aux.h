@@ -25,3 +25,6 @@ cudaError_t mk_launch_bf16_to_f32(const uint16_t* src, float* dst, int64_t n, cu
 // selects the direction.  Both buffers are device memory.
 cudaError_t mk_launch_kv_rows(uint16_t* plain, uint16_t* cache_layer, int kvh, int n_pos, int pos0, int max_seq, int hd,
                               int swz, int to_cache, cudaStream_t st);
+// Records a failed CUDA call as the text mk_last_cuda_error() returns ("what:
+// error string (code)") and maps it to MK_ERR_OOM or MK_ERR_CUDA.
+int mk_record_cuda_error(cudaError_t e, const char* what);

@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "../../include/mk.h"
+#include "mk_aux.h"
 
 namespace {
 
@@ -31,8 +32,11 @@ static_assert((long long)MK_NOALLOC_ARGMAX_MAX_N == (long long)MK_NOALLOC_ARGMAX
 static __device__ __align__(256) unsigned long long g_argmax_scratch[MK_NOALLOC_ARGMAX_BLOCKS];
 
 // Order-preserving key: larger float -> larger key; on equal values the lower
-// index wins (its complement is larger).
+// index wins (its complement is larger).  -0.0 and +0.0 compare equal as
+// floats, so both take the key of +0.0 (the lower index then wins, as in a
+// float comparison).
 __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+    if (v == 0.0f) v = 0.0f;
     uint32_t u = __float_as_uint(v);
     u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     return ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)idx);
@@ -82,17 +86,24 @@ __global__ void noalloc_argmax_final(const unsigned long long* part, int nblocks
 
 // Device address of the scratch array, looked up once per device (the
 // array's host-side name is only a handle for the runtime, not an address).
+// The address stays valid for the life of the device's context; after a
+// cudaDeviceReset the cached address is stale (the entry point is not for use
+// on that device afterwards).
 constexpr int kMaxDevices = 64;
 std::mutex g_lock;
 void* g_scratch_addr[kMaxDevices] = {};
 
 int scratch_for_current_device(unsigned long long** out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MK_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return mk_record_cuda_error(e, "mk_argmax_f32_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return MK_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> guard(g_lock);
     if (!g_scratch_addr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_argmax_scratch) != cudaSuccess || !p) return MK_ERR_CUDA;
+        e = cudaGetSymbolAddress(&p, g_argmax_scratch);
+        if (e != cudaSuccess) return mk_record_cuda_error(e, "mk_argmax_f32_noalloc: cudaGetSymbolAddress");
+        if (!p) return MK_ERR_CUDA;
         g_scratch_addr[dev] = p;
     }
     *out = reinterpret_cast<unsigned long long*>(g_scratch_addr[dev]);
@@ -109,7 +120,16 @@ extern "C" int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* ou
     if (rc != MK_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int nblocks = (n + kPerBlock - 1) / kPerBlock;
-    noalloc_argmax_partial<<<nblocks, kThreads, 0, st>>>(logits, n, scratch);
-    noalloc_argmax_final<<<1, kThreads, 0, st>>>(scratch, nblocks, out_token);
-    return cudaGetLastError() == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+    // cudaLaunchKernel returns the outcome of this launch itself, so an error
+    // an earlier, unrelated call left pending is neither taken for this
+    // call's nor cleared; a failure names the kernel that did not launch
+    void* a1[] = {(void*)&logits, (void*)&n, (void*)&scratch};
+    cudaError_t e = cudaLaunchKernel((const void*)noalloc_argmax_partial, dim3(nblocks), dim3(kThreads), a1, 0, st);
+    if (e != cudaSuccess) return mk_record_cuda_error(e, "mk_argmax_f32_noalloc: partial-argmax launch");
+    const unsigned long long* part = scratch;
+    int nb = nblocks;
+    void* a2[] = {(void*)&part, (void*)&nb, (void*)&out_token};
+    e = cudaLaunchKernel((const void*)noalloc_argmax_final, dim3(1), dim3(kThreads), a2, 0, st);
+    if (e != cudaSuccess) return mk_record_cuda_error(e, "mk_argmax_f32_noalloc: final-argmax launch");
+    return MK_OK;
 }

@@ -209,7 +209,7 @@ int mk_get_argmax(mk_ctx* ctx, int32_t* out, void* stream);
 int mk_status(mk_ctx* ctx);
 
 /* Unfused baseline of the same step: the same arithmetic launched as one
- * kernel per operator (about 7 per layer + 4), on plain row-major weights
+ * kernel per operator (9 per layer + 5: 149 for the 16-layer 1B shape), on plain row-major weights
  * (cloud.baidu.com/article/9434380, section 5, step 5 keeps the per-operator
  * path for comparison and debugging; section 7 asks for the fusion-off
  * ablation).  Needs mk_load_weights to have run with keep_rowmajor = 1 in
@@ -232,10 +232,14 @@ int mk_get_info(const mk_ctx* ctx, mk_info* out);
  * loads the library until the process exits.  n > MK_NOALLOC_ARGMAX_MAX_N (or
  * n < 1, or a NULL pointer) returns MK_ERR_INVALID_ARG without launching.
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
- * call shares the array: calls whose kernels overlap on the GPU (e.g. two
- * streams at once) race and must be serialized by the caller.  Runs on the
- * calling thread's current device; asynchronous on `stream`. */
+ * device current) and keeps it for the life of the process; make that first
+ * call before any stream capture, and do not use this entry point on a device
+ * after cudaDeviceReset (the reset unloads the array, and the kept address is
+ * then stale).  Every call shares the array: calls whose kernels overlap on
+ * the GPU (e.g. two streams at once) race and must be serialized by the
+ * caller.  -0.0 and +0.0 count as equal (the lower index wins).  A launch
+ * that fails returns MK_ERR_CUDA (mk_last_cuda_error names the kernel).
+ * Runs on the calling thread's current device; asynchronous on `stream`. */
 #define MK_NOALLOC_ARGMAX_BLOCKS 1024
 #define MK_NOALLOC_ARGMAX_MAX_N (MK_NOALLOC_ARGMAX_BLOCKS * 4096)
 int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, void* stream);

@@ -55,3 +55,49 @@ def test_noalloc_argmax_rejects_sizes_beyond_its_scratch():
     x[5] = 2.5
     assert lib.mk_argmax_f32_noalloc(x.data_ptr(), 8, out.data_ptr(), None) == mk.MK_OK
     assert int(out.item()) == 3
+
+
+def _argmax(x, n, out, stream=None):
+    rc = mk.load().mk_argmax_f32_noalloc(x.data_ptr(), n, out.data_ptr(), stream)
+    assert rc == mk.MK_OK, mk.mk_strerror(rc)
+    return int(out.item())
+
+
+def test_noalloc_argmax_across_blocks_then_a_smaller_call():
+    """n = 128256 (the 1B vocabulary: 31 full blocks of 4096 logits and a
+    partial one) needs the reduction across block partials.  The maximum sits
+    in the last, partial block; an equal value planted in an earlier block must
+    win (lowest index).  A call of n = 5000 follows on the same stream, with
+    the larger call's partials still in the shared scratch: it must read only
+    its own two."""
+    import torch
+
+    n = 128256
+    g = torch.Generator().manual_seed(1234)
+    x = torch.randn(n, generator=g, dtype=torch.float32).cuda()
+    out = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+    x[127000] = 9.0                     # last block only: it must win
+    assert _argmax(x, n, out) == 127000 == int(np.argmax(x.cpu().numpy()))
+    x[70000] = 9.0                      # an equal value in an earlier block: the lower index wins
+    assert _argmax(x, n, out) == 70000 == int(np.argmax(x.cpu().numpy()))
+    small = x[:5000].clone()
+    small[4500] = 7.5                   # in the second block of the smaller call
+    assert _argmax(small, 5000, out) == 4500 == int(np.argmax(small.cpu().numpy()))
+    assert _argmax(x, n, out) == 70000  # and the large call again after it
+
+
+def test_noalloc_argmax_nonfinite_and_signed_zero():
+    """No finite logit gives -1; NaN and infinities are skipped; -0.0 and +0.0
+    are equal, so the lower index wins whichever sign comes first."""
+    import torch
+
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nan = torch.full((9000,), float("nan"), dtype=torch.float32, device="cuda")
+    assert _argmax(nan, 9000, out) == -1
+    nan[8500] = -3.0
+    nan[100] = float("inf")
+    nan[200] = float("-inf")
+    assert _argmax(nan, 9000, out) == 8500
+    for vals in ([-0.0, 0.0], [0.0, -0.0]):
+        z = torch.tensor(vals, dtype=torch.float32, device="cuda")
+        assert _argmax(z, 2, out) == 0 == int(np.argmax(z.cpu().numpy()))
