@@ -154,7 +154,8 @@ MK_HD int mk_smem_layout(MkGeom& g) {
     g.off_xres = o; o += 4 * ((g.H / g.CPG + 4) & ~3);
     g.off_xres2 = o; o += 4 * ((g.H / g.nC + 4) & ~3);
     g.off_rope = o; o += 4 * g.hd;
-    g.off_red = o; o += 4 * 2 * MK_NCT;       // double-buffered row partials
+    o = (o + 15) & ~15;                       // 16-byte loads of the tensor-core attention's q fragments
+    g.off_red = o; o += 4 * 2 * MK_NCT;       // double-buffered row partials; the q fragments during attention
     g.off_sc = o; o += 4 * 2 * (8 * MK_NCT / g.hd);   // attention (m, l) per position group and head
     g.off_misc = o; o += MK_MISC_BYTES;       // softmax state, staging, flags
     g.smem_bytes = o;

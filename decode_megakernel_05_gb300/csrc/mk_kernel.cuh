@@ -207,20 +207,31 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
 };
 static_assert(sizeof(Misc) <= MK_MISC_BYTES, "misc area");
 
+// Dynamic shared memory of the kernel; Smem names its regions.  Each region's
+// address is computed where it is used, from the offset in the kernel
+// parameters (a constant-bank operand), instead of 13 pointers held in
+// registers for the whole launch.
+extern __shared__ __align__(1024) uint8_t mk_dsmem[];
 struct Smem {
-    uint8_t* ring;
-    uint64_t* full;
-    uint64_t* empty;
-    float* xv;    // [H]
-    float* ov;    // [G*hd]
-    float* part;  // [rows][NKB] column-block partial sums of the QKV / gate-up rows
-    float* u;     // [max_nj] SiLU(gate)*up
-    float* xres;  // raw residual of this CTA's O rows (group 0 only)
-    float* xres2; // raw residual of rows split(H, nC, c)
-    float* rope;  // cos[hd/2], sin[hd/2] at this position
-    float* red;   // [2][MK_NCT]
-    float* sc;    // attention (m, l) per position group and head: [2][PPP][G]
-    Misc* misc;
+    const MkGeom* g;   // the kernel parameters' geometry
+    __device__ __forceinline__ uint8_t* ring() const { return mk_dsmem; }
+    __device__ __forceinline__ uint64_t* full() const { return reinterpret_cast<uint64_t*>(mk_dsmem + g->off_full); }
+    __device__ __forceinline__ uint64_t* empty() const { return reinterpret_cast<uint64_t*>(mk_dsmem + g->off_empty); }
+    __device__ __forceinline__ float* xv() const { return reinterpret_cast<float*>(mk_dsmem + g->off_xv); }            // [H]
+    __device__ __forceinline__ float* ov() const { return reinterpret_cast<float*>(mk_dsmem + g->off_ov); }            // [G*hd]
+    // [rows][NKB] column-block partial sums of the QKV / gate-up rows
+    __device__ __forceinline__ float* part() const { return reinterpret_cast<float*>(mk_dsmem + g->off_part); }
+    __device__ __forceinline__ float* u() const { return reinterpret_cast<float*>(mk_dsmem + g->off_u); }              // [max_nj] SiLU(gate)*up
+    // raw residual of this CTA's O rows (group 0 only)
+    __device__ __forceinline__ float* xres() const { return reinterpret_cast<float*>(mk_dsmem + g->off_xres); }
+    // raw residual of rows split(H, nC, c)
+    __device__ __forceinline__ float* xres2() const { return reinterpret_cast<float*>(mk_dsmem + g->off_xres2); }
+    // cos[hd/2], sin[hd/2] at this position
+    __device__ __forceinline__ float* rope() const { return reinterpret_cast<float*>(mk_dsmem + g->off_rope); }
+    __device__ __forceinline__ float* red() const { return reinterpret_cast<float*>(mk_dsmem + g->off_red); }          // [2][MK_NCT]
+    // attention (m, l) per position group and head: [2][PPP][G]
+    __device__ __forceinline__ float* sc() const { return reinterpret_cast<float*>(mk_dsmem + g->off_sc); }
+    __device__ __forceinline__ Misc* misc() const { return reinterpret_cast<Misc*>(mk_dsmem + g->off_misc); }
 };
 
 // Segment trace (off unless MkParams::trace is set): thread 0 of the consumers
@@ -244,8 +255,8 @@ struct Smem {
 #define MK_TRACE_CWAIT(slot_)                                                            \
     do {                                                                                  \
         if (MK_TRACE_ON && p.trace && threadIdx.x == 0) {                                                \
-            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + (slot_)] = s.misc->cwait; \
-            s.misc->cwait = 0;                                                            \
+            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1024 + (slot_)] = s.misc()->cwait; \
+            s.misc()->cwait = 0;                                                            \
         }                                                                                 \
     } while (0)
 
@@ -330,7 +341,7 @@ __device__ __forceinline__ void walk_tiles(const MkParams& p, const MkCtaPlan& p
 }
 
 __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem& s) {
-    volatile int* abort = &s.misc->abort;
+    volatile int* abort = &s.misc()->abort;
     const int ns = p.geo.ns;
     const uint32_t slot_bytes = (uint32_t)p.geo.slot;
     const uint64_t pol = l2_evict_first_policy();
@@ -348,32 +359,32 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
         // not reused before tile k + ns - lim, so the parity is unambiguous).
         // Few bytes in flight while the consumers are latency-bound keep the
         // queues short for their flag polls and activation loads.
-        const uint32_t lim = *(volatile int*)&s.misc->streaming ? lim_s : lim_l;
+        const uint32_t lim = *(volatile int*)&s.misc()->streaming ? lim_s : lim_l;
         if (lim < (uint32_t)ns && k >= lim) {
             const bool wrap = slot < lim;   // tile k - lim sits in the previous round of slots
             const uint32_t s2 = wrap ? slot + ns - lim : slot - lim, ph2 = wrap ? ph ^ 1u : ph;
-            if (!wait_mbar(p, &s.full[s2], ph2, abort)) { stop = true; return; }
+            if (!wait_mbar(p, &s.full()[s2], ph2, abort)) { stop = true; return; }
         }
-        if (!wait_mbar(p, &s.empty[slot], ph ^ 1u, abort)) { stop = true; return; }
+        if (!wait_mbar(p, &s.empty()[slot], ph ^ 1u, abort)) { stop = true; return; }
         if (tr) {
             pwait += gtimer() - tw;
             if ((k & 15u) == 0 && (k >> 4) < 64) tr[1536 + (k >> 4)] = pwait;
         }
-        s.misc->tile_bytes[slot] = bytes;
-        *(volatile int*)&s.misc->slot_tile[slot] = (int)k;
+        s.misc()->tile_bytes[slot] = bytes;
+        *(volatile int*)&s.misc()->slot_tile[slot] = (int)k;
         if (tr && k < 512) tr[2560 + k] = gtimer();   // trace: issue time of tile k
-        mbar_expect_tx(&s.full[slot], bytes);
-        bulk_g2s(s.ring + (size_t)slot * slot_bytes, src, bytes, &s.full[slot], pol);
+        mbar_expect_tx(&s.full()[slot], bytes);
+        bulk_g2s(s.ring() + (size_t)slot * slot_bytes, src, bytes, &s.full()[slot], pol);
         ++k;
         if (++slot == (uint32_t)ns) { slot = 0; ph ^= 1u; }
-        *(volatile unsigned long long*)&s.misc->copy_bytes += bytes;
+        *(volatile unsigned long long*)&s.misc()->copy_bytes += bytes;
     });
     if (tr) tr[1535] = gtimer();
     // Drain: wait for the copies still in flight before this warp leaves.
     const uint32_t first = k > (uint32_t)ns ? k - ns : 0u;
     for (uint32_t q = first; q < k; ++q) {
         uint64_t t0 = gtimer();
-        while (!mbar_try_wait(&s.full[q % ns], (q / ns) & 1u)) {
+        while (!mbar_try_wait(&s.full()[q % ns], (q / ns) & 1u)) {
             if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) {
                 atomicOr(p.status, MK_ST_TIMEOUT | MK_ST_ABORT);
                 break;
@@ -394,7 +405,7 @@ __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem
 __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const Smem& s) {
     if (p.l2_pf_bytes <= 0) return;
     const int lane = threadIdx.x & 31;
-    volatile int* abort = &s.misc->abort;
+    volatile int* abort = &s.misc()->abort;
     const unsigned long long ahead = (unsigned long long)p.l2_pf_bytes;
     const unsigned long long lead = (unsigned long long)p.pf_lead_bytes;
     const bool two = p.pf_depth > 1;
@@ -408,8 +419,8 @@ __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const 
         uint64_t t0 = 0;
         const uint32_t kt = kw++;
         for (;;) {
-            const unsigned long long cb = *(volatile unsigned long long*)&s.misc->copy_bytes;
-            const bool streaming = *(volatile int*)&s.misc->streaming;
+            const unsigned long long cb = *(volatile unsigned long long*)&s.misc()->copy_bytes;
+            const bool streaming = *(volatile int*)&s.misc()->streaming;
             if (issued + bytes <= cb + lead) break;   // copied, or the ring fetches it next
             if (!streaming && issued <= cb + lead + ahead) {
                 if (tr && kt < 256) tr[1792 + kt] = gtimer();   // trace: when tile kt was warmed
@@ -440,7 +451,7 @@ __device__ void producer_prefetch(const MkParams& p, const MkCtaPlan& pl, const 
     asm volatile("xor.b32 %0, %0, %1;" : "+r"(sink) : "r"(prev));
     // a real use of every loaded word: without it the compiler may drop the
     // xors and with them the loads (or the waits for them)
-    if (lane == 0) *(volatile uint32_t*)&s.misc->pf_sink = sink;
+    if (lane == 0) *(volatile uint32_t*)&s.misc()->pf_sink = sink;
 }
 
 // ------------------------------------------------------------------ consumer pieces
@@ -474,35 +485,35 @@ __device__ __forceinline__ bool take_tile(const MkParams& p, const Smem& s, Ring
     bool ok = true;
     if ((threadIdx.x & 31) == 0) {
         const uint64_t tw = (MK_TRACE_ON && p.trace && p.trace_detail == 1) ? gtimer() : 0;
-        ok = !s.misc->abort;
-        if (ok && *(volatile int*)&s.misc->slot_tile[slot] != (int)rg.k) {
+        ok = !s.misc()->abort;
+        if (ok && *(volatile int*)&s.misc()->slot_tile[slot] != (int)rg.k) {
             const uint64_t t0 = gtimer();
-            while (*(volatile int*)&s.misc->slot_tile[slot] != (int)rg.k) {
-                if (s.misc->abort) { ok = false; break; }
+            while (*(volatile int*)&s.misc()->slot_tile[slot] != (int)rg.k) {
+                if (s.misc()->abort) { ok = false; break; }
                 if (gtimer() - t0 > (uint64_t)p.wait_limit_ns) {
                     atomicOr(p.status, MK_ST_TIMEOUT | MK_ST_ABORT);
-                    s.misc->abort = 1;
+                    s.misc()->abort = 1;
                     ok = false;
                     break;
                 }
                 __nanosleep(64);
             }
         }
-        ok = ok && wait_mbar(p, &s.full[slot], ph, &s.misc->abort);
+        ok = ok && wait_mbar(p, &s.full()[slot], ph, &s.misc()->abort);
         if (tw) {
             const uint64_t t1 = gtimer();
-            if (threadIdx.x == 0) s.misc->cwait += t1 - tw;
+            if (threadIdx.x == 0) s.misc()->cwait += t1 - tw;
             rg.t_take += t1 - tw;
             rg.t_mark = t1;
         }
-        if (ok && s.misc->tile_bytes[slot] != expect_bytes) {
+        if (ok && s.misc()->tile_bytes[slot] != expect_bytes) {
             atomicOr(p.status, MK_ST_SCHEDULE | MK_ST_ABORT);
-            s.misc->abort = 1;
+            s.misc()->abort = 1;
             ok = false;
         }
     }
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    tile = s.ring + (size_t)slot * p.geo.slot;
+    tile = s.ring() + (size_t)slot * p.geo.slot;
     if (MK_TRACE_ON && p.trace && p.trace_detail == 1 && (threadIdx.x & 31) == 0 && rg.k < 512)   // trace: a reader got tile k
         p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3072 + rg.k] = gtimer();
     return ok;
@@ -512,7 +523,7 @@ __device__ __forceinline__ void release_tile(const MkParams& p, const Smem& s, R
     const uint64_t t2 = (MK_TRACE_ON && p.trace && p.trace_detail == 1 && (threadIdx.x & 31) == 0) ? gtimer() : 0;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
-        mbar_arrive(&s.empty[rg.slot()], weight);
+        mbar_arrive(&s.empty()[rg.slot()], weight);
         if (t2 && rg.k < 512) p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 3584 + rg.k] = gtimer();
         if (t2) {
             rg.t_comp += t2 - rg.t_mark;
@@ -532,13 +543,13 @@ __device__ __forceinline__ bool take_landed(const MkParams& p, const Smem& s, Ri
     const uint32_t slot = rg.slot(), ph = rg.ph();
     bool fast = false;
     if (!(MK_TRACE_ON && p.trace && p.trace_detail == 1)) {
-        const int claim = *(volatile int*)&s.misc->slot_tile[slot];
-        const int abt = *(volatile int*)&s.misc->abort;
-        fast = claim == (int)rg.k && !abt && mbar_test_wait(&s.full[slot], ph) &&
-               s.misc->tile_bytes[slot] == expect_bytes;
+        const int claim = *(volatile int*)&s.misc()->slot_tile[slot];
+        const int abt = *(volatile int*)&s.misc()->abort;
+        fast = claim == (int)rg.k && !abt && mbar_test_wait(&s.full()[slot], ph) &&
+               s.misc()->tile_bytes[slot] == expect_bytes;
     }
     if (__all_sync(0xFFFFFFFFu, fast)) {
-        tile = s.ring + (size_t)slot * p.geo.slot;
+        tile = s.ring() + (size_t)slot * p.geo.slot;
         return true;
     }
     return take_tile(p, s, rg, expect_bytes, tile);
@@ -819,7 +830,7 @@ __device__ __forceinline__ float wide_row(const float* part, int R) {
 }
 
 // RMSNorm of x (fp32 global, or the bf16 embedding row when xb != nullptr) into
-// s.xv (split order, for the GEMV), with gain g (fp32).  The raw values of rows
+// s.xv() (split order, for the GEMV), with gain g (fp32).  The raw values of rows
 // [keep0, keep0 + nkeep) are also kept in `keep` (the residual this CTA adds
 // later).  All loads of a thread (x and gains) are issued together, so the
 // norm costs one L2 round trip.  Returns the uniform abort flag.
@@ -843,16 +854,16 @@ __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, 
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-    if ((t & 31) == 0) s.red[t >> 5] = ss;
+    if ((t & 31) == 0) s.red()[t >> 5] = ss;
     bool ab = bar_or(abort_in);
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < MK_NCW; ++w) tot += s.red[w];
+    for (int w = 0; w < MK_NCW; ++w) tot += s.red()[w];
     const float inv = rsqrtf(tot / (float)H + p.eps);
 #pragma unroll
     for (int k = 0; k < NPT; ++k) {
         const int i = t + k * MK_NCT;
-        if (i < H) s.xv[xsplit(i, H)] = xr[k] * inv * gv[k];   // split order for the GEMV
+        if (i < H) s.xv()[xsplit(i, H)] = xr[k] * inv * gv[k];   // split order for the GEMV
     }
     return bar_or(ab);
 }
@@ -895,14 +906,25 @@ struct Attn {
     // reduced over the DC lanes), rescales each head's running (m, l, acc)
     // once to the chunk's maximum and folds each position in with its exp2
     // weight.  q < nr from the ring tiles kt/vt, q == nr from the staged
-    // current row (st: K, then V).  No barrier.
+    // current row (st: K, then V).  No barrier.  The thread's 8 q dims per
+    // head (pre-scaled) are read from shared memory at qsa for every round of
+    // positions instead of being held in registers across the block loop:
+    // with them held, the kernel spilled under its 128-register budget.
     static __device__ __forceinline__ void online(const uint8_t* kt, const uint8_t* vt, int nr, const uint8_t* st,
-                                                  int n, int pos0, const float (&qr)[HPL][8], float (&m)[HPL],
+                                                  int n, int pos0, uint32_t qsa, float (&m)[HPL],
                                                   float (&lsum)[HPL], float2 (&a2)[HPL][4]) {
         constexpr int CH = 4;                          // positions per thread and chunk
         constexpr bool SWZ = mk_attn_tc(HD, G);        // ring rows chunk-permuted by position (pos0 + q)
         const int t = threadIdx.x, pp = t / TPP, dc = t % DC;
         for (int q0 = 0; q0 < n; q0 += CH * PPP) {     // uniform trip count across the warp
+            float qr[HPL][8];
+#pragma unroll
+            for (int j = 0; j < HPL; ++j) {   // volatile: re-read every round, not hoisted into registers
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(qr[j][0]), "=f"(qr[j][1]), "=f"(qr[j][2]), "=f"(qr[j][3]) : "r"(qsa + 4u * j * HD));
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(qr[j][4]), "=f"(qr[j][5]), "=f"(qr[j][6]), "=f"(qr[j][7]) : "r"(qsa + 4u * j * HD + 16u));
+            }
             float sc[CH][HPL];
             uint4 vw[CH];
 #pragma unroll
@@ -1000,10 +1022,10 @@ struct Attn {
 #pragma unroll
         for (int j = 0; j < HPL; ++j) {
             const int h = hg * HPL + j;
-            float4* sp = reinterpret_cast<float4*>(s.xv + grp * (G * HD) + h * HD + dc * 8);
+            float4* sp = reinterpret_cast<float4*>(s.xv() + grp * (G * HD) + h * HD + dc * 8);
             sp[0] = make_float4(a2[j][0].x, a2[j][0].y, a2[j][1].x, a2[j][1].y);
             sp[1] = make_float4(a2[j][2].x, a2[j][2].y, a2[j][3].x, a2[j][3].y);
-            if (dc == 0) { s.sc[grp * G + h] = m[j]; s.sc[NMG * G + grp * G + h] = lsum[j]; }
+            if (dc == 0) { s.sc()[grp * G + h] = m[j]; s.sc()[NMG * G + grp * G + h] = lsum[j]; }
         }
     }
 };
@@ -1040,9 +1062,12 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
 }
 // D = A B + C for one m16n8k16 tile whose A rows 8-15 are zero: only the
 // accumulator of rows 0-7 (c0, c1 of each lane) is carried.
+// volatile: kept in program order with the matrix loads around it, so a
+// product's operands are loaded just before it (hoisted loads of later
+// operands had made the kernel spill under its 128-register budget).
 __device__ __forceinline__ void mma_rows8(float& c0, float& c1, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
     float d2, d3;
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%10, %11, %12, %13};"
         : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
         : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(0.f), "f"(0.f));
@@ -1060,14 +1085,25 @@ __device__ __forceinline__ uint32_t split_bf2(float x, float y, bool lo) {
     return pack_bf2(x - __uint_as_float(h << 16), y - __uint_as_float(h & 0xFFFF0000u));
 }
 
+// Where the q poll leaves the score products' A fragments for the tensor-core
+// attention: fragment word f (= 2 * k step + half, 0 .. 2*HD/16 - 1) of lane L
+// at word (f / 4) * 128 + 4 * L + f % 4 of s.red() (free during the attention),
+// so a lane reads its words back with 16-byte loads.  Lane L holds row L / 4 of
+// [q_hi; q_lo]: head (L / 4) mod 4, the bf16 high parts for L < 16 and the
+// bf16 of the remainders for L >= 16, dims 16 ks + 8 half + 2 (L mod 4) (+1).
+__device__ __forceinline__ int qfrag_word(int f, int lane) { return (f >> 2) * 128 + 4 * lane + (f & 3); }
+
 // The block loop of the tensor-core attention (q of the group's heads already
-// in qs, unscaled).  Positions [ka, ke) come from the ring in blocks of KB
-// (K tile then V tile, rows chunk-permuted by position); the current position
-// (staged, plain row order) follows the last block when has_cur.  Returns the
-// abort flag (not yet uniform); the warps' states are parked for the caller.
+// split into A fragments in qf, pre-scaled).  Positions [ka, ke) come from the
+// ring in blocks of KB (K tile then V tile, rows chunk-permuted by position);
+// the current position (staged, plain row order) follows the last block when
+// has_cur.  Returns the abort flag (not yet uniform); the warps' states are
+// parked for the caller.  The fragments are read back from shared memory for
+// every 16-position chunk rather than held in registers across the loop: held,
+// they made the kernel spill under its 128-register budget.
 template <int HD, int G>
 __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
-                                               bool has_cur, float qscale, bool ab, const float* qs) {
+                                               bool has_cur, bool ab, const uint32_t* qf) {
     static_assert(mk_attn_tc(HD, G), "tensor-core attention: 4 heads of 64 dims per KV group");
     constexpr int NKS = HD / 16;         // 16-dim k steps of a score tile
     constexpr int ND = HD / 8;           // 8-dim tiles of O
@@ -1075,32 +1111,21 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
     static_assert(NMG == MK_NCW, "one parked group per consumer warp");
     const MkGeom& g = p.geo;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    static_assert(NKS == 4, "two 16-byte fragment loads per lane");
     const bool lo = lane >= 16;          // this lane's rows hold the remainder parts (4-7)
     const int qd = 2 * (lane & 3);       // first of this lane's two k (or n) indices in a tile
-    // A fragments of [q_hi; q_lo] (pre-scaled by log2(e)/sqrt(hd)) for the
-    // 16-dim k steps: row lane/4 (head (lane/4) mod 4), dims 16ks + qd (+8)
-    uint32_t qa[NKS][2];
-    {
-        const float* qh = qs + ((lane >> 2) & 3) * HD;
-#pragma unroll
-        for (int ks = 0; ks < NKS; ++ks)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int d = 16 * ks + 8 * hf + qd;
-                qa[ks][hf] = split_bf2(qh[d] * qscale, qh[d + 1] * qscale, lo);
-            }
-    }
+    const uint32_t qfa = smem_u32(qf + qfrag_word(0, lane));
     float o[ND][2];
 #pragma unroll
     for (int j = 0; j < ND; ++j) o[j][0] = o[j][1] = 0.f;
     float m = -INFINITY, lsum = 0.f;
     MK_TRACE_D(l, 1);
-    const uint32_t zaddr = smem_u32(&s.misc->zrow);
-    const uint32_t staddr = smem_u32(s.misc->stage);
+    const uint32_t zaddr = smem_u32(&s.misc()->zrow);
+    const uint32_t staddr = smem_u32(s.misc()->stage);
     const int nring = ke > ka ? ke - ka : 0;
     const int nblk = (nring + g.KB - 1) / g.KB;
     const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
-    if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 1;
+    if (t == 0 && nblk > 1) *(volatile int*)&s.misc()->streaming = 1;
     int cbase = 0;                       // chunks of the earlier blocks (warp w takes chunk indices = w mod NCW)
     for (int b = 0; b < nbt && !ab; ++b) {
         const int q0 = ka + b * g.KB;
@@ -1133,6 +1158,12 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
                     const int i = c0 + 8 * tt + (lane & 7);
+                    // A fragments of [q_hi; q_lo] for the 16-dim k steps (volatile: re-read per tile)
+                    uint32_t qa[NKS][2];
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1]) : "r"(qfa));
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(qa[2][0]), "=r"(qa[2][1]), "=r"(qa[3][0]), "=r"(qa[3][1]) : "r"(qfa + 512u));
                     uint32_t kb[NKS / 2][4];   // 8x8 matrices of chunks 4x .. 4x+3: two k steps each
 #pragma unroll
                     for (int x = 0; x < NKS / 2; ++x) ldsm_x4(kb[x], row(ka_, 0u, i, 4 * x + (lane >> 3)));
@@ -1175,7 +1206,7 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
         if (nr > 0) { release_tile(p, s, ring); release_tile(p, s, ring); }
         if (!ok) ab = true;     // made uniform by the caller's barrier
     }
-    if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 0;
+    if (t == 0 && nblk > 1) *(volatile int*)&s.misc()->streaming = 0;
     MK_TRACE_D(l, 2);
     // the warp's state: l summed over the quad, O rows h and h+4 added; park
     // (m, l) per head in sc and O in xv[warp] like the lane-parallel version
@@ -1188,10 +1219,10 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
     }
     if (!ab && !lo) {
         const int h = lane >> 2;
-        float* xp = s.xv + w * (G * HD) + h * HD + qd;
+        float* xp = s.xv() + w * (G * HD) + h * HD + qd;
 #pragma unroll
         for (int j = 0; j < ND; ++j) *reinterpret_cast<float2*>(xp + 8 * j) = make_float2(o[j][0], o[j][1]);
-        if ((lane & 3) == 0) { s.sc[w * G + h] = m; s.sc[NMG * G + w * G + h] = lsum; }
+        if ((lane & 3) == 0) { s.sc()[w * G + h] = m; s.sc()[NMG * G + w * G + h] = lsum; }
     }
     return ab;
 }
@@ -1205,7 +1236,7 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
                                          bool has_cur, float qscale, bool ab, bool late) {
     using A = Attn<HD, G, HPL>;
     const MkGeom& g = p.geo;
-    const MkCtaPlan& pl = s.misc->plan;
+    const MkCtaPlan& pl = s.misc()->plan;
     const int t = threadIdx.x;
     const int hg_ = (t % A::TPP) / A::DC, dc_ = t % A::DC;
     // q of the group's G heads (G*HD tagged words): every 16-byte chunk is
@@ -1213,20 +1244,34 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
     // warp instruction reads four whole 128-byte lines and the CTA reads each
     // line once (had every thread read the q values it needs, the 12 position
     // groups would read the same words, ~48x the requests on the same L2
-    // lines, in all CTAs of the group at once).  They meet in `ov`, free until
-    // the combine.
+    // lines, in all CTAs of the group at once).  The poller scales its two
+    // values by log2(e)/sqrt(hd) and leaves them in `ov` (free until the
+    // combine) for the lane-parallel build, or, for the tensor-core build,
+    // split into bf16 high and low parts in the A-fragment words they belong
+    // to (qfrag_word).
     constexpr int NQC = G * HD / 2;
-    float* qs = s.ov;
+    float* qs = s.ov();
+    uint32_t* qf = reinterpret_cast<uint32_t*>(s.red());
     if (!ab) {
-        const uint32_t tag = s.misc->tag;
+        const uint32_t tag = s.misc()->tag;
         const uint64_t* qsrc = p.qll + (size_t)l * g.qh * HD + (size_t)pl.g * G * HD;
         for (int c = t; c < NQC && !late; c += MK_NCT) {
             uint64_t t0 = 0;
             for (;;) {
                 const ulonglong2 w = ld_ll2(qsrc + 2 * c);
                 if (ll_ok(w, tag)) {
-                    *reinterpret_cast<float2*>(qs + 2 * c) =
-                        make_float2(__uint_as_float((uint32_t)w.x), __uint_as_float((uint32_t)w.y));
+                    const float q0 = __uint_as_float((uint32_t)w.x) * qscale;
+                    const float q1 = __uint_as_float((uint32_t)w.y) * qscale;
+                    if constexpr (TC) {
+                        // dims d, d+1 of head h: fragment word 2 (d / 16) + (d / 8) % 2 of
+                        // lane 4h + (d % 8) / 2 (high part) and of lane 16 + 4h + (d % 8) / 2
+                        const int h = (2 * c) / HD, d = (2 * c) % HD;
+                        const int f = 2 * (d >> 4) + ((d >> 3) & 1), ln = 4 * h + ((d & 7) >> 1);
+                        qf[qfrag_word(f, ln)] = split_bf2(q0, q1, false);
+                        qf[qfrag_word(f, ln + 16)] = split_bf2(q0, q1, true);
+                    } else {
+                        *reinterpret_cast<float2*>(qs + 2 * c) = make_float2(q0, q1);
+                    }
                     break;
                 }
                 if (!ll_backoff(p, t0)) { late = true; break; }
@@ -1235,17 +1280,8 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
     }
     ab = bar_or(ab || late);
     MK_TRACE_D(l, 0);   // q in shared memory
-    if constexpr (TC) return attn_tc_blocks<HD, G>(p, s, ring, l, ka, ke, has_cur, qscale, ab, qs);
-    float qr[HPL][8];
-    if (!ab) {
-#pragma unroll
-        for (int j = 0; j < HPL; ++j) {
-            const float4* q4 = reinterpret_cast<const float4*>(qs + (hg_ * HPL + j) * HD + dc_ * 8);
-            const float4 a = q4[0], b = q4[1];
-            qr[j][0] = a.x * qscale; qr[j][1] = a.y * qscale; qr[j][2] = a.z * qscale; qr[j][3] = a.w * qscale;
-            qr[j][4] = b.x * qscale; qr[j][5] = b.y * qscale; qr[j][6] = b.z * qscale; qr[j][7] = b.w * qscale;
-        }
-    }
+    if constexpr (TC) return attn_tc_blocks<HD, G>(p, s, ring, l, ka, ke, has_cur, ab, qf);
+    const uint32_t qsa = smem_u32(qs + (hg_ * HPL) * HD + dc_ * 8);   // this thread's q dims (pre-scaled)
     float m_[HPL], l_[HPL];
     float2 acc[HPL][4];
 #pragma unroll
@@ -1259,10 +1295,10 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
     const int nring = ke > ka ? ke - ka : 0;
     const int nblk = (nring + g.KB - 1) / g.KB;
     const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
-    const uint8_t* st = reinterpret_cast<const uint8_t*>(s.misc->stage);
+    const uint8_t* st = reinterpret_cast<const uint8_t*>(s.misc()->stage);
     // several K/V blocks (long contexts) stream like weights: lift the
     // producer's latency-phase in-flight limit for the block loop
-    if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 1;
+    if (t == 0 && nblk > 1) *(volatile int*)&s.misc()->streaming = 1;
     for (int b = 0; b < nbt && !ab; ++b) {
         const int q0 = ka + b * g.KB;
         const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
@@ -1275,12 +1311,12 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
             ok = take_tile(p, s, ring, (uint32_t)(nr * HD * 2), kt) && take_tile(p, s, rv, (uint32_t)(nr * HD * 2), vt);
         }
         if (b == 0) MK_TRACE_D(l, 5);   // first block's K and V taken
-        if (ok) A::online(kt, vt, nr, st, n, q0, qr, m_, l_, acc);
+        if (ok) A::online(kt, vt, nr, st, n, q0, qsa, m_, l_, acc);
         if (b == 0) MK_TRACE_D(l, 6);   // first block's softmax done
         if (nr > 0) { release_tile(p, s, ring); release_tile(p, s, ring); }
         if (!ok) ab = true;     // made uniform by the barrier below
     }
-    if (t == 0 && nblk > 1) *(volatile int*)&s.misc->streaming = 0;
+    if (t == 0 && nblk > 1) *(volatile int*)&s.misc()->streaming = 0;
     MK_TRACE_D(l, 2);   // softmax over the blocks done
     // merge the position groups: first those sharing a warp (shuffles), then
     // the warps' groups park (m, l) per head and acc in smem (xv, free between
@@ -1329,60 +1365,47 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     constexpr int LPRO = KO >= 32 * 4 ? KO / 32 : 4;   // short rows: 4 chunks per lane
     constexpr int MO = KO / (8 * LPRO);
     static_assert(LPRO <= 32 && 32 % LPRO == 0 && MO * 8 * LPRO == KO, "O-proj row mapping");
-    extern __shared__ __align__(1024) uint8_t smem[];
     const MkGeom& g = p.geo;
     Smem s;
-    s.ring = smem;
-    s.full = reinterpret_cast<uint64_t*>(smem + g.off_full);
-    s.empty = reinterpret_cast<uint64_t*>(smem + g.off_empty);
-    s.xv = reinterpret_cast<float*>(smem + g.off_xv);
-    s.ov = reinterpret_cast<float*>(smem + g.off_ov);
-    s.part = reinterpret_cast<float*>(smem + g.off_part);
-    s.u = reinterpret_cast<float*>(smem + g.off_u);
-    s.xres = reinterpret_cast<float*>(smem + g.off_xres);
-    s.xres2 = reinterpret_cast<float*>(smem + g.off_xres2);
-    s.rope = reinterpret_cast<float*>(smem + g.off_rope);
-    s.red = reinterpret_cast<float*>(smem + g.off_red);
-    s.sc = reinterpret_cast<float*>(smem + g.off_sc);
-    s.misc = reinterpret_cast<Misc*>(smem + g.off_misc);
+    s.g = &p.geo;
 
     const int t = threadIdx.x;
     const int c = blockIdx.x;
 
     if (t == 0) {
         for (int i = 0; i < g.ns; ++i) {
-            mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], MK_NCW);
-            s.misc->slot_tile[i] = -1;
+            mbar_init(&s.full()[i], 1);
+            mbar_init(&s.empty()[i], MK_NCW);
+            s.misc()->slot_tile[i] = -1;
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        s.misc->abort = 0;
-        s.misc->streaming = 0;
-        s.misc->copy_bytes = 0;
-        s.misc->cwait = 0;
-        s.misc->is_last = 0;
+        s.misc()->abort = 0;
+        s.misc()->streaming = 0;
+        s.misc()->copy_bytes = 0;
+        s.misc()->cwait = 0;
+        s.misc()->is_last = 0;
         int tok = p.token_ptr ? *p.token_ptr : p.token;
         if (tok < 0 || tok >= g.V) {
             if (c == 0) atomicOr(p.status, MK_ST_BADTOKEN);
             tok = 0;
         }
-        s.misc->token = tok;
-        s.misc->zrow = make_uint4(0u, 0u, 0u, 0u);
-        s.misc->plan = p.plans[c];
+        s.misc()->token = tok;
+        s.misc()->zrow = make_uint4(0u, 0u, 0u, 0u);
+        s.misc()->plan = p.plans[c];
         {
             constexpr int KO = G * HD, LPRO = KO >= 32 * 4 ? KO / 32 : 4;
-            gemv_cfg(s.misc->ocfg, s.misc->plan.norows, g.TRo, 32 / LPRO);
-            gemv_cfg(s.misc->lmcfg, s.misc->plan.nv, g.TRh, 1);
+            gemv_cfg(s.misc()->ocfg, s.misc()->plan.norows, g.TRo, 32 / LPRO);
+            gemv_cfg(s.misc()->lmcfg, s.misc()->plan.nv, g.TRh, 1);
         }
         {
             const uint32_t sq = *(volatile uint32_t*)p.seq;
-            s.misc->par = (int)(sq & 1u);
-            s.misc->tag = sq + 1u;
+            s.misc()->par = (int)(sq & 1u);
+            s.misc()->tag = sq + 1u;
         }
-        for (int h = 0; h < 8; ++h) s.misc->alpha[h] = 0.f;
+        for (int h = 0; h < 8; ++h) s.misc()->alpha[h] = 0.f;
     }
     __syncthreads();
-    const MkCtaPlan& pl = s.misc->plan;
+    const MkCtaPlan& pl = s.misc()->plan;
 
     const int warp = t >> 5;
     if (warp == MK_PRODUCER_WARP) {
@@ -1396,8 +1419,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
     // ======================= consumers (MK_NCT threads) =======================
     const int H = g.H, L = g.L, hd2 = HD / 2;
-    const int par = s.misc->par, token = s.misc->token;
-    // the launch tag of the tagged words is read from s.misc->tag where used
+    const int par = s.misc()->par, token = s.misc()->token;
+    // the launch tag of the tagged words is read from s.misc()->tag where used
     // (the layer loop runs at the register limit)
     const size_t state = (size_t)H;
     float* xa = p.xacc + (size_t)par * 2 * L * state;              // this launch's residual states
@@ -1414,8 +1437,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     const bool has_cur = (pl.i == g.CPG - 1);
     const int dr0 = (int)mk_split(H, g.nC, c), dr1 = (int)mk_split(H, g.nC, c + 1);   // rows whose residual I add
     for (int d = t; d < hd2; d += MK_NCT) {       // RoPE angles of this position
-        s.rope[d] = p.rope_cos[(size_t)p.pos * hd2 + d];
-        s.rope[hd2 + d] = p.rope_sin[(size_t)p.pos * hd2 + d];
+        s.rope()[d] = p.rope_cos[(size_t)p.pos * hd2 + d];
+        s.rope()[hd2 + d] = p.rope_sin[(size_t)p.pos * hd2 + d];
     }
     const float qscale = rsqrtf((float)HD) * 1.4426950408889634f;  // 1/sqrt(hd) * log2(e)
 
@@ -1427,18 +1450,18 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment A: RMSNorm + QKV GEMV + RoPE + K/V append
         MK_TRACE(16 * l + 0);
         const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
-        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres, pl.orow0,
+        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres(), pl.orow0,
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
-        ab = gemv_fifo<MH>(p, s, ring, s.xv, 2 * pl.npairs, g.TRh, ab, s.part);
+        ab = gemv_fifo<MH>(p, s, ring, s.xv(), 2 * pl.npairs, g.TRh, ab, s.part());
         MK_TRACE(16 * l + 2);
         MK_TRACE_CWAIT(8 * l + 0);
         if (!ab) {
             for (int j = t; j < pl.npairs; j += MK_NCT) {
                 const int pair = pl.pair0 + j, slot = pair / hd2, d = pair % hd2;
-                float a = wide_row<MH>(s.part, 2 * j), b = wide_row<MH>(s.part, 2 * j + 1);
+                float a = wide_row<MH>(s.part(), 2 * j), b = wide_row<MH>(s.part(), 2 * j + 1);
                 if (slot <= G) {
-                    const float cs = s.rope[d], sn = s.rope[hd2 + d];
+                    const float cs = s.rope()[d], sn = s.rope()[hd2 + d];
                     const float a2 = a * cs - b * sn, b2 = b * cs + a * sn;
                     a = a2; b = b2;
                 }
@@ -1447,14 +1470,14 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 const bool pub = !(p.dbg_skip_sync == 4 * l + 0 && p.dbg_skip_cta == c);
                 if (slot < G) {
                     uint64_t* q = p.qll + (size_t)l * g.qh * HD + (size_t)(pl.g * G + slot) * HD;
-                    if (pub) { st_ll(q + d, ll_pack(a, s.misc->tag)); st_ll(q + d + hd2, ll_pack(b, s.misc->tag)); }
+                    if (pub) { st_ll(q + d, ll_pack(a, s.misc()->tag)); st_ll(q + d + hd2, ll_pack(b, s.misc()->tag)); }
                 } else {
                     uint16_t* dst = (slot == G ? p.kc : p.vc) + ((size_t)l * g.kvh + pl.g) * g.max_seq * HD;
                     const uint16_t ab16 = f2bf(a), bb16 = f2bf(b);
                     dst[mk_kv_index(p.pos, d, HD, mk_attn_tc(HD, G))] = ab16;
                     dst[mk_kv_index(p.pos, d + hd2, HD, mk_attn_tc(HD, G))] = bb16;
                     uint64_t* kv = p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (slot - G)) * HD;
-                    if (pub) { st_ll(kv + d, ll_pack(bf2f(ab16), s.misc->tag)); st_ll(kv + d + hd2, ll_pack(bf2f(bb16), s.misc->tag)); }
+                    if (pub) { st_ll(kv + d, ll_pack(bf2f(ab16), s.misc()->tag)); st_ll(kv + d + hd2, ll_pack(bf2f(bb16), s.misc()->tag)); }
                 }
             }
         }
@@ -1470,13 +1493,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             if (!ab && has_cur && t < HD / 4) {
                 float kv[8];
                 late = !ll_read8(p, p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (t < HD / 8 ? 0 : 1)) * HD +
-                                        (t % (HD / 8)) * 8, s.misc->tag, kv);
+                                        (t % (HD / 8)) * 8, s.misc()->tag, kv);
                 uint4 w;
                 w.x = (uint32_t)f2bf(kv[0]) | ((uint32_t)f2bf(kv[1]) << 16);
                 w.y = (uint32_t)f2bf(kv[2]) | ((uint32_t)f2bf(kv[3]) << 16);
                 w.z = (uint32_t)f2bf(kv[4]) | ((uint32_t)f2bf(kv[5]) << 16);
                 w.w = (uint32_t)f2bf(kv[6]) | ((uint32_t)f2bf(kv[7]) << 16);
-                s.misc->stage[t] = w;
+                s.misc()->stage[t] = w;
             }
             // Blocks of up to KB past positions from the ring (the K tile and
             // the V tile of a block are held together); the last CTA of the
@@ -1496,18 +1519,18 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 const int h = i / HD;
                 float M = -INFINITY;
 #pragma unroll
-                for (int q = 0; q < PPP; ++q) M = fmaxf(M, s.sc[q * G + h]);
+                for (int q = 0; q < PPP; ++q) M = fmaxf(M, s.sc()[q * G + h]);
                 float a = 0.f, L = 0.f;
                 if (M != -INFINITY) {   // no position at all: an empty partial (m = -inf, l = 0)
 #pragma unroll
                     for (int q = 0; q < PPP; ++q) {
-                        const float wq = exp2f(s.sc[q * G + h] - M);
-                        a = fmaf(wq, s.xv[q * (G * HD) + i], a);
-                        L = fmaf(wq, s.sc[PPP * G + q * G + h], L);
+                        const float wq = exp2f(s.sc()[q * G + h] - M);
+                        a = fmaf(wq, s.xv()[q * (G * HD) + i], a);
+                        L = fmaf(wq, s.sc()[PPP * G + q * G + h], L);
                     }
                 }
-                st_ll(dst + i, ll_pack(a, s.misc->tag));
-                if (i % HD == 0) st_ll2(dst + G * HD + 2 * h, ll_pack(M, s.misc->tag), ll_pack(L, s.misc->tag));
+                st_ll(dst + i, ll_pack(a, s.misc()->tag));
+                if (i % HD == 0) st_ll2(dst + G * HD + 2 * h, ll_pack(M, s.misc()->tag), ll_pack(L, s.misc()->tag));
             }
         }
         ab = bar_or(ab);
@@ -1543,7 +1566,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     if (o4 < NO4 && j < g.CPG) {
                         const uint64_t* w = pg + (size_t)j * PSTR + o4 * 4;
                         const ulonglong2 a = ld_ll2(w), b = ld_ll2(w + 2);
-                        ok = ok & ll_ok(a, s.misc->tag) & ll_ok(b, s.misc->tag);
+                        ok = ok & ll_ok(a, s.misc()->tag) & ll_ok(b, s.misc()->tag);
                         v[k] = make_float4(__uint_as_float((uint32_t)a.x), __uint_as_float((uint32_t)a.y),
                                            __uint_as_float((uint32_t)b.x), __uint_as_float((uint32_t)b.y));
                     } else {
@@ -1559,16 +1582,16 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     if (!ll_backoff(p, t0)) return false;
                 }
             };
-            float* cw = s.red;                       // [CPG*G] maxima (red is free here)
+            float* cw = s.red();                       // [CPG*G] maxima (red is free here)
             {   // first batch and this thread's (m, l) words in one poll: one round trip
                 uint64_t t0 = 0;
                 for (;;) {
                     bool ok = load_batch_once(t / CT, 0);
                     for (int i = t; i < g.CPG * G; i += MK_NCT) {
                         const ulonglong2 w = ld_ll2(pg + (size_t)(i / G) * PSTR + G * HD + 2 * (i % G));
-                        ok = ok & ll_ok(w, s.misc->tag);
+                        ok = ok & ll_ok(w, s.misc()->tag);
                         cw[i] = __uint_as_float((uint32_t)w.x);
-                        s.misc->cl[i] = __uint_as_float((uint32_t)w.y);
+                        s.misc()->cl[i] = __uint_as_float((uint32_t)w.y);
                     }
                     if (ok) break;
                     if (!ll_backoff(p, t0)) { late = true; break; }
@@ -1587,12 +1610,12 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 for (int j = ln; j < g.CPG; j += 32) {
                     const float mj = cw[j * G + hh];
                     const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - mx);
-                    den = fmaf(wj, s.misc->cl[j * G + hh], den);
-                    s.misc->cwt[j * G + hh] = wj;
+                    den = fmaf(wj, s.misc()->cl[j * G + hh], den);
+                    s.misc()->cwt[j * G + hh] = wj;
                 }
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
-                if (ln == 0) s.misc->alpha[hh] = 1.f / den;
+                if (ln == 0) s.misc()->alpha[hh] = 1.f / den;
             }
             bar_or(false);
 #pragma unroll 1
@@ -1608,7 +1631,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     for (int k = 0; k < CB; ++k) {
                         const int j = cl_ + (k0 + k) * CT;
                         if (o4 < NO4 && j < g.CPG) {
-                            const float wt = s.misc->cwt[j * G + h];
+                            const float wt = s.misc()->cwt[j * G + h];
                             a.x = fmaf(wt, v[k].x, a.x); a.y = fmaf(wt, v[k].y, a.y);
                             a.z = fmaf(wt, v[k].z, a.z); a.w = fmaf(wt, v[k].w, a.w);
                         }
@@ -1620,9 +1643,9 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     a.z += __shfl_xor_sync(0xFFFFFFFFu, a.z, o); a.w += __shfl_xor_sync(0xFFFFFFFFu, a.w, o);
                 }
                 if (cl_ == 0 && o4 < NO4) {
-                    const float sc = s.misc->alpha[h];
+                    const float sc = s.misc()->alpha[h];
                     // 4 consecutive values of one head: one half of a split chunk
-                    *reinterpret_cast<float4*>(s.ov + xsplit(o4 * 4, G * HD)) =
+                    *reinterpret_cast<float4*>(s.ov() + xsplit(o4 * 4, G * HD)) =
                         make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
                 }
             }
@@ -1633,8 +1656,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
         // O-proj (rows of this CTA, columns of this group) + residual, atomically
         float* xo = xa + (size_t)(2 * l) * state;
-        ab = gemv_phase_t<MO, LPRO>(p, s, ring, s.ov, pl.norows, g.TRo, s.misc->ocfg, ab, [&](int r, float v) {
-            if (pl.g == 0) v += s.xres[r];   // group 0 carries the residual of these rows
+        ab = gemv_phase_t<MO, LPRO>(p, s, ring, s.ov(), pl.norows, g.TRo, s.misc()->ocfg, ab, [&](int r, float v) {
+            if (pl.g == 0) v += s.xres()[r];   // group 0 carries the residual of these rows
             atomicAdd(xo + pl.orow0 + r, v);
         });
         MK_TRACE(16 * l + 8);
@@ -1644,20 +1667,20 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 9);
 
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
-        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2, dr0, dr1 - dr0);
+        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2(), dr0, dr1 - dr0);
         MK_TRACE(16 * l + 10);
-        if (t == 0) *(volatile int*)&s.misc->streaming = 1;   // gate/up and down stream
+        if (t == 0) *(volatile int*)&s.misc()->streaming = 1;   // gate/up and down stream
         if (l == 3) trace_ring(p, ring, 4);   // everything before this layer's FFN (discarded)
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
             const int JT = g.JT;
-            ab = gemv_fifo<MH>(p, s, ring, s.xv, 2 * pl.nj, 2 * JT, ab, s.part);
+            ab = gemv_fifo<MH>(p, s, ring, s.xv(), 2 * pl.nj, 2 * JT, ab, s.part());
             for (int j = t; j < pl.nj; j += MK_NCT) {
                 const int q = j / JT, jj = j % JT;
                 const int n = min(JT, pl.nj - q * JT);
-                const float gt = wide_row<MH>(s.part, q * 2 * JT + jj);
-                const float up = wide_row<MH>(s.part, q * 2 * JT + n + jj);
-                s.u[j] = gt / (1.f + __expf(-gt)) * up;
+                const float gt = wide_row<MH>(s.part(), q * 2 * JT + jj);
+                const float up = wide_row<MH>(s.part(), q * 2 * JT + n + jj);
+                s.u()[j] = gt / (1.f + __expf(-gt)) * up;
             }
         }
         MK_TRACE(16 * l + 11);
@@ -1707,7 +1730,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 #pragma unroll
                     for (int jj = 0; jj < NJ; ++jj) {
                         if (ok && jj < n) {
-                            const float uj = s.u[j0 + jj];
+                            const float uj = s.u()[j0 + jj];
                             const float2 u2 = make_float2(uj, uj);
 #pragma unroll
                             for (int m = 0; m < CPT; ++m) {
@@ -1722,7 +1745,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                     if (ok) {
 #pragma unroll (CPT <= 2 ? 2 : 1)
                         for (int jj = 0; jj < n; ++jj) {
-                            const float uj = s.u[j0 + jj];
+                            const float uj = s.u()[j0 + jj];
                             const float2 u2 = make_float2(uj, uj);
                             const uint8_t* col = tile + (size_t)jj * H * 2;
 #pragma unroll
@@ -1740,7 +1763,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
             }
             MK_TRACE(16 * l + 14);
-            if (t == 0) *(volatile int*)&s.misc->streaming = 0;
+            if (t == 0) *(volatile int*)&s.misc()->streaming = 0;
             if (l == 3) trace_ring(p, ring, 1);
             // fold the phases: phase q adds what phase q+1 left in xv (element
             // e of chunk c at xv[e * NCH + c]: lane-consecutive, conflict free)
@@ -1754,15 +1777,15 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                         if (q < P - 1) {
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                da[m][k].x += s.xv[(2 * k) * NCH + cc];
-                                da[m][k].y += s.xv[(2 * k + 1) * NCH + cc];
+                                da[m][k].x += s.xv()[(2 * k) * NCH + cc];
+                                da[m][k].y += s.xv()[(2 * k + 1) * NCH + cc];
                             }
                         }
                         if (q > 0) {
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                s.xv[(2 * k) * NCH + cc] = da[m][k].x;
-                                s.xv[(2 * k + 1) * NCH + cc] = da[m][k].y;
+                                s.xv()[(2 * k) * NCH + cc] = da[m][k].x;
+                                s.xv()[(2 * k + 1) * NCH + cc] = da[m][k].y;
                             }
                         } else {
                             // rows 8cc .. 8cc+7; this CTA carries the residual of rows [dr0, dr1)
@@ -1771,7 +1794,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const int rr = 8 * cc + e - dr0;
-                                if ((unsigned)rr < (unsigned)(dr1 - dr0)) r[e] += s.xres2[rr];
+                                if ((unsigned)rr < (unsigned)(dr1 - dr0)) r[e] += s.xres2()[rr];
                             }
                             red_add_v4(xf + 8 * cc, make_float4(r[0], r[1], r[2], r[3]));
                             red_add_v4(xf + 8 * cc + 4, make_float4(r[4], r[5], r[6], r[7]));
@@ -1794,13 +1817,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         const float* xl = xa + (size_t)(2 * L - 1) * state;
         ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0);
         MK_TRACE(16 * L + 0);
-        if (t == 0) *(volatile int*)&s.misc->streaming = 1;   // the LM head streams
+        if (t == 0) *(volatile int*)&s.misc()->streaming = 1;   // the LM head streams
         if (c == 0 && !ab)
-            for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv[xsplit(i, H)];
+            for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv()[xsplit(i, H)];
         float bv = -INFINITY;
         int bi = -1;
         bool nonfinite = false;
-        ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv, pl.nv, g.TRh, s.misc->lmcfg, ab, [&](int r, float lg) {
+        ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv(), pl.nv, g.TRh, s.misc()->lmcfg, ab, [&](int r, float lg) {
             const int v = pl.v0 + r;
             if (p.logits) p.logits[v] = lg;
             if (isfinite(lg)) {
@@ -1815,14 +1838,14 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * L + 1);
         MK_TRACE_CWAIT(8 * L + 5);
         if (nonfinite) atomicOr(p.status, MK_ST_NUMERIC);
-        if ((t & 31) == 0) { s.misc->best_val[t >> 5] = bv; s.misc->best_idx[t >> 5] = bi; }
+        if ((t & 31) == 0) { s.misc()->best_val[t >> 5] = bv; s.misc()->best_idx[t >> 5] = bi; }
         ab = bar_or(ab);
         if (t == 0 && !ab) {
             float v = -INFINITY;
             int idx = -1;
             for (int i = 0; i < MK_NCW; ++i) {
-                const int ii = s.misc->best_idx[i];
-                const float vv = s.misc->best_val[i];
+                const int ii = s.misc()->best_idx[i];
+                const float vv = s.misc()->best_val[i];
                 if (ii >= 0 && (idx < 0 || vv > v || (vv == v && ii < idx))) { v = vv; idx = ii; }
             }
             if (idx >= 0) {
@@ -1836,14 +1859,14 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
     // ---------------- end of step: the last CTA publishes the token and resets the flags
     MK_TRACE(16 * L + 2);
-    if (t == 0 && ab) s.misc->abort = 1;   // lets the producer warps stop and drain
+    if (t == 0 && ab) s.misc()->abort = 1;   // lets the producer warps stop and drain
     if (t == 0) {
         __threadfence();
         const uint32_t prev = atomicAdd(p.cnt + mk_cnt_done(g), 1u);
-        s.misc->is_last = (prev == (uint32_t)g.nC - 1) ? 1 : 0;
+        s.misc()->is_last = (prev == (uint32_t)g.nC - 1) ? 1 : 0;
     }
     bar_or(false);
-    if (s.misc->is_last) {
+    if (s.misc()->is_last) {
         __threadfence();
         const int ntot = mk_cnt_done(g);
         for (int i = t; i < ntot; i += MK_NCT) p.cnt[i] = 0u;
