@@ -14,6 +14,8 @@ cascade.  Per step it records
 
 Tolerances (stated for the decode step): max |dlogit| <= 5e-2, hidden relative
 error <= 1e-2, greedy agreement >= 99% of steps with every disagreement a near tie.
+The agreement bar applies to runs of 100 steps or more, and to every run of one
+of the five benchmark workloads whatever its length (check(workload=True)).
 """
 from __future__ import annotations
 
@@ -37,19 +39,22 @@ class Report:
     flips_not_near_tie: int = 0
     self_argmax_mismatch: int = 0
     tokens: list = dataclasses.field(default_factory=list)
+    # every disagreement with the oracle: (step, oracle top-2 gap, max |dlogit| of that step)
+    flips: list = dataclasses.field(default_factory=list)
 
-    def check(self):
+    def check(self, workload: bool = False):
         assert self.steps > 0
         assert self.max_dlogit <= LOGIT_TOL, f"max |dlogit| {self.max_dlogit:.3e} > {LOGIT_TOL}"
         assert self.max_hidden_rel <= HIDDEN_TOL, f"hidden rel err {self.max_hidden_rel:.3e} > {HIDDEN_TOL}"
         assert self.self_argmax_mismatch == 0, "fused argmax differs from argmax of the GPU's own logits"
         assert self.flips_not_near_tie == 0, f"{self.flips_not_near_tie} argmax flips without a near tie"
-        if self.steps >= 100:
+        if workload or self.steps >= 100:
             assert self.agree / self.steps >= ARGMAX_AGREE, f"argmax agreement {self.agree}/{self.steps}"
 
     def summary(self):
+        fl = "".join(f" flip@{k}(gap {g:.2e}, dl {d:.2e})" for k, g, d in self.flips)
         return (f"steps={self.steps} max|dlogit|={self.max_dlogit:.3e} hidden_rel={self.max_hidden_rel:.3e} "
-                f"argmax {self.agree}/{self.steps}")
+                f"argmax {self.agree}/{self.steps}{fl}")
 
 
 def gpu_argmax_of(logits: np.ndarray) -> int:
@@ -66,11 +71,12 @@ def run_teacher_forced(dec, orc: oracle.OracleDecoder, tokens_in, start_pos: int
         pos = start_pos + k
         if k < len(tokens_in):
             tok = int(tokens_in[k])
-        lg_ref, h_ref = orc.step(tok, pos)
+        # the GPU step is queued first, so it runs while the oracle computes
         if perop:
             dec.step_perop(tok, pos)
         else:
             dec.step(tok, pos)
+        lg_ref, h_ref = orc.step(tok, pos)
         lg = dec.logits.cpu().numpy().astype(np.float64)
         h = dec.get_hidden().cpu().numpy().astype(np.float64)
         g_arg = dec.get_argmax()
@@ -84,7 +90,9 @@ def run_teacher_forced(dec, orc: oracle.OracleDecoder, tokens_in, start_pos: int
             rep.agree += 1
         else:
             top2 = np.sort(lg_ref.astype(np.float32))[-2:]
-            if float(top2[1] - top2[0]) >= 2 * max(dl, 1e-6):
+            gap = float(top2[1] - top2[0])
+            rep.flips.append((k, gap, dl))
+            if gap >= 2 * max(dl, 1e-6):
                 rep.flips_not_near_tie += 1
         rep.steps += 1
         rep.tokens.append(r_arg)
