@@ -196,15 +196,16 @@ bool check_schedule(const MkGeom& g, const std::vector<MkCtaPlan>& plans, int64_
     const uint16_t* Vc = reinterpret_cast<const uint16_t*>((uintptr_t)3 << 41);
     const int64_t kv_bytes = (int64_t)g.L * g.kvh * g.max_seq * g.hd * 2;
     const int poss[4] = {0, 1, g.max_seq / 2, g.max_seq - 1};
-    for (int pi = 0; pi < 4; ++pi) {
-        const int pos = poss[pi];
-        if (pos < 0 || pos >= g.max_seq) continue;
+    const int nas[4] = {1, 3, (g.CPG + 1) / 2, g.CPG};   // attention CTAs per group
+    for (int ci = 0; ci < 16; ++ci) {
+        const int pos = poss[ci / 4], na = nas[ci % 4];
+        if (pos < 0 || pos >= g.max_seq || na > g.CPG) continue;
         for (int c = 0; c < g.nC; ++c) {
             const MkCtaPlan& pl = plans[c];
             const int64_t lo = pl.stream_off, hi = pl.stream_off + mk_cta_stream_bytes(g, pl);
             int64_t wbytes = 0;
             bool ok = true;
-            mk_walk_tiles(g, pl, A, K, Vc, pos, [&](const void* src, uint32_t bytes) {
+            mk_walk_tiles(g, pl, A, K, Vc, pos, na, [&](const void* src, uint32_t bytes) {
                 const uint8_t* s = reinterpret_cast<const uint8_t*>(src);
                 if (bytes == 0 || bytes % 16 || (int64_t)bytes > g.slot || ((uintptr_t)s & 15)) ok = false;
                 const uint8_t* kb = reinterpret_cast<const uint8_t*>(K);
@@ -247,6 +248,10 @@ struct mk_ctx {
     const void* kernel_tc_trace = nullptr;
     int tc_min_per_cta = MK_ATTN_TC_MIN_PER_CTA;
     int attn_build = 0;                  // debug: 0 by context length, 1 lane-parallel, 2 tensor cores
+    // the length-adaptive split: A = ceil(ctx / attn_pos_per_cta) CTAs of each
+    // KV group (at most all of them) run a step's attention, or attn_ctas_force
+    int attn_pos_per_cta = MK_ATTN_POS_PER_CTA;
+    int attn_ctas_force = 0;
     std::vector<MkCtaPlan> plans;
     int64_t arena_bytes = 0, device_bytes = 0;
     bool weights_loaded = false;
@@ -328,8 +333,29 @@ MkParams base_params(const mk_ctx* c) {
     return p;
 }
 
-// Context length from which steps launch the tensor-core attention build.
-int64_t mk_tc_min_ctx(const mk_ctx* c) { return (int64_t)c->tc_min_per_cta * c->geo.CPG; }
+// The attention plan of the step at position pos: how many CTAs of each KV
+// group split the positions (the length-adaptive split) and whether the
+// tensor-core build runs it (from tc_min_per_cta positions per attention CTA;
+// default 0: always, where it exists).
+void attn_plan(const mk_ctx* c, int pos, int* A, bool* tc) {
+    const int64_t ctx = (int64_t)pos + 1, cpg = c->geo.CPG;
+    int64_t a = c->attn_ctas_force > 0 ? c->attn_ctas_force : (ctx + c->attn_pos_per_cta - 1) / c->attn_pos_per_cta;
+    a = a < 1 ? 1 : a > cpg ? cpg : a;
+    *A = (int)a;
+    *tc = c->kernel_tc && (c->attn_build == 2 ||
+                           (c->attn_build == 0 && ctx >= (int64_t)c->tc_min_per_cta * a));
+}
+
+// Context length from which steps launch the tensor-core attention build (-1: never).
+int64_t mk_tc_min_ctx(const mk_ctx* c) {
+    for (int pos = 0; pos < c->geo.max_seq; ++pos) {
+        int a;
+        bool tc;
+        attn_plan(c, pos, &a, &tc);
+        if (tc) return pos + 1;
+    }
+    return -1;
+}
 
 int launch_step(mk_ctx* c, MkParams& p, cudaStream_t st) {
     cudaLaunchConfig_t lc;
@@ -344,11 +370,9 @@ int launch_step(mk_ctx* c, MkParams& p, cudaStream_t st) {
     lc.attrs = attr;
     lc.numAttrs = 1;
     void* args[] = {&p};
-    // attention build by context length: the tensor-core build from
-    // tc_min_per_cta positions per CTA (default 0: always, where it exists),
-    // the lane-parallel build below that
-    const bool tc = c->kernel_tc && (c->attn_build == 2 ||
-                                     (c->attn_build == 0 && (int64_t)(p.pos + 1) >= mk_tc_min_ctx(c)));
+    // attention CTAs per group and attention build by context length
+    bool tc = false;
+    attn_plan(c, p.pos, &p.attn_ctas, &tc);
     const void* fn = tc ? (c->trace ? c->kernel_tc_trace : c->kernel_tc) : (c->trace ? c->kernel_trace : c->kernel);
     MK_CU(cudaLaunchKernelExC(&lc, fn, args));
     c->last_stream = st;
@@ -976,7 +1000,8 @@ int mk_get_info(const mk_ctx* c, mk_info* o) {
     o->kv_bytes_per_position = (int64_t)2 * c->geo.L * c->geo.kvh * c->geo.hd * 2;
     o->device_bytes = c->device_bytes;
     o->attn_tc = c->kernel_tc ? 1 : 0;
-    o->attn_tc_min_ctx = c->kernel_tc ? (int32_t)std::min<int64_t>(mk_tc_min_ctx(c), INT32_MAX) : -1;
+    o->attn_tc_min_ctx = c->kernel_tc ? (int32_t)mk_tc_min_ctx(c) : -1;
+    o->attn_pos_per_cta = c->attn_ctas_force > 0 ? 0 : c->attn_pos_per_cta;
     return MK_OK;
 }
 
@@ -1015,6 +1040,16 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_ATTN_BUILD) {
         if (value < 0 || value > 2 || (value == 2 && !c->kernel_tc)) return MK_ERR_INVALID_ARG;
         c->attn_build = (int)value;
+        return MK_OK;
+    }
+    if (knob == MK_DBG_ATTN_CTAS) {
+        if (value < 0 || value > c->geo.CPG) return MK_ERR_INVALID_ARG;
+        c->attn_ctas_force = (int)value;
+        return MK_OK;
+    }
+    if (knob == MK_DBG_ATTN_POS_PER_CTA) {
+        if (value < 1 || value > (int64_t)c->geo.max_seq) return MK_ERR_INVALID_ARG;
+        c->attn_pos_per_cta = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_ATTN_TC_MIN) {

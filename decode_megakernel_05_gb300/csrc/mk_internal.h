@@ -43,6 +43,12 @@
 // lane-parallel build at 13 positions per CTA and faster from there on (2% at
 // 54, 6% at 216), so every step of a shape that has it runs it.
 #define MK_ATTN_TC_MIN_PER_CTA 0
+// Length-adaptive attention split: a step at context ctx runs its attention on
+// ceil(ctx / MK_ATTN_POS_PER_CTA) CTAs of each KV group (at most all of them).
+// 192 is one 16-position chunk for each of the 12 consumer warps of the
+// tensor-core build: below a full group, fewer CTAs take the same time per
+// chunk and the combine waits on fewer partials.
+#define MK_ATTN_POS_PER_CTA 192
 
 // Device status word bits.
 #define MK_ST_TIMEOUT 0x1u
@@ -191,6 +197,7 @@ struct MkParams {
     uint32_t* status;
     uint32_t* seq;               // launch sequence number (selects the xacc parity)
     int32_t pos;
+    int32_t attn_ctas;           // A: CTAs of each KV group that run this step's attention (1..CPG)
     int32_t token;               // used when token_ptr == nullptr
     const int32_t* token_ptr;
     float* logits;               // [V] or nullptr
@@ -249,20 +256,38 @@ MK_HD int64_t mk_cta_stream_bytes(const MkGeom& g, const MkCtaPlan& p) {
 
 MK_HD int mk_imin(int a, int b) { return a < b ? a : b; }
 
+// The share of attended positions [0, pos] of CTA i of a KV group when the
+// first A CTAs of each group run the attention (the length-adaptive split:
+// cloud.baidu.com/article/9434380, section 8, problems 3 and 5): CTA i < A
+// takes split(pos + 1, A, i); the past positions of it, [*ka, *ke) clipped to
+// [0, pos), come from the cache, and CTA A - 1 also takes the current
+// position, which it reads from the step's own K/V.  CTAs i >= A take none.
+MK_HD void mk_attn_share(int pos, int A, int i, int* ka, int* ke, bool* has_cur) {
+    const int ctx = pos + 1;
+    int a = 0, e = 0;
+    if (i < A) {
+        a = (int)mk_split(ctx, A, i);
+        const int b = (int)mk_split(ctx, A, i + 1);
+        e = b < pos ? b : pos;
+    }
+    *ka = a;
+    *ke = e;
+    *has_cur = (i == A - 1);
+}
+
 // Walks every tile CTA `pl` consumes during the step at position `pos`, in
 // consumption order, calling f(src, bytes): per layer the QKV rows, then the
-// K and V blocks of its share of positions [0, pos) (the current position is
-// read directly, not streamed), then the O, gate/up and down tiles; then the
-// LM-head rows.  KV share of CTA i of its group: split(pos + 1, CPG, i)
-// clipped to [0, pos).
+// K and V blocks of its share of positions [0, pos) (mk_attn_share with A
+// attention CTAs per group; the current position is read directly, not
+// streamed), then the O, gate/up and down tiles; then the LM-head rows.
 template <class F>
 MK_HD void mk_walk_tiles(const MkGeom& g, const MkCtaPlan& pl, const uint8_t* arena, const uint16_t* kc,
-                         const uint16_t* vc, int pos, F&& f) {
+                         const uint16_t* vc, int pos, int A, F&& f) {
     const uint8_t* cur = arena + pl.stream_off;
-    const int H = g.H, ctx = pos + 1;
-    const int a = (int)mk_split(ctx, g.CPG, pl.i);
-    const int b = (int)mk_split(ctx, g.CPG, pl.i + 1);
-    const int e = b < pos ? b : pos;
+    const int H = g.H;
+    int a, e;
+    bool hc;
+    mk_attn_share(pos, A, pl.i, &a, &e, &hc);
     const int KO = g.G * g.hd;
     for (int l = 0; l < g.L; ++l) {
         const int nr = 2 * pl.npairs;

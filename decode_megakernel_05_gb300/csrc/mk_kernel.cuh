@@ -147,6 +147,9 @@ __device__ __forceinline__ bool bar_or(bool f) {
     return r != 0;
 }
 __device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+// A shared-memory value re-read where it is used (volatile: not kept in a
+// register across the code in between).
+__device__ __forceinline__ int ldv(const int& x) { return *reinterpret_cast<const volatile int*>(&x); }
 
 // 8 bf16 (one 16-byte chunk, lower address first) -> fp32
 __device__ __forceinline__ void unpack8(const uint4 w, float f[8]) {
@@ -199,6 +202,11 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     int streaming;           // consumers are in a streaming segment (sets the producer's in-flight limit)
     uint32_t tag;            // this launch's tag for tagged words (sequence number + 1)
     MkCtaPlan plan;          // this CTA's plan (read from here: keeps registers free in the layer loop)
+    // per-CTA constants of the step, read where used (not held in registers
+    // across the layer loop): the attention share [ka, ke) + current position
+    // (mk_attn_share), whether this CTA runs the attention, the residual rows
+    // [dr0, dr1) it adds in the down projection
+    int ka, ke, has_cur, att, dr0, dr1;
     GemvCfg ocfg, lmcfg;     // work split of the O-proj and LM-head phases
     float cwt[MK_MAX_CPG_G]; // attention-combine weights [CPG][G]
     float cl[MK_MAX_CPG_G];  // attention partial sums l [CPG][G]
@@ -337,7 +345,7 @@ __device__ __forceinline__ void arrive(const MkParams& p, int idx, int sync_id) 
 // The tile walk (mk_walk_tiles) lives in mk_internal.h so the host can check it.
 template <class F>
 __device__ __forceinline__ void walk_tiles(const MkParams& p, const MkCtaPlan& pl, F&& f) {
-    mk_walk_tiles(p.geo, pl, p.arena, p.kc, p.vc, p.pos, f);
+    mk_walk_tiles(p.geo, pl, p.arena, p.kc, p.vc, p.pos, p.attn_ctas, f);
 }
 
 __device__ void producer_copy(const MkParams& p, const MkCtaPlan& pl, const Smem& s) {
@@ -1233,7 +1241,9 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
 // in smem for the partial.  Returns the uniform abort flag (one barrier).
 template <int HD, int G, int HPL, bool TC>
 __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
-                                         bool has_cur, float qscale, bool ab, bool late) {
+                                         bool has_cur, bool ab, bool late) {
+    constexpr float qscale = (HD == 64 ? 0.125f : 0.08838834764831845f) * 1.4426950408889634f;   // log2(e)/sqrt(hd)
+    static_assert(HD == 64 || HD == 128, "attention head sizes");
     using A = Attn<HD, G, HPL>;
     const MkGeom& g = p.geo;
     const MkCtaPlan& pl = s.misc()->plan;
@@ -1393,6 +1403,17 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         s.misc()->zrow = make_uint4(0u, 0u, 0u, 0u);
         s.misc()->plan = p.plans[c];
         {
+            int ka_, ke_;
+            bool hc_;
+            mk_attn_share(p.pos, p.attn_ctas, s.misc()->plan.i, &ka_, &ke_, &hc_);
+            s.misc()->ka = ka_;
+            s.misc()->ke = ke_;
+            s.misc()->has_cur = hc_ ? 1 : 0;
+            s.misc()->att = s.misc()->plan.i < p.attn_ctas ? 1 : 0;
+            s.misc()->dr0 = (int)mk_split(g.H, g.nC, c);
+            s.misc()->dr1 = (int)mk_split(g.H, g.nC, c + 1);
+        }
+        {
             constexpr int KO = G * HD, LPRO = KO >= 32 * 4 ? KO / 32 : 4;
             gemv_cfg(s.misc()->ocfg, s.misc()->plan.norows, g.TRo, 32 / LPRO);
             gemv_cfg(s.misc()->lmcfg, s.misc()->plan.nv, g.TRh, 1);
@@ -1431,16 +1452,14 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         for (size_t i = lo + t; i < hi; i += MK_NCT) xz[i] = 0.f;
     }
     const uint16_t* emb = p.embed + (size_t)token * H;
-    const int ctx = p.pos + 1;
-    const int ka = (int)mk_split(ctx, g.CPG, pl.i), kb_ = (int)mk_split(ctx, g.CPG, pl.i + 1);
-    const int ke = kb_ < p.pos ? kb_ : p.pos;
-    const bool has_cur = (pl.i == g.CPG - 1);
-    const int dr0 = (int)mk_split(H, g.nC, c), dr1 = (int)mk_split(H, g.nC, c + 1);   // rows whose residual I add
+    // this CTA's share of the attention (the first A CTAs of each KV group
+    // split the positions, the others go from the QKV straight to the combine)
+    // and the rows whose residual it adds: s.misc() (ka, ke, has_cur, att, dr0, dr1)
+    const int A = p.attn_ctas;
     for (int d = t; d < hd2; d += MK_NCT) {       // RoPE angles of this position
         s.rope()[d] = p.rope_cos[(size_t)p.pos * hd2 + d];
         s.rope()[hd2 + d] = p.rope_sin[(size_t)p.pos * hd2 + d];
     }
-    const float qscale = rsqrtf((float)HD) * 1.4426950408889634f;  // 1/sqrt(hd) * log2(e)
 
     Ring ring;
     bool ab = false;
@@ -1488,9 +1507,9 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment B: split-K attention over this CTA's positions
         MK_TRACE_D(l, 7);        // segment B entered
         {
-            // stage K[pos], V[pos] (bf16) from their tagged copies (last CTA of the group)
+            // stage K[pos], V[pos] (bf16) from their tagged copies (last attention CTA of the group)
             bool late = false;
-            if (!ab && has_cur && t < HD / 4) {
+            if (!ab && ldv(s.misc()->has_cur) && t < HD / 4) {
                 float kv[8];
                 late = !ll_read8(p, p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (t < HD / 8 ? 0 : 1)) * HD +
                                         (t % (HD / 8)) * 8, s.misc()->tag, kv);
@@ -1502,17 +1521,17 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 s.misc()->stage[t] = w;
             }
             // Blocks of up to KB past positions from the ring (the K tile and
-            // the V tile of a block are held together); the last CTA of the
-            // group appends the current position (staged) to its last block,
-            // or runs it as a block of its own when it has no past.
-            const int nring = ke > ka ? ke - ka : 0;
-            const int nblk = (nring + g.KB - 1) / g.KB;
-            (void)nblk;
-            ab = attn_run<HD, G, 1, LC != 0>(p, s, ring, l, ka, ke, has_cur, qscale, ab, late);
+            // the V tile of a block are held together); the last attention
+            // CTA of the group appends the current position (staged) to its
+            // last block, or runs it as a block of its own when it has no past.
+            // (att is the same for the whole CTA: the barriers inside stay uniform.)
+            if (ldv(s.misc()->att))
+                ab = attn_run<HD, G, 1, LC != 0>(p, s, ring, l, ldv(s.misc()->ka), ldv(s.misc()->ke),
+                                                 ldv(s.misc()->has_cur) != 0, ab, late);
         }
         ab = bar_or(ab);
         constexpr int PSTR = G * HD + 2 * G;                   // tagged words per partial
-        if (!ab && !(p.dbg_skip_sync == 4 * l + 1 && p.dbg_skip_cta == c)) {
+        if (ldv(s.misc()->att) && !ab && !(p.dbg_skip_sync == 4 * l + 1 && p.dbg_skip_cta == c)) {
             constexpr int PPP = Attn<HD, G>::NMG;               // parked groups (the same for both lane layouts)
             uint64_t* dst = p.partll + (((size_t)l * g.kvh + pl.g) * g.CPG + pl.i) * PSTR;
             for (int i = t; i < G * HD; i += MK_NCT) {
@@ -1538,7 +1557,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE_CWAIT(8 * l + 1);
         MK_TRACE(16 * l + 6);
 
-        // combine the group's partials -> o (the G heads of this KV group):
+        // combine the group's A partials -> o (the G heads of this KV group):
         // weights exp2(m_j - M) / sum_j exp2(m_j - M) l_j.  A team of CT lanes
         // owns one float4 of o and takes the partials j = lane (mod CT); the
         // team sums with shuffles.  The partials are tagged words polled
@@ -1563,7 +1582,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 #pragma unroll
                 for (int k = 0; k < CB; ++k) {
                     const int j = cl_ + (k0 + k) * CT;
-                    if (o4 < NO4 && j < g.CPG) {
+                    if (o4 < NO4 && j < A) {
                         const uint64_t* w = pg + (size_t)j * PSTR + o4 * 4;
                         const ulonglong2 a = ld_ll2(w), b = ld_ll2(w + 2);
                         ok = ok & ll_ok(a, s.misc()->tag) & ll_ok(b, s.misc()->tag);
@@ -1587,7 +1606,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 uint64_t t0 = 0;
                 for (;;) {
                     bool ok = load_batch_once(t / CT, 0);
-                    for (int i = t; i < g.CPG * G; i += MK_NCT) {
+                    for (int i = t; i < A * G; i += MK_NCT) {
                         const ulonglong2 w = ld_ll2(pg + (size_t)(i / G) * PSTR + G * HD + 2 * (i % G));
                         ok = ok & ll_ok(w, s.misc()->tag);
                         cw[i] = __uint_as_float((uint32_t)w.x);
@@ -1603,11 +1622,11 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             if (!ab && (t >> 5) < G) {   // warp h: head h, lanes over the partials
                 const int hh = t >> 5, ln = t & 31;
                 float mx = -INFINITY;
-                for (int j = ln; j < g.CPG; j += 32) mx = fmaxf(mx, cw[j * G + hh]);
+                for (int j = ln; j < A; j += 32) mx = fmaxf(mx, cw[j * G + hh]);
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
                 float den = 0.f;
-                for (int j = ln; j < g.CPG; j += 32) {
+                for (int j = ln; j < A; j += 32) {
                     const float mj = cw[j * G + hh];
                     const float wj = (mj == -INFINITY) ? 0.f : exp2f(mj - mx);
                     den = fmaf(wj, s.misc()->cl[j * G + hh], den);
@@ -1623,14 +1642,14 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 const int o4 = t / CT + ps * (MK_NCT / CT);
                 const int h = (o4 * 4) / HD;
                 float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int k0 = 0; k0 * CT < g.CPG; k0 += CB) {
+                for (int k0 = 0; k0 * CT < A; k0 += CB) {
                     if (k0 > 0 || ps > 0) {   // further batches (large groups or several passes)
                         if (!load_batch(o4, k0)) late = true;
                     }
 #pragma unroll
                     for (int k = 0; k < CB; ++k) {
                         const int j = cl_ + (k0 + k) * CT;
-                        if (o4 < NO4 && j < g.CPG) {
+                        if (o4 < NO4 && j < A) {
                             const float wt = s.misc()->cwt[j * G + h];
                             a.x = fmaf(wt, v[k].x, a.x); a.y = fmaf(wt, v[k].y, a.y);
                             a.z = fmaf(wt, v[k].z, a.z); a.w = fmaf(wt, v[k].w, a.w);
@@ -1667,7 +1686,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 9);
 
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
-        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2(), dr0, dr1 - dr0);
+        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2(),
+                                                             ldv(s.misc()->dr0), ldv(s.misc()->dr1) - ldv(s.misc()->dr0));
         MK_TRACE(16 * l + 10);
         if (t == 0) *(volatile int*)&s.misc()->streaming = 1;   // gate/up and down stream
         if (l == 3) trace_ring(p, ring, 4);   // everything before this layer's FFN (discarded)
@@ -1789,6 +1809,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                             }
                         } else {
                             // rows 8cc .. 8cc+7; this CTA carries the residual of rows [dr0, dr1)
+                            const int dr0 = ldv(s.misc()->dr0), dr1 = ldv(s.misc()->dr1);
                             float r[8] = {da[m][0].x, da[m][0].y, da[m][1].x, da[m][1].y,
                                           da[m][2].x, da[m][2].y, da[m][3].x, da[m][3].y};
 #pragma unroll

@@ -35,6 +35,8 @@ MK_DBG_PF_LEAD = 8
 MK_DBG_PF_DEPTH = 9
 MK_DBG_ATTN_BUILD = 10
 MK_DBG_ATTN_TC_MIN = 11
+MK_DBG_ATTN_CTAS = 12
+MK_DBG_ATTN_POS_PER_CTA = 13
 MK_NOALLOC_ARGMAX_BLOCKS = 1024
 MK_NOALLOC_ARGMAX_MAX_N = MK_NOALLOC_ARGMAX_BLOCKS * 4096
 
@@ -61,7 +63,8 @@ class mk_info(ctypes.Structure):
     _fields_ = [("grid_ctas", _i32), ("ctas_per_group", _i32), ("block_threads", _i32), ("ring_stages", _i32),
                 ("slot_bytes", _i32), ("smem_bytes", _i32), ("sm_count", _i32), ("l2_prefetch_bytes", _i32),
                 ("arena_bytes", _i64), ("weight_bytes_per_token", _i64), ("kv_bytes_per_position", _i64),
-                ("device_bytes", _i64), ("attn_tc", _i32), ("attn_tc_min_ctx", _i32)]
+                ("device_bytes", _i64), ("attn_tc", _i32), ("attn_tc_min_ctx", _i32),
+                ("attn_pos_per_cta", _i32)]
 
 
 # (name, restype, argtypes) of every exported function, in header order.

@@ -111,6 +111,10 @@ typedef struct {
     int32_t attn_tc_min_ctx;         /* context length (pos + 1) from which a step launches that
                                         build; shorter contexts run the lane-parallel attention
                                         (-1 without attn_tc) */
+    int32_t attn_pos_per_cta;        /* length-adaptive split: a step at context ctx runs its
+                                        attention on ceil(ctx / attn_pos_per_cta) CTAs of each KV
+                                        group, at most ctas_per_group (0: the count is forced
+                                        with MK_DBG_ATTN_CTAS) */
 } mk_info;
 
 /* Create a context on CUDA device `device`: validates the shape, sizes the
@@ -297,6 +301,12 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
  * (default 0: every step; 0 .. max_seq). */
 #define MK_DBG_ATTN_BUILD 10
 #define MK_DBG_ATTN_TC_MIN 11
+/* MK_DBG_ATTN_CTAS: value = CTAs of each KV group that run every step's
+ * attention, 1 .. ctas_per_group (0 = by context length, the default).
+ * MK_DBG_ATTN_POS_PER_CTA: positions per attention CTA of the default split
+ * (1 .. max_seq; the default is mk_info.attn_pos_per_cta). */
+#define MK_DBG_ATTN_CTAS 12
+#define MK_DBG_ATTN_POS_PER_CTA 13
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
 const char* mk_strerror(int code);

@@ -35,7 +35,10 @@ def test_skipped_arrival_times_out_and_context_recovers(tiny, sync_id):
         dec.step(int(prompt[p]), p)
     assert dec.status() == mk.MK_OK
     dec.set_debug(mk.MK_DBG_WAIT_LIMIT_NS, 20_000_000)
-    dec.set_debug(mk.MK_DBG_SKIP_ARRIVAL, 5 * 65536 + sync_id)
+    # CTA 5 skips its arrival; the attention partials (sync_id 1) come only
+    # from the CTAs that run the step's attention, which always include CTA 0
+    cta = 0 if sync_id == 1 else 5
+    dec.set_debug(mk.MK_DBG_SKIP_ARRIVAL, cta * 65536 + sync_id)
     dec.step(int(prompt[3]), 3)
     assert dec.status() == mk.MK_ERR_DEVICE_TIMEOUT
     dec.set_debug(mk.MK_DBG_SKIP_ARRIVAL, -1)
@@ -73,6 +76,15 @@ def test_argument_errors_return_codes_without_launch(tiny):
     assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_TC_MIN, -1) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_TC_MIN, dec.max_seq + 1) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_BUILD, 0) == mk.MK_OK
+    # attention-split knobs: 0 .. CTAs per group, positions per CTA >= 1
+    cpg = dec.info.ctas_per_group
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_CTAS, -1) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_CTAS, cpg + 1) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_POS_PER_CTA, 0) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_CTAS, cpg) == mk.MK_OK
+    assert mk.mk_get_info(dec.ctx).attn_pos_per_cta == 0
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_ATTN_CTAS, 0) == mk.MK_OK
+    assert mk.mk_get_info(dec.ctx).attn_pos_per_cta == dec.info.attn_pos_per_cta > 0
     # a K/V window past the end of the cache
     k = np.zeros((w.shape.n_kv_heads, 2, w.shape.head_dim), dtype=np.uint16)
     v = np.zeros_like(k)

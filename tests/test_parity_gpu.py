@@ -112,10 +112,55 @@ def test_attention_build_switch_by_context():
     7 CTAs per group the switch comes at context 21, inside one teacher-forced
     run from position 0, and parity holds on both sides of it."""
     m, dec, orc = make(MID, 71, 8192, gains="normal", std=0.04, tuning=mk.tuning(grid_ctas=14))
+    dec.set_debug(mk.MK_DBG_ATTN_CTAS, 7)   # all 7 CTAs of a group attend at every context
     dec.set_debug(mk.MK_DBG_ATTN_TC_MIN, 3)
     info = mk.mk_get_info(dec.ctx)
     assert info.attn_tc == 1 and info.attn_tc_min_ctx == 21
     rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, MID.vocab, 71, 3), 0, 40)
+    print(rep.summary())
+    rep.check()
+    dec.close()
+
+
+@pytest.mark.parametrize("grid,prefill,ctas,build", [(0, 300, 1, 2), (0, 300, 2, 2), (0, 300, 5, 2), (0, 300, 76, 2),
+                                                     (14, 900, 3, 2), (14, 900, 3, 1), (0, 40, 1, 1), (14, 0, 4, 2)])
+def test_attention_split_forced(grid, prefill, ctas, build):
+    """The length-adaptive split: the first `ctas` CTAs of each KV group run
+    the attention (the others go from the QKV to the combine), forced at 1 ..
+    all 76 CTAs per group of the full grid and at 3 of 7, with the tensor-core
+    build (2) and the lane-parallel one (1); decoding from position 0 with
+    more attention CTAs than positions gives CTAs with empty shares."""
+    tun = mk.tuning(grid_ctas=grid) if grid else None
+    m, dec, orc = make(MID, 79, 2048, gains="normal", std=0.04, tuning=tun)
+    dec.set_debug(mk.MK_DBG_ATTN_BUILD, build)
+    dec.set_debug(mk.MK_DBG_ATTN_CTAS, ctas)
+    if prefill:
+        ks, vs = synth.make_kv(MID, prefill, 83)
+        dec.set_kv(ks, vs, prefill)
+        orc.set_kv(ks, vs, prefill)
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, MID.vocab, 79, 3), prefill, 10)
+    print(grid, prefill, ctas, build, rep.summary())
+    rep.check()
+    dec.close()
+
+
+def test_attention_split_grows_with_context():
+    """By default a step at context ctx runs its attention on
+    ceil(ctx / attn_pos_per_cta) CTAs per KV group: with 7 positions per CTA
+    the count grows from 1 to 6 inside one run from position 0 (the
+    tensor-core build) and from 1 to 3 on the hd=128 shape (lane-parallel)."""
+    m, dec, orc = make(MID, 89, 256, gains="normal", std=0.04, tuning=mk.tuning(grid_ctas=14))
+    assert dec.info.attn_pos_per_cta > 0
+    dec.set_debug(mk.MK_DBG_ATTN_POS_PER_CTA, 7)
+    assert mk.mk_get_info(dec.ctx).attn_pos_per_cta == 7
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, MID.vocab, 89, 3), 0, 40)
+    print(rep.summary())
+    rep.check()
+    dec.close()
+    s = synth.ModelShape(2, 1024, 8, 2, 128, 1536, 4099, 1e-5, 500000.0, False)
+    m, dec, orc = make(s, 97, 256, gains="normal", std=0.03, tuning=mk.tuning(grid_ctas=6))
+    dec.set_debug(mk.MK_DBG_ATTN_POS_PER_CTA, 6)
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, s.vocab, 97, 3), 0, 16)
     print(rep.summary())
     rep.check()
     dec.close()
