@@ -273,6 +273,7 @@ struct mk_ctx {
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
     int trace_detail = 1;
     int inflight = 0, inflight_lat = 0;
+    int stream_tail = 0;
     int pf_lead_tiles = -1, pf_depth = 0;  // L2 warmer (debug knobs; -1 / 0 = defaults)
     int64_t wait_limit_ns = 1000000000LL;
     unsigned long long* trace = nullptr;
@@ -325,6 +326,7 @@ MkParams base_params(const mk_ctx* c) {
     p.trace_detail = c->trace_detail;
     p.inflight = c->inflight > 0 ? c->inflight : 3;
     p.inflight_lat = c->inflight_lat > 0 ? c->inflight_lat : 1;
+    p.stream_tail = c->stream_tail;
     p.pf_lead_bytes = (c->pf_lead_tiles >= 0 ? c->pf_lead_tiles : c->geo.ns) * c->geo.slot;
     p.pf_depth = c->pf_depth > 0 ? c->pf_depth : 1;
     p.wait_limit_ns = c->wait_limit_ns;
@@ -1040,6 +1042,11 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_ATTN_BUILD) {
         if (value < 0 || value > 2 || (value == 2 && !c->kernel_tc)) return MK_ERR_INVALID_ARG;
         c->attn_build = (int)value;
+        return MK_OK;
+    }
+    if (knob == MK_DBG_STREAM_TAIL) {
+        if (value < 0 || value > 2) return MK_ERR_INVALID_ARG;
+        c->stream_tail = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_ATTN_CTAS) {

@@ -213,6 +213,8 @@ struct MkParams {
     int32_t trace_detail;        // with trace: also per-tile and ring-wait slots
     int32_t inflight;            // most tiles in flight per CTA in streaming segments (>= ns: no limit)
     int32_t inflight_lat;        // the same in latency-bound segments
+    int32_t stream_tail;         // where a layer's streaming mode ends: 0 after the down loop, 1 after
+                                 // the FFN-block flag wait, 2 after the next layer's QKV GEMV
     int32_t pf_lead_bytes;       // L2 warmer: bytes past the copy cursor it leaves to the ring
     int32_t pf_depth;            // L2 warmer: tiles of warming loads in flight (1 or 2)
     int64_t wait_limit_ns;

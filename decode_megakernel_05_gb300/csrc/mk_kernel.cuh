@@ -250,12 +250,12 @@ struct Smem {
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + (slot_)] = gtimer();           \
     } while (0)
 
-// Detail marks (trace with detail only): slot 1600 + 8*layer + (ev_), thread 0's
+// Detail marks (trace with detail only): slot 1600 + 16*layer + (ev_), thread 0's
 // time (detail 2: its SM clock instead, and no per-tile records), for the first 24 layers.
 #define MK_TRACE_D(l_, ev_)                                                              \
     do {                                                                                  \
         if (MK_TRACE_ON && p.trace && p.trace_detail && threadIdx.x == 0 && (l_) < 24)    \
-            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1600 + 8 * (l_) + (ev_)] =      \
+            p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + 1600 + 16 * (l_) + (ev_)] =     \
                 p.trace_detail == 2 ? (unsigned long long)clock64() : gtimer();             \
     } while (0)
 
@@ -656,7 +656,7 @@ __device__ void gemv_cfg(GemvCfg& c, int nrows, int TR, int RPP) {
 template <int MR, int LPR, class Epi>
 __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec,
                                              int nrows, int TR, const GemvCfg& cfg, bool ab, Epi&& epi,
-                                             int trace_slot = -1) {
+                                             int trace_slot = -1, int dl = 0, int dmark = -1) {
     constexpr int K = MR * 8 * LPR;
     constexpr int RPP = 32 / LPR;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -675,6 +675,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
         const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
         if (trace_slot >= 0 && MK_TRACE_ON && p.trace && p.trace_detail == 1 && threadIdx.x == 0 && ti < 256)
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
+        if (dmark >= 0 && ti == 0) MK_TRACE_D(dl, dmark);   // thread 0 took its first tile
         if (ok) {
             for (int base = wg * rows_per_warp; base < R; base += wpg * rows_per_warp) {
                 // this lane group's rows: base + sub + k*RPP, k < rw
@@ -682,6 +683,12 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                 const int nv = r0 < R ? min(rw, (R - r0 + RPP - 1) / RPP) : 0;
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
                 if (nv > 0) dot_rows4<MR, LPR>(tile + r0 * rb, rb * RPP, nv, vec, K, ll, v);
+                if (dmark >= 0 && ti == 0 && base == 0) {   // detail trace: the first pass's dot products done
+                    float z = v[0] + v[1] + v[2] + v[3];
+                    asm volatile("" : "+f"(z));
+                    if (z == 12345.f) v[0] += 1.f;
+                    MK_TRACE_D(dl, 13);
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     if (k < rw) {
@@ -694,11 +701,14 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                     for (int k = 0; k < 4; ++k)
                         if (k < nv) epi(ti * TR + r0 + k * RPP, v[k]);
                 }
+                if (dmark >= 0 && ti == 0 && base == 0) MK_TRACE_D(dl, 14);   // its sums handed to epi
             }
         }
         release_tile(p, s, ring, (uint32_t)(MK_NCW / wpg));
+        if (dmark >= 0 && ti == 0) MK_TRACE_D(dl, 15);   // the first tile released
         if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
     }
+    if (dmark >= 0) MK_TRACE_D(dl, dmark + 1);   // thread 0 done with its tiles
     return bar_or(ab);
 }
 
@@ -1241,7 +1251,8 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
 // in smem for the partial.  Returns the uniform abort flag (one barrier).
 template <int HD, int G, int HPL, bool TC>
 __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
-                                         bool has_cur, bool ab, bool late) {
+                                         bool has_cur, bool ab) {
+    bool late = false;
     constexpr float qscale = (HD == 64 ? 0.125f : 0.08838834764831845f) * 1.4426950408889634f;   // log2(e)/sqrt(hd)
     static_assert(HD == 64 || HD == 128, "attention head sizes");
     using A = Attn<HD, G, HPL>;
@@ -1260,8 +1271,24 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
     // split into bf16 high and low parts in the A-fragment words they belong
     // to (qfrag_word).
     constexpr int NQC = G * HD / 2;
+    static_assert(NQC + HD / 4 <= MK_NCT, "q poll and current-row staging side by side");
     float* qs = s.ov();
     uint32_t* qf = reinterpret_cast<uint32_t*>(s.red());
+    // The CTA that also takes the current position stages its K and V rows
+    // (bf16, from their tagged copies) with the threads after the q pollers,
+    // so both polls cost one L2 round trip.
+    if (!ab && has_cur && t >= NQC && t < NQC + HD / 4) {
+        const int u = t - NQC;
+        float kv[8];
+        late = !ll_read8(p, p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (u < HD / 8 ? 0 : 1)) * HD + (u % (HD / 8)) * 8,
+                         s.misc()->tag, kv);
+        uint4 w;
+        w.x = (uint32_t)f2bf(kv[0]) | ((uint32_t)f2bf(kv[1]) << 16);
+        w.y = (uint32_t)f2bf(kv[2]) | ((uint32_t)f2bf(kv[3]) << 16);
+        w.z = (uint32_t)f2bf(kv[4]) | ((uint32_t)f2bf(kv[5]) << 16);
+        w.w = (uint32_t)f2bf(kv[6]) | ((uint32_t)f2bf(kv[7]) << 16);
+        s.misc()->stage[u] = w;
+    }
     if (!ab) {
         const uint32_t tag = s.misc()->tag;
         const uint64_t* qsrc = p.qll + (size_t)l * g.qh * HD + (size_t)pl.g * G * HD;
@@ -1473,6 +1500,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
         ab = gemv_fifo<MH>(p, s, ring, s.xv(), 2 * pl.npairs, g.TRh, ab, s.part());
+        if (t == 0 && p.stream_tail == 2) *(volatile int*)&s.misc()->streaming = 0;
         MK_TRACE(16 * l + 2);
         MK_TRACE_CWAIT(8 * l + 0);
         if (!ab) {
@@ -1507,19 +1535,6 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment B: split-K attention over this CTA's positions
         MK_TRACE_D(l, 7);        // segment B entered
         {
-            // stage K[pos], V[pos] (bf16) from their tagged copies (last attention CTA of the group)
-            bool late = false;
-            if (!ab && ldv(s.misc()->has_cur) && t < HD / 4) {
-                float kv[8];
-                late = !ll_read8(p, p.kvll + (((size_t)l * g.kvh + pl.g) * 2 + (t < HD / 8 ? 0 : 1)) * HD +
-                                        (t % (HD / 8)) * 8, s.misc()->tag, kv);
-                uint4 w;
-                w.x = (uint32_t)f2bf(kv[0]) | ((uint32_t)f2bf(kv[1]) << 16);
-                w.y = (uint32_t)f2bf(kv[2]) | ((uint32_t)f2bf(kv[3]) << 16);
-                w.z = (uint32_t)f2bf(kv[4]) | ((uint32_t)f2bf(kv[5]) << 16);
-                w.w = (uint32_t)f2bf(kv[6]) | ((uint32_t)f2bf(kv[7]) << 16);
-                s.misc()->stage[t] = w;
-            }
             // Blocks of up to KB past positions from the ring (the K tile and
             // the V tile of a block are held together); the last attention
             // CTA of the group appends the current position (staged) to its
@@ -1527,7 +1542,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             // (att is the same for the whole CTA: the barriers inside stay uniform.)
             if (ldv(s.misc()->att))
                 ab = attn_run<HD, G, 1, LC != 0>(p, s, ring, l, ldv(s.misc()->ka), ldv(s.misc()->ke),
-                                                 ldv(s.misc()->has_cur) != 0, ab, late);
+                                                 ldv(s.misc()->has_cur) != 0, ab);
         }
         ab = bar_or(ab);
         constexpr int PSTR = G * HD + 2 * G;                   // tagged words per partial
@@ -1636,6 +1651,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
                 if (ln == 0) s.misc()->alpha[hh] = 1.f / den;
             }
+            MK_TRACE_D(l, 10);   // combine weights done (thread 0)
             bar_or(false);
 #pragma unroll 1
             for (int ps = 0; ps < NPASS && !ab; ++ps) {
@@ -1669,6 +1685,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 }
             }
             if (late) ab = true;      // made uniform by the barrier below
+            MK_TRACE_D(l, 11);   // thread 0's share of o written
         }
         ab = bar_or(ab);
         MK_TRACE(16 * l + 7);
@@ -1678,10 +1695,11 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         ab = gemv_phase_t<MO, LPRO>(p, s, ring, s.ov(), pl.norows, g.TRo, s.misc()->ocfg, ab, [&](int r, float v) {
             if (pl.g == 0) v += s.xres()[r];   // group 0 carries the residual of these rows
             atomicAdd(xo + pl.orow0 + r, v);
-        });
+        }, -1, l, 8);
         MK_TRACE(16 * l + 8);
         MK_TRACE_CWAIT(8 * l + 2);
         if (t == 0 && !ab) arrive(p, mk_cnt_C(g, l), 4 * l + 2);
+        MK_TRACE_D(l, 12);   // attention-block arrival issued
         ab = sync_wait(p, mk_cnt_C(g, l), (uint32_t)g.nC, ab);
         MK_TRACE(16 * l + 9);
 
@@ -1783,7 +1801,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
             }
             MK_TRACE(16 * l + 14);
-            if (t == 0) *(volatile int*)&s.misc()->streaming = 0;
+            if (t == 0 && p.stream_tail == 0) *(volatile int*)&s.misc()->streaming = 0;
             if (l == 3) trace_ring(p, ring, 1);
             // fold the phases: phase q adds what phase q+1 left in xv (element
             // e of chunk c at xv[e * NCH + c]: lane-consecutive, conflict free)
@@ -1830,6 +1848,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE_CWAIT(8 * l + 4);
         if (t == 0 && !ab) arrive(p, mk_cnt_E(g, l), 4 * l + 3);
         ab = sync_wait(p, mk_cnt_E(g, l), (uint32_t)g.nC, ab);
+        if (t == 0 && p.stream_tail == 1) *(volatile int*)&s.misc()->streaming = 0;
         MK_TRACE(16 * l + 13);
     }
 

@@ -37,6 +37,7 @@ MK_DBG_ATTN_BUILD = 10
 MK_DBG_ATTN_TC_MIN = 11
 MK_DBG_ATTN_CTAS = 12
 MK_DBG_ATTN_POS_PER_CTA = 13
+MK_DBG_STREAM_TAIL = 14
 MK_NOALLOC_ARGMAX_BLOCKS = 1024
 MK_NOALLOC_ARGMAX_MAX_N = MK_NOALLOC_ARGMAX_BLOCKS * 4096
 

@@ -272,8 +272,13 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
 #define MK_DBG_TRACE 3
 /* MK_DBG_TRACE_DETAIL: 1 (default) = the trace also records the per-tile and
  * ring-wait slots; 0 = segment ends only (the least perturbed timing); 2 =
- * segment ends, and the attention and combine detail marks as SM clock counts
- * (for durations within a CTA) without the per-tile records. */
+ * segment ends, and the detail marks as SM clock counts (for durations within
+ * a CTA) without the per-tile records.  Detail marks (thread 0, layers < 24)
+ * sit at slot 1600 + 16*layer + m: m = 7 attention segment entered, 0 q polled,
+ * 1 q ready for every warp, 5 first K/V block taken, 6 its scores done, 2 all
+ * blocks done, 3 first partials seen, 4 every thread's first partials seen,
+ * 10 combine weights done, 11 its share of o written, 8 first O-proj tile
+ * taken, 9 O-proj tiles done, 12 attention-block arrival issued. */
 #define MK_DBG_TRACE_DETAIL 5
 /* MK_DBG_INFLIGHT: value = most weight tiles each CTA keeps in flight (issued,
  * not yet landed) at once during the streaming segments, 1..16 (0 = the
@@ -307,6 +312,10 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
  * (1 .. max_seq; the default is mk_info.attn_pos_per_cta). */
 #define MK_DBG_ATTN_CTAS 12
 #define MK_DBG_ATTN_POS_PER_CTA 13
+/* MK_DBG_STREAM_TAIL: where a layer's streaming segment (the copy producer's
+ * larger in-flight limit) ends: 0 (default) after the down projection's tiles,
+ * 1 after the FFN-block flag wait, 2 after the next layer's QKV GEMV. */
+#define MK_DBG_STREAM_TAIL 14
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
 const char* mk_strerror(int code);
