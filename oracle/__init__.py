@@ -77,6 +77,9 @@ def lib():
             L.oracle_sample_f32.argtypes = [_P, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_int,
                                             ctypes.POINTER(ctypes.c_int)]
             L.oracle_sample_f32.restype = ctypes.c_int
+            L.oracle_sample_topp_f32.argtypes = [_P, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_uint64,
+                                                 ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+            L.oracle_sample_topp_f32.restype = ctypes.c_int
             for f in (L.oracle_rmsnorm, L.oracle_gemv, L.oracle_rope, L.oracle_softmax, L.oracle_attention_head):
                 f.restype = None
             _lib = L
@@ -165,6 +168,16 @@ def sample_f32(logits, inv_temp: float, seed: int, pos: int):
     nf = ctypes.c_int(0)
     idx = lib().oracle_sample_f32(pl, lg.size, ctypes.c_float(inv_temp), ctypes.c_uint64(seed), int(pos),
                                   ctypes.byref(nf))
+    return idx, bool(nf.value)
+
+
+def sample_topp_f32(logits, inv_temp: float, top_p: float, seed: int, pos: int):
+    """(token, any non-finite logit): Gumbel-max sample of softmax(logits * inv_temp) restricted to
+    the nucleus {v : mass of the tokens strictly more probable than v < top_p}; top_p >= 1 keeps all."""
+    lg, pl = _c(logits, np.float64)
+    nf = ctypes.c_int(0)
+    idx = lib().oracle_sample_topp_f32(pl, lg.size, ctypes.c_float(inv_temp), ctypes.c_double(top_p),
+                                       ctypes.c_uint64(seed), int(pos), ctypes.byref(nf))
     return idx, bool(nf.value)
 
 

@@ -213,6 +213,65 @@ int oracle_sample_f32(const double* logits, int n, float inv_temp, uint64_t seed
     return best;
 }
 
+/* Nucleus (top-p) sampling (cloud.baidu.com/article/9434380, section 5,
+ * step 1 names top-p beside the temperature as a fixed sampling parameter;
+ * the page gives no rule, the one taken is the usual nucleus restriction made
+ * independent of how ties are ordered): with x_v = float(logit_v) * (1/T) in
+ * float and probabilities q_v = exp(x_v - max x) / sum_u exp(x_u - max x) in
+ * double, token v is kept iff the probability of the tokens strictly more
+ * probable than it is below p:  sum_{u : x_u > x_v} q_u < p.  The token is
+ * then the Gumbel-max choice (as oracle_sample_f32) over the kept tokens only,
+ * which samples from softmax(x) restricted to the kept set and renormalised.
+ * top_p >= 1 keeps every token; inv_temp <= 0 is greedy.  Plain O(n log n):
+ * sort by x descending and accumulate the mass of each group of equal x. */
+static const float* g_sort_x;
+static int cmp_x_desc(const void* a, const void* b) {
+    const float xa = g_sort_x[*(const int*)a], xb = g_sort_x[*(const int*)b];
+    return (xa < xb) - (xa > xb);
+}
+
+int oracle_sample_topp_f32(const double* logits, int n, float inv_temp, double top_p, uint64_t seed, int pos,
+                           int* nonfinite) {
+    if (!(inv_temp > 0.0f) || !(top_p < 1.0)) return oracle_sample_f32(logits, n, inv_temp, seed, pos, nonfinite);
+    float* x = (float*)malloc(sizeof(float) * (size_t)n);
+    int* idx = (int*)malloc(sizeof(int) * (size_t)n);
+    unsigned char* keep = (unsigned char*)calloc((size_t)n, 1);
+    int m = 0;
+    *nonfinite = 0;
+    for (int v = 0; v < n; ++v) {
+        const float y = (float)logits[v];
+        if (!isfinite(y)) { *nonfinite = 1; continue; }
+        x[v] = y * inv_temp;
+        idx[m++] = v;
+    }
+    int best = -1;
+    if (m > 0) {
+        g_sort_x = x;
+        qsort(idx, (size_t)m, sizeof(int), cmp_x_desc);
+        const double xmax = (double)x[idx[0]];
+        double z = 0.0;
+        for (int k = 0; k < m; ++k) z += exp((double)x[idx[k]] - xmax);
+        double above = 0.0;                      /* mass of the tokens strictly more probable */
+        for (int k = 0; k < m;) {
+            int e = k;
+            double grp = 0.0;
+            while (e < m && x[idx[e]] == x[idx[k]]) { grp += exp((double)x[idx[e]] - xmax); ++e; }
+            const int kept = above < top_p * z;
+            for (int q = k; q < e; ++q) keep[idx[q]] = (unsigned char)kept;
+            above += grp;
+            k = e;
+        }
+        float bk = 0.0f;
+        for (int v = 0; v < n; ++v) {
+            if (!keep[v]) continue;
+            const float key = fmaf((float)logits[v], inv_temp, oracle_gumbel_f32(seed, pos, v));
+            if (best < 0 || key > bk) { best = v; bk = key; }
+        }
+    }
+    free(x); free(idx); free(keep);
+    return best;
+}
+
 /* One decode step: feed `token` at position `pos`, append its K/V to the
  * cache, return logits [vocab] and the final-norm hidden state [hidden].
  * kcache / vcache: bf16 [n_layers][n_kv_heads][max_seq][head_dim]; positions

@@ -31,6 +31,8 @@ MUTATIONS = {
     "residual_dropped": ("for (int i = 0; i < H; ++i) x[i] += o[i];\n        /* segment C",
                          "for (int i = 0; i < H; ++i) x[i] = o[i];\n        /* segment C"),
     "gate_up_swapped": ("u[j] = oracle_silu(gate[j]) * up[j];", "u[j] = oracle_silu(up[j]) * gate[j];"),
+    "topp_own_mass_included": ("const int kept = above < top_p * z;", "const int kept = above + grp < top_p * z;"),
+    "topp_untempered": ("x[v] = y * inv_temp;", "x[v] = y;"),
 }
 
 

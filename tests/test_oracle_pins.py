@@ -416,3 +416,60 @@ def test_sampling_limits_and_special_values():
     tok, nf = oracle.sample_f32(bad, 1.0, 3, 0)
     assert nf and tok != greedy
     assert oracle.sample_f32(np.full(4, np.inf), 1.0, 3, 0) == (-1, True)   # no finite logit
+
+
+# ---------------------------------------------------------------- top-p (nucleus) sampling
+
+def _draw_counts(logits, inv, top_p, n, seed=77):
+    counts = np.zeros(len(logits))
+    for k in range(n):
+        tok, nf = oracle.sample_topp_f32(logits, inv, top_p, seed, k)
+        assert not nf
+        counts[tok] += 1
+    return counts
+
+
+@pytest.mark.parametrize("temperature,top_p,expect", [
+    # q = [0.5, 0.3, 0.15, 0.05]: mass strictly above each token 0, 0.5, 0.8, 0.95
+    (1.0, 0.7, [0.5 / 0.8, 0.3 / 0.8, 0.0, 0.0]),
+    (1.0, 0.81, [0.5 / 0.95, 0.3 / 0.95, 0.15 / 0.95, 0.0]),
+    # T = 0.5 squares the probabilities: q' = [0.25, 0.09, 0.0225, 0.0025] / 0.365, mass above
+    # token 2 = 0.34 / 0.365 = 0.9315 >= 0.9 (untempered it would be 0.8 < 0.9 and token 2 kept)
+    (0.5, 0.9, [0.25 / 0.34, 0.09 / 0.34, 0.0, 0.0]),
+])
+def test_topp_draws_follow_the_truncated_renormalised_softmax(temperature, top_p, expect):
+    """Closed-form nucleus: logits ln q with q known, so the kept set and the
+    renormalised distribution are worked out by hand (comments); 30 000 draws
+    must match it (chi-square) and never leave the kept set."""
+    logits = np.log(np.array([0.5, 0.3, 0.15, 0.05]))
+    inv = float(np.float32(1.0 / temperature))
+    n = 30000
+    counts = _draw_counts(logits, inv, top_p, n)
+    expect = np.array(expect)
+    assert np.all(counts[expect == 0] == 0), counts
+    kept = expect > 0
+    chi2 = float(np.sum((counts[kept] - n * expect[kept]) ** 2 / (n * expect[kept])))
+    assert chi2 < 13.8, (chi2, counts / n, expect)   # at most 2 degrees of freedom, p = 0.001
+
+
+def test_topp_ties_and_limits():
+    # two tokens tie for the top: each has no mass strictly above it, so both are kept
+    logits = np.array([1.0, 1.0, 0.0, -5.0])
+    counts = _draw_counts(logits, 1.0, 0.1, 20000)
+    assert counts[2] == 0 and counts[3] == 0
+    assert abs(counts[0] / 20000 - 0.5) < 0.02
+    # top_p >= 1 keeps every token: the same draws as plain sampling
+    rng = np.random.default_rng(6)
+    lg = rng.normal(size=40)
+    for pos in range(100):
+        assert oracle.sample_topp_f32(lg, 0.8, 1.0, 5, pos)[0] == oracle.sample_f32(lg, 0.8, 5, pos)[0]
+    # a tiny nucleus holds only the most probable token
+    top = int(np.argmax(lg))
+    assert all(oracle.sample_topp_f32(lg, 1.0, 1e-9, 5, pos)[0] == top for pos in range(50))
+    # temperature <= 0 stays greedy whatever top_p is
+    assert oracle.sample_topp_f32(lg, 0.0, 0.5, 5, 3)[0] == top
+    # non-finite logits are skipped and flagged
+    bad = lg.copy()
+    bad[top] = np.nan
+    tok, nf = oracle.sample_topp_f32(bad, 1.0, 0.9, 5, 0)
+    assert nf and tok != top
