@@ -268,6 +268,9 @@ struct mk_ctx {
     unsigned long long* amax = nullptr;
     int32_t *next_token = nullptr, *tokens_dev = nullptr, *prompt_dev = nullptr;
     int32_t* stop = nullptr;             // generation stopped (mk_generate with a stop token)
+    float* lgs = nullptr;                // [V] logits scratch of top-p steps
+    MkTopP* tp = nullptr;                // top-p threshold-search scratch
+    float top_p = 1.f;                   // nucleus mass of sampled steps (mk_set_top_p); 1 = every token
     uint32_t* status_host = nullptr;     // pinned copy of the status word (read behind generate calls)
     // debug
     int dbg_skip_cta = -1, dbg_skip_sync = -1;
@@ -332,6 +335,9 @@ MkParams base_params(const mk_ctx* c) {
     p.wait_limit_ns = c->wait_limit_ns;
     p.trace = c->trace;
     p.out_idx = 0;
+    p.top_p = 1.f;   // sampled steps set the context's value
+    p.lgs = c->lgs;
+    p.tp = c->tp;
     return p;
 }
 
@@ -540,7 +546,8 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         (rc = c->dalloc(&c->cnt, (size_t)mk_cnt_total(g) * 4)) || (rc = c->dalloc(&c->status, 4)) ||
         (rc = c->dalloc(&c->seq, 4)) || (rc = c->dalloc(&c->amax, 8)) || (rc = c->dalloc(&c->next_token, 4)) ||
         (rc = c->dalloc(&c->tokens_dev, (size_t)g.max_seq * 4)) ||
-        (rc = c->dalloc(&c->prompt_dev, (size_t)g.max_seq * 4)) || (rc = c->dalloc(&c->stop, 4)))
+        (rc = c->dalloc(&c->prompt_dev, (size_t)g.max_seq * 4)) || (rc = c->dalloc(&c->stop, 4)) ||
+        (rc = c->dalloc(&c->lgs, V * 4)) || (rc = c->dalloc(&c->tp, sizeof(MkTopP))))
         return fail(rc);
     if ((e = cudaHostAlloc(reinterpret_cast<void**>(&c->status_host), 4, cudaHostAllocDefault)) != cudaSuccess)
         return fail(cuda_fail(e, "cudaHostAlloc"));
@@ -552,7 +559,7 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         (e = cudaMemset(c->kvll, 0, kvll_bytes)) || (e = cudaMemset(c->partll, 0, partll_bytes)) || (e = cudaMemset(c->cnt, 0, (size_t)mk_cnt_total(g) * 4)) ||
         (e = cudaMemset(c->status, 0, 4)) || (e = cudaMemset(c->seq, 0, 4)) || (e = cudaMemset(c->amax, 0, 8)) ||
         (e = cudaMemset(c->next_token, 0, 4)) || (e = cudaMemset(c->tokens_dev, 0, (size_t)g.max_seq * 4)) ||
-        (e = cudaMemset(c->stop, 0, 4)))
+        (e = cudaMemset(c->stop, 0, 4)) || (e = cudaMemset(c->tp, 0, sizeof(MkTopP))))
         return fail(cuda_fail(e, "context init"));
     if ((e = mk_launch_rope_table(c->rope_cos, c->rope_sin, g.max_seq, g.hd, (double)cfg->rope_theta, st)) ||
         (e = cudaDeviceSynchronize()))
@@ -878,6 +885,7 @@ int mk_decode_step_sample(mk_ctx* c, int32_t token, int32_t pos, float temperatu
     p.logits = logits_out;
     p.tokens_out = nullptr;
     p.inv_temp = temperature > 0.f ? 1.0f / temperature : 0.f;
+    p.top_p = c->top_p;
     p.seed = seed;
     return launch_step(c, p, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -904,6 +912,7 @@ int mk_generate(mk_ctx* c, const int32_t* prompt, int32_t n_prompt, int32_t star
         p.tokens_out = (k >= n_prompt - 1) ? c->tokens_dev : nullptr;
         p.out_idx = (int32_t)(k - (n_prompt - 1));
         p.inv_temp = inv_temp;
+        p.top_p = c->top_p;
         p.seed = seed;
         p.eos_id = eos_id;
         p.stop = eos_id >= 0 ? c->stop : nullptr;
@@ -922,6 +931,12 @@ int mk_generate(mk_ctx* c, const int32_t* prompt, int32_t n_prompt, int32_t star
     for (int32_t i = n; i < n_new; ++i) out_tokens[i] = -1;
     if (n_out) *n_out = n;
     return dev;
+}
+
+int mk_set_top_p(mk_ctx* c, float top_p) {
+    if (!c || !(top_p > 0.f) || !(top_p <= 1.f)) return MK_ERR_INVALID_ARG;
+    c->top_p = top_p;
+    return MK_OK;
 }
 
 int mk_get_hidden(mk_ctx* c, float* out, void* stream) {

@@ -50,6 +50,19 @@
 // chunk and the combine waits on fewer partials.
 #define MK_ATTN_POS_PER_CTA 192
 
+// Top-p sampling inside the launch: rounds of the 33-way bisection for the
+// nucleus threshold (each one grid-wide reduction of 33 masses); the boundary
+// is resolved to 104 / 32^MK_TP_ITERS in logit / temperature.
+#define MK_TP_ITERS 7
+#define MK_TP_BINS 33
+
+// Global scratch of the top-p threshold search, zeroed by the launch's last
+// CTA after a top-p step (and once at context creation).
+struct MkTopP {
+    unsigned long long mkey;               // packed maximum of logit / temperature
+    float hist[MK_TP_ITERS][MK_TP_BINS];   // per round: mass of each candidate interval
+};
+
 // Device status word bits.
 #define MK_ST_TIMEOUT 0x1u
 #define MK_ST_NUMERIC 0x2u
@@ -209,6 +222,9 @@ struct MkParams {
     uint64_t seed;               // noise generator seed
     int32_t eos_id;              // with stop: a generated token equal to it sets *stop
     int32_t* stop;               // nullptr, or a flag that makes every later launch return at once
+    float top_p;                 // nucleus mass (sampling only); >= 1 keeps every token
+    float* lgs;                  // [V] logits scratch of a top-p step
+    MkTopP* tp;                  // threshold-search scratch of a top-p step
     int32_t dbg_skip_cta, dbg_skip_sync;
     int32_t trace_detail;        // with trace: also per-tile and ring-wait slots
     int32_t inflight;            // most tiles in flight per CTA in streaming segments (>= ns: no limit)
@@ -231,7 +247,9 @@ MK_HD int mk_cnt_A(const MkGeom& g, int l, int grp) { return l * g.kvh + grp; }
 MK_HD int mk_cnt_B(const MkGeom& g, int l, int grp) { return g.L * g.kvh + l * g.kvh + grp; }
 MK_HD int mk_cnt_C(const MkGeom& g, int l) { return 2 * g.L * g.kvh + l; }
 MK_HD int mk_cnt_E(const MkGeom& g, int l) { return 2 * g.L * g.kvh + g.L + l; }
-MK_HD int mk_cnt_done(const MkGeom& g) { return 2 * g.L * g.kvh + 2 * g.L; }
+// grid-wide syncs of a top-p step's threshold search: k < MK_TP_ITERS + 1
+MK_HD int mk_cnt_tp(const MkGeom& g, int k) { return 2 * g.L * g.kvh + 2 * g.L + k; }
+MK_HD int mk_cnt_done(const MkGeom& g) { return 2 * g.L * g.kvh + 2 * g.L + MK_TP_ITERS + 1; }
 MK_HD int mk_cnt_total(const MkGeom& g) { return mk_cnt_done(g) + 1; }
 
 // Per-CTA plan; stream offsets are filled by the caller.

@@ -886,6 +886,26 @@ __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, 
     return bar_or(ab);
 }
 
+// Grid-wide barrier on counter idx: every CTA's writes before it (made
+// visible by the consumer barrier and the release arrival) are seen by every
+// CTA after it.  Returns the uniform abort flag.
+__device__ __forceinline__ bool grid_sync(const MkParams& p, int idx, bool ab) {
+    ab = bar_or(ab);
+    if (threadIdx.x == 0 && !ab) red_release_add(p.cnt + idx, 1u);
+    bool bad = ab;
+    if (threadIdx.x == 0 && !bad) bad = !wait_counter(p, p.cnt + idx, (uint32_t)p.geo.nC);
+    return bar_or(bad);
+}
+
+// Order-preserving 32-bit key of a float (larger float -> larger key).
+__device__ __forceinline__ uint32_t f2key(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Thread 0 waits on a counter; the result is made uniform by the barrier.
 __device__ __forceinline__ bool sync_wait(const MkParams& p, int idx, uint32_t target, bool abort_in) {
     bool bad = abort_in;
@@ -1863,21 +1883,105 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         float bv = -INFINITY;
         int bi = -1;
         bool nonfinite = false;
+        // top-p: the logits go to scratch and the phase only finds max(logit / T)
+        const bool topp = p.inv_temp > 0.f && p.top_p < 1.f;
         ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv(), pl.nv, g.TRh, s.misc()->lmcfg, ab, [&](int r, float lg) {
             const int v = pl.v0 + r;
             if (p.logits) p.logits[v] = lg;
             if (isfinite(lg)) {
-                // greedy: the logit; sampling: logit / T plus this token's Gumbel noise
-                // (inline behind a uniform branch: measured the cheapest form for greedy steps)
-                const float key = p.inv_temp > 0.f ? fmaf(lg, p.inv_temp, mk_gumbel(p.seed, p.pos, v)) : lg;
-                if (key > bv || (key == bv && v < bi)) { bv = key; bi = v; }
+                if (topp) {
+                    p.lgs[v] = lg;
+                    bv = fmaxf(bv, lg * p.inv_temp);
+                } else {
+                    // greedy: the logit; sampling: logit / T plus this token's Gumbel noise
+                    // (inline behind a uniform branch: measured the cheapest form for greedy steps)
+                    const float key = p.inv_temp > 0.f ? fmaf(lg, p.inv_temp, mk_gumbel(p.seed, p.pos, v)) : lg;
+                    if (key > bv || (key == bv && v < bi)) { bv = key; bi = v; }
+                }
             } else {
+                if (topp) p.lgs[v] = lg;
                 nonfinite = true;
             }
         }, 2048);
         MK_TRACE(16 * L + 1);
         MK_TRACE_CWAIT(8 * L + 5);
         if (nonfinite) atomicOr(p.status, MK_ST_NUMERIC);
+        if (topp) {
+            // Nucleus (cloud.baidu.com/article/9434380, section 5, step 1: top-p
+            // beside the temperature): with x = logit / T, keep the tokens whose
+            // strictly more probable tokens carry less than p of the mass, then
+            // Gumbel-max among them.  The threshold is found by bisection on x:
+            // the interval (lo, hi] holds it, with mass(x > lo) >= p Z and
+            // mass(x > hi) < p Z; each round splits it at 32 candidates, every
+            // CTA adds the exp(x - M) of its logits into the 33 intervals, the
+            // sums meet in global memory across a grid-wide barrier, and every
+            // CTA keeps the sub-interval where the mass above crosses p Z.  After
+            // MK_TP_ITERS rounds the kept tokens are those with x > lo.
+            float* hs = s.red();                  // [0, 33) interval masses; [40..42] lo, hi, pZ
+            if ((t & 31) == 0) s.misc()->best_val[t >> 5] = bv;
+            ab = bar_or(ab);
+            if (t == 0 && !ab) {
+                float m = -INFINITY;
+                for (int i = 0; i < MK_NCW; ++i) m = fmaxf(m, s.misc()->best_val[i]);
+                if (m != -INFINITY) atomicMax(&p.tp->mkey, (unsigned long long)f2key(m));
+            }
+            ab = grid_sync(p, mk_cnt_tp(g, 0), ab);
+            const unsigned long long mk_ = __ldcg(&p.tp->mkey);
+            const float M = mk_ ? key2f((uint32_t)mk_) : 0.f;
+            if (t == 0) { hs[40] = M - 104.f; hs[41] = M; hs[42] = 0.f; }
+            for (int it = 0; it < MK_TP_ITERS && !ab; ++it) {
+                if (t < MK_TP_BINS) hs[t] = 0.f;
+                ab = bar_or(ab);
+                const float lo = hs[40], hi = hs[41], w = (hi - lo) * (1.f / 32.f);
+                for (int r = t; r < pl.nv; r += MK_NCT) {
+                    const float y = __ldcg(p.lgs + pl.v0 + r);
+                    const float x = y * p.inv_temp;
+                    if (!isfinite(y) || !(x > lo)) continue;
+                    // interval b: tau_b < x <= tau_b+1, tau_k = lo + k w (tau_32 = hi); 32: x > hi
+                    int b = 32;
+                    if (!(x > hi)) {
+                        b = min(31, max(0, (int)((x - lo) / w)));
+                        while (b > 0 && !(fmaf(w, (float)b, lo) < x)) --b;
+                        while (b < 31 && fmaf(w, (float)(b + 1), lo) < x) ++b;
+                    }
+                    atomicAdd(&hs[b], exp2f((x - M) * 1.4426950408889634f));
+                }
+                ab = bar_or(ab);
+                if (t < MK_TP_BINS && !ab && hs[t] != 0.f) atomicAdd(&p.tp->hist[it][t], hs[t]);
+                ab = grid_sync(p, mk_cnt_tp(g, it + 1), ab);
+                if (t == 0 && !ab) {
+                    // C_k = mass(x > tau_k) = sum of intervals k .. 32
+                    float cs[MK_TP_BINS];
+                    float cum = 0.f;
+                    for (int k = MK_TP_BINS - 1; k >= 0; --k) { cum += __ldcg(&p.tp->hist[it][k]); cs[k] = cum; }
+                    float pz = hs[42];
+                    if (it == 0) { pz = p.top_p * cs[0]; hs[42] = pz; }
+                    int ks = 0;                       // the last candidate with mass above >= p Z
+                    for (int k = 31; k > 0; --k) if (cs[k] >= pz) { ks = k; break; }
+                    hs[40] = ks == 0 ? lo : fmaf(w, (float)ks, lo);
+                    hs[41] = ks == 31 ? hi : fmaf(w, (float)(ks + 1), lo);
+                }
+                ab = bar_or(ab);
+            }
+            // Gumbel-max over the kept tokens
+            const float lo = hs[40];
+            bv = -INFINITY;
+            bi = -1;
+            for (int r = t; r < pl.nv; r += MK_NCT) {
+                const int v = pl.v0 + r;
+                const float y = __ldcg(p.lgs + v);
+                if (!isfinite(y) || !(y * p.inv_temp > lo)) continue;
+                const float key = fmaf(y, p.inv_temp, mk_gumbel(p.seed, p.pos, v));
+                if (key > bv || (key == bv && v < bi)) { bv = key; bi = v; }
+            }
+            // the thread's best into lane 0 of its warp (as the phase above leaves it)
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+                if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) { bv = ov; bi = oi; }
+            }
+        }
         if ((t & 31) == 0) { s.misc()->best_val[t >> 5] = bv; s.misc()->best_idx[t >> 5] = bi; }
         ab = bar_or(ab);
         if (t == 0 && !ab) {
@@ -1919,6 +2023,11 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             if (p.tokens_out) p.tokens_out[p.out_idx] = tok;
             if (p.stop && p.tokens_out && tok == p.eos_id) *p.stop = 1;   // generated the stop token
             *p.amax = 0ull;
+            if (p.inv_temp > 0.f && p.top_p < 1.f) {
+                p.tp->mkey = 0ull;
+                for (int k = 0; k < MK_TP_ITERS; ++k)
+                    for (int b = 0; b < MK_TP_BINS; ++b) p.tp->hist[k][b] = 0.f;
+            }
             p.cnt[ntot] = 0u;
             atomicAdd(p.seq, 1u);
             atomicAnd(p.status, ~MK_ST_ABORT);

@@ -89,6 +89,10 @@ class Decoder:
         mk.mk_decode_step_sample(self.ctx, int(token), int(pos), float(temperature), int(seed), ptr, self.stream)
         return self.logits if logits else None
 
+    def set_top_p(self, top_p: float):
+        """Nucleus mass of the sampled steps from now on (1 = every token)."""
+        mk.mk_set_top_p(self.ctx, float(top_p))
+
     def step_perop(self, token: int, pos: int, logits=True) -> int:
         ptr = self.logits.data_ptr() if logits else None
         return mk.mk_decode_step_perop(self.ctx, int(token), int(pos), ptr, self.stream)

@@ -78,6 +78,7 @@ SIGNATURES = [
     ("mk_decode_step_greedy", _i32, [_P, _i32, _P, _P]),
     ("mk_generate_greedy", _i32, [_P, _P, _i32, _i32, _i32, _P, _P]),
     ("mk_decode_step_sample", _i32, [_P, _i32, _i32, ctypes.c_float, ctypes.c_uint64, _P, _P]),
+    ("mk_set_top_p", _i32, [_P, ctypes.c_float]),
     ("mk_generate", _i32, [_P, _P, _i32, _i32, _i32, ctypes.c_float, ctypes.c_uint64, _i32, _P, _P, _P]),
     ("mk_get_hidden", _i32, [_P, _P, _P]),
     ("mk_get_argmax", _i32, [_P, _P, _P]),
@@ -207,6 +208,10 @@ def mk_generate_greedy(ctx: int, prompt_ptr: int, n_prompt: int, start_pos: int,
 def mk_decode_step_sample(ctx: int, token: int, pos: int, temperature: float, seed: int, logits_ptr: int | None,
                           stream: int = 0) -> None:
     check(load().mk_decode_step_sample(ctx, token, pos, temperature, seed, logits_ptr, stream), "mk_decode_step_sample")
+
+
+def mk_set_top_p(ctx: int, top_p: float) -> None:
+    check(load().mk_set_top_p(ctx, top_p), "mk_set_top_p")
 
 
 def mk_generate(ctx: int, prompt_ptr: int, n_prompt: int, start_pos: int, n_new: int, temperature: float, seed: int,

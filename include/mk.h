@@ -182,13 +182,24 @@ int mk_generate_greedy(mk_ctx* ctx, const int32_t* prompt, int32_t n_prompt, int
  * U_v = ((z >> 41) + 0.5) * 2^-23 with z output i = pos * 2^32 + v of
  * SplitMix64 seeded with `seed` in its counter form, mix(seed + (i + 1) *
  * 0x9E3779B97F4A7C15) (Steele, Lea and Flood, OOPSLA 2014).  temperature <= 0
- * is greedy.  Top-p is not supported.
+ * is greedy.  With a top-p below 1 (mk_set_top_p) the Gumbel-max runs over the
+ * nucleus only: with x_v = logit_v * (1/temperature), token v is kept iff the
+ * tokens with a larger x carry less than top_p of softmax(x)'s mass (tied
+ * tokens are kept or dropped together), which samples from softmax(x)
+ * restricted to the nucleus and renormalised.  The threshold is found inside
+ * the same launch (a bisection on x over grid-wide reductions, 8 of them; the
+ * boundary is resolved to 104 / 32^7 in x, and the masses are fp32 sums).
  *
  * One sampled step: as mk_decode_step, fed `token` (0..V-1), or with token =
  * -1 the previous step's chosen token from device memory.  The chosen token
  * is left on the device (mk_get_argmax).  Asynchronous. */
 int mk_decode_step_sample(mk_ctx* ctx, int32_t token, int32_t pos, float temperature, uint64_t seed,
                           float* logits_out, void* stream);
+
+/* Nucleus mass of the sampled steps of this context (mk_decode_step_sample,
+ * mk_generate with temperature > 0) from now on: 0 < top_p <= 1, 1 (the
+ * default) keeps every token.  Anything else returns MK_ERR_INVALID_ARG. */
+int mk_set_top_p(mk_ctx* ctx, float top_p);
 
 /* Generation with sampling and a stop token: as mk_generate_greedy, with the
  * tokens chosen as in mk_decode_step_sample.  With eos_id >= 0, generation

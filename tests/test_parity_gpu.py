@@ -372,3 +372,87 @@ def test_generate_with_sampling_and_stop_token():
     rc, got, n = dec.generate(prompt, 0, n_new, temperature, seed)
     assert rc == 0 and n == n_new and list(got) == want
     dec.close()
+
+
+def _nucleus_bounds(lg_ref, inv, top_p, dl):
+    """Loose and strict nucleus of the oracle's logits: the GPU decides membership
+    from logits within dl of the oracle's (x within dl/T) with fp32 sums, so near
+    the boundary either decision is valid.  Returns (loose set, strict set)."""
+    x = lg_ref.astype(np.float32) * np.float32(inv)
+    e = np.exp(x.astype(np.float64) - float(x.max()))
+    z = e.sum()
+    order = np.argsort(-x, kind="stable")
+    xs, es = x[order], e[order]
+    above = np.zeros(len(x))
+    acc, k = 0.0, 0
+    while k < len(xs):
+        j = k
+        while j < len(xs) and xs[j] == xs[k]:
+            j += 1
+        above[order[k:j]] = acc
+        acc += es[k:j].sum()
+        k = j
+    slack = top_p * (np.exp(2.0 * dl * inv) - 1.0) + 1e-4
+    return set(np.nonzero(above < (top_p + slack) * z)[0]), set(np.nonzero(above < (top_p - slack) * z)[0])
+
+
+@pytest.mark.parametrize("temperature,top_p", [(1.0, 0.9), (0.2, 0.5)])
+def test_topp_sampling_matches_oracle(temperature, top_p):
+    """Top-p inside the launch (H=512 shape, V = 5003): the fused choice equals
+    the oracle's nucleus sample from its own logits, except where the nucleus
+    boundary or the top two keys sit within the logit error (both choices
+    valid); the chosen token is always inside the loosened nucleus and no key
+    of the tightened nucleus beats it."""
+    m, dec, orc = make(MID, 67, 256, gains="normal", std=0.04)
+    dec.set_top_p(top_p)
+    inv = float(np.float32(1.0 / temperature))
+    seed = 0x70B0 + int(100 * top_p)
+    tok, agree, steps = 11, 0, 24
+    for pos in range(steps):
+        dec.step_sample(tok, pos, temperature, seed, logits=True)
+        lg_ref, _ = orc.step(tok, pos)
+        lg = dec.logits.cpu().numpy().astype(np.float64)
+        got = dec.get_argmax()
+        want, nf = oracle.sample_topp_f32(lg_ref, inv, top_p, seed, pos)
+        assert not nf
+        dl = float(np.max(np.abs(lg - lg_ref)))
+        assert dl <= 5e-2
+        if got == want:
+            agree += 1
+        else:
+            loose, strict = _nucleus_bounds(lg_ref, inv, top_p, dl)
+            keys = _oracle_keys(lg_ref, inv, seed, pos)
+            assert got in loose, (pos, got, want)
+            assert keys[got] >= max(keys[v] for v in strict) - (2 * dl * inv + 1e-5), (pos, got, want)
+        tok = want
+    assert agree >= steps - 2, agree
+    assert dec.status() == 0
+    dec.close()
+
+
+def test_topp_tiny_nucleus_then_back_to_plain_sampling():
+    """A nucleus of 1e-6 of the mass holds only the most probable token, so the
+    sampled token is the argmax of the step's own logits; setting top_p back to
+    1 then samples as without it (the oracle's plain Gumbel-max choice, near
+    ties allowed); out-of-range values are refused."""
+    m, dec, orc = make(MID, 71, 64, gains="normal", std=0.04)
+    inv = float(np.float32(1.0 / 0.8))
+    dec.set_top_p(1e-6)
+    for pos in range(6):
+        lg = dec.step_sample(5 + pos, pos, 0.8, 4242, logits=True).cpu().numpy()
+        orc.step(5 + pos, pos)
+        assert dec.get_argmax() == int(np.argmax(lg))
+    dec.set_top_p(1.0)
+    for pos in range(6, 12):
+        lg = dec.step_sample(5 + pos, pos, 0.8, 4242, logits=True).cpu().numpy().astype(np.float64)
+        lg_ref, _ = orc.step(5 + pos, pos)
+        got, (want, _) = dec.get_argmax(), oracle.sample_f32(lg_ref, inv, 4242, pos)
+        if got != want:
+            dl = float(np.max(np.abs(lg - lg_ref)))
+            keys = np.sort(_oracle_keys(lg_ref, inv, 4242, pos))
+            assert keys[-1] - keys[-2] <= 2 * dl * inv + 1e-5, (pos, got, want)
+    lib = mk.load()
+    for bad in (0.0, -0.5, 1.5, float("nan")):
+        assert lib.mk_set_top_p(dec.ctx, bad) == mk.MK_ERR_INVALID_ARG
+    assert dec.status() == 0
+    dec.close()
