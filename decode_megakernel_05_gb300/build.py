@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmk.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["mk_api.cu", "mk_aux.cu", "mk_perop.cu", "mk_noalloc.cu"]
+SOURCES = ["mk_api.cu", "mk_aux.cu", "mk_perop.cu", "mk_prefill.cu", "mk_noalloc.cu"]
 # (head_dim, query heads per KV group, hidden / 256) of the fused kernel, one
 # object each; keep in sync with MK_VARIANTS in csrc/mk_api.cu
 VARIANTS = [(64, 2, 1), (64, 4, 2), (64, 4, 4), (64, 4, 8), (64, 4, 16), (128, 4, 4), (128, 4, 8), (128, 4, 16)]

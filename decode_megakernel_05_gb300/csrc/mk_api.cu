@@ -13,6 +13,7 @@
 #include "mk_aux.h"
 #include "mk_internal.h"
 #include "mk_perop.h"
+#include "mk_prefill.h"
 
 // One object per kernel variant: mk_kernel.cu compiled with -DMK_HD_V=<head_dim>
 // -DMK_G_V=<q heads per kv head> -DMK_MH_V=<hidden / 256> (-DMK_LC_V=1 for the
@@ -283,6 +284,9 @@ struct mk_ctx {
     // per-operator baseline
     bool perop_enabled = false, perop_ready = false;
     MkPerOp perop{};
+    // batched prefill workspace (rows of capacity pf_rows), grown on demand
+    int pf_rows = 0;
+    float *pf_x = nullptr, *pf_xn = nullptr, *pf_qkv = nullptr, *pf_att = nullptr, *pf_gu = nullptr, *pf_u = nullptr;
 
     template <class T>
     int dalloc(T** p, size_t bytes) {
@@ -572,6 +576,8 @@ void mk_destroy(mk_ctx* c) {
     if (!c) return;
     cudaSetDevice(c->device);
     for (void* p : c->allocs) cudaFree(p);
+    for (float* p : {c->pf_x, c->pf_xn, c->pf_qkv, c->pf_att, c->pf_gu, c->pf_u})
+        if (p) cudaFree(p);
     if (c->status_host) cudaFreeHost(c->status_host);
     for (uint16_t* p : c->perop.wqkv) cudaFree(p);
     for (uint16_t* p : c->perop.wo) cudaFree(p);
@@ -997,6 +1003,57 @@ int mk_decode_step_perop(mk_ctx* c, int32_t token, int32_t pos, float* logits_ou
     const int n = mk_perop_step(c->perop, token, nullptr, pos, logits_out, st, &e);
     if (e != cudaSuccess) return cuda_fail(e, "per-operator step");
     if (n_launches) *n_launches = n;
+    c->last_stream = st;
+    return MK_OK;
+}
+
+int mk_prefill(mk_ctx* c, const int32_t* tokens, int32_t n, int32_t start_pos, float* logits_out, void* stream) {
+    if (!c || !tokens || n < 1 || start_pos < 0) return MK_ERR_INVALID_ARG;
+    if (!c->weights_loaded || !c->perop_ready) return MK_ERR_STATE;
+    const MkGeom& g = c->geo;
+    if ((int64_t)start_pos + n > g.max_seq) return MK_ERR_INVALID_ARG;
+    if (g.F % 8 || g.H % 8) return MK_ERR_UNSUPPORTED;   // 16-byte weight pieces along K
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= g.V) return MK_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    MK_CU(cudaSetDevice(c->device));
+    const size_t H = g.H, F = g.F, nqkv = (size_t)(g.qh + 2 * g.kvh) * g.hd, qd = (size_t)g.qh * g.hd;
+    if (n > c->pf_rows) {   // grow the workspace (the buffers of a shorter prompt are freed first)
+        MK_CU(cudaStreamSynchronize(st));
+        if (c->pf_rows == 0) MK_CU(mk_prefill_prepare());
+        for (float** p : {&c->pf_x, &c->pf_xn, &c->pf_qkv, &c->pf_att, &c->pf_gu, &c->pf_u})
+            if (*p) { cudaFree(*p); *p = nullptr; }
+        c->pf_rows = 0;
+        const size_t rows = (size_t)n;
+        MK_CU(cudaMalloc(&c->pf_x, rows * H * 4));
+        MK_CU(cudaMalloc(&c->pf_xn, rows * H * 4));
+        MK_CU(cudaMalloc(&c->pf_qkv, rows * nqkv * 4));
+        MK_CU(cudaMalloc(&c->pf_att, rows * qd * 4));
+        MK_CU(cudaMalloc(&c->pf_gu, rows * 2 * F * 4));
+        MK_CU(cudaMalloc(&c->pf_u, rows * F * 4));
+        c->pf_rows = n;
+    }
+    MK_CU(cudaMemcpyAsync(c->prompt_dev, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, st));
+    const MkPerOp& P = c->perop;
+    MkPrefillArgs a{};
+    a.L = g.L; a.H = g.H; a.qh = g.qh; a.kvh = g.kvh; a.hd = g.hd; a.F = g.F; a.V = g.V; a.max_seq = g.max_seq;
+    a.eps = c->cfg.rms_eps;
+    a.n = n; a.start = start_pos; a.swz = g.kv_swz;
+    a.tokens = c->prompt_dev;
+    std::vector<const uint16_t*> wqkv(P.wqkv.begin(), P.wqkv.end()), wo(P.wo.begin(), P.wo.end()),
+        wgu(P.wgu.begin(), P.wgu.end()), wd(P.wd.begin(), P.wd.end());
+    a.wqkv = wqkv.data(); a.wo = wo.data(); a.wgu = wgu.data(); a.wd = wd.data();
+    a.embed = P.embed; a.lm = P.lm;
+    a.attn_norm = c->attn_norm; a.ffn_norm = c->ffn_norm; a.final_norm = c->final_norm;
+    a.rope_cos = c->rope_cos; a.rope_sin = c->rope_sin; a.kc = c->kc; a.vc = c->vc;
+    a.x = c->pf_x; a.xn = c->pf_xn; a.qkv = c->pf_qkv; a.att = c->pf_att; a.gu = c->pf_gu; a.u = c->pf_u;
+    a.hidden = c->hidden;
+    a.logits = logits_out ? logits_out : P.logits_tmp;
+    a.amax_part = P.amax_part; a.amax_blocks = P.amax_blocks;
+    a.next_token = c->next_token; a.status = c->status;
+    cudaError_t e = cudaSuccess;
+    mk_prefill_launch(a, st, &e);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill");
     c->last_stream = st;
     return MK_OK;
 }

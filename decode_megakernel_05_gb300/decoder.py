@@ -93,6 +93,14 @@ class Decoder:
         """Nucleus mass of the sampled steps from now on (1 = every token)."""
         mk.mk_set_top_p(self.ctx, float(top_p))
 
+    def prefill(self, tokens, start_pos: int = 0, logits=True):
+        """Batched prefill of host tokens at positions start_pos..; returns the device logits of
+        the last token (or None).  Needs the decoder built with perop=True (row-major weights)."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        ptr = self.logits.data_ptr() if logits else None
+        mk.mk_prefill(self.ctx, t.ctypes.data, t.size, int(start_pos), ptr, self.stream)
+        return self.logits if logits else None
+
     def step_perop(self, token: int, pos: int, logits=True) -> int:
         ptr = self.logits.data_ptr() if logits else None
         return mk.mk_decode_step_perop(self.ctx, int(token), int(pos), ptr, self.stream)

@@ -85,6 +85,7 @@ SIGNATURES = [
     ("mk_status", _i32, [_P]),
     ("mk_enable_perop", _i32, [_P, _i32]),
     ("mk_decode_step_perop", _i32, [_P, _i32, _i32, _P, _P, ctypes.POINTER(_i32)]),
+    ("mk_prefill", _i32, [_P, _P, _i32, _i32, _P, _P]),
     ("mk_get_info", _i32, [_P, ctypes.POINTER(mk_info)]),
     ("mk_argmax_f32_noalloc", _i32, [_P, _i32, _P, _P]),
     ("mk_set_debug", _i32, [_P, _i32, _i64]),
@@ -235,6 +236,10 @@ def mk_status(ctx: int) -> int:
 
 def mk_enable_perop(ctx: int, keep_rowmajor: bool = True) -> None:
     check(load().mk_enable_perop(ctx, int(keep_rowmajor)), "mk_enable_perop")
+
+
+def mk_prefill(ctx: int, tokens_ptr: int, n: int, start_pos: int, logits_ptr: int | None, stream: int = 0) -> None:
+    check(load().mk_prefill(ctx, tokens_ptr, n, start_pos, logits_ptr, stream), "mk_prefill")
 
 
 def mk_decode_step_perop(ctx: int, token: int, pos: int, logits_ptr: int | None, stream: int = 0) -> int:

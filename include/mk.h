@@ -234,6 +234,26 @@ int mk_enable_perop(mk_ctx* ctx, int32_t keep_rowmajor);
 int mk_decode_step_perop(mk_ctx* ctx, int32_t token, int32_t pos, float* logits_out, void* stream,
                          int32_t* n_launches);
 
+/* Batched prefill (cloud.baidu.com/article/9434380, sections 2 and 8, problem
+ * 2: prefill and decode are separate phases; the prompt is a dense,
+ * compute-bound contraction).  Runs the n prompt tokens (host int32, each in
+ * 0..V-1) at positions start_pos .. start_pos + n - 1 through every layer
+ * together: RMSNorm, tensor-core GEMMs for QKV, O, gate/up and down (bf16
+ * weights, each fp32 activation split into two bf16 parts), RoPE, the K/V rows
+ * written to the cache, causal attention over positions [0, position].  The
+ * cache then holds what n decode steps would have written (up to rounding
+ * order), the last row's final-norm hidden state is kept (mk_get_hidden), its
+ * logits go to logits_out (device fp32 [V], or NULL), and its greedy token is
+ * left on the device for mk_decode_step_greedy / mk_get_argmax.  Needs the
+ * row-major weight copies (mk_enable_perop(ctx, 1) before mk_load_weights;
+ * MK_ERR_STATE otherwise) and F, H multiples of 8 (MK_ERR_UNSUPPORTED).
+ * Requires start_pos + n <= max_seq.  Allocates its fp32 workspace (about
+ * n * (4H + 3F + qkv rows + qh*hd) * 4 bytes) on the first call and when a
+ * longer prompt arrives, synchronizing the stream then; otherwise
+ * asynchronous.  Device-side errors (a non-finite logit) are latched in the
+ * status word (mk_status). */
+int mk_prefill(mk_ctx* ctx, const int32_t* tokens, int32_t n, int32_t start_pos, float* logits_out, void* stream);
+
 int mk_get_info(const mk_ctx* ctx, mk_info* out);
 
 /* Greedy token over a caller's fp32 logits without allocating anything (the
