@@ -32,8 +32,15 @@ class _OracleModelC(ctypes.Structure):
         ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double),
         ("embed", _P), ("lm_head", _P), ("final_norm", _P),
         ("attn_norm", _P), ("wq", _P), ("wk", _P), ("wv", _P), ("wo", _P),
-        ("ffn_norm", _P), ("w_gate", _P), ("w_up", _P), ("w_down", _P),
+        ("ffn_norm", _P), ("w_gate", _P), ("w_up", _P), ("w_down", _P), ("q8", _P),
     ]
+
+
+class _OracleQ8C(ctypes.Structure):
+    _fields_ = [("q", _P * 7), ("s", _P * 7), ("lm_q", _P), ("lm_s", _P)]
+
+# the int8 matrices in the order of oracle_q8 (w_down's scales are per input column)
+Q8_KINDS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
 
 
 def build(force: bool = False) -> str:
@@ -68,6 +75,10 @@ def lib():
             L.oracle_argmax_f32.restype = ctypes.c_int
             L.oracle_decode_step.argtypes = [ctypes.POINTER(_OracleModelC), _P, _P, ctypes.c_int, ctypes.c_int, _P, _P]
             L.oracle_decode_step.restype = ctypes.c_int
+            L.oracle_quantize_q8.argtypes = [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P]
+            L.oracle_quantize_q8.restype = None
+            L.oracle_gemv_q8.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _P, _P]
+            L.oracle_gemv_q8.restype = None
             L.oracle_splitmix64_output.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
             L.oracle_splitmix64_output.restype = ctypes.c_uint64
             L.oracle_uniform_f32.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int]
@@ -181,12 +192,40 @@ def sample_topp_f32(logits, inv_temp: float, top_p: float, seed: int, pos: int):
     return idx, bool(nf.value)
 
 
+def quantize_q8(w_bf16, col_scaled: bool = False):
+    """(int8 codes [rows][cols], fp32 scales [rows] or [cols]) of a bf16 matrix (oracle_quantize_q8)."""
+    w, pw = _c(w_bf16, np.uint16)
+    rows, cols = w.shape
+    q = np.empty((rows, cols), dtype=np.int8)
+    sc = np.empty(cols if col_scaled else rows, dtype=np.float32)
+    lib().oracle_quantize_q8(pw, rows, cols, int(col_scaled), q.ctypes.data, sc.ctypes.data)
+    return q, sc
+
+
+def gemv_q8(q, scale, x, col_scaled: bool = False) -> np.ndarray:
+    q, pq = _c(q, np.int8)
+    sc, ps = _c(scale, np.float32)
+    x, px = _c(x, np.float64)
+    y = np.empty(q.shape[0], dtype=np.float64)
+    lib().oracle_gemv_q8(pq, ps, int(col_scaled), q.shape[0], q.shape[1], px, y.ctypes.data)
+    return y
+
+
+def quantize_model_q8(model: dict) -> dict:
+    """The oracle's own weight-only INT8 form of a model: per layer and matrix
+    kind (codes, scales), and the LM head's (the embedding's when tied)."""
+    out = {k: [quantize_q8(w, col_scaled=(k == "w_down")) for w in model[k]] for k in Q8_KINDS}
+    out["lm_head"] = quantize_q8(model["embed"] if model["lm_head"] is None else model["lm_head"])
+    return out
+
+
 # ---------------------------------------------------------------- decode step
 
 class OracleDecoder:
     """The oracle's model + its own bf16 K/V cache [L][kv_heads][max_seq][head_dim]."""
 
-    def __init__(self, model: dict, max_seq: int):
+    def __init__(self, model: dict, max_seq: int, q8: dict | None = None):
+        """q8: the model's int8 form (quantize_model_q8) to compute with instead of the bf16 matrices."""
         s = model["shape"]
         self.shape, self.max_seq, self._keep = s, int(max_seq), []
         c = _OracleModelC()
@@ -209,6 +248,27 @@ class OracleDecoder:
         c.final_norm = ptr(model["final_norm"])
         for name in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down"):
             setattr(c, name, ptrs(model[name]))
+        c.q8 = None
+        if q8 is not None:
+            qc = _OracleQ8C()
+
+            def keep(a, dt):
+                a = np.ascontiguousarray(a, dtype=dt)
+                self._keep.append(a)
+                return a.ctypes.data
+
+            def plist(lst):
+                arr = (ctypes.c_void_p * len(lst))(*lst)
+                self._keep.append(arr)
+                return ctypes.cast(arr, ctypes.c_void_p).value
+
+            for i, kind in enumerate(Q8_KINDS):
+                qc.q[i] = plist([keep(q, np.int8) for q, _ in q8[kind]])
+                qc.s[i] = plist([keep(sc, np.float32) for _, sc in q8[kind]])
+            qc.lm_q = keep(q8["lm_head"][0], np.int8)
+            qc.lm_s = keep(q8["lm_head"][1], np.float32)
+            self._keep.append(qc)
+            c.q8 = ctypes.cast(ctypes.pointer(qc), ctypes.c_void_p).value
         self._c = c
         shp = (s.n_layers, s.n_kv_heads, self.max_seq, s.head_dim)
         self.kcache = np.zeros(shp, dtype=np.uint16)

@@ -31,6 +31,18 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* Weight-only INT8 form of the model's matrices (stapisi.com/news/3904786,
+ * section 6: quantization fused into the kernels), see oracle_quantize_q8.
+ * Index 0..6 = wq, wk, wv, wo, w_gate, w_up, w_down; per layer an int8
+ * matrix [out][in] and its scales: one per output row, except w_down, one per
+ * input column. */
+typedef struct {
+    const int8_t* const* q[7];
+    const float* const* s[7];
+    const int8_t* lm_q;   /* [vocab][hidden] */
+    const float* lm_s;    /* [vocab] */
+} oracle_q8;
+
 typedef struct {
     int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, max_seq;
     double rms_eps, rope_theta;
@@ -46,6 +58,7 @@ typedef struct {
     const uint16_t* const* w_gate;    /* per layer [ffn][hidden] */
     const uint16_t* const* w_up;      /* per layer [ffn][hidden] */
     const uint16_t* const* w_down;    /* per layer [hidden][ffn] */
+    const oracle_q8* q8;              /* NULL: the bf16 matrices above; else these int8 ones */
 } oracle_model;
 
 /* bf16 bit pattern -> double (exact). */
@@ -89,6 +102,57 @@ void oracle_gemv(const uint16_t* W, int64_t rows, int64_t cols, const double* x,
         for (int64_t c = 0; c < cols; ++c) acc += bf2d(w[c]) * x[c];
         y[r] = acc;
     }
+}
+
+/* Weight-only INT8 quantization (stapisi.com/news/3904786, section 6 names
+ * quantization among the work fused into kernels; the page gives no scheme,
+ * the one taken is symmetric absmax per channel): for each group g of
+ * weights (a row, or for col_scaled a column) of a bf16 matrix [rows][cols],
+ * the scale is s_g = max|w| / 127 and each code is q = round(w / s_g), ties to
+ * even, so w ~ q * s_g with |w - q s_g| <= s_g / 2 and |q| <= 127.  Both the
+ * scale and the quotient are float operations rounded to nearest (the
+ * precision the codes are decided in); a group of zeros gets s = 0, q = 0. */
+void oracle_quantize_q8(const uint16_t* W, int64_t rows, int64_t cols, int col_scaled, int8_t* q, float* scale) {
+    const int64_t ng = col_scaled ? cols : rows, len = col_scaled ? rows : cols;
+    for (int64_t gi = 0; gi < ng; ++gi) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < len; ++k) {
+            const int64_t idx = col_scaled ? k * cols + gi : gi * cols + k;
+            const float w = (float)bf2d(W[idx]);
+            if (fabsf(w) > amax) amax = fabsf(w);
+        }
+        const float sg = amax / 127.0f;
+        scale[gi] = sg;
+        for (int64_t k = 0; k < len; ++k) {
+            const int64_t idx = col_scaled ? k * cols + gi : gi * cols + k;
+            float c = 0.0f;
+            if (sg > 0.0f) c = rintf((float)bf2d(W[idx]) / sg);
+            if (c > 127.0f) c = 127.0f;
+            if (c < -127.0f) c = -127.0f;
+            q[idx] = (int8_t)c;
+        }
+    }
+}
+
+/* y = W' x for the dequantized matrix W'[r][c] = q[r][c] * s (s = scale[r],
+ * or scale[c] when col_scaled), in double. */
+void oracle_gemv_q8(const int8_t* q, const float* scale, int col_scaled, int64_t rows, int64_t cols, const double* x,
+                    double* y) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const int8_t* w = q + r * cols;
+        double acc = 0.0;
+        for (int64_t c = 0; c < cols; ++c)
+            acc += (double)w[c] * (double)(col_scaled ? scale[c] : scale[r]) * x[c];
+        y[r] = acc;
+    }
+}
+
+/* Matrix kind k (0..6 as in oracle_q8) of layer l: the bf16 matrix or its int8 form. */
+static void mat_gemv(const oracle_model* m, int k, int l, const uint16_t* bf, int64_t rows, int64_t cols,
+                     const double* x, double* y) {
+    if (m->q8) oracle_gemv_q8(m->q8->q[k][l], m->q8->s[k][l], k == 6, rows, cols, x, y);
+    else oracle_gemv(bf, rows, cols, x, y);
 }
 
 /* Rotary position encoding of one head vector v[hd] at position pos
@@ -299,9 +363,9 @@ int oracle_decode_step(const oracle_model* m, uint16_t* kcache, uint16_t* vcache
     for (int l = 0; l < m->n_layers; ++l) {
         /* segment A: RMSNorm, Q/K/V projections, RoPE on q and k, K/V append */
         oracle_rmsnorm(x, m->attn_norm[l], H, m->rms_eps, xn);
-        oracle_gemv(m->wq[l], (int64_t)qh * hd, H, xn, q);
-        oracle_gemv(m->wk[l], (int64_t)kvh * hd, H, xn, k);
-        oracle_gemv(m->wv[l], (int64_t)kvh * hd, H, xn, v);
+        mat_gemv(m, 0, l, m->wq[l], (int64_t)qh * hd, H, xn, q);
+        mat_gemv(m, 1, l, m->wk[l], (int64_t)kvh * hd, H, xn, k);
+        mat_gemv(m, 2, l, m->wv[l], (int64_t)kvh * hd, H, xn, v);
         for (int h = 0; h < qh; ++h) oracle_rope(q + (int64_t)h * hd, hd, pos, m->rope_theta);
         for (int g = 0; g < kvh; ++g) oracle_rope(k + (int64_t)g * hd, hd, pos, m->rope_theta);
         for (int g = 0; g < kvh; ++g) {
@@ -320,20 +384,21 @@ int oracle_decode_step(const oracle_model* m, uint16_t* kcache, uint16_t* vcache
             int64_t base = ((int64_t)l * kvh + g) * m->max_seq * hd;
             oracle_attention_head(q + (int64_t)h * hd, kcache + base, vcache + base, pos + 1, hd, att + (int64_t)h * hd);
         }
-        oracle_gemv(m->wo[l], H, (int64_t)qh * hd, att, o);
+        mat_gemv(m, 3, l, m->wo[l], H, (int64_t)qh * hd, att, o);
         for (int i = 0; i < H; ++i) x[i] += o[i];
         /* segment C: RMSNorm, gate/up projections, SwiGLU, down projection,
          * residual add */
         oracle_rmsnorm(x, m->ffn_norm[l], H, m->rms_eps, xn);
-        oracle_gemv(m->w_gate[l], F, H, xn, gate);
-        oracle_gemv(m->w_up[l], F, H, xn, up);
+        mat_gemv(m, 4, l, m->w_gate[l], F, H, xn, gate);
+        mat_gemv(m, 5, l, m->w_up[l], F, H, xn, up);
         for (int j = 0; j < F; ++j) u[j] = oracle_silu(gate[j]) * up[j];
-        oracle_gemv(m->w_down[l], H, F, u, o);
+        mat_gemv(m, 6, l, m->w_down[l], H, F, u, o);
         for (int i = 0; i < H; ++i) x[i] += o[i];
     }
     /* final norm, LM head */
     oracle_rmsnorm(x, m->final_norm, H, m->rms_eps, hidden);
-    oracle_gemv(m->lm_head, m->vocab, H, hidden, logits);
+    if (m->q8) oracle_gemv_q8(m->q8->lm_q, m->q8->lm_s, 0, m->vocab, H, hidden, logits);
+    else oracle_gemv(m->lm_head, m->vocab, H, hidden, logits);
 
     free(x); free(xn); free(q); free(k); free(v); free(att); free(o); free(gate); free(up); free(u);
     return 0;

@@ -33,6 +33,11 @@ MUTATIONS = {
     "gate_up_swapped": ("u[j] = oracle_silu(gate[j]) * up[j];", "u[j] = oracle_silu(up[j]) * gate[j];"),
     "topp_own_mass_included": ("const int kept = above < top_p * z;", "const int kept = above + grp < top_p * z;"),
     "topp_untempered": ("x[v] = y * inv_temp;", "x[v] = y;"),
+    "q8_truncating_codes": ("if (sg > 0.0f) c = rintf((float)bf2d(W[idx]) / sg);",
+                            "if (sg > 0.0f) c = truncf((float)bf2d(W[idx]) / sg);"),
+    "q8_scale_255": ("const float sg = amax / 127.0f;", "const float sg = amax / 255.0f;"),
+    "q8_down_row_scaled": ("oracle_gemv_q8(m->q8->q[k][l], m->q8->s[k][l], k == 6, rows, cols, x, y);",
+                           "oracle_gemv_q8(m->q8->q[k][l], m->q8->s[k][l], 0, rows, cols, x, y);"),
 }
 
 

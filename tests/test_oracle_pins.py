@@ -177,12 +177,22 @@ def as_t(bits):
     return torch.from_numpy(bf16_vals(bits))
 
 
-def torch_causal_forward(m, tokens):
+def torch_causal_forward(m, tokens, mats=None):
     """Full causal forward over the whole sequence with torch fp64 library ops
     (F.rms_norm, F.scaled_dot_product_attention with is_causal and enable_gqa,
     F.silu, matmul).  K and V are rounded to bf16 (via float32, torch's
-    rounding) after RoPE, as a bf16 cache holds them."""
+    rounding) after RoPE, as a bf16 cache holds them.  mats: fp64 tensors to
+    use for the matrices instead of the model's bf16 ones (per kind a list
+    per layer, and "lm_head")."""
     s = m["shape"]
+    if mats is not None:
+        def W(kind, l=None):
+            return mats[kind] if l is None else mats[kind][l]
+    else:
+        def W(kind, l=None):
+            if l is not None:
+                return as_t(m[kind][l])
+            return as_t(m["embed"] if m["lm_head"] is None else m["lm_head"])
     T, hd = len(tokens), s.head_dim
     x = as_t(m["embed"])[torch.as_tensor(tokens, dtype=torch.long)]
     pos = torch.arange(T, dtype=torch.float64)
@@ -199,18 +209,17 @@ def torch_causal_forward(m, tokens):
 
     for l in range(s.n_layers):
         xn = F.rms_norm(x, (s.hidden,), as_t(m["attn_norm"][l]), eps=s.rms_eps)
-        q = (xn @ as_t(m["wq"][l]).T).view(T, s.n_q_heads, hd).transpose(0, 1)
-        k = (xn @ as_t(m["wk"][l]).T).view(T, s.n_kv_heads, hd).transpose(0, 1)
-        v = (xn @ as_t(m["wv"][l]).T).view(T, s.n_kv_heads, hd).transpose(0, 1)
+        q = (xn @ W("wq", l).T).view(T, s.n_q_heads, hd).transpose(0, 1)
+        k = (xn @ W("wk", l).T).view(T, s.n_kv_heads, hd).transpose(0, 1)
+        v = (xn @ W("wv", l).T).view(T, s.n_kv_heads, hd).transpose(0, 1)
         q, k, v = rope(q), rb(rope(k)), rb(v)
         o = F.scaled_dot_product_attention(q[None], k[None], v[None], is_causal=True, enable_gqa=True)[0]
-        x = x + o.transpose(0, 1).reshape(T, -1) @ as_t(m["wo"][l]).T
+        x = x + o.transpose(0, 1).reshape(T, -1) @ W("wo", l).T
         xn = F.rms_norm(x, (s.hidden,), as_t(m["ffn_norm"][l]), eps=s.rms_eps)
-        u = F.silu(xn @ as_t(m["w_gate"][l]).T) * (xn @ as_t(m["w_up"][l]).T)
-        x = x + u @ as_t(m["w_down"][l]).T
+        u = F.silu(xn @ W("w_gate", l).T) * (xn @ W("w_up", l).T)
+        x = x + u @ W("w_down", l).T
     h = F.rms_norm(x, (s.hidden,), as_t(m["final_norm"]), eps=s.rms_eps)
-    lm = m["embed"] if m["lm_head"] is None else m["lm_head"]
-    return (h @ as_t(lm).T).numpy(), h.numpy()
+    return (h @ W("lm_head").T).numpy(), h.numpy()
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(tie_embeddings=True), dict(n_kv_heads=4), dict(n_kv_heads=1)])
@@ -473,3 +482,68 @@ def test_topp_ties_and_limits():
     bad[top] = np.nan
     tok, nf = oracle.sample_topp_f32(bad, 1.0, 0.9, 5, 0)
     assert nf and tok != top
+
+
+
+# ---------------------------------------------------------------- weight-only INT8
+
+def test_q8_quantizer_exact_cases_and_bound():
+    """Rows that are integer multiples of a power-of-two step quantize exactly
+    (the scale is max|w| / 127 and every code is the multiple); any row obeys
+    |w - q s| <= s / 2 (plus the float rounding of w / s) with |q| <= 127 and
+    the largest |w| at code +-127; a
+    zero row gets scale 0 and codes 0; per-column scaling is the same on W^T."""
+    k = np.array([[-127, -3, 0, 5, 127, 64], [1, -1, 2, -2, 0, 0], [0, 0, 0, 0, 0, 0]], dtype=np.float64)
+    steps = np.array([2.0 ** -10, 2.0 ** -4, 1.0])
+    w = (k * steps[:, None]).astype(np.float32)
+    bits = (w.view(np.uint32) >> 16).astype(np.uint16)           # exact in bf16
+    q, sc = oracle.quantize_q8(bits)
+    assert np.array_equal(q[0], k[0].astype(np.int8))             # max|w| = 127 steps: scale = step
+    assert sc[0] == np.float32(2.0 ** -10) and sc[2] == 0.0 and not q[2].any()
+    assert np.array_equal(q[1], np.round(k[1] * 127 / 2).astype(np.int8))   # row 1: max 2 -> scale 2/127
+    rng = np.random.default_rng(3)
+    wr = synth.normal_bf16((17, 40), 9, 1, 0.0, 0.05)
+    q, sc = oracle.quantize_q8(wr)
+    vals = bf16_vals(wr)
+    assert np.all(np.abs(q.astype(np.int32)) <= 127)
+    # the quotient w / s is rounded in float before the code is: |w/s - q| <= 1/2 + 128 * 2^-24
+    bound = sc[:, None].astype(np.float64) * (0.5 + 128 * 2.0 ** -24)
+    assert np.all(np.abs(vals - q * sc[:, None].astype(np.float64)) <= bound)
+    assert np.all(np.abs(q[np.arange(17), np.argmax(np.abs(vals), axis=1)]) == 127)
+    qc, scc = oracle.quantize_q8(wr, col_scaled=True)
+    qt, sct = oracle.quantize_q8(np.ascontiguousarray(wr.T))
+    assert np.array_equal(qc, qt.T) and np.array_equal(scc, sct)
+
+
+def test_q8_gemv_equals_dequantized_matmul():
+    rng = np.random.default_rng(5)
+    wr = synth.normal_bf16((23, 31), 4, 2, 0.0, 0.1)
+    x = rng.normal(size=31)
+    for col in (False, True):
+        q, sc = oracle.quantize_q8(wr, col_scaled=col)
+        deq = q.astype(np.float64) * (sc[None, :] if col else sc[:, None]).astype(np.float64)
+        np.testing.assert_allclose(oracle.gemv_q8(q, sc, x, col_scaled=col), deq @ x, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(tie_embeddings=True)])
+def test_q8_decode_matches_torch_causal_forward_on_dequantized_weights(kw):
+    """The oracle's int8 decode step equals the torch fp64 causal forward run
+    on the dequantized matrices (codes times their row scales, or column scales
+    for w_down), at every position."""
+    s = tiny_shape(**kw)
+    m = synth.make_model(s, seed=8, std=0.2, gains="normal")
+    q8 = oracle.quantize_model_q8(m)
+
+    def deq(kind, pair):
+        q, sc = pair
+        return torch.from_numpy(q.astype(np.float64) * (sc[None, :] if kind == "w_down" else sc[:, None]))
+
+    mats = {kind: [deq(kind, p) for p in q8[kind]] for kind in oracle.Q8_KINDS}
+    mats["lm_head"] = deq("lm_head", q8["lm_head"])
+    tokens = synth.uniform_tokens(10, s.vocab, 8, 98)
+    want_logits, want_h = torch_causal_forward(m, tokens, mats)
+    o = oracle.OracleDecoder(m, max_seq=16, q8=q8)
+    for p, t in enumerate(tokens):
+        lg, h = o.step(int(t), p)
+        np.testing.assert_allclose(lg, want_logits[p], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(h, want_h[p], rtol=1e-9, atol=1e-11)
