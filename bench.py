@@ -3,10 +3,10 @@
 
 Default workload: the Llama-3.2-1B shape (16 layers, hidden 2048, 32 q / 8 kv
 heads, head_dim 64, SwiGLU 8192, vocab 128256, tied embeddings, RoPE theta
-500000), random-init bf16 weights N(0, 0.02), a 512-token uniform prompt decoded
-one token at a time (untimed), then greedy decode steps at context lengths
-513..768; a timed run longer than 256 steps rewinds to position 512 so every
-step stays inside that window.
+500000), random-init bf16 weights N(0, 0.02), a 512-token uniform prompt (run
+through the batched prefill, timed on its own), then greedy decode steps at
+context lengths 513..768; a timed run longer than 256 steps rewinds to position
+512 so every step stays inside that window.
 
 One step = one decode token = one kernel launch: RMSNorm + QKV GEMV + RoPE +
 K/V append, GQA attention, O-proj + residual, RMSNorm + gate/up + SiLU + down +
@@ -22,6 +22,13 @@ replica on its own GPU and `value` is the total tokens/s of all replicas.
 
 --impl reference times the CPU oracle (the plain fp64 C reference) on the host
 cores, on the same workload, metric and unit.
+
+For the prompt workloads the line also carries "prefill": the 512-token prompt
+through the batched prefill (mk_prefill, tensor-core GEMMs), CUDA-event timed
+on its own and against the same prompt as 512 fused decode launches; its
+roofline is tensor-bound against the measured bf16 peak.  It also carries
+"int8": the same decode steps on a weight-only INT8 context (the int8 build of
+the fused kernel), CUDA-event timed, with its own HBM roofline.
 """
 from __future__ import annotations
 
@@ -57,6 +64,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the batched-prefill measurement")
+    ap.add_argument("--no-int8", action="store_true", help="skip the weight-only INT8 decode measurement")
     return ap.parse_args()
 
 
@@ -182,6 +191,116 @@ def measured_peak():
         return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
 
 
+def measured_bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except Exception:
+        return 1900.0, "fallback 1.9 PFLOP/s bf16 (no MEASURED_PEAKS.json)"
+
+
+def prefill_flops(s, n: int) -> float:
+    """Algorithmic FLOPs of a batched prefill of n tokens: 2 per weight of the
+    layer matrices per token, the causal attention (q.k and p.v over the
+    positions each row attends, all heads), and the LM head for the last row."""
+    per_layer = ((s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim * s.hidden + s.hidden * s.n_q_heads * s.head_dim
+                 + 3 * s.ffn * s.hidden)
+    attn = 4 * s.n_q_heads * s.head_dim * (n * (n + 1) // 2)
+    return float(2 * s.n_layers * per_layer * n + s.n_layers * attn + 2 * s.vocab * s.hidden)
+
+
+def time_prefill(dec, w, torch, reps: int = 5):
+    """CUDA-event time of the batched prefill of the workload's prompt (warm,
+    then reps timed calls, each rewriting positions 0..n-1), and of the same
+    prompt as one fused decode launch per token."""
+    import synth
+
+    prompt = synth.make_prompt(w)
+    st = torch.cuda.current_stream()
+    for _ in range(2):
+        dec.prefill(prompt, 0, logits=False)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        dec.prefill(prompt, 0, logits=False)
+    e1.record(st)
+    torch.cuda.synchronize()
+    pf_ms = e0.elapsed_time(e1) / reps
+    e0.record(st)
+    rc, _ = dec.generate_greedy(prompt, 0, 1)
+    e1.record(st)
+    torch.cuda.synchronize()
+    assert rc == 0, f"prompt run failed: {rc}"
+    dl_ms = e0.elapsed_time(e1)
+    dec.prefill(prompt, 0, logits=False)   # leaves the prefill's cache and next token for the decode steps
+    torch.cuda.synchronize()
+    n = len(prompt)
+    fl = prefill_flops(w.shape, n)
+    peak, src = measured_bf16_peak()
+    achieved = fl / (pf_ms * 1e-3) / 1e12
+    return {"prompt_tokens": n, "ms": pf_ms, "tokens_per_s": n / (pf_ms * 1e-3),
+            "launches": 9 * w.shape.n_layers + 5,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": src,
+                         "algorithmic_flops": fl,
+                         "note": "mma.sync bf16 with each fp32 activation as three bf16 parts: "
+                                 "3x the tensor work of the algorithmic FLOPs"},
+            "decode_launch_prompt_ms": dl_ms, "speedup_vs_decode_launches": dl_ms / pf_ms}
+
+
+def time_int8(a, w, local, torch, positions, peak, peak_src):
+    """The same decode steps on a weight-only INT8 context (codes and per-row /
+    per-column fp32 scales streamed, dequantized in registers): its context
+    built the way the bf16 one was (pre-filled cache, or the prompt as decode
+    launches), then W warm-up and K CUDA-event-timed greedy steps at the same
+    positions; roofline against the int8 stream's algorithmic bytes."""
+    import synth
+    from decode_megakernel_05_gb300 import Decoder, mk
+
+    s = w.shape
+    max_seq = (w.start_pos + w.decode + 64 + 63) // 64 * 64
+    m = synth.make_model(s, w.seed_weights)
+    dec = Decoder(m, max_seq, device=local, tuning=mk.tuning(a.ring_stages, a.slot_kib, a.l2_prefetch_kib, 0, 1))
+    del m
+    info = dec.info
+    st = torch.cuda.current_stream()
+    if w.prefill:
+        ks, vs = synth.make_kv(s, w.prefill, w.seed_kv)
+        dec.set_kv(ks, vs, w.prefill)
+        del ks, vs
+        dec.step(synth.make_first_token(w), w.prefill, logits=False)
+    else:
+        rc, _ = dec.generate_greedy(synth.make_prompt(w), 0, 1)
+        assert rc == 0, f"int8 prompt run failed: {rc}"
+    for k in range(a.warmup):
+        dec.step_greedy(positions[k])
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps + 1)]
+    ev[0].record(st)
+    for k in range(a.steps):
+        dec.step_greedy(positions[a.warmup + k])
+        ev[k + 1].record(st)
+    torch.cuda.synchronize()
+    assert dec.status() == 0, f"int8 device status {dec.status()}"
+    per = sorted(ev[k].elapsed_time(ev[k + 1]) for k in range(a.steps))
+    total_s = ev[0].elapsed_time(ev[-1]) / 1e3
+    ctxs = [p + 1 for p in positions[a.warmup:]]
+    alg = info.weight_bytes_per_token + info.kv_bytes_per_position * float(np.mean(ctxs))
+    achieved = alg / (total_s / a.steps) / 1e9
+    dec.close()
+    return {"value": a.steps / total_s, "unit": UNIT, "ms_per_token_p50": per[len(per) // 2],
+            "ms_per_token_p99": per[min(len(per) - 1, int(round(0.99 * (len(per) - 1))))],
+            "gpu_launches": a.steps, "dtype": "int8 weights, fp32 arithmetic",
+            "weights": "symmetric absmax int8, fp32 scale per output row (per input column for w_down), "
+                       "quantized on the device at load",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_src, "traffic": None,
+                         "algorithmic_bytes_per_launch": alg,
+                         "kernel": "mk_decode_kernel, int8 build (1 launch = 1 token)"}}
+
+
 KERNEL_SOURCES = ("mk_kernel.cuh", "mk_kernel.cu", "mk_internal.h")
 
 
@@ -270,11 +389,15 @@ def run_ours(a, world, rank, local):
     max_seq = (max_seq + 63) // 64 * 64
     tun = mk.tuning(a.ring_stages, a.slot_kib, a.l2_prefetch_kib, 0)
     m = synth.make_model(s, w.seed_weights)
-    dec = Decoder(m, max_seq, device=local, tuning=tun, perop=a.perop)
+    # the row-major weight copies serve the per-operator baseline and the batched prefill
+    want_prefill = bool(w.prompt_len) and not a.no_prefill and not a.perop
+    dec = Decoder(m, max_seq, device=local, tuning=tun, perop=a.perop or want_prefill)
     del m
     info = dec.info
     stream = torch.cuda.current_stream()
-    # context: prompt decoded one token at a time (untimed), or a pre-filled cache
+    # context: the prompt (batched prefill, timed on its own; or one decode launch
+    # per token, untimed), or a pre-filled cache
+    prefill = None
     if w.prefill:
         ks, vs = synth.make_kv(s, w.prefill, w.seed_kv)
         dec.set_kv(ks, vs, w.prefill)
@@ -282,6 +405,9 @@ def run_ours(a, world, rank, local):
         first = synth.make_first_token(w)
         dec.step(first, w.prefill, logits=False)
         pos0 = w.prefill + 1
+    elif want_prefill:
+        prefill = time_prefill(dec, w, torch)
+        pos0 = w.prompt_len
     else:
         prompt = synth.make_prompt(w)
         rc, _ = dec.generate_greedy(prompt, 0, 1)
@@ -357,6 +483,11 @@ def run_ours(a, world, rank, local):
         e2e = {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4,
                "api": "mk_generate_greedy(host prompt of 1 token, 1 new token) per step, pinned buffers"}
 
+    int8 = None
+    if not a.no_int8 and not a.perop:
+        dec.close()
+        int8 = time_int8(a, w, local, torch, positions, peak, peak_src)
+
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         dec.close()
@@ -391,6 +522,10 @@ def run_ours(a, world, rank, local):
             "launches_per_token": launches_per_step,
             "clocks": clk.summary(),
         }
+        if prefill:
+            line["prefill"] = prefill
+        if int8:
+            line["int8"] = int8
         if e2e:
             line["e2e"] = e2e
         if cpu:

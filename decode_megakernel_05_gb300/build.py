@@ -28,6 +28,10 @@ VARIANTS = [(64, 2, 1), (64, 4, 2), (64, 4, 4), (64, 4, 8), (64, 4, 16), (128, 4
 # each CTA at least MK_ATTN_TC_MIN_PER_CTA positions; keep in sync with MK_LC_VARIANTS in
 # csrc/mk_api.cu
 LC_VARIANTS = [(64, 4, 2), (64, 4, 8)]
+# weight-only INT8 builds (-DMK_WB_V=1) of the standard and long-context kernels; keep in sync
+# with MK_Q8_VARIANTS and MK_Q8_LC_VARIANTS in csrc/mk_api.cu
+Q8_VARIANTS = [(64, 2, 1), (64, 4, 8), (128, 4, 16)]
+Q8_LC_VARIANTS = [(64, 4, 8)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -60,12 +64,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
                     "-I", INCLUDE, "-I", CSRC]
     jobs = [(src, os.path.join(BUILD, src.replace(".cu", ".o")), []) for src in SOURCES]
-    for hd, g, mh, lc in [v + (0,) for v in VARIANTS] + [v + (1,) for v in LC_VARIANTS]:
+    kernels = ([v + (0, 2) for v in VARIANTS] + [v + (1, 2) for v in LC_VARIANTS] +
+               [v + (0, 1) for v in Q8_VARIANTS] + [v + (1, 1) for v in Q8_LC_VARIANTS])
+    for hd, g, mh, lc, wb in kernels:
         for tr in (False, True):   # each without and with the segment trace compiled in
-            name = f"mk_kernel_{hd}_{g}_{mh}{'_lc' if lc else ''}{'_trace' if tr else ''}.o"
-            jobs.append(("mk_kernel.cu", os.path.join(BUILD, name),
-                         [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}", f"-DMK_MH_V={mh}", f"-DMK_LC_V={lc}"] +
-                         ([] if tr else ["-DMK_NO_TRACE"])))
+            sfx = ("_lc" if lc else "") + ("_q8" if wb == 1 else "") + ("_trace" if tr else "")
+            jobs.append(("mk_kernel.cu", os.path.join(BUILD, f"mk_kernel_{hd}_{g}_{mh}{sfx}.o"),
+                         [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}", f"-DMK_MH_V={mh}", f"-DMK_LC_V={lc}",
+                          f"-DMK_WB_V={wb}"] + ([] if tr else ["-DMK_NO_TRACE"])))
 
     def compile_one(job):
         src, obj, defs = job

@@ -22,6 +22,10 @@
 #define MK_VARIANTS(X) \
     X(64, 2, 1) X(64, 4, 2) X(64, 4, 4) X(64, 4, 8) X(64, 4, 16) X(128, 4, 4) X(128, 4, 8) X(128, 4, 16)
 #define MK_LC_VARIANTS(X) X(64, 4, 2) X(64, 4, 8)
+// Weight-only INT8 builds (-DMK_WB_V=1; keep in sync with Q8_VARIANTS and
+// Q8_LC_VARIANTS in build.py).
+#define MK_Q8_VARIANTS(X) X(64, 2, 1) X(64, 4, 8) X(128, 4, 16)
+#define MK_Q8_LC_VARIANTS(X) X(64, 4, 8)
 // Each variant exists twice: without trace code (launched normally) and with
 // it (launched while a segment trace is requested).
 #define MK_DECL(hd, g, mh)                                         \
@@ -30,30 +34,44 @@
 #define MK_DECL_LC(hd, g, mh)                                          \
     extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh##_lc(void); \
     extern "C" const void* mk_kernel_trace_ptr_##hd##_##g##_##mh##_lc(void);
+#define MK_DECL_Q8(hd, g, mh)                                          \
+    extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh##_q8(void); \
+    extern "C" const void* mk_kernel_trace_ptr_##hd##_##g##_##mh##_q8(void);
+#define MK_DECL_LC_Q8(hd, g, mh)                                          \
+    extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh##_lc_q8(void); \
+    extern "C" const void* mk_kernel_trace_ptr_##hd##_##g##_##mh##_lc_q8(void);
 MK_VARIANTS(MK_DECL)
 MK_LC_VARIANTS(MK_DECL_LC)
+MK_Q8_VARIANTS(MK_DECL_Q8)
+MK_Q8_LC_VARIANTS(MK_DECL_LC_Q8)
 #undef MK_DECL
 #undef MK_DECL_LC
+#undef MK_DECL_Q8
+#undef MK_DECL_LC_Q8
 
-// The kernel for a shape; with long_ctx, its long-context (tensor-core
-// attention) build where one exists.
-// Returns 1 for a long-context build, 0 for the standard one, -1 if none fits.
-static int mk_kernel_variant(int hd, int G, int H, bool long_ctx, const void** fn, const void** fn_trace) {
-#define MK_PICK_LC(hd_, g_, mh_)                                      \
-    if (long_ctx && hd == hd_ && G == g_ && H == 256 * mh_) {         \
-        *fn = mk_kernel_ptr_##hd_##_##g_##_##mh_##_lc();              \
-        *fn_trace = mk_kernel_trace_ptr_##hd_##_##g_##_##mh_##_lc();  \
-        return 1;                                                     \
+// The kernel for a shape and weight width (wb = 2 bf16, 1 weight-only INT8);
+// with long_ctx, its long-context (tensor-core attention) build where one
+// exists.  Returns 1 for a long-context build, 0 for the standard one, -1 if
+// none fits.
+static int mk_kernel_variant(int hd, int G, int H, int wb, bool long_ctx, const void** fn, const void** fn_trace) {
+#define MK_PICK(hd_, g_, mh_, wb_, lc_, sfx)                                  \
+    if ((!lc_ || long_ctx) && wb == wb_ && hd == hd_ && G == g_ && H == 256 * mh_) { \
+        *fn = mk_kernel_ptr_##hd_##_##g_##_##mh_##sfx();                      \
+        *fn_trace = mk_kernel_trace_ptr_##hd_##_##g_##_##mh_##sfx();          \
+        return lc_;                                                           \
     }
+#define MK_PICK_LC(hd_, g_, mh_) MK_PICK(hd_, g_, mh_, 2, 1, _lc)
+#define MK_PICK_STD(hd_, g_, mh_) MK_PICK(hd_, g_, mh_, 2, 0, )
+#define MK_PICK_LC_Q8(hd_, g_, mh_) MK_PICK(hd_, g_, mh_, 1, 1, _lc_q8)
+#define MK_PICK_Q8(hd_, g_, mh_) MK_PICK(hd_, g_, mh_, 1, 0, _q8)
     MK_LC_VARIANTS(MK_PICK_LC)
+    MK_Q8_LC_VARIANTS(MK_PICK_LC_Q8)
+    MK_VARIANTS(MK_PICK_STD)
+    MK_Q8_VARIANTS(MK_PICK_Q8)
 #undef MK_PICK_LC
-#define MK_PICK(hd_, g_, mh_)                                         \
-    if (hd == hd_ && G == g_ && H == 256 * mh_) {                     \
-        *fn = mk_kernel_ptr_##hd_##_##g_##_##mh_();                   \
-        *fn_trace = mk_kernel_trace_ptr_##hd_##_##g_##_##mh_();       \
-        return 0;                                                     \
-    }
-    MK_VARIANTS(MK_PICK)
+#undef MK_PICK_STD
+#undef MK_PICK_LC_Q8
+#undef MK_PICK_Q8
 #undef MK_PICK
     *fn = *fn_trace = nullptr;
     return -1;
@@ -82,15 +100,26 @@ namespace {
         if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
     } while (0)
 
+// Where each weight goes in the arena: row copies (with, for int8 streams,
+// where the row's scale goes), column blocks of W_down, and for int8 the
+// W_down column scales kept in the GU tiles.
 struct Maps {
-    std::vector<std::vector<MkRowCopy>> q, k, v, o, gate, up;
+    std::vector<std::vector<MkRowCopyQ>> q, k, v, o, gate, up;
     std::vector<std::vector<MkColCopy>> down;
-    std::vector<MkRowCopy> lm;
+    std::vector<std::vector<MkScaleCopy>> down_scale;
+    std::vector<MkRowCopyQ> lm;
 };
+
+std::vector<MkRowCopy> plain_rows(const std::vector<MkRowCopyQ>& v) {
+    std::vector<MkRowCopy> r;
+    r.reserve(v.size());
+    for (const MkRowCopyQ& o : v) r.push_back(MkRowCopy{o.dst_off, o.src_row, o.col0, o.ncols});
+    return r;
+}
 
 // Tuning with defaults applied (grid size needs the SM count).
 struct Tune {
-    int ns_req, slot, l2pf, grid;
+    int ns_req, slot, l2pf, grid, wb;
 };
 
 Tune resolve_tuning(const mk_tuning* t) {
@@ -99,12 +128,13 @@ Tune resolve_tuning(const mk_tuning* t) {
     r.slot = (t && t->slot_kib > 0) ? t->slot_kib * 1024 : 32 * 1024;
     r.l2pf = (t && t->l2_prefetch_kib > 0) ? t->l2_prefetch_kib * 1024 : 0;   // default off (measured slower)
     r.grid = (t && t->grid_ctas > 0) ? t->grid_ctas : 0;
+    r.wb = (t && t->weight_int8) ? 1 : 2;
     return r;
 }
 
 // Shape checks shared by mk_create and the host layout utilities; the fused
 // kernel must also be built for the shape when need_kernel is set.
-int check_shape(const mk_config* c, bool need_kernel = true) {
+int check_shape(const mk_config* c, bool need_kernel = true, int wb = 2) {
     if (!c) return MK_ERR_INVALID_ARG;
     if (c->n_layers < 1 || c->hidden < 8 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 2 ||
         c->ffn < 1 || c->vocab < 1 || c->max_seq < 1 || !(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f))
@@ -113,7 +143,7 @@ int check_shape(const mk_config* c, bool need_kernel = true) {
     if (c->head_dim != 64 && c->head_dim != 128) return MK_ERR_UNSUPPORTED;
     const int G = c->n_q_heads / c->n_kv_heads;
     const void *fn = nullptr, *fn_trace = nullptr;
-    if (need_kernel && mk_kernel_variant(c->head_dim, G, c->hidden, false, &fn, &fn_trace) < 0)
+    if (need_kernel && mk_kernel_variant(c->head_dim, G, c->hidden, wb, false, &fn, &fn_trace) < 0)
         return MK_ERR_UNSUPPORTED;
     // GEMV row length K: 8-column chunks spread over min(32, K/8) lanes, so
     // K/8 divides 32 (short rows) or K is a multiple of 256 (long rows).
@@ -129,7 +159,7 @@ int check_shape(const mk_config* c, bool need_kernel = true) {
 
 int build_geom(const mk_config* c, const Tune& tu, int grid, int ns, MkGeom& g) {
     if (!mk_geom_init(g, c->n_layers, c->hidden, c->n_q_heads, c->n_kv_heads, c->head_dim, c->ffn, c->vocab,
-                      c->max_seq, grid, tu.slot, ns))
+                      c->max_seq, grid, tu.slot, ns, tu.wb))
         return MK_ERR_INVALID_ARG;
     if (g.TRh < 2 || g.TRo < 2 || g.JD < 1 || g.KB < 1 || tu.slot % 16) return MK_ERR_INVALID_ARG;
     if (ns < 1 || ns > 16) return MK_ERR_INVALID_ARG;
@@ -151,40 +181,50 @@ void build_plans(const MkGeom& g, std::vector<MkCtaPlan>& plans, int64_t& arena)
 }
 
 void build_maps(const MkGeom& g, const std::vector<MkCtaPlan>& plans, Maps& m) {
-    const int L = g.L, H = g.H, KO = g.G * g.hd;
+    const int L = g.L, H = g.H, KO = g.G * g.hd, wb = g.wb;
     m.q.assign(L, {}); m.k.assign(L, {}); m.v.assign(L, {}); m.o.assign(L, {});
-    m.gate.assign(L, {}); m.up.assign(L, {}); m.down.assign(L, {}); m.lm.clear();
+    m.gate.assign(L, {}); m.up.assign(L, {}); m.down.assign(L, {}); m.down_scale.assign(L, {}); m.lm.clear();
+    // rows of tiles of at most TR rows of K weights from `off` on: row i of a
+    // tile of R rows at tile + i * K * wb, its scale (int8) at tile + R * K + 4 i
+    auto row_tiles = [&](int64_t& off, int nrows, int TR, int K, auto&& emit) {
+        for (int r = 0; r < nrows; r += TR) {
+            const int R = std::min(TR, nrows - r);
+            for (int i = 0; i < R; ++i)
+                emit(r + i, off + (int64_t)i * K * wb, off + (int64_t)R * K + 4LL * i);
+            off += mk_row_tile_bytes(R, K, wb, 0);
+        }
+    };
     for (int c = 0; c < g.nC; ++c) {
         const MkCtaPlan& p = plans[c];
         for (int l = 0; l < L; ++l) {
-            const int64_t base = p.stream_off + (int64_t)l * p.layer_bytes;
-            int64_t off = base;
-            for (int r = 0; r < 2 * p.npairs; ++r) {
+            int64_t off = p.stream_off + (int64_t)l * p.layer_bytes;
+            row_tiles(off, 2 * p.npairs, g.TRh, H, [&](int r, int64_t d, int64_t so) {
                 int mat, row;
                 mk_qkv_row(g, p.g, p.pair0 + r / 2, r % 2, mat, row);
-                MkRowCopy rc{off, row, 0, H};
-                (mat == 0 ? m.q : mat == 1 ? m.k : m.v)[l].push_back(rc);
-                off += (int64_t)H * 2;
-            }
-            for (int r = 0; r < p.norows; ++r) {
-                m.o[l].push_back(MkRowCopy{off, (int64_t)(p.orow0 + r), p.g * KO, KO});
-                off += (int64_t)KO * 2;
-            }
+                (mat == 0 ? m.q : mat == 1 ? m.k : m.v)[l].push_back(MkRowCopyQ{d, row, 0, H, so});
+            });
+            row_tiles(off, p.norows, g.TRo, KO, [&](int r, int64_t d, int64_t so) {
+                m.o[l].push_back(MkRowCopyQ{d, (int64_t)(p.orow0 + r), p.g * KO, KO, so});
+            });
+            // a GU tile: n gate rows, n up rows (then for int8 their 2n scales
+            // and the n W_down column scales of the same j's)
             for (int j = 0; j < p.nj; j += g.JT) {
                 const int n = std::min(g.JT, p.nj - j);
-                for (int jj = 0; jj < n; ++jj)
-                    m.gate[l].push_back(MkRowCopy{off + (int64_t)jj * H * 2, (int64_t)(p.j0 + j + jj), 0, H});
-                for (int jj = 0; jj < n; ++jj)
-                    m.up[l].push_back(MkRowCopy{off + (int64_t)(n + jj) * H * 2, (int64_t)(p.j0 + j + jj), 0, H});
-                off += (int64_t)2 * n * H * 2;
+                const int64_t sc = off + (int64_t)2 * n * H;
+                for (int jj = 0; jj < n; ++jj) {
+                    const int64_t src = p.j0 + j + jj;
+                    m.gate[l].push_back(MkRowCopyQ{off + (int64_t)jj * H * wb, src, 0, H, sc + 4LL * jj});
+                    m.up[l].push_back(MkRowCopyQ{off + (int64_t)(n + jj) * H * wb, src, 0, H, sc + 4LL * (n + jj)});
+                    if (wb == 1) m.down_scale[l].push_back(MkScaleCopy{sc + 4LL * (2 * n + jj), src});
+                }
+                off += mk_row_tile_bytes(2 * n, H, wb, n);
             }
             if (p.nj > 0) m.down[l].push_back(MkColCopy{off, p.j0, p.nj});
         }
         int64_t off = p.stream_off + (int64_t)L * p.layer_bytes;
-        for (int r = 0; r < p.nv; ++r) {
-            m.lm.push_back(MkRowCopy{off, (int64_t)(p.v0 + r), 0, H});
-            off += (int64_t)H * 2;
-        }
+        row_tiles(off, p.nv, g.TRh, H, [&](int r, int64_t d, int64_t so) {
+            m.lm.push_back(MkRowCopyQ{d, (int64_t)(p.v0 + r), 0, H, so});
+        });
     }
 }
 
@@ -221,16 +261,21 @@ bool check_schedule(const MkGeom& g, const std::vector<MkCtaPlan>& plans, int64_
                     wbytes += bytes;
                 }
             });
-            if (!ok || wbytes != (int64_t)g.L * pl.layer_bytes + (int64_t)pl.nv * g.H * 2) return false;
+            if (!ok || wbytes != (int64_t)g.L * pl.layer_bytes + mk_lm_bytes(g, pl)) return false;
         }
     }
     return true;
 }
 
-int64_t weight_bytes_per_token(const mk_config* c) {
+// Weight bytes one step must read: every matrix once (bf16, or int8 codes
+// plus one fp32 scale per row / W_down column), the norm gains and one
+// embedding row (counted at 2 bytes per value).
+int64_t weight_bytes_per_token(const mk_config* c, int wb) {
     const int64_t H = c->hidden, qd = (int64_t)c->n_q_heads * c->head_dim, kvd = (int64_t)c->n_kv_heads * c->head_dim;
-    const int64_t per_layer = qd * H + 2 * kvd * H + H * qd + 3 * (int64_t)c->ffn * H + 2 * H;
-    return 2 * ((int64_t)c->n_layers * per_layer + (int64_t)c->vocab * H + H + H);
+    const int64_t F = c->ffn, V = c->vocab, L = c->n_layers;
+    const int64_t mat = L * (qd * H + 2 * kvd * H + H * qd + 3 * F * H) + V * H;
+    const int64_t scales = wb == 1 ? 4 * (L * (qd + 2 * kvd + H + 3 * F) + V) : 0;
+    return mat * wb + scales + 2 * (L * 2 * H + H + H);
 }
 
 }  // namespace
@@ -452,6 +497,7 @@ int mk_relayout_host(const mk_config* cfg, const mk_tuning* tuning, int32_t grid
     if (!w || !arena_out || grid_ctas < 1 || w->on_device) return MK_ERR_INVALID_ARG;
     if (!cfg->tie_embeddings && !w->lm_head) return MK_ERR_INVALID_ARG;
     Tune tu = resolve_tuning(tuning);
+    if (tu.wb != 2) return MK_ERR_UNSUPPORTED;   // int8 streams are quantized on the device only
     MkGeom g;
     if ((rc = build_geom(cfg, tu, grid_ctas, 1, g)) != MK_OK) return rc;
     std::vector<MkCtaPlan> plans;
@@ -461,9 +507,9 @@ int mk_relayout_host(const mk_config* cfg, const mk_tuning* tuning, int32_t grid
     build_maps(g, plans, m);
     uint8_t* A = reinterpret_cast<uint8_t*>(arena_out);
     memset(A, 0, (size_t)arena);
-    auto rows = [&](const std::vector<MkRowCopy>& ops, const void* src, int64_t cols) {
+    auto rows = [&](const std::vector<MkRowCopyQ>& ops, const void* src, int64_t cols) {
         const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
-        for (const MkRowCopy& op : ops) memcpy(A + op.dst_off, s + op.src_row * cols + op.col0, (size_t)op.ncols * 2);
+        for (const MkRowCopyQ& op : ops) memcpy(A + op.dst_off, s + op.src_row * cols + op.col0, (size_t)op.ncols * 2);
     };
     const int64_t H = g.H, qd = (int64_t)g.qh * g.hd;
     for (int l = 0; l < g.L; ++l) {
@@ -487,7 +533,7 @@ int mk_relayout_host(const mk_config* cfg, const mk_tuning* tuning, int32_t grid
 int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx** out) {
     if (!out) return MK_ERR_INVALID_ARG;
     *out = nullptr;
-    int rc = check_shape(cfg);
+    int rc = check_shape(cfg, true, resolve_tuning(tuning).wb);
     if (rc != MK_OK) return rc;
     mk_ctx* c = new mk_ctx();
     c->cfg = *cfg;
@@ -511,9 +557,11 @@ int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx*
         if ((rc = build_geom(cfg, c->tune, grid, ns, g)) != MK_OK) return fail(rc);
         if (g.smem_bytes + 1024 <= smem_optin) { c->geo = g; break; }
     }
-    if (mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, false, &c->kernel, &c->kernel_trace) < 0)
+    const int wb = c->tune.wb;
+    if (mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, wb, false, &c->kernel,
+                          &c->kernel_trace) < 0)
         return fail(MK_ERR_UNSUPPORTED);
-    if (mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, true, &c->kernel_tc,
+    if (mk_kernel_variant(cfg->head_dim, cfg->n_q_heads / kvh, cfg->hidden, wb, true, &c->kernel_tc,
                           &c->kernel_tc_trace) != 1)
         c->kernel_tc = c->kernel_tc_trace = nullptr;
     // both builds of a tensor-core shape read (and append) chunk-permuted K/V rows
@@ -588,6 +636,7 @@ void mk_destroy(mk_ctx* c) {
 
 int mk_enable_perop(mk_ctx* c, int32_t keep_rowmajor) {
     if (!c) return MK_ERR_INVALID_ARG;
+    if (keep_rowmajor && c->geo.wb != 2) return MK_ERR_UNSUPPORTED;   // the per-operator kernels read bf16
     if (c->weights_loaded && keep_rowmajor && !c->perop_ready) return MK_ERR_STATE;
     c->perop_enabled = keep_rowmajor != 0;
     return MK_OK;
@@ -616,23 +665,29 @@ int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
     Maps m;
     build_maps(g, c->plans, m);
 
+    const bool q8 = g.wb == 1;
+    const size_t max_elems = std::max({V * H, F * H, qd * H, kvd * H, H});
     uint16_t* staging = nullptr;
-    size_t staging_elems = 0;
-    if (!on_dev) {
-        staging_elems = std::max({V * H, F * H, qd * H, kvd * H, H});
-        MK_CU(cudaMalloc(&staging, staging_elems * 2));
-    }
+    if (!on_dev) MK_CU(cudaMalloc(&staging, max_elems * 2));
     MkRowCopy* d_rows = nullptr;
     MkColCopy* d_cols = nullptr;
-    size_t cap_rows = 0, cap_cols = 0;
+    MkRowCopyQ* d_rowsq = nullptr;
+    MkScaleCopy* d_scl = nullptr;
+    size_t cap_rows = 0, cap_cols = 0, cap_rowsq = 0, cap_scl = 0;
     uint16_t* gain_tmp = nullptr;
+    int8_t* q_tmp = nullptr;     // int8 streams: one matrix's codes and scales
+    float* s_tmp = nullptr;
     int rc = MK_OK;
     auto cleanup = [&]() {
         cudaStreamSynchronize(st);
         if (staging) cudaFree(staging);
         if (d_rows) cudaFree(d_rows);
         if (d_cols) cudaFree(d_cols);
+        if (d_rowsq) cudaFree(d_rowsq);
+        if (d_scl) cudaFree(d_scl);
         if (gain_tmp) cudaFree(gain_tmp);
+        if (q_tmp) cudaFree(q_tmp);
+        if (s_tmp) cudaFree(s_tmp);
     };
 #define MK_TRY(x)                       \
     do {                                \
@@ -645,13 +700,31 @@ int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
         if (e_ != cudaSuccess) { rc = cuda_fail(e_, #x); cleanup(); return rc; } \
     } while (0)
 
-    auto gather_rows = [&](const std::vector<MkRowCopy>& ops, const void* src, size_t rows, size_t cols) -> int {
+    if (q8) {
+        cudaError_t e = cudaMalloc(&q_tmp, max_elems);
+        if (e == cudaSuccess) e = cudaMalloc(&s_tmp, std::max({V, F, H, qd, kvd}) * 4);
+        if (e != cudaSuccess) { rc = cuda_fail(e, "int8 staging"); cleanup(); return rc; }
+    }
+    // bf16 streams copy the rows; int8 streams quantize the matrix (per row)
+    // and copy codes and row scales
+    auto gather_rows = [&](const std::vector<MkRowCopyQ>& ops, const void* src, size_t rows, size_t cols) -> int {
         const uint16_t* d = nullptr;
         int r = copy_matrix_to_device(src, on_dev, rows * cols * 2, staging, &d, st);
         if (r != MK_OK) return r;
-        r = upload_ops(ops, &d_rows, &cap_rows, st);
-        if (r != MK_OK) return r;
-        cudaError_t e = mk_launch_relayout_rows(c->arena, d, (int64_t)cols, d_rows, (int)ops.size(), st);
+        cudaError_t e;
+        if (q8) {
+            e = mk_launch_quantize_q8(d, (int64_t)rows, (int64_t)cols, 0, q_tmp, s_tmp, st);
+            if (e != cudaSuccess) return cuda_fail(e, "quantize rows");
+            r = upload_ops(ops, &d_rowsq, &cap_rowsq, st);
+            if (r != MK_OK) return r;
+            e = mk_launch_relayout_rows_q8(c->arena, q_tmp, (int64_t)cols, s_tmp, d_rowsq, (int)ops.size(), st);
+        } else {
+            const std::vector<MkRowCopy> plain = plain_rows(ops);
+            r = upload_ops(plain, &d_rows, &cap_rows, st);
+            if (r != MK_OK) return r;
+            e = mk_launch_relayout_rows(c->arena, d, (int64_t)cols, d_rows, (int)ops.size(), st);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(st);   // `plain` must outlive its copy
+        }
         if (e != cudaSuccess) return cuda_fail(e, "relayout rows");
         e = cudaStreamSynchronize(st);   // staging and the op buffer are reused by the next matrix
         return e == cudaSuccess ? MK_OK : cuda_fail(e, "relayout rows sync");
@@ -683,7 +756,15 @@ int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
             const uint16_t* d = nullptr;
             MK_TRY(copy_matrix_to_device(w->w_down[l], on_dev, H * F * 2, staging, &d, st));
             MK_TRY(upload_ops(m.down[l], &d_cols, &cap_cols, st));
-            MK_TRYCU(mk_launch_relayout_cols(c->arena, d, (int)H, (int)F, d_cols, (int)m.down[l].size(), st));
+            if (q8) {   // per-column scales, kept in the GU tiles of the same j's
+                MK_TRYCU(mk_launch_quantize_q8(d, (int64_t)H, (int64_t)F, 1, q_tmp, s_tmp, st));
+                MK_TRYCU(mk_launch_relayout_cols_q8(c->arena, q_tmp, (int)H, (int)F, d_cols, (int)m.down[l].size(),
+                                                    st));
+                MK_TRY(upload_ops(m.down_scale[l], &d_scl, &cap_scl, st));
+                MK_TRYCU(mk_launch_scatter_scales(c->arena, s_tmp, d_scl, (int)m.down_scale[l].size(), st));
+            } else {
+                MK_TRYCU(mk_launch_relayout_cols(c->arena, d, (int)H, (int)F, d_cols, (int)m.down[l].size(), st));
+            }
             MK_TRYCU(cudaStreamSynchronize(st));
         }
         if (c->perop_enabled && !c->perop_ready) {
@@ -788,6 +869,17 @@ int mk_set_kv(mk_ctx* c, int32_t layer, const void* k, const void* v, int32_t n_
         MK_CU(cudaMemcpyAsync(c->kc + dst, (const uint8_t*)k + h * row, row, cudaMemcpyDefault, st));
         MK_CU(cudaMemcpyAsync(c->vc + dst, (const uint8_t*)v + h * row, row, cudaMemcpyDefault, st));
     }
+    MK_CU(cudaStreamSynchronize(st));
+    return MK_OK;
+}
+
+int mk_read_arena(mk_ctx* c, int64_t offset, int64_t bytes, void* out, void* stream) {
+    if (!c || !out || offset < 0 || bytes < 0 || offset > c->arena_bytes || bytes > c->arena_bytes - offset)
+        return MK_ERR_INVALID_ARG;
+    if (!c->weights_loaded) return MK_ERR_STATE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    MK_CU(cudaSetDevice(c->device));
+    if (bytes > 0) MK_CU(cudaMemcpyAsync(out, c->arena + offset, (size_t)bytes, cudaMemcpyDefault, st));
     MK_CU(cudaStreamSynchronize(st));
     return MK_OK;
 }
@@ -1009,6 +1101,7 @@ int mk_decode_step_perop(mk_ctx* c, int32_t token, int32_t pos, float* logits_ou
 
 int mk_prefill(mk_ctx* c, const int32_t* tokens, int32_t n, int32_t start_pos, float* logits_out, void* stream) {
     if (!c || !tokens || n < 1 || start_pos < 0) return MK_ERR_INVALID_ARG;
+    if (c->geo.wb != 2) return MK_ERR_UNSUPPORTED;   // the prefill GEMMs read the bf16 row-major copies
     if (!c->weights_loaded || !c->perop_ready) return MK_ERR_STATE;
     const MkGeom& g = c->geo;
     if ((int64_t)start_pos + n > g.max_seq) return MK_ERR_INVALID_ARG;
@@ -1070,12 +1163,13 @@ int mk_get_info(const mk_ctx* c, mk_info* o) {
     o->sm_count = c->sm_count;
     o->l2_prefetch_bytes = c->tune.l2pf;
     o->arena_bytes = c->arena_bytes;
-    o->weight_bytes_per_token = weight_bytes_per_token(&c->cfg);
+    o->weight_bytes_per_token = weight_bytes_per_token(&c->cfg, c->geo.wb);
     o->kv_bytes_per_position = (int64_t)2 * c->geo.L * c->geo.kvh * c->geo.hd * 2;
     o->device_bytes = c->device_bytes;
     o->attn_tc = c->kernel_tc ? 1 : 0;
     o->attn_tc_min_ctx = c->kernel_tc ? (int32_t)mk_tc_min_ctx(c) : -1;
     o->attn_pos_per_cta = c->attn_ctas_force > 0 ? 0 : c->attn_pos_per_cta;
+    o->weight_int8 = c->geo.wb == 1 ? 1 : 0;
     return MK_OK;
 }
 

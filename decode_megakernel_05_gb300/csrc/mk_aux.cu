@@ -65,6 +65,88 @@ __global__ void mk_kv_rows_kernel(uint4* plain, uint4* cache_layer, int kvh, int
     else plain[i] = *c;
 }
 
+// One block per group (a row, or a column when col_scaled): the group's
+// largest |w| by a block reduction, then every code.
+__global__ void mk_quantize_q8_kernel(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int8_t* q,
+                                      float* scale) {
+    __shared__ float red[32];
+    const int64_t gi = blockIdx.x;
+    const int64_t len = col_scaled ? rows : cols;
+    auto at = [&](int64_t k) { return col_scaled ? k * cols + gi : gi * cols + k; };
+    float amax = 0.f;
+    for (int64_t k = threadIdx.x; k < len; k += blockDim.x)
+        amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)w[at(k)] << 16)));
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
+    const float sg = __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0) scale[gi] = sg;
+    for (int64_t k = threadIdx.x; k < len; k += blockDim.x) {
+        float c = 0.f;
+        if (sg > 0.f) c = rintf(__fdiv_rn(__uint_as_float((uint32_t)w[at(k)] << 16), sg));
+        c = fminf(fmaxf(c, -127.f), 127.f);
+        q[at(k)] = (int8_t)c;
+    }
+}
+
+// One block per stored row: ncols int8 (a multiple of 16) and the row's scale.
+__global__ void mk_relayout_rows_q8_kernel(uint8_t* arena, const int8_t* q, int64_t cols, const float* scale,
+                                           const MkRowCopyQ* ops, int n) {
+    const int i = blockIdx.x;
+    if (i >= n) return;
+    const MkRowCopyQ op = ops[i];
+    const uint4* s = reinterpret_cast<const uint4*>(q + op.src_row * cols + op.col0);
+    uint4* d = reinterpret_cast<uint4*>(arena + op.dst_off);
+    for (int k = threadIdx.x; k < op.ncols / 16; k += blockDim.x) d[k] = s[k];
+    if (threadIdx.x == 0) *reinterpret_cast<float*>(arena + op.scale_off) = scale[op.src_row];
+}
+
+// Column gather of an int8 W_down [H][F]: columns j0 .. j0+nj-1 as H contiguous bytes each.
+__global__ void mk_relayout_cols_q8_kernel(uint8_t* arena, const int8_t* q, int H, int F, const MkColCopy* ops, int n) {
+    const int i = blockIdx.x;
+    if (i >= n) return;
+    const MkColCopy op = ops[i];
+    const int r = blockIdx.y * blockDim.x + threadIdx.x;
+    if (r >= H) return;
+    int8_t* d = reinterpret_cast<int8_t*>(arena + op.dst_off);
+    const int8_t* s = q + (int64_t)r * F + op.j0;
+    for (int jj = 0; jj < op.nj; ++jj) d[(int64_t)jj * H + r] = s[jj];
+}
+
+__global__ void mk_scatter_scales_kernel(uint8_t* arena, const float* scale, const MkScaleCopy* ops, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) *reinterpret_cast<float*>(arena + ops[i].dst_off) = scale[ops[i].idx];
+}
+
+cudaError_t mk_launch_quantize_q8(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int8_t* q,
+                                  float* scale, cudaStream_t st) {
+    const int64_t ng = col_scaled ? cols : rows;
+    if (ng <= 0) return cudaSuccess;
+    mk_quantize_q8_kernel<<<(unsigned)ng, 256, 0, st>>>(w, rows, cols, col_scaled, q, scale);
+    return cudaGetLastError();
+}
+cudaError_t mk_launch_relayout_rows_q8(uint8_t* arena, const int8_t* q, int64_t cols, const float* scale,
+                                       const MkRowCopyQ* ops, int n, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    mk_relayout_rows_q8_kernel<<<n, 128, 0, st>>>(arena, q, cols, scale, ops, n);
+    return cudaGetLastError();
+}
+cudaError_t mk_launch_relayout_cols_q8(uint8_t* arena, const int8_t* q, int H, int F, const MkColCopy* ops, int n,
+                                       cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    dim3 grid(n, (H + 255) / 256);
+    mk_relayout_cols_q8_kernel<<<grid, 256, 0, st>>>(arena, q, H, F, ops, n);
+    return cudaGetLastError();
+}
+cudaError_t mk_launch_scatter_scales(uint8_t* arena, const float* scale, const MkScaleCopy* ops, int n,
+                                     cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    mk_scatter_scales_kernel<<<(n + 255) / 256, 256, 0, st>>>(arena, scale, ops, n);
+    return cudaGetLastError();
+}
+
 cudaError_t mk_launch_kv_rows(uint16_t* plain, uint16_t* cache_layer, int kvh, int n_pos, int pos0, int max_seq, int hd,
                               int swz, int to_cache, cudaStream_t st) {
     const int nch = hd / 8;

@@ -13,6 +13,33 @@ struct MkColCopy {     // arena + dst_off <- columns j0 .. j0+nj-1 of W_down, ea
     int32_t j0, nj;
 };
 
+// Weight-only INT8 re-layout: arena + dst_off <- ncols int8 of q[src_row][col0 ..],
+// and the row's scale (fp32) at arena + scale_off.
+struct MkRowCopyQ {
+    int64_t dst_off;
+    int64_t src_row;
+    int32_t col0, ncols;
+    int64_t scale_off;
+};
+// arena + dst_off (fp32) <- scale[idx]
+struct MkScaleCopy {
+    int64_t dst_off;
+    int64_t idx;
+};
+
+// Symmetric absmax INT8 quantization of a bf16 matrix [rows][cols] per row
+// (or per column with col_scaled): scale = max|w| / 127, code = round(w /
+// scale) ties to even, both float operations rounded to nearest; a group of
+// zeros gets scale 0 and codes 0.
+cudaError_t mk_launch_quantize_q8(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int8_t* q,
+                                  float* scale, cudaStream_t st);
+cudaError_t mk_launch_relayout_rows_q8(uint8_t* arena, const int8_t* q, int64_t cols, const float* scale,
+                                       const MkRowCopyQ* ops, int n, cudaStream_t st);
+cudaError_t mk_launch_relayout_cols_q8(uint8_t* arena, const int8_t* q, int H, int F, const MkColCopy* ops, int n,
+                                       cudaStream_t st);
+cudaError_t mk_launch_scatter_scales(uint8_t* arena, const float* scale, const MkScaleCopy* ops, int n,
+                                     cudaStream_t st);
+
 cudaError_t mk_launch_relayout_rows(uint8_t* arena, const uint16_t* src, int64_t src_cols, const MkRowCopy* ops, int n,
                                     cudaStream_t st);
 cudaError_t mk_launch_relayout_cols(uint8_t* arena, const uint16_t* src, int H, int F, const MkColCopy* ops, int n,

@@ -25,6 +25,14 @@
 //   LM    : rows v in split(V, nC, c) of the LM head (the embedding when tied).
 // A tile is TRh rows (QKV, LM), TRo rows (O), one GU group, or JD columns (D);
 // the last tile of a block may be short.  Every tile is a multiple of 16 bytes.
+//
+// Weight-only INT8 streams (wb = 1) store each weight as one signed byte with
+// a float scale per output row (QKV, O, gate, up, LM head) or per input
+// column (W_down): a row tile is its R rows of K bytes, then the R rows'
+// scales; a GU tile is its n gate rows and n up rows, then their 2n scales,
+// then the n column scales of W_down for the same j's (the down projection
+// folds them into SiLU(gate) * up); a D tile is columns of H bytes.  Each tile
+// is padded to 16 bytes.
 #pragma once
 #include <stdint.h>
 
@@ -78,9 +86,25 @@ struct MkTopP {
 
 MK_HD int64_t mk_split(int64_t n, int64_t parts, int64_t k) { return (k * n) / parts; }
 
-// Rows per tile for a row-major GEMV tile of K bf16 columns: as many as fill
-// a ring slot, even (QKV pairs and gate/up groups never straddle a tile).
-MK_HD int mk_tile_rows(int K, int slot_bytes) { return (slot_bytes / (2 * K)) & ~1; }
+// Bytes of a row tile: R rows of K weights of wb bytes, and for int8 (wb = 1)
+// the R row scales plus `extra` more scales, padded to 16 bytes.
+MK_HD int mk_row_tile_bytes(int R, int K, int wb, int extra) {
+    int64_t b = (int64_t)R * K * wb;
+    if (wb == 1) b += 4LL * (R + extra);
+    return (int)((b + 15) & ~(int64_t)15);
+}
+
+// Rows per tile for a row-major GEMV tile of K columns: as many as fill a
+// ring slot, even (QKV pairs and gate/up groups never straddle a tile).  For
+// int8 the tile also holds the scales: gu_extra adds the half-as-many W_down
+// column scales of a GU tile.
+MK_HD int mk_tile_rows_wb(int K, int slot_bytes, int wb, bool gu_extra) {
+    if (wb == 2) return (slot_bytes / (2 * K)) & ~1;
+    int r = (slot_bytes / K) & ~1;
+    while (r > 2 && mk_row_tile_bytes(r, K, 1, gu_extra ? r / 2 : 0) > slot_bytes) r -= 2;
+    return r;
+}
+MK_HD int mk_tile_rows(int K, int slot_bytes) { return mk_tile_rows_wb(K, slot_bytes, 2, false); }
 
 // Column blocks of the hidden-width GEMV (QKV, gate/up): rows of H = 256 * MH
 // columns are split into min(4, MH) blocks, one per consumer warp of a row slot.
@@ -104,6 +128,7 @@ struct MkGeom {
     int32_t max_rows, max_nj;    // per-CTA maxima (QKV rows, FFN slice)
     int32_t smem_bytes;
     int32_t kv_swz;              // K/V cache rows chunk-permuted (mk_kv_index); set with the long-context build
+    int32_t wb;                  // bytes per weight in the stream: 2 bf16, 1 int8 (weight-only INT8)
     // shared-memory carve-up (byte offsets from the dynamic smem base)
     int32_t off_full, off_empty, off_xv, off_ov, off_part, off_u, off_xres, off_xres2, off_rope,
         off_red, off_sc, off_misc;
@@ -131,9 +156,11 @@ MK_HD constexpr bool mk_attn_tc(int hd, int G) { return hd == 64 && G == 4; }
 // Fills everything but smem offsets from the shape; returns false if the
 // shape is outside what the kernels support.
 MK_HD bool mk_geom_init(MkGeom& g, int L, int H, int qh, int kvh, int hd, int F, int V, int max_seq, int nC,
-                        int slot_bytes, int ns) {
+                        int slot_bytes, int ns, int wb = 2) {
     g.L = L; g.H = H; g.qh = qh; g.kvh = kvh; g.hd = hd; g.F = F; g.V = V; g.max_seq = max_seq;
     g.kv_swz = 0;
+    g.wb = wb;
+    if (wb != 1 && wb != 2) return false;
     if (L < 1 || H < 8 || qh < 1 || kvh < 1 || F < 1 || V < 1 || max_seq < 1 || nC < 1) return false;
     if (qh % kvh != 0 || nC % kvh != 0) return false;
     g.G = qh / kvh;
@@ -145,10 +172,10 @@ MK_HD bool mk_geom_init(MkGeom& g, int L, int H, int qh, int kvh, int hd, int F,
     // a consumer lane holds its share of a hidden-width tile in registers
     // (16 chunks of 16 bytes at most): slots of 32 KB at most
     if (slot_bytes > 32768) return false;
-    g.TRh = mk_tile_rows(H, slot_bytes);
-    g.TRo = mk_tile_rows(g.G * hd, slot_bytes);
+    g.TRh = mk_tile_rows_wb(H, slot_bytes, wb, true);
+    g.TRo = mk_tile_rows_wb(g.G * hd, slot_bytes, wb, false);
     g.JT = g.TRh / 2;
-    g.JD = slot_bytes / (2 * H);
+    g.JD = slot_bytes / (wb * H);
     g.KB = slot_bytes / (2 * hd);
     g.max_rows = 2 * (int)((g.NP + g.CPG - 1) / g.CPG);
     g.max_nj = (F + nC - 1) / nC;
@@ -252,6 +279,22 @@ MK_HD int mk_cnt_tp(const MkGeom& g, int k) { return 2 * g.L * g.kvh + 2 * g.L +
 MK_HD int mk_cnt_done(const MkGeom& g) { return 2 * g.L * g.kvh + 2 * g.L + MK_TP_ITERS + 1; }
 MK_HD int mk_cnt_total(const MkGeom& g) { return mk_cnt_done(g) + 1; }
 
+MK_HD int mk_imin(int a, int b) { return a < b ? a : b; }
+
+// Bytes of the weight tiles of one layer of a CTA's stream (QKV, O, GU, D).
+MK_HD int64_t mk_layer_bytes(const MkGeom& g, const MkCtaPlan& p) {
+    int64_t b = 0;
+    const int nr = 2 * p.npairs, KO = g.G * g.hd;
+    for (int r = 0; r < nr; r += g.TRh) b += mk_row_tile_bytes(mk_imin(g.TRh, nr - r), g.H, g.wb, 0);
+    for (int r = 0; r < p.norows; r += g.TRo) b += mk_row_tile_bytes(mk_imin(g.TRo, p.norows - r), KO, g.wb, 0);
+    for (int j = 0; j < p.nj; j += g.JT) {
+        const int n = mk_imin(g.JT, p.nj - j);
+        b += mk_row_tile_bytes(2 * n, g.H, g.wb, n);
+    }
+    for (int j = 0; j < p.nj; j += g.JD) b += (int64_t)mk_imin(g.JD, p.nj - j) * g.H * g.wb;
+    return b;
+}
+
 // Per-CTA plan; stream offsets are filled by the caller.
 MK_HD void mk_cta_plan(const MkGeom& g, int c, MkCtaPlan& p) {
     p.g = c / g.CPG;
@@ -264,17 +307,20 @@ MK_HD void mk_cta_plan(const MkGeom& g, int c, MkCtaPlan& p) {
     p.j0 = (int)a; p.nj = (int)(b - a);
     a = mk_split(g.V, g.nC, c); b = mk_split(g.V, g.nC, c + 1);
     p.v0 = (int)a; p.nv = (int)(b - a);
-    p.layer_bytes = (int64_t)2 * p.npairs * g.H * 2 + (int64_t)p.norows * g.G * g.hd * 2 +
-                    (int64_t)2 * p.nj * g.H * 2 + (int64_t)p.nj * g.H * 2;
+    p.layer_bytes = mk_layer_bytes(g, p);
     p.stream_off = 0;
 }
 
-MK_HD int64_t mk_cta_stream_bytes(const MkGeom& g, const MkCtaPlan& p) {
-    int64_t b = (int64_t)g.L * p.layer_bytes + (int64_t)p.nv * g.H * 2;
-    return (b + 255) & ~(int64_t)255;
+MK_HD int64_t mk_lm_bytes(const MkGeom& g, const MkCtaPlan& p) {
+    int64_t b = 0;
+    for (int r = 0; r < p.nv; r += g.TRh) b += mk_row_tile_bytes(mk_imin(g.TRh, p.nv - r), g.H, g.wb, 0);
+    return b;
 }
 
-MK_HD int mk_imin(int a, int b) { return a < b ? a : b; }
+MK_HD int64_t mk_cta_stream_bytes(const MkGeom& g, const MkCtaPlan& p) {
+    int64_t b = (int64_t)g.L * p.layer_bytes + mk_lm_bytes(g, p);
+    return (b + 255) & ~(int64_t)255;
+}
 
 // The share of attended positions [0, pos] of CTA i of a KV group when the
 // first A CTAs of each group run the attention (the length-adaptive split:
@@ -312,7 +358,7 @@ MK_HD void mk_walk_tiles(const MkGeom& g, const MkCtaPlan& pl, const uint8_t* ar
     for (int l = 0; l < g.L; ++l) {
         const int nr = 2 * pl.npairs;
         for (int r = 0; r < nr; r += g.TRh) {
-            uint32_t by = (uint32_t)(mk_imin(g.TRh, nr - r) * H * 2);
+            uint32_t by = (uint32_t)mk_row_tile_bytes(mk_imin(g.TRh, nr - r), H, g.wb, 0);
             f((const void*)cur, by); cur += by;
         }
         const int64_t kvoff = ((int64_t)l * g.kvh + pl.g) * g.max_seq * g.hd;
@@ -322,20 +368,21 @@ MK_HD void mk_walk_tiles(const MkGeom& g, const MkCtaPlan& pl, const uint8_t* ar
             f((const void*)(vc + kvoff + (int64_t)q * g.hd), by);
         }
         for (int r = 0; r < pl.norows; r += g.TRo) {
-            uint32_t by = (uint32_t)(mk_imin(g.TRo, pl.norows - r) * KO * 2);
+            uint32_t by = (uint32_t)mk_row_tile_bytes(mk_imin(g.TRo, pl.norows - r), KO, g.wb, 0);
             f((const void*)cur, by); cur += by;
         }
         for (int j = 0; j < pl.nj; j += g.JT) {
-            uint32_t by = (uint32_t)(2 * mk_imin(g.JT, pl.nj - j) * H * 2);
+            const int n = mk_imin(g.JT, pl.nj - j);
+            uint32_t by = (uint32_t)mk_row_tile_bytes(2 * n, H, g.wb, n);
             f((const void*)cur, by); cur += by;
         }
         for (int j = 0; j < pl.nj; j += g.JD) {
-            uint32_t by = (uint32_t)(mk_imin(g.JD, pl.nj - j) * H * 2);
+            uint32_t by = (uint32_t)(mk_imin(g.JD, pl.nj - j) * H * g.wb);
             f((const void*)cur, by); cur += by;
         }
     }
     for (int r = 0; r < pl.nv; r += g.TRh) {
-        uint32_t by = (uint32_t)(mk_imin(g.TRh, pl.nv - r) * H * 2);
+        uint32_t by = (uint32_t)mk_row_tile_bytes(mk_imin(g.TRh, pl.nv - r), H, g.wb, 0);
         f((const void*)cur, by); cur += by;
     }
 }

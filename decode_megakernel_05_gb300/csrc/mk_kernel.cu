@@ -11,8 +11,15 @@
 #ifndef MK_LC_V
 #define MK_LC_V 0   // 1: the long-context build (see mk_decode_kernel)
 #endif
-#if MK_LC_V
+#ifndef MK_WB_V
+#define MK_WB_V 2   // bytes per streamed weight: 2 bf16, 1 weight-only INT8
+#endif
+#if MK_LC_V && MK_WB_V == 1
+#define MK_SFX _lc_q8
+#elif MK_LC_V
 #define MK_SFX _lc
+#elif MK_WB_V == 1
+#define MK_SFX _q8
 #else
 #define MK_SFX
 #endif
@@ -24,10 +31,10 @@
 // kernel launched while a segment trace is requested).
 #ifdef MK_NO_TRACE
 extern "C" const void* MK_CAT(mk_kernel_ptr_, MK_HD_V, MK_G_V, MK_MH_V, MK_SFX)(void) {
-    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V, MK_LC_V>;
+    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V, MK_LC_V, MK_WB_V>;
 }
 #else
 extern "C" const void* MK_CAT(mk_kernel_trace_ptr_, MK_HD_V, MK_G_V, MK_MH_V, MK_SFX)(void) {
-    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V, MK_LC_V>;
+    return (const void*)&mk::mk_decode_kernel<MK_HD_V, MK_G_V, MK_MH_V, MK_LC_V, MK_WB_V>;
 }
 #endif

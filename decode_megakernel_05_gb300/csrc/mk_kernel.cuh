@@ -609,9 +609,45 @@ __device__ __forceinline__ void fma_chunk(const uint4 w, const float4 xl, const 
     a1 = __ffma2_rn(bf2_lo_hi(w.w), make_float2(xh.z, xh.w), a1);
 }
 
+// Weight-only INT8 chunks: 8 int8 weights (8 bytes, columns in the same order
+// as a bf16 chunk's 8 columns) -> fp32.  Each byte, offset by 128 (the xor
+// with 0x80), becomes the low byte of the mantissa of 2^23 (exact), and
+// 2^23 + 128 comes off: bytes k and k+1 of a give the pair of values.
+__device__ __forceinline__ uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ float2 i8pair(uint32_t a, int k) {
+    const float x = __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7540u + k));
+    const float y = __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7540u + k + 1));
+    return __fadd2_rn(make_float2(x, y), make_float2(-8388736.f, -8388736.f));
+}
+__device__ __forceinline__ void fma_chunk8(const uint2 w, const float4 xl, const float4 xh, float2& a0, float2& a1) {
+    const uint32_t lo = w.x ^ 0x80808080u, hi = w.y ^ 0x80808080u;
+    a0 = __ffma2_rn(i8pair(lo, 0), make_float2(xl.x, xl.y), a0);
+    a1 = __ffma2_rn(i8pair(lo, 2), make_float2(xl.z, xl.w), a1);
+    a0 = __ffma2_rn(i8pair(hi, 0), make_float2(xh.x, xh.y), a0);
+    a1 = __ffma2_rn(i8pair(hi, 2), make_float2(xh.z, xh.w), a1);
+}
+// A chunk of 8 weights: 16 bytes of bf16 (WB = 2) or 8 bytes of int8 (WB = 1).
+template <int WB> struct WChunk;
+template <> struct WChunk<2> {
+    using T = uint4;
+    static __device__ __forceinline__ T load(const void* p) { return lds128(p); }
+    static __device__ __forceinline__ T zero() { return make_uint4(0u, 0u, 0u, 0u); }
+    static __device__ __forceinline__ void fma(const T w, const float4 xl, const float4 xh, float2& a0, float2& a1) {
+        fma_chunk(w, xl, xh, a0, a1);
+    }
+};
+template <> struct WChunk<1> {
+    using T = uint2;
+    static __device__ __forceinline__ T load(const void* p) { return lds64(p); }
+    static __device__ __forceinline__ T zero() { return make_uint2(0x80808080u ^ 0x80808080u, 0u); }
+    static __device__ __forceinline__ void fma(const T w, const float4 xl, const float4 xh, float2& a0, float2& a1) {
+        fma_chunk8(w, xl, xh, a0, a1);
+    }
+};
+
 // Dot products of up to 4 rows (nv valid, rows r0 + k*step) with the
-// split-order vector xs; each lane covers MR chunks of 8 columns.
-template <int MR, int LPR>
+// split-order vector xs; each lane covers MR chunks of 8 columns (8 * WB bytes).
+template <int MR, int LPR, int WB = 2>
 __device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t step, int nv, const float* xs, int K, int ll,
                                           float o[4]) {
     float2 a[4][2];
@@ -625,7 +661,7 @@ __device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t step, int nv
         const float4 xl = xlo[ch], xh = xhi[ch];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-            if (r < nv) fma_chunk(lds128(r0 + r * step + (size_t)ch * 16), xl, xh, a[r][0], a[r][1]);
+            if (r < nv) WChunk<WB>::fma(WChunk<WB>::load(r0 + r * step + (size_t)ch * (8 * WB)), xl, xh, a[r][0], a[r][1]);
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) o[r] = (a[r][0].x + a[r][0].y) + (a[r][1].x + a[r][1].y);
@@ -653,7 +689,9 @@ __device__ void gemv_cfg(GemvCfg& c, int nrows, int TR, int RPP) {
     for (int w = 0; w < MK_NCW; ++w) { c.grp[w] = (int8_t)(w / wpg); c.wg[w] = (int8_t)(w % wpg); }
 }
 
-template <int MR, int LPR, class Epi>
+// WB = 1: int8 rows, each row's sum times the row's scale from the tile's
+// tail before epi() gets it.
+template <int MR, int LPR, int WB, class Epi>
 __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec,
                                              int nrows, int TR, const GemvCfg& cfg, bool ab, Epi&& epi,
                                              int trace_slot = -1, int dl = 0, int dmark = -1) {
@@ -664,7 +702,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
     const int ntiles = cfg.ntiles, rw = cfg.rw, wpg = cfg.wpg, ngrp = cfg.ngrp;
     const int grp = cfg.grp[w], wg = cfg.wg[w];
     const int rows_per_warp = rw * RPP;
-    const size_t rb = (size_t)K * 2;
+    const size_t rb = (size_t)K * WB;
     int turn = 0;   // ti mod ngrp
     for (int ti = 0; ti < ntiles && !ab; ++ti) {
         const bool mine = turn == grp;
@@ -672,7 +710,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
         if (!mine) { ring.advance(p.geo.ns); continue; }   // another group's tile
         const int R = min(TR, nrows - ti * TR);
         const uint8_t* tile;
-        const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
+        const bool ok = take_tile(p, s, ring, (uint32_t)mk_row_tile_bytes(R, K, WB, 0), tile);
         if (trace_slot >= 0 && MK_TRACE_ON && p.trace && p.trace_detail == 1 && threadIdx.x == 0 && ti < 256)
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
         if (dmark >= 0 && ti == 0) MK_TRACE_D(dl, dmark);   // thread 0 took its first tile
@@ -682,7 +720,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                 const int r0 = base + sub;
                 const int nv = r0 < R ? min(rw, (R - r0 + RPP - 1) / RPP) : 0;
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
-                if (nv > 0) dot_rows4<MR, LPR>(tile + r0 * rb, rb * RPP, nv, vec, K, ll, v);
+                if (nv > 0) dot_rows4<MR, LPR, WB>(tile + r0 * rb, rb * RPP, nv, vec, K, ll, v);
                 if (dmark >= 0 && ti == 0 && base == 0) {   // detail trace: the first pass's dot products done
                     float z = v[0] + v[1] + v[2] + v[3];
                     asm volatile("" : "+f"(z));
@@ -697,9 +735,10 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                     }
                 }
                 if (ll == 0) {
+                    const float* scl = reinterpret_cast<const float*>(tile + (size_t)R * K);   // int8: row scales
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        if (k < nv) epi(ti * TR + r0 + k * RPP, v[k]);
+                        if (k < nv) epi(ti * TR + r0 + k * RPP, WB == 1 ? v[k] * scl[r0 + k * RPP] : v[k]);
                 }
                 if (dmark >= 0 && ti == 0 && base == 0) MK_TRACE_D(dl, 14);   // its sums handed to epi
             }
@@ -738,14 +777,22 @@ struct WideGemv {
 template <int MH>
 struct WidePart { static constexpr int NKB = MH < 4 ? MH : 4; };
 
-template <int MH, int NG>
+// WB = 1 (int8 rows): the same columns per chunk (8 bytes instead of 16), and
+// each row's partials times the row's scale from the tile's tail; a GU tile's
+// W_down column scales (after the row scales) go to tsink[j] for the j's it
+// covers (the caller multiplies them into SiLU(gate) * up).
+template <int MH, int NG, int WB>
 __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring& ring, const float* xs, int nrows,
-                                          int TR, bool ab, float* part) {
+                                          int TR, bool ab, float* part, float* tsink) {
     using W = WideGemv<MH, NG>;
+    using C = WChunk<WB>;
     constexpr int K = W::K, NKB = W::NKB, CPL = W::CPL, NRS = W::NRS, WPG = W::WPG;
     constexpr int PS = WidePart<MH>::NKB;
     static_assert(W::ok && NKB <= PS, "wide GEMV mapping");
-    constexpr int RPW = 16 / CPL;   // rows of a tile per warp at most (16 chunks per lane: slots of 32 KB at most)
+    // rows of a tile per warp at most: 16 chunks of 16 bytes per lane (slots of
+    // 32 KB at most), or 32 chunks of 8 bytes for int8
+    constexpr int RPW = (16 / CPL) * (3 - WB);
+    constexpr int NPS = RPW / 4;    // passes of four rows
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = w / WPG, wg = w % WPG;
     const int cb = wg % NKB, rs = wg / NKB;
@@ -761,11 +808,25 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
         if (NG > 1 && (ti % NG) != grp) { ring.advance(p.geo.ns); continue; }   // another group's tile
         const int R0 = ti * TR, R = min(TR, nrows - R0);
         const uint8_t* tile;
-        const bool ok = take_tile(p, s, ring, (uint32_t)(R * K * 2), tile);
+        const bool ok = take_tile(p, s, ring, (uint32_t)mk_row_tile_bytes(R, K, WB, tsink ? R / 2 : 0), tile);
         // this warp's rows of the tile: r0, r0 + NRS, ... (nrow of them)
         int r0 = rs - R0 % NRS;
         if (r0 < 0) r0 += NRS;
         const int nrow = (ok && r0 < R) ? (R - r0 + NRS - 1) / NRS : 0;
+        // int8: the R row scales follow the rows (then, in a GU tile, the R / 2
+        // W_down column scales of its j's); each lane that writes a row's
+        // partial keeps that row's scale per pass (read before the release)
+        float scl[NPS];
+        if constexpr (WB == 1) {
+            const float* sc = reinterpret_cast<const float*>(tile + (size_t)R * K);
+            if (tsink && ok && wg == 0)
+                for (int i = lane; i < R / 2; i += 32) tsink[R0 / 2 + i] = sc[R + i];
+#pragma unroll
+            for (int pb = 0; pb < NPS; ++pb) {
+                const int rr = 4 * pb + (lane >> 3);
+                scl[pb] = rr < nrow ? sc[r0 + rr * NRS] : 0.f;
+            }
+        }
         // rows qb .. qb+3 of the share: dot products, transposed butterfly (lane
         // bit 4 picks rows {0,1} / {2,3}, bit 3 one row of the pair; bits 0-2
         // finish the sum) and the column-block partials into `part`
@@ -778,7 +839,7 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
             for (int j = 0; j < CPL; ++j)
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    if (qb + q < nrow) fma_chunk(chunk(qb + q, j), xl[j], xh[j], a[q][0], a[q][1]);
+                    if (qb + q < nrow) C::fma(chunk(qb + q, j), xl[j], xh[j], a[q][0], a[q][1]);
             float v[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) v[q] = (a[q][0].x + a[q][0].y) + (a[q][1].x + a[q][1].y);
@@ -791,6 +852,7 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
             kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 4);
             kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 2);
             kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 1);
+            if constexpr (WB == 1) kk *= scl[qb >> 2];
             const int q = lane >> 3;               // row of the four this lane holds
             if ((lane & 7) == 0 && q < nv) {
                 float* pr = part + (R0 + r0 + (qb + q) * NRS) * PS;
@@ -801,18 +863,20 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
                 }
             }
         };
-        auto at = [&](int q, int j) {              // this lane's 16 bytes of row q, chunk j of the share
-            return tile + (size_t)(r0 + q * NRS) * (K * 2) + ((cb * CPL + j) * 32 + lane) * 16;
+        auto at = [&](int q, int j) {              // this lane's chunk of row q, chunk j of the share
+            return tile + (size_t)(r0 + q * NRS) * (K * WB) + ((cb * CPL + j) * 32 + lane) * (8 * WB);
         };
-        if constexpr (CPL <= 2) {
+        // (int8 rows of 256 columns, up to 32 per warp, are read as used: held
+        // whole beside their scales they spilled)
+        if constexpr (CPL <= 2 && !(WB == 1 && CPL == 1)) {
             // Load the warp's whole share of the tile, then release the slot at
             // once: the copy producer refills it while this warp computes (the
             // arrival's release semantics order it after these loads).
-            uint4 wv[RPW][CPL];
+            typename C::T wv[RPW][CPL];
 #pragma unroll
             for (int q = 0; q < RPW; ++q)
 #pragma unroll
-                for (int j = 0; j < CPL; ++j) wv[q][j] = q < nrow ? lds128(at(q, j)) : make_uint4(0u, 0u, 0u, 0u);
+                for (int j = 0; j < CPL; ++j) wv[q][j] = q < nrow ? C::load(at(q, j)) : C::zero();
             release_tile(p, s, ring, (uint32_t)NG);
 #pragma unroll
             for (int qb = 0; qb < RPW; qb += 4)
@@ -822,7 +886,7 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
             // the registers beside them, so it is read as used, released after
 #pragma unroll
             for (int qb = 0; qb < RPW; qb += 4)
-                if (qb < nrow) pass(qb, [&](int q, int j) { return lds128(at(q, j)); });
+                if (qb < nrow) pass(qb, [&](int q, int j) { return C::load(at(q, j)); });
             release_tile(p, s, ring, (uint32_t)NG);
         }
         if (!ok) ab = true;     // this warp gave up; the barrier below makes it uniform
@@ -832,10 +896,10 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
 // Three groups of four warps measured fastest of 1, 2, 3 and 6 groups on the
 // 1B shape; a compile-time choice keeps one copy of the loop in the layer code.
 constexpr int MK_GEMV_GROUPS = 3;
-template <int MH>
+template <int MH, int WB>
 __device__ __forceinline__ bool gemv_fifo(const MkParams& p, const Smem& s, Ring& ring, const float* xs, int nrows,
-                                          int TR, bool ab, float* part) {
-    return gemv_wide<MH, MK_GEMV_GROUPS>(p, s, ring, xs, nrows, TR, ab, part);
+                                          int TR, bool ab, float* part, float* tsink = nullptr) {
+    return gemv_wide<MH, MK_GEMV_GROUPS, WB>(p, s, ring, xs, nrows, TR, ab, part, tsink);
 }
 // Sum of the NKB column-block partials of row R of a FIFO GEMV phase.
 template <int MH>
@@ -1411,7 +1475,8 @@ __device__ __forceinline__ float mk_gumbel(uint64_t seed, int pos, int v) {
 // pays once every CTA attends to more positions than one chunk per warp; on
 // short contexts the lane-parallel attention of the standard build has the
 // shorter dependency chain.  The host picks the build per step.
-template <int HD, int G, int MH, int LC>
+// WB: bytes per streamed weight, 2 (bf16) or 1 (weight-only INT8).
+template <int HD, int G, int MH, int LC, int WB>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
     static_assert(G <= MK_NCW, "one consumer warp per query head of a KV group (softmax, combine weights)");
     static_assert(!LC || mk_attn_tc(HD, G), "the long-context build's attention runs on 4 heads of 64 dims");
@@ -1519,7 +1584,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres(), pl.orow0,
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
-        ab = gemv_fifo<MH>(p, s, ring, s.xv(), 2 * pl.npairs, g.TRh, ab, s.part());
+        ab = gemv_fifo<MH, WB>(p, s, ring, s.xv(), 2 * pl.npairs, g.TRh, ab, s.part());
         if (t == 0 && p.stream_tail == 2) *(volatile int*)&s.misc()->streaming = 0;
         MK_TRACE(16 * l + 2);
         MK_TRACE_CWAIT(8 * l + 0);
@@ -1712,7 +1777,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
         // O-proj (rows of this CTA, columns of this group) + residual, atomically
         float* xo = xa + (size_t)(2 * l) * state;
-        ab = gemv_phase_t<MO, LPRO>(p, s, ring, s.ov(), pl.norows, g.TRo, s.misc()->ocfg, ab, [&](int r, float v) {
+        ab = gemv_phase_t<MO, LPRO, WB>(p, s, ring, s.ov(), pl.norows, g.TRo, s.misc()->ocfg, ab, [&](int r, float v) {
             if (pl.g == 0) v += s.xres()[r];   // group 0 carries the residual of these rows
             atomicAdd(xo + pl.orow0 + r, v);
         }, -1, l, 8);
@@ -1731,14 +1796,16 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         if (l == 3) trace_ring(p, ring, 4);   // everything before this layer's FFN (discarded)
         {
             // a GU tile holds n gate rows then the n up rows of the same j's
+            // (int8: and W_down's column scales of those j's, which the GEMV
+            // leaves in u and which multiply into SiLU(gate) * up)
             const int JT = g.JT;
-            ab = gemv_fifo<MH>(p, s, ring, s.xv(), 2 * pl.nj, 2 * JT, ab, s.part());
+            ab = gemv_fifo<MH, WB>(p, s, ring, s.xv(), 2 * pl.nj, 2 * JT, ab, s.part(), WB == 1 ? s.u() : nullptr);
             for (int j = t; j < pl.nj; j += MK_NCT) {
                 const int q = j / JT, jj = j % JT;
                 const int n = min(JT, pl.nj - q * JT);
                 const float gt = wide_row<MH>(s.part(), q * 2 * JT + jj);
                 const float up = wide_row<MH>(s.part(), q * 2 * JT + n + jj);
-                s.u()[j] = gt / (1.f + __expf(-gt)) * up;
+                s.u()[j] = gt / (1.f + __expf(-gt)) * up * (WB == 1 ? s.u()[j] : 1.f);
             }
         }
         MK_TRACE(16 * l + 11);
@@ -1770,8 +1837,8 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 if (b % P != jp) { ring.advance(p.geo.ns); continue; }   // another group's tile
                 const int n = min(g.JD, pl.nj - j0);
                 const uint8_t* tile;
-                const bool ok = take_tile(p, s, ring, (uint32_t)(n * H * 2), tile);
-                if constexpr (TP == 128 && CPT <= 2 && !LC) {
+                const bool ok = take_tile(p, s, ring, (uint32_t)(n * H * WB), tile);
+                if constexpr (TP == 128 && CPT <= 2 && !LC && WB == 2) {
                     // a thread's share is 16 chunks (slots of 32 KB): loaded
                     // whole, then the slot is released before the arithmetic
                     // (not in the long-context build, whose attention already
@@ -1805,14 +1872,23 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                         for (int jj = 0; jj < n; ++jj) {
                             const float uj = s.u()[j0 + jj];
                             const float2 u2 = make_float2(uj, uj);
-                            const uint8_t* col = tile + (size_t)jj * H * 2;
+                            const uint8_t* col = tile + (size_t)jj * H * WB;
 #pragma unroll
                             for (int m = 0; m < CPT; ++m) {
-                                const uint4 w = lds128(col + (size_t)(tp + m * TP) * 16);
-                                da[m][0] = __ffma2_rn(bf2_lo_hi(w.x), u2, da[m][0]);
-                                da[m][1] = __ffma2_rn(bf2_lo_hi(w.y), u2, da[m][1]);
-                                da[m][2] = __ffma2_rn(bf2_lo_hi(w.z), u2, da[m][2]);
-                                da[m][3] = __ffma2_rn(bf2_lo_hi(w.w), u2, da[m][3]);
+                                if constexpr (WB == 2) {
+                                    const uint4 w = lds128(col + (size_t)(tp + m * TP) * 16);
+                                    da[m][0] = __ffma2_rn(bf2_lo_hi(w.x), u2, da[m][0]);
+                                    da[m][1] = __ffma2_rn(bf2_lo_hi(w.y), u2, da[m][1]);
+                                    da[m][2] = __ffma2_rn(bf2_lo_hi(w.z), u2, da[m][2]);
+                                    da[m][3] = __ffma2_rn(bf2_lo_hi(w.w), u2, da[m][3]);
+                                } else {   // 8 rows of int8 (u already carries W_down's column scale)
+                                    const uint2 w = lds64(col + (size_t)(tp + m * TP) * 8);
+                                    const uint32_t lo = w.x ^ 0x80808080u, hi = w.y ^ 0x80808080u;
+                                    da[m][0] = __ffma2_rn(i8pair(lo, 0), u2, da[m][0]);
+                                    da[m][1] = __ffma2_rn(i8pair(lo, 2), u2, da[m][1]);
+                                    da[m][2] = __ffma2_rn(i8pair(hi, 0), u2, da[m][2]);
+                                    da[m][3] = __ffma2_rn(i8pair(hi, 2), u2, da[m][3]);
+                                }
                             }
                         }
                     }
@@ -1885,7 +1961,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         bool nonfinite = false;
         // top-p: the logits go to scratch and the phase only finds max(logit / T)
         const bool topp = p.inv_temp > 0.f && p.top_p < 1.f;
-        ab = gemv_phase_t<MH, 32>(p, s, ring, s.xv(), pl.nv, g.TRh, s.misc()->lmcfg, ab, [&](int r, float lg) {
+        ab = gemv_phase_t<MH, 32, WB>(p, s, ring, s.xv(), pl.nv, g.TRh, s.misc()->lmcfg, ab, [&](int r, float lg) {
             const int v = pl.v0 + r;
             if (p.logits) p.logits[v] = lg;
             if (isfinite(lg)) {

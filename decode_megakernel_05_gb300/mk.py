@@ -51,7 +51,8 @@ class mk_config(ctypes.Structure):
 
 
 class mk_tuning(ctypes.Structure):
-    _fields_ = [("ring_stages", _i32), ("slot_kib", _i32), ("l2_prefetch_kib", _i32), ("grid_ctas", _i32)]
+    _fields_ = [("ring_stages", _i32), ("slot_kib", _i32), ("l2_prefetch_kib", _i32), ("grid_ctas", _i32),
+                ("weight_int8", _i32)]
 
 
 class mk_weights(ctypes.Structure):
@@ -65,7 +66,7 @@ class mk_info(ctypes.Structure):
                 ("slot_bytes", _i32), ("smem_bytes", _i32), ("sm_count", _i32), ("l2_prefetch_bytes", _i32),
                 ("arena_bytes", _i64), ("weight_bytes_per_token", _i64), ("kv_bytes_per_position", _i64),
                 ("device_bytes", _i64), ("attn_tc", _i32), ("attn_tc_min_ctx", _i32),
-                ("attn_pos_per_cta", _i32)]
+                ("attn_pos_per_cta", _i32), ("weight_int8", _i32)]
 
 
 # (name, restype, argtypes) of every exported function, in header order.
@@ -74,6 +75,7 @@ SIGNATURES = [
     ("mk_load_weights", _i32, [_P, ctypes.POINTER(mk_weights), _P]),
     ("mk_set_kv", _i32, [_P, _i32, _P, _P, _i32, _P]),
     ("mk_get_kv", _i32, [_P, _i32, _i32, _i32, _P, _P, _P]),
+    ("mk_read_arena", _i32, [_P, _i64, _i64, _P, _P]),
     ("mk_decode_step", _i32, [_P, _i32, _i32, _P, _P]),
     ("mk_decode_step_greedy", _i32, [_P, _i32, _P, _P]),
     ("mk_generate_greedy", _i32, [_P, _P, _i32, _i32, _i32, _P, _P]),
@@ -142,8 +144,8 @@ def config_from_shape(shape, max_seq: int) -> mk_config:
                      shape.vocab, max_seq, shape.rms_eps, shape.rope_theta, int(shape.tie_embeddings))
 
 
-def tuning(ring_stages=0, slot_kib=0, l2_prefetch_kib=0, grid_ctas=0) -> mk_tuning:
-    return mk_tuning(ring_stages, slot_kib, l2_prefetch_kib, grid_ctas)
+def tuning(ring_stages=0, slot_kib=0, l2_prefetch_kib=0, grid_ctas=0, weight_int8=0) -> mk_tuning:
+    return mk_tuning(ring_stages, slot_kib, l2_prefetch_kib, grid_ctas, int(weight_int8))
 
 
 class _PtrTable:
@@ -190,6 +192,10 @@ def mk_set_kv(ctx: int, layer: int, k_ptr: int, v_ptr: int, n_pos: int, stream: 
 
 def mk_get_kv(ctx: int, layer: int, pos0: int, n_pos: int, k_out: int, v_out: int, stream: int = 0) -> None:
     check(load().mk_get_kv(ctx, layer, pos0, n_pos, k_out, v_out, stream), "mk_get_kv")
+
+
+def mk_read_arena(ctx: int, offset: int, nbytes: int, out_ptr: int, stream: int = 0) -> None:
+    check(load().mk_read_arena(ctx, offset, nbytes, out_ptr, stream), "mk_read_arena")
 
 
 def mk_decode_step(ctx: int, token: int, pos: int, logits_ptr: int | None, stream: int = 0) -> None:

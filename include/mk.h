@@ -78,6 +78,18 @@ typedef struct {
                                 extra L2 traffic cost more than the hidden latency saved) */
     int32_t grid_ctas;       /* CTAs of the persistent grid (default: n_kv_heads * floor(SMs / n_kv_heads));
                                 must be a multiple of n_kv_heads and fit one CTA per SM */
+    int32_t weight_int8;     /* nonzero: weight-only INT8 (stapisi.com/news/3904786, section 6:
+                                quantization fused into the kernels).  mk_load_weights quantizes
+                                every matrix on the device -- symmetric absmax, one fp32 scale
+                                s = max|w| / 127 per output row (per input column for w_down),
+                                codes round(w / s) ties to even in [-127, 127], both divisions
+                                rounded to nearest -- and the step streams the codes and scales,
+                                dequantizing in registers (activations, accumulation, norms, the
+                                embedding row and the KV cache stay as in the bf16 path).
+                                Built for (head_dim, q heads per KV head, hidden) = (64, 2, 256),
+                                (64, 4, 2048) and (128, 4, 4096); other shapes return
+                                MK_ERR_UNSUPPORTED from mk_create, as do mk_enable_perop(.., 1),
+                                mk_prefill and mk_relayout_host on an int8 context / tuning */
 } mk_tuning;
 
 /* Weights, row-major [out, in] bf16 (raw 16-bit patterns).  Either all host
@@ -103,7 +115,8 @@ typedef struct {
     int32_t grid_ctas, ctas_per_group, block_threads, ring_stages, slot_bytes;
     int32_t smem_bytes, sm_count, l2_prefetch_bytes;
     int64_t arena_bytes;             /* re-laid-out weight stream bytes on the device */
-    int64_t weight_bytes_per_token;  /* bf16 weight bytes one step reads (matrices + gains + 1 embedding row) */
+    int64_t weight_bytes_per_token;  /* weight bytes one step reads: matrices (bf16, or int8 codes + fp32
+                                        scales), gains and 1 embedding row at 2 bytes a value */
     int64_t kv_bytes_per_position;   /* bf16 K+V bytes one attended position costs (all layers) */
     int64_t device_bytes;            /* everything the context allocated on the device */
     int32_t attn_tc;                 /* 1: a build whose attention runs on the tensor cores exists
@@ -115,6 +128,7 @@ typedef struct {
                                         attention on ceil(ctx / attn_pos_per_cta) CTAs of each KV
                                         group, at most ctas_per_group (0: the count is forced
                                         with MK_DBG_ATTN_CTAS) */
+    int32_t weight_int8;             /* 1: the context streams weight-only INT8 (mk_tuning) */
 } mk_info;
 
 /* Create a context on CUDA device `device`: validates the shape, sizes the
@@ -144,6 +158,13 @@ int mk_set_kv(mk_ctx* ctx, int32_t layer, const void* k, const void* v, int32_t 
  * the cache's layout; a temporary device buffer as for mk_set_kv).
  * Synchronizes `stream`. */
 int mk_get_kv(mk_ctx* ctx, int32_t layer, int32_t pos0, int32_t n_pos, void* k_out, void* v_out, void* stream);
+
+/* Copy bytes [offset, offset + bytes) of the device weight arena (the
+ * re-laid-out tile streams, mk_info.arena_bytes long) to `out` (host or
+ * device memory); synchronizes `stream`.  For layout checks of streams only
+ * the device builds (weight-only INT8).  MK_ERR_INVALID_ARG for a range
+ * outside the arena, MK_ERR_STATE before mk_load_weights. */
+int mk_read_arena(mk_ctx* ctx, int64_t offset, int64_t bytes, void* out, void* stream);
 
 /* One decode step (one kernel launch): feed `token` at position `pos`, write
  * its K/V into cache slot `pos`, attend over slots [0, pos], and write the

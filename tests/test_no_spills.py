@@ -51,5 +51,6 @@ def test_production_kernels_do_not_spill():
             assert m.group(1) == "0" and m.group(2) == "0", f"{head}: {fn}: {line}"
             checked += 1
             fused += "mk_decode_kernel" in fn
-    assert fused == len(build.VARIANTS) + len(build.LC_VARIANTS), fused
+    assert fused == (len(build.VARIANTS) + len(build.LC_VARIANTS) + len(build.Q8_VARIANTS) +
+                     len(build.Q8_LC_VARIANTS)), fused
     assert checked > fused
