@@ -87,7 +87,7 @@ __global__ void mk_quantize_q8_kernel(const uint16_t* w, int64_t rows, int64_t c
         float c = 0.f;
         if (sg > 0.f) c = rintf(__fdiv_rn(__uint_as_float((uint32_t)w[at(k)] << 16), sg));
         c = fminf(fmaxf(c, -127.f), 127.f);
-        q[at(k)] = (int8_t)c;
+        reinterpret_cast<uint8_t*>(q)[at(k)] = (uint8_t)((int)c + 128);   // stored biased: q + 128
     }
 }
 

@@ -30,7 +30,7 @@ struct MkScaleCopy {
 // Symmetric absmax INT8 quantization of a bf16 matrix [rows][cols] per row
 // (or per column with col_scaled): scale = max|w| / 127, code = round(w /
 // scale) ties to even, both float operations rounded to nearest; a group of
-// zeros gets scale 0 and codes 0.
+// zeros gets scale 0 and codes 0.  Each code q is written as the byte q + 128.
 cudaError_t mk_launch_quantize_q8(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int8_t* q,
                                   float* scale, cudaStream_t st);
 cudaError_t mk_launch_relayout_rows_q8(uint8_t* arena, const int8_t* q, int64_t cols, const float* scale,

@@ -26,8 +26,8 @@
 // A tile is TRh rows (QKV, LM), TRo rows (O), one GU group, or JD columns (D);
 // the last tile of a block may be short.  Every tile is a multiple of 16 bytes.
 //
-// Weight-only INT8 streams (wb = 1) store each weight as one signed byte with
-// a float scale per output row (QKV, O, gate, up, LM head) or per input
+// Weight-only INT8 streams (wb = 1) store each weight's code q as the byte
+// q + 128, with a float scale per output row (QKV, O, gate, up, LM head) or per input
 // column (W_down): a row tile is its R rows of K bytes, then the R rows'
 // scales; a GU tile is its n gate rows and n up rows, then their 2n scales,
 // then the n column scales of W_down for the same j's (the down projection

@@ -609,9 +609,9 @@ __device__ __forceinline__ void fma_chunk(const uint4 w, const float4 xl, const 
     a1 = __ffma2_rn(bf2_lo_hi(w.w), make_float2(xh.z, xh.w), a1);
 }
 
-// Weight-only INT8 chunks: 8 int8 weights (8 bytes, columns in the same order
-// as a bf16 chunk's 8 columns) -> fp32.  Each byte, offset by 128 (the xor
-// with 0x80), becomes the low byte of the mantissa of 2^23 (exact), and
+// Weight-only INT8 chunks: 8 codes (8 bytes, columns in the same order as a
+// bf16 chunk's 8 columns) -> fp32.  The stream stores each code q as the
+// byte q + 128, which becomes the low byte of the mantissa of 2^23 (exact);
 // 2^23 + 128 comes off: bytes k and k+1 of a give the pair of values.
 __device__ __forceinline__ uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
 __device__ __forceinline__ float2 i8pair(uint32_t a, int k) {
@@ -620,7 +620,7 @@ __device__ __forceinline__ float2 i8pair(uint32_t a, int k) {
     return __fadd2_rn(make_float2(x, y), make_float2(-8388736.f, -8388736.f));
 }
 __device__ __forceinline__ void fma_chunk8(const uint2 w, const float4 xl, const float4 xh, float2& a0, float2& a1) {
-    const uint32_t lo = w.x ^ 0x80808080u, hi = w.y ^ 0x80808080u;
+    const uint32_t lo = w.x, hi = w.y;
     a0 = __ffma2_rn(i8pair(lo, 0), make_float2(xl.x, xl.y), a0);
     a1 = __ffma2_rn(i8pair(lo, 2), make_float2(xl.z, xl.w), a1);
     a0 = __ffma2_rn(i8pair(hi, 0), make_float2(xh.x, xh.y), a0);
@@ -639,7 +639,7 @@ template <> struct WChunk<2> {
 template <> struct WChunk<1> {
     using T = uint2;
     static __device__ __forceinline__ T load(const void* p) { return lds64(p); }
-    static __device__ __forceinline__ T zero() { return make_uint2(0x80808080u ^ 0x80808080u, 0u); }
+    static __device__ __forceinline__ T zero() { return make_uint2(0x80808080u, 0x80808080u); }   // codes 0
     static __device__ __forceinline__ void fma(const T w, const float4 xl, const float4 xh, float2& a0, float2& a1) {
         fma_chunk8(w, xl, xh, a0, a1);
     }
@@ -1883,7 +1883,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                                     da[m][3] = __ffma2_rn(bf2_lo_hi(w.w), u2, da[m][3]);
                                 } else {   // 8 rows of int8 (u already carries W_down's column scale)
                                     const uint2 w = lds64(col + (size_t)(tp + m * TP) * 8);
-                                    const uint32_t lo = w.x ^ 0x80808080u, hi = w.y ^ 0x80808080u;
+                                    const uint32_t lo = w.x, hi = w.y;
                                     da[m][0] = __ffma2_rn(i8pair(lo, 0), u2, da[m][0]);
                                     da[m][1] = __ffma2_rn(i8pair(lo, 2), u2, da[m][1]);
                                     da[m][2] = __ffma2_rn(i8pair(hi, 0), u2, da[m][2]);

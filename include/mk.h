@@ -83,7 +83,8 @@ typedef struct {
                                 every matrix on the device -- symmetric absmax, one fp32 scale
                                 s = max|w| / 127 per output row (per input column for w_down),
                                 codes round(w / s) ties to even in [-127, 127], both divisions
-                                rounded to nearest -- and the step streams the codes and scales,
+                                rounded to nearest -- and the step streams the codes (each as the
+                                byte code + 128) and the scales,
                                 dequantizing in registers (activations, accumulation, norms, the
                                 embedding row and the KV cache stay as in the bf16 path).
                                 Built for (head_dim, q heads per KV head, hidden) = (64, 2, 256),

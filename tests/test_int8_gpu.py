@@ -72,12 +72,11 @@ def decode_arena_q8(arena, s, grid):
               for k, sh in shapes.items()}
     lm_q, lm_s = np.zeros((V, H), np.int8), np.full(V, np.nan, np.float32)
     cover = np.zeros(arena.size, np.int32)
-    i8 = arena.view(np.int8)
     off = 0
 
-    def codes_at(o, n):
+    def codes_at(o, n):   # the stream stores each code q as the byte q + 128
         cover[o:o + n] += 1
-        return i8[o:o + n]
+        return (arena[o:o + n] ^ np.uint8(0x80)).view(np.int8)
 
     def f32_at(o, n):
         return arena[o:o + 4 * n].view(np.float32)
