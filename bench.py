@@ -296,7 +296,8 @@ def time_int8(a, w, local, torch, positions, peak, peak_src):
             "weights": "symmetric absmax int8, fp32 scale per output row (per input column for w_down), "
                        "quantized on the device at load",
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_src, "traffic": None,
+                         "frac": achieved / peak, "peak_source": peak_src,
+                         "traffic": (load_profile_traffic(a.workload + "_int8") or {}).get("dram_bytes_per_launch"),
                          "algorithmic_bytes_per_launch": alg,
                          "kernel": "mk_decode_kernel, int8 build (1 launch = 1 token)"}}
 
