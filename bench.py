@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=1024)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="1b", help="tiny | 1b | 1b-2k | 8b-4k | 1b-32k")
+    ap.add_argument("--workload", default="1b", help="tiny | 1b | 1b-2k | 8b-4k | 1b-32k (8b-4l-4k: profiling case)")
     ap.add_argument("--perop", action="store_true", help="time the unfused per-operator baseline instead")
     ap.add_argument("--ring-stages", type=int, default=0)
     ap.add_argument("--slot-kib", type=int, default=0)
@@ -504,7 +504,9 @@ def run_ours(a, world, rank, local):
                              "tiny": "tiny llama-style bs=1 decode (L2-resident)",
                              "1b-2k": "llama-3.2-1b-shape bs=1 decode, KV pre-filled 2048",
                              "8b-4k": "llama-3-8b-shape bs=1 decode, KV pre-filled 4096",
-                             "1b-32k": "llama-3.2-1b-shape bs=1 decode, KV pre-filled 32768"}[a.workload],
+                             "1b-32k": "llama-3.2-1b-shape bs=1 decode, KV pre-filled 32768",
+                             "8b-4l-4k": "4-layer slice of the llama-3-8b shape (vocab 32000), KV pre-filled "
+                                         "4096: profiling case"}[a.workload],
                 "weights": "bf16 random-init N(0,0.02), fp32 activations and accumulation, bf16 KV cache",
                 "path": "per-operator baseline" if a.perop else "fused megakernel, 1 launch per token",
                 "l2": f"inputs larger than L2: {info.weight_bytes_per_token / 1e9:.2f} GB of weights per step",

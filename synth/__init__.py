@@ -134,6 +134,10 @@ WORKLOADS = {
     "1b-2k": Workload("1b-2k", 2, LLAMA_1B, prompt_len=0, prefill=2048, decode=128),
     "8b-4k": Workload("8b-4k", 3, LLAMA_8B, prompt_len=0, prefill=4096, decode=128),
     "1b-32k": Workload("1b-32k", 4, LLAMA_1B, prompt_len=0, prefill=32768, decode=64),
+    # a 4-layer slice of the 8B shape (vocab 32000): the 8B kernels on about 1-2 GB, for full profiler
+    # captures (not a benchmark workload)
+    "8b-4l-4k": Workload("8b-4l-4k", 5, dataclasses.replace(LLAMA_8B, n_layers=4, vocab=32000), prompt_len=0,
+                         prefill=4096, decode=16),
 }
 
 # Stream ids of every drawn tensor.
