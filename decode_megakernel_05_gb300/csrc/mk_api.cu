@@ -332,6 +332,8 @@ struct mk_ctx {
     // batched prefill workspace (rows of capacity pf_rows), grown on demand
     int pf_rows = 0;
     float *pf_x = nullptr, *pf_xn = nullptr, *pf_qkv = nullptr, *pf_att = nullptr, *pf_gu = nullptr, *pf_u = nullptr;
+    uint16_t* pf_parts = nullptr;        // the GEMM activations' three bf16 parts (tcgen05 path)
+    int prefill_gemm = 0;                // debug: 0 tcgen05 GEMMs, 1 mma.sync GEMMs
 
     template <class T>
     int dalloc(T** p, size_t bytes) {
@@ -626,6 +628,7 @@ void mk_destroy(mk_ctx* c) {
     for (void* p : c->allocs) cudaFree(p);
     for (float* p : {c->pf_x, c->pf_xn, c->pf_qkv, c->pf_att, c->pf_gu, c->pf_u})
         if (p) cudaFree(p);
+    if (c->pf_parts) cudaFree(c->pf_parts);
     if (c->status_host) cudaFreeHost(c->status_host);
     for (uint16_t* p : c->perop.wqkv) cudaFree(p);
     for (uint16_t* p : c->perop.wo) cudaFree(p);
@@ -1116,6 +1119,7 @@ int mk_prefill(mk_ctx* c, const int32_t* tokens, int32_t n, int32_t start_pos, f
         if (c->pf_rows == 0) MK_CU(mk_prefill_prepare());
         for (float** p : {&c->pf_x, &c->pf_xn, &c->pf_qkv, &c->pf_att, &c->pf_gu, &c->pf_u})
             if (*p) { cudaFree(*p); *p = nullptr; }
+        if (c->pf_parts) { cudaFree(c->pf_parts); c->pf_parts = nullptr; }
         c->pf_rows = 0;
         const size_t rows = (size_t)n;
         MK_CU(cudaMalloc(&c->pf_x, rows * H * 4));
@@ -1124,6 +1128,9 @@ int mk_prefill(mk_ctx* c, const int32_t* tokens, int32_t n, int32_t start_pos, f
         MK_CU(cudaMalloc(&c->pf_att, rows * qd * 4));
         MK_CU(cudaMalloc(&c->pf_gu, rows * 2 * F * 4));
         MK_CU(cudaMalloc(&c->pf_u, rows * F * 4));
+        // [3][rows rounded up to 128][widest K]: the longest K a GEMM reads is H, F or qh*hd
+        const size_t mp = (rows + 127) / 128 * 128, kmax = std::max({H, F, qd});
+        MK_CU(cudaMalloc(&c->pf_parts, 3 * mp * kmax * 2));
         c->pf_rows = n;
     }
     MK_CU(cudaMemcpyAsync(c->prompt_dev, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, st));
@@ -1140,6 +1147,7 @@ int mk_prefill(mk_ctx* c, const int32_t* tokens, int32_t n, int32_t start_pos, f
     a.attn_norm = c->attn_norm; a.ffn_norm = c->ffn_norm; a.final_norm = c->final_norm;
     a.rope_cos = c->rope_cos; a.rope_sin = c->rope_sin; a.kc = c->kc; a.vc = c->vc;
     a.x = c->pf_x; a.xn = c->pf_xn; a.qkv = c->pf_qkv; a.att = c->pf_att; a.gu = c->pf_gu; a.u = c->pf_u;
+    a.parts = c->prefill_gemm == 0 ? c->pf_parts : nullptr;
     a.hidden = c->hidden;
     a.logits = logits_out ? logits_out : P.logits_tmp;
     a.amax_part = P.amax_part; a.amax_blocks = P.amax_blocks;
@@ -1208,6 +1216,11 @@ int mk_set_debug(mk_ctx* c, int32_t knob, int64_t value) {
     if (knob == MK_DBG_ATTN_BUILD) {
         if (value < 0 || value > 2 || (value == 2 && !c->kernel_tc)) return MK_ERR_INVALID_ARG;
         c->attn_build = (int)value;
+        return MK_OK;
+    }
+    if (knob == MK_DBG_PREFILL_GEMM) {
+        if (value < 0 || value > 1) return MK_ERR_INVALID_ARG;
+        c->prefill_gemm = (int)value;
         return MK_OK;
     }
     if (knob == MK_DBG_STREAM_TAIL) {

@@ -20,6 +20,7 @@
 // about 2^-26 relative, as exactly as the decode path's fp32 activations.
 // (Two parts, 2^-17, were measured first: after 16 layers of attention the
 // K/V rows drifted to 80% bit-equal with the token-by-token oracle.)
+#include <cuda.h>   // CUtensorMap and its enums; the encoder itself comes through the runtime
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -198,6 +199,239 @@ __global__ void __launch_bounds__(128) gemm_split_kernel(const float* __restrict
                     if (c + 1 < N) dst[1] = v1 + (RES ? R[(size_t)r * N + c + 1] : 0.f);
                 }
             }
+}
+
+// ---------------------------------------------------------------- tcgen05 GEMM
+//
+// The same product on the fifth-generation tensor cores.  A's three bf16 parts
+// are written first (split_parts_kernel) as one bf16 matrix [3][Mp][K] (Mp =
+// M rounded up to 128, the padding rows zero).  A CTA owns a 128 x 128 tile
+// of C and walks K in blocks of 64 (one 128-byte row of each operand):
+//   - warp 0, one thread: TMA (cp.async.bulk.tensor) copies of the three A
+//     part tiles and the W tile of a K block into one of three stages, with
+//     the 128-byte swizzle, completing on the stage's full barrier;
+//   - warp 1: allocates 128 TMEM columns (the fp32 accumulator: lane = row
+//     of the tile, column = column); one thread issues, per K block, 12
+//     tcgen05.mma (3 parts x 4 steps of K = 16, M = 128, N = 128, bf16 in,
+//     fp32 accumulate, smallest part first) and commits them to the stage's
+//     empty barrier, and after the last block to the done barrier;
+//   - warps 2-5: wait for done, read the accumulator with tcgen05.ld (warp w
+//     reads TMEM lanes 32 (w mod 4) ..), add the residual and store C.
+// Every wait is bounded (%globaltimer, 2 s); a time-out sets the time-out bit
+// (0x1) of the status word and the CTA still frees its TMEM.  The K tail and the rows of W
+// past N come in as zeros (TMA's out-of-bounds fill).
+constexpr int TBM = 128, TBN = 128, TBK = 64, TST = 3;
+constexpr uint32_t T_PART = TBM * TBK * 2;                  // 16 KB: one part's A tile
+constexpr uint32_t T_WT = TBN * TBK * 2;                    // 16 KB: the W tile
+constexpr uint32_t T_STAGE = 3 * T_PART + T_WT;             // 64 KB
+constexpr uint32_t T_SMEM = TST * T_STAGE + 1024 + 128;     // stages, alignment slack, barriers
+constexpr uint64_t T_WAIT_NS = 2000000000ull;
+
+__device__ __forceinline__ uint64_t gtimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+// Bounded wait for phase `parity` of an mbarrier; false (and the status bit) on time-out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = gtimer_ns();
+    while (!mbar_try(bar, parity)) {
+        if (gtimer_ns() - t0 > T_WAIT_NS) {
+            atomicOr(status, 0x1u);
+            return false;
+        }
+    }
+    return true;
+}
+// Shared-memory matrix descriptor of a K-major operand tile with the 128-byte
+// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);   // start address / 16
+    d |= (uint64_t)1 << 16;                              // leading-dimension offset (not used with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;                    // stride between 8-row groups / 16
+    d |= (uint64_t)1 << 46;                              // descriptor version
+    d |= (uint64_t)2 << 61;                              // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor: kind::f16, bf16 A and B (both K-major), fp32 D, M = 128, N = 128.
+constexpr uint32_t T_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TBN >> 3) << 17) |
+                             ((uint32_t)(TBM >> 4) << 24);
+
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const float* R,
+                   float* C, int M, int N, int K, int Mp, uint32_t* status) {
+    extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
+    // the stages need 1024-byte alignment (the swizzle pattern repeats every 8 rows of 128 bytes)
+    const uint32_t raw = smem_u32(tc_smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bars = base + TST * T_STAGE;           // full[TST], empty[TST], done, then the TMEM address
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (TST + s); };
+    const uint32_t done = bars + 8u * (2 * TST);
+    const uint32_t taddr_slot = done + 8u;
+    uint32_t* taddr_ptr = reinterpret_cast<uint32_t*>(tc_smem_raw + (taddr_slot - raw));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * TBM, n0 = blockIdx.x * TBN;
+    const int nkb = (K + TBK - 1) / TBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TST; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(taddr_slot),
+                     "r"((uint32_t)TBN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    }
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(taddr_ptr);
+
+    if (warp == 0 && lane == 0) {
+        // producer
+        const uint64_t pa = reinterpret_cast<uint64_t>(&tmA), pw = reinterpret_cast<uint64_t>(&tmW);
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % TST;
+            const uint32_t ph = (uint32_t)(kb / TST) & 1u;
+            if (kb >= TST && !mbar_wait(empty(s), ph ^ 1u, status)) break;
+            const uint32_t st = base + (uint32_t)s * T_STAGE;
+            mbar_expect(full(s), T_STAGE);
+            for (int part = 0; part < 3; ++part)
+                asm volatile(
+                    "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+                    "[%4];" ::"r"(st + (uint32_t)part * T_PART),
+                    "l"(pa), "r"(kb * TBK), "r"(part * Mp + m0), "r"(full(s))
+                    : "memory");
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+                "[%4];" ::"r"(st + 3u * T_PART),
+                "l"(pw), "r"(kb * TBK), "r"(n0), "r"(full(s))
+                : "memory");
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer
+        bool ok = true;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+            const int s = kb % TST;
+            const uint32_t ph = (uint32_t)(kb / TST) & 1u;
+            if (!mbar_wait(full(s), ph, status)) { ok = false; break; }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t st = base + (uint32_t)s * T_STAGE;
+            const uint64_t wd = sw128_desc(st + 3u * T_PART);
+            for (int part = 2; part >= 0; --part) {
+                const uint64_t ad = sw128_desc(st + (uint32_t)part * T_PART);
+#pragma unroll
+                for (int kk = 0; kk < TBK / 16; ++kk) {
+                    // advancing K by 16 bf16 (32 bytes) inside the swizzle row: start address + 2 (16-byte units)
+                    const uint32_t acc = (kb > 0 || part < 2 || kk > 0) ? 1u : 0u;
+                    asm volatile(
+                        "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem),
+                        "l"(ad + 2ull * kk), "l"(wd + 2ull * kk), "r"(T_IDESC), "r"(acc)
+                        : "memory");
+                }
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(empty(s))
+                         : "memory");
+        }
+        if (ok)
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(done)
+                         : "memory");
+    } else if (warp >= 2) {
+        // epilogue: TMEM lanes 32 q .. 32 q + 31 are rows m0 + 32 q + lane
+        const bool ok = mbar_wait(done, 0u, status);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const int q = warp & 3;
+        const int row = m0 + 32 * q + lane;
+#pragma unroll 1
+        for (int c0 = 0; c0 < TBN && ok; c0 += 32) {
+            uint32_t v[32];
+            const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+                "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                  "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                  "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                  "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+                  "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                : "r"(ta)
+                : "memory");
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            if (row < M) {
+                const int cb = n0 + c0;
+                float* dst = C + (size_t)row * N + cb;
+                const float* res = R ? R + (size_t)row * N + cb : nullptr;
+                if ((N & 3) == 0 && cb + 32 <= N) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        float4 o = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                        if (res) {
+                            const float4 r4 = *reinterpret_cast<const float4*>(res + j);
+                            o.x += r4.x; o.y += r4.y; o.z += r4.z; o.w += r4.w;
+                        }
+                        *reinterpret_cast<float4*>(dst + j) = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (cb + j < N) dst[j] = __uint_as_float(v[j]) + (res ? res[j] : 0.f);
+                }
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)TBN)
+                     : "memory");
+    }
+}
+
+// A fp32 [M][K] -> its three bf16 parts [3][Mp][K] (rows M .. Mp - 1 zero).
+__global__ void split_parts_kernel(const float* A, int M, int K, int Mp, uint16_t* P) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;   // one group of 4 columns
+    const size_t per_row = (size_t)K / 4;
+    if (i >= (size_t)Mp * per_row) return;
+    const int r = (int)(i / per_row), c = (int)(i % per_row) * 4;
+    float e[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < M) {
+        const float4 a = *reinterpret_cast<const float4*>(A + (size_t)r * K + c);
+        e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w;
+    }
+#pragma unroll
+    for (int part = 0; part < 3; ++part) {
+        const uint32_t p01 = pack_bf2(e[0], e[1]), p23 = pack_bf2(e[2], e[3]);
+        *reinterpret_cast<uint2*>(P + ((size_t)part * Mp + r) * K + c) = make_uint2(p01, p23);
+        e[0] -= __uint_as_float(p01 << 16);
+        e[1] -= __uint_as_float(p01 & 0xFFFF0000u);
+        e[2] -= __uint_as_float(p23 << 16);
+        e[3] -= __uint_as_float(p23 & 0xFFFF0000u);
+    }
 }
 
 // ---------------------------------------------------------------- row kernels
@@ -385,6 +619,39 @@ void gemm(const float* A, const uint16_t* W, const float* R, float* C, int M, in
     gemm_split_kernel<RES><<<grid, 128, sizeof(GemmSmem), st>>>(A, W, R, C, M, N, K);
 }
 
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime (no
+// link against the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Tensor map of a row-major bf16 matrix [rows][inner] read in boxes of 64 x
+// box_rows with the 128-byte swizzle (out-of-bounds elements read as zero).
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)TBK, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return g_encode && g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// C = A . W^T (+ R) on the tcgen05 path: the parts of A, then the GEMM (2 launches).
+cudaError_t gemm_tc(const float* A, const uint16_t* W, const float* R, float* C, int M, int N, int K,
+                    uint16_t* parts, uint32_t* status, cudaStream_t st) {
+    const int Mp = (M + TBM - 1) / TBM * TBM;
+    const size_t groups = (size_t)Mp * (K / 4);
+    split_parts_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(A, M, K, Mp, parts);
+    CUtensorMap ma, mw;
+    if (!make_map(&ma, parts, (uint64_t)K, (uint64_t)3 * Mp, TBM) || !make_map(&mw, W, (uint64_t)K, (uint64_t)N, TBN))
+        return cudaErrorInvalidValue;
+    const dim3 grid((N + TBN - 1) / TBN, Mp / TBM);
+    gemm_tc_kernel<<<grid, 192, T_SMEM, st>>>(ma, mw, R, C, M, N, K, Mp, status);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t mk_prefill_prepare() {
@@ -393,6 +660,15 @@ cudaError_t mk_prefill_prepare() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(GemmSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)T_SMEM);
+    if (e == cudaSuccess && !g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn) g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        else if (e == cudaSuccess) e = cudaErrorSymbolNotFound;
+    }
     return e;
 }
 
@@ -401,10 +677,23 @@ int mk_prefill_launch(const MkPrefillArgs& a, cudaStream_t st, cudaError_t* err)
     const int nqkv = (qh + 2 * kvh) * hd, qd = qh * hd;
     int launches = 0;
     *err = cudaSuccess;
+    // the tcgen05 GEMM (parts + GEMM: 2 launches) when a parts buffer is given, else the mma.sync one
+#define GEMM(A_, W_, R_, C_, M_, N_, K_)                                                                  \
+    do {                                                                                                   \
+        if (a.parts) {                                                                                     \
+            cudaError_t e_ = gemm_tc(A_, W_, R_, C_, M_, N_, K_, a.parts, a.status, st);                    \
+            if (e_ != cudaSuccess && *err == cudaSuccess) *err = e_;                                       \
+            launches += 2;                                                                                 \
+        } else {                                                                                           \
+            if (R_) gemm<true>(A_, W_, R_, C_, M_, N_, K_, st);                                             \
+            else gemm<false>(A_, W_, R_, C_, M_, N_, K_, st);                                               \
+            launches += 1;                                                                                 \
+        }                                                                                                  \
+    } while (0)
     embed_rows_kernel<<<n, 256, 0, st>>>(a.embed, a.tokens, n, a.V, H, a.x, a.status); ++launches;
     for (int l = 0; l < a.L; ++l) {
         rmsnorm_rows_kernel<<<n, 256, 0, st>>>(a.x, a.attn_norm + (size_t)l * H, H, a.eps, a.xn); ++launches;
-        gemm<false>(a.xn, a.wqkv[l], nullptr, a.qkv, n, nqkv, H, st); ++launches;
+        GEMM(a.xn, a.wqkv[l], nullptr, a.qkv, n, nqkv, H);
         rope_kv_rows_kernel<<<dim3(((qh + 2 * kvh) * hd / 2 + 127) / 128, n), 128, 0, st>>>(
             a.qkv, nqkv, a.rope_cos, a.rope_sin, a.start, qh, kvh, hd, a.max_seq, l, a.kc, a.vc, a.swz); ++launches;
         const int warps = n * qh;
@@ -415,18 +704,20 @@ int mk_prefill_launch(const MkPrefillArgs& a, cudaStream_t st, cudaError_t* err)
             attn_rows_kernel<128><<<(warps + 3) / 4, 128, 0, st>>>(a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh,
                                                                     a.max_seq, l, a.swz, a.att);
         ++launches;
-        gemm<true>(a.att, a.wo[l], a.x, a.x, n, H, qd, st); ++launches;   // residual in place
+        GEMM(a.att, a.wo[l], a.x, a.x, n, H, qd);   // residual in place
         rmsnorm_rows_kernel<<<n, 256, 0, st>>>(a.x, a.ffn_norm + (size_t)l * H, H, a.eps, a.xn); ++launches;
-        gemm<false>(a.xn, a.wgu[l], nullptr, a.gu, n, 2 * F, H, st); ++launches;
+        GEMM(a.xn, a.wgu[l], nullptr, a.gu, n, 2 * F, H);
         silu_mul_kernel<<<(int)(((size_t)n * F + 255) / 256), 256, 0, st>>>(a.gu, n, F, a.u); ++launches;
-        gemm<true>(a.u, a.wd[l], a.x, a.x, n, H, F, st); ++launches;
+        GEMM(a.u, a.wd[l], a.x, a.x, n, H, F);
     }
     // the last row: final norm (kept as the step's hidden state), LM head, argmax
     const float* xlast = a.x + (size_t)(n - 1) * H;
     rmsnorm_rows_kernel<<<1, 256, 0, st>>>(xlast, a.final_norm, H, a.eps, a.hidden); ++launches;
-    gemm<false>(a.hidden, a.lm, nullptr, a.logits, 1, a.V, H, st); ++launches;
+    GEMM(a.hidden, a.lm, nullptr, a.logits, 1, a.V, H);
     argmax_blocks_kernel<<<a.amax_blocks, 256, 0, st>>>(a.logits, a.V, a.amax_part, a.status); ++launches;
     argmax_final_kernel<<<1, 32, 0, st>>>(a.amax_part, a.amax_blocks, a.next_token, a.status); ++launches;
-    *err = cudaGetLastError();
+#undef GEMM
+    const cudaError_t e = cudaGetLastError();
+    if (*err == cudaSuccess) *err = e;
     return launches;
 }

@@ -19,6 +19,9 @@ struct MkPrefillArgs {
     uint16_t *kc, *vc;
     // fp32 workspace: x, xn [n][H], qkv [n][qkv rows], att [n][qh*hd], gu [n][2F], u [n][F]
     float *x, *xn, *qkv, *att, *gu, *u;
+    // the three bf16 parts of a GEMM's activations, [3][n rounded up to 128][max(H, F, qh*hd)]; null: the
+    // GEMMs run on mma.sync instead of tcgen05
+    uint16_t* parts;
     float* hidden;                 // [H] final-norm output of the last row
     float* logits;                 // [V] logits of the last row
     unsigned long long* amax_part;
@@ -27,7 +30,8 @@ struct MkPrefillArgs {
     uint32_t* status;
 };
 
-// Allows the GEMM its dynamic shared memory (once per device).
+// Allows the GEMMs their dynamic shared memory and fetches the tensor-map
+// encoder (once per device).
 cudaError_t mk_prefill_prepare();
 // Enqueues the whole prefill on st; returns the number of kernel launches.
 int mk_prefill_launch(const MkPrefillArgs& a, cudaStream_t st, cudaError_t* err);

@@ -38,6 +38,7 @@ MK_DBG_ATTN_TC_MIN = 11
 MK_DBG_ATTN_CTAS = 12
 MK_DBG_ATTN_POS_PER_CTA = 13
 MK_DBG_STREAM_TAIL = 14
+MK_DBG_PREFILL_GEMM = 15
 MK_NOALLOC_ARGMAX_BLOCKS = 1024
 MK_NOALLOC_ARGMAX_MAX_N = MK_NOALLOC_ARGMAX_BLOCKS * 4096
 

@@ -98,6 +98,23 @@ def test_prefill_mid_shape(grid, prefill, n):
     dec.close()
 
 
+@pytest.mark.parametrize("gemm", [0, 1], ids=["tcgen05", "mma_sync"])
+def test_prefill_gemm_paths(gemm):
+    """Both GEMM engines of the prefill (MK_DBG_PREFILL_GEMM: 0 tcgen05 with TMA
+    tiles and TMEM accumulators, the default; 1 mma.sync) on the ragged H=512
+    shape, 130 rows after 41 pre-filled positions (two 128-row tiles, N and K
+    tails), meet the same bars against the oracle."""
+    m = synth.make_model(MID, 113, std=0.04, gains="normal")
+    dec = Decoder(m, 1024, perop=True)
+    dec.set_debug(mk.MK_DBG_PREFILL_GEMM, gemm)
+    orc = oracle.OracleDecoder(m, 1024)
+    ks, vs = synth.make_kv(MID, 41, 117)
+    dec.set_kv(ks, vs, 41)
+    orc.set_kv(ks, vs, 41)
+    _prefill_vs_oracle(dec, orc, MID, synth.uniform_tokens(130, MID.vocab, 113, 9), 41)
+    dec.close()
+
+
 def test_prefill_head_dim_128():
     """hd=128 (the 8B head layout, plain cache rows) with 100 pre-filled positions."""
     m = synth.make_model(HD128, 107, std=0.03, gains="normal")
@@ -125,6 +142,7 @@ def test_prefill_argument_errors():
     assert lib.mk_prefill(dec.ctx, bad.ctypes.data, 8, 0, None, dec.stream) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_prefill(dec.ctx, toks.ctypes.data, 8, 56, None, dec.stream) == mk.MK_OK
     assert dec.status() == mk.MK_OK
+    assert lib.mk_set_debug(dec.ctx, mk.MK_DBG_PREFILL_GEMM, 2) == mk.MK_ERR_INVALID_ARG
     dec.close()
 
 
