@@ -333,7 +333,7 @@ struct mk_ctx {
     int pf_rows = 0;
     float *pf_x = nullptr, *pf_xn = nullptr, *pf_qkv = nullptr, *pf_att = nullptr, *pf_gu = nullptr, *pf_u = nullptr;
     uint16_t* pf_parts = nullptr;        // the GEMM activations' three bf16 parts (tcgen05 path)
-    int prefill_gemm = 0;                // debug: 0 tcgen05 GEMMs, 1 mma.sync GEMMs
+    int prefill_gemm = 0;                // debug: 0 tcgen05 GEMMs + tensor-core attention, 1 the mma.sync GEMMs and CUDA-core attention
 
     template <class T>
     int dalloc(T** p, size_t bytes) {
@@ -1148,6 +1148,7 @@ int mk_prefill(mk_ctx* c, const int32_t* tokens, int32_t n, int32_t start_pos, f
     a.rope_cos = c->rope_cos; a.rope_sin = c->rope_sin; a.kc = c->kc; a.vc = c->vc;
     a.x = c->pf_x; a.xn = c->pf_xn; a.qkv = c->pf_qkv; a.att = c->pf_att; a.gu = c->pf_gu; a.u = c->pf_u;
     a.parts = c->prefill_gemm == 0 ? c->pf_parts : nullptr;
+    a.attn_tc = (c->prefill_gemm == 0 && g.G <= 8) ? 1 : 0;
     a.hidden = c->hidden;
     a.logits = logits_out ? logits_out : P.logits_tmp;
     a.amax_part = P.amax_part; a.amax_blocks = P.amax_blocks;

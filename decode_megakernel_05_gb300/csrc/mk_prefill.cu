@@ -613,6 +613,167 @@ __global__ void argmax_final_kernel(const unsigned long long* part, int n, int32
     }
 }
 
+// Causal attention on the tensor cores (flash style, mma.sync m16n8k16): a
+// CTA takes 16 query rows (positions start + r0 ..) and the G query heads of
+// one KV group, warp w the head g * G + w, so the group's K/V tile of 16
+// positions is loaded once (un-permuting the cache's chunk order) and read by
+// the G warps.  Per tile: S = q . K^T with q split into its bf16 rounding and
+// the rounding of the remainder (q . k to about 2^-17 relative), the causal
+// mask, an online softmax in base 2 (q pre-scaled by log2(e) / sqrt(hd)), P
+// split the same way, O += P . V (V read transposed by ldmatrix).  The score
+// accumulator of two 8-position tiles is, lane for lane, the A fragment of
+// P . V, so P never goes through shared memory.
+template <int HD>
+__global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int nqkv, const uint16_t* kc,
+                                                            const uint16_t* vc, int n, int start, int qh, int kvh,
+                                                            int max_seq, int layer, int swz, float* out) {
+    constexpr int KL = HD + 8;                 // padded smem rows: 8 ldmatrix row addresses hit 8 bank groups
+    extern __shared__ __align__(16) uint16_t at_smem[];
+    const int G = qh / kvh;
+    uint16_t* ks = at_smem;                    // [16][KL]
+    uint16_t* vs = ks + 16 * KL;               // [16][KL]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
+    uint16_t* qs = vs + 16 * KL + warp * (2 * 16 * KL);   // this warp's q parts [2][16][KL]
+    const int r0 = blockIdx.x * 16, grp = blockIdx.y, h = grp * G + warp;
+    const float qscale = 1.4426950408889634f * rsqrtf((float)HD);
+    // q rows r0 .. r0 + 15 of head h -> two bf16 parts in smem (rows past n are zero)
+    for (int i = lane; i < 16 * HD / 2; i += 32) {
+        const int r = i / (HD / 2), d = (i % (HD / 2)) * 2;
+        float x = 0.f, y = 0.f;
+        if (r0 + r < n) {
+            const float* q = QKV + (size_t)(r0 + r) * nqkv + (size_t)h * HD + d;
+            x = q[0] * qscale;
+            y = q[1] * qscale;
+        }
+        const uint32_t hi = pack_bf2(x, y);
+        const uint32_t lo = pack_bf2(x - __uint_as_float(hi << 16), y - __uint_as_float(hi & 0xFFFF0000u));
+        *reinterpret_cast<uint32_t*>(qs + r * KL + d) = hi;
+        *reinterpret_cast<uint32_t*>(qs + 16 * KL + r * KL + d) = lo;
+    }
+    const uint16_t* K = kc + ((size_t)layer * kvh + grp) * max_seq * HD;
+    const uint16_t* Vv = vc + ((size_t)layer * kvh + grp) * max_seq * HD;
+    const int kend = min(start + r0 + 16, start + n);   // keys [0, kend): the last row attends start + r0 + 15
+    float o[HD / 8][4];
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows g8 and g8 + 8
+    const int qp0 = start + r0 + g8, qp1 = qp0 + 8;             // their positions
+    for (int j0 = 0; j0 < kend; j0 += 16) {
+        __syncthreads();   // the previous tile is consumed (and, first time, q is stored)
+        // K and V rows j0 .. j0 + 15 -> smem in plain chunk order; rows past kend read as zero
+        for (int i = threadIdx.x; i < 2 * 16 * (HD / 8); i += blockDim.x) {
+            const int which = i / (16 * (HD / 8)), rem = i % (16 * (HD / 8));
+            const int r = rem / (HD / 8), c = rem % (HD / 8), p = j0 + r;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (p < kend) {
+                const int pc = swz ? (c ^ (p & 7)) : c;
+                v = reinterpret_cast<const uint4*>((which ? Vv : K) + (size_t)p * HD)[pc];
+            }
+            *reinterpret_cast<uint4*>((which ? vs : ks) + r * KL + 8 * c) = v;
+        }
+        __syncthreads();
+        // S = q . K^T: 16 rows x 16 positions (two n-tiles of 8)
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < HD; kk += 16) {
+            uint32_t kb[4];   // b fragments of positions 0-7 (kb[0], kb[1]) and 8-15 (kb[2], kb[3])
+            {
+                const int mtx = lane >> 3, key = (mtx >> 1) * 8 + (lane & 7), dim = kk + (mtx & 1) * 8;
+                ldsm_x4(kb, smem_u32(ks + key * KL + dim));
+            }
+#pragma unroll
+            for (int part = 1; part >= 0; --part) {
+                uint32_t qa[4];
+                const int row = lane & 15, dim = kk + (lane >> 4) * 8;
+                ldsm_x4(qa, smem_u32(qs + part * 16 * KL + row * KL + dim));
+                mma_bf16(sc[0], qa, kb[0], kb[1]);
+                mma_bf16(sc[1], qa, kb[2], kb[3]);
+            }
+        }
+        // causal mask; lane holds rows g8 (e 0, 1) and g8 + 8 (e 2, 3), positions j0 + 8 nt + 2 t4 (+1)
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kp = j0 + 8 * nt + 2 * t4 + (e & 1);
+                const int qp = (e < 2) ? qp0 : qp1;
+                if (kp > qp || kp >= kend) sc[nt][e] = -INFINITY;
+                if (e < 2) mx0 = fmaxf(mx0, sc[nt][e]); else mx1 = fmaxf(mx1, sc[nt][e]);
+            }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        // a row with no visible position yet (a padding row) keeps m = -inf and weights 0
+        const float c0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0), c1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+        float ps0 = 0.f, ps1 = 0.f;
+        uint32_t pa[2][4];   // P as the A fragment of P . V: [part][reg]
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float pv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float mm = (e < 2) ? mn0 : mn1;
+                pv[e] = (sc[nt][e] == -INFINITY) ? 0.f : exp2f(sc[nt][e] - mm);
+            }
+            ps0 += pv[0] + pv[1];
+            ps1 += pv[2] + pv[3];
+            // a0a1 = rows g8, positions 2t4 .. (tile 0) / a4a5 (tile 1); a2a3, a6a7 the rows g8 + 8
+            const uint32_t h01 = pack_bf2(pv[0], pv[1]), h23 = pack_bf2(pv[2], pv[3]);
+            pa[0][2 * nt] = h01;
+            pa[0][2 * nt + 1] = h23;
+            pa[1][2 * nt] = pack_bf2(pv[0] - __uint_as_float(h01 << 16), pv[1] - __uint_as_float(h01 & 0xFFFF0000u));
+            pa[1][2 * nt + 1] = pack_bf2(pv[2] - __uint_as_float(h23 << 16), pv[3] - __uint_as_float(h23 & 0xFFFF0000u));
+        }
+        ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 1);
+        ps0 += __shfl_xor_sync(0xFFFFFFFFu, ps0, 2);
+        ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 1);
+        ps1 += __shfl_xor_sync(0xFFFFFFFFu, ps1, 2);
+        l0 = l0 * c0 + ps0;
+        l1 = l1 * c1 + ps1;
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int j = 0; j < HD / 8; ++j) {
+            o[j][0] *= c0; o[j][1] *= c0;
+            o[j][2] *= c1; o[j][3] *= c1;
+        }
+        // O += P . V: dims in n-tiles of 8, two per transposed 8x8 quad load
+#pragma unroll
+        for (int nd = 0; nd < HD; nd += 16) {
+            uint32_t vb[4];
+            {
+                const int mtx = lane >> 3, key = (mtx & 1) * 8 + (lane & 7), dim = nd + (mtx >> 1) * 8;
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(vb[0]), "=r"(vb[1]), "=r"(vb[2]), "=r"(vb[3])
+                             : "r"(smem_u32(vs + key * KL + dim)));
+            }
+#pragma unroll
+            for (int part = 1; part >= 0; --part) {
+                mma_bf16(o[nd / 8], pa[part], vb[0], vb[1]);
+                mma_bf16(o[nd / 8 + 1], pa[part], vb[2], vb[3]);
+            }
+        }
+    }
+    // rows r0 + g8 and r0 + g8 + 8, dims 8 j + 2 t4 (+1)
+    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) {
+        const int d = 8 * j + 2 * t4;
+        if (r0 + g8 < n)
+            *reinterpret_cast<float2*>(out + (size_t)(r0 + g8) * qh * HD + (size_t)h * HD + d) =
+                make_float2(o[j][0] * i0, o[j][1] * i0);
+        if (r0 + g8 + 8 < n)
+            *reinterpret_cast<float2*>(out + (size_t)(r0 + g8 + 8) * qh * HD + (size_t)h * HD + d) =
+                make_float2(o[j][2] * i1, o[j][3] * i1);
+    }
+}
+
+template <int HD>
+size_t attn_tc_smem(int G) { return (size_t)(2 * 16 + G * 2 * 16) * (HD + 8) * 2; }
+
 template <bool RES>
 void gemm(const float* A, const uint16_t* W, const float* R, float* C, int M, int N, int K, cudaStream_t st) {
     const dim3 grid((N + GBN - 1) / GBN, (M + GBM - 1) / GBM);
@@ -662,6 +823,12 @@ cudaError_t mk_prefill_prepare() {
                                  (int)sizeof(GemmSmem));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)T_SMEM);
+    if (e == cudaSuccess)   // up to 8 query heads per KV group
+        e = cudaFuncSetAttribute(attn_tc_rows_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn_tc_smem<64>(8));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_tc_rows_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn_tc_smem<128>(8));
     if (e == cudaSuccess && !g_encode) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -696,8 +863,16 @@ int mk_prefill_launch(const MkPrefillArgs& a, cudaStream_t st, cudaError_t* err)
         GEMM(a.xn, a.wqkv[l], nullptr, a.qkv, n, nqkv, H);
         rope_kv_rows_kernel<<<dim3(((qh + 2 * kvh) * hd / 2 + 127) / 128, n), 128, 0, st>>>(
             a.qkv, nqkv, a.rope_cos, a.rope_sin, a.start, qh, kvh, hd, a.max_seq, l, a.kc, a.vc, a.swz); ++launches;
-        const int warps = n * qh;
-        if (hd == 64)
+        const int warps = n * qh, G = qh / kvh;
+        const dim3 tgrid((n + 15) / 16, kvh);
+        if (a.attn_tc && hd == 64)
+            attn_tc_rows_kernel<64><<<tgrid, 32 * G, attn_tc_smem<64>(G), st>>>(a.qkv, nqkv, a.kc, a.vc, n, a.start,
+                                                                               qh, kvh, a.max_seq, l, a.swz, a.att);
+        else if (a.attn_tc)
+            attn_tc_rows_kernel<128><<<tgrid, 32 * G, attn_tc_smem<128>(G), st>>>(a.qkv, nqkv, a.kc, a.vc, n,
+                                                                                 a.start, qh, kvh, a.max_seq, l,
+                                                                                 a.swz, a.att);
+        else if (hd == 64)
             attn_rows_kernel<64><<<(warps + 3) / 4, 128, 0, st>>>(a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh,
                                                                    a.max_seq, l, a.swz, a.att);
         else

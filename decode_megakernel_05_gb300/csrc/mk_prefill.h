@@ -22,6 +22,7 @@ struct MkPrefillArgs {
     // the three bf16 parts of a GEMM's activations, [3][n rounded up to 128][max(H, F, qh*hd)]; null: the
     // GEMMs run on mma.sync instead of tcgen05
     uint16_t* parts;
+    int attn_tc;                   // 1: the causal attention on the tensor cores (query heads per KV group <= 8)
     float* hidden;                 // [H] final-norm output of the last row
     float* logits;                 // [V] logits of the last row
     unsigned long long* amax_part;

@@ -369,8 +369,10 @@ int mk_argmax_f32_noalloc(const float* logits, int32_t n, int32_t* out_token, vo
  * larger in-flight limit) ends: 0 (default) after the down projection's tiles,
  * 1 after the FFN-block flag wait, 2 after the next layer's QKV GEMV. */
 #define MK_DBG_STREAM_TAIL 14
-/* MK_DBG_PREFILL_GEMM: the GEMMs of mk_prefill: 0 (default) tcgen05 (TMA tiles,
- * TMEM accumulators), 1 the warp-level mma.sync ones (the ablation). */
+/* MK_DBG_PREFILL_GEMM: the engines of mk_prefill: 0 (default) tcgen05 GEMMs
+ * (TMA tiles, TMEM accumulators) and the causal attention on the tensor cores
+ * (mma.sync, up to 8 query heads per KV group); 1 the warp-level mma.sync GEMMs
+ * and the CUDA-core attention (the ablation). */
 #define MK_DBG_PREFILL_GEMM 15
 int mk_set_debug(mk_ctx* ctx, int32_t knob, int64_t value);
 
