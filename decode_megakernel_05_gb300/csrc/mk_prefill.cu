@@ -206,26 +206,37 @@ __global__ void __launch_bounds__(128) gemm_split_kernel(const float* __restrict
 // The same product on the fifth-generation tensor cores.  A's three bf16 parts
 // are written first (split_parts_kernel) as one bf16 matrix [3][Mp][K] (Mp =
 // M rounded up to 128, the padding rows zero).  A CTA owns a 128 x 128 tile
-// of C and walks K in blocks of 64 (one 128-byte row of each operand):
+// of C (128 x 256 for wide outputs: half the activation re-reads from L2) and
+// walks K in blocks of 64 (one 128-byte row of each operand):
 //   - warp 0, one thread: TMA (cp.async.bulk.tensor) copies of the three A
 //     part tiles and the W tile of a K block into one of three stages, with
 //     the 128-byte swizzle, completing on the stage's full barrier;
-//   - warp 1: allocates 128 TMEM columns (the fp32 accumulator: lane = row
+//   - warp 1: allocates BN TMEM columns (the fp32 accumulator: lane = row
 //     of the tile, column = column); one thread issues, per K block, 12
-//     tcgen05.mma (3 parts x 4 steps of K = 16, M = 128, N = 128, bf16 in,
+//     tcgen05.mma (3 parts x 4 steps of K = 16, M = 128, N = BN, bf16 in,
 //     fp32 accumulate, smallest part first) and commits them to the stage's
 //     empty barrier, and after the last block to the done barrier;
 //   - warps 2-5: wait for done, read the accumulator with tcgen05.ld (warp w
-//     reads TMEM lanes 32 (w mod 4) ..), add the residual and store C.
+//     reads TMEM lanes 32 (w mod 4) ..), add the residual and store C; or,
+//     when the residual is C itself, add the product into C with vector
+//     atomics, which lets ksplit CTAs (grid z) share one tile's K range (the
+//     outputs of 2048 columns would otherwise fill 64 of the 152 SMs).
 // Every wait is bounded (%globaltimer, 2 s); a time-out sets the time-out bit
 // (0x1) of the status word and the CTA still frees its TMEM.  The K tail and the rows of W
 // past N come in as zeros (TMA's out-of-bounds fill).
-constexpr int TBM = 128, TBN = 128, TBK = 64, TST = 3;
+constexpr int TBM = 128, TBK = 64;
 constexpr uint32_t T_PART = TBM * TBK * 2;                  // 16 KB: one part's A tile
-constexpr uint32_t T_WT = TBN * TBK * 2;                    // 16 KB: the W tile
-constexpr uint32_t T_STAGE = 3 * T_PART + T_WT;             // 64 KB
-constexpr uint32_t T_SMEM = TST * T_STAGE + 1024 + 128;     // stages, alignment slack, barriers
 constexpr uint64_t T_WAIT_NS = 2000000000ull;
+// Tile width, stages and shared memory per width: 128 wide in 3 stages of 64 KB, 256 wide in 2 of 80 KB.
+template <int BN> struct TcCfg {
+    static constexpr int ST = BN == 256 ? 2 : 3;
+    static constexpr uint32_t WT = (uint32_t)BN * TBK * 2;          // the W tile
+    static constexpr uint32_t STAGE = 3 * T_PART + WT;
+    static constexpr uint32_t SMEM = ST * STAGE + 1024 + 128;       // stages, alignment slack, barriers
+    // instruction descriptor: kind::f16, bf16 A and B (both K-major), fp32 D, M = 128, N = BN
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                      ((uint32_t)(TBM >> 4) << 24);
+};
 
 __device__ __forceinline__ uint64_t gtimer_ns() {
     uint64_t t;
@@ -268,13 +279,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     d |= (uint64_t)2 << 61;                              // 128-byte swizzle
     return d;
 }
-// Instruction descriptor: kind::f16, bf16 A and B (both K-major), fp32 D, M = 128, N = 128.
-constexpr uint32_t T_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TBN >> 3) << 17) |
-                             ((uint32_t)(TBM >> 4) << 24);
-
+template <int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const float* R,
-                   float* C, int M, int N, int K, int Mp, uint32_t* status) {
+                   float* C, int M, int N, int K, int Mp, int ksplit, uint32_t* status) {
+    using Cfg = TcCfg<BN>;
+    constexpr int TST = Cfg::ST;
+    constexpr int TBN = BN;
+    constexpr uint32_t T_STAGE = Cfg::STAGE, T_IDESC = Cfg::IDESC;
     extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
     // the stages need 1024-byte alignment (the swizzle pattern repeats every 8 rows of 128 bytes)
     const uint32_t raw = smem_u32(tc_smem_raw);
@@ -287,7 +299,11 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t* taddr_ptr = reinterpret_cast<uint32_t*>(tc_smem_raw + (taddr_slot - raw));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * TBM, n0 = blockIdx.x * TBN;
-    const int nkb = (K + TBK - 1) / TBK;
+    // this CTA's K blocks [kb0, kb0 + nkb); ksplit > 1 only with the atomic epilogue (R == C)
+    const int nkb_all = (K + TBK - 1) / TBK;
+    const int kb0 = (int)(((int64_t)blockIdx.z * nkb_all) / ksplit);
+    const int nkb = (int)(((int64_t)(blockIdx.z + 1) * nkb_all) / ksplit) - kb0;
+    const bool atomic_add = R == C;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TST; ++s) {
@@ -322,12 +338,12 @@ __global__ void __launch_bounds__(192, 1)
                 asm volatile(
                     "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
                     "[%4];" ::"r"(st + (uint32_t)part * T_PART),
-                    "l"(pa), "r"(kb * TBK), "r"(part * Mp + m0), "r"(full(s))
+                    "l"(pa), "r"((kb0 + kb) * TBK), "r"(part * Mp + m0), "r"(full(s))
                     : "memory");
             asm volatile(
                 "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
                 "[%4];" ::"r"(st + 3u * T_PART),
-                "l"(pw), "r"(kb * TBK), "r"(n0), "r"(full(s))
+                "l"(pw), "r"((kb0 + kb) * TBK), "r"(n0), "r"(full(s))
                 : "memory");
         }
     } else if (warp == 1 && lane == 0) {
@@ -380,7 +396,22 @@ __global__ void __launch_bounds__(192, 1)
                 : "r"(ta)
                 : "memory");
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (row < M) {
+            if (row < M && atomic_add) {
+                const int cb = n0 + c0;
+                float* dst = C + (size_t)row * N + cb;
+                if ((N & 3) == 0 && cb + 32 <= N) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + j), "f"(__uint_as_float(v[j])),
+                                     "f"(__uint_as_float(v[j + 1])), "f"(__uint_as_float(v[j + 2])),
+                                     "f"(__uint_as_float(v[j + 3]))
+                                     : "memory");
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (cb + j < N) atomicAdd(dst + j, __uint_as_float(v[j]));
+                }
+            } else if (row < M) {
                 const int cb = n0 + c0;
                 float* dst = C + (size_t)row * N + cb;
                 const float* res = R ? R + (size_t)row * N + cb : nullptr;
@@ -800,16 +831,26 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
 }
 
 // C = A . W^T (+ R) on the tcgen05 path: the parts of A, then the GEMM (2 launches).
+// Outputs of 8192 columns or more take 256-wide tiles.
 cudaError_t gemm_tc(const float* A, const uint16_t* W, const float* R, float* C, int M, int N, int K,
                     uint16_t* parts, uint32_t* status, cudaStream_t st) {
     const int Mp = (M + TBM - 1) / TBM * TBM;
     const size_t groups = (size_t)Mp * (K / 4);
     split_parts_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(A, M, K, Mp, parts);
+    const int bn = N >= 8192 ? 256 : 128;
     CUtensorMap ma, mw;
-    if (!make_map(&ma, parts, (uint64_t)K, (uint64_t)3 * Mp, TBM) || !make_map(&mw, W, (uint64_t)K, (uint64_t)N, TBN))
+    if (!make_map(&ma, parts, (uint64_t)K, (uint64_t)3 * Mp, TBM) || !make_map(&mw, W, (uint64_t)K, (uint64_t)N, bn))
         return cudaErrorInvalidValue;
-    const dim3 grid((N + TBN - 1) / TBN, Mp / TBM);
-    gemm_tc_kernel<<<grid, 192, T_SMEM, st>>>(ma, mw, R, C, M, N, K, Mp, status);
+    const int tiles = ((N + bn - 1) / bn) * (Mp / TBM), nkb = (K + TBK - 1) / TBK;
+    // a residual product adds into C with atomics, so its K range may be split until the grid covers the SMs
+    int ksplit = 1;
+    if (R == C)
+        while (ksplit < 4 && tiles * ksplit * 2 <= 160 && nkb >= 8 * ksplit * 2) ksplit *= 2;
+    const dim3 grid((N + bn - 1) / bn, Mp / TBM, ksplit);
+    if (bn == 256)
+        gemm_tc_kernel<256><<<grid, 192, TcCfg<256>::SMEM, st>>>(ma, mw, R, C, M, N, K, Mp, ksplit, status);
+    else
+        gemm_tc_kernel<128><<<grid, 192, TcCfg<128>::SMEM, st>>>(ma, mw, R, C, M, N, K, Mp, ksplit, status);
     return cudaGetLastError();
 }
 
@@ -822,7 +863,11 @@ cudaError_t mk_prefill_prepare() {
         e = cudaFuncSetAttribute(gemm_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(GemmSmem));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)T_SMEM);
+        e = cudaFuncSetAttribute(gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)TcCfg<128>::SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)TcCfg<256>::SMEM);
     if (e == cudaSuccess)   // up to 8 query heads per KV group
         e = cudaFuncSetAttribute(attn_tc_rows_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)attn_tc_smem<64>(8));
