@@ -1147,8 +1147,11 @@ int mk_prefill(mk_ctx* c, const int32_t* tokens, int32_t n, int32_t start_pos, f
     a.attn_norm = c->attn_norm; a.ffn_norm = c->ffn_norm; a.final_norm = c->final_norm;
     a.rope_cos = c->rope_cos; a.rope_sin = c->rope_sin; a.kc = c->kc; a.vc = c->vc;
     a.x = c->pf_x; a.xn = c->pf_xn; a.qkv = c->pf_qkv; a.att = c->pf_att; a.gu = c->pf_gu; a.u = c->pf_u;
-    a.parts = c->prefill_gemm == 0 ? c->pf_parts : nullptr;
-    a.attn_tc = (c->prefill_gemm == 0 && g.G <= 8) ? 1 : 0;
+    // tcgen05 GEMMs and the tensor-core attention (which writes the O-proj input's parts) go together
+    const bool tc = c->prefill_gemm == 0 && g.G <= 8;
+    a.parts = tc ? c->pf_parts : nullptr;
+    a.parts_rows = c->pf_rows;
+    a.attn_tc = tc ? 1 : 0;
     a.hidden = c->hidden;
     a.logits = logits_out ? logits_out : P.logits_tmp;
     a.amax_part = P.amax_part; a.amax_blocks = P.amax_blocks;

@@ -204,8 +204,9 @@ __global__ void __launch_bounds__(128) gemm_split_kernel(const float* __restrict
 // ---------------------------------------------------------------- tcgen05 GEMM
 //
 // The same product on the fifth-generation tensor cores.  A's three bf16 parts
-// are written first (split_parts_kernel) as one bf16 matrix [3][Mp][K] (Mp =
-// M rounded up to 128, the padding rows zero).  A CTA owns a 128 x 128 tile
+// come from the kernel that produced A (RMSNorm, attention, SiLU * up write
+// them instead of fp32), stored [3][rows][K]; the tensor map sees them as a
+// [3][M][K] box grid, so rows past M read as zero.  A CTA owns a 128 x 128 tile
 // of C (128 x 256 for wide outputs: half the activation re-reads from L2) and
 // walks K in blocks of 64 (one 128-byte row of each operand):
 //   - warp 0, one thread: TMA (cp.async.bulk.tensor) copies of the three A
@@ -282,7 +283,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 template <int BN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, const float* R,
-                   float* C, int M, int N, int K, int Mp, int ksplit, uint32_t* status) {
+                   float* C, int M, int N, int K, int ksplit, uint32_t* status) {
     using Cfg = TcCfg<BN>;
     constexpr int TST = Cfg::ST;
     constexpr int TBN = BN;
@@ -336,9 +337,9 @@ __global__ void __launch_bounds__(192, 1)
             mbar_expect(full(s), T_STAGE);
             for (int part = 0; part < 3; ++part)
                 asm volatile(
-                    "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-                    "[%4];" ::"r"(st + (uint32_t)part * T_PART),
-                    "l"(pa), "r"((kb0 + kb) * TBK), "r"(part * Mp + m0), "r"(full(s))
+                    "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+                    "%4}], [%5];" ::"r"(st + (uint32_t)part * T_PART),
+                    "l"(pa), "r"((kb0 + kb) * TBK), "r"(m0), "r"(part), "r"(full(s))
                     : "memory");
             asm volatile(
                 "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
@@ -443,25 +444,15 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-// A fp32 [M][K] -> its three bf16 parts [3][Mp][K] (rows M .. Mp - 1 zero).
-__global__ void split_parts_kernel(const float* A, int M, int K, int Mp, uint16_t* P) {
-    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;   // one group of 4 columns
-    const size_t per_row = (size_t)K / 4;
-    if (i >= (size_t)Mp * per_row) return;
-    const int r = (int)(i / per_row), c = (int)(i % per_row) * 4;
-    float e[4] = {0.f, 0.f, 0.f, 0.f};
-    if (r < M) {
-        const float4 a = *reinterpret_cast<const float4*>(A + (size_t)r * K + c);
-        e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w;
-    }
+// The three bf16 parts of v (its rounding, the rounding of the remainder, and
+// of what is left) at P[i], P[i + ps], P[i + 2 ps]; a pair (x, y) at i, i + 1.
+__device__ __forceinline__ void store_parts2(uint16_t* P, size_t ps, size_t i, float x, float y) {
 #pragma unroll
     for (int part = 0; part < 3; ++part) {
-        const uint32_t p01 = pack_bf2(e[0], e[1]), p23 = pack_bf2(e[2], e[3]);
-        *reinterpret_cast<uint2*>(P + ((size_t)part * Mp + r) * K + c) = make_uint2(p01, p23);
-        e[0] -= __uint_as_float(p01 << 16);
-        e[1] -= __uint_as_float(p01 & 0xFFFF0000u);
-        e[2] -= __uint_as_float(p23 << 16);
-        e[3] -= __uint_as_float(p23 & 0xFFFF0000u);
+        const uint32_t b = pack_bf2(x, y);
+        *reinterpret_cast<uint32_t*>(P + part * ps + i) = b;
+        x -= __uint_as_float(b << 16);
+        y -= __uint_as_float(b & 0xFFFF0000u);
     }
 }
 
@@ -478,8 +469,10 @@ __global__ void embed_rows_kernel(const uint16_t* E, const int32_t* tok, int n, 
     for (int d = threadIdx.x; d < H; d += blockDim.x) X[(size_t)i * H + d] = bf(E[(size_t)tk * H + d]);
 }
 
-// y = x / sqrt(mean(x^2) + eps) * g for row blockIdx.x
-__global__ void rmsnorm_rows_kernel(const float* X, const float* g, int H, float eps, float* Y) {
+// y = x / sqrt(mean(x^2) + eps) * g for row blockIdx.x, to Y (fp32) and/or
+// to the parts P (row stride H, part stride ps).
+__global__ void rmsnorm_rows_kernel(const float* X, const float* g, int H, float eps, float* Y, uint16_t* P,
+                                    size_t ps) {
     __shared__ float red[32];
     const float* x = X + (size_t)blockIdx.x * H;
     float ss = 0.f;
@@ -490,8 +483,13 @@ __global__ void rmsnorm_rows_kernel(const float* X, const float* g, int H, float
     float tot = 0.f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
     const float inv = rsqrtf(tot / (float)H + eps);
-    float* y = Y + (size_t)blockIdx.x * H;
-    for (int d = threadIdx.x; d < H; d += blockDim.x) y[d] = x[d] * inv * g[d];
+    if (Y) {
+        float* y = Y + (size_t)blockIdx.x * H;
+        for (int d = threadIdx.x; d < H; d += blockDim.x) y[d] = x[d] * inv * g[d];
+    }
+    if (P)
+        for (int d = 2 * threadIdx.x; d < H; d += 2 * blockDim.x)
+            store_parts2(P, ps, (size_t)blockIdx.x * H + d, x[d] * inv * g[d], x[d + 1] * inv * g[d + 1]);
 }
 
 // RoPE on the q and k heads of row blockIdx.y (position start + row), then the
@@ -590,12 +588,21 @@ __global__ void attn_rows_kernel(const float* QKV, int nqkv, const uint16_t* kc,
 }
 
 // U[row][j] = silu(GU[row][j]) * GU[row][F + j]
-__global__ void silu_mul_kernel(const float* GU, int n, int F, float* U) {
-    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+// u = SiLU(gate) * up per row, to U (fp32) or to the parts P (part stride ps);
+// a thread takes two neighbouring columns (F is even).
+__global__ void silu_mul_kernel(const float* GU, int n, int F, float* U, uint16_t* P, size_t ps) {
+    const size_t i = 2 * ((size_t)blockIdx.x * blockDim.x + threadIdx.x);
     if (i >= (size_t)n * F) return;
     const size_t row = i / F, j = i % F;
-    const float gt = GU[row * 2 * F + j], up = GU[row * 2 * F + F + j];
-    U[i] = gt / (1.f + __expf(-gt)) * up;
+    const float* gu = GU + row * 2 * F;
+    const float g0 = gu[j], g1 = gu[j + 1], u0 = gu[F + j], u1 = gu[F + j + 1];
+    const float a = g0 / (1.f + __expf(-g0)) * u0, b = g1 / (1.f + __expf(-g1)) * u1;
+    if (P) {
+        store_parts2(P, ps, i, a, b);
+    } else {
+        U[i] = a;
+        U[i + 1] = b;
+    }
 }
 
 __device__ __forceinline__ unsigned long long pack_key(float v, int idx) {
@@ -657,7 +664,8 @@ __global__ void argmax_final_kernel(const unsigned long long* part, int n, int32
 template <int HD>
 __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int nqkv, const uint16_t* kc,
                                                             const uint16_t* vc, int n, int start, int qh, int kvh,
-                                                            int max_seq, int layer, int swz, float* out) {
+                                                            int max_seq, int layer, int swz, float* out, uint16_t* P,
+                                                            size_t ps) {
     constexpr int KL = HD + 8;                 // padded smem rows: 8 ldmatrix row addresses hit 8 bank groups
     extern __shared__ __align__(16) uint16_t at_smem[];
     const int G = qh / kvh;
@@ -788,17 +796,20 @@ __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int
             }
         }
     }
-    // rows r0 + g8 and r0 + g8 + 8, dims 8 j + 2 t4 (+1)
+    // rows r0 + g8 and r0 + g8 + 8, dims 8 j + 2 t4 (+1): fp32 to out, or the parts to P
     const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
     for (int j = 0; j < HD / 8; ++j) {
         const int d = 8 * j + 2 * t4;
-        if (r0 + g8 < n)
-            *reinterpret_cast<float2*>(out + (size_t)(r0 + g8) * qh * HD + (size_t)h * HD + d) =
-                make_float2(o[j][0] * i0, o[j][1] * i0);
-        if (r0 + g8 + 8 < n)
-            *reinterpret_cast<float2*>(out + (size_t)(r0 + g8 + 8) * qh * HD + (size_t)h * HD + d) =
-                make_float2(o[j][2] * i1, o[j][3] * i1);
+        const size_t e0 = (size_t)(r0 + g8) * qh * HD + (size_t)h * HD + d, e1 = e0 + (size_t)8 * qh * HD;
+        if (r0 + g8 < n) {
+            if (P) store_parts2(P, ps, e0, o[j][0] * i0, o[j][1] * i0);
+            else *reinterpret_cast<float2*>(out + e0) = make_float2(o[j][0] * i0, o[j][1] * i0);
+        }
+        if (r0 + g8 + 8 < n) {
+            if (P) store_parts2(P, ps, e1, o[j][2] * i1, o[j][3] * i1);
+            else *reinterpret_cast<float2*>(out + e1) = make_float2(o[j][2] * i1, o[j][3] * i1);
+        }
     }
 }
 
@@ -830,16 +841,27 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// C = A . W^T (+ R) on the tcgen05 path: the parts of A, then the GEMM (2 launches).
+// Tensor map of the three parts [3][rows][K] of an M-row activation, read in
+// boxes of 64 x 128 x 1: rows M .. past the last tile read as zero.
+bool make_parts_map(CUtensorMap* m, const uint16_t* parts, uint64_t K, uint64_t M, uint64_t rows) {
+    const cuuint64_t dims[3] = {K, M, 3};
+    const cuuint64_t strides[2] = {K * 2, rows * K * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)TBK, (cuuint32_t)TBM, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return g_encode && g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(parts), dims, strides,
+                                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// C = A . W^T (+ R) on the tcgen05 path, A given as its parts [3][rows][K] (1 launch).
 // Outputs of 8192 columns or more take 256-wide tiles.
-cudaError_t gemm_tc(const float* A, const uint16_t* W, const float* R, float* C, int M, int N, int K,
-                    uint16_t* parts, uint32_t* status, cudaStream_t st) {
+cudaError_t gemm_tc(const uint16_t* parts, int rows, const uint16_t* W, const float* R, float* C, int M, int N, int K,
+                    uint32_t* status, cudaStream_t st) {
     const int Mp = (M + TBM - 1) / TBM * TBM;
-    const size_t groups = (size_t)Mp * (K / 4);
-    split_parts_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(A, M, K, Mp, parts);
     const int bn = N >= 8192 ? 256 : 128;
     CUtensorMap ma, mw;
-    if (!make_map(&ma, parts, (uint64_t)K, (uint64_t)3 * Mp, TBM) || !make_map(&mw, W, (uint64_t)K, (uint64_t)N, bn))
+    if (!make_parts_map(&ma, parts, (uint64_t)K, (uint64_t)M, (uint64_t)rows) ||
+        !make_map(&mw, W, (uint64_t)K, (uint64_t)N, bn))
         return cudaErrorInvalidValue;
     const int tiles = ((N + bn - 1) / bn) * (Mp / TBM), nkb = (K + TBK - 1) / TBK;
     // a residual product adds into C with atomics, so its K range may be split until the grid covers the SMs
@@ -848,9 +870,9 @@ cudaError_t gemm_tc(const float* A, const uint16_t* W, const float* R, float* C,
         while (ksplit < 4 && tiles * ksplit * 2 <= 160 && nkb >= 8 * ksplit * 2) ksplit *= 2;
     const dim3 grid((N + bn - 1) / bn, Mp / TBM, ksplit);
     if (bn == 256)
-        gemm_tc_kernel<256><<<grid, 192, TcCfg<256>::SMEM, st>>>(ma, mw, R, C, M, N, K, Mp, ksplit, status);
+        gemm_tc_kernel<256><<<grid, 192, TcCfg<256>::SMEM, st>>>(ma, mw, R, C, M, N, K, ksplit, status);
     else
-        gemm_tc_kernel<128><<<grid, 192, TcCfg<128>::SMEM, st>>>(ma, mw, R, C, M, N, K, Mp, ksplit, status);
+        gemm_tc_kernel<128><<<grid, 192, TcCfg<128>::SMEM, st>>>(ma, mw, R, C, M, N, K, ksplit, status);
     return cudaGetLastError();
 }
 
@@ -889,34 +911,33 @@ int mk_prefill_launch(const MkPrefillArgs& a, cudaStream_t st, cudaError_t* err)
     const int nqkv = (qh + 2 * kvh) * hd, qd = qh * hd;
     int launches = 0;
     *err = cudaSuccess;
-    // the tcgen05 GEMM (parts + GEMM: 2 launches) when a parts buffer is given, else the mma.sync one
-#define GEMM(A_, W_, R_, C_, M_, N_, K_)                                                                  \
-    do {                                                                                                   \
-        if (a.parts) {                                                                                     \
-            cudaError_t e_ = gemm_tc(A_, W_, R_, C_, M_, N_, K_, a.parts, a.status, st);                    \
-            if (e_ != cudaSuccess && *err == cudaSuccess) *err = e_;                                       \
-            launches += 2;                                                                                 \
-        } else {                                                                                           \
-            if (R_) gemm<true>(A_, W_, R_, C_, M_, N_, K_, st);                                             \
-            else gemm<false>(A_, W_, R_, C_, M_, N_, K_, st);                                               \
-            launches += 1;                                                                                 \
-        }                                                                                                  \
-    } while (0)
+    // tcgen05 path (a.parts): each GEMM's activation goes from its producer to the parts buffer as
+    // [3][parts_rows][K]; otherwise fp32 activations and the mma.sync GEMMs
+    const bool tc = a.parts != nullptr;
+    uint16_t* P = a.parts;
+    const size_t prow = (size_t)a.parts_rows;
+    auto note = [&](cudaError_t e) { if (e != cudaSuccess && *err == cudaSuccess) *err = e; };
+    auto gemm_any = [&](const float* A, const uint16_t* W, const float* R, float* C, int M, int N, int K) {
+        if (tc) note(gemm_tc(P, (int)prow, W, R, C, M, N, K, a.status, st));
+        else if (R) gemm<true>(A, W, R, C, M, N, K, st);
+        else gemm<false>(A, W, R, C, M, N, K, st);
+        ++launches;
+    };
     embed_rows_kernel<<<n, 256, 0, st>>>(a.embed, a.tokens, n, a.V, H, a.x, a.status); ++launches;
     for (int l = 0; l < a.L; ++l) {
-        rmsnorm_rows_kernel<<<n, 256, 0, st>>>(a.x, a.attn_norm + (size_t)l * H, H, a.eps, a.xn); ++launches;
-        GEMM(a.xn, a.wqkv[l], nullptr, a.qkv, n, nqkv, H);
+        rmsnorm_rows_kernel<<<n, 256, 0, st>>>(a.x, a.attn_norm + (size_t)l * H, H, a.eps, tc ? nullptr : a.xn, P,
+                                               prow * H); ++launches;
+        gemm_any(a.xn, a.wqkv[l], nullptr, a.qkv, n, nqkv, H);
         rope_kv_rows_kernel<<<dim3(((qh + 2 * kvh) * hd / 2 + 127) / 128, n), 128, 0, st>>>(
             a.qkv, nqkv, a.rope_cos, a.rope_sin, a.start, qh, kvh, hd, a.max_seq, l, a.kc, a.vc, a.swz); ++launches;
         const int warps = n * qh, G = qh / kvh;
         const dim3 tgrid((n + 15) / 16, kvh);
         if (a.attn_tc && hd == 64)
-            attn_tc_rows_kernel<64><<<tgrid, 32 * G, attn_tc_smem<64>(G), st>>>(a.qkv, nqkv, a.kc, a.vc, n, a.start,
-                                                                               qh, kvh, a.max_seq, l, a.swz, a.att);
+            attn_tc_rows_kernel<64><<<tgrid, 32 * G, attn_tc_smem<64>(G), st>>>(
+                a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh, a.max_seq, l, a.swz, a.att, P, prow * qd);
         else if (a.attn_tc)
-            attn_tc_rows_kernel<128><<<tgrid, 32 * G, attn_tc_smem<128>(G), st>>>(a.qkv, nqkv, a.kc, a.vc, n,
-                                                                                 a.start, qh, kvh, a.max_seq, l,
-                                                                                 a.swz, a.att);
+            attn_tc_rows_kernel<128><<<tgrid, 32 * G, attn_tc_smem<128>(G), st>>>(
+                a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh, a.max_seq, l, a.swz, a.att, P, prow * qd);
         else if (hd == 64)
             attn_rows_kernel<64><<<(warps + 3) / 4, 128, 0, st>>>(a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh,
                                                                    a.max_seq, l, a.swz, a.att);
@@ -924,20 +945,20 @@ int mk_prefill_launch(const MkPrefillArgs& a, cudaStream_t st, cudaError_t* err)
             attn_rows_kernel<128><<<(warps + 3) / 4, 128, 0, st>>>(a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh,
                                                                     a.max_seq, l, a.swz, a.att);
         ++launches;
-        GEMM(a.att, a.wo[l], a.x, a.x, n, H, qd);   // residual in place
-        rmsnorm_rows_kernel<<<n, 256, 0, st>>>(a.x, a.ffn_norm + (size_t)l * H, H, a.eps, a.xn); ++launches;
-        GEMM(a.xn, a.wgu[l], nullptr, a.gu, n, 2 * F, H);
-        silu_mul_kernel<<<(int)(((size_t)n * F + 255) / 256), 256, 0, st>>>(a.gu, n, F, a.u); ++launches;
-        GEMM(a.u, a.wd[l], a.x, a.x, n, H, F);
+        gemm_any(a.att, a.wo[l], a.x, a.x, n, H, qd);   // residual in place
+        rmsnorm_rows_kernel<<<n, 256, 0, st>>>(a.x, a.ffn_norm + (size_t)l * H, H, a.eps, tc ? nullptr : a.xn, P,
+                                               prow * H); ++launches;
+        gemm_any(a.xn, a.wgu[l], nullptr, a.gu, n, 2 * F, H);
+        silu_mul_kernel<<<(int)(((size_t)n * F / 2 + 255) / 256), 256, 0, st>>>(a.gu, n, F, a.u, P, prow * F);
+        ++launches;
+        gemm_any(a.u, a.wd[l], a.x, a.x, n, H, F);
     }
     // the last row: final norm (kept as the step's hidden state), LM head, argmax
     const float* xlast = a.x + (size_t)(n - 1) * H;
-    rmsnorm_rows_kernel<<<1, 256, 0, st>>>(xlast, a.final_norm, H, a.eps, a.hidden); ++launches;
-    GEMM(a.hidden, a.lm, nullptr, a.logits, 1, a.V, H);
+    rmsnorm_rows_kernel<<<1, 256, 0, st>>>(xlast, a.final_norm, H, a.eps, a.hidden, P, prow * H); ++launches;
+    gemm_any(a.hidden, a.lm, nullptr, a.logits, 1, a.V, H);
     argmax_blocks_kernel<<<a.amax_blocks, 256, 0, st>>>(a.logits, a.V, a.amax_part, a.status); ++launches;
     argmax_final_kernel<<<1, 32, 0, st>>>(a.amax_part, a.amax_blocks, a.next_token, a.status); ++launches;
-#undef GEMM
-    const cudaError_t e = cudaGetLastError();
-    if (*err == cudaSuccess) *err = e;
+    note(cudaGetLastError());
     return launches;
 }

@@ -19,9 +19,10 @@ struct MkPrefillArgs {
     uint16_t *kc, *vc;
     // fp32 workspace: x, xn [n][H], qkv [n][qkv rows], att [n][qh*hd], gu [n][2F], u [n][F]
     float *x, *xn, *qkv, *att, *gu, *u;
-    // the three bf16 parts of a GEMM's activations, [3][n rounded up to 128][max(H, F, qh*hd)]; null: the
-    // GEMMs run on mma.sync instead of tcgen05
+    // the three bf16 parts of a GEMM's activations, [3][parts_rows][K] for the GEMM's K (room for
+    // max(H, F, qh*hd)); null: fp32 activations and the GEMMs on mma.sync instead of tcgen05
     uint16_t* parts;
+    int parts_rows;
     int attn_tc;                   // 1: the causal attention on the tensor cores (query heads per KV group <= 8)
     float* hidden;                 // [H] final-norm output of the last row
     float* logits;                 // [V] logits of the last row
