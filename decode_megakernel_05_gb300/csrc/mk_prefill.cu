@@ -655,7 +655,8 @@ __global__ void argmax_final_kernel(const unsigned long long* part, int n, int32
 // CTA takes 16 query rows (positions start + r0 ..) and the G query heads of
 // one KV group, warp w the head g * G + w, so the group's K/V tile of 16
 // positions is loaded once (un-permuting the cache's chunk order) and read by
-// the G warps.  Per tile: S = q . K^T with q split into its bf16 rounding and
+// the G warps; the next tile's cp.async copies are in flight while a tile is
+// used (two buffers).  Per tile: S = q . K^T with q split into its bf16 rounding and
 // the rounding of the remainder (q . k to about 2^-17 relative), the causal
 // mask, an online softmax in base 2 (q pre-scaled by log2(e) / sqrt(hd)), P
 // split the same way, O += P . V (V read transposed by ldmatrix).  The score
@@ -669,10 +670,10 @@ __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int
     constexpr int KL = HD + 8;                 // padded smem rows: 8 ldmatrix row addresses hit 8 bank groups
     extern __shared__ __align__(16) uint16_t at_smem[];
     const int G = qh / kvh;
-    uint16_t* ks = at_smem;                    // [16][KL]
-    uint16_t* vs = ks + 16 * KL;               // [16][KL]
+    uint16_t* ks0 = at_smem;                   // [2 buffers][16][KL]
+    uint16_t* vs0 = ks0 + 2 * 16 * KL;         // [2 buffers][16][KL]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
-    uint16_t* qs = vs + 16 * KL + warp * (2 * 16 * KL);   // this warp's q parts [2][16][KL]
+    uint16_t* qs = vs0 + 2 * 16 * KL + warp * (2 * 16 * KL);   // this warp's q parts [2][16][KL]
     const int r0 = blockIdx.x * 16, grp = blockIdx.y, h = grp * G + warp;
     const float qscale = 1.4426950408889634f * rsqrtf((float)HD);
     // q rows r0 .. r0 + 15 of head h -> two bf16 parts in smem (rows past n are zero)
@@ -697,20 +698,29 @@ __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int
     for (int j = 0; j < HD / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows g8 and g8 + 8
     const int qp0 = start + r0 + g8, qp1 = qp0 + 8;             // their positions
-    for (int j0 = 0; j0 < kend; j0 += 16) {
-        __syncthreads();   // the previous tile is consumed (and, first time, q is stored)
-        // K and V rows j0 .. j0 + 15 -> smem in plain chunk order; rows past kend read as zero
+    // K and V rows j0 .. j0 + 15 -> buffer b in plain chunk order (cp.async; rows past kend zero-filled)
+    auto load_tile = [&](int j0, int b) {
         for (int i = threadIdx.x; i < 2 * 16 * (HD / 8); i += blockDim.x) {
             const int which = i / (16 * (HD / 8)), rem = i % (16 * (HD / 8));
             const int r = rem / (HD / 8), c = rem % (HD / 8), p = j0 + r;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (p < kend) {
-                const int pc = swz ? (c ^ (p & 7)) : c;
-                v = reinterpret_cast<const uint4*>((which ? Vv : K) + (size_t)p * HD)[pc];
-            }
-            *reinterpret_cast<uint4*>((which ? vs : ks) + r * KL + 8 * c) = v;
+            const bool in = p < kend;
+            const int pc = (swz && in) ? (c ^ (p & 7)) : c;
+            const uint16_t* src = (which ? Vv : K) + (size_t)(in ? p : 0) * HD + 8 * pc;
+            cp_async16(smem_u32((which ? vs0 : ks0) + (b * 16 + r) * KL + 8 * c), src, in ? 16u : 0u);
         }
-        __syncthreads();
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    load_tile(0, 0);
+    for (int j0 = 0, b = 0; j0 < kend; j0 += 16, b ^= 1) {
+        const uint16_t* ks = ks0 + b * 16 * KL;
+        const uint16_t* vs = vs0 + b * 16 * KL;
+        if (j0 + 16 < kend) {
+            load_tile(j0 + 16, b ^ 1);   // its buffer was released by the barrier ending the last round
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();   // this tile landed for every thread (and, first time, q is stored)
         // S = q . K^T: 16 rows x 16 positions (two n-tiles of 8)
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -795,6 +805,7 @@ __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int
                 mma_bf16(o[nd / 8 + 1], pa[part], vb[2], vb[3]);
             }
         }
+        __syncthreads();   // every warp is done with this buffer before the copy two tiles on refills it
     }
     // rows r0 + g8 and r0 + g8 + 8, dims 8 j + 2 t4 (+1): fp32 to out, or the parts to P
     const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
@@ -814,7 +825,7 @@ __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int
 }
 
 template <int HD>
-size_t attn_tc_smem(int G) { return (size_t)(2 * 16 + G * 2 * 16) * (HD + 8) * 2; }
+size_t attn_tc_smem(int G) { return (size_t)(4 * 16 + G * 2 * 16) * (HD + 8) * 2; }
 
 template <bool RES>
 void gemm(const float* A, const uint16_t* W, const float* R, float* C, int M, int N, int K, cudaStream_t st) {
