@@ -24,7 +24,8 @@ replica on its own GPU and `value` is the total tokens/s of all replicas.
 cores, on the same workload, metric and unit.
 
 For the prompt workloads the line also carries "prefill": the 512-token prompt
-through the batched prefill (mk_prefill, tensor-core GEMMs), CUDA-event timed
+through the batched prefill (mk_prefill: tcgen05 GEMMs, tensor-core causal
+attention), CUDA-event timed
 on its own and against the same prompt as 512 fused decode launches; its
 roofline is tensor-bound against the measured bf16 peak.  It also carries
 "int8": the same decode steps on a weight-only INT8 context (the int8 build of
@@ -245,8 +246,10 @@ def time_prefill(dec, w, torch, reps: int = 5):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_source": src,
                          "algorithmic_flops": fl,
-                         "note": "mma.sync bf16 with each fp32 activation as three bf16 parts: "
-                                 "3x the tensor work of the algorithmic FLOPs"},
+                         "tensor_work_tflops": 3 * achieved,
+                         "note": "tcgen05 GEMMs (TMA tiles, TMEM accumulators) with each fp32 activation as "
+                                 "three bf16 parts: about 3x the tensor work of the algorithmic FLOPs "
+                                 "(tensor_work_tflops counts it); causal attention on mma.sync"},
             "decode_launch_prompt_ms": dl_ms, "speedup_vs_decode_launches": dl_ms / pf_ms}
 
 
