@@ -271,6 +271,38 @@ def test_int8_generate_matches_oracle_tokens():
     dec.close()
 
 
+def test_int8_topp_sampling_matches_oracle():
+    """Temperature and top-p on the int8 stream (the LM head's int8 rows feed
+    the same in-launch nucleus search): the fused draw equals the oracle's
+    nucleus sample from its int8 logits, up to the boundary cases the logit
+    error allows."""
+    from tests.test_parity_gpu import _nucleus_bounds, _oracle_keys
+    m, q8, dec, orc = make_q8(TINY, 71, 128)
+    dec.set_top_p(0.9)
+    inv = float(np.float32(1.0 / 1.0))
+    seed, tok, agree, steps = 0x5EED, 7, 0, 24
+    for pos in range(steps):
+        dec.step_sample(tok, pos, 1.0, seed, logits=True)
+        lg_ref, _ = orc.step(tok, pos)
+        lg = dec.logits.cpu().numpy().astype(np.float64)
+        got = dec.get_argmax()
+        want, nf = oracle.sample_topp_f32(lg_ref, inv, 0.9, seed, pos)
+        assert not nf
+        dl = float(np.max(np.abs(lg - lg_ref)))
+        assert dl <= 5e-2
+        if got == want:
+            agree += 1
+        else:
+            loose, strict = _nucleus_bounds(lg_ref, inv, 0.9, dl)
+            keys = _oracle_keys(lg_ref, inv, seed, pos)
+            assert got in loose, (pos, got, want)
+            assert keys[got] >= max(keys[v] for v in strict) - (2 * dl * inv + 1e-5), (pos, got, want)
+        tok = want
+    assert agree >= steps - 2, agree
+    assert dec.status() == 0
+    dec.close()
+
+
 def test_int8_refuses_the_bf16_only_paths():
     w = synth.WORKLOADS["tiny"]
     m = synth.make_model(w.shape, 3)
