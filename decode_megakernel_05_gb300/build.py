@@ -27,11 +27,11 @@ VARIANTS = [(64, 2, 1), (64, 4, 2), (64, 4, 4), (64, 4, 8), (64, 4, 16), (128, 4
 # long-context builds (attention on the tensor cores), launched for steps whose context gives
 # each CTA at least MK_ATTN_TC_MIN_PER_CTA positions; keep in sync with MK_LC_VARIANTS in
 # csrc/mk_api.cu
-LC_VARIANTS = [(64, 4, 2), (64, 4, 8)]
+LC_VARIANTS = [(64, 4, 2), (64, 4, 8), (128, 4, 4), (128, 4, 16)]
 # weight-only INT8 builds (-DMK_WB_V=1) of the standard and long-context kernels; keep in sync
 # with MK_Q8_VARIANTS and MK_Q8_LC_VARIANTS in csrc/mk_api.cu
 Q8_VARIANTS = [(64, 2, 1), (64, 4, 8), (128, 4, 16)]
-Q8_LC_VARIANTS = [(64, 4, 8)]
+Q8_LC_VARIANTS = [(64, 4, 8), (128, 4, 16)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

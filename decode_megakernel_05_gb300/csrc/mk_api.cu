@@ -21,11 +21,11 @@
 // with VARIANTS in build.py.
 #define MK_VARIANTS(X) \
     X(64, 2, 1) X(64, 4, 2) X(64, 4, 4) X(64, 4, 8) X(64, 4, 16) X(128, 4, 4) X(128, 4, 8) X(128, 4, 16)
-#define MK_LC_VARIANTS(X) X(64, 4, 2) X(64, 4, 8)
+#define MK_LC_VARIANTS(X) X(64, 4, 2) X(64, 4, 8) X(128, 4, 4) X(128, 4, 16)
 // Weight-only INT8 builds (-DMK_WB_V=1; keep in sync with Q8_VARIANTS and
 // Q8_LC_VARIANTS in build.py).
 #define MK_Q8_VARIANTS(X) X(64, 2, 1) X(64, 4, 8) X(128, 4, 16)
-#define MK_Q8_LC_VARIANTS(X) X(64, 4, 8)
+#define MK_Q8_LC_VARIANTS(X) X(64, 4, 8) X(128, 4, 16)
 // Each variant exists twice: without trace code (launched normally) and with
 // it (launched while a segment trace is requested).
 #define MK_DECL(hd, g, mh)                                         \

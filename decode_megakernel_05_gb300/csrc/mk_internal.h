@@ -146,12 +146,9 @@ MK_HD int64_t mk_kv_index(int64_t pos, int d, int hd, int swz) {
     return pos * hd + ((int64_t)((swz ? (c ^ (int)(pos & 7)) : c) << 3) | (d & 7));
 }
 
-// Shapes whose attention runs on the tensor cores (4 query heads of 64 dims
-// per KV group); their K/V cache rows are chunk-permuted (mk_kv_index).  With
-// 128 dims the O accumulators (32 registers a lane) spill under the kernel's
-// 128-register budget and the 8B-shape step measured 2.8% slower, so those
-// shapes keep the lane-parallel attention and plain rows.
-MK_HD constexpr bool mk_attn_tc(int hd, int G) { return hd == 64 && G == 4; }
+// Shapes whose attention can run on the tensor cores (4 query heads of 64 or
+// 128 dims per KV group); their K/V cache rows are chunk-permuted (mk_kv_index).
+MK_HD constexpr bool mk_attn_tc(int hd, int G) { return (hd == 64 || hd == 128) && G == 4; }
 
 // Fills everything but smem offsets from the shape; returns false if the
 // shape is outside what the kernels support.

@@ -1132,7 +1132,7 @@ struct Attn {
     }
 };
 
-// ---- long-context attention on the tensor cores (HD = 64, G = 4)
+// ---- long-context attention on the tensor cores (HD = 64 or 128, G = 4)
 //
 // At long contexts a CTA attends to thousands of positions per layer, and the
 // per-position arithmetic of the lane-parallel softmax above (partial dots
@@ -1153,7 +1153,10 @@ struct Attn {
 // of bank conflicts.  Warps take the 16-position chunks of the CTA's range in
 // turn (continuing across blocks); each keeps its own online softmax state
 // (m, l per head, O rows) and parks it in the same form as the lane-parallel
-// version, so the partial that leaves the CTA is computed the same way.
+// version, so the partial that leaves the CTA is computed the same way.  With
+// 128-dim heads four warps take each chunk: all four compute its scores over
+// the 128 dims (the same arithmetic, so the same m and l) and each accumulates
+// 32 dims of O (mk_attn_tc_split).
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
@@ -1193,6 +1196,12 @@ __device__ __forceinline__ uint32_t split_bf2(float x, float y, bool lo) {
 // so a lane reads its words back with 16-byte loads.  Lane L holds row L / 4 of
 // [q_hi; q_lo]: head (L / 4) mod 4, the bf16 high parts for L < 16 and the
 // bf16 of the remainders for L >= 16, dims 16 ks + 8 half + 2 (L mod 4) (+1).
+// Warps that share each 16-position chunk of the tensor-core attention (each
+// accumulates HD / split dims of O: with all 128 dims in one warp, or 64, the
+// 8B-width build spilled under its 128-register budget) and the groups its
+// warps park.
+__host__ __device__ constexpr int mk_attn_tc_split(int hd) { return hd == 128 ? 4 : 1; }
+__host__ __device__ constexpr int mk_attn_tc_groups(int hd) { return MK_NCW / mk_attn_tc_split(hd); }
 __device__ __forceinline__ int qfrag_word(int f, int lane) { return (f >> 2) * 128 + 4 * lane + (f & 3); }
 
 // The block loop of the tensor-core attention (q of the group's heads already
@@ -1203,17 +1212,23 @@ __device__ __forceinline__ int qfrag_word(int f, int lane) { return (f >> 2) * 1
 // parked for the caller.  The fragments are read back from shared memory for
 // every 16-position chunk rather than held in registers across the loop: held,
 // they made the kernel spill under its 128-register budget.
-template <int HD, int G>
+// PAIRED (128-dim heads): the two 8-position score tiles of a chunk share each
+// round of q fragments and run as two independent product chains (the int8
+// build keeps one tile at a time: with both it spilled).
+template <int HD, int G, bool PAIRED>
 __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
                                                bool has_cur, bool ab, const uint32_t* qf) {
-    static_assert(mk_attn_tc(HD, G), "tensor-core attention: 4 heads of 64 dims per KV group");
+    static_assert(mk_attn_tc(HD, G), "tensor-core attention: 4 heads of 64 or 128 dims per KV group");
     constexpr int NKS = HD / 16;         // 16-dim k steps of a score tile
-    constexpr int ND = HD / 8;           // 8-dim tiles of O
-    constexpr int NMG = Attn<HD, G>::NMG;
-    static_assert(NMG == MK_NCW, "one parked group per consumer warp");
+    constexpr int DS = mk_attn_tc_split(HD);   // warps sharing a chunk, each carrying HD / DS dims of O
+    constexpr int NWP = MK_NCW / DS;     // chunk streams (warp sets) = parked groups
+    constexpr int DW = HD / DS;          // dims of O per warp
+    constexpr int ND = DW / 8;           // 8-dim tiles of O per warp
+    constexpr int NMG = mk_attn_tc_groups(HD);
+    static_assert(NMG == NWP && NMG * G * HD <= 8 * MK_NCT, "parked groups fit the xv scratch");
     const MkGeom& g = p.geo;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
-    static_assert(NKS == 4, "two 16-byte fragment loads per lane");
+    const int dh = DS == 1 ? 0 : w / NWP, wi = DS == 1 ? w : w % NWP;   // this warp's dims of O, its chunk stream
     const bool lo = lane >= 16;          // this lane's rows hold the remainder parts (4-7)
     const int qd = 2 * (lane & 3);       // first of this lane's two k (or n) indices in a tile
     const uint32_t qfa = smem_u32(qf + qfrag_word(0, lane));
@@ -1228,7 +1243,7 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
     const int nblk = (nring + g.KB - 1) / g.KB;
     const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
     if (t == 0 && nblk > 1) *(volatile int*)&s.misc()->streaming = 1;
-    int cbase = 0;                       // chunks of the earlier blocks (warp w takes chunk indices = w mod NCW)
+    int cbase = 0;                       // chunks of the earlier blocks (stream wi takes chunk indices = wi mod NWP)
     for (int b = 0; b < nbt && !ab; ++b) {
         const int q0 = ka + b * g.KB;
         const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
@@ -1251,34 +1266,93 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
                 return zaddr;
             };
             const int nch = (n + 15) >> 4;
-            int ci = w - cbase % MK_NCW;
-            if (ci < 0) ci += MK_NCW;
-            for (; ci < nch; ci += MK_NCW) {
+            int ci = wi - cbase % NWP;
+            if (ci < 0) ci += NWP;
+            for (; ci < nch; ci += NWP) {
                 const int c0 = 16 * ci;
-                // scores of the chunk's two 8-position tiles
+                // scores of the chunk's two 8-position tiles (over all HD dims:
+                // the DS warps of a chunk compute the same scores)
                 float sv[2][2];
+                if constexpr (HD == 64) {
 #pragma unroll
-                for (int tt = 0; tt < 2; ++tt) {
-                    const int i = c0 + 8 * tt + (lane & 7);
-                    // A fragments of [q_hi; q_lo] for the 16-dim k steps (volatile: re-read per tile)
-                    uint32_t qa[NKS][2];
-                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1]) : "r"(qfa));
-                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(qa[2][0]), "=r"(qa[2][1]), "=r"(qa[3][0]), "=r"(qa[3][1]) : "r"(qfa + 512u));
-                    uint32_t kb[NKS / 2][4];   // 8x8 matrices of chunks 4x .. 4x+3: two k steps each
+                    for (int tt = 0; tt < 2; ++tt) {
+                        const int i = c0 + 8 * tt + (lane & 7);
+                        // A fragments of [q_hi; q_lo] (volatile: re-read per tile)
+                        uint32_t qa[NKS][2];
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1]) : "r"(qfa));
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(qa[2][0]), "=r"(qa[2][1]), "=r"(qa[3][0]), "=r"(qa[3][1]) : "r"(qfa + 512u));
+                        uint32_t kb[NKS / 2][4];   // 8x8 matrices of chunks 4x .. 4x+3: two k steps each
 #pragma unroll
-                    for (int x = 0; x < NKS / 2; ++x) ldsm_x4(kb[x], row(ka_, 0u, i, 4 * x + (lane >> 3)));
-                    float c0_ = 0.f, c1_ = 0.f;
+                        for (int x = 0; x < NKS / 2; ++x) ldsm_x4(kb[x], row(ka_, 0u, i, 4 * x + (lane >> 3)));
+                        float c0_ = 0.f, c1_ = 0.f;
 #pragma unroll
-                    for (int ks = 0; ks < NKS; ++ks)
-                        mma_rows8(c0_, c1_, qa[ks][0], qa[ks][1], kb[ks >> 1][2 * (ks & 1)], kb[ks >> 1][2 * (ks & 1) + 1]);
-                    // high part + remainder: lanes 16 apart hold the same head and positions
-                    c0_ += __shfl_xor_sync(0xFFFFFFFFu, c0_, 16);
-                    c1_ += __shfl_xor_sync(0xFFFFFFFFu, c1_, 16);
-                    const int pi = c0 + 8 * tt + qd;
-                    sv[tt][0] = pi < n ? c0_ : -INFINITY;
-                    sv[tt][1] = pi + 1 < n ? c1_ : -INFINITY;
+                        for (int ks = 0; ks < NKS; ++ks)
+                            mma_rows8(c0_, c1_, qa[ks][0], qa[ks][1], kb[ks >> 1][2 * (ks & 1)], kb[ks >> 1][2 * (ks & 1) + 1]);
+                        // high part + remainder: lanes 16 apart hold the same head and positions
+                        c0_ += __shfl_xor_sync(0xFFFFFFFFu, c0_, 16);
+                        c1_ += __shfl_xor_sync(0xFFFFFFFFu, c1_, 16);
+                        const int pi = c0 + 8 * tt + qd;
+                        sv[tt][0] = pi < n ? c0_ : -INFINITY;
+                        sv[tt][1] = pi + 1 < n ? c1_ : -INFINITY;
+                    }
+                } else if constexpr (PAIRED) {
+                    // both 8-position tiles at once, two k steps (32 dims) per
+                    // round: the q fragments of a round serve both tiles, whose
+                    // products form two independent chains; the rounds are not
+                    // unrolled (the fragments of all eight k steps at once spilled)
+                    float c[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+                    const int i = c0 + (lane & 7);
+#pragma unroll 1
+                    for (int kp = 0; kp < NKS / 2; ++kp) {
+                        uint32_t qa[2][2];
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1])
+                                     : "r"(qfa + 512u * kp));
+#pragma unroll
+                        for (int tt = 0; tt < 2; ++tt) {
+                            uint32_t kb[4];   // the tile's 8x8 matrices of chunks 4kp .. 4kp+3
+                            ldsm_x4(kb, row(ka_, 0u, i + 8 * tt, 4 * kp + (lane >> 3)));
+                            mma_rows8(c[tt][0], c[tt][1], qa[0][0], qa[0][1], kb[0], kb[1]);
+                            mma_rows8(c[tt][0], c[tt][1], qa[1][0], qa[1][1], kb[2], kb[3]);
+                        }
+                    }
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt) {
+                        // high part + remainder: lanes 16 apart hold the same head and positions
+                        const float c0_ = c[tt][0] + __shfl_xor_sync(0xFFFFFFFFu, c[tt][0], 16);
+                        const float c1_ = c[tt][1] + __shfl_xor_sync(0xFFFFFFFFu, c[tt][1], 16);
+                        const int pi = c0 + 8 * tt + qd;
+                        sv[tt][0] = pi < n ? c0_ : -INFINITY;
+                        sv[tt][1] = pi + 1 < n ? c1_ : -INFINITY;
+                    }
+                } else {
+                    // one tile at a time, two k steps (32 dims) per round, the
+                    // rounds not unrolled (the fragments of all eight k steps at
+                    // once spilled)
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt) {
+                        const int i = c0 + 8 * tt + (lane & 7);
+                        float c0_ = 0.f, c1_ = 0.f;
+#pragma unroll 1
+                        for (int kp = 0; kp < NKS / 2; ++kp) {
+                            uint32_t qa[2][2];
+                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1])
+                                         : "r"(qfa + 512u * kp));
+                            uint32_t kb[4];   // 8x8 matrices of chunks 4kp .. 4kp+3
+                            ldsm_x4(kb, row(ka_, 0u, i, 4 * kp + (lane >> 3)));
+                            mma_rows8(c0_, c1_, qa[0][0], qa[0][1], kb[0], kb[1]);
+                            mma_rows8(c0_, c1_, qa[1][0], qa[1][1], kb[2], kb[3]);
+                        }
+                        // high part + remainder: lanes 16 apart hold the same head and positions
+                        c0_ += __shfl_xor_sync(0xFFFFFFFFu, c0_, 16);
+                        c1_ += __shfl_xor_sync(0xFFFFFFFFu, c1_, 16);
+                        const int pi = c0 + 8 * tt + qd;
+                        sv[tt][0] = pi < n ? c0_ : -INFINITY;
+                        sv[tt][1] = pi + 1 < n ? c1_ : -INFINITY;
+                    }
                 }
                 // online softmax per head (row): the quad of lanes sharing a row agrees on the maximum
                 float cm = fmaxf(fmaxf(m, fmaxf(sv[0][0], sv[0][1])), fmaxf(sv[1][0], sv[1][1]));
@@ -1292,12 +1366,14 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
 #pragma unroll
                 for (int j = 0; j < ND; ++j) { o[j][0] *= corr; o[j][1] *= corr; }
                 const uint32_t pa0 = split_bf2(p00, p01, lo), pa2 = split_bf2(p10, p11, lo);
-                // O += P V: V^T fragments of d tiles 2jj, 2jj+1 (rows c0.. and c0+8..)
+                // O += P V over this warp's dims: V^T fragments of d tiles
+                // ND dh + 2jj, ND dh + 2jj + 1 (rows c0.. and c0+8..)
 #pragma unroll
                 for (int jj = 0; jj < ND / 2; ++jj) {
                     const int mt = lane >> 3;
                     uint32_t vb[4];
-                    ldsm_x4_trans(vb, row(va_, (uint32_t)(HD * 2), c0 + 8 * (mt & 1) + (lane & 7), 2 * jj + (mt >> 1)));
+                    ldsm_x4_trans(vb, row(va_, (uint32_t)(HD * 2), c0 + 8 * (mt & 1) + (lane & 7),
+                                          ND * dh + 2 * jj + (mt >> 1)));
                     mma_rows8(o[2 * jj][0], o[2 * jj][1], pa0, pa2, vb[0], vb[1]);
                     mma_rows8(o[2 * jj + 1][0], o[2 * jj + 1][1], pa0, pa2, vb[2], vb[3]);
                 }
@@ -1311,7 +1387,8 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
     if (t == 0 && nblk > 1) *(volatile int*)&s.misc()->streaming = 0;
     MK_TRACE_D(l, 2);
     // the warp's state: l summed over the quad, O rows h and h+4 added; park
-    // (m, l) per head in sc and O in xv[warp] like the lane-parallel version
+    // (m, l) per head in sc and O (this warp's dims) in xv[wi] like the
+    // lane-parallel version (the DS warps of a stream hold the same m and l)
     lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
     lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
 #pragma unroll
@@ -1321,10 +1398,10 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
     }
     if (!ab && !lo) {
         const int h = lane >> 2;
-        float* xp = s.xv() + w * (G * HD) + h * HD + qd;
+        float* xp = s.xv() + wi * (G * HD) + h * HD + DW * dh + qd;
 #pragma unroll
         for (int j = 0; j < ND; ++j) *reinterpret_cast<float2*>(xp + 8 * j) = make_float2(o[j][0], o[j][1]);
-        if ((lane & 3) == 0) { s.sc()[w * G + h] = m; s.sc()[NMG * G + w * G + h] = lsum; }
+        if ((lane & 3) == 0 && dh == 0) { s.sc()[wi * G + h] = m; s.sc()[NMG * G + wi * G + h] = lsum; }
     }
     return ab;
 }
@@ -1333,7 +1410,7 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
 // thread's q dims (tagged words), the block loop (online softmax), the merge
 // of the position groups sharing a warp and the parking of the warps' groups
 // in smem for the partial.  Returns the uniform abort flag (one barrier).
-template <int HD, int G, int HPL, bool TC>
+template <int HD, int G, int HPL, bool TC, bool PAIRED>
 __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
                                          bool has_cur, bool ab) {
     bool late = false;
@@ -1401,7 +1478,7 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
     }
     ab = bar_or(ab || late);
     MK_TRACE_D(l, 0);   // q in shared memory
-    if constexpr (TC) return attn_tc_blocks<HD, G>(p, s, ring, l, ka, ke, has_cur, ab, qf);
+    if constexpr (TC) return attn_tc_blocks<HD, G, PAIRED>(p, s, ring, l, ka, ke, has_cur, ab, qf);
     const uint32_t qsa = smem_u32(qs + (hg_ * HPL) * HD + dc_ * 8);   // this thread's q dims (pre-scaled)
     float m_[HPL], l_[HPL];
     float2 acc[HPL][4];
@@ -1479,7 +1556,7 @@ __device__ __forceinline__ float mk_gumbel(uint64_t seed, int pos, int v) {
 template <int HD, int G, int MH, int LC, int WB>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
     static_assert(G <= MK_NCW, "one consumer warp per query head of a KV group (softmax, combine weights)");
-    static_assert(!LC || mk_attn_tc(HD, G), "the long-context build's attention runs on 4 heads of 64 dims");
+    static_assert(!LC || mk_attn_tc(HD, G), "the long-context build's attention runs on 4 heads of 64 or 128 dims");
     // generation already stopped (an earlier launch sampled the stop token):
     // every CTA returns before touching any state
     if (p.stop && *(volatile int32_t*)p.stop) return;
@@ -1626,13 +1703,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             // last block, or runs it as a block of its own when it has no past.
             // (att is the same for the whole CTA: the barriers inside stay uniform.)
             if (ldv(s.misc()->att))
-                ab = attn_run<HD, G, 1, LC != 0>(p, s, ring, l, ldv(s.misc()->ka), ldv(s.misc()->ke),
+                ab = attn_run<HD, G, 1, LC != 0, WB == 2>(p, s, ring, l, ldv(s.misc()->ka), ldv(s.misc()->ke),
                                                  ldv(s.misc()->has_cur) != 0, ab);
         }
         ab = bar_or(ab);
         constexpr int PSTR = G * HD + 2 * G;                   // tagged words per partial
         if (ldv(s.misc()->att) && !ab && !(p.dbg_skip_sync == 4 * l + 1 && p.dbg_skip_cta == c)) {
-            constexpr int PPP = Attn<HD, G>::NMG;               // parked groups (the same for both lane layouts)
+            constexpr int PPP = LC ? mk_attn_tc_groups(HD) : Attn<HD, G>::NMG;   // parked groups
             uint64_t* dst = p.partll + (((size_t)l * g.kvh + pl.g) * g.CPG + pl.i) * PSTR;
             for (int i = t; i < G * HD; i += MK_NCT) {
                 const int h = i / HD;

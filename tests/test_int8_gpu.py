@@ -238,8 +238,13 @@ def test_wide_int8_both_attention_builds(prefill, build):
     dec.close()
 
 
-def test_hd128_int8():
+@pytest.mark.parametrize("build", [1, 2])
+def test_hd128_int8(build):
+    """The 8B layer width and head layout on the int8 stream, both attention
+    builds (1: lane-parallel, 2: tensor cores) over 300 pre-filled positions."""
     m, q8, dec, orc = make_q8(WIDE_HD128, 41, 512)
+    assert dec.info.attn_tc == 1
+    dec.set_debug(mk.MK_DBG_ATTN_BUILD, build)
     ks, vs = synth.make_kv(WIDE_HD128, 300, 43)
     dec.set_kv(ks, vs, 300)
     orc.set_kv(ks, vs, 300)

@@ -147,8 +147,8 @@ def test_attention_split_forced(grid, prefill, ctas, build):
 def test_attention_split_grows_with_context():
     """By default a step at context ctx runs its attention on
     ceil(ctx / attn_pos_per_cta) CTAs per KV group: with 7 positions per CTA
-    the count grows from 1 to 6 inside one run from position 0 (the
-    tensor-core build) and from 1 to 3 on the hd=128 shape (lane-parallel)."""
+    the count grows from 1 to 6 inside one run from position 0, and from 1 to
+    3 on the hd=128 shape (both on the tensor-core build)."""
     m, dec, orc = make(MID, 89, 256, gains="normal", std=0.04, tuning=mk.tuning(grid_ctas=14))
     assert dec.info.attn_pos_per_cta > 0
     dec.set_debug(mk.MK_DBG_ATTN_POS_PER_CTA, 7)
@@ -194,15 +194,18 @@ def test_kv_rows_round_trip_long_context():
     dec.close()
 
 
-@pytest.mark.parametrize("grid", [0, 6])
-def test_head_dim_128_shape(grid):
-    """hd=128, G=4 (the 8B head layout, lane-parallel attention on plain rows):
-    200 pre-filled positions spread over the full grid and over 3 CTAs per KV
-    group (two 128-row blocks per CTA)."""
+@pytest.mark.parametrize("grid,build", [(0, 1), (0, 2), (6, 1), (6, 2)])
+def test_head_dim_128_shape(grid, build):
+    """hd=128, G=4 (the 8B head layout, chunk-permuted cache rows), both
+    attention builds (1: lane-parallel, 2: tensor cores, four warps per
+    16-position chunk with 32 dims of O each): 200 pre-filled positions spread
+    over the full grid and over 3 CTAs per KV group (two 128-row blocks per
+    CTA)."""
     s = synth.ModelShape(2, 1024, 8, 2, 128, 1536, 4099, 1e-5, 500000.0, False)
     tun = mk.tuning(grid_ctas=grid) if grid else None
     m, dec, orc = make(s, 31, 512, gains="normal", std=0.03, tuning=tun)
-    assert dec.info.attn_tc == 0
+    assert dec.info.attn_tc == 1
+    dec.set_debug(mk.MK_DBG_ATTN_BUILD, build)
     ks, vs = synth.make_kv(s, 200, 37)
     dec.set_kv(ks, vs, 200)
     orc.set_kv(ks, vs, 200)

@@ -143,7 +143,7 @@ def test_prefill_8b_width():
 
 
 def test_prefill_head_dim_128():
-    """hd=128 (the 8B head layout, plain cache rows) with 100 pre-filled positions."""
+    """hd=128 (the 8B head layout, chunk-permuted cache rows) with 100 pre-filled positions."""
     m = synth.make_model(HD128, 107, std=0.03, gains="normal")
     dec, orc = Decoder(m, 512, perop=True), oracle.OracleDecoder(m, 512)
     ks, vs = synth.make_kv(HD128, 100, 109)
