@@ -1202,6 +1202,13 @@ __device__ __forceinline__ uint32_t split_bf2(float x, float y, bool lo) {
 // warps park.
 __host__ __device__ constexpr int mk_attn_tc_split(int hd) { return hd == 128 ? 4 : 1; }
 __host__ __device__ constexpr int mk_attn_tc_groups(int hd) { return MK_NCW / mk_attn_tc_split(hd); }
+// Barrier of the DS warps of chunk stream wi (named barriers 2, 3, 4; the
+// consumers' barrier is 1).
+__device__ __forceinline__ void stream_sync(int wi) {
+    if (wi == 0) asm volatile("bar.sync 2, 128;" ::: "memory");
+    else if (wi == 1) asm volatile("bar.sync 3, 128;" ::: "memory");
+    else asm volatile("bar.sync 4, 128;" ::: "memory");
+}
 __device__ __forceinline__ int qfrag_word(int f, int lane) { return (f >> 2) * 128 + 4 * lane + (f & 3); }
 
 // The block loop of the tensor-core attention (q of the group's heads already
@@ -1212,10 +1219,7 @@ __device__ __forceinline__ int qfrag_word(int f, int lane) { return (f >> 2) * 1
 // parked for the caller.  The fragments are read back from shared memory for
 // every 16-position chunk rather than held in registers across the loop: held,
 // they made the kernel spill under its 128-register budget.
-// PAIRED (128-dim heads): the two 8-position score tiles of a chunk share each
-// round of q fragments and run as two independent product chains (the int8
-// build keeps one tile at a time: with both it spilled).
-template <int HD, int G, bool PAIRED>
+template <int HD, int G>
 __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
                                                bool has_cur, bool ab, const uint32_t* qf) {
     static_assert(mk_attn_tc(HD, G), "tensor-core attention: 4 heads of 64 or 128 dims per KV group");
@@ -1225,7 +1229,9 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
     constexpr int DW = HD / DS;          // dims of O per warp
     constexpr int ND = DW / 8;           // 8-dim tiles of O per warp
     constexpr int NMG = mk_attn_tc_groups(HD);
-    static_assert(NMG == NWP && NMG * G * HD <= 8 * MK_NCT, "parked groups fit the xv scratch");
+    static_assert(NMG == NWP && NMG * G * HD + (DS > 1 ? 2 * NWP * DS * 64 : 0) <= 8 * MK_NCT,
+                  "parked groups and the score exchange fit the xv scratch");
+    static_assert(DS == 1 || (DS * 32 == 128 && NWP == 3), "named barriers of 128 threads, one per stream");
     const MkGeom& g = p.geo;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     const int dh = DS == 1 ? 0 : w / NWP, wi = DS == 1 ? w : w % NWP;   // this warp's dims of O, its chunk stream
@@ -1244,6 +1250,7 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
     const int nbt = (nblk == 0 && has_cur) ? 1 : nblk;
     if (t == 0 && nblk > 1) *(volatile int*)&s.misc()->streaming = 1;
     int cbase = 0;                       // chunks of the earlier blocks (stream wi takes chunk indices = wi mod NWP)
+    uint32_t rnd = 0;                    // 128 dims: chunk rounds of this stream (the score exchange's buffer)
     for (int b = 0; b < nbt && !ab; ++b) {
         const int q0 = ka + b * g.KB;
         const int nr = (b < nblk) ? min(g.KB, ke - q0) : 0;
@@ -1255,6 +1262,9 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
             rv.advance(g.ns);            // the V tile follows the K tile in the stream
             ok = take_landed(p, s, ring, (uint32_t)(nr * HD * 2), kt) && take_landed(p, s, rv, (uint32_t)(nr * HD * 2), vt);
         }
+        // 128 dims: the warps of a stream meet at a named barrier, which has no
+        // time limit, so they all run a block's chunks or none of them
+        if constexpr (DS > 1) ok = !bar_or(!ok);
         if (b == 0) MK_TRACE_D(l, 5);
         if (ok) {
             const uint32_t ka_ = kt ? smem_u32(kt) : 0u, va_ = vt ? smem_u32(vt) : 0u;
@@ -1297,62 +1307,46 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
                         sv[tt][0] = pi < n ? c0_ : -INFINITY;
                         sv[tt][1] = pi + 1 < n ? c1_ : -INFINITY;
                     }
-                } else if constexpr (PAIRED) {
-                    // both 8-position tiles at once, two k steps (32 dims) per
-                    // round: the q fragments of a round serve both tiles, whose
-                    // products form two independent chains; the rounds are not
-                    // unrolled (the fragments of all eight k steps at once spilled)
-                    float c[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-                    const int i = c0 + (lane & 7);
-#pragma unroll 1
-                    for (int kp = 0; kp < NKS / 2; ++kp) {
-                        uint32_t qa[2][2];
-                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1])
-                                     : "r"(qfa + 512u * kp));
-#pragma unroll
-                        for (int tt = 0; tt < 2; ++tt) {
-                            uint32_t kb[4];   // the tile's 8x8 matrices of chunks 4kp .. 4kp+3
-                            ldsm_x4(kb, row(ka_, 0u, i + 8 * tt, 4 * kp + (lane >> 3)));
-                            mma_rows8(c[tt][0], c[tt][1], qa[0][0], qa[0][1], kb[0], kb[1]);
-                            mma_rows8(c[tt][0], c[tt][1], qa[1][0], qa[1][1], kb[2], kb[3]);
-                        }
-                    }
-#pragma unroll
-                    for (int tt = 0; tt < 2; ++tt) {
-                        // high part + remainder: lanes 16 apart hold the same head and positions
-                        const float c0_ = c[tt][0] + __shfl_xor_sync(0xFFFFFFFFu, c[tt][0], 16);
-                        const float c1_ = c[tt][1] + __shfl_xor_sync(0xFFFFFFFFu, c[tt][1], 16);
-                        const int pi = c0 + 8 * tt + qd;
-                        sv[tt][0] = pi < n ? c0_ : -INFINITY;
-                        sv[tt][1] = pi + 1 < n ? c1_ : -INFINITY;
-                    }
                 } else {
-                    // one tile at a time, two k steps (32 dims) per round, the
-                    // rounds not unrolled (the fragments of all eight k steps at
-                    // once spilled)
+                    // 128 dims: the DS warps of a stream split the scores' k
+                    // steps (warp dh takes dims 32 dh .. 32 dh + 31), leave their
+                    // partial scores in shared memory (double-buffered by round),
+                    // meet at the stream's named barrier and add the DS partials
+                    // in the same order, so all of them hold the same scores (and
+                    // so the same m, l and P)
+                    float c[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+                    uint32_t qa[2][2];
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1])
+                                 : "r"(qfa + 512u * dh));
 #pragma unroll
                     for (int tt = 0; tt < 2; ++tt) {
-                        const int i = c0 + 8 * tt + (lane & 7);
-                        float c0_ = 0.f, c1_ = 0.f;
-#pragma unroll 1
-                        for (int kp = 0; kp < NKS / 2; ++kp) {
-                            uint32_t qa[2][2];
-                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                         : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1])
-                                         : "r"(qfa + 512u * kp));
-                            uint32_t kb[4];   // 8x8 matrices of chunks 4kp .. 4kp+3
-                            ldsm_x4(kb, row(ka_, 0u, i, 4 * kp + (lane >> 3)));
-                            mma_rows8(c0_, c1_, qa[0][0], qa[0][1], kb[0], kb[1]);
-                            mma_rows8(c0_, c1_, qa[1][0], qa[1][1], kb[2], kb[3]);
-                        }
-                        // high part + remainder: lanes 16 apart hold the same head and positions
-                        c0_ += __shfl_xor_sync(0xFFFFFFFFu, c0_, 16);
-                        c1_ += __shfl_xor_sync(0xFFFFFFFFu, c1_, 16);
-                        const int pi = c0 + 8 * tt + qd;
-                        sv[tt][0] = pi < n ? c0_ : -INFINITY;
-                        sv[tt][1] = pi + 1 < n ? c1_ : -INFINITY;
+                        uint32_t kb[4];   // the tile's 8x8 matrices of chunks 4dh .. 4dh+3
+                        ldsm_x4(kb, row(ka_, 0u, c0 + 8 * tt + (lane & 7), 4 * dh + (lane >> 3)));
+                        mma_rows8(c[tt][0], c[tt][1], qa[0][0], qa[0][1], kb[0], kb[1]);
+                        mma_rows8(c[tt][0], c[tt][1], qa[1][0], qa[1][1], kb[2], kb[3]);
                     }
+                    // high part + remainder: lanes 16 apart hold the same head and positions
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt) {
+                        c[tt][0] += __shfl_xor_sync(0xFFFFFFFFu, c[tt][0], 16);
+                        c[tt][1] += __shfl_xor_sync(0xFFFFFFFFu, c[tt][1], 16);
+                    }
+                    float4* xb = reinterpret_cast<float4*>(s.xv() + NMG * G * HD) + ((rnd & 1) * NWP + wi) * (DS * 16);
+                    ++rnd;
+                    if (lane < 16) xb[dh * 16 + lane] = make_float4(c[0][0], c[0][1], c[1][0], c[1][1]);
+                    stream_sync(wi);
+                    float4 sc4 = xb[lane & 15];
+#pragma unroll
+                    for (int q = 1; q < DS; ++q) {
+                        const float4 v = xb[q * 16 + (lane & 15)];
+                        sc4.x += v.x; sc4.y += v.y; sc4.z += v.z; sc4.w += v.w;
+                    }
+                    const int pi = c0 + qd;
+                    sv[0][0] = pi < n ? sc4.x : -INFINITY;
+                    sv[0][1] = pi + 1 < n ? sc4.y : -INFINITY;
+                    sv[1][0] = pi + 8 < n ? sc4.z : -INFINITY;
+                    sv[1][1] = pi + 9 < n ? sc4.w : -INFINITY;
                 }
                 // online softmax per head (row): the quad of lanes sharing a row agrees on the maximum
                 float cm = fmaxf(fmaxf(m, fmaxf(sv[0][0], sv[0][1])), fmaxf(sv[1][0], sv[1][1]));
@@ -1410,7 +1404,7 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
 // thread's q dims (tagged words), the block loop (online softmax), the merge
 // of the position groups sharing a warp and the parking of the warps' groups
 // in smem for the partial.  Returns the uniform abort flag (one barrier).
-template <int HD, int G, int HPL, bool TC, bool PAIRED>
+template <int HD, int G, int HPL, bool TC>
 __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring& ring, int l, int ka, int ke,
                                          bool has_cur, bool ab) {
     bool late = false;
@@ -1478,7 +1472,7 @@ __device__ __forceinline__ bool attn_run(const MkParams& p, const Smem& s, Ring&
     }
     ab = bar_or(ab || late);
     MK_TRACE_D(l, 0);   // q in shared memory
-    if constexpr (TC) return attn_tc_blocks<HD, G, PAIRED>(p, s, ring, l, ka, ke, has_cur, ab, qf);
+    if constexpr (TC) return attn_tc_blocks<HD, G>(p, s, ring, l, ka, ke, has_cur, ab, qf);
     const uint32_t qsa = smem_u32(qs + (hg_ * HPL) * HD + dc_ * 8);   // this thread's q dims (pre-scaled)
     float m_[HPL], l_[HPL];
     float2 acc[HPL][4];
@@ -1703,7 +1697,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             // last block, or runs it as a block of its own when it has no past.
             // (att is the same for the whole CTA: the barriers inside stay uniform.)
             if (ldv(s.misc()->att))
-                ab = attn_run<HD, G, 1, LC != 0, WB == 2>(p, s, ring, l, ldv(s.misc()->ka), ldv(s.misc()->ke),
+                ab = attn_run<HD, G, 1, LC != 0>(p, s, ring, l, ldv(s.misc()->ka), ldv(s.misc()->ke),
                                                  ldv(s.misc()->has_cur) != 0, ab);
         }
         ab = bar_or(ab);
