@@ -31,7 +31,7 @@ LC_VARIANTS = [(64, 4, 2), (64, 4, 8), (128, 4, 4), (128, 4, 16)]
 # weight-only INT8 builds (-DMK_WB_V=1) of the standard and long-context kernels; keep in sync
 # with MK_Q8_VARIANTS and MK_Q8_LC_VARIANTS in csrc/mk_api.cu
 Q8_VARIANTS = [(64, 2, 1), (64, 4, 8), (128, 4, 16)]
-Q8_LC_VARIANTS = [(64, 4, 8), (128, 4, 16)]
+Q8_LC_VARIANTS = [(64, 4, 8)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -25,7 +25,7 @@
 // Weight-only INT8 builds (-DMK_WB_V=1; keep in sync with Q8_VARIANTS and
 // Q8_LC_VARIANTS in build.py).
 #define MK_Q8_VARIANTS(X) X(64, 2, 1) X(64, 4, 8) X(128, 4, 16)
-#define MK_Q8_LC_VARIANTS(X) X(64, 4, 8) X(128, 4, 16)
+#define MK_Q8_LC_VARIANTS(X) X(64, 4, 8)
 // Each variant exists twice: without trace code (launched normally) and with
 // it (launched while a segment trace is requested).
 #define MK_DECL(hd, g, mh)                                         \

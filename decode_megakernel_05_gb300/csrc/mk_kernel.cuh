@@ -191,6 +191,7 @@ struct Misc {                // lives at geo.off_misc (MK_MISC_BYTES)
     int token;
     int par;
     int is_last;
+    float xscale;            // int8 build: scale of the digits in xv (mk_xdigits)
     unsigned long long copy_bytes;  // bytes issued by the copy producer (paces the L2 prefetcher)
     uint32_t pf_sink;               // the L2 warmer's xor of what it loaded (keeps the loads)
     unsigned long long cwait;       // trace: ns thread 0 spent waiting for ring data
@@ -645,6 +646,38 @@ template <> struct WChunk<1> {
     }
 };
 
+// ---- int8 dot products on integers (mk_xdigits)
+//
+// In the int8 build the hidden-width activation y (the RMSNorm output that
+// QKV, gate/up and the LM head read) is held as y = X * sx with X an integer
+// of at most 22 bits plus sign, written as three signed bytes,
+// X = d2 * 2^16 + d1 * 2^8 + d0.  A row's dot product with the biased codes
+// b = q + 128 is then three exact integer sums per lane, sum b * d_k, each
+// 4 products per dp4a, less the per-lane constant 128 * sum d_k, combined in
+// fp32 and scaled by sx and the row scale.  xv holds, per group of 4
+// split-order columns (uint4 entry 4m .. 4m+3), the words of d0, d1 and d2.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {   // sum of unsigned a bytes x signed b bytes
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ float dig_combine(const int (&acc)[3], const int (&bias)[3]) {
+    return fmaf((float)(acc[2] - bias[2]), 65536.f, fmaf((float)(acc[1] - bias[1]), 256.f, (float)(acc[0] - bias[0])));
+}
+// The lane's digit words of chunk ch (4 low-half and 4 high-half columns) and
+// their share of the per-lane constant (128 * sum of the digits).
+__device__ __forceinline__ void dig_load(const uint4* xq, int K, int ch, uint32_t (&d)[6], int (&bias)[3]) {
+    const uint4 a = xq[ch], b = xq[K / 8 + ch];
+    d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = b.x; d[4] = b.y; d[5] = b.z;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) bias[k] = dp4a_us(0x80808080u, d[k + 3], dp4a_us(0x80808080u, d[k], bias[k]));
+}
+// 8 biased codes (w.x: the 4 low-half columns, w.y: the 4 high-half ones) into the three sums.
+__device__ __forceinline__ void dig_fma(const uint2 w, const uint32_t (&d)[6], int (&acc)[3]) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) acc[k] = dp4a_us(w.y, d[k + 3], dp4a_us(w.x, d[k], acc[k]));
+}
+
 // Dot products of up to 4 rows (nv valid, rows r0 + k*step) with the
 // split-order vector xs; each lane covers MR chunks of 8 columns (8 * WB bytes).
 template <int MR, int LPR, int WB = 2>
@@ -665,6 +698,26 @@ __device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t step, int nv
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) o[r] = (a[r][0].x + a[r][0].y) + (a[r][1].x + a[r][1].y);
+}
+// The same over int8 rows and the digits of the activation (xq); bias: the
+// lane's constant over its MR chunks.  o[r] is in units of the activation scale.
+template <int MR, int LPR>
+__device__ __forceinline__ void dot_rows4_dig(const uint8_t* r0, size_t step, int nv, const uint4* xq, int K, int ll,
+                                              const int (&bias)[3], float o[4]) {
+    int acc[4][3];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = acc[r][2] = 0;
+#pragma unroll (MR < 8 ? MR : 8)
+    for (int j = 0; j < MR; ++j) {
+        const int ch = j * LPR + ll;
+        const uint4 a = xq[ch], b = xq[K / 8 + ch];
+        const uint32_t d[6] = {a.x, a.y, a.z, b.x, b.y, b.z};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            if (r < nv) dig_fma(lds64(r0 + r * step + (size_t)ch * 8), d, acc[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) o[r] = dig_combine(acc[r], bias);
 }
 
 // GEMV over one phase's tiles (rows of K = MR * 8 * LPR columns, LPR lanes per
@@ -691,10 +744,13 @@ __device__ void gemv_cfg(GemvCfg& c, int nrows, int TR, int RPP) {
 
 // WB = 1: int8 rows, each row's sum times the row's scale from the tile's
 // tail before epi() gets it.
-template <int MR, int LPR, int WB, class Epi>
+// DIG (int8 rows only): vec holds the activation's digits (mk_xdigits), and
+// each row's sum is also scaled by s.misc()->xscale.
+template <int MR, int LPR, int WB, bool DIG = false, class Epi>
 __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec,
                                              int nrows, int TR, const GemvCfg& cfg, bool ab, Epi&& epi,
                                              int trace_slot = -1, int dl = 0, int dmark = -1) {
+    static_assert(!DIG || WB == 1, "digits are the int8 rows' activation form");
     constexpr int K = MR * 8 * LPR;
     constexpr int RPP = 32 / LPR;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -703,6 +759,17 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
     const int grp = cfg.grp[w], wg = cfg.wg[w];
     const int rows_per_warp = rw * RPP;
     const size_t rb = (size_t)K * WB;
+    int bias[3] = {0, 0, 0};
+    float xsc = 1.f;
+    if constexpr (DIG) {
+        const uint4* xq = reinterpret_cast<const uint4*>(vec);
+#pragma unroll (MR < 8 ? MR : 8)
+        for (int j = 0; j < MR; ++j) {
+            uint32_t d[6];
+            dig_load(xq, K, j * LPR + ll, d, bias);
+        }
+        xsc = s.misc()->xscale;
+    }
     int turn = 0;   // ti mod ngrp
     for (int ti = 0; ti < ntiles && !ab; ++ti) {
         const bool mine = turn == grp;
@@ -720,7 +787,13 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                 const int r0 = base + sub;
                 const int nv = r0 < R ? min(rw, (R - r0 + RPP - 1) / RPP) : 0;
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
-                if (nv > 0) dot_rows4<MR, LPR, WB>(tile + r0 * rb, rb * RPP, nv, vec, K, ll, v);
+                if constexpr (DIG) {
+                    if (nv > 0)
+                        dot_rows4_dig<MR, LPR>(tile + r0 * rb, rb * RPP, nv, reinterpret_cast<const uint4*>(vec), K, ll,
+                                               bias, v);
+                } else {
+                    if (nv > 0) dot_rows4<MR, LPR, WB>(tile + r0 * rb, rb * RPP, nv, vec, K, ll, v);
+                }
                 if (dmark >= 0 && ti == 0 && base == 0) {   // detail trace: the first pass's dot products done
                     float z = v[0] + v[1] + v[2] + v[3];
                     asm volatile("" : "+f"(z));
@@ -738,7 +811,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                     const float* scl = reinterpret_cast<const float*>(tile + (size_t)R * K);   // int8: row scales
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        if (k < nv) epi(ti * TR + r0 + k * RPP, WB == 1 ? v[k] * scl[r0 + k * RPP] : v[k]);
+                        if (k < nv) epi(ti * TR + r0 + k * RPP, WB == 1 ? v[k] * (scl[r0 + k * RPP] * xsc) : v[k]);
                 }
                 if (dmark >= 0 && ti == 0 && base == 0) MK_TRACE_D(dl, 14);   // its sums handed to epi
             }
@@ -796,13 +869,23 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = w / WPG, wg = w % WPG;
     const int cb = wg % NKB, rs = wg / NKB;
-    float4 xl[CPL], xh[CPL];
+    // the lane's activations for the whole phase: fp32 (bf16 rows), or the
+    // digits and the lane's constant (int8 rows, mk_xdigits)
+    float4 xl[WB == 2 ? CPL : 1], xh[WB == 2 ? CPL : 1];
+    uint32_t xd[WB == 1 ? CPL : 1][6];
+    int bias[3] = {0, 0, 0};
+    float xsc = 1.f;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
         const int ch = (cb * CPL + j) * 32 + lane;
-        xl[j] = reinterpret_cast<const float4*>(xs)[ch];
-        xh[j] = reinterpret_cast<const float4*>(xs + K / 2)[ch];
+        if constexpr (WB == 2) {
+            xl[j] = reinterpret_cast<const float4*>(xs)[ch];
+            xh[j] = reinterpret_cast<const float4*>(xs + K / 2)[ch];
+        } else {
+            dig_load(reinterpret_cast<const uint4*>(xs), K, ch, xd[j], bias);
+        }
     }
+    if constexpr (WB == 1) xsc = s.misc()->xscale;
     const int ntiles = (nrows + TR - 1) / TR;
     for (int ti = 0; ti < ntiles && !ab; ++ti) {
         if (NG > 1 && (ti % NG) != grp) { ring.advance(p.geo.ns); continue; }   // another group's tile
@@ -824,7 +907,7 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
 #pragma unroll
             for (int pb = 0; pb < NPS; ++pb) {
                 const int rr = 4 * pb + (lane >> 3);
-                scl[pb] = rr < nrow ? sc[r0 + rr * NRS] : 0.f;
+                scl[pb] = rr < nrow ? sc[r0 + rr * NRS] * xsc : 0.f;
             }
         }
         // rows qb .. qb+3 of the share: dot products, transposed butterfly (lane
@@ -832,17 +915,30 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
         // finish the sum) and the column-block partials into `part`
         auto pass = [&](int qb, auto&& chunk) {
             const int nv = min(4, nrow - qb);
-            float2 a[4][2];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) a[q][0] = a[q][1] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < CPL; ++j)
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (qb + q < nrow) C::fma(chunk(qb + q, j), xl[j], xh[j], a[q][0], a[q][1]);
             float v[4];
+            if constexpr (WB == 2) {
+                float2 a[4][2];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = (a[q][0].x + a[q][0].y) + (a[q][1].x + a[q][1].y);
+                for (int q = 0; q < 4; ++q) a[q][0] = a[q][1] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (qb + q < nrow) C::fma(chunk(qb + q, j), xl[j], xh[j], a[q][0], a[q][1]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = (a[q][0].x + a[q][0].y) + (a[q][1].x + a[q][1].y);
+            } else {
+                int acc[4][3];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = acc[q][2] = 0;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (qb + q < nrow) dig_fma(chunk(qb + q, j), xd[j], acc[q]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[q] = dig_combine(acc[q], bias);   // rows past nrow: not stored
+            }
             const bool up = lane & 16, b3 = lane & 8;
             float k0 = up ? v[2] : v[0], k1 = up ? v[3] : v[1];
             k0 += __shfl_xor_sync(0xFFFFFFFFu, up ? v[0] : v[2], 16);
@@ -947,6 +1043,99 @@ __device__ bool rmsnorm_to_xv(const MkParams& p, const Smem& s, const float* x, 
         const int i = t + k * MK_NCT;
         if (i < H) s.xv()[xsplit(i, H)] = xr[k] * inv * gv[k];   // split order for the GEMV
     }
+    return bar_or(ab);
+}
+
+// The same norm for the int8 build's integer dot products: s.xv() receives
+// y = x * rsqrt(mean x^2 + eps) * g as digits (mk_xdigits), its scale goes to
+// s.misc()->xscale, and hid (if given) receives y itself.  A thread takes
+// groups of 8 consecutive elements: their x and g load as 16-byte vectors and
+// their digits leave as two 16-byte entries (the group's low and high split
+// halves).  sx = max |y| / (2^22 - 1), so every X = rint(y / sx) has at most 22
+// bits plus sign; a non-finite value makes sx non-finite, and the step's
+// logits with it.
+template <int NPG>   // ceil(H / 8 / consumer threads) groups per thread
+__device__ bool rmsnorm_to_dig(const MkParams& p, const Smem& s, const float* x, const uint16_t* xb, const float* g,
+                               bool abort_in, float* keep, int keep0, int nkeep, float* hid = nullptr) {
+    const int H = p.geo.H, t = threadIdx.x;
+    float xr[NPG][8], gv[NPG][8];
+#pragma unroll
+    for (int k = 0; k < NPG; ++k) {
+        const int e0 = 8 * (t + k * MK_NCT);
+        if (e0 < H) {
+            if (xb) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(xb + e0));
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f = bf2_lo_hi(ww[q]);
+                    xr[k][2 * q] = f.x; xr[k][2 * q + 1] = f.y;
+                }
+            } else {
+                const float4 a = __ldcg(reinterpret_cast<const float4*>(x + e0));
+                const float4 b = __ldcg(reinterpret_cast<const float4*>(x + e0 + 4));
+                xr[k][0] = a.x; xr[k][1] = a.y; xr[k][2] = a.z; xr[k][3] = a.w;
+                xr[k][4] = b.x; xr[k][5] = b.y; xr[k][6] = b.z; xr[k][7] = b.w;
+            }
+            const float4 c = __ldg(reinterpret_cast<const float4*>(g + e0));
+            const float4 d = __ldg(reinterpret_cast<const float4*>(g + e0 + 4));
+            gv[k][0] = c.x; gv[k][1] = c.y; gv[k][2] = c.z; gv[k][3] = c.w;
+            gv[k][4] = d.x; gv[k][5] = d.y; gv[k][6] = d.z; gv[k][7] = d.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xr[k][q] = gv[k][q] = 0.f;
+        }
+    }
+    float ss = 0.f, mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < NPG; ++k)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = 8 * (t + k * MK_NCT) + q;
+            if ((unsigned)(i - keep0) < (unsigned)nkeep) keep[i - keep0] = xr[k][q];
+            ss = fmaf(xr[k][q], xr[k][q], ss);
+            const float a = fabsf(xr[k][q] * gv[k][q]);
+            mx = (a != a) ? INFINITY : fmaxf(mx, a);   // max |x g|; NaN counts as +inf
+        }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    if ((t & 31) == 0) { s.red()[t >> 5] = ss; s.red()[MK_NCW + (t >> 5)] = mx; }
+    bool ab = bar_or(abort_in);
+    float tot = 0.f, m = 0.f;
+#pragma unroll
+    for (int w = 0; w < MK_NCW; ++w) { tot += s.red()[w]; m = fmaxf(m, s.red()[MK_NCW + w]); }
+    const float inv = rsqrtf(tot / (float)H + p.eps);
+    const float my = m * inv;
+    const float sx = my == 0.f ? 1.f : my * (1.f / 4194303.f);
+    const float isx = 1.f / sx;
+    uint4* xq = reinterpret_cast<uint4*>(s.xv());
+#pragma unroll
+    for (int k = 0; k < NPG; ++k) {
+        const int a = t + k * MK_NCT, e0 = 8 * a;
+        if (e0 < H) {
+            uint32_t w[2][3] = {{0u, 0u, 0u}, {0u, 0u, 0u}};   // [low/high half][digit]
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float y = xr[k][q] * inv * gv[k][q];
+                if (hid) hid[e0 + q] = y;
+                const int xi = __float2int_rn(y * isx);
+                const int d0 = (int)(int8_t)(xi & 0xFF);
+                const int x1 = (xi - d0) >> 8;
+                const int d1 = (int)(int8_t)(x1 & 0xFF);
+                const int d2 = (x1 - d1) >> 8;
+                const int sh = 8 * (q & 3);
+                w[q >> 2][0] |= (uint32_t)(d0 & 0xFF) << sh;
+                w[q >> 2][1] |= (uint32_t)(d1 & 0xFF) << sh;
+                w[q >> 2][2] |= (uint32_t)(d2 & 0xFF) << sh;
+            }
+            xq[a] = make_uint4(w[0][0], w[0][1], w[0][2], 0u);             // split positions 4a .. 4a+3
+            xq[H / 8 + a] = make_uint4(w[1][0], w[1][1], w[1][2], 0u);     // H/2 + 4a .. H/2 + 4a+3
+        }
+    }
+    if (t == 0) s.misc()->xscale = sx;
     return bar_or(ab);
 }
 
@@ -1652,7 +1841,11 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment A: RMSNorm + QKV GEMV + RoPE + K/V append
         MK_TRACE(16 * l + 0);
         const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
-        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres(), pl.orow0,
+        if constexpr (WB == 1)
+            ab = rmsnorm_to_dig<(MH * 32 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H,
+                                                               ab, s.xres(), pl.orow0, pl.g == 0 ? pl.norows : 0);
+        else
+            ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres(), pl.orow0,
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
         ab = gemv_fifo<MH, WB>(p, s, ring, s.xv(), 2 * pl.npairs, g.TRh, ab, s.part());
@@ -1860,8 +2053,12 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 9);
 
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
-        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2(),
-                                                             ldv(s.misc()->dr0), ldv(s.misc()->dr1) - ldv(s.misc()->dr0));
+        if constexpr (WB == 1)
+            ab = rmsnorm_to_dig<(MH * 32 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2(),
+                                                               ldv(s.misc()->dr0), ldv(s.misc()->dr1) - ldv(s.misc()->dr0));
+        else
+            ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2(),
+                                                                 ldv(s.misc()->dr0), ldv(s.misc()->dr1) - ldv(s.misc()->dr0));
         MK_TRACE(16 * l + 10);
         if (t == 0) *(volatile int*)&s.misc()->streaming = 1;   // gate/up and down stream
         if (l == 3) trace_ring(p, ring, 4);   // everything before this layer's FFN (discarded)
@@ -2022,17 +2219,21 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     // ---------------- final RMSNorm + LM head + argmax
     {
         const float* xl = xa + (size_t)(2 * L - 1) * state;
-        ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0);
+        if constexpr (WB == 1)
+            ab = rmsnorm_to_dig<(MH * 32 + MK_NCT - 1) / MK_NCT>(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0,
+                                                               c == 0 ? p.hidden : nullptr);
+        else
+            ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0);
         MK_TRACE(16 * L + 0);
         if (t == 0) *(volatile int*)&s.misc()->streaming = 1;   // the LM head streams
-        if (c == 0 && !ab)
+        if (WB == 2 && c == 0 && !ab)
             for (int i = t; i < H; i += MK_NCT) p.hidden[i] = s.xv()[xsplit(i, H)];
         float bv = -INFINITY;
         int bi = -1;
         bool nonfinite = false;
         // top-p: the logits go to scratch and the phase only finds max(logit / T)
         const bool topp = p.inv_temp > 0.f && p.top_p < 1.f;
-        ab = gemv_phase_t<MH, 32, WB>(p, s, ring, s.xv(), pl.nv, g.TRh, s.misc()->lmcfg, ab, [&](int r, float lg) {
+        ab = gemv_phase_t<MH, 32, WB, WB == 1>(p, s, ring, s.xv(), pl.nv, g.TRh, s.misc()->lmcfg, ab, [&](int r, float lg) {
             const int v = pl.v0 + r;
             if (p.logits) p.logits[v] = lg;
             if (isfinite(lg)) {

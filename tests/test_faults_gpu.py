@@ -102,3 +102,26 @@ def test_decode_before_weights_is_a_state_error():
         assert mk.load().mk_decode_step(ctx, 1, 0, None, None) == mk.MK_ERR_STATE
     finally:
         mk.mk_destroy(ctx)
+
+
+@pytest.mark.parametrize("int8", [False, True], ids=["bf16", "int8"])
+def test_nonfinite_logits_report_numeric(int8):
+    """An infinite final-norm gain makes the step's logits non-finite: the step
+    reports MK_ERR_NUMERIC (the int8 build's integer dot products carry it
+    through the activation scale), and once the gain is finite again the next
+    context decodes cleanly."""
+    w = synth.WORKLOADS["tiny"]
+    m = synth.make_model(w.shape, w.seed_weights)
+    bad = dict(m)
+    bad["final_norm"] = m["final_norm"].copy()
+    bad["final_norm"][5] = 0x7F80   # bf16 +inf
+    dec = Decoder(bad, w.max_seq(), int8=int8)
+    lg = dec.step(3, 0, logits=True)
+    assert dec.status() == mk.MK_ERR_NUMERIC
+    assert not np.isfinite(lg.cpu().numpy()).all()
+    dec.close()
+    dec = Decoder(m, w.max_seq(), int8=int8)
+    lg = dec.step(3, 0, logits=True)
+    assert dec.status() == mk.MK_OK
+    assert np.isfinite(lg.cpu().numpy()).all()
+    dec.close()
