@@ -653,42 +653,50 @@ __global__ void argmax_final_kernel(const unsigned long long* part, int n, int32
 
 // Causal attention on the tensor cores (flash style, mma.sync m16n8k16): a
 // CTA takes 16 query rows (positions start + r0 ..) and the G query heads of
-// one KV group, warp w the head g * G + w, so the group's K/V tile of 16
-// positions is loaded once (un-permuting the cache's chunk order) and read by
-// the G warps; the next tile's cp.async copies are in flight while a tile is
-// used (two buffers).  Per tile: S = q . K^T with q split into its bf16 rounding and
-// the rounding of the remainder (q . k to about 2^-17 relative), the causal
-// mask, an online softmax in base 2 (q pre-scaled by log2(e) / sqrt(hd)), P
-// split the same way, O += P . V (V read transposed by ldmatrix).  The score
-// accumulator of two 8-position tiles is, lane for lane, the A fragment of
-// P . V, so P never goes through shared memory.
-template <int HD>
+// one KV group.  Its keys are split NS ways: key set s (warps s*G .. s*G+G-1,
+// warp s*G + i on head g * G + i) takes the 16-position K/V tiles s, s + NS,
+// ..., so each tile is loaded once (un-permuting the cache's chunk order) and
+// read by the G warps of its set, the set's next tile in flight while one is
+// used (two buffers, cp.async, the set's own named barrier).  Per tile: S =
+// q . K^T with q split into its bf16 rounding and the rounding of the
+// remainder (q . k to about 2^-17 relative), the causal mask, an online
+// softmax in base 2 (q pre-scaled by log2(e) / sqrt(hd)), P split the same
+// way, O += P . V (V read transposed by ldmatrix).  The score accumulator of
+// two 8-position tiles is, lane for lane, the A fragment of P . V, so P never
+// goes through shared memory.  At the end the key sets' (m, l, O) meet in
+// shared memory and set 0 writes the rows.  (The last row block of a prompt
+// walks all of its keys; with NS = 2 that walk is half as long.)
+template <int HD, int NS>
 __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int nqkv, const uint16_t* kc,
                                                             const uint16_t* vc, int n, int start, int qh, int kvh,
                                                             int max_seq, int layer, int swz, float* out, uint16_t* P,
                                                             size_t ps) {
+    static_assert(NS == 1 || NS == 2, "one or two key sets (named barriers 1 and 2)");
     constexpr int KL = HD + 8;                 // padded smem rows: 8 ldmatrix row addresses hit 8 bank groups
     extern __shared__ __align__(16) uint16_t at_smem[];
     const int G = qh / kvh;
-    uint16_t* ks0 = at_smem;                   // [2 buffers][16][KL]
-    uint16_t* vs0 = ks0 + 2 * 16 * KL;         // [2 buffers][16][KL]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
-    uint16_t* qs = vs0 + 2 * 16 * KL + warp * (2 * 16 * KL);   // this warp's q parts [2][16][KL]
-    const int r0 = blockIdx.x * 16, grp = blockIdx.y, h = grp * G + warp;
+    const int ks_ = warp / G, hw = warp % G, nt_ = 32 * G;   // key set, head in the group, threads per set
+    uint16_t* ks0 = at_smem + ks_ * (4 * 16 * KL);   // this set's K [2 buffers][16][KL], then V
+    uint16_t* vs0 = ks0 + 2 * 16 * KL;
+    uint16_t* qs = at_smem + NS * (4 * 16 * KL) + hw * (2 * 16 * KL);   // the head's q parts [2][16][KL]
+    const int r0 = blockIdx.x * 16, grp = blockIdx.y, h = grp * G + hw;
     const float qscale = 1.4426950408889634f * rsqrtf((float)HD);
-    // q rows r0 .. r0 + 15 of head h -> two bf16 parts in smem (rows past n are zero)
-    for (int i = lane; i < 16 * HD / 2; i += 32) {
-        const int r = i / (HD / 2), d = (i % (HD / 2)) * 2;
-        float x = 0.f, y = 0.f;
-        if (r0 + r < n) {
-            const float* q = QKV + (size_t)(r0 + r) * nqkv + (size_t)h * HD + d;
-            x = q[0] * qscale;
-            y = q[1] * qscale;
+    // q rows r0 .. r0 + 15 of head h -> two bf16 parts in smem (rows past n are zero), by key set 0
+    if (ks_ == 0) {
+        for (int i = lane; i < 16 * HD / 2; i += 32) {
+            const int r = i / (HD / 2), d = (i % (HD / 2)) * 2;
+            float x = 0.f, y = 0.f;
+            if (r0 + r < n) {
+                const float* q = QKV + (size_t)(r0 + r) * nqkv + (size_t)h * HD + d;
+                x = q[0] * qscale;
+                y = q[1] * qscale;
+            }
+            const uint32_t hi = pack_bf2(x, y);
+            const uint32_t lo = pack_bf2(x - __uint_as_float(hi << 16), y - __uint_as_float(hi & 0xFFFF0000u));
+            *reinterpret_cast<uint32_t*>(qs + r * KL + d) = hi;
+            *reinterpret_cast<uint32_t*>(qs + 16 * KL + r * KL + d) = lo;
         }
-        const uint32_t hi = pack_bf2(x, y);
-        const uint32_t lo = pack_bf2(x - __uint_as_float(hi << 16), y - __uint_as_float(hi & 0xFFFF0000u));
-        *reinterpret_cast<uint32_t*>(qs + r * KL + d) = hi;
-        *reinterpret_cast<uint32_t*>(qs + 16 * KL + r * KL + d) = lo;
     }
     const uint16_t* K = kc + ((size_t)layer * kvh + grp) * max_seq * HD;
     const uint16_t* Vv = vc + ((size_t)layer * kvh + grp) * max_seq * HD;
@@ -698,9 +706,10 @@ __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int
     for (int j = 0; j < HD / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows g8 and g8 + 8
     const int qp0 = start + r0 + g8, qp1 = qp0 + 8;             // their positions
+    const int st_ = threadIdx.x - ks_ * nt_;                    // thread index in the key set
     // K and V rows j0 .. j0 + 15 -> buffer b in plain chunk order (cp.async; rows past kend zero-filled)
     auto load_tile = [&](int j0, int b) {
-        for (int i = threadIdx.x; i < 2 * 16 * (HD / 8); i += blockDim.x) {
+        for (int i = st_; i < 2 * 16 * (HD / 8); i += nt_) {
             const int which = i / (16 * (HD / 8)), rem = i % (16 * (HD / 8));
             const int r = rem / (HD / 8), c = rem % (HD / 8), p = j0 + r;
             const bool in = p < kend;
@@ -710,17 +719,23 @@ __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    load_tile(0, 0);
-    for (int j0 = 0, b = 0; j0 < kend; j0 += 16, b ^= 1) {
+    // the key set's barrier (named barrier 1 + set; the whole CTA uses 0)
+    auto set_sync = [&]() {   // constant barrier ids (a register id would reserve all 16)
+        if (ks_ == 0) asm volatile("bar.sync 1, %0;" ::"r"(nt_) : "memory");
+        else asm volatile("bar.sync 2, %0;" ::"r"(nt_) : "memory");
+    };
+    if (16 * ks_ < kend) load_tile(16 * ks_, 0);
+    __syncthreads();   // q is stored
+    for (int j0 = 16 * ks_, b = 0; j0 < kend; j0 += 16 * NS, b ^= 1) {
         const uint16_t* ks = ks0 + b * 16 * KL;
         const uint16_t* vs = vs0 + b * 16 * KL;
-        if (j0 + 16 < kend) {
-            load_tile(j0 + 16, b ^ 1);   // its buffer was released by the barrier ending the last round
+        if (j0 + 16 * NS < kend) {
+            load_tile(j0 + 16 * NS, b ^ 1);   // its buffer was released by the barrier ending the last round
             asm volatile("cp.async.wait_group 1;" ::: "memory");
         } else {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
-        __syncthreads();   // this tile landed for every thread (and, first time, q is stored)
+        set_sync();   // this tile landed for every thread of the set
         // S = q . K^T: 16 rows x 16 positions (two n-tiles of 8)
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -805,7 +820,43 @@ __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int
                 mma_bf16(o[nd / 8 + 1], pa[part], vb[2], vb[3]);
             }
         }
-        __syncthreads();   // every warp is done with this buffer before the copy two tiles on refills it
+        set_sync();   // every warp of the set is done with this buffer before the copy two tiles on refills it
+    }
+    if constexpr (NS > 1) {
+        // key sets 1 .. NS-1 leave (m, l, O) in shared memory (the tile buffers and q are free now), lane by
+        // lane; set 0 merges them with exp2 weights to the common maximum
+        constexpr int NV = HD / 2 + 4;             // floats per lane
+        float* mb = reinterpret_cast<float*>(at_smem);
+        __syncthreads();
+        if (ks_ > 0) {
+            float* d = mb + ((size_t)((ks_ - 1) * G + hw) * NV) * 32 + lane;
+#pragma unroll
+            for (int j = 0; j < HD / 8; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[(4 * j + e) * 32] = o[j][e];
+            d[(HD / 2) * 32] = m0; d[(HD / 2 + 1) * 32] = m1; d[(HD / 2 + 2) * 32] = l0; d[(HD / 2 + 3) * 32] = l1;
+        }
+        __syncthreads();
+        if (ks_ > 0) return;
+#pragma unroll 1
+        for (int q = 1; q < NS; ++q) {
+            const float* d = mb + ((size_t)((q - 1) * G + hw) * NV) * 32 + lane;
+            const float mb0 = d[(HD / 2) * 32], mb1 = d[(HD / 2 + 1) * 32];
+            const float M0 = fmaxf(m0, mb0), M1 = fmaxf(m1, mb1);
+            const float a0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0), b0 = mb0 == -INFINITY ? 0.f : exp2f(mb0 - M0);
+            const float a1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1), b1 = mb1 == -INFINITY ? 0.f : exp2f(mb1 - M1);
+            l0 = a0 * l0 + b0 * d[(HD / 2 + 2) * 32];
+            l1 = a1 * l1 + b1 * d[(HD / 2 + 3) * 32];
+#pragma unroll
+            for (int j = 0; j < HD / 8; ++j) {
+                o[j][0] = a0 * o[j][0] + b0 * d[(4 * j + 0) * 32];
+                o[j][1] = a0 * o[j][1] + b0 * d[(4 * j + 1) * 32];
+                o[j][2] = a1 * o[j][2] + b1 * d[(4 * j + 2) * 32];
+                o[j][3] = a1 * o[j][3] + b1 * d[(4 * j + 3) * 32];
+            }
+            m0 = M0;
+            m1 = M1;
+        }
     }
     // rows r0 + g8 and r0 + g8 + 8, dims 8 j + 2 t4 (+1): fp32 to out, or the parts to P
     const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
@@ -824,8 +875,14 @@ __global__ void __launch_bounds__(256) attn_tc_rows_kernel(const float* QKV, int
     }
 }
 
+// Key sets of the prefill attention: two where the CTA stays within 256 threads.
+inline int attn_tc_sets(int G) { return G <= 4 ? 2 : 1; }
 template <int HD>
-size_t attn_tc_smem(int G) { return (size_t)(4 * 16 + G * 2 * 16) * (HD + 8) * 2; }
+size_t attn_tc_smem(int G) {
+    const size_t tiles = (size_t)(attn_tc_sets(G) * 4 * 16 + G * 2 * 16) * (HD + 8) * 2;
+    const size_t merge = (size_t)(attn_tc_sets(G) - 1) * G * (HD / 2 + 4) * 32 * 4;   // fits inside `tiles`
+    return tiles > merge ? tiles : merge;
+}
 
 template <bool RES>
 void gemm(const float* A, const uint16_t* W, const float* R, float* C, int M, int N, int K, cudaStream_t st) {
@@ -901,12 +958,19 @@ cudaError_t mk_prefill_prepare() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)TcCfg<256>::SMEM);
-    if (e == cudaSuccess)   // up to 8 query heads per KV group
-        e = cudaFuncSetAttribute(attn_tc_rows_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // up to 8 query heads per KV group (one key set), or 4 with two sets
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_tc_rows_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)attn_tc_smem<64>(8));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(attn_tc_rows_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(attn_tc_rows_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)attn_tc_smem<128>(8));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_tc_rows_kernel<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn_tc_smem<64>(4));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_tc_rows_kernel<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)attn_tc_smem<128>(4));
     if (e == cudaSuccess && !g_encode) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -943,11 +1007,18 @@ int mk_prefill_launch(const MkPrefillArgs& a, cudaStream_t st, cudaError_t* err)
             a.qkv, nqkv, a.rope_cos, a.rope_sin, a.start, qh, kvh, hd, a.max_seq, l, a.kc, a.vc, a.swz); ++launches;
         const int warps = n * qh, G = qh / kvh;
         const dim3 tgrid((n + 15) / 16, kvh);
-        if (a.attn_tc && hd == 64)
-            attn_tc_rows_kernel<64><<<tgrid, 32 * G, attn_tc_smem<64>(G), st>>>(
+        const int nsets = attn_tc_sets(G);
+        if (a.attn_tc && hd == 64 && nsets == 2)
+            attn_tc_rows_kernel<64, 2><<<tgrid, 32 * G * 2, attn_tc_smem<64>(G), st>>>(
+                a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh, a.max_seq, l, a.swz, a.att, P, prow * qd);
+        else if (a.attn_tc && hd == 64)
+            attn_tc_rows_kernel<64, 1><<<tgrid, 32 * G, attn_tc_smem<64>(G), st>>>(
+                a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh, a.max_seq, l, a.swz, a.att, P, prow * qd);
+        else if (a.attn_tc && nsets == 2)
+            attn_tc_rows_kernel<128, 2><<<tgrid, 32 * G * 2, attn_tc_smem<128>(G), st>>>(
                 a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh, a.max_seq, l, a.swz, a.att, P, prow * qd);
         else if (a.attn_tc)
-            attn_tc_rows_kernel<128><<<tgrid, 32 * G, attn_tc_smem<128>(G), st>>>(
+            attn_tc_rows_kernel<128, 1><<<tgrid, 32 * G, attn_tc_smem<128>(G), st>>>(
                 a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh, a.max_seq, l, a.swz, a.att, P, prow * qd);
         else if (hd == 64)
             attn_rows_kernel<64><<<(warps + 3) / 4, 128, 0, st>>>(a.qkv, nqkv, a.kc, a.vc, n, a.start, qh, kvh,
