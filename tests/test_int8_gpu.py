@@ -238,6 +238,30 @@ def test_wide_int8_both_attention_builds(prefill, build):
     dec.close()
 
 
+def test_int8_digits_with_activation_outliers():
+    """The int8 build holds the norm output as 22-bit fixed point with one
+    scale per vector, set by its largest entry.  Norm gains of 64 and 32 on a
+    few channels make those entries ~50x the rest (which then keep ~16 bits
+    relative to themselves); the teacher-forced logits and hidden state stay
+    within the parity bounds of the oracle's fp64 int8 forward."""
+    m = synth.make_model(WIDE, 47, std=0.03, gains="normal")
+    for kind in ("attn_norm", "ffn_norm"):
+        for l in range(WIDE.n_layers):
+            g = m[kind][l].copy()
+            g[7], g[1000], g[2047] = 0x4280, 0x4200, 0x4280   # bf16 64, 32, 64
+            m[kind][l] = g
+    fn = m["final_norm"].copy()
+    fn[3] = 0x4280
+    m["final_norm"] = fn
+    q8 = oracle.quantize_model_q8(m)
+    dec = Decoder(m, 256, int8=True)
+    orc = oracle.OracleDecoder(m, 256, q8=q8)
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, WIDE.vocab, 47, 3), 0, 10)
+    print(rep.summary())
+    rep.check()
+    dec.close()
+
+
 def test_hd128_int8():
     """The 8B layer width and head layout on the int8 stream (integer dot
     products over the activation's digits; this width has no tensor-core
