@@ -1473,25 +1473,28 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
                 // the DS warps of a chunk compute the same scores)
                 float sv[2][2];
                 if constexpr (HD == 64) {
+                    // both 8-position tiles at once: the q fragments serve both, and
+                    // their products form two independent chains
+                    uint32_t qa[NKS][2];   // A fragments of [q_hi; q_lo] (volatile: re-read per chunk)
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1]) : "r"(qfa));
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(qa[2][0]), "=r"(qa[2][1]), "=r"(qa[3][0]), "=r"(qa[3][1]) : "r"(qfa + 512u));
+                    float c[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+                    for (int x = 0; x < NKS / 2; ++x)
+#pragma unroll
+                        for (int tt = 0; tt < 2; ++tt) {
+                            uint32_t kb[4];   // the tile's 8x8 matrices of chunks 4x .. 4x+3: two k steps
+                            ldsm_x4(kb, row(ka_, 0u, c0 + 8 * tt + (lane & 7), 4 * x + (lane >> 3)));
+                            mma_rows8(c[tt][0], c[tt][1], qa[2 * x][0], qa[2 * x][1], kb[0], kb[1]);
+                            mma_rows8(c[tt][0], c[tt][1], qa[2 * x + 1][0], qa[2 * x + 1][1], kb[2], kb[3]);
+                        }
 #pragma unroll
                     for (int tt = 0; tt < 2; ++tt) {
-                        const int i = c0 + 8 * tt + (lane & 7);
-                        // A fragments of [q_hi; q_lo] (volatile: re-read per tile)
-                        uint32_t qa[NKS][2];
-                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(qa[0][0]), "=r"(qa[0][1]), "=r"(qa[1][0]), "=r"(qa[1][1]) : "r"(qfa));
-                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(qa[2][0]), "=r"(qa[2][1]), "=r"(qa[3][0]), "=r"(qa[3][1]) : "r"(qfa + 512u));
-                        uint32_t kb[NKS / 2][4];   // 8x8 matrices of chunks 4x .. 4x+3: two k steps each
-#pragma unroll
-                        for (int x = 0; x < NKS / 2; ++x) ldsm_x4(kb[x], row(ka_, 0u, i, 4 * x + (lane >> 3)));
-                        float c0_ = 0.f, c1_ = 0.f;
-#pragma unroll
-                        for (int ks = 0; ks < NKS; ++ks)
-                            mma_rows8(c0_, c1_, qa[ks][0], qa[ks][1], kb[ks >> 1][2 * (ks & 1)], kb[ks >> 1][2 * (ks & 1) + 1]);
                         // high part + remainder: lanes 16 apart hold the same head and positions
-                        c0_ += __shfl_xor_sync(0xFFFFFFFFu, c0_, 16);
-                        c1_ += __shfl_xor_sync(0xFFFFFFFFu, c1_, 16);
+                        const float c0_ = c[tt][0] + __shfl_xor_sync(0xFFFFFFFFu, c[tt][0], 16);
+                        const float c1_ = c[tt][1] + __shfl_xor_sync(0xFFFFFFFFu, c[tt][1], 16);
                         const int pi = c0 + 8 * tt + qd;
                         sv[tt][0] = pi < n ? c0_ : -INFINITY;
                         sv[tt][1] = pi + 1 < n ? c1_ : -INFINITY;
