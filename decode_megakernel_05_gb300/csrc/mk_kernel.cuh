@@ -781,6 +781,56 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
         if (trace_slot >= 0 && MK_TRACE_ON && p.trace && p.trace_detail == 1 && threadIdx.x == 0 && ti < 256)
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
         if (dmark >= 0 && ti == 0) MK_TRACE_D(dl, dmark);   // thread 0 took its first tile
+        if constexpr (DIG && MR <= 8) {
+            // int8 rows of up to 2048 columns, one pass per warp on this tile:
+            // the warp's codes and row scales go to registers and the slot is
+            // released before the arithmetic, so the copy producer refills it
+            // while the warp computes (a slot's turn is then the copy's latency
+            // plus the loads, not plus the whole pass)
+            if (ok && wpg * rows_per_warp >= R) {
+                const int r0 = wg * rows_per_warp + sub;
+                const int nv = r0 < R ? min(rw, (R - r0 + RPP - 1) / RPP) : 0;
+                uint2 cw[4][MR];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int j = 0; j < MR; ++j)
+                        cw[r][j] = r < nv ? lds64(tile + (size_t)(r0 + r * RPP) * rb + (size_t)(j * LPR + ll) * 8)
+                                          : make_uint2(0x80808080u, 0x80808080u);
+                const float* scl = reinterpret_cast<const float*>(tile + (size_t)R * K);
+                float sr[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sr[k] = k < nv ? scl[r0 + k * RPP] * xsc : 0.f;
+                release_tile(p, s, ring, (uint32_t)(MK_NCW / wpg));
+                int acc[4][3];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = acc[r][2] = 0;
+                const uint4* xq = reinterpret_cast<const uint4*>(vec);
+#pragma unroll
+                for (int j = 0; j < MR; ++j) {
+                    const int ch = j * LPR + ll;
+                    const uint4 a = xq[ch], b = xq[K / 8 + ch];
+                    const uint32_t d[6] = {a.x, a.y, a.z, b.x, b.y, b.z};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) dig_fma(cw[r][j], d, acc[r]);
+                }
+                float v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    v[k] = dig_combine(acc[k], bias);
+                    if (k < rw) {
+#pragma unroll
+                        for (int o = LPR >> 1; o >= 1; o >>= 1) v[k] += __shfl_xor_sync(0xFFFFFFFFu, v[k], o);
+                    }
+                }
+                if (ll == 0) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (k < nv) epi(ti * TR + r0 + k * RPP, v[k] * sr[k]);
+                }
+                continue;
+            }
+        }
         if (ok) {
             for (int base = wg * rows_per_warp; base < R; base += wpg * rows_per_warp) {
                 // this lane group's rows: base + sub + k*RPP, k < rw
