@@ -729,11 +729,11 @@ __device__ __forceinline__ void dot_rows4_dig(const uint8_t* r0, size_t step, in
 // RPP rows side by side per warp: rows per lane group (rw) the largest of 4, 2,
 // 1 that still lets every tile of a short phase run at once (or 4 when the
 // phase has many tiles); groups of wpg warps take the tiles in turn.
-__device__ void gemv_cfg(GemvCfg& c, int nrows, int TR, int RPP) {
+__device__ void gemv_cfg(GemvCfg& c, int nrows, int TR, int RPP, int rwmax = 4) {
     const int ntiles = (nrows + TR - 1) / TR;
-    int rw = 4, wpg = group_size((TR + 4 * RPP - 1) / (4 * RPP));
+    int rw = rwmax, wpg = group_size((TR + rwmax * RPP - 1) / (rwmax * RPP));
     if (ntiles < MK_NCW / wpg) {
-        for (int cand = 1; cand <= 4; cand <<= 1) {
+        for (int cand = 1; cand <= rwmax; cand <<= 1) {
             const int wp = group_size((TR + cand * RPP - 1) / (cand * RPP));
             if (MK_NCW / wp >= ntiles) { rw = cand; wpg = wp; break; }
         }
@@ -781,30 +781,31 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
         if (trace_slot >= 0 && MK_TRACE_ON && p.trace && p.trace_detail == 1 && threadIdx.x == 0 && ti < 256)
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
         if (dmark >= 0 && ti == 0) MK_TRACE_D(dl, dmark);   // thread 0 took its first tile
-        if constexpr (DIG && MR <= 8) {
+        if constexpr (DIG && MR <= 16) {
             // int8 rows of up to 2048 columns, one pass per warp on this tile:
             // the warp's codes and row scales go to registers and the slot is
             // released before the arithmetic, so the copy producer refills it
             // while the warp computes (a slot's turn is then the copy's latency
             // plus the loads, not plus the whole pass)
-            if (ok && wpg * rows_per_warp >= R) {
+            constexpr int HR = MR <= 8 ? 4 : 2;   // rows held (64 registers of codes)
+            if (ok && wpg * rows_per_warp >= R && rw <= HR) {
                 const int r0 = wg * rows_per_warp + sub;
                 const int nv = r0 < R ? min(rw, (R - r0 + RPP - 1) / RPP) : 0;
-                uint2 cw[4][MR];
+                uint2 cw[HR][MR];
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
+                for (int r = 0; r < HR; ++r)
 #pragma unroll
                     for (int j = 0; j < MR; ++j)
                         cw[r][j] = r < nv ? lds64(tile + (size_t)(r0 + r * RPP) * rb + (size_t)(j * LPR + ll) * 8)
                                           : make_uint2(0x80808080u, 0x80808080u);
                 const float* scl = reinterpret_cast<const float*>(tile + (size_t)R * K);
-                float sr[4];
+                float sr[HR];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) sr[k] = k < nv ? scl[r0 + k * RPP] * xsc : 0.f;
+                for (int k = 0; k < HR; ++k) sr[k] = k < nv ? scl[r0 + k * RPP] * xsc : 0.f;
                 release_tile(p, s, ring, (uint32_t)(MK_NCW / wpg));
-                int acc[4][3];
+                int acc[HR][3];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) acc[r][0] = acc[r][1] = acc[r][2] = 0;
+                for (int r = 0; r < HR; ++r) acc[r][0] = acc[r][1] = acc[r][2] = 0;
                 const uint4* xq = reinterpret_cast<const uint4*>(vec);
 #pragma unroll
                 for (int j = 0; j < MR; ++j) {
@@ -812,11 +813,11 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                     const uint4 a = xq[ch], b = xq[K / 8 + ch];
                     const uint32_t d[6] = {a.x, a.y, a.z, b.x, b.y, b.z};
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) dig_fma(cw[r][j], d, acc[r]);
+                    for (int r = 0; r < HR; ++r) dig_fma(cw[r][j], d, acc[r]);
                 }
-                float v[4];
+                float v[HR];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < HR; ++k) {
                     v[k] = dig_combine(acc[k], bias);
                     if (k < rw) {
 #pragma unroll
@@ -825,7 +826,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                 }
                 if (ll == 0) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
+                    for (int k = 0; k < HR; ++k)
                         if (k < nv) epi(ti * TR + r0 + k * RPP, v[k] * sr[k]);
                 }
                 continue;
@@ -1841,7 +1842,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         {
             constexpr int KO = G * HD, LPRO = KO >= 32 * 4 ? KO / 32 : 4;
             gemv_cfg(s.misc()->ocfg, s.misc()->plan.norows, g.TRo, 32 / LPRO);
-            gemv_cfg(s.misc()->lmcfg, s.misc()->plan.nv, g.TRh, 1);
+            gemv_cfg(s.misc()->lmcfg, s.misc()->plan.nv, g.TRh, 1, (WB == 1 && MH > 8) ? 2 : 4);
         }
         {
             const uint32_t sq = *(volatile uint32_t*)p.seq;
