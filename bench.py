@@ -309,14 +309,18 @@ KERNEL_SOURCES = ("mk_kernel.cuh", "mk_kernel.cu", "mk_internal.h")
 
 
 def kernel_source_hash() -> str:
-    """sha256 over the fused kernel's source files (the ncu traffic figure is
-    only valid for the kernel it was measured on)."""
+    """sha256 over the fused kernel's source files with their comments and
+    blank lines removed (the ncu traffic figure is only valid for the kernel
+    it was measured on; a comment does not change the kernel)."""
     import hashlib
+    import re
 
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "decode_megakernel_05_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "decode_megakernel_05_gb300", "csrc", f)) as fh:
+            src = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in src.splitlines())
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()
 
 

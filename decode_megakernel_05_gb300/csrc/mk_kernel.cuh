@@ -1394,9 +1394,10 @@ struct Attn {
 // turn (continuing across blocks); each keeps its own online softmax state
 // (m, l per head, O rows) and parks it in the same form as the lane-parallel
 // version, so the partial that leaves the CTA is computed the same way.  With
-// 128-dim heads four warps take each chunk: all four compute its scores over
-// the 128 dims (the same arithmetic, so the same m and l) and each accumulates
-// 32 dims of O (mk_attn_tc_split).
+// 128-dim heads four warps take each chunk: each computes the scores' partial
+// sums over 32 of the 128 dims, the four meet through shared memory and add
+// the partials in the same order (so they hold the same scores, m and l), and
+// each accumulates 32 dims of O (mk_attn_tc_split).
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
@@ -1520,8 +1521,7 @@ __device__ __forceinline__ bool attn_tc_blocks(const MkParams& p, const Smem& s,
             if (ci < 0) ci += NWP;
             for (; ci < nch; ci += NWP) {
                 const int c0 = 16 * ci;
-                // scores of the chunk's two 8-position tiles (over all HD dims:
-                // the DS warps of a chunk compute the same scores)
+                // scores of the chunk's two 8-position tiles
                 float sv[2][2];
                 if constexpr (HD == 64) {
                     // both 8-position tiles at once: the q fragments serve both, and
