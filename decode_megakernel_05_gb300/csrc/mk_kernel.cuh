@@ -745,8 +745,10 @@ __device__ void gemv_cfg(GemvCfg& c, int nrows, int TR, int RPP, int rwmax = 4) 
 // WB = 1: int8 rows, each row's sum times the row's scale from the tile's
 // tail before epi() gets it.
 // DIG (int8 rows only): vec holds the activation's digits (mk_xdigits), and
-// each row's sum is also scaled by s.misc()->xscale.
-template <int MR, int LPR, int WB, bool DIG = false, class Epi>
+// each row's sum is also scaled by s.misc()->xscale.  HOLDF (bf16 rows of at
+// most 4 chunks a lane): a warp with one pass on a tile loads its chunks into
+// registers and releases the slot before the arithmetic.
+template <int MR, int LPR, int WB, bool DIG = false, bool HOLDF = false, class Epi>
 __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec,
                                              int nrows, int TR, const GemvCfg& cfg, bool ab, Epi&& epi,
                                              int trace_slot = -1, int dl = 0, int dmark = -1) {
@@ -828,6 +830,50 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
 #pragma unroll
                     for (int k = 0; k < HR; ++k)
                         if (k < nv) epi(ti * TR + r0 + k * RPP, v[k] * sr[k]);
+                }
+                continue;
+            }
+        }
+        if constexpr (HOLDF && !DIG && WB == 2 && MR <= 4) {
+            // bf16 rows of up to MR * 8 * LPR columns, one pass per warp on this
+            // tile: the warp's chunks go to registers and the slot is released
+            // before the arithmetic
+            if (ok && wpg * rows_per_warp >= R) {
+                const int r0 = wg * rows_per_warp + sub;
+                const int nv = r0 < R ? min(rw, (R - r0 + RPP - 1) / RPP) : 0;
+                uint4 cw[4][MR];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int j = 0; j < MR; ++j)
+                        cw[r][j] = r < nv ? lds128(tile + (size_t)(r0 + r * RPP) * rb + (size_t)(j * LPR + ll) * 16)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+                release_tile(p, s, ring, (uint32_t)(MK_NCW / wpg));
+                float2 a[4][2];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) a[r][0] = a[r][1] = make_float2(0.f, 0.f);
+                const float4* xlo = reinterpret_cast<const float4*>(vec);
+                const float4* xhi = reinterpret_cast<const float4*>(vec + (K >> 1));
+#pragma unroll
+                for (int j = 0; j < MR; ++j) {
+                    const int ch = j * LPR + ll;
+                    const float4 xl = xlo[ch], xh = xhi[ch];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) fma_chunk(cw[r][j], xl, xh, a[r][0], a[r][1]);
+                }
+                float v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    v[k] = (a[k][0].x + a[k][0].y) + (a[k][1].x + a[k][1].y);
+                    if (k < rw) {
+#pragma unroll
+                        for (int o = LPR >> 1; o >= 1; o >>= 1) v[k] += __shfl_xor_sync(0xFFFFFFFFu, v[k], o);
+                    }
+                }
+                if (ll == 0) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (k < nv) epi(ti * TR + r0 + k * RPP, v[k]);
                 }
                 continue;
             }
@@ -2095,7 +2141,10 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
         // O-proj (rows of this CTA, columns of this group) + residual, atomically
         float* xo = xa + (size_t)(2 * l) * state;
-        ab = gemv_phase_t<MO, LPRO, WB>(p, s, ring, s.ov(), pl.norows, g.TRo, s.misc()->ocfg, ab, [&](int r, float v) {
+        // (the O-proj's slots released before its arithmetic, so the copy producer
+        // refills them with gate/up tiles sooner: in the 1B-width long-context
+        // build, where it fits the registers; the other builds spilled with it)
+        ab = gemv_phase_t<MO, LPRO, WB, false, (KO == 256 && LC != 0 && MH >= 8)>(p, s, ring, s.ov(), pl.norows, g.TRo, s.misc()->ocfg, ab, [&](int r, float v) {
             if (pl.g == 0) v += s.xres()[r];   // group 0 carries the residual of these rows
             atomicAdd(xo + pl.orow0 + r, v);
         }, -1, l, 8);
