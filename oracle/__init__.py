@@ -77,6 +77,8 @@ def lib():
             L.oracle_decode_step.restype = ctypes.c_int
             L.oracle_quantize_q8.argtypes = [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P]
             L.oracle_quantize_q8.restype = None
+            L.oracle_quantize_q4.argtypes = [_P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _P, _P]
+            L.oracle_quantize_q4.restype = None
             L.oracle_gemv_q8.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _P, _P]
             L.oracle_gemv_q8.restype = None
             L.oracle_splitmix64_output.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
@@ -202,6 +204,17 @@ def quantize_q8(w_bf16, col_scaled: bool = False):
     return q, sc
 
 
+def quantize_q4(w_bf16, col_scaled: bool = False):
+    """(int4 codes in [-7, 7], one per int8 [rows][cols]; fp32 scales [rows] or [cols]) of a bf16
+    matrix (oracle_quantize_q4)."""
+    w, pw = _c(w_bf16, np.uint16)
+    rows, cols = w.shape
+    q = np.empty((rows, cols), dtype=np.int8)
+    sc = np.empty(cols if col_scaled else rows, dtype=np.float32)
+    lib().oracle_quantize_q4(pw, rows, cols, int(col_scaled), q.ctypes.data, sc.ctypes.data)
+    return q, sc
+
+
 def gemv_q8(q, scale, x, col_scaled: bool = False) -> np.ndarray:
     q, pq = _c(q, np.int8)
     sc, ps = _c(scale, np.float32)
@@ -219,13 +232,22 @@ def quantize_model_q8(model: dict) -> dict:
     return out
 
 
+def quantize_model_q4(model: dict) -> dict:
+    """The oracle's weight-only INT4 form of a model, laid out like quantize_model_q8's (codes in
+    [-7, 7] held one per int8); OracleDecoder(q8=...) computes with it the same way."""
+    out = {k: [quantize_q4(w, col_scaled=(k == "w_down")) for w in model[k]] for k in Q8_KINDS}
+    out["lm_head"] = quantize_q4(model["embed"] if model["lm_head"] is None else model["lm_head"])
+    return out
+
+
 # ---------------------------------------------------------------- decode step
 
 class OracleDecoder:
     """The oracle's model + its own bf16 K/V cache [L][kv_heads][max_seq][head_dim]."""
 
     def __init__(self, model: dict, max_seq: int, q8: dict | None = None):
-        """q8: the model's int8 form (quantize_model_q8) to compute with instead of the bf16 matrices."""
+        """q8: the model's int8 (quantize_model_q8) or int4 (quantize_model_q4) form to compute with
+        instead of the bf16 matrices."""
         s = model["shape"]
         self.shape, self.max_seq, self._keep = s, int(max_seq), []
         c = _OracleModelC()

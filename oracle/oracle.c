@@ -134,6 +134,32 @@ void oracle_quantize_q8(const uint16_t* W, int64_t rows, int64_t cols, int col_s
     }
 }
 
+/* Weight-only INT4 quantization (stapisi.com/news/3904786, section 6, as for
+ * INT8 above; the page names no scheme): the same symmetric absmax per group,
+ * with 7 levels a side instead of 127, s_g = max|w| / 7 and q = round(w / s_g),
+ * ties to even, clamped to [-7, 7]; both float operations rounded to nearest,
+ * a group of zeros gets s = 0, q = 0.  The codes are returned one per int8_t
+ * (the packing into nibbles is the GPU stream's business, not the method's);
+ * oracle_gemv_q8 and the decode step read them like INT8 codes. */
+void oracle_quantize_q4(const uint16_t* W, int64_t rows, int64_t cols, int col_scaled, int8_t* q, float* scale) {
+    const int64_t ng = col_scaled ? cols : rows, len = col_scaled ? rows : cols;
+    for (int64_t gi = 0; gi < ng; ++gi) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < len; ++k) {
+            const float w = (float)bf2d(W[col_scaled ? k * cols + gi : gi * cols + k]);
+            amax = fabsf(w) > amax ? fabsf(w) : amax;
+        }
+        const float s4 = amax / 7.0f;
+        scale[gi] = s4;
+        for (int64_t k = 0; k < len; ++k) {
+            const int64_t at = col_scaled ? k * cols + gi : gi * cols + k;
+            float code = s4 > 0.0f ? rintf((float)bf2d(W[at]) / s4) : 0.0f;
+            code = code > 7.0f ? 7.0f : (code < -7.0f ? -7.0f : code);
+            q[at] = (int8_t)code;
+        }
+    }
+}
+
 /* y = W' x for the dequantized matrix W'[r][c] = q[r][c] * s (s = scale[r],
  * or scale[c] when col_scaled), in double. */
 void oracle_gemv_q8(const int8_t* q, const float* scale, int col_scaled, int64_t rows, int64_t cols, const double* x,

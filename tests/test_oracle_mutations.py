@@ -38,6 +38,9 @@ MUTATIONS = {
     "q8_scale_255": ("const float sg = amax / 127.0f;", "const float sg = amax / 255.0f;"),
     "q8_down_row_scaled": ("oracle_gemv_q8(m->q8->q[k][l], m->q8->s[k][l], k == 6, rows, cols, x, y);",
                            "oracle_gemv_q8(m->q8->q[k][l], m->q8->s[k][l], 0, rows, cols, x, y);"),
+    "q4_scale_8": ("const float s4 = amax / 7.0f;", "const float s4 = amax / 8.0f;"),
+    "q4_signed_max": ("amax = fabsf(w) > amax ? fabsf(w) : amax;", "amax = w > amax ? w : amax;"),
+    "q4_truncating_codes": ("rintf((float)bf2d(W[at]) / s4)", "truncf((float)bf2d(W[at]) / s4)"),
 }
 
 

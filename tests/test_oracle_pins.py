@@ -547,3 +547,75 @@ def test_q8_decode_matches_torch_causal_forward_on_dequantized_weights(kw):
         lg, h = o.step(int(t), p)
         np.testing.assert_allclose(lg, want_logits[p], rtol=1e-9, atol=1e-11)
         np.testing.assert_allclose(h, want_h[p], rtol=1e-9, atol=1e-11)
+
+
+# ---------------------------------------------------------------- weight-only INT4
+
+def test_q4_quantizer_exact_cases_and_bound():
+    """The INT4 quantizer (symmetric absmax, 7 levels a side): rows that are
+    integer multiples of a power-of-two step with max 7 steps come back exactly;
+    a row of max 7 steps with half-step values puts them at exact ties, which go
+    to the even code (2.5 -> 2, 3.5 -> 4, -0.5 -> 0, -1.5 -> -2); any row obeys |w - q s| <= s/2
+    (plus the float rounding of w / s) with |q| <= 7 and the largest |w| at +-7;
+    a zero row gets scale 0 and codes 0; per-column scaling is the same on W^T."""
+    k = np.array([[-7, -3, 0, 5, 7, 1], [7, 2.5, 3.5, -0.5, -1.5, 0], [0, 0, 0, 0, 0, 0]], dtype=np.float64)
+    steps = np.array([2.0 ** -6, 2.0 ** -4, 1.0])
+    w = (k * steps[:, None]).astype(np.float32)
+    bits = (w.view(np.uint32) >> 16).astype(np.uint16)           # exact in bf16
+    q, sc = oracle.quantize_q4(bits)
+    assert np.array_equal(q[0], k[0].astype(np.int8))             # max|w| = 7 steps: scale = step
+    assert sc[0] == np.float32(2.0 ** -6) and sc[2] == 0.0 and not q[2].any()
+    assert sc[1] == np.float32(2.0 ** -4)
+    assert np.array_equal(q[1], np.array([7, 2, 4, 0, -2, 0], dtype=np.int8))    # ties to even
+    wr = synth.normal_bf16((19, 48), 9, 3, 0.0, 0.05)
+    q, sc = oracle.quantize_q4(wr)
+    vals = bf16_vals(wr)
+    assert np.all(np.abs(q.astype(np.int32)) <= 7) and len(np.unique(q)) == 15
+    bound = sc[:, None].astype(np.float64) * (0.5 + 8 * 2.0 ** -24)
+    assert np.all(np.abs(vals - q * sc[:, None].astype(np.float64)) <= bound)
+    assert np.all(np.abs(q[np.arange(19), np.argmax(np.abs(vals), axis=1)]) == 7)
+    qc, scc = oracle.quantize_q4(wr, col_scaled=True)
+    qt, sct = oracle.quantize_q4(np.ascontiguousarray(wr.T))
+    assert np.array_equal(qc, qt.T) and np.array_equal(scc, sct)
+
+
+def test_q4_codes_are_q8_codes_of_a_coarser_grid():
+    """Brute force over every bf16 value in [-1, 1] against a row maximum of 1:
+    the INT4 code of w is the nearest integer (ties to even) to w * 7, the
+    closed form of absmax with 7 levels, computed here in float like the
+    quantizer's own division."""
+    u = np.arange(0x0000, 0x3F81, dtype=np.uint32)          # +0 .. 1.0 in bf16
+    mags = (u << 16).view(np.float32)
+    vals = np.concatenate([mags, -mags])
+    bits = ((vals.view(np.uint32) >> 16).astype(np.uint16))
+    row = np.concatenate([bits, np.array([0x3F80], dtype=np.uint16)])[None, :]   # max|w| = 1 exactly
+    q, sc = oracle.quantize_q4(row)
+    s = np.float32(1.0) / np.float32(7.0)
+    assert sc[0] == s
+    want = np.rint(np.concatenate([vals, [1.0]]).astype(np.float32) / s).clip(-7, 7)
+    assert np.array_equal(q[0].astype(np.float32), want)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(tie_embeddings=True)])
+def test_q4_decode_matches_torch_causal_forward_on_dequantized_weights(kw):
+    """The oracle's int4 decode step equals the torch fp64 causal forward run
+    on the dequantized matrices (codes times their row scales, or column scales
+    for w_down), at every position."""
+    s = tiny_shape(**kw)
+    m = synth.make_model(s, seed=18, std=0.2, gains="normal")
+    q4 = oracle.quantize_model_q4(m)
+    assert all(np.abs(q).max() <= 7 for kind in oracle.Q8_KINDS for q, _ in q4[kind])
+
+    def deq(kind, pair):
+        q, sc = pair
+        return torch.from_numpy(q.astype(np.float64) * (sc[None, :] if kind == "w_down" else sc[:, None]))
+
+    mats = {kind: [deq(kind, p) for p in q4[kind]] for kind in oracle.Q8_KINDS}
+    mats["lm_head"] = deq("lm_head", q4["lm_head"])
+    tokens = synth.uniform_tokens(10, s.vocab, 9, 98)
+    want_logits, want_h = torch_causal_forward(m, tokens, mats)
+    o = oracle.OracleDecoder(m, max_seq=16, q8=q4)
+    for p, t in enumerate(tokens):
+        lg, h = o.step(int(t), p)
+        np.testing.assert_allclose(lg, want_logits[p], rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(h, want_h[p], rtol=1e-9, atol=1e-11)
