@@ -28,8 +28,9 @@ through the batched prefill (mk_prefill: tcgen05 GEMMs, tensor-core causal
 attention), CUDA-event timed
 on its own and against the same prompt as 512 fused decode launches; its
 roofline is tensor-bound against the measured bf16 peak.  It also carries
-"int8": the same decode steps on a weight-only INT8 context (the int8 build of
-the fused kernel), CUDA-event timed, with its own HBM roofline.
+"int8" and "int4": the same decode steps on a weight-only INT8 / INT4 context
+(the int8 / int4 build of the fused kernel), CUDA-event timed, each with its
+own HBM roofline.
 """
 from __future__ import annotations
 
@@ -67,6 +68,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-prefill", action="store_true", help="skip the batched-prefill measurement")
     ap.add_argument("--no-int8", action="store_true", help="skip the weight-only INT8 decode measurement")
+    ap.add_argument("--no-int4", action="store_true", help="skip the weight-only INT4 decode measurement")
     return ap.parse_args()
 
 
@@ -253,19 +255,22 @@ def time_prefill(dec, w, torch, reps: int = 5):
             "decode_launch_prompt_ms": dl_ms, "speedup_vs_decode_launches": dl_ms / pf_ms}
 
 
-def time_int8(a, w, local, torch, positions, peak, peak_src):
-    """The same decode steps on a weight-only INT8 context (codes and per-row /
-    per-column fp32 scales streamed, dequantized in registers): its context
-    built the way the bf16 one was (pre-filled cache, or the prompt as decode
-    launches), then W warm-up and K CUDA-event-timed greedy steps at the same
-    positions; roofline against the int8 stream's algorithmic bytes."""
+def time_int8(a, w, local, torch, positions, peak, peak_src, bits=8):
+    """The same decode steps on a weight-only INT8 (bits = 8) or INT4 (bits = 4)
+    context (codes and per-row / per-column fp32 scales streamed, dequantized
+    in registers): its context built the way the bf16 one was (pre-filled
+    cache, or the prompt as decode launches), then W warm-up and K
+    CUDA-event-timed greedy steps at the same positions; roofline against the
+    quantized stream's algorithmic bytes."""
     import synth
     from decode_megakernel_05_gb300 import Decoder, mk
 
     s = w.shape
     max_seq = (w.start_pos + w.decode + 64 + 63) // 64 * 64
     m = synth.make_model(s, w.seed_weights)
-    dec = Decoder(m, max_seq, device=local, tuning=mk.tuning(a.ring_stages, a.slot_kib, a.l2_prefetch_kib, 0, 1))
+    dec = Decoder(m, max_seq, device=local, tuning=mk.tuning(a.ring_stages, a.slot_kib, a.l2_prefetch_kib, 0,
+                                                             int(bits == 8), int(bits == 4)))
+    tag = f"int{bits}"
     del m
     info = dec.info
     st = torch.cuda.current_stream()
@@ -276,7 +281,7 @@ def time_int8(a, w, local, torch, positions, peak, peak_src):
         dec.step(synth.make_first_token(w), w.prefill, logits=False)
     else:
         rc, _ = dec.generate_greedy(synth.make_prompt(w), 0, 1)
-        assert rc == 0, f"int8 prompt run failed: {rc}"
+        assert rc == 0, f"{tag} prompt run failed: {rc}"
     for k in range(a.warmup):
         dec.step_greedy(positions[k])
     torch.cuda.synchronize()
@@ -286,7 +291,7 @@ def time_int8(a, w, local, torch, positions, peak, peak_src):
         dec.step_greedy(positions[a.warmup + k])
         ev[k + 1].record(st)
     torch.cuda.synchronize()
-    assert dec.status() == 0, f"int8 device status {dec.status()}"
+    assert dec.status() == 0, f"{tag} device status {dec.status()}"
     per = sorted(ev[k].elapsed_time(ev[k + 1]) for k in range(a.steps))
     total_s = ev[0].elapsed_time(ev[-1]) / 1e3
     ctxs = [p + 1 for p in positions[a.warmup:]]
@@ -295,14 +300,14 @@ def time_int8(a, w, local, torch, positions, peak, peak_src):
     dec.close()
     return {"value": a.steps / total_s, "unit": UNIT, "ms_per_token_p50": per[len(per) // 2],
             "ms_per_token_p99": per[min(len(per) - 1, int(round(0.99 * (len(per) - 1))))],
-            "gpu_launches": a.steps, "dtype": "int8 weights, fp32 arithmetic",
-            "weights": "symmetric absmax int8, fp32 scale per output row (per input column for w_down), "
-                       "quantized on the device at load",
+            "gpu_launches": a.steps, "dtype": f"{tag} weights, fp32 arithmetic",
+            "weights": f"symmetric absmax {tag} (codes in [-{2 ** (bits - 1) - 1}, {2 ** (bits - 1) - 1}]), "
+                       "fp32 scale per output row (per input column for w_down), quantized on the device at load",
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": (load_profile_traffic(a.workload + "_int8") or {}).get("dram_bytes_per_launch"),
+                         "traffic": (load_profile_traffic(a.workload + "_" + tag) or {}).get("dram_bytes_per_launch"),
                          "algorithmic_bytes_per_launch": alg,
-                         "kernel": "mk_decode_kernel, int8 build (1 launch = 1 token)"}}
+                         "kernel": f"mk_decode_kernel, {tag} build (1 launch = 1 token)"}}
 
 
 KERNEL_SOURCES = ("mk_kernel.cuh", "mk_kernel.cu", "mk_internal.h")
@@ -491,10 +496,13 @@ def run_ours(a, world, rank, local):
         e2e = {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4,
                "api": "mk_generate_greedy(host prompt of 1 token, 1 new token) per step, pinned buffers"}
 
-    int8 = None
+    int8 = int4 = None
     if not a.no_int8 and not a.perop:
         dec.close()
         int8 = time_int8(a, w, local, torch, positions, peak, peak_src)
+    if not a.no_int4 and not a.perop:
+        dec.close()
+        int4 = time_int8(a, w, local, torch, positions, peak, peak_src, bits=4)
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
@@ -536,6 +544,8 @@ def run_ours(a, world, rank, local):
             line["prefill"] = prefill
         if int8:
             line["int8"] = int8
+        if int4:
+            line["int4"] = int4
         if e2e:
             line["e2e"] = e2e
         if cpu:

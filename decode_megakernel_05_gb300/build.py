@@ -32,6 +32,9 @@ LC_VARIANTS = [(64, 4, 2), (64, 4, 8), (128, 4, 4), (128, 4, 16)]
 # with MK_Q8_VARIANTS and MK_Q8_LC_VARIANTS in csrc/mk_api.cu
 Q8_VARIANTS = [(64, 2, 1), (64, 4, 8), (128, 4, 16)]
 Q8_LC_VARIANTS = [(64, 4, 8)]
+# weight-only INT4 builds (-DMK_WB_V=0); keep in sync with MK_Q4_VARIANTS and MK_Q4_LC_VARIANTS
+Q4_VARIANTS = [(64, 2, 1), (64, 4, 8), (128, 4, 16)]
+Q4_LC_VARIANTS = [(64, 4, 8)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -65,10 +68,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
                     "-I", INCLUDE, "-I", CSRC]
     jobs = [(src, os.path.join(BUILD, src.replace(".cu", ".o")), []) for src in SOURCES]
     kernels = ([v + (0, 2) for v in VARIANTS] + [v + (1, 2) for v in LC_VARIANTS] +
-               [v + (0, 1) for v in Q8_VARIANTS] + [v + (1, 1) for v in Q8_LC_VARIANTS])
+               [v + (0, 1) for v in Q8_VARIANTS] + [v + (1, 1) for v in Q8_LC_VARIANTS] +
+               [v + (0, 0) for v in Q4_VARIANTS] + [v + (1, 0) for v in Q4_LC_VARIANTS])
     for hd, g, mh, lc, wb in kernels:
         for tr in (False, True):   # each without and with the segment trace compiled in
-            sfx = ("_lc" if lc else "") + ("_q8" if wb == 1 else "") + ("_trace" if tr else "")
+            sfx = ("_lc" if lc else "") + {2: "", 1: "_q8", 0: "_q4"}[wb] + ("_trace" if tr else "")
             jobs.append(("mk_kernel.cu", os.path.join(BUILD, f"mk_kernel_{hd}_{g}_{mh}{sfx}.o"),
                          [f"-DMK_HD_V={hd}", f"-DMK_G_V={g}", f"-DMK_MH_V={mh}", f"-DMK_LC_V={lc}",
                           f"-DMK_WB_V={wb}"] + ([] if tr else ["-DMK_NO_TRACE"])))

@@ -26,6 +26,10 @@
 // Q8_LC_VARIANTS in build.py).
 #define MK_Q8_VARIANTS(X) X(64, 2, 1) X(64, 4, 8) X(128, 4, 16)
 #define MK_Q8_LC_VARIANTS(X) X(64, 4, 8)
+// Weight-only INT4 builds (-DMK_WB_V=0; keep in sync with Q4_VARIANTS and
+// Q4_LC_VARIANTS in build.py).
+#define MK_Q4_VARIANTS(X) X(64, 2, 1) X(64, 4, 8) X(128, 4, 16)
+#define MK_Q4_LC_VARIANTS(X) X(64, 4, 8)
 // Each variant exists twice: without trace code (launched normally) and with
 // it (launched while a segment trace is requested).
 #define MK_DECL(hd, g, mh)                                         \
@@ -40,16 +44,26 @@
 #define MK_DECL_LC_Q8(hd, g, mh)                                          \
     extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh##_lc_q8(void); \
     extern "C" const void* mk_kernel_trace_ptr_##hd##_##g##_##mh##_lc_q8(void);
+#define MK_DECL_Q4(hd, g, mh)                                          \
+    extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh##_q4(void); \
+    extern "C" const void* mk_kernel_trace_ptr_##hd##_##g##_##mh##_q4(void);
+#define MK_DECL_LC_Q4(hd, g, mh)                                          \
+    extern "C" const void* mk_kernel_ptr_##hd##_##g##_##mh##_lc_q4(void); \
+    extern "C" const void* mk_kernel_trace_ptr_##hd##_##g##_##mh##_lc_q4(void);
 MK_VARIANTS(MK_DECL)
 MK_LC_VARIANTS(MK_DECL_LC)
 MK_Q8_VARIANTS(MK_DECL_Q8)
 MK_Q8_LC_VARIANTS(MK_DECL_LC_Q8)
+MK_Q4_VARIANTS(MK_DECL_Q4)
+MK_Q4_LC_VARIANTS(MK_DECL_LC_Q4)
 #undef MK_DECL
 #undef MK_DECL_LC
 #undef MK_DECL_Q8
 #undef MK_DECL_LC_Q8
+#undef MK_DECL_Q4
+#undef MK_DECL_LC_Q4
 
-// The kernel for a shape and weight width (wb = 2 bf16, 1 weight-only INT8);
+// The kernel for a shape and weight form (wb = 2 bf16, 1 weight-only INT8, 0 INT4);
 // with long_ctx, its long-context (tensor-core attention) build where one
 // exists.  Returns 1 for a long-context build, 0 for the standard one, -1 if
 // none fits.
@@ -64,14 +78,20 @@ static int mk_kernel_variant(int hd, int G, int H, int wb, bool long_ctx, const 
 #define MK_PICK_STD(hd_, g_, mh_) MK_PICK(hd_, g_, mh_, 2, 0, )
 #define MK_PICK_LC_Q8(hd_, g_, mh_) MK_PICK(hd_, g_, mh_, 1, 1, _lc_q8)
 #define MK_PICK_Q8(hd_, g_, mh_) MK_PICK(hd_, g_, mh_, 1, 0, _q8)
+#define MK_PICK_LC_Q4(hd_, g_, mh_) MK_PICK(hd_, g_, mh_, 0, 1, _lc_q4)
+#define MK_PICK_Q4(hd_, g_, mh_) MK_PICK(hd_, g_, mh_, 0, 0, _q4)
     MK_LC_VARIANTS(MK_PICK_LC)
     MK_Q8_LC_VARIANTS(MK_PICK_LC_Q8)
+    MK_Q4_LC_VARIANTS(MK_PICK_LC_Q4)
     MK_VARIANTS(MK_PICK_STD)
     MK_Q8_VARIANTS(MK_PICK_Q8)
+    MK_Q4_VARIANTS(MK_PICK_Q4)
 #undef MK_PICK_LC
 #undef MK_PICK_STD
 #undef MK_PICK_LC_Q8
 #undef MK_PICK_Q8
+#undef MK_PICK_LC_Q4
+#undef MK_PICK_Q4
 #undef MK_PICK
     *fn = *fn_trace = nullptr;
     return -1;
@@ -128,7 +148,7 @@ Tune resolve_tuning(const mk_tuning* t) {
     r.slot = (t && t->slot_kib > 0) ? t->slot_kib * 1024 : 32 * 1024;
     r.l2pf = (t && t->l2_prefetch_kib > 0) ? t->l2_prefetch_kib * 1024 : 0;   // default off (measured slower)
     r.grid = (t && t->grid_ctas > 0) ? t->grid_ctas : 0;
-    r.wb = (t && t->weight_int8) ? 1 : 2;
+    r.wb = (t && t->weight_int4) ? 0 : (t && t->weight_int8) ? 1 : 2;
     return r;
 }
 
@@ -185,12 +205,14 @@ void build_maps(const MkGeom& g, const std::vector<MkCtaPlan>& plans, Maps& m) {
     m.q.assign(L, {}); m.k.assign(L, {}); m.v.assign(L, {}); m.o.assign(L, {});
     m.gate.assign(L, {}); m.up.assign(L, {}); m.down.assign(L, {}); m.down_scale.assign(L, {}); m.lm.clear();
     // rows of tiles of at most TR rows of K weights from `off` on: row i of a
-    // tile of R rows at tile + i * K * wb, its scale (int8) at tile + R * K + 4 i
+    // tile of R rows at tile + i * rb (rb = the row's bytes), its scale (int8,
+    // int4) at tile + R * rb + 4 i
     auto row_tiles = [&](int64_t& off, int nrows, int TR, int K, auto&& emit) {
+        const int64_t rb = mk_wbytes(K, wb);
         for (int r = 0; r < nrows; r += TR) {
             const int R = std::min(TR, nrows - r);
             for (int i = 0; i < R; ++i)
-                emit(r + i, off + (int64_t)i * K * wb, off + (int64_t)R * K + 4LL * i);
+                emit(r + i, off + (int64_t)i * rb, off + (int64_t)R * rb + 4LL * i);
             off += mk_row_tile_bytes(R, K, wb, 0);
         }
     };
@@ -206,16 +228,17 @@ void build_maps(const MkGeom& g, const std::vector<MkCtaPlan>& plans, Maps& m) {
             row_tiles(off, p.norows, g.TRo, KO, [&](int r, int64_t d, int64_t so) {
                 m.o[l].push_back(MkRowCopyQ{d, (int64_t)(p.orow0 + r), p.g * KO, KO, so});
             });
-            // a GU tile: n gate rows, n up rows (then for int8 their 2n scales
-            // and the n W_down column scales of the same j's)
+            // a GU tile: n gate rows, n up rows (then for int8 / int4 their 2n
+            // scales and the n W_down column scales of the same j's)
+            const int64_t hb = mk_wbytes(H, wb);
             for (int j = 0; j < p.nj; j += g.JT) {
                 const int n = std::min(g.JT, p.nj - j);
-                const int64_t sc = off + (int64_t)2 * n * H;
+                const int64_t sc = off + (int64_t)2 * n * hb;
                 for (int jj = 0; jj < n; ++jj) {
                     const int64_t src = p.j0 + j + jj;
-                    m.gate[l].push_back(MkRowCopyQ{off + (int64_t)jj * H * wb, src, 0, H, sc + 4LL * jj});
-                    m.up[l].push_back(MkRowCopyQ{off + (int64_t)(n + jj) * H * wb, src, 0, H, sc + 4LL * (n + jj)});
-                    if (wb == 1) m.down_scale[l].push_back(MkScaleCopy{sc + 4LL * (2 * n + jj), src});
+                    m.gate[l].push_back(MkRowCopyQ{off + (int64_t)jj * hb, src, 0, H, sc + 4LL * jj});
+                    m.up[l].push_back(MkRowCopyQ{off + (int64_t)(n + jj) * hb, src, 0, H, sc + 4LL * (n + jj)});
+                    if (wb != 2) m.down_scale[l].push_back(MkScaleCopy{sc + 4LL * (2 * n + jj), src});
                 }
                 off += mk_row_tile_bytes(2 * n, H, wb, n);
             }
@@ -267,15 +290,15 @@ bool check_schedule(const MkGeom& g, const std::vector<MkCtaPlan>& plans, int64_
     return true;
 }
 
-// Weight bytes one step must read: every matrix once (bf16, or int8 codes
-// plus one fp32 scale per row / W_down column), the norm gains and one
+// Weight bytes one step must read: every matrix once (bf16, or int8 / int4
+// codes plus one fp32 scale per row / W_down column), the norm gains and one
 // embedding row (counted at 2 bytes per value).
 int64_t weight_bytes_per_token(const mk_config* c, int wb) {
     const int64_t H = c->hidden, qd = (int64_t)c->n_q_heads * c->head_dim, kvd = (int64_t)c->n_kv_heads * c->head_dim;
     const int64_t F = c->ffn, V = c->vocab, L = c->n_layers;
     const int64_t mat = L * (qd * H + 2 * kvd * H + H * qd + 3 * F * H) + V * H;
-    const int64_t scales = wb == 1 ? 4 * (L * (qd + 2 * kvd + H + 3 * F) + V) : 0;
-    return mat * wb + scales + 2 * (L * 2 * H + H + H);
+    const int64_t scales = wb != 2 ? 4 * (L * (qd + 2 * kvd + H + 3 * F) + V) : 0;
+    return mk_wbytes(mat, wb) + scales + 2 * (L * 2 * H + H + H);
 }
 
 }  // namespace
@@ -499,7 +522,8 @@ int mk_relayout_host(const mk_config* cfg, const mk_tuning* tuning, int32_t grid
     if (!w || !arena_out || grid_ctas < 1 || w->on_device) return MK_ERR_INVALID_ARG;
     if (!cfg->tie_embeddings && !w->lm_head) return MK_ERR_INVALID_ARG;
     Tune tu = resolve_tuning(tuning);
-    if (tu.wb != 2) return MK_ERR_UNSUPPORTED;   // int8 streams are quantized on the device only
+    if (tuning && tuning->weight_int8 && tuning->weight_int4) return MK_ERR_INVALID_ARG;
+    if (tu.wb != 2) return MK_ERR_UNSUPPORTED;   // int8 / int4 streams are quantized on the device only
     MkGeom g;
     if ((rc = build_geom(cfg, tu, grid_ctas, 1, g)) != MK_OK) return rc;
     std::vector<MkCtaPlan> plans;
@@ -535,6 +559,7 @@ int mk_relayout_host(const mk_config* cfg, const mk_tuning* tuning, int32_t grid
 int mk_create(const mk_config* cfg, const mk_tuning* tuning, int device, mk_ctx** out) {
     if (!out) return MK_ERR_INVALID_ARG;
     *out = nullptr;
+    if (tuning && tuning->weight_int8 && tuning->weight_int4) return MK_ERR_INVALID_ARG;   // one weight form
     int rc = check_shape(cfg, true, resolve_tuning(tuning).wb);
     if (rc != MK_OK) return rc;
     mk_ctx* c = new mk_ctx();
@@ -668,7 +693,8 @@ int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
     Maps m;
     build_maps(g, c->plans, m);
 
-    const bool q8 = g.wb == 1;
+    const bool q8 = g.wb != 2;              // int8 or int4 codes
+    const int qbits = g.wb == 0 ? 4 : 8;
     const size_t max_elems = std::max({V * H, F * H, qd * H, kvd * H, H});
     uint16_t* staging = nullptr;
     if (!on_dev) MK_CU(cudaMalloc(&staging, max_elems * 2));
@@ -706,21 +732,23 @@ int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
     if (q8) {
         cudaError_t e = cudaMalloc(&q_tmp, max_elems);
         if (e == cudaSuccess) e = cudaMalloc(&s_tmp, std::max({V, F, H, qd, kvd}) * 4);
-        if (e != cudaSuccess) { rc = cuda_fail(e, "int8 staging"); cleanup(); return rc; }
+        if (e != cudaSuccess) { rc = cuda_fail(e, "int8/int4 staging"); cleanup(); return rc; }
     }
-    // bf16 streams copy the rows; int8 streams quantize the matrix (per row)
-    // and copy codes and row scales
+    // bf16 streams copy the rows; int8 / int4 streams quantize the matrix (per
+    // row) and copy (int4: pack) codes and row scales
     auto gather_rows = [&](const std::vector<MkRowCopyQ>& ops, const void* src, size_t rows, size_t cols) -> int {
         const uint16_t* d = nullptr;
         int r = copy_matrix_to_device(src, on_dev, rows * cols * 2, staging, &d, st);
         if (r != MK_OK) return r;
         cudaError_t e;
         if (q8) {
-            e = mk_launch_quantize_q8(d, (int64_t)rows, (int64_t)cols, 0, q_tmp, s_tmp, st);
+            e = mk_launch_quantize(d, (int64_t)rows, (int64_t)cols, 0, qbits, q_tmp, s_tmp, st);
             if (e != cudaSuccess) return cuda_fail(e, "quantize rows");
             r = upload_ops(ops, &d_rowsq, &cap_rowsq, st);
             if (r != MK_OK) return r;
-            e = mk_launch_relayout_rows_q8(c->arena, q_tmp, (int64_t)cols, s_tmp, d_rowsq, (int)ops.size(), st);
+            e = qbits == 4
+                    ? mk_launch_relayout_rows_q4(c->arena, q_tmp, (int64_t)cols, s_tmp, d_rowsq, (int)ops.size(), st)
+                    : mk_launch_relayout_rows_q8(c->arena, q_tmp, (int64_t)cols, s_tmp, d_rowsq, (int)ops.size(), st);
         } else {
             const std::vector<MkRowCopy> plain = plain_rows(ops);
             r = upload_ops(plain, &d_rows, &cap_rows, st);
@@ -760,9 +788,13 @@ int mk_load_weights(mk_ctx* c, const mk_weights* w, void* stream) {
             MK_TRY(copy_matrix_to_device(w->w_down[l], on_dev, H * F * 2, staging, &d, st));
             MK_TRY(upload_ops(m.down[l], &d_cols, &cap_cols, st));
             if (q8) {   // per-column scales, kept in the GU tiles of the same j's
-                MK_TRYCU(mk_launch_quantize_q8(d, (int64_t)H, (int64_t)F, 1, q_tmp, s_tmp, st));
-                MK_TRYCU(mk_launch_relayout_cols_q8(c->arena, q_tmp, (int)H, (int)F, d_cols, (int)m.down[l].size(),
-                                                    st));
+                MK_TRYCU(mk_launch_quantize(d, (int64_t)H, (int64_t)F, 1, qbits, q_tmp, s_tmp, st));
+                if (qbits == 4)
+                    MK_TRYCU(mk_launch_relayout_cols_q4(c->arena, q_tmp, (int)H, (int)F, d_cols,
+                                                        (int)m.down[l].size(), st));
+                else
+                    MK_TRYCU(mk_launch_relayout_cols_q8(c->arena, q_tmp, (int)H, (int)F, d_cols,
+                                                        (int)m.down[l].size(), st));
                 MK_TRY(upload_ops(m.down_scale[l], &d_scl, &cap_scl, st));
                 MK_TRYCU(mk_launch_scatter_scales(c->arena, s_tmp, d_scl, (int)m.down_scale[l].size(), st));
             } else {
@@ -1182,6 +1214,7 @@ int mk_get_info(const mk_ctx* c, mk_info* o) {
     o->attn_tc_min_ctx = c->kernel_tc ? (int32_t)mk_tc_min_ctx(c) : -1;
     o->attn_pos_per_cta = c->attn_ctas_force > 0 ? 0 : c->attn_pos_per_cta;
     o->weight_int8 = c->geo.wb == 1 ? 1 : 0;
+    o->weight_int4 = c->geo.wb == 0 ? 1 : 0;
     return MK_OK;
 }
 

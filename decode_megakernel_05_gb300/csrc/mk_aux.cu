@@ -67,8 +67,10 @@ __global__ void mk_kv_rows_kernel(uint4* plain, uint4* cache_layer, int kvh, int
 
 // One block per group (a row, or a column when col_scaled): the group's
 // largest |w| by a block reduction, then every code.
-__global__ void mk_quantize_q8_kernel(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int8_t* q,
-                                      float* scale) {
+// qmax: 127 (int8, codes stored as q + 128) or 7 (int4, codes stored as q + 8,
+// one a byte until the re-layout packs them).
+__global__ void mk_quantize_q8_kernel(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int qmax,
+                                      int8_t* q, float* scale) {
     __shared__ float red[32];
     const int64_t gi = blockIdx.x;
     const int64_t len = col_scaled ? rows : cols;
@@ -81,14 +83,48 @@ __global__ void mk_quantize_q8_kernel(const uint16_t* w, int64_t rows, int64_t c
     __syncthreads();
     amax = 0.f;
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, red[i]);
-    const float sg = __fdiv_rn(amax, 127.0f);
+    const float qm = (float)qmax;
+    const float sg = __fdiv_rn(amax, qm);
     if (threadIdx.x == 0) scale[gi] = sg;
+    const int bias = qmax == 7 ? 8 : 128;
     for (int64_t k = threadIdx.x; k < len; k += blockDim.x) {
         float c = 0.f;
         if (sg > 0.f) c = rintf(__fdiv_rn(__uint_as_float((uint32_t)w[at(k)] << 16), sg));
-        c = fminf(fmaxf(c, -127.f), 127.f);
-        reinterpret_cast<uint8_t*>(q)[at(k)] = (uint8_t)((int)c + 128);   // stored biased: q + 128
+        c = fminf(fmaxf(c, -qm), qm);
+        reinterpret_cast<uint8_t*>(q)[at(k)] = (uint8_t)((int)c + bias);   // stored biased
     }
+}
+
+// INT4 rows: one block per stored row, ncols biased codes (one a byte, a
+// multiple of 8) packed two a byte (group of 8 -> 4 bytes, byte k = weight k
+// low, weight k + 4 high), and the row's scale.
+__global__ void mk_relayout_rows_q4_kernel(uint8_t* arena, const int8_t* q, int64_t cols, const float* scale,
+                                           const MkRowCopyQ* ops, int n) {
+    const int i = blockIdx.x;
+    if (i >= n) return;
+    const MkRowCopyQ op = ops[i];
+    const uint8_t* s = reinterpret_cast<const uint8_t*>(q) + op.src_row * cols + op.col0;
+    uint8_t* d = arena + op.dst_off;
+    for (int b = threadIdx.x; b < op.ncols / 2; b += blockDim.x) {
+        const int c0 = 8 * (b >> 2) + (b & 3);
+        d[b] = (uint8_t)((s[c0] & 0xF) | ((s[c0 + 4] & 0xF) << 4));
+    }
+    if (threadIdx.x == 0) *reinterpret_cast<float*>(arena + op.scale_off) = scale[op.src_row];
+}
+
+// INT4 W_down [H][F]: columns j0 .. j0+nj-1 as H/2 contiguous bytes each, rows
+// packed as above (byte b: rows 8 (b / 4) + b % 4 and 4 more).
+__global__ void mk_relayout_cols_q4_kernel(uint8_t* arena, const int8_t* q, int H, int F, const MkColCopy* ops, int n) {
+    const int i = blockIdx.x;
+    if (i >= n) return;
+    const MkColCopy op = ops[i];
+    const int b = blockIdx.y * blockDim.x + threadIdx.x;
+    if (b >= H / 2) return;
+    const int r0 = 8 * (b >> 2) + (b & 3);
+    const uint8_t* lo = reinterpret_cast<const uint8_t*>(q) + (int64_t)r0 * F + op.j0;
+    const uint8_t* hi = lo + 4LL * F;
+    uint8_t* d = arena + op.dst_off + b;
+    for (int jj = 0; jj < op.nj; ++jj) d[(int64_t)jj * (H / 2)] = (uint8_t)((lo[jj] & 0xF) | ((hi[jj] & 0xF) << 4));
 }
 
 // One block per stored row: ncols int8 (a multiple of 16) and the row's scale.
@@ -120,11 +156,29 @@ __global__ void mk_scatter_scales_kernel(uint8_t* arena, const float* scale, con
     if (i < n) *reinterpret_cast<float*>(arena + ops[i].dst_off) = scale[ops[i].idx];
 }
 
-cudaError_t mk_launch_quantize_q8(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int8_t* q,
-                                  float* scale, cudaStream_t st) {
+cudaError_t mk_launch_quantize(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int bits, int8_t* q,
+                               float* scale, cudaStream_t st) {
     const int64_t ng = col_scaled ? cols : rows;
     if (ng <= 0) return cudaSuccess;
-    mk_quantize_q8_kernel<<<(unsigned)ng, 256, 0, st>>>(w, rows, cols, col_scaled, q, scale);
+    if (bits != 8 && bits != 4) return cudaErrorInvalidValue;
+    mk_quantize_q8_kernel<<<(unsigned)ng, 256, 0, st>>>(w, rows, cols, col_scaled, bits == 8 ? 127 : 7, q, scale);
+    return cudaGetLastError();
+}
+cudaError_t mk_launch_quantize_q8(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int8_t* q,
+                                  float* scale, cudaStream_t st) {
+    return mk_launch_quantize(w, rows, cols, col_scaled, 8, q, scale, st);
+}
+cudaError_t mk_launch_relayout_rows_q4(uint8_t* arena, const int8_t* q, int64_t cols, const float* scale,
+                                       const MkRowCopyQ* ops, int n, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    mk_relayout_rows_q4_kernel<<<n, 128, 0, st>>>(arena, q, cols, scale, ops, n);
+    return cudaGetLastError();
+}
+cudaError_t mk_launch_relayout_cols_q4(uint8_t* arena, const int8_t* q, int H, int F, const MkColCopy* ops, int n,
+                                       cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    dim3 grid((unsigned)n, (unsigned)((H / 2 + 127) / 128));
+    mk_relayout_cols_q4_kernel<<<grid, 128, 0, st>>>(arena, q, H, F, ops, n);
     return cudaGetLastError();
 }
 cudaError_t mk_launch_relayout_rows_q8(uint8_t* arena, const int8_t* q, int64_t cols, const float* scale,

@@ -37,6 +37,16 @@ cudaError_t mk_launch_relayout_rows_q8(uint8_t* arena, const int8_t* q, int64_t 
                                        const MkRowCopyQ* ops, int n, cudaStream_t st);
 cudaError_t mk_launch_relayout_cols_q8(uint8_t* arena, const int8_t* q, int H, int F, const MkColCopy* ops, int n,
                                        cudaStream_t st);
+// The same quantization with bits = 8 (as above) or 4 (scale = max|w| / 7,
+// codes in [-7, 7], each written as the byte q + 8).
+cudaError_t mk_launch_quantize(const uint16_t* w, int64_t rows, int64_t cols, int col_scaled, int bits, int8_t* q,
+                               float* scale, cudaStream_t st);
+// INT4 re-layout of such codes: rows (ncols codes -> ncols / 2 bytes) and
+// W_down columns (H codes -> H / 2 bytes), packed as the stream keeps them.
+cudaError_t mk_launch_relayout_rows_q4(uint8_t* arena, const int8_t* q, int64_t cols, const float* scale,
+                                       const MkRowCopyQ* ops, int n, cudaStream_t st);
+cudaError_t mk_launch_relayout_cols_q4(uint8_t* arena, const int8_t* q, int H, int F, const MkColCopy* ops, int n,
+                                       cudaStream_t st);
 cudaError_t mk_launch_scatter_scales(uint8_t* arena, const float* scale, const MkScaleCopy* ops, int n,
                                      cudaStream_t st);
 

@@ -33,6 +33,13 @@
 // then the n column scales of W_down for the same j's (the down projection
 // folds them into SiLU(gate) * up); a D tile is columns of H bytes.  Each tile
 // is padded to 16 bytes.
+//
+// Weight-only INT4 streams (wb = 0) have the same tiles and scales with two
+// codes a byte, each stored as the nibble q + 8: every group of 8 consecutive
+// weights of a row (or of a W_down column) is 4 bytes, byte k holding weight k
+// in its low nibble and weight k + 4 in its high one, so the low nibbles of
+// the word are the group's first four weights and the high nibbles its last
+// four -- the same halves as an int8 group's two words.
 #pragma once
 #include <stdint.h>
 
@@ -86,11 +93,15 @@ struct MkTopP {
 
 MK_HD int64_t mk_split(int64_t n, int64_t parts, int64_t k) { return (k * n) / parts; }
 
-// Bytes of a row tile: R rows of K weights of wb bytes, and for int8 (wb = 1)
-// the R row scales plus `extra` more scales, padded to 16 bytes.
+// Stream bytes of K weights: 2 each (bf16, wb = 2), 1 (int8, wb = 1) or half
+// a byte (int4, wb = 0: two codes a byte).
+MK_HD int64_t mk_wbytes(int64_t K, int wb) { return wb == 0 ? K / 2 : K * wb; }
+
+// Bytes of a row tile: R rows of K weights, and for int8 / int4 (wb < 2) the R
+// row scales plus `extra` more scales, padded to 16 bytes.
 MK_HD int mk_row_tile_bytes(int R, int K, int wb, int extra) {
-    int64_t b = (int64_t)R * K * wb;
-    if (wb == 1) b += 4LL * (R + extra);
+    int64_t b = (int64_t)R * mk_wbytes(K, wb);
+    if (wb != 2) b += 4LL * (R + extra);
     return (int)((b + 15) & ~(int64_t)15);
 }
 
@@ -100,8 +111,8 @@ MK_HD int mk_row_tile_bytes(int R, int K, int wb, int extra) {
 // column scales of a GU tile.
 MK_HD int mk_tile_rows_wb(int K, int slot_bytes, int wb, bool gu_extra) {
     if (wb == 2) return (slot_bytes / (2 * K)) & ~1;
-    int r = (slot_bytes / K) & ~1;
-    while (r > 2 && mk_row_tile_bytes(r, K, 1, gu_extra ? r / 2 : 0) > slot_bytes) r -= 2;
+    int r = (int)(slot_bytes / mk_wbytes(K, wb)) & ~1;
+    while (r > 2 && mk_row_tile_bytes(r, K, wb, gu_extra ? r / 2 : 0) > slot_bytes) r -= 2;
     return r;
 }
 MK_HD int mk_tile_rows(int K, int slot_bytes) { return mk_tile_rows_wb(K, slot_bytes, 2, false); }
@@ -128,7 +139,7 @@ struct MkGeom {
     int32_t max_rows, max_nj;    // per-CTA maxima (QKV rows, FFN slice)
     int32_t smem_bytes;
     int32_t kv_swz;              // K/V cache rows chunk-permuted (mk_kv_index); set with the long-context build
-    int32_t wb;                  // bytes per weight in the stream: 2 bf16, 1 int8 (weight-only INT8)
+    int32_t wb;                  // weight form in the stream: 2 bf16, 1 int8, 0 int4 (weight-only INT8 / INT4)
     // shared-memory carve-up (byte offsets from the dynamic smem base)
     int32_t off_full, off_empty, off_xv, off_ov, off_part, off_u, off_xres, off_xres2, off_rope,
         off_red, off_sc, off_misc;
@@ -157,7 +168,7 @@ MK_HD bool mk_geom_init(MkGeom& g, int L, int H, int qh, int kvh, int hd, int F,
     g.L = L; g.H = H; g.qh = qh; g.kvh = kvh; g.hd = hd; g.F = F; g.V = V; g.max_seq = max_seq;
     g.kv_swz = 0;
     g.wb = wb;
-    if (wb != 1 && wb != 2) return false;
+    if (wb < 0 || wb > 2) return false;
     if (L < 1 || H < 8 || qh < 1 || kvh < 1 || F < 1 || V < 1 || max_seq < 1 || nC < 1) return false;
     if (qh % kvh != 0 || nC % kvh != 0) return false;
     g.G = qh / kvh;
@@ -172,7 +183,7 @@ MK_HD bool mk_geom_init(MkGeom& g, int L, int H, int qh, int kvh, int hd, int F,
     g.TRh = mk_tile_rows_wb(H, slot_bytes, wb, true);
     g.TRo = mk_tile_rows_wb(g.G * hd, slot_bytes, wb, false);
     g.JT = g.TRh / 2;
-    g.JD = slot_bytes / (wb * H);
+    g.JD = (int32_t)(slot_bytes / mk_wbytes(H, wb));
     g.KB = slot_bytes / (2 * hd);
     g.max_rows = 2 * (int)((g.NP + g.CPG - 1) / g.CPG);
     g.max_nj = (F + nC - 1) / nC;
@@ -288,7 +299,7 @@ MK_HD int64_t mk_layer_bytes(const MkGeom& g, const MkCtaPlan& p) {
         const int n = mk_imin(g.JT, p.nj - j);
         b += mk_row_tile_bytes(2 * n, g.H, g.wb, n);
     }
-    for (int j = 0; j < p.nj; j += g.JD) b += (int64_t)mk_imin(g.JD, p.nj - j) * g.H * g.wb;
+    for (int j = 0; j < p.nj; j += g.JD) b += (int64_t)mk_imin(g.JD, p.nj - j) * mk_wbytes(g.H, g.wb);
     return b;
 }
 
@@ -374,7 +385,7 @@ MK_HD void mk_walk_tiles(const MkGeom& g, const MkCtaPlan& pl, const uint8_t* ar
             f((const void*)cur, by); cur += by;
         }
         for (int j = 0; j < pl.nj; j += g.JD) {
-            uint32_t by = (uint32_t)(mk_imin(g.JD, pl.nj - j) * H * g.wb);
+            uint32_t by = (uint32_t)(mk_imin(g.JD, pl.nj - j) * mk_wbytes(H, g.wb));
             f((const void*)cur, by); cur += by;
         }
     }

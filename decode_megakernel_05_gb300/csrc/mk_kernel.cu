@@ -12,14 +12,18 @@
 #define MK_LC_V 0   // 1: the long-context build (see mk_decode_kernel)
 #endif
 #ifndef MK_WB_V
-#define MK_WB_V 2   // bytes per streamed weight: 2 bf16, 1 weight-only INT8
+#define MK_WB_V 2   // streamed weight form: 2 bf16, 1 weight-only INT8, 0 weight-only INT4
 #endif
 #if MK_LC_V && MK_WB_V == 1
 #define MK_SFX _lc_q8
+#elif MK_LC_V && MK_WB_V == 0
+#define MK_SFX _lc_q4
 #elif MK_LC_V
 #define MK_SFX _lc
 #elif MK_WB_V == 1
 #define MK_SFX _q8
+#elif MK_WB_V == 0
+#define MK_SFX _q4
 #else
 #define MK_SFX
 #endif

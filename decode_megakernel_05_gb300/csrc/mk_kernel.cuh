@@ -627,7 +627,31 @@ __device__ __forceinline__ void fma_chunk8(const uint2 w, const float4 xl, const
     a0 = __ffma2_rn(i8pair(hi, 0), make_float2(xh.x, xh.y), a0);
     a1 = __ffma2_rn(i8pair(hi, 2), make_float2(xh.z, xh.w), a1);
 }
-// A chunk of 8 weights: 16 bytes of bf16 (WB = 2) or 8 bytes of int8 (WB = 1).
+// Weight-only INT4 chunks: 8 codes in one word, byte k holding code k + 8 in
+// its low nibble and code k + 4 + 8 in its high one (columns as a bf16
+// chunk's); the nibbles, spread one a byte, take the int8 route above with
+// 2^23 + 8 coming off.
+__device__ __forceinline__ uint32_t lds32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
+__device__ __forceinline__ uint32_t nib_lo(uint32_t w) { return w & 0x0F0F0F0Fu; }          // codes 0..3
+__device__ __forceinline__ uint32_t nib_hi(uint32_t w) { return (w >> 4) & 0x0F0F0F0Fu; }   // codes 4..7
+__device__ __forceinline__ float2 i4pair(uint32_t a, int k) {
+    const float x = __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7540u + k));
+    const float y = __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7540u + k + 1));
+    return __fadd2_rn(make_float2(x, y), make_float2(-8388616.f, -8388616.f));
+}
+__device__ __forceinline__ void fma_chunk4(const uint32_t w, const float4 xl, const float4 xh, float2& a0, float2& a1) {
+    const uint32_t lo = nib_lo(w), hi = nib_hi(w);
+    a0 = __ffma2_rn(i4pair(lo, 0), make_float2(xl.x, xl.y), a0);
+    a1 = __ffma2_rn(i4pair(lo, 2), make_float2(xl.z, xl.w), a1);
+    a0 = __ffma2_rn(i4pair(hi, 0), make_float2(xh.x, xh.y), a0);
+    a1 = __ffma2_rn(i4pair(hi, 2), make_float2(xh.z, xh.w), a1);
+}
+// Stream bytes of K weights of form WB (2 bf16, 1 int8, 0 int4), and of one
+// 8-weight chunk.
+template <int WB> __host__ __device__ constexpr int wrow_bytes(int K) { return WB == 0 ? K / 2 : K * WB; }
+template <int WB> __host__ __device__ constexpr int wchunk_bytes() { return WB == 0 ? 4 : 8 * WB; }
+// A chunk of 8 weights: 16 bytes of bf16 (WB = 2), 8 bytes of int8 (WB = 1)
+// or 4 bytes of int4 (WB = 0).
 template <int WB> struct WChunk;
 template <> struct WChunk<2> {
     using T = uint4;
@@ -643,6 +667,14 @@ template <> struct WChunk<1> {
     static __device__ __forceinline__ T zero() { return make_uint2(0x80808080u, 0x80808080u); }   // codes 0
     static __device__ __forceinline__ void fma(const T w, const float4 xl, const float4 xh, float2& a0, float2& a1) {
         fma_chunk8(w, xl, xh, a0, a1);
+    }
+};
+template <> struct WChunk<0> {
+    using T = uint32_t;
+    static __device__ __forceinline__ T load(const void* p) { return lds32(p); }
+    static __device__ __forceinline__ T zero() { return 0x88888888u; }   // codes 0
+    static __device__ __forceinline__ void fma(const T w, const float4 xl, const float4 xh, float2& a0, float2& a1) {
+        fma_chunk4(w, xl, xh, a0, a1);
     }
 };
 
@@ -665,21 +697,28 @@ __device__ __forceinline__ float dig_combine(const int (&acc)[3], const int (&bi
     return fmaf((float)(acc[2] - bias[2]), 65536.f, fmaf((float)(acc[1] - bias[1]), 256.f, (float)(acc[0] - bias[0])));
 }
 // The lane's digit words of chunk ch (4 low-half and 4 high-half columns) and
-// their share of the per-lane constant (128 * sum of the digits).
+// their share of the per-lane constant (the code bias, 128 for int8 and 8 for
+// int4 (WB = 0), times the sum of the digits).
+template <int WB = 1>
 __device__ __forceinline__ void dig_load(const uint4* xq, int K, int ch, uint32_t (&d)[6], int (&bias)[3]) {
+    constexpr uint32_t BIAS = WB == 0 ? 0x08080808u : 0x80808080u;
     const uint4 a = xq[ch], b = xq[K / 8 + ch];
     d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = b.x; d[4] = b.y; d[5] = b.z;
 #pragma unroll
-    for (int k = 0; k < 3; ++k) bias[k] = dp4a_us(0x80808080u, d[k + 3], dp4a_us(0x80808080u, d[k], bias[k]));
+    for (int k = 0; k < 3; ++k) bias[k] = dp4a_us(BIAS, d[k + 3], dp4a_us(BIAS, d[k], bias[k]));
 }
 // 8 biased codes (w.x: the 4 low-half columns, w.y: the 4 high-half ones) into the three sums.
 __device__ __forceinline__ void dig_fma(const uint2 w, const uint32_t (&d)[6], int (&acc)[3]) {
 #pragma unroll
     for (int k = 0; k < 3; ++k) acc[k] = dp4a_us(w.y, d[k + 3], dp4a_us(w.x, d[k], acc[k]));
 }
+// The same for an int4 chunk: its low nibbles are the low-half columns' codes, its high ones the others'.
+__device__ __forceinline__ void dig_fma(const uint32_t w, const uint32_t (&d)[6], int (&acc)[3]) {
+    dig_fma(make_uint2(nib_lo(w), nib_hi(w)), d, acc);
+}
 
 // Dot products of up to 4 rows (nv valid, rows r0 + k*step) with the
-// split-order vector xs; each lane covers MR chunks of 8 columns (8 * WB bytes).
+// split-order vector xs; each lane covers MR chunks of 8 columns (wchunk_bytes<WB>() bytes).
 template <int MR, int LPR, int WB = 2>
 __device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t step, int nv, const float* xs, int K, int ll,
                                           float o[4]) {
@@ -694,14 +733,14 @@ __device__ __forceinline__ void dot_rows4(const uint8_t* r0, size_t step, int nv
         const float4 xl = xlo[ch], xh = xhi[ch];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-            if (r < nv) WChunk<WB>::fma(WChunk<WB>::load(r0 + r * step + (size_t)ch * (8 * WB)), xl, xh, a[r][0], a[r][1]);
+            if (r < nv) WChunk<WB>::fma(WChunk<WB>::load(r0 + r * step + (size_t)ch * wchunk_bytes<WB>()), xl, xh, a[r][0], a[r][1]);
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) o[r] = (a[r][0].x + a[r][0].y) + (a[r][1].x + a[r][1].y);
 }
-// The same over int8 rows and the digits of the activation (xq); bias: the
-// lane's constant over its MR chunks.  o[r] is in units of the activation scale.
-template <int MR, int LPR>
+// The same over int8 / int4 rows and the digits of the activation (xq); bias:
+// the lane's constant over its MR chunks.  o[r] is in units of the activation scale.
+template <int MR, int LPR, int WB = 1>
 __device__ __forceinline__ void dot_rows4_dig(const uint8_t* r0, size_t step, int nv, const uint4* xq, int K, int ll,
                                               const int (&bias)[3], float o[4]) {
     int acc[4][3];
@@ -714,7 +753,7 @@ __device__ __forceinline__ void dot_rows4_dig(const uint8_t* r0, size_t step, in
         const uint32_t d[6] = {a.x, a.y, a.z, b.x, b.y, b.z};
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-            if (r < nv) dig_fma(lds64(r0 + r * step + (size_t)ch * 8), d, acc[r]);
+            if (r < nv) dig_fma(WChunk<WB>::load(r0 + r * step + (size_t)ch * wchunk_bytes<WB>()), d, acc[r]);
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) o[r] = dig_combine(acc[r], bias);
@@ -742,9 +781,9 @@ __device__ void gemv_cfg(GemvCfg& c, int nrows, int TR, int RPP, int rwmax = 4) 
     for (int w = 0; w < MK_NCW; ++w) { c.grp[w] = (int8_t)(w / wpg); c.wg[w] = (int8_t)(w % wpg); }
 }
 
-// WB = 1: int8 rows, each row's sum times the row's scale from the tile's
-// tail before epi() gets it.
-// DIG (int8 rows only): vec holds the activation's digits (mk_xdigits), and
+// WB = 1 / 0: int8 / int4 rows, each row's sum times the row's scale from the
+// tile's tail before epi() gets it.
+// DIG (int8 / int4 rows only): vec holds the activation's digits (mk_xdigits), and
 // each row's sum is also scaled by s.misc()->xscale.  HOLDF (bf16 rows of at
 // most 4 chunks a lane): a warp with one pass on a tile loads its chunks into
 // registers and releases the slot before the arithmetic.
@@ -752,15 +791,16 @@ template <int MR, int LPR, int WB, bool DIG = false, bool HOLDF = false, class E
 __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, Ring& ring, const float* vec,
                                              int nrows, int TR, const GemvCfg& cfg, bool ab, Epi&& epi,
                                              int trace_slot = -1, int dl = 0, int dmark = -1) {
-    static_assert(!DIG || WB == 1, "digits are the int8 rows' activation form");
+    static_assert(!DIG || WB != 2, "digits are the int8 / int4 rows' activation form");
     constexpr int K = MR * 8 * LPR;
     constexpr int RPP = 32 / LPR;
+    constexpr int CBY = wchunk_bytes<WB>();
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane / LPR, ll = lane % LPR;
     const int ntiles = cfg.ntiles, rw = cfg.rw, wpg = cfg.wpg, ngrp = cfg.ngrp;
     const int grp = cfg.grp[w], wg = cfg.wg[w];
     const int rows_per_warp = rw * RPP;
-    const size_t rb = (size_t)K * WB;
+    const size_t rb = (size_t)wrow_bytes<WB>(K);
     int bias[3] = {0, 0, 0};
     float xsc = 1.f;
     if constexpr (DIG) {
@@ -768,7 +808,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
 #pragma unroll (MR < 8 ? MR : 8)
         for (int j = 0; j < MR; ++j) {
             uint32_t d[6];
-            dig_load(xq, K, j * LPR + ll, d, bias);
+            dig_load<WB>(xq, K, j * LPR + ll, d, bias);
         }
         xsc = s.misc()->xscale;
     }
@@ -784,7 +824,7 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
             p.trace[(size_t)blockIdx.x * MK_TRACE_STRIDE + trace_slot + ti] = gtimer();
         if (dmark >= 0 && ti == 0) MK_TRACE_D(dl, dmark);   // thread 0 took its first tile
         if constexpr (DIG && MR <= 16) {
-            // int8 rows of up to 2048 columns, one pass per warp on this tile:
+            // int8 / int4 rows of up to 2048 columns, one pass per warp on this tile:
             // the warp's codes and row scales go to registers and the slot is
             // released before the arithmetic, so the copy producer refills it
             // while the warp computes (a slot's turn is then the copy's latency
@@ -793,14 +833,14 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
             if (ok && wpg * rows_per_warp >= R && rw <= HR) {
                 const int r0 = wg * rows_per_warp + sub;
                 const int nv = r0 < R ? min(rw, (R - r0 + RPP - 1) / RPP) : 0;
-                uint2 cw[HR][MR];
+                typename WChunk<WB>::T cw[HR][MR];
 #pragma unroll
                 for (int r = 0; r < HR; ++r)
 #pragma unroll
                     for (int j = 0; j < MR; ++j)
-                        cw[r][j] = r < nv ? lds64(tile + (size_t)(r0 + r * RPP) * rb + (size_t)(j * LPR + ll) * 8)
-                                          : make_uint2(0x80808080u, 0x80808080u);
-                const float* scl = reinterpret_cast<const float*>(tile + (size_t)R * K);
+                        cw[r][j] = r < nv ? WChunk<WB>::load(tile + (size_t)(r0 + r * RPP) * rb + (size_t)(j * LPR + ll) * CBY)
+                                          : WChunk<WB>::zero();
+                const float* scl = reinterpret_cast<const float*>(tile + (size_t)R * rb);
                 float sr[HR];
 #pragma unroll
                 for (int k = 0; k < HR; ++k) sr[k] = k < nv ? scl[r0 + k * RPP] * xsc : 0.f;
@@ -886,8 +926,8 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                 float v[4] = {0.f, 0.f, 0.f, 0.f};
                 if constexpr (DIG) {
                     if (nv > 0)
-                        dot_rows4_dig<MR, LPR>(tile + r0 * rb, rb * RPP, nv, reinterpret_cast<const uint4*>(vec), K, ll,
-                                               bias, v);
+                        dot_rows4_dig<MR, LPR, WB>(tile + r0 * rb, rb * RPP, nv, reinterpret_cast<const uint4*>(vec), K,
+                                                   ll, bias, v);
                 } else {
                     if (nv > 0) dot_rows4<MR, LPR, WB>(tile + r0 * rb, rb * RPP, nv, vec, K, ll, v);
                 }
@@ -905,10 +945,10 @@ __device__ __forceinline__ bool gemv_phase_t(const MkParams& p, const Smem& s, R
                     }
                 }
                 if (ll == 0) {
-                    const float* scl = reinterpret_cast<const float*>(tile + (size_t)R * K);   // int8: row scales
+                    const float* scl = reinterpret_cast<const float*>(tile + (size_t)R * rb);   // int8 / int4: row scales
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        if (k < nv) epi(ti * TR + r0 + k * RPP, WB == 1 ? v[k] * (scl[r0 + k * RPP] * xsc) : v[k]);
+                        if (k < nv) epi(ti * TR + r0 + k * RPP, WB != 2 ? v[k] * (scl[r0 + k * RPP] * xsc) : v[k]);
                 }
                 if (dmark >= 0 && ti == 0 && base == 0) MK_TRACE_D(dl, 14);   // its sums handed to epi
             }
@@ -947,8 +987,8 @@ struct WideGemv {
 template <int MH>
 struct WidePart { static constexpr int NKB = MH < 4 ? MH : 4; };
 
-// WB = 1 (int8 rows): the same columns per chunk (8 bytes instead of 16), and
-// each row's partials times the row's scale from the tile's tail; a GU tile's
+// WB = 1 / 0 (int8 / int4 rows): the same columns per chunk (8 or 4 bytes
+// instead of 16), and each row's partials times the row's scale from the tile's tail; a GU tile's
 // W_down column scales (after the row scales) go to tsink[j] for the j's it
 // covers (the caller multiplies them into SiLU(gate) * up).
 template <int MH, int NG, int WB>
@@ -960,8 +1000,9 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
     constexpr int PS = WidePart<MH>::NKB;
     static_assert(W::ok && NKB <= PS, "wide GEMV mapping");
     // rows of a tile per warp at most: 16 chunks of 16 bytes per lane (slots of
-    // 32 KB at most), or 32 chunks of 8 bytes for int8
-    constexpr int RPW = (16 / CPL) * (3 - WB);
+    // 32 KB at most), 32 chunks of 8 bytes for int8, 64 of 4 bytes for int4
+    constexpr int RPW = (16 / CPL) * (WB == 2 ? 1 : WB == 1 ? 2 : 4);
+    constexpr int RB = wrow_bytes<WB>(K), CBY = wchunk_bytes<WB>();
     constexpr int NPS = RPW / 4;    // passes of four rows
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = w / WPG, wg = w % WPG;
@@ -969,7 +1010,7 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
     // the lane's activations for the whole phase: fp32 (bf16 rows), or the
     // digits and the lane's constant (int8 rows, mk_xdigits)
     float4 xl[WB == 2 ? CPL : 1], xh[WB == 2 ? CPL : 1];
-    uint32_t xd[WB == 1 ? CPL : 1][6];
+    uint32_t xd[WB != 2 ? CPL : 1][6];
     int bias[3] = {0, 0, 0};
     float xsc = 1.f;
 #pragma unroll
@@ -979,10 +1020,10 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
             xl[j] = reinterpret_cast<const float4*>(xs)[ch];
             xh[j] = reinterpret_cast<const float4*>(xs + K / 2)[ch];
         } else {
-            dig_load(reinterpret_cast<const uint4*>(xs), K, ch, xd[j], bias);
+            dig_load<WB>(reinterpret_cast<const uint4*>(xs), K, ch, xd[j], bias);
         }
     }
-    if constexpr (WB == 1) xsc = s.misc()->xscale;
+    if constexpr (WB != 2) xsc = s.misc()->xscale;
     const int ntiles = (nrows + TR - 1) / TR;
     for (int ti = 0; ti < ntiles && !ab; ++ti) {
         if (NG > 1 && (ti % NG) != grp) { ring.advance(p.geo.ns); continue; }   // another group's tile
@@ -993,18 +1034,25 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
         int r0 = rs - R0 % NRS;
         if (r0 < 0) r0 += NRS;
         const int nrow = (ok && r0 < R) ? (R - r0 + NRS - 1) / NRS : 0;
-        // int8: the R row scales follow the rows (then, in a GU tile, the R / 2
-        // W_down column scales of its j's); each lane that writes a row's
-        // partial keeps that row's scale per pass (read before the release)
-        float scl[NPS];
-        if constexpr (WB == 1) {
-            const float* sc = reinterpret_cast<const float*>(tile + (size_t)R * K);
+        // int8 / int4: the R row scales follow the rows (then, in a GU tile,
+        // the R / 2 W_down column scales of its j's); each lane that writes a
+        // row's partial keeps that row's scale per pass (read before the
+        // release), or, for int4 shares of up to 32 rows, lane i keeps row i's
+        // and a pass fetches it with a shuffle (one register instead of eight)
+        constexpr bool LANE_SCL = WB == 0 && RPW <= 32;
+        float scl[LANE_SCL ? 1 : NPS];
+        if constexpr (WB != 2) {
+            const float* sc = reinterpret_cast<const float*>(tile + (size_t)R * RB);
             if (tsink && ok && wg == 0)
                 for (int i = lane; i < R / 2; i += 32) tsink[R0 / 2 + i] = sc[R + i];
+            if constexpr (LANE_SCL) {
+                scl[0] = lane < nrow ? sc[r0 + lane * NRS] * xsc : 0.f;
+            } else {
 #pragma unroll
-            for (int pb = 0; pb < NPS; ++pb) {
-                const int rr = 4 * pb + (lane >> 3);
-                scl[pb] = rr < nrow ? sc[r0 + rr * NRS] * xsc : 0.f;
+                for (int pb = 0; pb < NPS; ++pb) {
+                    const int rr = 4 * pb + (lane >> 3);
+                    scl[pb] = rr < nrow ? sc[r0 + rr * NRS] * xsc : 0.f;
+                }
             }
         }
         // rows qb .. qb+3 of the share: dot products, transposed butterfly (lane
@@ -1045,7 +1093,8 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
             kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 4);
             kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 2);
             kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 1);
-            if constexpr (WB == 1) kk *= scl[qb >> 2];
+            if constexpr (LANE_SCL) kk *= __shfl_sync(0xFFFFFFFFu, scl[0], qb + (lane >> 3));
+            else if constexpr (WB != 2) kk *= scl[qb >> 2];
             const int q = lane >> 3;               // row of the four this lane holds
             if ((lane & 7) == 0 && q < nv) {
                 float* pr = part + (R0 + r0 + (qb + q) * NRS) * PS;
@@ -1057,11 +1106,11 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
             }
         };
         auto at = [&](int q, int j) {              // this lane's chunk of row q, chunk j of the share
-            return tile + (size_t)(r0 + q * NRS) * (K * WB) + ((cb * CPL + j) * 32 + lane) * (8 * WB);
+            return tile + (size_t)(r0 + q * NRS) * RB + ((cb * CPL + j) * 32 + lane) * CBY;
         };
-        // (int8 rows of 256 columns, up to 32 per warp, are read as used: held
-        // whole beside their scales they spilled)
-        if constexpr (CPL <= 2 && !(WB == 1 && CPL == 1)) {
+        // (int8 / int4 rows of 256 columns, up to 32 / 64 per warp, are read as
+        // used: held whole beside their scales they spilled)
+        if constexpr (CPL <= 2 && !(WB != 2 && CPL == 1)) {
             // Load the warp's whole share of the tile, then release the slot at
             // once: the copy producer refills it while this warp computes (the
             // arrival's release semantics order it after these loads).
@@ -1835,7 +1884,7 @@ __device__ __forceinline__ float mk_gumbel(uint64_t seed, int pos, int v) {
 // pays once every CTA attends to more positions than one chunk per warp; on
 // short contexts the lane-parallel attention of the standard build has the
 // shorter dependency chain.  The host picks the build per step.
-// WB: bytes per streamed weight, 2 (bf16) or 1 (weight-only INT8).
+// WB: streamed weight form, 2 (bf16), 1 (weight-only INT8) or 0 (weight-only INT4).
 template <int HD, int G, int MH, int LC, int WB>
 __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_constant__ MkParams p) {
     static_assert(G <= MK_NCW, "one consumer warp per query head of a KV group (softmax, combine weights)");
@@ -1888,7 +1937,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         {
             constexpr int KO = G * HD, LPRO = KO >= 32 * 4 ? KO / 32 : 4;
             gemv_cfg(s.misc()->ocfg, s.misc()->plan.norows, g.TRo, 32 / LPRO);
-            gemv_cfg(s.misc()->lmcfg, s.misc()->plan.nv, g.TRh, 1, (WB == 1 && MH > 8) ? 2 : 4);
+            gemv_cfg(s.misc()->lmcfg, s.misc()->plan.nv, g.TRh, 1, (WB != 2 && MH > 8) ? 2 : 4);
         }
         {
             const uint32_t sq = *(volatile uint32_t*)p.seq;
@@ -1941,7 +1990,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         // ---------------- segment A: RMSNorm + QKV GEMV + RoPE + K/V append
         MK_TRACE(16 * l + 0);
         const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
-        if constexpr (WB == 1)
+        if constexpr (WB != 2)
             ab = rmsnorm_to_dig<(MH * 32 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H,
                                                                ab, s.xres(), pl.orow0, pl.g == 0 ? pl.norows : 0);
         else
@@ -2156,7 +2205,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         MK_TRACE(16 * l + 9);
 
         // ---------------- segment C: RMSNorm + gate/up + SiLU*up, then down
-        if constexpr (WB == 1)
+        if constexpr (WB != 2)
             ab = rmsnorm_to_dig<(MH * 32 + MK_NCT - 1) / MK_NCT>(p, s, xo, nullptr, p.ffn_norm + (size_t)l * H, ab, s.xres2(),
                                                                ldv(s.misc()->dr0), ldv(s.misc()->dr1) - ldv(s.misc()->dr0));
         else
@@ -2170,13 +2219,13 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             // (int8: and W_down's column scales of those j's, which the GEMV
             // leaves in u and which multiply into SiLU(gate) * up)
             const int JT = g.JT;
-            ab = gemv_fifo<MH, WB>(p, s, ring, s.xv(), 2 * pl.nj, 2 * JT, ab, s.part(), WB == 1 ? s.u() : nullptr);
+            ab = gemv_fifo<MH, WB>(p, s, ring, s.xv(), 2 * pl.nj, 2 * JT, ab, s.part(), WB != 2 ? s.u() : nullptr);
             for (int j = t; j < pl.nj; j += MK_NCT) {
                 const int q = j / JT, jj = j % JT;
                 const int n = min(JT, pl.nj - q * JT);
                 const float gt = wide_row<MH>(s.part(), q * 2 * JT + jj);
                 const float up = wide_row<MH>(s.part(), q * 2 * JT + n + jj);
-                s.u()[j] = gt / (1.f + __expf(-gt)) * up * (WB == 1 ? s.u()[j] : 1.f);
+                s.u()[j] = gt / (1.f + __expf(-gt)) * up * (WB != 2 ? s.u()[j] : 1.f);
             }
         }
         MK_TRACE(16 * l + 11);
@@ -2208,7 +2257,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                 if (b % P != jp) { ring.advance(p.geo.ns); continue; }   // another group's tile
                 const int n = min(g.JD, pl.nj - j0);
                 const uint8_t* tile;
-                const bool ok = take_tile(p, s, ring, (uint32_t)(n * H * WB), tile);
+                const bool ok = take_tile(p, s, ring, (uint32_t)(n * wrow_bytes<WB>(H)), tile);
                 if constexpr (TP == 128 && CPT <= 2 && !LC && WB == 2) {
                     // a thread's share is 16 chunks (slots of 32 KB): loaded
                     // whole, then the slot is released before the arithmetic
@@ -2243,7 +2292,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                         for (int jj = 0; jj < n; ++jj) {
                             const float uj = s.u()[j0 + jj];
                             const float2 u2 = make_float2(uj, uj);
-                            const uint8_t* col = tile + (size_t)jj * H * WB;
+                            const uint8_t* col = tile + (size_t)jj * wrow_bytes<WB>(H);
 #pragma unroll
                             for (int m = 0; m < CPT; ++m) {
                                 if constexpr (WB == 2) {
@@ -2252,13 +2301,20 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
                                     da[m][1] = __ffma2_rn(bf2_lo_hi(w.y), u2, da[m][1]);
                                     da[m][2] = __ffma2_rn(bf2_lo_hi(w.z), u2, da[m][2]);
                                     da[m][3] = __ffma2_rn(bf2_lo_hi(w.w), u2, da[m][3]);
-                                } else {   // 8 rows of int8 (u already carries W_down's column scale)
+                                } else if constexpr (WB == 1) {   // 8 rows of int8 (u already carries W_down's column scale)
                                     const uint2 w = lds64(col + (size_t)(tp + m * TP) * 8);
                                     const uint32_t lo = w.x, hi = w.y;
                                     da[m][0] = __ffma2_rn(i8pair(lo, 0), u2, da[m][0]);
                                     da[m][1] = __ffma2_rn(i8pair(lo, 2), u2, da[m][1]);
                                     da[m][2] = __ffma2_rn(i8pair(hi, 0), u2, da[m][2]);
                                     da[m][3] = __ffma2_rn(i8pair(hi, 2), u2, da[m][3]);
+                                } else {   // 8 rows of int4 (low nibbles rows 0-3, high ones rows 4-7)
+                                    const uint32_t w = lds32(col + (size_t)(tp + m * TP) * 4);
+                                    const uint32_t lo = nib_lo(w), hi = nib_hi(w);
+                                    da[m][0] = __ffma2_rn(i4pair(lo, 0), u2, da[m][0]);
+                                    da[m][1] = __ffma2_rn(i4pair(lo, 2), u2, da[m][1]);
+                                    da[m][2] = __ffma2_rn(i4pair(hi, 0), u2, da[m][2]);
+                                    da[m][3] = __ffma2_rn(i4pair(hi, 2), u2, da[m][3]);
                                 }
                             }
                         }
@@ -2322,7 +2378,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
     // ---------------- final RMSNorm + LM head + argmax
     {
         const float* xl = xa + (size_t)(2 * L - 1) * state;
-        if constexpr (WB == 1)
+        if constexpr (WB != 2)
             ab = rmsnorm_to_dig<(MH * 32 + MK_NCT - 1) / MK_NCT>(p, s, xl, nullptr, p.final_norm, ab, nullptr, 0, 0,
                                                                c == 0 ? p.hidden : nullptr);
         else
@@ -2336,7 +2392,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
         bool nonfinite = false;
         // top-p: the logits go to scratch and the phase only finds max(logit / T)
         const bool topp = p.inv_temp > 0.f && p.top_p < 1.f;
-        ab = gemv_phase_t<MH, 32, WB, WB == 1>(p, s, ring, s.xv(), pl.nv, g.TRh, s.misc()->lmcfg, ab, [&](int r, float lg) {
+        ab = gemv_phase_t<MH, 32, WB, WB != 2>(p, s, ring, s.xv(), pl.nv, g.TRh, s.misc()->lmcfg, ab, [&](int r, float lg) {
             const int v = pl.v0 + r;
             if (p.logits) p.logits[v] = lg;
             if (isfinite(lg)) {

@@ -17,15 +17,17 @@ _LAYER_NAMES = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up
 
 class Decoder:
     def __init__(self, model: dict, max_seq: int, device: int = 0, tuning: mk.mk_tuning | None = None,
-                 perop: bool = False, int8: bool = False):
-        """int8: stream weight-only INT8 matrices (quantized on the device at load, mk_tuning.weight_int8)."""
+                 perop: bool = False, int8: bool = False, int4: bool = False):
+        """int8 / int4: stream weight-only INT8 / INT4 matrices (quantized on the device at load,
+        mk_tuning.weight_int8 / weight_int4)."""
         import torch
 
-        if int8:
+        if int8 or int4:
             t = mk.mk_tuning()
             if tuning is not None:
                 ctypes.memmove(ctypes.byref(t), ctypes.byref(tuning), ctypes.sizeof(t))
-            t.weight_int8 = 1
+            t.weight_int8 = int(bool(int8))
+            t.weight_int4 = int(bool(int4))
             tuning = t
 
         self.torch = torch

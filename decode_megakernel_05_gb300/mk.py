@@ -53,7 +53,7 @@ class mk_config(ctypes.Structure):
 
 class mk_tuning(ctypes.Structure):
     _fields_ = [("ring_stages", _i32), ("slot_kib", _i32), ("l2_prefetch_kib", _i32), ("grid_ctas", _i32),
-                ("weight_int8", _i32)]
+                ("weight_int8", _i32), ("weight_int4", _i32)]
 
 
 class mk_weights(ctypes.Structure):
@@ -67,7 +67,7 @@ class mk_info(ctypes.Structure):
                 ("slot_bytes", _i32), ("smem_bytes", _i32), ("sm_count", _i32), ("l2_prefetch_bytes", _i32),
                 ("arena_bytes", _i64), ("weight_bytes_per_token", _i64), ("kv_bytes_per_position", _i64),
                 ("device_bytes", _i64), ("attn_tc", _i32), ("attn_tc_min_ctx", _i32),
-                ("attn_pos_per_cta", _i32), ("weight_int8", _i32)]
+                ("attn_pos_per_cta", _i32), ("weight_int8", _i32), ("weight_int4", _i32)]
 
 
 # (name, restype, argtypes) of every exported function, in header order.
@@ -145,8 +145,8 @@ def config_from_shape(shape, max_seq: int) -> mk_config:
                      shape.vocab, max_seq, shape.rms_eps, shape.rope_theta, int(shape.tie_embeddings))
 
 
-def tuning(ring_stages=0, slot_kib=0, l2_prefetch_kib=0, grid_ctas=0, weight_int8=0) -> mk_tuning:
-    return mk_tuning(ring_stages, slot_kib, l2_prefetch_kib, grid_ctas, int(weight_int8))
+def tuning(ring_stages=0, slot_kib=0, l2_prefetch_kib=0, grid_ctas=0, weight_int8=0, weight_int4=0) -> mk_tuning:
+    return mk_tuning(ring_stages, slot_kib, l2_prefetch_kib, grid_ctas, int(weight_int8), int(weight_int4))
 
 
 class _PtrTable:

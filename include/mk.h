@@ -91,6 +91,14 @@ typedef struct {
                                 (64, 4, 2048) and (128, 4, 4096); other shapes return
                                 MK_ERR_UNSUPPORTED from mk_create, as do mk_enable_perop(.., 1),
                                 mk_prefill and mk_relayout_host on an int8 context / tuning */
+    int32_t weight_int4;     /* nonzero: weight-only INT4 (the same page and section), the INT8
+                                scheme with 7 levels a side: s = max|w| / 7 per output row (per
+                                input column for w_down), codes round(w / s) ties to even in
+                                [-7, 7], both divisions rounded to nearest; the step streams two
+                                codes a byte (each as the nibble code + 8) and the fp32 scales.
+                                Built for the same three shapes as INT8, with the same
+                                restrictions; setting both weight_int8 and weight_int4 is
+                                MK_ERR_INVALID_ARG from mk_create and mk_relayout_host */
 } mk_tuning;
 
 /* Weights, row-major [out, in] bf16 (raw 16-bit patterns).  Either all host
@@ -116,8 +124,8 @@ typedef struct {
     int32_t grid_ctas, ctas_per_group, block_threads, ring_stages, slot_bytes;
     int32_t smem_bytes, sm_count, l2_prefetch_bytes;
     int64_t arena_bytes;             /* re-laid-out weight stream bytes on the device */
-    int64_t weight_bytes_per_token;  /* weight bytes one step reads: matrices (bf16, or int8 codes + fp32
-                                        scales), gains and 1 embedding row at 2 bytes a value */
+    int64_t weight_bytes_per_token;  /* weight bytes one step reads: matrices (bf16, or int8 / int4 codes
+                                        + fp32 scales), gains and 1 embedding row at 2 bytes a value */
     int64_t kv_bytes_per_position;   /* bf16 K+V bytes one attended position costs (all layers) */
     int64_t device_bytes;            /* everything the context allocated on the device */
     int32_t attn_tc;                 /* 1: a build whose attention runs on the tensor cores exists
@@ -130,6 +138,7 @@ typedef struct {
                                         group, at most ctas_per_group (0: the count is forced
                                         with MK_DBG_ATTN_CTAS) */
     int32_t weight_int8;             /* 1: the context streams weight-only INT8 (mk_tuning) */
+    int32_t weight_int4;             /* 1: the context streams weight-only INT4 (mk_tuning) */
 } mk_info;
 
 /* Create a context on CUDA device `device`: validates the shape, sizes the

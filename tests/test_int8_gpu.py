@@ -41,29 +41,45 @@ def pad16(b):
     return (b + 15) // 16 * 16
 
 
-def tile_bytes(R, K, extra):
-    """R int8 rows of K, their R scales and `extra` more scales, padded to 16 bytes."""
-    return pad16(R * K + 4 * (R + extra))
+def row_bytes(K, bits=8):
+    """Stream bytes of K codes: one a byte (int8) or two a byte (int4)."""
+    return K if bits == 8 else K // 2
 
 
-def tile_rows(K, gu_extra):
+def tile_bytes(R, K, extra, bits=8):
+    """R int8 / int4 rows of K, their R scales and `extra` more scales, padded to 16 bytes."""
+    return pad16(R * row_bytes(K, bits) + 4 * (R + extra))
+
+
+def tile_rows(K, gu_extra, bits=8):
     """Even rows per tile: as many as fit a slot with their scales (and, for the
     hidden-width tiles, the half-as-many W_down column scales of a GU tile)."""
-    r = (SLOT // K) & ~1
-    while r > 2 and tile_bytes(r, K, r // 2 if gu_extra else 0) > SLOT:
+    r = (SLOT // row_bytes(K, bits)) & ~1
+    while r > 2 and tile_bytes(r, K, r // 2 if gu_extra else 0, bits) > SLOT:
         r -= 2
     return r
 
 
-def decode_arena_q8(arena, s, grid):
-    """Codes and scales of every matrix read out of an int8 arena, the
-    W_down column scales, and a per-byte coverage count of the code bytes."""
+def unpack_q4(b):
+    """int4 codes from stream bytes: each 4-byte group holds 8 codes, byte k
+    code k in its low nibble and code k + 4 in its high one, each as q + 8."""
+    g = b.reshape(-1, 4)
+    out = np.empty((g.shape[0], 8), np.int8)
+    out[:, :4] = (g & 0x0F).astype(np.int8) - 8
+    out[:, 4:] = (g >> 4).astype(np.int8) - 8
+    return out.reshape(-1)
+
+
+def decode_arena_q8(arena, s, grid, bits=8):
+    """Codes and scales of every matrix read out of an int8 (or, bits = 4,
+    int4) arena, the W_down column scales, and a per-byte coverage count of
+    the code bytes."""
     H, hd, kvh, F, V, L = s.hidden, s.head_dim, s.n_kv_heads, s.ffn, s.vocab, s.n_layers
     G = s.n_q_heads // kvh
     CPG, hd2, KO = grid // kvh, hd // 2, G * hd
     NP = (G + 2) * hd2
-    TRh, TRo = tile_rows(H, True), tile_rows(KO, False)
-    JT, JD = TRh // 2, SLOT // H
+    TRh, TRo = tile_rows(H, True, bits), tile_rows(KO, False, bits)
+    JT, JD = TRh // 2, SLOT // row_bytes(H, bits)
     qd, kvd = s.n_q_heads * hd, kvh * hd
     shapes = {"wq": (qd, H), "wk": (kvd, H), "wv": (kvd, H), "wo": (H, qd), "w_gate": (F, H), "w_up": (F, H),
               "w_down": (H, F)}
@@ -74,8 +90,11 @@ def decode_arena_q8(arena, s, grid):
     cover = np.zeros(arena.size, np.int32)
     off = 0
 
-    def codes_at(o, n):   # the stream stores each code q as the byte q + 128
-        cover[o:o + n] += 1
+    def codes_at(o, n):   # the stream stores each code q as the byte q + 128 (int4: packed nibbles)
+        nb = row_bytes(n, bits)
+        cover[o:o + nb] += 1
+        if bits == 4:
+            return unpack_q4(arena[o:o + nb])
         return (arena[o:o + n] ^ np.uint8(0x80)).view(np.int8)
 
     def f32_at(o, n):
@@ -91,10 +110,11 @@ def decode_arena_q8(arena, s, grid):
         nonlocal off
         for r in range(0, len(rows), TR):
             R = min(TR, len(rows) - r)
-            sc = f32_at(off + R * K, R)
+            rb = row_bytes(K, bits)
+            sc = f32_at(off + R * rb, R)
             for i in range(R):
-                sink(r + i, codes_at(off + i * K, K), sc[i])
-            off += tile_bytes(R, K, 0)
+                sink(r + i, codes_at(off + i * rb, K), sc[i])
+            off += tile_bytes(R, K, 0, bits)
 
     for c in range(grid):
         g, i = c // CPG, c % CPG
@@ -125,20 +145,21 @@ def decode_arena_q8(arena, s, grid):
                 codes["wo"][l][r0 + k, g * KO:(g + 1) * KO] = cd
                 put_scale(scales["wo"][l], r0 + k, sc)
             row_tiles(list(range(r0, r1)), KO, TRo, o_sink)
+            hb = row_bytes(H, bits)
             for j in range(j0, j1, JT):
                 n = min(JT, j1 - j)
-                sc = f32_at(off + 2 * n * H, 3 * n)
+                sc = f32_at(off + 2 * n * hb, 3 * n)
                 for jj in range(n):
-                    codes["w_gate"][l][j + jj] = codes_at(off + jj * H, H)
-                    codes["w_up"][l][j + jj] = codes_at(off + (n + jj) * H, H)
+                    codes["w_gate"][l][j + jj] = codes_at(off + jj * hb, H)
+                    codes["w_up"][l][j + jj] = codes_at(off + (n + jj) * hb, H)
                     put_scale(scales["w_gate"][l], j + jj, sc[jj])
                     put_scale(scales["w_up"][l], j + jj, sc[n + jj])
                     put_scale(scales["w_down"][l], j + jj, sc[2 * n + jj])
-                off += tile_bytes(2 * n, H, n)
+                off += tile_bytes(2 * n, H, n, bits)
             for j in range(j0, j1, JD):
                 for jj in range(j, min(j + JD, j1)):
                     codes["w_down"][l][:, jj] = codes_at(off, H)
-                    off += H
+                    off += hb
 
         def lm_sink(k, cd, sc):
             lm_q[v0 + k] = cd

@@ -52,5 +52,5 @@ def test_production_kernels_do_not_spill():
             checked += 1
             fused += "mk_decode_kernel" in fn
     assert fused == (len(build.VARIANTS) + len(build.LC_VARIANTS) + len(build.Q8_VARIANTS) +
-                     len(build.Q8_LC_VARIANTS)), fused
+                     len(build.Q8_LC_VARIANTS) + len(build.Q4_VARIANTS) + len(build.Q4_LC_VARIANTS)), fused
     assert checked > fused
