@@ -70,9 +70,11 @@ typedef struct {
  * tile granularity, pipeline depth and on-chip buffer split are configuration,
  * not constants).  Zero in any field selects the default. */
 typedef struct {
-    int32_t ring_stages;     /* shared-memory ring slots per CTA (default: as many as fit, <= 6);
-                                1 = no overlap of loading and compute ("prefetch off") */
-    int32_t slot_kib;        /* bytes per ring slot / weight tile, KiB (default and maximum 32) */
+    int32_t ring_stages;     /* shared-memory ring slots per CTA (default: as many as fit, <= 6,
+                                or <= 8 for weight_int4); 1 = no overlap of loading and compute
+                                ("prefetch off") */
+    int32_t slot_kib;        /* bytes per ring slot / weight tile, KiB (maximum 32; default 32, or 24
+                                for weight_int4) */
     int32_t l2_prefetch_kib; /* how far (KiB of tile stream) each CTA prefetches into L2 ahead of
                                 its ring copies (default, zero or negative: off -- on this path the
                                 extra L2 traffic cost more than the hidden latency saved) */

@@ -47,9 +47,12 @@ def test_arena_holds_the_oracle_int4_codes_and_scales(shape, grid, tied):
     q4 = oracle.quantize_model_q4(m)
     dec = Decoder(m, 64, tuning=tun, int4=True)
     info = dec.info
-    assert info.weight_int4 == 1 and info.weight_int8 == 0 and info.slot_bytes == SLOT
+    # int4 streams default to 24 KB tiles in 8 ring slots (the same 192 KB ring)
+    assert info.weight_int4 == 1 and info.weight_int8 == 0
+    assert info.slot_bytes == 3 * SLOT // 4 and info.ring_stages == 8
     arena = read_arena(dec)
-    codes, scales, lm_q, lm_s, cover, end = decode_arena_q8(arena, shape, info.grid_ctas, bits=4)
+    codes, scales, lm_q, lm_s, cover, end = decode_arena_q8(arena, shape, info.grid_ctas, bits=4,
+                                                            slot=info.slot_bytes)
     assert end == info.arena_bytes
     for name in oracle.Q8_KINDS:
         for l in range(shape.n_layers):
@@ -102,11 +105,14 @@ def test_tiny_int4_multi_tile(grid, tied, prefill):
     dec.close()
 
 
-@pytest.mark.parametrize("prefill,build", [(0, 0), (3000, 1), (3000, 2)])
-def test_wide_int4_both_attention_builds(prefill, build):
+@pytest.mark.parametrize("prefill,build,slot_kib", [(0, 0, 0), (3000, 1, 0), (3000, 2, 0), (0, 0, 32)])
+def test_wide_int4_both_attention_builds(prefill, build, slot_kib):
     """The 1B layout on the int4 stream: the standard build, and after a
-    3000-position prefill both attention builds (lane-parallel, tensor cores)."""
-    m, q4, dec, orc = make_q4(WIDE, 33, 4096)
+    3000-position prefill both attention builds (lane-parallel, tensor cores);
+    also with 32 KB tiles (30 rows of 2048 codes, a warp's share of a tile
+    in 8 passes of four rows) instead of the default 24 KB."""
+    tun = mk.tuning(ring_stages=6, slot_kib=32) if slot_kib else None
+    m, q4, dec, orc = make_q4(WIDE, 33, 4096, tuning=tun)
     assert dec.info.attn_tc == 1
     dec.set_debug(mk.MK_DBG_ATTN_BUILD, build)
     if prefill:

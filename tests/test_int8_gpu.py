@@ -51,11 +51,11 @@ def tile_bytes(R, K, extra, bits=8):
     return pad16(R * row_bytes(K, bits) + 4 * (R + extra))
 
 
-def tile_rows(K, gu_extra, bits=8):
+def tile_rows(K, gu_extra, bits=8, slot=SLOT):
     """Even rows per tile: as many as fit a slot with their scales (and, for the
     hidden-width tiles, the half-as-many W_down column scales of a GU tile)."""
-    r = (SLOT // row_bytes(K, bits)) & ~1
-    while r > 2 and tile_bytes(r, K, r // 2 if gu_extra else 0, bits) > SLOT:
+    r = (slot // row_bytes(K, bits)) & ~1
+    while r > 2 and tile_bytes(r, K, r // 2 if gu_extra else 0, bits) > slot:
         r -= 2
     return r
 
@@ -70,7 +70,7 @@ def unpack_q4(b):
     return out.reshape(-1)
 
 
-def decode_arena_q8(arena, s, grid, bits=8):
+def decode_arena_q8(arena, s, grid, bits=8, slot=SLOT):
     """Codes and scales of every matrix read out of an int8 (or, bits = 4,
     int4) arena, the W_down column scales, and a per-byte coverage count of
     the code bytes."""
@@ -78,8 +78,8 @@ def decode_arena_q8(arena, s, grid, bits=8):
     G = s.n_q_heads // kvh
     CPG, hd2, KO = grid // kvh, hd // 2, G * hd
     NP = (G + 2) * hd2
-    TRh, TRo = tile_rows(H, True, bits), tile_rows(KO, False, bits)
-    JT, JD = TRh // 2, SLOT // row_bytes(H, bits)
+    TRh, TRo = tile_rows(H, True, bits, slot), tile_rows(KO, False, bits, slot)
+    JT, JD = TRh // 2, slot // row_bytes(H, bits)
     qd, kvd = s.n_q_heads * hd, kvh * hd
     shapes = {"wq": (qd, H), "wk": (kvd, H), "wv": (kvd, H), "wo": (H, qd), "w_gate": (F, H), "w_up": (F, H),
               "w_down": (H, F)}
