@@ -34,7 +34,7 @@ Q8_VARIANTS = [(64, 2, 1), (64, 4, 8), (128, 4, 16)]
 Q8_LC_VARIANTS = [(64, 4, 8)]
 # weight-only INT4 builds (-DMK_WB_V=0); keep in sync with MK_Q4_VARIANTS and MK_Q4_LC_VARIANTS
 Q4_VARIANTS = [(64, 2, 1), (64, 4, 8), (128, 4, 16)]
-Q4_LC_VARIANTS = [(64, 4, 8)]
+Q4_LC_VARIANTS = [(64, 4, 8), (128, 4, 16)]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

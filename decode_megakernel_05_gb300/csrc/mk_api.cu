@@ -29,7 +29,7 @@
 // Weight-only INT4 builds (-DMK_WB_V=0; keep in sync with Q4_VARIANTS and
 // Q4_LC_VARIANTS in build.py).
 #define MK_Q4_VARIANTS(X) X(64, 2, 1) X(64, 4, 8) X(128, 4, 16)
-#define MK_Q4_LC_VARIANTS(X) X(64, 4, 8)
+#define MK_Q4_LC_VARIANTS(X) X(64, 4, 8) X(128, 4, 16)
 // Each variant exists twice: without trace code (launched normally) and with
 // it (launched while a segment trace is requested).
 #define MK_DECL(hd, g, mh)                                         \

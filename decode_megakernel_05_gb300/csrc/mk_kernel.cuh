@@ -990,8 +990,10 @@ struct WidePart { static constexpr int NKB = MH < 4 ? MH : 4; };
 // WB = 1 / 0 (int8 / int4 rows): the same columns per chunk (8 or 4 bytes
 // instead of 16), and each row's partials times the row's scale from the tile's tail; a GU tile's
 // W_down column scales (after the row scales) go to tsink[j] for the j's it
-// covers (the caller multiplies them into SiLU(gate) * up).
-template <int MH, int NG, int WB>
+// covers (the caller multiplies them into SiLU(gate) * up).  DG: the int rows
+// as integer dot products over the activation's digits (xs holds mk_xdigits),
+// or, DG = false, dequantized to fp32 against an fp32 xs.
+template <int MH, int NG, int WB, bool DG = (WB != 2)>
 __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring& ring, const float* xs, int nrows,
                                           int TR, bool ab, float* part, float* tsink) {
     using W = WideGemv<MH, NG>;
@@ -1007,23 +1009,24 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = w / WPG, wg = w % WPG;
     const int cb = wg % NKB, rs = wg / NKB;
-    // the lane's activations for the whole phase: fp32 (bf16 rows), or the
-    // digits and the lane's constant (int8 rows, mk_xdigits)
-    float4 xl[WB == 2 ? CPL : 1], xh[WB == 2 ? CPL : 1];
-    uint32_t xd[WB != 2 ? CPL : 1][6];
+    // the lane's activations for the whole phase: fp32, or the digits and
+    // the lane's constant (int rows with DG, mk_xdigits)
+    static_assert(!DG || WB != 2, "digits are the int rows' activation form");
+    float4 xl[DG ? 1 : CPL], xh[DG ? 1 : CPL];
+    uint32_t xd[DG ? CPL : 1][6];
     int bias[3] = {0, 0, 0};
     float xsc = 1.f;
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
         const int ch = (cb * CPL + j) * 32 + lane;
-        if constexpr (WB == 2) {
+        if constexpr (!DG) {
             xl[j] = reinterpret_cast<const float4*>(xs)[ch];
             xh[j] = reinterpret_cast<const float4*>(xs + K / 2)[ch];
         } else {
             dig_load<WB>(reinterpret_cast<const uint4*>(xs), K, ch, xd[j], bias);
         }
     }
-    if constexpr (WB != 2) xsc = s.misc()->xscale;
+    if constexpr (DG) xsc = s.misc()->xscale;
     const int ntiles = (nrows + TR - 1) / TR;
     for (int ti = 0; ti < ntiles && !ab; ++ti) {
         if (NG > 1 && (ti % NG) != grp) { ring.advance(p.geo.ns); continue; }   // another group's tile
@@ -1061,7 +1064,7 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
         auto pass = [&](int qb, auto&& chunk) {
             const int nv = min(4, nrow - qb);
             float v[4];
-            if constexpr (WB == 2) {
+            if constexpr (!DG) {
                 float2 a[4][2];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) a[q][0] = a[q][1] = make_float2(0.f, 0.f);
@@ -1138,10 +1141,10 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
 // Three groups of four warps measured fastest of 1, 2, 3 and 6 groups on the
 // 1B shape; a compile-time choice keeps one copy of the loop in the layer code.
 constexpr int MK_GEMV_GROUPS = 3;
-template <int MH, int WB>
+template <int MH, int WB, bool DG = (WB != 2)>
 __device__ __forceinline__ bool gemv_fifo(const MkParams& p, const Smem& s, Ring& ring, const float* xs, int nrows,
                                           int TR, bool ab, float* part, float* tsink = nullptr) {
-    return gemv_wide<MH, MK_GEMV_GROUPS, WB>(p, s, ring, xs, nrows, TR, ab, part, tsink);
+    return gemv_wide<MH, MK_GEMV_GROUPS, WB, DG>(p, s, ring, xs, nrows, TR, ab, part, tsink);
 }
 // Sum of the NKB column-block partials of row R of a FIFO GEMV phase.
 template <int MH>
@@ -1984,20 +1987,25 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
 
     Ring ring;
     bool ab = false;
+    // QKV of int rows as integer dot products over the norm output's digits,
+    // except in the 8B-width long-context build, where that GEMV beside the
+    // tensor-core attention of 128-dim heads spilled 44-48 bytes: there the
+    // attention norm writes fp32 and QKV dequantizes its rows to fp32
+    constexpr bool QDIG = WB != 2 && !(LC != 0 && MH > 8);
 
     MK_TRACE(16 * L + 3);
     for (int l = 0; l < L && !ab; ++l) {
         // ---------------- segment A: RMSNorm + QKV GEMV + RoPE + K/V append
         MK_TRACE(16 * l + 0);
         const float* xin = (l == 0) ? nullptr : xa + (size_t)(2 * l - 1) * state;
-        if constexpr (WB != 2)
+        if constexpr (QDIG)
             ab = rmsnorm_to_dig<(MH * 32 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H,
                                                                ab, s.xres(), pl.orow0, pl.g == 0 ? pl.norows : 0);
         else
             ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres(), pl.orow0,
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
-        ab = gemv_fifo<MH, WB>(p, s, ring, s.xv(), 2 * pl.npairs, g.TRh, ab, s.part());
+        ab = gemv_fifo<MH, WB, QDIG>(p, s, ring, s.xv(), 2 * pl.npairs, g.TRh, ab, s.part());
         if (t == 0 && p.stream_tail == 2) *(volatile int*)&s.misc()->streaming = 0;
         MK_TRACE(16 * l + 2);
         MK_TRACE_CWAIT(8 * l + 0);

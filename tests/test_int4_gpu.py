@@ -125,11 +125,14 @@ def test_wide_int4_both_attention_builds(prefill, build, slot_kib):
     dec.close()
 
 
-def test_hd128_int4():
+@pytest.mark.parametrize("build", [0, 1, 2])
+def test_hd128_int4(build):
     """The 8B layer width and head layout on the int4 stream over 300
-    pre-filled positions (lane-parallel attention, as for int8)."""
+    pre-filled positions, with each attention build (by context, lane-parallel,
+    tensor cores; the long-context build computes QKV in the float form)."""
     m, q4, dec, orc = make_q4(WIDE_HD128, 45, 512)
-    assert dec.info.attn_tc == 0
+    assert dec.info.attn_tc == 1
+    dec.set_debug(mk.MK_DBG_ATTN_BUILD, build)
     ks, vs = synth.make_kv(WIDE_HD128, 300, 47)
     dec.set_kv(ks, vs, 300)
     orc.set_kv(ks, vs, 300)
