@@ -163,6 +163,60 @@ def test_int4_generate_matches_oracle_tokens():
     dec.close()
 
 
+def test_int4_digits_with_activation_outliers():
+    """Norm gains of 64 and 32 on a few channels make those entries of the
+    norm output ~50x the rest and set the 22-bit digits' scale; the int4
+    stream's teacher-forced logits and hidden state stay within the parity
+    bounds of the oracle's fp64 int4 forward."""
+    m = synth.make_model(WIDE, 49, std=0.03, gains="normal")
+    for kind in ("attn_norm", "ffn_norm"):
+        for l in range(WIDE.n_layers):
+            g = m[kind][l].copy()
+            g[5], g[999], g[2046] = 0x4280, 0x4200, 0x4280   # bf16 64, 32, 64
+            m[kind][l] = g
+    fn = m["final_norm"].copy()
+    fn[11] = 0x4280
+    m["final_norm"] = fn
+    q4 = oracle.quantize_model_q4(m)
+    dec = Decoder(m, 256, int4=True)
+    orc = oracle.OracleDecoder(m, 256, q8=q4)
+    rep = run_teacher_forced(dec, orc, synth.uniform_tokens(4, WIDE.vocab, 49, 3), 0, 10)
+    print(rep.summary())
+    rep.check()
+    dec.close()
+
+
+def test_int4_topp_sampling_matches_oracle():
+    """Temperature and top-p on the int4 stream: the fused draw equals the
+    oracle's nucleus sample from its int4 logits, up to the boundary cases
+    the logit error allows."""
+    from tests.test_parity_gpu import _nucleus_bounds, _oracle_keys
+    m, q4, dec, orc = make_q4(TINY, 73, 128)
+    dec.set_top_p(0.9)
+    inv = float(np.float32(1.0 / 0.8))
+    seed, tok, agree, steps = 0x5EED4, 9, 0, 24
+    for pos in range(steps):
+        dec.step_sample(tok, pos, 0.8, seed, logits=True)
+        lg_ref, _ = orc.step(tok, pos)
+        lg = dec.logits.cpu().numpy().astype(np.float64)
+        got = dec.get_argmax()
+        want, nf = oracle.sample_topp_f32(lg_ref, inv, 0.9, seed, pos)
+        assert not nf
+        dl = float(np.max(np.abs(lg - lg_ref)))
+        assert dl <= 5e-2
+        if got == want:
+            agree += 1
+        else:
+            loose, strict = _nucleus_bounds(lg_ref, inv, 0.9, dl)
+            keys = _oracle_keys(lg_ref, inv, seed, pos)
+            assert got in loose, (pos, got, want)
+            assert keys[got] >= max(keys[v] for v in strict) - (2 * dl * inv + 1e-5), (pos, got, want)
+        tok = want
+    assert agree >= steps - 2, agree
+    assert dec.status() == 0
+    dec.close()
+
+
 def test_int4_refusals():
     """One weight form at a time, and the bf16-only paths stay closed."""
     w = synth.WORKLOADS["tiny"]
