@@ -187,7 +187,7 @@ int build_geom(const mk_config* c, const Tune& tu, int grid, int ns, MkGeom& g) 
     if (!mk_geom_init(g, c->n_layers, c->hidden, c->n_q_heads, c->n_kv_heads, c->head_dim, c->ffn, c->vocab,
                       c->max_seq, grid, tu.slot, ns, tu.wb))
         return MK_ERR_INVALID_ARG;
-    if (g.TRh < 2 || g.TRo < 2 || g.JD < 1 || g.KB < 1 || tu.slot % 16) return MK_ERR_INVALID_ARG;
+    if (g.TRh < 2 || g.TRq < 2 || g.TRo < 2 || g.JD < 1 || g.KB < 1 || tu.slot % 16) return MK_ERR_INVALID_ARG;
     if (ns < 1 || ns > 16) return MK_ERR_INVALID_ARG;
     if (g.max_rows > 4096 || g.max_nj > 8192) return MK_ERR_UNSUPPORTED;
     if (g.CPG * g.G > MK_MAX_CPG_G) return MK_ERR_UNSUPPORTED;
@@ -226,7 +226,7 @@ void build_maps(const MkGeom& g, const std::vector<MkCtaPlan>& plans, Maps& m) {
         const MkCtaPlan& p = plans[c];
         for (int l = 0; l < L; ++l) {
             int64_t off = p.stream_off + (int64_t)l * p.layer_bytes;
-            row_tiles(off, 2 * p.npairs, g.TRh, H, [&](int r, int64_t d, int64_t so) {
+            row_tiles(off, 2 * p.npairs, g.TRq, H, [&](int r, int64_t d, int64_t so) {
                 int mat, row;
                 mk_qkv_row(g, p.g, p.pair0 + r / 2, r % 2, mat, row);
                 (mat == 0 ? m.q : mat == 1 ? m.k : m.v)[l].push_back(MkRowCopyQ{d, row, 0, H, so});

@@ -23,7 +23,7 @@
 //           of the group, then the up rows of the same j's.
 //     D   : columns j0 .. j0 + nj - 1 of W_down, each stored as H contiguous bf16.
 //   LM    : rows v in split(V, nC, c) of the LM head (the embedding when tied).
-// A tile is TRh rows (QKV, LM), TRo rows (O), one GU group, or JD columns (D);
+// A tile is TRq rows (QKV), TRh rows (LM), TRo rows (O), one GU group, or JD columns (D);
 // the last tile of a block may be short.  Every tile is a multiple of 16 bytes.
 //
 // Weight-only INT8 streams (wb = 1) store each weight's code q as the byte
@@ -44,6 +44,7 @@
 #include <stdint.h>
 
 #define MK_NCW 12                    // consumer warps
+#define MK_WIDE_GROUPS 3             // consumer groups that take the hidden-width GEMVs' tiles in turn
 #define MK_NCT (MK_NCW * 32)         // consumer threads
 #define MK_PRODUCER_WARP MK_NCW      // bulk-copy producer
 #define MK_PREFETCH_WARP (MK_NCW + 1)// L2 prefetch walker
@@ -135,7 +136,7 @@ struct MkGeom {
     int32_t L, H, qh, kvh, hd, F, V, max_seq;
     int32_t G, CPG, nC, NP;
     int32_t slot, ns;            // ring slot bytes, ring stages
-    int32_t TRh, TRo, JT, JD, KB;
+    int32_t TRh, TRq, TRo, JT, JD, KB;
     int32_t max_rows, max_nj;    // per-CTA maxima (QKV rows, FFN slice)
     int32_t smem_bytes;
     int32_t kv_swz;              // K/V cache rows chunk-permuted (mk_kv_index); set with the long-context build
@@ -186,6 +187,17 @@ MK_HD bool mk_geom_init(MkGeom& g, int L, int H, int qh, int kvh, int hd, int F,
     g.JD = (int32_t)(slot_bytes / mk_wbytes(H, wb));
     g.KB = slot_bytes / (2 * hd);
     g.max_rows = 2 * (int)((g.NP + g.CPG - 1) / g.CPG);
+    // QKV tiles: TRh rows, or for int8 / int4 rows (which fit 1.75x / 2.75x
+    // as many rows in a slot) few enough that a CTA's QKV rows make a tile
+    // for each consumer group: one group on all of them was the longest
+    // segment of the int4 layer
+    g.TRq = g.TRh;
+    if (wb != 2) {
+        int t = (g.max_rows + MK_WIDE_GROUPS - 1) / MK_WIDE_GROUPS;
+        t = (t + 1) & ~1;
+        if (t < 2) t = 2;
+        if (t < g.TRq) g.TRq = t;
+    }
     g.max_nj = (F + nC - 1) / nC;
     return true;
 }
@@ -293,7 +305,7 @@ MK_HD int mk_imin(int a, int b) { return a < b ? a : b; }
 MK_HD int64_t mk_layer_bytes(const MkGeom& g, const MkCtaPlan& p) {
     int64_t b = 0;
     const int nr = 2 * p.npairs, KO = g.G * g.hd;
-    for (int r = 0; r < nr; r += g.TRh) b += mk_row_tile_bytes(mk_imin(g.TRh, nr - r), g.H, g.wb, 0);
+    for (int r = 0; r < nr; r += g.TRq) b += mk_row_tile_bytes(mk_imin(g.TRq, nr - r), g.H, g.wb, 0);
     for (int r = 0; r < p.norows; r += g.TRo) b += mk_row_tile_bytes(mk_imin(g.TRo, p.norows - r), KO, g.wb, 0);
     for (int j = 0; j < p.nj; j += g.JT) {
         const int n = mk_imin(g.JT, p.nj - j);
@@ -365,8 +377,8 @@ MK_HD void mk_walk_tiles(const MkGeom& g, const MkCtaPlan& pl, const uint8_t* ar
     const int KO = g.G * g.hd;
     for (int l = 0; l < g.L; ++l) {
         const int nr = 2 * pl.npairs;
-        for (int r = 0; r < nr; r += g.TRh) {
-            uint32_t by = (uint32_t)mk_row_tile_bytes(mk_imin(g.TRh, nr - r), H, g.wb, 0);
+        for (int r = 0; r < nr; r += g.TRq) {
+            uint32_t by = (uint32_t)mk_row_tile_bytes(mk_imin(g.TRq, nr - r), H, g.wb, 0);
             f((const void*)cur, by); cur += by;
         }
         const int64_t kvoff = ((int64_t)l * g.kvh + pl.g) * g.max_seq * g.hd;

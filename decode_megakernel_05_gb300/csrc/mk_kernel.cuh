@@ -1140,7 +1140,7 @@ __device__ __forceinline__ bool gemv_wide(const MkParams& p, const Smem& s, Ring
 }
 // Three groups of four warps measured fastest of 1, 2, 3 and 6 groups on the
 // 1B shape; a compile-time choice keeps one copy of the loop in the layer code.
-constexpr int MK_GEMV_GROUPS = 3;
+constexpr int MK_GEMV_GROUPS = MK_WIDE_GROUPS;
 template <int MH, int WB, bool DG = (WB != 2)>
 __device__ __forceinline__ bool gemv_fifo(const MkParams& p, const Smem& s, Ring& ring, const float* xs, int nrows,
                                           int TR, bool ab, float* part, float* tsink = nullptr) {
@@ -2005,7 +2005,7 @@ __global__ void __launch_bounds__(MK_BLOCK, 1) mk_decode_kernel(const __grid_con
             ab = rmsnorm_to_xv<(MH * 256 + MK_NCT - 1) / MK_NCT>(p, s, xin, l == 0 ? emb : nullptr, p.attn_norm + (size_t)l * H, ab, s.xres(), pl.orow0,
                            pl.g == 0 ? pl.norows : 0);
         MK_TRACE(16 * l + 1);
-        ab = gemv_fifo<MH, WB, QDIG>(p, s, ring, s.xv(), 2 * pl.npairs, g.TRh, ab, s.part());
+        ab = gemv_fifo<MH, WB, QDIG>(p, s, ring, s.xv(), 2 * pl.npairs, g.TRq, ab, s.part());
         if (t == 0 && p.stream_tail == 2) *(volatile int*)&s.misc()->streaming = 0;
         MK_TRACE(16 * l + 2);
         MK_TRACE_CWAIT(8 * l + 0);

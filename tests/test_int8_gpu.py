@@ -80,6 +80,10 @@ def decode_arena_q8(arena, s, grid, bits=8, slot=SLOT):
     NP = (G + 2) * hd2
     TRh, TRo = tile_rows(H, True, bits, slot), tile_rows(KO, False, bits, slot)
     JT, JD = TRh // 2, slot // row_bytes(H, bits)
+    # QKV tiles hold at most a third of the largest per-CTA QKV share (rounded
+    # up to an even count, at least 2), so three consumer groups share the rows
+    max_rows = 2 * -(-NP // CPG)
+    TRq = min(TRh, max(2, (-(-max_rows // 3) + 1) // 2 * 2))
     qd, kvd = s.n_q_heads * hd, kvh * hd
     shapes = {"wq": (qd, H), "wk": (kvd, H), "wv": (kvd, H), "wo": (H, qd), "w_gate": (F, H), "w_up": (F, H),
               "w_down": (H, F)}
@@ -139,7 +143,7 @@ def decode_arena_q8(arena, s, grid, bits=8, slot=SLOT):
                 name, row = qkv[k]
                 codes[name][l][row] = cd
                 put_scale(scales[name][l], row, sc)
-            row_tiles(qkv, H, TRh, qkv_sink)
+            row_tiles(qkv, H, TRq, qkv_sink)
 
             def o_sink(k, cd, sc):
                 codes["wo"][l][r0 + k, g * KO:(g + 1) * KO] = cd
