@@ -59,7 +59,8 @@ def test_ring_slot_limit():
 
 def test_every_kernel_build_is_in_the_library():
     """Each (head_dim, q heads per kv head, hidden/256) variant exists twice
-    (without and with the segment trace), and so does each long-context build."""
+    (without and with the segment trace), and so does each long-context and
+    each weight-only INT8 / INT4 build."""
     from decode_megakernel_05_gb300 import build
     lib = mk.load()
     for hd, g, mh in build.VARIANTS:
@@ -68,6 +69,12 @@ def test_every_kernel_build_is_in_the_library():
     for hd, g, mh in build.LC_VARIANTS:
         for pre in ("mk_kernel_ptr_", "mk_kernel_trace_ptr_"):
             assert hasattr(lib, f"{pre}{hd}_{g}_{mh}_lc"), (pre, hd, g, mh)
+    # the weight-only INT8 / INT4 builds, standard and long-context
+    for table, sfx in ((build.Q8_VARIANTS, "_q8"), (build.Q8_LC_VARIANTS, "_lc_q8"),
+                       (build.Q4_VARIANTS, "_q4"), (build.Q4_LC_VARIANTS, "_lc_q4")):
+        for hd, g, mh in table:
+            for pre in ("mk_kernel_ptr_", "mk_kernel_trace_ptr_"):
+                assert hasattr(lib, f"{pre}{hd}_{g}_{mh}{sfx}"), (pre, hd, g, mh, sfx)
 
 
 def test_no_closed_cuda_calls_in_sources():
@@ -82,7 +89,8 @@ def test_no_closed_cuda_calls_in_sources():
 
 def test_binding_constants_match_header():
     """Every MK_DBG_* / MK_ERR_* / MK_OK number the header defines has the same
-    value in the Python binding, and mk_info's fields are mirrored in order."""
+    value in the Python binding, and mk_info's and mk_tuning's fields are
+    mirrored in order and width."""
     src = open(os.path.join(ROOT, "include", "mk.h")).read()
     defs = dict(re.findall(r"#define\s+(MK_(?:DBG|ERR)_[A-Z0-9_]+|MK_OK)\s+\(?(-?\d+)\)?", src))
     assert "MK_DBG_ATTN_BUILD" in defs and "MK_DBG_ATTN_TC_MIN" in defs
@@ -90,8 +98,12 @@ def test_binding_constants_match_header():
         if hasattr(mk, name):
             assert getattr(mk, name) == int(val), name
     assert all(hasattr(mk, n) for n in defs if n.startswith("MK_DBG_")), defs
-    end = src.index("} mk_info;")
-    body = src[src.rindex("typedef struct {", 0, end):end]
-    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
-    fields = [f.strip() for decl in re.findall(r"int(?:32|64)_t\s+([^;]+);", body) for f in decl.split(",")]
-    assert fields == [f for f, _ in mk.mk_info._fields_], fields
+    for name, cls in (("mk_info", mk.mk_info), ("mk_tuning", mk.mk_tuning)):
+        end = src.index("} %s;" % name)
+        body = src[src.rindex("typedef struct {", 0, end):end]
+        body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+        fields = [f.strip() for decl in re.findall(r"int(?:32|64)_t\s+([^;]+);", body) for f in decl.split(",")]
+        assert fields == [f for f, _ in cls._fields_], (name, fields)
+        # and the widths: every field of these two structs is int32_t or int64_t
+        widths = [w for decl_w, decl in re.findall(r"int(32|64)_t\s+([^;]+);", body) for w in [decl_w] * len(decl.split(","))]
+        assert [8 if w == "64" else 4 for w in widths] == [mk.ctypes.sizeof(t) for _, t in cls._fields_], name
