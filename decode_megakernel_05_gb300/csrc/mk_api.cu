@@ -512,6 +512,7 @@ const char* mk_last_cuda_error(void) { return g_cuda_err.c_str(); }
 
 int64_t mk_arena_bytes(const mk_config* cfg, const mk_tuning* tuning, int32_t grid_ctas) {
     if (check_shape(cfg, false) != MK_OK || grid_ctas < 1) return -1;
+    if (tuning && tuning->weight_int8 && tuning->weight_int4) return -1;   // one weight form
     Tune tu = resolve_tuning(tuning);
     MkGeom g;
     if (build_geom(cfg, tu, grid_ctas, 1, g) != MK_OK) return -1;

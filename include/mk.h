@@ -393,9 +393,11 @@ const char* mk_last_cuda_error(void);
 void mk_destroy(mk_ctx* ctx);
 
 /* Host-only layout utilities (no GPU needed).  mk_arena_bytes: size of the
- * re-laid-out weight arena for `grid_ctas` CTAs.  mk_relayout_host: build that
- * arena on the host from host weights (the same layout mk_load_weights writes
- * on the device). */
+ * re-laid-out weight arena for `grid_ctas` CTAs, for the tuning's weight form
+ * (bf16, weight_int8 or weight_int4); -1 for an invalid shape, grid or tuning
+ * (both weight forms at once).  mk_relayout_host: build that arena on the host
+ * from host weights (the same layout mk_load_weights writes on the device;
+ * bf16 only). */
 int64_t mk_arena_bytes(const mk_config* cfg, const mk_tuning* tuning, int32_t grid_ctas);
 int mk_relayout_host(const mk_config* cfg, const mk_tuning* tuning, int32_t grid_ctas, const mk_weights* w,
                      void* arena_out);
